@@ -1,0 +1,343 @@
+/*
+ * CPU oracle for the FP8 GEMM path.  TEST INFRASTRUCTURE ONLY: the tests,
+ * the smoke check and the bench's CPU-baseline leg use it; the library never
+ * does.  It shares no code, header or table with the CUDA path.
+ *
+ * What it computes (plain definitions, fp64):
+ *
+ *   dense   D[m,n]   = bf16_rne( sum_k dec(A[m,k]) * dec(B[n,k]) )
+ *   masked  D[g,m,n] = bf16_rne( sum_k dec(A[g,m,k]) * dec(B[g,n,k]) )
+ *                       for m < masked_m[g]; other rows of D untouched.
+ *
+ * Sources:
+ *  - "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践"
+ *    (sheratonhq.com/news/187119), §1.3: A and B are FP8 (E4M3/E5M2
+ *    selectable), the accumulator is FP32; §3.1: E4M3 is 4 exponent + 3
+ *    mantissa bits, E5M2 is 5 + 2.
+ *  - "一次“转置”，半张算力：DeepSeek SwapAB 漂流史" (hwcomputing.csdn.net),
+ *    §3.1/§3.3: the masked grouped GEMM m_grouped_fp8_gemm_nt_masked, where
+ *    only the first valid_m token rows of each group are real.
+ *
+ * Readings (the pages give only the bit splits of the two formats):
+ *  - FP8 codes follow the OCP 8-bit float definitions as NVIDIA hardware
+ *    implements them: E4M3 has bias 7, no infinity and NaN only at S.1111.111;
+ *    E5M2 has bias 15, IEEE-style infinities and NaNs at exponent 31.
+ *  - The GPU accumulates in FP32 in hardware order; the oracle accumulates the
+ *    exact products in double in ascending k (each product of two FP8 values is
+ *    exact in double) and rounds once to BF16, round-to-nearest-even.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <sched.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#define ORACLE_E4M3 0
+#define ORACLE_E5M2 1
+
+/* ---- FP8 decode, from the closed form of each format ------------------ */
+
+/* E4M3: s | e(4) | m(3), bias 7.
+ *   e == 0          : (-1)^s * (m/8) * 2^-6       (subnormal, incl. +-0)
+ *   e == 15, m == 7 : NaN                         (no infinities)
+ *   otherwise       : (-1)^s * (1 + m/8) * 2^(e-7)
+ * E5M2: s | e(5) | m(2), bias 15.
+ *   e == 0          : (-1)^s * (m/4) * 2^-14
+ *   e == 31         : +-inf if m == 0, else NaN
+ *   otherwise       : (-1)^s * (1 + m/4) * 2^(e-15)
+ */
+double oracle_decode_fp8(uint8_t code, int fmt)
+{
+    int s = (code >> 7) & 1;
+    double v;
+    if (fmt == ORACLE_E4M3) {
+        int e = (code >> 3) & 0xF;
+        int m = code & 0x7;
+        if (e == 15 && m == 7)
+            return NAN;
+        if (e == 0)
+            v = ((double)m / 8.0) * ldexp(1.0, -6);
+        else
+            v = (1.0 + (double)m / 8.0) * ldexp(1.0, e - 7);
+    } else {
+        int e = (code >> 2) & 0x1F;
+        int m = code & 0x3;
+        if (e == 31)
+            return m == 0 ? (s ? -INFINITY : INFINITY) : NAN;
+        if (e == 0)
+            v = ((double)m / 4.0) * ldexp(1.0, -14);
+        else
+            v = (1.0 + (double)m / 4.0) * ldexp(1.0, e - 15);
+    }
+    return s ? -v : v;
+}
+
+/* Fill a 256-entry table with oracle_decode_fp8 of every code. */
+void oracle_decode_table(int fmt, double *out256)
+{
+    for (int c = 0; c < 256; ++c)
+        out256[c] = oracle_decode_fp8((uint8_t)c, fmt);
+}
+
+/* ---- BF16 rounding ----------------------------------------------------- */
+
+/* Round a double to the nearest BF16 (1 sign, 8 exponent, 7 stored mantissa
+ * bits, bias 127), ties to even, overflow to infinity, gradual underflow.
+ * Written from the format definition: find the binade of |x|, divide by the
+ * spacing of that binade (a power of two, so exact), round the quotient to an
+ * integer with ties to even, and re-pack. */
+uint16_t oracle_round_bf16(double x)
+{
+    if (isnan(x))
+        return 0x7FC0;
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs(x);
+    if (a == 0.0)
+        return sign;
+    if (isinf(a))
+        return sign | 0x7F80;
+
+    int e2;
+    (void)frexp(a, &e2);          /* a = f * 2^e2, f in [0.5, 1)         */
+    int E = e2 - 1;               /* floor(log2 a)                       */
+    if (E < -126)
+        E = -126;                 /* below the normal range: fixed spacing */
+    double spacing = ldexp(1.0, E - 7);
+    double q = a / spacing;       /* exact: division by a power of two   */
+    double f = floor(q);
+    double rem = q - f;           /* exact                               */
+    if (rem > 0.5 || (rem == 0.5 && fmod(f, 2.0) != 0.0))
+        f += 1.0;
+
+    if (f >= 256.0) {             /* rounded up into the next binade     */
+        f = 128.0;
+        E += 1;
+    }
+    if (f < 128.0)                /* subnormal (only possible at E=-126) */
+        return sign | (uint16_t)f;
+    if (E > 127)
+        return sign | 0x7F80;     /* overflow                            */
+    return sign | (uint16_t)(((E + 127) << 7) | ((int)f - 128));
+}
+
+/* BF16 code -> double (exact). */
+double oracle_bf16_to_double(uint16_t h)
+{
+    int s = (h >> 15) & 1;
+    int e = (h >> 7) & 0xFF;
+    int m = h & 0x7F;
+    double v;
+    if (e == 0xFF)
+        v = m ? NAN : INFINITY;
+    else if (e == 0)
+        v = (double)m * ldexp(1.0, -133);
+    else
+        v = (double)(128 + m) * ldexp(1.0, e - 134);
+    return s ? -v : v;
+}
+
+/* ---- threading helper (splits output rows; no change to arithmetic) --- */
+
+static int oracle_cpu_count(void)
+{
+#ifdef CPU_COUNT
+    cpu_set_t set;
+    if (sched_getaffinity(0, sizeof(set), &set) == 0) {
+        int c = CPU_COUNT(&set);
+        if (c > 0)
+            return c;
+    }
+#endif
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int)n : 1;
+}
+
+int oracle_default_threads(void) { return oracle_cpu_count(); }
+
+typedef void (*row_fn)(void *ctx, int64_t row);
+
+typedef struct {
+    row_fn fn;
+    void *ctx;
+    int64_t rows;
+    int64_t next;
+    pthread_mutex_t lock;
+} row_pool;
+
+static void *row_worker(void *arg)
+{
+    row_pool *p = (row_pool *)arg;
+    for (;;) {
+        pthread_mutex_lock(&p->lock);
+        int64_t r = p->next++;
+        pthread_mutex_unlock(&p->lock);
+        if (r >= p->rows)
+            break;
+        p->fn(p->ctx, r);
+    }
+    return NULL;
+}
+
+static void run_rows(row_fn fn, void *ctx, int64_t rows, int nthreads)
+{
+    if (nthreads <= 0)
+        nthreads = oracle_cpu_count();
+    if (nthreads > rows)
+        nthreads = (int)(rows > 0 ? rows : 1);
+    row_pool p;
+    p.fn = fn;
+    p.ctx = ctx;
+    p.rows = rows;
+    p.next = 0;
+    pthread_mutex_init(&p.lock, NULL);
+    if (nthreads <= 1) {
+        row_worker(&p);
+    } else {
+        pthread_t *t = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+        for (int i = 0; i < nthreads; ++i)
+            pthread_create(&t[i], NULL, row_worker, &p);
+        for (int i = 0; i < nthreads; ++i)
+            pthread_join(t[i], NULL);
+        free(t);
+    }
+    pthread_mutex_destroy(&p.lock);
+}
+
+/* ---- the contraction --------------------------------------------------- */
+
+/* One output element: the exact dot product of row a (K codes, format fa)
+ * with row b (K codes, format fb), summed in double in ascending k.  Also
+ * returns sum_k |a_k * b_k|, which scales the tolerance of the GPU result. */
+static double dot_row(const uint8_t *a, const uint8_t *b, int64_t K,
+                      const double *ta, const double *tb, double *absdot)
+{
+    double s = 0.0, sa = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        double p = ta[a[k]] * tb[b[k]];
+        s += p;
+        sa += fabs(p);
+    }
+    *absdot = sa;
+    return s;
+}
+
+typedef struct {
+    const uint8_t *A, *B;
+    int64_t M, N, K;
+    double ta[256], tb[256];
+    uint16_t *D;       /* [M,N] bf16 codes, may be NULL */
+    double *exact;     /* [M,N] double sums, may be NULL */
+    double *absdot;    /* [M,N], may be NULL */
+} gemm_ctx;
+
+static void gemm_row(void *vctx, int64_t m)
+{
+    gemm_ctx *c = (gemm_ctx *)vctx;
+    const uint8_t *a = c->A + m * c->K;
+    for (int64_t n = 0; n < c->N; ++n) {
+        double ad;
+        double s = dot_row(a, c->B + n * c->K, c->K, c->ta, c->tb, &ad);
+        int64_t o = m * c->N + n;
+        if (c->D)
+            c->D[o] = oracle_round_bf16(s);
+        if (c->exact)
+            c->exact[o] = s;
+        if (c->absdot)
+            c->absdot[o] = ad;
+    }
+}
+
+/* Dense D[M,N] = A[M,K] * B[N,K]^T.  A and B are row-major with K
+ * contiguous (the "NT" layout).  nthreads <= 0 uses every core available. */
+void oracle_gemm_nt(const uint8_t *A, const uint8_t *B, int64_t M, int64_t N,
+                    int64_t K, int fa, int fb, uint16_t *D, double *exact,
+                    double *absdot, int nthreads)
+{
+    gemm_ctx c;
+    c.A = A;
+    c.B = B;
+    c.M = M;
+    c.N = N;
+    c.K = K;
+    oracle_decode_table(fa, c.ta);
+    oracle_decode_table(fb, c.tb);
+    c.D = D;
+    c.exact = exact;
+    c.absdot = absdot;
+    run_rows(gemm_row, &c, M, nthreads);
+}
+
+/* Selected elements of the dense product: out[i] = D[ms[i], ns[i]]. */
+void oracle_gemm_nt_entries(const uint8_t *A, const uint8_t *B, int64_t K,
+                            int fa, int fb, const int64_t *ms,
+                            const int64_t *ns, int64_t count, uint16_t *D,
+                            double *exact, double *absdot)
+{
+    double ta[256], tb[256];
+    oracle_decode_table(fa, ta);
+    oracle_decode_table(fb, tb);
+    for (int64_t i = 0; i < count; ++i) {
+        double ad;
+        double s = dot_row(A + ms[i] * K, B + ns[i] * K, K, ta, tb, &ad);
+        if (D)
+            D[i] = oracle_round_bf16(s);
+        if (exact)
+            exact[i] = s;
+        if (absdot)
+            absdot[i] = ad;
+    }
+}
+
+typedef struct {
+    const uint8_t *A, *B;
+    const int32_t *masked_m;
+    int64_t G, M_max, N, K;
+    double ta[256], tb[256];
+    uint16_t *D;
+    double *absdot;
+} grouped_ctx;
+
+/* One (group, row) pair; rows at or beyond the group's valid count are left
+ * exactly as the caller passed them. */
+static void grouped_row(void *vctx, int64_t gm)
+{
+    grouped_ctx *c = (grouped_ctx *)vctx;
+    int64_t g = gm / c->M_max, m = gm % c->M_max;
+    if (m >= (int64_t)c->masked_m[g])
+        return;
+    const uint8_t *a = c->A + (g * c->M_max + m) * c->K;
+    const uint8_t *b = c->B + g * c->N * c->K;
+    for (int64_t n = 0; n < c->N; ++n) {
+        double ad;
+        double s = dot_row(a, b + n * c->K, c->K, c->ta, c->tb, &ad);
+        int64_t o = (g * c->M_max + m) * c->N + n;
+        c->D[o] = oracle_round_bf16(s);
+        if (c->absdot)
+            c->absdot[o] = ad;
+    }
+}
+
+/* Masked grouped D[g,m,n] for m < masked_m[g]; A[G,M_max,K], B[G,N,K],
+ * D[G,M_max,N].  masked_m values must already lie in [0, M_max]. */
+void oracle_gemm_grouped_masked(const uint8_t *A, const uint8_t *B,
+                                const int32_t *masked_m, int64_t G,
+                                int64_t M_max, int64_t N, int64_t K, int fa,
+                                int fb, uint16_t *D, double *absdot,
+                                int nthreads)
+{
+    grouped_ctx c;
+    c.A = A;
+    c.B = B;
+    c.masked_m = masked_m;
+    c.G = G;
+    c.M_max = M_max;
+    c.N = N;
+    c.K = K;
+    oracle_decode_table(fa, c.ta);
+    oracle_decode_table(fb, c.tb);
+    c.D = D;
+    c.absdot = absdot;
+    run_rows(grouped_row, &c, G * M_max, nthreads);
+}

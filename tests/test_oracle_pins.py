@@ -1,0 +1,356 @@
+"""Pins for the CPU oracle: each check ties an oracle function to something
+other than itself -- torch's float8 / bfloat16 conversions, exact rational
+brute force, closed forms of structured products, printed fixtures -- so that
+a dropped term, a wrong sign or index, or a transposed operand fails here."""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+FMTS = {"e4m3": oracle.E4M3, "e5m2": oracle.E5M2}
+TORCH_FP8 = {oracle.E4M3: torch.float8_e4m3fn, oracle.E5M2: torch.float8_e5m2}
+
+
+def torch_decode_all(fmt):
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return codes.view(TORCH_FP8[fmt]).to(torch.float64).numpy()
+
+
+def torch_decode(codes: np.ndarray, fmt) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(codes, np.uint8))
+    return t.view(TORCH_FP8[fmt]).to(torch.float64).numpy()
+
+
+# ---- FP8 decode --------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_decode_all_codes_match_torch(fmt):
+    mine = oracle.decode_table(fmt)
+    ref = torch_decode_all(fmt)
+    nan_m, nan_r = np.isnan(mine), np.isnan(ref)
+    assert np.array_equal(nan_m, nan_r)
+    assert np.array_equal(mine[~nan_m], ref[~nan_r])
+    # signed zeros: 0x80 is -0 in both formats
+    assert math.copysign(1.0, mine[0x80]) == -1.0
+    for c in range(256):
+        assert oracle.decode_fp8(c, fmt) == mine[c] or (np.isnan(mine[c]))
+
+
+def _golden_points():
+    pts = []
+    with open(os.path.join(GOLDEN, "fp8_format_points.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            fmt, code, val = line.split()
+            pts.append((FMTS[fmt], int(code, 16), val))
+    return pts
+
+
+@pytest.mark.parametrize("fmt,code,val", _golden_points())
+def test_decode_golden_points(fmt, code, val):
+    got = oracle.decode_fp8(code, fmt)
+    if val == "nan":
+        assert math.isnan(got)
+    elif val in ("inf", "-inf"):
+        assert got == float(val)
+    elif val == "-0":
+        assert got == 0.0 and math.copysign(1.0, got) == -1.0
+    else:
+        assert Fraction(got) == Fraction(val)
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_decode_structure(fmt):
+    """Positive finite codes are strictly increasing in code order, the
+    negative half mirrors the positive half, and NaN counts match the
+    format (E4M3: 2 NaN codes, no inf; E5M2: 6 NaN codes, 2 inf)."""
+    t = oracle.decode_table(fmt)
+    pos = t[:128]
+    fin = pos[np.isfinite(pos)]
+    assert np.all(np.diff(fin) > 0)
+    for c in range(128):
+        if np.isnan(t[c]):
+            assert np.isnan(t[c | 0x80])
+        else:
+            assert t[c | 0x80] == -t[c]
+    n_nan = int(np.isnan(t).sum())
+    n_inf = int(np.isinf(t).sum())
+    assert (n_nan, n_inf) == ((2, 0) if fmt == oracle.E4M3 else (6, 2))
+
+
+# ---- BF16 rounding -----------------------------------------------------------
+
+def test_round_bf16_matches_torch_on_float32_values():
+    rng = np.random.default_rng(1234)
+    bits = rng.integers(0, 2**32, size=20000, dtype=np.uint64).astype(np.uint32)
+    f = bits.view(np.float32)
+    f = f[np.isfinite(f)]
+    # add values right at and around BF16 midpoints
+    mids = (rng.integers(0, 2**16, 5000, dtype=np.uint64).astype(np.uint32) << 16) | 0x8000
+    near = np.concatenate([mids, mids + 1, mids - 1]).astype(np.uint32).view(np.float32)
+    near = near[np.isfinite(near)]
+    vals = np.concatenate([f, near]).astype(np.float32)
+    ref = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    mine = oracle.round_bf16_array(vals.astype(np.float64))
+    # torch maps NaN to a canonical NaN too; none here (finite inputs only)
+    assert np.array_equal(mine, ref)
+
+
+def test_round_bf16_ties_and_specials_exact():
+    # 1 + 2^-8 is the midpoint of 1 and 1 + 2^-7: ties to even -> 1.0
+    assert oracle.round_bf16(1.0 + 2**-8) == 0x3F80
+    # 1 + 3*2^-8 is the midpoint of 1+2^-7 (odd) and 1+2^-6 (even) -> up
+    assert oracle.round_bf16(1.0 + 3 * 2**-8) == 0x3F82
+    # just above a tie rounds up (needs more than float32 precision)
+    assert oracle.round_bf16(1.0 + 2**-8 + 2**-40) == 0x3F81
+    assert oracle.round_bf16(-(1.0 + 2**-8 + 2**-40)) == 0xBF81
+    assert oracle.round_bf16(0.0) == 0x0000
+    assert oracle.round_bf16(-0.0) == 0x8000
+    assert oracle.round_bf16(float("inf")) == 0x7F80
+    assert oracle.round_bf16(3.5e38) == 0x7F80           # overflow
+    assert oracle.round_bf16(2.0**-133) == 0x0001        # smallest subnormal
+    assert oracle.round_bf16(2.0**-134) == 0x0000        # tie to even (zero)
+    assert oracle.round_bf16(3 * 2.0**-134) == 0x0002    # tie to even (2)
+    assert oracle.round_bf16(255.5) == oracle.round_bf16(256.0) == 0x4380
+    for h in (0x3F80, 0x4000, 0x0001, 0x7F7F, 0x8001):
+        assert oracle.round_bf16(oracle.bf16_to_double(h)) == h
+
+
+def _rne_fraction_to_bf16(x: Fraction) -> int:
+    """Independent exact rounding of a rational to BF16 by search over the
+    representable neighbours (no floating point involved)."""
+    if x == 0:
+        return 0
+    sign = 0x8000 if x < 0 else 0
+    a = abs(x)
+    # candidate codes: find k with 2^k <= a < 2^(k+1)
+    k = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** k > a:
+        k -= 1
+    while Fraction(2) ** (k + 1) <= a:
+        k += 1
+    k = max(k, -126)
+    sp = Fraction(2) ** (k - 7)
+    lo = (a / sp).__floor__()
+    cands = [lo, lo + 1]
+    best = min(cands, key=lambda c: (abs(a - c * sp), c % 2))
+    val = best * sp
+    # encode val exactly
+    num = val / Fraction(2) ** -133
+    if num < 128:
+        return sign | int(num)
+    e = val.numerator.bit_length() - val.denominator.bit_length()
+    while Fraction(2) ** e > val:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= val:
+        e += 1
+    m = val / Fraction(2) ** (e - 7) - 128
+    return sign | ((e + 127) << 7) | int(m)
+
+
+# ---- the contraction -----------------------------------------------------------
+
+def _rand_codes(shape, seed, fmt, std=1.0):
+    return synth.normal_fp8(shape, seed, 0.0, std, fmt)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (2, 3, 16), (3, 2, 17),
+                                   (16, 17, 32), (17, 16, 3), (5, 7, 32)])
+@pytest.mark.parametrize("fa,fb", [(0, 0), (0, 1), (1, 0), (1, 1)])
+def test_gemm_exact_rational_bruteforce(M, N, K, fa, fb):
+    """Exact rational triple loop (values from torch's float8 decode) rounded
+    exactly to BF16 must equal the oracle bit for bit."""
+    A = _rand_codes((M, K), 11 + M * 7 + K, fa, std=4.0)
+    B = _rand_codes((N, K), 97 + N * 5 + K, fb, std=4.0)
+    da, db = torch_decode(A, fa), torch_decode(B, fb)
+    D, absdot, exact = oracle.gemm_nt(A, B, fa, fb, want_exact=True)
+    for m in range(M):
+        for n in range(N):
+            s = sum((Fraction(da[m, k]) * Fraction(db[n, k]) for k in range(K)),
+                    Fraction(0))
+            assert D[m, n] == _rne_fraction_to_bf16(s), (m, n)
+            assert Fraction(exact[m, n]) == s          # small K: double exact
+            assert absdot[m, n] == float(sum(abs(Fraction(da[m, k]) * Fraction(db[n, k]))
+                                             for k in range(K)))
+
+
+@pytest.mark.parametrize("fa,fb", [(0, 0), (0, 1), (1, 1)])
+def test_gemm_matches_numpy_matmul(fa, fb):
+    """Against a library routine: numpy float64 matmul of torch-decoded
+    operands; agreement to double rounding noise, and BF16 codes within one
+    ulp (double rounding near ties can move the last bit)."""
+    M, N, K = 33, 47, 1000
+    A = _rand_codes((M, K), 5, fa)
+    B = _rand_codes((N, K), 6, fb)
+    D, absdot, exact = oracle.gemm_nt(A, B, fa, fb, want_exact=True)
+    ref = torch_decode(A, fa) @ torch_decode(B, fb).T
+    assert np.all(np.abs(exact - ref) <= 1e-12 * absdot + 1e-300)
+    ref_bits = torch.from_numpy(ref.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    d = np.abs(D.astype(np.int64) - ref_bits.astype(np.int64))
+    assert d.max() <= 1
+    assert np.mean(d == 0) > 0.99
+
+
+@pytest.mark.parametrize("fmt,one", [(oracle.E4M3, 0x38), (oracle.E5M2, 0x3C)])
+def test_gemm_identity_gives_transpose(fmt, one):
+    """A = I (M = K) gives D = B^T exactly, since every FP8 value is exact in
+    BF16; a transposed operand or a wrong index fails this (B is random and
+    not symmetric)."""
+    K, N = 48, 40
+    A = np.zeros((K, K), np.uint8)
+    A[np.arange(K), np.arange(K)] = one
+    B = _rand_codes((N, K), 77, fmt)
+    D, _ = oracle.gemm_nt(A, B, fmt, fmt)
+    ref = torch.from_numpy(torch_decode(B, fmt).T.copy()).to(torch.bfloat16)
+    assert np.array_equal(D, ref.view(torch.int16).numpy().view(np.uint16))
+
+
+def test_gemm_permutation_permutes_rows():
+    K, N = 32, 24
+    perm = np.random.default_rng(3).permutation(K)
+    A = np.zeros((K, K), np.uint8)
+    A[np.arange(K), perm] = 0x38          # row m picks k = perm[m]
+    B = _rand_codes((N, K), 78, oracle.E4M3)
+    D, _ = oracle.gemm_nt(A, B)
+    Dt, _ = oracle.gemm_nt(np.eye(K, dtype=np.uint8) * 0x38, B)
+    assert np.array_equal(D, Dt[perm])
+
+
+def test_gemm_single_nonzero_k_is_exact_product():
+    fa, fb = oracle.E4M3, oracle.E5M2
+    K = 64
+    for kk, ca, cb in [(0, 0x38, 0x40), (17, 0x7E, 0x3C), (63, 0xB9, 0x3D), (5, 0x01, 0x04)]:
+        A = np.zeros((1, K), np.uint8)
+        B = np.zeros((1, K), np.uint8)
+        A[0, kk], B[0, kk] = ca, cb
+        D, _, ex = oracle.gemm_nt(A, B, fa, fb, want_exact=True)
+        p = oracle.decode_fp8(ca, fa) * oracle.decode_fp8(cb, fb)
+        assert ex[0, 0] == p
+        assert D[0, 0] == oracle.round_bf16(p)
+
+
+def test_gemm_integer_valued_products_exact():
+    """Entries in {-2,-1,0,1,2} (exact in both formats) with |sum| <= 256 give
+    exact BF16 results equal to an integer matmul."""
+    rng = np.random.default_rng(9)
+    vals = np.array([-2, -1, 0, 1, 2])
+    enc = {oracle.E4M3: {-2: 0xC0, -1: 0xB8, 0: 0x00, 1: 0x38, 2: 0x40},
+           oracle.E5M2: {-2: 0xC0, -1: 0xBC, 0: 0x00, 1: 0x3C, 2: 0x40}}
+    M, N, K = 20, 30, 64
+    ia = rng.choice(vals, (M, K))
+    ib = rng.choice(vals, (N, K))
+    for fa, fb in [(0, 0), (0, 1), (1, 1)]:
+        A = np.vectorize(enc[fa].get)(ia).astype(np.uint8)
+        B = np.vectorize(enc[fb].get)(ib).astype(np.uint8)
+        D, _ = oracle.gemm_nt(A, B, fa, fb)
+        ref = ia.astype(np.int64) @ ib.T.astype(np.int64)
+        assert np.abs(ref).max() <= 256
+        got = oracle.bf16_bits_to_f64(D)
+        assert np.array_equal(got, ref.astype(np.float64))
+
+
+@pytest.mark.parametrize("K", [1, 16, 128, 255, 256])
+def test_gemm_all_ones_is_K(K):
+    A = np.full((3, K), 0x38, np.uint8)
+    B = np.full((5, K), 0x38, np.uint8)
+    D, absdot = oracle.gemm_nt(A, B)
+    assert np.all(oracle.bf16_bits_to_f64(D) == K)
+    assert np.all(absdot == K)
+
+
+def test_gemm_entries_match_full():
+    A = _rand_codes((40, 200), 1, oracle.E4M3)
+    B = _rand_codes((30, 200), 2, oracle.E5M2)
+    D, absdot = oracle.gemm_nt(A, B, 0, 1)
+    ms = np.array([0, 39, 7, 20, 13])
+    ns = np.array([0, 29, 11, 3, 29])
+    d, ad, _ = oracle.gemm_nt_entries(A, B, ms, ns, 0, 1)
+    assert np.array_equal(d, D[ms, ns])
+    assert np.array_equal(ad, absdot[ms, ns])
+
+
+def test_gemm_threads_do_not_change_results():
+    A = _rand_codes((64, 300), 3, oracle.E4M3)
+    B = _rand_codes((50, 300), 4, oracle.E4M3)
+    D1, a1 = oracle.gemm_nt(A, B, nthreads=1)
+    D8, a8 = oracle.gemm_nt(A, B, nthreads=8)
+    assert np.array_equal(D1, D8) and np.array_equal(a1, a8)
+
+
+# ---- masked grouped --------------------------------------------------------------
+
+def test_grouped_masked_rows_and_untouched_padding():
+    G, M_max, N, K = 5, 24, 16, 48
+    A = _rand_codes((G, M_max, K), 21, oracle.E4M3)
+    B = _rand_codes((G, N, K), 22, oracle.E4M3)
+    mm = np.array([0, 1, 24, 7, 16], np.int32)
+    D0 = synth.u16_pattern((G, M_max, N), 23)
+    D, absdot = oracle.gemm_grouped_masked(A, B, mm, D0)
+    for g in range(G):
+        m = mm[g]
+        ref, _ = oracle.gemm_nt(A[g, :m], B[g])
+        assert np.array_equal(D[g, :m], ref)
+        assert np.array_equal(D[g, m:], D0[g, m:])      # never written
+        assert np.all(absdot[g, m:] == 0)
+
+
+def test_grouped_masked_nan_padding_does_not_leak():
+    G, M_max, N, K = 2, 16, 8, 32
+    A = _rand_codes((G, M_max, K), 31, oracle.E4M3)
+    B = _rand_codes((G, N, K), 32, oracle.E4M3)
+    mm = np.array([5, 9], np.int32)
+    A2 = A.copy()
+    for g in range(G):
+        A2[g, mm[g]:] = 0x7F                               # NaN codes in padding
+    D0 = np.zeros((G, M_max, N), np.uint16)
+    Da, _ = oracle.gemm_grouped_masked(A, B, mm, D0)
+    Db, _ = oracle.gemm_grouped_masked(A2, B, mm, D0)
+    assert np.array_equal(Da, Db)
+
+
+# ---- acceptance rule -----------------------------------------------------------
+
+def test_check_bf16_rule():
+    ref = np.array([0x3F80, 0x3F80, 0x3F80, 0x0000, 0x3F80], np.uint16)   # 1.0 ...
+    absdot = np.array([1.0, 1.0, 1.0, 1.0, 1e6])
+    one_ulp = np.array([0x3F81, 0x3F7F, 0x3F80, 0x0000, 0x3F83], np.uint16)
+    ok, rep = oracle.check_bf16(one_ulp, ref, absdot)
+    assert ok, rep                                   # last one: 3 ulp < 1e-6*1e6
+    two_ulp = np.array([0x3F82], np.uint16)
+    ok, _ = oracle.check_bf16(two_ulp, ref[:1], absdot[:1])
+    assert not ok
+    ok, _ = oracle.check_bf16(np.array([0x7FC0], np.uint16), ref[:1], absdot[:1])
+    assert not ok                                    # NaN never passes
+    assert oracle.ulp_bf16(np.array([0x3F80]))[0] == 2.0**-7
+    assert oracle.ulp_bf16(np.array([0x0000]))[0] == 0.0
+
+
+def test_planted_transpose_mistake_is_caught():
+    """A plausible oracle bug (B indexed as [k, n] instead of [n, k]) must be
+    caught by the identity pin: emulate it on the CPU and check the pin's
+    comparison fails."""
+    K = 32
+    A = np.eye(K, dtype=np.uint8) * 0x38
+    B = _rand_codes((K, K), 79, oracle.E4M3)
+    wrong, _ = oracle.gemm_nt(A, np.ascontiguousarray(B.T))    # planted bug
+    ref = torch.from_numpy(torch_decode(B, 0).T.copy()).to(torch.bfloat16)
+    assert not np.array_equal(wrong, ref.view(torch.int16).numpy().view(np.uint16))
+
+
+def test_planted_sign_mistake_is_caught():
+    """Negating a decoded term (a sign error) is caught by the rational brute
+    force: the results differ on random data."""
+    A = _rand_codes((4, 16), 81, oracle.E4M3)
+    B = _rand_codes((4, 16), 82, oracle.E4M3)
+    D, _ = oracle.gemm_nt(A, B)
+    Dneg, _ = oracle.gemm_nt(A ^ 0x80, B)           # planted: flipped sign bits
+    assert not np.array_equal(D, Dneg)
