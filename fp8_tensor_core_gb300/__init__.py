@@ -1,0 +1,151 @@
+"""fp8_tensor_core_gb300 -- FP8 GEMM for GB300 (sm_103a).
+
+Thin Python binding over the C ABI in ``include/fp8g.h``: it checks dtypes,
+shapes, contiguity and devices, then passes raw pointers and the current CUDA
+stream.  Every step of the computation runs in the library's CUDA kernels;
+there is no CPU or library fallback.
+
+    fp8_gemm_nt(A, B)                        D[M,N] = A[M,K] . B[N,K]^T (BF16)
+    fp8_gemm_grouped_masked(A, B, masked_m)  D[g,m,:] for m < masked_m[g]
+"""
+from __future__ import annotations
+
+import ctypes
+
+from . import _lib
+
+E4M3 = 0
+E5M2 = 1
+SWAP_AUTO = 0
+SWAP_ON = 1
+SWAP_OFF = 2
+DEBUG_ONE_STAGE = 0x10
+DEBUG_DROP_FIRST_LOAD = 0x20
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_MISALIGNED = 2
+ERR_UNSUPPORTED = 3
+ERR_CUDA = 4
+ERR_TIMEOUT = 5
+ERR_NO_DEVICE = 6
+ERR_MASKED_M_RANGE = 7
+
+
+class Fp8gError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__("%s: %s" % (where, fp8g_status_string(code)))
+
+
+def fp8g_status_string(code: int) -> str:
+    return _lib.load().fp8g_status_string(int(code)).decode()
+
+
+def fp8g_version() -> int:
+    return int(_lib.load().fp8g_version())
+
+
+def fp8g_set_wait_timeout_ns(ns: int) -> int:
+    return int(_lib.load().fp8g_set_wait_timeout_ns(int(ns)))
+
+
+def fp8g_get_device_status(stream=None):
+    """Synchronise `stream` (default: current), read and clear the device
+    status word.  Returns (code, block, role, detail)."""
+    import torch
+    info = (ctypes.c_int32 * 4)()
+    s = _stream_handle(stream)
+    rc = _lib.load().fp8g_get_device_status(info, s)
+    if rc != OK:
+        raise Fp8gError(rc, "fp8g_get_device_status")
+    return tuple(int(v) for v in info)
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _fp8_code(t, explicit):
+    import torch
+    if t.dtype == torch.float8_e4m3fn:
+        return E4M3 if explicit is None else explicit
+    if t.dtype == torch.float8_e5m2:
+        return E5M2 if explicit is None else explicit
+    if t.dtype == torch.uint8:
+        if explicit is None:
+            raise TypeError("uint8 operand needs an explicit FP8 format (E4M3 or E5M2)")
+        return explicit
+    raise TypeError("operand dtype %s is not an FP8 code type" % t.dtype)
+
+
+def _check_operand(t, name, ndim):
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dim() != ndim:
+        raise ValueError("%s must have %d dimensions, got %s" % (name, ndim, tuple(t.shape)))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous (row-major, K innermost)" % name)
+
+
+def fp8_gemm_nt(A, B, D=None, a_dtype=None, b_dtype=None, flags: int = 0, stream=None):
+    """D[M,N] (bf16) = A[M,K] . B[N,K]^T with FP8 A and B (float8 dtypes, or
+    uint8 codes with an explicit format).  Returns D."""
+    import torch
+    _check_operand(A, "A", 2)
+    _check_operand(B, "B", 2)
+    fa, fb = _fp8_code(A, a_dtype), _fp8_code(B, b_dtype)
+    M, K = A.shape
+    N, K2 = B.shape
+    if K != K2:
+        raise ValueError("K mismatch: A has %d, B has %d" % (K, K2))
+    if A.device != B.device:
+        raise ValueError("A and B on different devices")
+    if D is None:
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    else:
+        _check_operand(D, "D", 2)
+        if D.dtype != torch.bfloat16 or tuple(D.shape) != (M, N) or D.device != A.device:
+            raise ValueError("D must be a contiguous bf16 [M, N] tensor on A's device")
+    with torch.cuda.device(A.device):
+        rc = _lib.load().fp8_gemm_nt(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K,
+                                     fa, fb, int(flags), _stream_handle(stream))
+    if rc != OK:
+        raise Fp8gError(rc, "fp8_gemm_nt")
+    return D
+
+
+def fp8_gemm_grouped_masked(A, B, masked_m, D=None, max_m_hint: int = 0, a_dtype=None,
+                            b_dtype=None, flags: int = 0, stream=None):
+    """Masked grouped GEMM: A[G,M_max,K], B[G,N,K], masked_m int32[G] on the
+    device.  Rows m < masked_m[g] of D[g] are written; the others are left
+    untouched.  Returns D (allocated uninitialised if not given)."""
+    import torch
+    _check_operand(A, "A", 3)
+    _check_operand(B, "B", 3)
+    fa, fb = _fp8_code(A, a_dtype), _fp8_code(B, b_dtype)
+    G, M_max, K = A.shape
+    G2, N, K2 = B.shape
+    if G != G2 or K != K2:
+        raise ValueError("shape mismatch: A %s, B %s" % (tuple(A.shape), tuple(B.shape)))
+    if not masked_m.is_cuda or masked_m.dtype != torch.int32 or tuple(masked_m.shape) != (G,) \
+            or not masked_m.is_contiguous():
+        raise ValueError("masked_m must be a contiguous int32 CUDA tensor of shape [G]")
+    if D is None:
+        D = torch.empty((G, M_max, N), dtype=torch.bfloat16, device=A.device)
+    else:
+        _check_operand(D, "D", 3)
+        if D.dtype != torch.bfloat16 or tuple(D.shape) != (G, M_max, N):
+            raise ValueError("D must be a contiguous bf16 [G, M_max, N] tensor")
+    with torch.cuda.device(A.device):
+        rc = _lib.load().fp8_gemm_grouped_masked(
+            A.data_ptr(), B.data_ptr(), D.data_ptr(), masked_m.data_ptr(), G, M_max, N, K,
+            int(max_m_hint), fa, fb, int(flags), _stream_handle(stream))
+    if rc != OK:
+        raise Fp8gError(rc, "fp8_gemm_grouped_masked")
+    return D

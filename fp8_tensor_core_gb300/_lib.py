@@ -1,0 +1,52 @@
+"""ctypes loader for the in-tree CUDA library ``_build/libfp8g.so``.
+
+There is no fallback: if the library has not been built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libfp8g.so")
+
+# Symbols declared in include/fp8g.h, with their ctypes signatures.
+_c_void_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+SIGNATURES = {
+    "fp8_gemm_nt": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _i64, _i64,
+                                   ctypes.c_int, ctypes.c_int, ctypes.c_uint32, _c_void_p]),
+    "fp8_gemm_grouped_masked": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                               _i64, _i64, _i64, _i64, _i64, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_uint32, _c_void_p]),
+    "fp8g_get_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), _c_void_p]),
+    "fp8g_set_wait_timeout_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
+    "fp8g_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "fp8g_version": (ctypes.c_int, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class LibraryNotBuilt(RuntimeError):
+    pass
+
+
+def load() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise LibraryNotBuilt(
+                "fp8g CUDA library not built (%s missing); run "
+                "`python -c 'import __graft_entry__ as g; g.build()'`" % LIB_PATH)
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib

@@ -1,0 +1,410 @@
+// Host side of the C ABI declared in include/fp8g.h: argument validation,
+// variant selection (SwapAB or not, tile sizes, pipeline depth, split-K),
+// TMA tensor-map encoding and kernel launch.
+//
+// Sources: "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践"
+// (sheratonhq.com/news/187119) §1.3 (large shapes fill every SM; small
+// shapes take a simpler path), §3.3 (TMA descriptors prepared by the host),
+// §6.2-6.4 (every K step clipped to the real length; alignment of the
+// descriptor fields matters); "一次“转置”，半张算力：DeepSeek SwapAB 漂流史"
+// (hwcomputing.csdn.net) §3.1 (ENABLE_SWAPAB switch), §3.5 (swap only
+// pays for small per-expert token counts; the switch-over depends on the
+// shape and the SM count); "MLS 三个访存 Bug 深度剖析" Bug 1 (base
+// addresses and offsets kept in 64 bits: tensor maps take full pointers).
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fp8g.h"
+#include "kernels.cuh"
+
+namespace fp8g {
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+constexpr int kMaxDevices = 64;
+// SwapAB is chosen automatically when a problem has at most this many
+// token rows per group (the weights then fill the 128-row MMA side and the
+// tokens a narrow runtime N).
+constexpr int64_t kSwapAutoMaxTokens = 128;
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
+
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0;
+    int cc_major = 0, cc_minor = 0;
+    int smem_optin = 0;
+};
+
+struct Workspace {
+    float *ws = nullptr;
+    size_t ws_bytes = 0;
+    int32_t *counters = nullptr;
+    size_t counter_bytes = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+Workspace g_ws[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+int current_device(int *dev, DeviceInfo *info)
+{
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess || count <= 0) {
+        cudaGetLastError();
+        return FP8G_ERR_NO_DEVICE;
+    }
+    if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices)
+        return FP8G_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo &d = g_dev[*dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, *dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, *dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, *dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, *dev) !=
+                cudaSuccess)
+            return FP8G_ERR_CUDA;
+        d.ready = true;
+    }
+    *info = d;
+    // The kernels are built for sm_103a only.
+    if (info->cc_major != 10 || info->cc_minor != 3)
+        return FP8G_ERR_UNSUPPORTED;
+    return FP8G_OK;
+}
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 3-D map over a [groups, rows, k] byte tensor, box {128 bytes of K, box_rows, 1},
+// 128-byte swizzle, out-of-bounds elements read as zero.
+bool make_map(CUtensorMap *m, const void *base, int64_t k, int64_t rows, int64_t groups,
+              uint32_t box_rows)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(groups)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(k),
+                                   static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(k)};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kBlockK), box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    std::memset(m, 0, sizeof(*m));
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int stage_budget(const DeviceInfo &d)
+{
+    return d.smem_optin - kCtlBytes - kSmemAlignPad;
+}
+
+int pick_stages(const DeviceInfo &d, int stage_bytes, uint32_t flags)
+{
+    if (flags & FP8G_DEBUG_ONE_STAGE)
+        return 1;
+    const int s = stage_budget(d) / stage_bytes;
+    return std::max(1, std::min(kMaxStages, s));
+}
+
+// Split-K workspace of the current device, grown on demand (the first call
+// needing a larger one allocates; later calls reuse it).
+int ensure_workspace(int dev, size_t ws_bytes, size_t counter_bytes, float **ws, int32_t **counters)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    Workspace &w = g_ws[dev];
+    if (w.ws_bytes < ws_bytes) {
+        if (w.ws)
+            cudaFree(w.ws);
+        w.ws = nullptr;
+        w.ws_bytes = 0;
+        if (cudaMalloc(&w.ws, ws_bytes) != cudaSuccess)
+            return FP8G_ERR_CUDA;
+        w.ws_bytes = ws_bytes;
+    }
+    if (w.counter_bytes < counter_bytes) {
+        if (w.counters)
+            cudaFree(w.counters);
+        w.counters = nullptr;
+        w.counter_bytes = 0;
+        if (cudaMalloc(&w.counters, counter_bytes) != cudaSuccess)
+            return FP8G_ERR_CUDA;
+        if (cudaMemset(w.counters, 0, counter_bytes) != cudaSuccess)
+            return FP8G_ERR_CUDA;
+        w.counter_bytes = counter_bytes;
+    }
+    *ws = w.ws;
+    *counters = w.counters;
+    return FP8G_OK;
+}
+
+int check_common(const void *A, const void *B, void *D, int64_t N, int64_t K, int a_dtype,
+                 int b_dtype)
+{
+    if (!A || !B || !D)
+        return FP8G_ERR_INVALID_ARG;
+    if (N <= 0 || K <= 0 || N > kMaxDim || K > kMaxDim)
+        return FP8G_ERR_INVALID_ARG;
+    if (K % 16 != 0 || N % 8 != 0)
+        return FP8G_ERR_INVALID_ARG;
+    if ((a_dtype != FP8G_E4M3 && a_dtype != FP8G_E5M2) ||
+        (b_dtype != FP8G_E4M3 && b_dtype != FP8G_E5M2))
+        return FP8G_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(D))
+        return FP8G_ERR_MISALIGNED;
+    return FP8G_OK;
+}
+
+// N tile of the non-swapped kernel: the candidate with the fewest tile
+// column-equivalents over whole waves of SMs.
+int pick_tile_n(int64_t m_tiles_total, int64_t N, int sms)
+{
+    static const int cands[] = {256, 224, 192, 160, 128};
+    int best = 256;
+    double best_cost = 1e300;
+    for (int tn : cands) {
+        const int64_t units = m_tiles_total * cdiv(N, tn);
+        const int64_t waves = cdiv(units, sms);
+        const double cost = static_cast<double>(waves) * (tn + 32);
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = tn;
+        }
+    }
+    return best;
+}
+
+// K partitions for the swap kernel: fewest k-block-equivalents over whole
+// waves, each unit charged one extra k-block for its epilogue.
+int pick_k_splits(int64_t tiles, int num_kb, int sms)
+{
+    int best = 1;
+    double best_cost = 1e300;
+    const int max_ks = std::min(16, num_kb);
+    for (int ks = 1; ks <= max_ks; ++ks) {
+        const int64_t waves = cdiv(tiles * ks, sms);
+        const double cost = static_cast<double>(waves) * (static_cast<double>(cdiv(num_kb, ks)) + 1.0);
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = ks;
+        }
+    }
+    return best;
+}
+
+struct Problem {
+    const void *A, *B;
+    void *D;
+    const int32_t *masked_m;
+    int64_t G, rows_a, N, K;
+    int64_t token_hint;   // expected valid tokens per group (<= rows_a)
+    int a_dtype, b_dtype;
+    uint32_t flags;
+};
+
+int launch(const Problem &p, cudaStream_t stream)
+{
+    int dev = 0;
+    DeviceInfo info;
+    int st = current_device(&dev, &info);
+    if (st != FP8G_OK)
+        return st;
+
+    const uint32_t mode = p.flags & FP8G_SWAP_MASK;
+    if (mode == 3u)
+        return FP8G_ERR_INVALID_ARG;
+    const bool swap = mode == FP8G_SWAP_ON || (mode == FP8G_SWAP_AUTO && p.token_hint <= kSwapAutoMaxTokens);
+    const int num_kb = static_cast<int>(cdiv(p.K, kBlockK));
+
+    GemmArgs args;
+    std::memset(&args, 0, sizeof(args));
+    args.rows_a = static_cast<int32_t>(p.rows_a);
+    args.n = static_cast<int32_t>(p.N);
+    args.k = static_cast<int32_t>(p.K);
+    args.groups = static_cast<int32_t>(p.G);
+    args.num_kb = num_kb;
+    args.masked_m = p.masked_m;
+    args.d = p.D;
+    args.a_fmt = static_cast<uint32_t>(p.a_dtype);
+    args.b_fmt = static_cast<uint32_t>(p.b_dtype);
+    args.flags = p.flags;
+    args.timeout_ns = g_timeout_ns.load();
+    args.k_splits = 1;
+    args.raster_band = 1;
+
+    CUtensorMap tm0, tm1;
+    if (swap) {
+        const int64_t cap = std::min<int64_t>(256, cdiv(std::max<int64_t>(p.token_hint, 1), 16) * 16);
+        const int64_t chunks = cdiv(p.rows_a, cap);
+        const int64_t n_tiles = cdiv(p.N, kTileM);
+        const int64_t tiles_upper = p.G * chunks * n_tiles;
+        // Dense problems: the tile count is exact, so split K to fill the SMs.
+        int ks = 1;
+        if (!p.masked_m)
+            ks = pick_k_splits(tiles_upper, num_kb, info.sms);
+        if (tiles_upper * ks > kMaxDim)
+            return FP8G_ERR_UNSUPPORTED;
+        args.tile_n = static_cast<int32_t>(cap);
+        args.stage_bytes = static_cast<int32_t>(kTileM * kBlockK + cap * kBlockK);
+        args.stages = pick_stages(info, args.stage_bytes, p.flags);
+        args.k_splits = ks;
+        if (ks > 1) {
+            const size_t ws_bytes = static_cast<size_t>(tiles_upper) * ks * kTileM * cap * sizeof(float);
+            const size_t cnt_bytes = static_cast<size_t>(tiles_upper) * 4 * sizeof(int32_t);
+            st = ensure_workspace(dev, ws_bytes, cnt_bytes, &args.workspace, &args.counters);
+            if (st != FP8G_OK)
+                return st;
+        }
+        if (!make_map(&tm0, p.B, p.K, p.N, p.G, kTileM) || !make_map(&tm1, p.A, p.K, p.rows_a, p.G, 16))
+            return FP8G_ERR_CUDA;
+        const int grid = static_cast<int>(std::min<int64_t>(tiles_upper * ks, info.sms));
+        if (grid <= 0)
+            return FP8G_OK;
+        return launch_gemm_swap(tm0, tm1, args, grid, static_cast<size_t>(info.smem_optin), stream) == cudaSuccess
+                   ? FP8G_OK
+                   : FP8G_ERR_CUDA;
+    }
+
+    const int64_t m_tiles = cdiv(p.rows_a, kTileM);
+    const int tile_n = pick_tile_n(p.G * m_tiles, p.N, info.sms);
+    const int64_t units_upper = p.G * m_tiles * cdiv(p.N, tile_n);
+    if (units_upper > kMaxDim)
+        return FP8G_ERR_UNSUPPORTED;
+    args.tile_n = tile_n;
+    args.stage_bytes = kTileM * kBlockK + tile_n * kBlockK;
+    args.stages = pick_stages(info, args.stage_bytes, p.flags);
+    // Bands of M tiles whose token rows total about 48 MB stay resident in L2
+    // while the weight tiles stream past them.
+    const int64_t band = (48ll << 20) / (kTileM * p.K);
+    args.raster_band = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(band, m_tiles)));
+    if (!make_map(&tm0, p.A, p.K, p.rows_a, p.G, kTileM) ||
+        !make_map(&tm1, p.B, p.K, p.N, p.G, static_cast<uint32_t>(tile_n)))
+        return FP8G_ERR_CUDA;
+    const int grid = static_cast<int>(std::min<int64_t>(units_upper, info.sms));
+    if (grid <= 0)
+        return FP8G_OK;
+    return launch_gemm_mn(tm0, tm1, args, grid, static_cast<size_t>(info.smem_optin), stream) == cudaSuccess
+               ? FP8G_OK
+               : FP8G_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace fp8g
+
+using namespace fp8g;
+
+extern "C" int fp8_gemm_nt(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K,
+                           int a_dtype, int b_dtype, uint32_t flags, cudaStream_t stream)
+{
+    int st = check_common(A, B, D, N, K, a_dtype, b_dtype);
+    if (st != FP8G_OK)
+        return st;
+    if (M <= 0 || M > kMaxDim)
+        return FP8G_ERR_INVALID_ARG;
+    Problem p{A, B, D, nullptr, 1, M, N, K, M, a_dtype, b_dtype, flags};
+    return launch(p, stream);
+}
+
+extern "C" int fp8_gemm_grouped_masked(const void *A, const void *B, void *D, const int32_t *masked_m,
+                                       int64_t G, int64_t M_max, int64_t N, int64_t K,
+                                       int64_t max_m_hint, int a_dtype, int b_dtype, uint32_t flags,
+                                       cudaStream_t stream)
+{
+    int st = check_common(A, B, D, N, K, a_dtype, b_dtype);
+    if (st != FP8G_OK)
+        return st;
+    if (!masked_m)
+        return FP8G_ERR_INVALID_ARG;
+    if (G <= 0 || M_max <= 0 || M_max > kMaxDim || max_m_hint < 0 || max_m_hint > M_max)
+        return FP8G_ERR_INVALID_ARG;
+    if (G > kMaxGroups)
+        return FP8G_ERR_UNSUPPORTED;
+    if (G * M_max > kMaxDim || G * N > kMaxDim)
+        return FP8G_ERR_UNSUPPORTED;
+    if (!aligned16(masked_m))
+        return FP8G_ERR_MISALIGNED;
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, masked_m) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8G_ERR_INVALID_ARG;
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+        return FP8G_ERR_INVALID_ARG;
+    const int64_t hint = max_m_hint > 0 ? max_m_hint : M_max;
+    Problem p{A, B, D, masked_m, G, M_max, N, K, hint, a_dtype, b_dtype, flags};
+    return launch(p, stream);
+}
+
+extern "C" int fp8g_get_device_status(int32_t *info, cudaStream_t stream)
+{
+    if (!info)
+        return FP8G_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return FP8G_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess)
+        return FP8G_ERR_CUDA;
+    if (read_and_clear_status(info) != cudaSuccess)
+        return FP8G_ERR_CUDA;
+    if (info[0] == FP8G_ERR_TIMEOUT) {
+        // An aborted split-K launch can leave arrival counts behind.
+        std::lock_guard<std::mutex> lk(g_mu);
+        Workspace &w = g_ws[dev];
+        if (w.counters && cudaMemset(w.counters, 0, w.counter_bytes) != cudaSuccess)
+            return FP8G_ERR_CUDA;
+    }
+    return FP8G_OK;
+}
+
+extern "C" uint64_t fp8g_set_wait_timeout_ns(uint64_t ns)
+{
+    return g_timeout_ns.exchange(ns ? ns : kDefaultTimeoutNs);
+}
+
+extern "C" const char *fp8g_status_string(int code)
+{
+    switch (code) {
+    case FP8G_OK: return "FP8G_OK";
+    case FP8G_ERR_INVALID_ARG: return "FP8G_ERR_INVALID_ARG";
+    case FP8G_ERR_MISALIGNED: return "FP8G_ERR_MISALIGNED";
+    case FP8G_ERR_UNSUPPORTED: return "FP8G_ERR_UNSUPPORTED";
+    case FP8G_ERR_CUDA: return "FP8G_ERR_CUDA";
+    case FP8G_ERR_TIMEOUT: return "FP8G_ERR_TIMEOUT";
+    case FP8G_ERR_NO_DEVICE: return "FP8G_ERR_NO_DEVICE";
+    case FP8G_ERR_MASKED_M_RANGE: return "FP8G_ERR_MASKED_M_RANGE";
+    default: return "FP8G_UNKNOWN_STATUS";
+    }
+}
+
+extern "C" int fp8g_version(void) { return 100; }

@@ -1,0 +1,732 @@
+// FP8 GEMM kernels for sm_103a (GB300).
+//
+// Both kernels are persistent (one CTA per SM, looping over work units) and
+// warp-specialised:
+//   warp 0      loader: TMA copies of 128-byte K slices into a ring of
+//               shared-memory stages (full/empty mbarrier pairs);
+//   warp 1      MMA issuer: one thread issues tcgen05.mma kind::f8f6f4 into
+//               a TMEM accumulator (two accumulators, so the epilogue of one
+//               unit overlaps the main loop of the next);
+//   warps 2-5   epilogue: tcgen05.ld TMEM -> registers, FP32 -> BF16 (round
+//               to nearest even), stores to D.
+//
+// k_gemm_mn    tokens (A) on the MMA M side (128-row tiles), weights (B) on
+//              N (tile_n columns).  Dense, or grouped with a valid-row count
+//              per group.
+// k_gemm_swap  SwapAB: weights (B) on the M side (128 weight rows), tokens
+//              (A) on N with a per-unit runtime N = valid tokens rounded up
+//              to 16, written into the instruction descriptor.  Optional
+//              split-K with a deterministic fixed-order reduction.
+//
+// Sources: "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践"
+// (sheratonhq.com/news/187119) §3.3 (producer/consumer warp roles), §4.3
+// (multi-stage ring), §6.2-6.4 (K tails clipped exactly, no wrap-around);
+// "一次“转置”，半张算力：DeepSeek SwapAB 漂流史" (hwcomputing.csdn.net)
+// §1.1 (TMEM 128 lanes x 512 columns, lane m holds row m; M in {64,128} for
+// one CTA, N a multiple of 8 up to 256 and writable at run time), §3.2
+// (swap operand roles), §3.3 (instruction-descriptor N set to the valid
+// tokens; the first MMA of a tile does not accumulate), §3.5 (epilogue
+// walks TMEM columns = tokens).
+//
+// Every barrier wait is bounded (GemmArgs::timeout_ns).  When a wait runs
+// out the block records FP8G_ERR_TIMEOUT, every role leaves its loop, the
+// loader waits (bounded) for the copies it issued, the MMA issuer waits
+// (bounded) for its tensor-core work, TMEM is freed and the block returns.
+#include <cuda_bf16.h>
+
+#include "fp8g.h"
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace fp8g {
+
+// Per-device status word: {code, block, role, detail}.  First error wins.
+__device__ int32_t g_status[4];
+
+__device__ __forceinline__ void record_status(int32_t code, int32_t role, int32_t detail)
+{
+    if (atomicCAS(&g_status[0], 0, code) == 0) {
+        g_status[1] = static_cast<int32_t>(blockIdx.x);
+        g_status[2] = role;
+        g_status[3] = detail;
+        __threadfence();
+    }
+}
+
+struct alignas(16) SmemCtl {
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    volatile int32_t abort;
+    int32_t units_total;
+    int32_t pad_;
+    int32_t group_prefix[kMaxGroups + 1];  // work units before group g
+    int32_t group_m[kMaxGroups];           // valid token rows of group g (clamped)
+};
+static_assert(sizeof(SmemCtl) <= kCtlBytes, "control block too large");
+
+// Warp-uniform bounded wait on an mbarrier phase.  Returns false when the
+// block is aborting (another role timed out) or this wait ran out.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, SmemCtl &ctl,
+                                          uint64_t timeout_ns, int role, int detail)
+{
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity)))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity)))
+            return true;
+        if ((it & 15u) == 0) {
+            int stop = 0;
+            if ((threadIdx.x & 31) == 0) {
+                if (ctl.abort) {
+                    stop = 1;
+                } else if (globaltimer_ns() - t0 > timeout_ns) {
+                    stop = 1;
+                    ctl.abort = 1;
+                    record_status(FP8G_ERR_TIMEOUT, role, detail);
+                }
+            }
+            if (__shfl_sync(0xffffffffu, stop, 0))
+                return false;
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag (used while draining).
+__device__ __forceinline__ bool warp_wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns)
+{
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity)))
+            return true;
+        int late = 0;
+        if ((threadIdx.x & 31) == 0)
+            late = (globaltimer_ns() - t0 > timeout_ns) ? 1 : 0;
+        if (__shfl_sync(0xffffffffu, late, 0))
+            return false;
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_bits, uint32_t hi_bits)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo_bits), __uint_as_float(hi_bits));
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Group table: valid rows per group (clamped to [0, rows_a]) and the
+// exclusive prefix of work units.  Run by one warp.
+template <typename UnitsFn>
+__device__ void build_group_table(SmemCtl &ctl, const GemmArgs &a, UnitsFn units_of)
+{
+    const int lane = threadIdx.x & 31;
+    int running = 0;
+    for (int base = 0; base < a.groups; base += 32) {
+        const int g = base + lane;
+        int cnt = 0;
+        if (g < a.groups) {
+            int m = a.masked_m ? __ldg(a.masked_m + g) : a.rows_a;
+            if (m < 0 || m > a.rows_a) {
+                if (blockIdx.x == 0)
+                    record_status(FP8G_ERR_MASKED_M_RANGE, kRoleScheduler, g);
+                m = m < 0 ? 0 : a.rows_a;
+            }
+            ctl.group_m[g] = m;
+            cnt = units_of(m);
+        }
+        int x = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o)
+                x += y;
+        }
+        if (g < a.groups)
+            ctl.group_prefix[g] = running + x - cnt;
+        running += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (lane == 0) {
+        ctl.group_prefix[a.groups] = running;
+        ctl.units_total = running;
+    }
+}
+
+// Group g with prefix[g] <= u < prefix[g+1].
+__device__ __forceinline__ int find_group(const SmemCtl &ctl, int groups, int u)
+{
+    int lo = 0, hi = groups;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (ctl.group_prefix[mid] <= u)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Shared-memory carve-up common to both kernels: `stages` stages of
+// `stage_bytes` starting at a 1024-byte aligned base, then the control block.
+struct Smem {
+    uint8_t *stages;
+    SmemCtl *ctl;
+};
+
+__device__ __forceinline__ Smem carve(uint8_t *raw, const GemmArgs &a)
+{
+    const uint32_t base = smem_addr(raw);
+    const uint32_t pad = (1024u - (base & 1023u)) & 1023u;
+    Smem s;
+    s.stages = raw + pad;
+    s.ctl = reinterpret_cast<SmemCtl *>(s.stages + static_cast<size_t>(a.stages) * a.stage_bytes);
+    return s;
+}
+
+__device__ __forceinline__ void init_barriers(SmemCtl &ctl, int stages)
+{
+    for (int s = 0; s < stages; ++s) {
+        mbar_init(smem_addr(&ctl.full[s]), 1);
+        mbar_init(smem_addr(&ctl.empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+        mbar_init(smem_addr(&ctl.tfull[b]), 1);
+        mbar_init(smem_addr(&ctl.tempty[b]), 4 * 32);
+    }
+    mbar_init(smem_addr(&ctl.drain), 1);
+    ctl.abort = 0;
+    fence_mbar_init();
+}
+
+// Loader epilogue: after the last issue, wait until the consumer has
+// released every stage (so no tensor-core arrive is still headed for this
+// block's shared memory).  When aborting, instead wait for the copies
+// still in flight.
+__device__ __forceinline__ void loader_tail(SmemCtl &ctl, const GemmArgs &a, int stage,
+                                            uint32_t phase, long long issued, bool aborted,
+                                            bool dropped_first)
+{
+    if (!aborted) {
+        int st = stage;
+        uint32_t ph = phase;
+        bool ok = true;
+        for (int i = 0; i < a.stages; ++i) {
+            if (!warp_wait(smem_addr(&ctl.empty[st]), ph ^ 1u, ctl, a.timeout_ns, kRoleLoader, st)) {
+                ok = false;
+                break;
+            }
+            if (++st == a.stages) {
+                st = 0;
+                ph ^= 1u;
+            }
+        }
+        if (ok)
+            return;
+        // Another role aborted while copies may still be landing: drain.
+    }
+    // Aborting: stage s was last filled in the current phase if s < stage,
+    // else in the previous one.
+    const long long n = issued < a.stages ? issued : a.stages;
+    for (int s = 0; s < a.stages; ++s) {
+        if (issued <= s && n < a.stages)
+            continue;                       // never filled
+        if (dropped_first && issued <= a.stages && s == 0)
+            continue;                       // its only fill was skipped on purpose
+        const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
+        warp_wait_drain(smem_addr(&ctl.full[s]), par, a.timeout_ns);
+    }
+}
+
+// MMA issuer tail: wait until every tensor-core operation it issued has
+// completed, so TMEM can be freed.
+__device__ __forceinline__ void mma_drain(SmemCtl &ctl, const GemmArgs &a, bool issued_any)
+{
+    if (!issued_any)
+        return;
+    if ((threadIdx.x & 31) == 0)
+        mma_commit(smem_addr(&ctl.drain));
+    __syncwarp();
+    warp_wait_drain(smem_addr(&ctl.drain), 0, a.timeout_ns);
+}
+
+// =====================================================================================
+// k_gemm_mn: tokens on M, weights on N.
+// =====================================================================================
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_mn(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+              const GemmArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const Smem sm = carve(smem_raw, a);
+    SmemCtl &ctl = *sm.ctl;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int n_tiles = ceil_div(a.n, a.tile_n);
+    const uint32_t a_bytes = kTileM * kBlockK;                  // 16 KB A box
+    const uint32_t tx_bytes = a_bytes + static_cast<uint32_t>(a.tile_n) * kBlockK;
+
+    if (threadIdx.x == 0)
+        init_barriers(ctl, a.stages);
+    if (warp == 0)
+        build_group_table(ctl, a, [&](int m) { return ceil_div(m, kTileM) * n_tiles; });
+    if (warp == 1) {
+        tmem_alloc(smem_addr(&ctl.tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ctl.tmem_base;
+    const int total = ctl.units_total;
+
+    // Unit u -> (group, first row, first column).  Inside a group, bands of
+    // raster_band M tiles are walked M-fastest so concurrent CTAs share the
+    // same weight tiles and a bounded set of token tiles in L2.
+    auto decode = [&](int u, int &g, int &m0, int &n0, int &m_valid) {
+        g = find_group(ctl, a.groups, u);
+        const int local = u - ctl.group_prefix[g];
+        m_valid = ctl.group_m[g];
+        const int m_tiles = ceil_div(m_valid, kTileM);
+        const int band_units = a.raster_band * n_tiles;
+        const int band = local / band_units;
+        const int in_band = local - band * band_units;
+        const int rows_left = m_tiles - band * a.raster_band;
+        const int gm = rows_left < a.raster_band ? rows_left : a.raster_band;
+        m0 = (band * a.raster_band + in_band % gm) * kTileM;
+        n0 = (in_band / gm) * a.tile_n;
+    };
+
+    if (warp == 0) {
+        // ------------------------------- loader -------------------------------
+        if (lane == 0) {
+            tma_prefetch_map(&tm_a);
+            tma_prefetch_map(&tm_b);
+        }
+        int stage = 0;
+        uint32_t phase = 0;
+        long long issued = 0;
+        bool aborted = false;
+        const bool drop = (a.flags & FP8G_DEBUG_DROP_FIRST_LOAD) && blockIdx.x == 0;
+        for (int u = blockIdx.x; u < total && !aborted; u += gridDim.x) {
+            int g, m0, n0, mv;
+            decode(u, g, m0, n0, mv);
+            for (int kb = 0; kb < a.num_kb; ++kb) {
+                if (!warp_wait(smem_addr(&ctl.empty[stage]), phase ^ 1u, ctl, a.timeout_ns,
+                               kRoleLoader, stage)) {
+                    aborted = true;
+                    break;
+                }
+                if (lane == 0 && !(drop && issued == 0)) {
+                    uint8_t *sa = sm.stages + static_cast<size_t>(stage) * a.stage_bytes;
+                    const uint32_t fb = smem_addr(&ctl.full[stage]);
+                    mbar_arrive_expect_tx(fb, tx_bytes);
+                    tma_load_3d(smem_addr(sa), &tm_a, fb, kb * kBlockK, m0, g);
+                    tma_load_3d(smem_addr(sa + a_bytes), &tm_b, fb, kb * kBlockK, n0, g);
+                }
+                __syncwarp();
+                ++issued;
+                if (++stage == a.stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        loader_tail(ctl, a, stage, phase, issued, aborted, drop);
+    } else if (warp == 1) {
+        // ----------------------------- MMA issuer -----------------------------
+        const uint32_t idesc = make_idesc(a.a_fmt, a.b_fmt, kTileM, a.tile_n);
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool issued_any = false;
+        for (int u = blockIdx.x; u < total; u += gridDim.x) {
+            if (!warp_wait(smem_addr(&ctl.tempty[acc]), acc_phase ^ 1u, ctl, a.timeout_ns, kRoleMma,
+                           100 + acc))
+                break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccStride);
+            bool ok = true;
+            for (int kb = 0; kb < a.num_kb; ++kb) {
+                if (!warp_wait(smem_addr(&ctl.full[stage]), phase, ctl, a.timeout_ns, kRoleMma,
+                               stage)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t sa = smem_addr(sm.stages + static_cast<size_t>(stage) * a.stage_bytes);
+                    const uint64_t adesc = smem_desc_k_sw128(sa);
+                    const uint64_t bdesc = smem_desc_k_sw128(sa + a_bytes);
+#pragma unroll
+                    for (int k = 0; k < kBlockK / 32; ++k) {
+                        // +32 bytes of K per instruction = +2 in the address field
+                        mma_f8f6f4(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc,
+                                   (kb | k) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(smem_addr(&ctl.empty[stage]));
+                }
+                __syncwarp();
+                issued_any = true;
+                if (++stage == a.stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok)
+                break;
+            if (lane == 0)
+                mma_commit(smem_addr(&ctl.tfull[acc]));
+            __syncwarp();
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+        mma_drain(ctl, a, issued_any);
+    } else {
+        // ------------------------------ epilogue ------------------------------
+        const int q = warp & 3;  // TMEM lane quadrant this warp may read
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        __nv_bfloat16 *dout = static_cast<__nv_bfloat16 *>(a.d);
+        for (int u = blockIdx.x; u < total; u += gridDim.x) {
+            int g, m0, n0, mv;
+            decode(u, g, m0, n0, mv);
+            if (!warp_wait(smem_addr(&ctl.tfull[acc]), acc_phase, ctl, a.timeout_ns, kRoleEpilogue,
+                           200 + acc))
+                break;
+            tc_fence_after();
+            const int row = m0 + q * 32 + lane;
+            const bool row_ok = row < mv;
+            __nv_bfloat16 *drow =
+                dout + (static_cast<int64_t>(g) * a.rows_a + row) * static_cast<int64_t>(a.n);
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(acc * kAccStride);
+            for (int c = 0; c < a.tile_n; c += 32) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c), r);
+                if (row_ok) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int col = n0 + c + 8 * j;
+                        if (col < a.n) {
+                            uint4 v;
+                            v.x = pack_bf16x2(r[8 * j + 0], r[8 * j + 1]);
+                            v.y = pack_bf16x2(r[8 * j + 2], r[8 * j + 3]);
+                            v.z = pack_bf16x2(r[8 * j + 4], r[8 * j + 5]);
+                            v.w = pack_bf16x2(r[8 * j + 6], r[8 * j + 7]);
+                            *reinterpret_cast<uint4 *>(drow + col) = v;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(smem_addr(&ctl.tempty[acc]));
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// =====================================================================================
+// k_gemm_swap: SwapAB.  Weights (B) on M, tokens (A) on a runtime N.
+// =====================================================================================
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_swap(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_t,
+                const GemmArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const Smem sm = carve(smem_raw, a);
+    SmemCtl &ctl = *sm.ctl;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int n_tiles = ceil_div(a.n, kTileM);   // 128 weight rows per tile
+    const int cap = a.tile_n;                    // tokens per chunk
+    const int ks_n = a.k_splits;
+    const uint32_t w_bytes = kTileM * kBlockK;   // 16 KB weight box
+    constexpr int kTokBox = 16;                  // token rows per TMA box
+    constexpr uint32_t kTokBoxBytes = kTokBox * kBlockK;
+
+    if (threadIdx.x == 0)
+        init_barriers(ctl, a.stages);
+    if (warp == 0)
+        build_group_table(ctl, a, [&](int m) { return ceil_div(m, cap) * n_tiles * ks_n; });
+    if (warp == 1) {
+        tmem_alloc(smem_addr(&ctl.tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ctl.tmem_base;
+    const int total = ctl.units_total;
+
+    // Unit u -> group, token chunk, weight tile, K split (split fastest, so
+    // the parts of one output tile run close together in time).
+    struct U {
+        int g, tok0, n_tok, n_mma, w0, ks, kb0, kb1, tile;
+    };
+    auto decode = [&](int u) {
+        U x;
+        x.g = find_group(ctl, a.groups, u);
+        const int local = u - ctl.group_prefix[x.g];
+        x.ks = local % ks_n;
+        const int rest = local / ks_n;
+        const int nt = rest % n_tiles;
+        const int chunk = rest / n_tiles;
+        x.tok0 = chunk * cap;
+        const int left = ctl.group_m[x.g] - x.tok0;
+        x.n_tok = left < cap ? left : cap;
+        x.n_mma = (x.n_tok + 15) & ~15;
+        x.w0 = nt * kTileM;
+        x.kb0 = static_cast<int>((static_cast<long long>(x.ks) * a.num_kb) / ks_n);
+        x.kb1 = static_cast<int>((static_cast<long long>(x.ks + 1) * a.num_kb) / ks_n);
+        x.tile = u / ks_n;
+        return x;
+    };
+
+    if (warp == 0) {
+        // ------------------------------- loader -------------------------------
+        if (lane == 0) {
+            tma_prefetch_map(&tm_w);
+            tma_prefetch_map(&tm_t);
+        }
+        int stage = 0;
+        uint32_t phase = 0;
+        long long issued = 0;
+        bool aborted = false;
+        const bool drop = (a.flags & FP8G_DEBUG_DROP_FIRST_LOAD) && blockIdx.x == 0;
+        const uint64_t w_policy = policy_evict_first();   // weights are read once
+        for (int u = blockIdx.x; u < total && !aborted; u += gridDim.x) {
+            const U x = decode(u);
+            const uint32_t tx = w_bytes + static_cast<uint32_t>(x.n_mma) * kBlockK;
+            for (int kb = x.kb0; kb < x.kb1; ++kb) {
+                if (!warp_wait(smem_addr(&ctl.empty[stage]), phase ^ 1u, ctl, a.timeout_ns,
+                               kRoleLoader, stage)) {
+                    aborted = true;
+                    break;
+                }
+                if (lane == 0 && !(drop && issued == 0)) {
+                    uint8_t *sw = sm.stages + static_cast<size_t>(stage) * a.stage_bytes;
+                    const uint32_t fb = smem_addr(&ctl.full[stage]);
+                    mbar_arrive_expect_tx(fb, tx);
+                    tma_load_3d_hint(smem_addr(sw), &tm_w, fb, kb * kBlockK, x.w0, x.g, w_policy);
+                    for (int r = 0; r < x.n_mma; r += kTokBox)
+                        tma_load_3d(smem_addr(sw + w_bytes + (r / kTokBox) * kTokBoxBytes), &tm_t, fb,
+                                    kb * kBlockK, x.tok0 + r, x.g);
+                }
+                __syncwarp();
+                ++issued;
+                if (++stage == a.stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        loader_tail(ctl, a, stage, phase, issued, aborted, drop);
+    } else if (warp == 1) {
+        // ----------------------------- MMA issuer -----------------------------
+        // MMA operand A = weight tile (format of B), operand B = token tile
+        // (format of A).
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool issued_any = false;
+        for (int u = blockIdx.x; u < total; u += gridDim.x) {
+            const U x = decode(u);
+            const uint32_t idesc = make_idesc(a.b_fmt, a.a_fmt, kTileM, static_cast<uint32_t>(x.n_mma));
+            if (!warp_wait(smem_addr(&ctl.tempty[acc]), acc_phase ^ 1u, ctl, a.timeout_ns, kRoleMma,
+                           100 + acc))
+                break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccStride);
+            bool ok = true;
+            for (int kb = x.kb0; kb < x.kb1; ++kb) {
+                if (!warp_wait(smem_addr(&ctl.full[stage]), phase, ctl, a.timeout_ns, kRoleMma,
+                               stage)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t sw = smem_addr(sm.stages + static_cast<size_t>(stage) * a.stage_bytes);
+                    const uint64_t wdesc = smem_desc_k_sw128(sw);
+                    const uint64_t tdesc = smem_desc_k_sw128(sw + w_bytes);
+#pragma unroll
+                    for (int k = 0; k < kBlockK / 32; ++k)
+                        mma_f8f6f4(d_tmem, wdesc + 2u * k, tdesc + 2u * k, idesc,
+                                   (kb != x.kb0 || k != 0) ? 1u : 0u);
+                    mma_commit(smem_addr(&ctl.empty[stage]));
+                }
+                __syncwarp();
+                issued_any = true;
+                if (++stage == a.stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok)
+                break;
+            if (lane == 0)
+                mma_commit(smem_addr(&ctl.tfull[acc]));
+            __syncwarp();
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+        mma_drain(ctl, a, issued_any);
+    } else {
+        // ------------------------------ epilogue ------------------------------
+        // Thread = weight row n (TMEM lane), registers = tokens (TMEM columns).
+        // For a fixed token the 32 lanes of a warp write 32 consecutive n.
+        const int q = warp & 3;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        __nv_bfloat16 *dout = static_cast<__nv_bfloat16 *>(a.d);
+        for (int u = blockIdx.x; u < total; u += gridDim.x) {
+            const U x = decode(u);
+            if (!warp_wait(smem_addr(&ctl.tfull[acc]), acc_phase, ctl, a.timeout_ns, kRoleEpilogue,
+                           200 + acc))
+                break;
+            tc_fence_after();
+            const int nrow = x.w0 + q * 32 + lane;
+            const bool n_ok = nrow < a.n;
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(acc * kAccStride);
+            __nv_bfloat16 *dcol = dout + static_cast<int64_t>(x.g) * a.rows_a * static_cast<int64_t>(a.n) +
+                                  nrow;
+            bool last = true;
+            if (ks_n > 1) {
+                // Publish this split's partial tile, then count arrivals for
+                // this (tile, quadrant); the last of the ks_n arrivals reduces
+                // all partials in split order.
+                float *ws = a.workspace +
+                            (static_cast<int64_t>(x.tile) * ks_n + x.ks) * (kTileM * static_cast<int64_t>(cap));
+                for (int c = 0; c < x.n_mma; c += 16) {
+                    uint32_t r[16];
+                    tmem_ld_32x32b_x16(t_row + static_cast<uint32_t>(c), r);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (c + j < x.n_tok)
+                            ws[(c + j) * kTileM + q * 32 + lane] = __uint_as_float(r[j]);
+                }
+                __threadfence();
+                __syncwarp();
+                int prev = 0;
+                if (lane == 0)
+                    prev = atomicAdd(a.counters + static_cast<int64_t>(x.tile) * 4 + q, 1);
+                prev = __shfl_sync(0xffffffffu, prev, 0);
+                last = (prev == ks_n - 1);
+                if (last) {
+                    __threadfence();
+                    if (lane == 0)
+                        a.counters[static_cast<int64_t>(x.tile) * 4 + q] = 0;  // ready for the next launch
+                }
+            }
+            if (last) {
+                for (int c = 0; c < x.n_mma; c += 16) {
+                    uint32_t r[16];
+                    tmem_ld_32x32b_x16(t_row + static_cast<uint32_t>(c), r);
+                    float v[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        v[j] = __uint_as_float(r[j]);
+                    if (ks_n > 1) {
+                        const float *base = a.workspace +
+                                            static_cast<int64_t>(x.tile) * ks_n * (kTileM * static_cast<int64_t>(cap));
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            if (c + j >= x.n_tok)
+                                continue;
+                            float s = 0.0f;
+                            for (int p = 0; p < ks_n; ++p) {
+                                const float t = (p == x.ks)
+                                                    ? v[j]
+                                                    : __ldcg(base + static_cast<int64_t>(p) * kTileM * cap +
+                                                             (c + j) * kTileM + q * 32 + lane);
+                                s = (p == 0) ? t : s + t;
+                            }
+                            v[j] = s;
+                        }
+                    }
+                    if (n_ok) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            if (c + j < x.n_tok)
+                                dcol[static_cast<int64_t>(x.tok0 + c + j) * a.n] = __float2bfloat16_rn(v[j]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(smem_addr(&ctl.tempty[acc]));
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// =====================================================================================
+// Launchers
+// =====================================================================================
+cudaError_t launch_gemm_mn(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const GemmArgs &args,
+                           int grid, size_t smem, cudaStream_t stream)
+{
+    if (smem < smem_bytes_for(args.stages, args.stage_bytes))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_mn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess)
+        return e;
+    k_gemm_mn<<<grid, kThreads, smem, stream>>>(tm_a, tm_b, args);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_swap(const CUtensorMap &tm_w, const CUtensorMap &tm_t,
+                             const GemmArgs &args, int grid, size_t smem, cudaStream_t stream)
+{
+    if (smem < smem_bytes_for(args.stages, args.stage_bytes))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_swap, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess)
+        return e;
+    k_gemm_swap<<<grid, kThreads, smem, stream>>>(tm_w, tm_t, args);
+    return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_status(int32_t info[4])
+{
+    cudaError_t e = cudaMemcpyFromSymbol(info, g_status, 4 * sizeof(int32_t));
+    if (e != cudaSuccess)
+        return e;
+    const int32_t zero[4] = {0, 0, 0, 0};
+    return cudaMemcpyToSymbol(g_status, zero, 4 * sizeof(int32_t));
+}
+
+}  // namespace fp8g

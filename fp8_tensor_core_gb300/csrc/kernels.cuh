@@ -1,0 +1,65 @@
+// Launch interface between the host API (api.cu) and the sm_103a kernels
+// (kernels.cu).  Plain structs only; no torch types.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fp8g {
+
+constexpr int kBlockK = 128;         // K bytes per pipeline stage (one 128-byte swizzle row)
+constexpr int kTileM = 128;          // MMA M: rows of the operand on the M side
+constexpr int kMaxStages = 16;
+constexpr int kMaxGroups = 1024;
+constexpr int kThreads = 192;        // warp 0 loader, warp 1 MMA issuer, warps 2-5 epilogue
+constexpr int kTmemCols = 512;       // two accumulators of up to 256 columns
+constexpr int kAccStride = 256;
+constexpr int kCtlBytes = 10240;     // barriers, TMEM slot, per-group tables
+constexpr int kSmemAlignPad = 1024;  // dynamic smem base rounded up to 1024 B
+
+// Roles recorded in the device status word.
+enum Role : int { kRoleLoader = 0, kRoleMma = 1, kRoleEpilogue = 2, kRoleScheduler = 3 };
+
+struct GemmArgs {
+    // Problem.  Token operand A is [groups, rows_a, k]; weight operand B is
+    // [groups, n, k]; output D is [groups, rows_a, n] BF16.
+    int32_t rows_a;            // M (dense) or M_max (grouped)
+    int32_t n;
+    int32_t k;
+    int32_t groups;
+    int32_t num_kb;            // ceil(k / kBlockK)
+    const int32_t *masked_m;   // device [groups] or nullptr (all rows valid)
+    void *d;
+    // Tiling.
+    int32_t tile_n;            // mn kernel: N tile (32..256, multiple of 32)
+                               // swap kernel: token chunk (16..256, multiple of 16)
+    int32_t stages;            // pipeline depth (1..kMaxStages)
+    int32_t stage_bytes;       // bytes per stage (multiple of 1024)
+    int32_t k_splits;          // swap kernel: K partitions per output tile (1 = none)
+    int32_t raster_band;       // mn kernel: M tiles per rasterisation band
+    uint32_t a_fmt, b_fmt;     // 0 = E4M3, 1 = E5M2 (of A and B as passed by the caller)
+    uint32_t flags;            // FP8G_DEBUG_* bits
+    uint64_t timeout_ns;       // limit of every barrier wait
+    float *workspace;          // swap kernel, k_splits > 1: FP32 partial tiles
+    int32_t *counters;         // swap kernel, k_splits > 1: arrivals per (tile, warp)
+};
+
+// Shared-memory footprint of a launch (stages + control block + alignment).
+inline size_t smem_bytes_for(int stages, int stage_bytes)
+{
+    return static_cast<size_t>(stages) * stage_bytes + kCtlBytes + kSmemAlignPad;
+}
+
+// `smem` must be at least smem_bytes_for(args.stages, args.stage_bytes); the
+// host passes the whole per-block budget so that exactly one CTA (and one
+// 512-column TMEM allocation) is resident per SM.
+cudaError_t launch_gemm_mn(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const GemmArgs &args,
+                           int grid, size_t smem, cudaStream_t stream);
+cudaError_t launch_gemm_swap(const CUtensorMap &tm_w, const CUtensorMap &tm_t,
+                             const GemmArgs &args, int grid, size_t smem, cudaStream_t stream);
+
+// Status word of the current device: read it, then clear it.
+cudaError_t read_and_clear_status(int32_t info[4]);
+
+}  // namespace fp8g

@@ -1,0 +1,153 @@
+/*
+ * fp8g.h -- C ABI of the GB300 (sm_103a) FP8 GEMM library.
+ *
+ * Two compute entry points:
+ *
+ *   fp8_gemm_nt              D[M,N] = A[M,K] . B[N,K]^T
+ *   fp8_gemm_grouped_masked  D[g,m,n] = A[g,m,:] . B[g,n,:]  for m < masked_m[g]
+ *
+ * A and B hold FP8 codes (E4M3 or E5M2, chosen per operand), products are
+ * accumulated in FP32 by the tensor cores, and D is BF16 (round to nearest
+ * even).  Sources:
+ *   "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践"
+ *     (sheratonhq.com/news/187119) -- §1.3 (FP8 inputs, E4M3/E5M2
+ *     selectable, FP32 accumulator), §3.1 (the two formats), §6.2-6.4
+ *     (K tails and edge shapes must be handled exactly).
+ *   "一次“转置”，半张算力：DeepSeek SwapAB 漂流史" (hwcomputing.csdn.net)
+ *     -- §3.1 (m_grouped_fp8_gemm_nt_masked: masked grouped FP8 GEMM for
+ *     MoE decode, ENABLE_SWAPAB switch), §3.2 (SwapAB: weights on the
+ *     instruction's M side, tokens on N), §3.3 (runtime N in the
+ *     instruction descriptor shrinks the tail to the valid tokens), §3.5
+ *     (swap pays for small token counts only; selection is per shape).
+ *   "MLS 三个访存 Bug 深度剖析" (chatdocs.ruinique.com) -- Bug 1 (64-bit
+ *     address arithmetic), Bug 2 (a fully masked tail issues no load),
+ *     Bug 3 (invalid padding must not reach valid outputs).
+ *
+ * Conventions for every call:
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *    library keeps no reference once the enqueued work has completed.
+ *  - Calls enqueue work on `stream` and return without synchronising.
+ *  - The return value is an fp8g_status code.  Invalid arguments are
+ *    rejected before anything is enqueued.  Errors found on the device
+ *    (a bounded wait that ran out, masked_m out of range) are recorded in a
+ *    per-device status word read by fp8g_get_device_status().
+ *  - Offsets are computed in 64 bits throughout.
+ *  - Not thread-safe for concurrent calls from several host threads on the
+ *    same device while fp8g_set_wait_timeout_ns() is being changed.
+ */
+#ifndef FP8G_H
+#define FP8G_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA runtime's stream handle (same declaration as driver_types.h). */
+struct CUstream_st;
+typedef struct CUstream_st *cudaStream_t;
+
+/* FP8 element formats of A and B. */
+typedef enum {
+    FP8G_E4M3 = 0, /* 1 sign, 4 exponent (bias 7), 3 mantissa; max 448     */
+    FP8G_E5M2 = 1  /* 1 sign, 5 exponent (bias 15), 2 mantissa; max 57344  */
+} fp8g_dtype;
+
+/* Status codes. */
+typedef enum {
+    FP8G_OK = 0,
+    FP8G_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, bad dtype, ...  */
+    FP8G_ERR_MISALIGNED = 2,    /* a pointer is not 16-byte aligned                  */
+    FP8G_ERR_UNSUPPORTED = 3,   /* shape outside the supported range, not sm_103     */
+    FP8G_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed              */
+    FP8G_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out; kernel returned   */
+    FP8G_ERR_NO_DEVICE = 6,     /* no CUDA device is visible                         */
+    FP8G_ERR_MASKED_M_RANGE = 7 /* device: a masked_m entry was outside [0, M_max]
+                                   and was clamped                                   */
+} fp8g_status;
+
+/* `flags` bits 0-1: operand placement (the pages' ENABLE_SWAPAB switch). */
+#define FP8G_SWAP_AUTO 0u  /* library picks by token count (the default)          */
+#define FP8G_SWAP_ON 1u    /* weights (B) on the MMA M side, tokens (A) on N       */
+#define FP8G_SWAP_OFF 2u   /* tokens (A) on the MMA M side, weights (B) on N       */
+#define FP8G_SWAP_MASK 3u
+/* Debug bits (bench and tests only; never needed for correct results). */
+#define FP8G_DEBUG_ONE_STAGE 0x10u       /* one shared-memory stage: load,
+                                            compute, load ... (isolates races
+                                            from address bugs)                  */
+#define FP8G_DEBUG_DROP_FIRST_LOAD 0x20u /* block 0's producer skips its first
+                                            load, so its consumer's bounded wait
+                                            runs out: exercises the timeout
+                                            path; the call's output is invalid  */
+
+/*
+ * fp8_gemm_nt -- dense D = A . B^T.
+ *   A  [M, K] FP8 codes, row-major, K contiguous (row stride K bytes).
+ *   B  [N, K] FP8 codes, row-major, K contiguous (row stride K bytes).
+ *   D  [M, N] BF16, row-major (row stride 2N bytes); every element written.
+ *   M, N, K  >= 1;  K % 16 == 0 (16-byte row stride for the tensor copy
+ *            engine);  N % 8 == 0 (16-byte rows of D);  each < 2^31.
+ *   a_dtype, b_dtype  fp8g_dtype of A and B (mixed pairs allowed).
+ *   flags  FP8G_SWAP_* (plus debug bits).
+ *   stream  CUDA stream to enqueue on (0 = legacy default stream).
+ * Returns FP8G_OK or an error code; on error nothing is enqueued.
+ */
+int fp8_gemm_nt(const void *A, const void *B, void *D, int64_t M, int64_t N,
+                int64_t K, int a_dtype, int b_dtype, uint32_t flags,
+                cudaStream_t stream);
+
+/*
+ * fp8_gemm_grouped_masked -- MoE-decode masked grouped GEMM.
+ *   A         [G, M_max, K] FP8 token rows; only rows m < masked_m[g] of
+ *             group g are valid (padding rows may hold any bytes, NaN codes
+ *             included, and never affect valid outputs).
+ *   B         [G, N, K] FP8 expert weights, K contiguous.
+ *   D         [G, M_max, N] BF16.  Rows m < masked_m[g] are written; rows
+ *             m >= masked_m[g] are NOT touched.
+ *   masked_m  DEVICE pointer to G int32 valid-row counts, read on the device
+ *             (no host synchronisation).  Entries outside [0, M_max] are
+ *             clamped and flagged FP8G_ERR_MASKED_M_RANGE in the device status.
+ *   G         1 .. 1024 groups.  M_max >= 1.
+ *   max_m_hint  host-side upper bound the caller expects for masked_m (0 =
+ *             unknown, taken as M_max).  It only sizes the token tile; groups
+ *             above it are still computed correctly.
+ *   N % 8 == 0, K % 16 == 0, sizes < 2^31, dtypes and flags as above.
+ * Returns FP8G_OK or an error code; on error nothing is enqueued.
+ */
+int fp8_gemm_grouped_masked(const void *A, const void *B, void *D,
+                            const int32_t *masked_m, int64_t G, int64_t M_max,
+                            int64_t N, int64_t K, int64_t max_m_hint,
+                            int a_dtype, int b_dtype, uint32_t flags,
+                            cudaStream_t stream);
+
+/*
+ * fp8g_get_device_status -- synchronise `stream`, then read and clear the
+ * status word of the current device.  info[0] = first fp8g_status recorded
+ * on the device since the last read (FP8G_OK if none), info[1] = block
+ * index, info[2] = role (0 loader, 1 MMA issuer, 2 epilogue, 3 scheduler),
+ * info[3] = detail (pipeline stage or group).  `info` is host memory of 4
+ * int32.  Returns FP8G_OK or FP8G_ERR_CUDA / FP8G_ERR_INVALID_ARG.
+ */
+int fp8g_get_device_status(int32_t *info, cudaStream_t stream);
+
+/*
+ * fp8g_set_wait_timeout_ns -- limit, in nanoseconds of device time, of every
+ * barrier wait inside the kernels launched after this call (default 2e9).
+ * A wait that runs out records FP8G_ERR_TIMEOUT, stops the block's pipeline,
+ * drains its in-flight copies and tensor-core work, frees its tensor memory
+ * and returns.  0 restores the default.  Returns the previous value.
+ */
+uint64_t fp8g_set_wait_timeout_ns(uint64_t ns);
+
+/* Human-readable name of a status code (static string). */
+const char *fp8g_status_string(int code);
+
+/* Library ABI version: major*10000 + minor*100 + patch. */
+int fp8g_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8G_H */

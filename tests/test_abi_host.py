@@ -1,0 +1,109 @@
+"""The C-ABI library loads and exports every symbol include/fp8g.h declares,
+and rejects invalid arguments on the host before touching the GPU.  No
+compute call is made (these tests also run where no GPU exists)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__  # noqa: F401  (puts the repo root on sys.path)
+from fp8_tensor_core_gb300 import _lib
+from fp8_tensor_core_gb300 import build as cuda_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8g.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z0-9_]+)\s*\(",
+                       src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_expected_entry_points():
+    names = declared_functions()
+    for n in ("fp8_gemm_nt", "fp8_gemm_grouped_masked", "fp8g_get_device_status",
+              "fp8g_status_string", "fp8g_version", "fp8g_set_wait_timeout_ns"):
+        assert n in names
+    assert set(names) == set(_lib.SIGNATURES), "binding and header disagree"
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+        assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
+
+
+def test_status_strings_and_version(lib):
+    names = [lib.fp8g_status_string(i).decode() for i in range(8)]
+    assert names[0] == "FP8G_OK" and names[5] == "FP8G_ERR_TIMEOUT"
+    assert len(set(names)) == 8
+    assert lib.fp8g_status_string(99).decode() == "FP8G_UNKNOWN_STATUS"
+    assert lib.fp8g_version() >= 100
+
+
+def test_timeout_setting_roundtrip(lib):
+    prev = lib.fp8g_set_wait_timeout_ns(12345)
+    assert lib.fp8g_set_wait_timeout_ns(0) == 12345
+    assert lib.fp8g_set_wait_timeout_ns(prev) == 2_000_000_000
+
+
+ALIGNED = 0x10000   # never dereferenced: every case below fails validation first
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, ALIGNED, ALIGNED, 16, 16, 16, 0, 0, 0), 1),        # null A
+    ((ALIGNED, ALIGNED, 0, 16, 16, 16, 0, 0, 0), 1),        # null D
+    ((ALIGNED, ALIGNED, ALIGNED, 0, 16, 16, 0, 0, 0), 1),   # M = 0
+    ((ALIGNED, ALIGNED, ALIGNED, 16, 16, 24, 0, 0, 0), 1),  # K % 16
+    ((ALIGNED, ALIGNED, ALIGNED, 16, 12, 16, 0, 0, 0), 1),  # N % 8
+    ((ALIGNED, ALIGNED, ALIGNED, 16, 16, 16, 2, 0, 0), 1),  # bad dtype
+    ((ALIGNED, ALIGNED, ALIGNED, 16, 16, -16, 0, 0, 0), 1), # negative K
+    ((ALIGNED, ALIGNED, ALIGNED, 1 << 31, 16, 16, 0, 0, 0), 1),  # M too large
+    ((ALIGNED + 8, ALIGNED, ALIGNED, 16, 16, 16, 0, 0, 0), 2),  # misaligned A
+    ((ALIGNED, ALIGNED, ALIGNED + 2, 16, 16, 16, 0, 0, 0), 2),  # misaligned D
+])
+def test_dense_validation(lib, args, code):
+    assert lib.fp8_gemm_nt(*args, None) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    ((ALIGNED, ALIGNED, ALIGNED, 0, 4, 64, 64, 64, 0, 0, 0, 0), 1),        # null masked_m
+    ((ALIGNED, ALIGNED, ALIGNED, ALIGNED, 0, 64, 64, 64, 0, 0, 0, 0), 1),  # G = 0
+    ((ALIGNED, ALIGNED, ALIGNED, ALIGNED, 4, 64, 64, 64, 65, 0, 0, 0), 1), # hint > M_max
+    ((ALIGNED, ALIGNED, ALIGNED, ALIGNED, 4, 64, 64, 64, -1, 0, 0, 0), 1), # hint < 0
+    ((ALIGNED, ALIGNED, ALIGNED, ALIGNED, 2048, 64, 64, 64, 0, 0, 0, 0), 3),  # too many groups
+    ((ALIGNED, ALIGNED, ALIGNED, ALIGNED + 4, 4, 64, 64, 64, 0, 0, 0, 0), 2), # masked_m misaligned
+    ((ALIGNED, ALIGNED, ALIGNED, ALIGNED, 4, 64, 60, 64, 0, 0, 0, 0), 1),  # N % 8
+])
+def test_grouped_validation(lib, args, code):
+    assert lib.fp8_gemm_grouped_masked(*args, None) == code
+
+
+def test_invalid_swap_mode(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("would reach the device with fake pointers")
+    # without a device the call stops at device discovery
+    assert lib.fp8_gemm_nt(ALIGNED, ALIGNED, ALIGNED, 16, 16, 16, 0, 0, 0, None) == 6
+
+
+def test_get_device_status_rejects_null(lib):
+    assert lib.fp8g_get_device_status(None, None) == 1
+
+
+def test_binding_refuses_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    import fp8_tensor_core_gb300 as fp8g
+    a = torch.zeros((16, 16), dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        fp8g.fp8_gemm_nt(a, a, a_dtype=0, b_dtype=0)

@@ -1,0 +1,265 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle,
+element by element, on seeded inputs (small shapes spanning several tiles
+and ragged tails, edge cases, then the workload sizes).
+
+Acceptance per element: |gpu - oracle| <= ulp_bf16(oracle) + 1e-6 * sum|a b|
+(exactly representable cases must match bit for bit)."""
+import numpy as np
+import pytest
+import torch
+
+import __graft_entry__  # noqa: F401
+import fp8_tensor_core_gb300 as fp8g
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+E4, E5 = synth.E4M3, synth.E5M2
+OFF, ON, AUTO = fp8g.SWAP_OFF, fp8g.SWAP_ON, fp8g.SWAP_AUTO
+
+
+@pytest.fixture(scope="module", autouse=True)
+def device():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from fp8_tensor_core_gb300 import build as cuda_build
+    cuda_build.build()
+    torch.cuda.set_device(0)
+    fp8g.fp8g_get_device_status()      # clear anything left from before
+    yield torch.device("cuda:0")
+
+
+def dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).to("cuda:0")
+
+
+def bits(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def assert_status_ok():
+    st = fp8g.fp8g_get_device_status()
+    assert st[0] == fp8g.OK, "device status %s" % (st,)
+
+
+def dense_inputs(M, N, K, fa, fb, seed, dist="normal", std=1.0):
+    if dist == "uniform":
+        A = synth.uniform_fp8((M, K), seed, -2.0, 2.0, fa)
+        B = synth.uniform_fp8((N, K), seed + 1, -2.0, 2.0, fb)
+    else:
+        A = synth.normal_fp8((M, K), seed, 0.0, std, fa)
+        B = synth.normal_fp8((N, K), seed + 1, 0.0, std, fb)
+    return A, B
+
+
+def run_dense(A, B, fa, fb, flags):
+    D = fp8g.fp8_gemm_nt(dev(A), dev(B), a_dtype=fa, b_dtype=fb, flags=flags)
+    torch.cuda.synchronize()
+    assert_status_ok()
+    return bits(D)
+
+
+def check_dense(M, N, K, fa=E4, fb=E4, flags=AUTO, seed=1, dist="normal", std=1.0):
+    A, B = dense_inputs(M, N, K, fa, fb, seed, dist, std)
+    got = run_dense(A, B, fa, fb, flags)
+    ref, absdot = oracle.gemm_nt(A, B, fa, fb)
+    ok, rep = oracle.check_bf16(got, ref, absdot)
+    assert ok, rep
+    return rep
+
+
+# ---- first: one tile, then a few -------------------------------------------
+
+@pytest.mark.parametrize("flags", [OFF, ON])
+def test_single_tile(flags):
+    check_dense(128, 128, 128, flags=flags, seed=11)
+
+
+@pytest.mark.parametrize("flags", [OFF, ON])
+def test_exact_integer_products_bit_exact(flags):
+    """Entries in {-2..2}: every partial sum is an integer of magnitude
+    <= 256, exact in FP32 and BF16, so the GPU must match bit for bit."""
+    rng = np.random.default_rng(5)
+    enc = {-2: 0xC0, -1: 0xB8, 0: 0x00, 1: 0x38, 2: 0x40}
+    M, N, K = 160, 192, 64
+    ia = rng.choice([-2, -1, 0, 1, 2], (M, K))
+    ib = rng.choice([-2, -1, 0, 1, 2], (N, K))
+    A = np.vectorize(enc.get)(ia).astype(np.uint8)
+    B = np.vectorize(enc.get)(ib).astype(np.uint8)
+    got = run_dense(A, B, E4, E4, flags)
+    ref, _ = oracle.gemm_nt(A, B)
+    assert np.array_equal(got, ref)
+
+
+def test_all_ones_K_up_to_256():
+    for K in (16, 48, 128, 144, 256):
+        A = np.full((130, K), 0x38, np.uint8)
+        B = np.full((136, K), 0x38, np.uint8)
+        for flags in (OFF, ON):
+            got = run_dense(A, B, E4, E4, flags)
+            assert np.all(oracle.bf16_bits_to_f64(got) == K), (K, flags)
+
+
+def test_identity_gives_transpose():
+    K, N = 256, 320
+    A = np.zeros((K, K), np.uint8)
+    A[np.arange(K), np.arange(K)] = 0x38
+    B = synth.normal_fp8((N, K), 91, 0.0, 1.0, E4)
+    for flags in (OFF, ON):
+        got = run_dense(A, B, E4, E4, flags)
+        ref, _ = oracle.gemm_nt(A, B)
+        assert np.array_equal(got, ref)
+
+
+# ---- shapes: several tiles, ragged tails, K tails -------------------------------
+
+SHAPES = [
+    (256, 256, 256),
+    (1, 8, 16),
+    (7, 24, 48),
+    (64, 1024, 384),
+    (129, 136, 144),
+    (200, 520, 1280),
+    (300, 264, 400),
+    (513, 776, 272),
+]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("flags", [OFF, ON, AUTO])
+def test_dense_shapes(M, N, K, flags):
+    check_dense(M, N, K, flags=flags, seed=M * 31 + N * 7 + K)
+
+
+def test_dense_uniform_256_cube():
+    """The 256^3 U[-2,2] E4M3 workload, every element."""
+    rep = check_dense(256, 256, 256, dist="uniform", seed=synth.seed_for(0))
+    assert rep["bad"] == 0
+
+
+@pytest.mark.parametrize("fa,fb", [(E4, E5), (E5, E4), (E5, E5)])
+@pytest.mark.parametrize("flags", [OFF, ON])
+def test_mixed_formats(fa, fb, flags):
+    check_dense(192, 384, 512, fa=fa, fb=fb, flags=flags, seed=17 + fa * 2 + fb, std=0.5)
+
+
+@pytest.mark.parametrize("flags", [OFF, ON])
+def test_one_stage_pipeline_matches(flags):
+    """The one-stage debug pipeline (load, compute, load ...) computes the
+    same result as the deep ring."""
+    A, B = dense_inputs(150, 264, 640, E4, E4, 23)
+    deep = run_dense(A, B, E4, E4, flags)
+    one = run_dense(A, B, E4, E4, flags | fp8g.DEBUG_ONE_STAGE)
+    assert np.array_equal(deep, one)
+
+
+def test_accumulator_keeps_small_terms():
+    """One product of 256 and 16383 products of 2^-10: the exact sum
+    256 + 16383/1024 needs FP32 accumulation; an accumulator that drops the
+    small terms returns 256, outside the tolerance."""
+    K = 16384
+    A = np.full((128, K), 0x10, np.uint8)       # 2^-5
+    B = np.full((128, K), 0x10, np.uint8)
+    A[:, 0] = 0x58                               # 16
+    B[:, 0] = 0x58
+    for flags in (OFF, ON):
+        got = run_dense(A, B, E4, E4, flags)
+        ref, absdot = oracle.gemm_nt(A, B)
+        ok, rep = oracle.check_bf16(got, ref, absdot)
+        assert ok, rep
+        assert np.all(oracle.bf16_bits_to_f64(got) == 272.0)
+
+
+def test_deterministic_repeat():
+    A, B = dense_inputs(64, 7168, 4096, E4, E4, 29)      # small M: split-K path
+    Ad, Bd = dev(A), dev(B)
+    D1 = fp8g.fp8_gemm_nt(Ad, Bd, a_dtype=E4, b_dtype=E4, flags=ON)
+    D2 = fp8g.fp8_gemm_nt(Ad, Bd, a_dtype=E4, b_dtype=E4, flags=ON)
+    torch.cuda.synchronize()
+    assert_status_ok()
+    assert torch.equal(D1.view(torch.int16), D2.view(torch.int16))
+    ref, absdot = oracle.gemm_nt(A, B)
+    ok, rep = oracle.check_bf16(bits(D1), ref, absdot)
+    assert ok, rep
+
+
+def test_side_stream():
+    A, B = dense_inputs(256, 512, 512, E4, E4, 37)
+    s = torch.cuda.Stream()
+    Ad, Bd = dev(A), dev(B)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        D = fp8g.fp8_gemm_nt(Ad, Bd, a_dtype=E4, b_dtype=E4)
+    s.synchronize()
+    assert_status_ok()
+    ref, absdot = oracle.gemm_nt(A, B)
+    ok, rep = oracle.check_bf16(bits(D), ref, absdot)
+    assert ok, rep
+
+
+# ---- masked grouped --------------------------------------------------------------
+
+def grouped_case(G, M_max, N, K, mm, flags, hint, seed, nan_padding=False, fa=E4, fb=E4):
+    A = synth.normal_fp8((G, M_max, K), seed, 0.0, 0.5, fa)
+    B = synth.normal_fp8((G, N, K), seed + 1, 0.0, 0.5, fb)
+    mm = np.asarray(mm, np.int32)
+    if nan_padding:
+        for g in range(G):
+            A[g, mm[g]:] = 0x7F
+    D0 = synth.u16_pattern((G, M_max, N), seed + 2)
+    D0[..., ::97] = 0x7FC1                      # NaN codes among the canaries
+    Dt = dev(D0.view(np.int16)).view(torch.bfloat16)
+    fp8g.fp8_gemm_grouped_masked(dev(A), dev(B), dev(mm), D=Dt, max_m_hint=hint,
+                                 a_dtype=fa, b_dtype=fb, flags=flags)
+    torch.cuda.synchronize()
+    assert_status_ok()
+    got = bits(Dt)
+    ref, absdot = oracle.gemm_grouped_masked(A, B, mm, D0, fa, fb)
+    for g in range(G):
+        m = mm[g]
+        ok, rep = oracle.check_bf16(got[g, :m], ref[g, :m], absdot[g, :m])
+        assert ok, (g, rep)
+        assert np.array_equal(got[g, m:], D0[g, m:]), "padding rows of group %d written" % g
+
+
+@pytest.mark.parametrize("flags,hint", [(ON, 32), (ON, 0), (OFF, 0), (AUTO, 32), (AUTO, 0)])
+def test_grouped_edge_counts(flags, hint):
+    mm = [0, 1, 7, 8, 15, 16, 17, 31, 32, 64]
+    grouped_case(len(mm), 64, 256, 512, mm, flags, hint, seed=101)
+
+
+@pytest.mark.parametrize("flags", [ON, OFF])
+def test_grouped_nan_padding_never_reaches_valid_rows(flags):
+    grouped_case(4, 48, 384, 640, [3, 0, 48, 20], flags, 0, seed=111, nan_padding=True)
+
+
+def test_grouped_all_empty_writes_nothing():
+    grouped_case(3, 32, 128, 256, [0, 0, 0], ON, 16, seed=121)
+    grouped_case(3, 32, 128, 256, [0, 0, 0], OFF, 0, seed=122)
+
+
+def test_grouped_hint_below_actual_counts_is_still_correct():
+    grouped_case(5, 96, 256, 384, [90, 3, 40, 96, 17], ON, 16, seed=131)
+
+
+def test_grouped_masked_m_out_of_range_is_clamped_and_flagged():
+    G, M_max, N, K = 3, 32, 128, 256
+    A = synth.normal_fp8((G, M_max, K), 141, 0.0, 0.5, E4)
+    B = synth.normal_fp8((G, N, K), 142, 0.0, 0.5, E4)
+    mm = np.array([-5, 40, 7], np.int32)
+    D0 = synth.u16_pattern((G, M_max, N), 143)
+    Dt = dev(D0.view(np.int16)).view(torch.bfloat16)
+    fp8g.fp8_gemm_grouped_masked(dev(A), dev(B), dev(mm), D=Dt, a_dtype=E4, b_dtype=E4, flags=ON)
+    st = fp8g.fp8g_get_device_status()
+    assert st[0] == fp8g.ERR_MASKED_M_RANGE
+    clamped = np.array([0, 32, 7], np.int32)
+    ref, absdot = oracle.gemm_grouped_masked(A, B, clamped, D0)
+    got = bits(Dt)
+    ok, rep = oracle.check_bf16(got[1], ref[1], absdot[1])
+    assert ok, rep
+    assert np.array_equal(got[0], D0[0])
+    assert_status_ok()
+
+
+def test_grouped_mixed_formats():
+    grouped_case(3, 40, 256, 384, [40, 9, 25], ON, 40, seed=151, fb=E5)
