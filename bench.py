@@ -1,0 +1,528 @@
+"""FP8 GEMM benchmark on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload dense4096|cube256|proj|masked|smallm] [...]
+
+One step = one pass of the hot path over one batch of synthetic input: one
+FP8 GEMM (dense D = A.B^T, or the masked grouped MoE-decode GEMM) through
+the C ABI.  Prints ONE JSON line (rank 0).  The default workload is the
+dense 4096^3 E4M3 GEMM (FP32 accumulate, BF16 out) reported in TFLOP/s.
+
+Multi-GPU: one process per GPU (torchrun); every rank runs its own shard of
+the same shape (independent output slices, no data-path collective), so
+scaling is weak; the timed region is bracketed by a barrier and a device
+synchronise and the maximum time over ranks is reported.
+
+--impl reference times the CPU oracle (the plain fp64 implementation the
+tests compare against) on the host cores, on a bounded sample of the same
+workload, and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "FP8 GEMM TFLOPS and % of roofline (tensor peak or HBM) on 1 GB300 vs CPU oracle"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_PER_BF16 = 2.0      # nominal dense FP8 : BF16 tensor-core rate on this part (4.5 : 2.25 PF)
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+
+class Workload:
+    """A named problem: shapes, input recipe, algorithmic FLOPs and bytes."""
+
+    def __init__(self, name, kind, desc, **kw):
+        self.name, self.kind, self.desc = name, kind, desc
+        self.__dict__.update(kw)
+
+    # algorithmic work of one step (padded MMA rows/columns are not counted)
+    def flops(self, masked_m=None):
+        if self.kind == "dense":
+            return 2.0 * self.M * self.N * self.K
+        return 2.0 * float(sum(masked_m)) * self.N * self.K
+
+    def bytes(self, masked_m=None):
+        if self.kind == "dense":
+            return float(self.M * self.K + self.N * self.K + 2 * self.M * self.N)
+        live = [m for m in masked_m if m > 0]
+        return float(len(live) * self.N * self.K + sum(live) * self.K + 2 * sum(live) * self.N)
+
+
+def make_workload(name: str, rank: int = 0) -> Workload:
+    import synth
+    if name == "dense4096":
+        return Workload(name, "dense", "dense GEMM M=N=K=4096, A,B E4M3 from N(0,1), FP32 accumulate, BF16 out",
+                        M=4096, N=4096, K=4096, fa=synth.E4M3, fb=synth.E4M3, dist="normal", std=1.0,
+                        seed=synth.seed_for(1, rank), bound="tensor", flags=0)
+    if name == "cube256":
+        return Workload(name, "dense", "dense GEMM M=N=K=256, A,B E4M3 from U[-2,2]",
+                        M=256, N=256, K=256, fa=synth.E4M3, fb=synth.E4M3, dist="uniform", std=None,
+                        seed=synth.seed_for(0, rank), bound="tensor", flags=0)
+    if name.startswith("proj"):
+        # proj:N:K[:e5m2]  -- M=8192 token projection shapes
+        parts = name.split(":")
+        N, K = int(parts[1]), int(parts[2])
+        fb = synth.E5M2 if len(parts) > 3 and parts[3] == "e5m2" else synth.E4M3
+        return Workload(name, "dense", "projection GEMM M=8192 N=%d K=%d, A E4M3, B %s, N(0,0.5)"
+                        % (N, K, "E5M2" if fb else "E4M3"),
+                        M=8192, N=N, K=K, fa=synth.E4M3, fb=fb, dist="normal", std=0.5,
+                        seed=synth.seed_for(2, rank), bound="tensor", flags=0)
+    if name == "masked":
+        return Workload(name, "masked", "masked grouped GEMM G=32 M_max=128 N=4096 K=7168, m_g~U{0..32}, "
+                        "E4M3 N(0,0.5), SwapAB", G=32, M_max=128, N=4096, K=7168, fa=synth.E4M3,
+                        fb=synth.E4M3, dist="normal", std=0.5, seed=synth.seed_for(3, rank), bound="hbm",
+                        hint=32, flags=1)
+    if name.startswith("smallm"):
+        # smallm:M:N:K[:swap|noswap]
+        parts = name.split(":")
+        M, N, K = int(parts[1]), int(parts[2]), int(parts[3])
+        mode = parts[4] if len(parts) > 4 else "swap"
+        return Workload(name, "dense", "small-M weight-streaming GEMM M=%d N=%d K=%d, E4M3 N(0,1), %s"
+                        % (M, N, K, "SwapAB" if mode == "swap" else "non-swapped"),
+                        M=M, N=N, K=K, fa=synth.E4M3, fb=synth.E4M3, dist="normal", std=1.0,
+                        seed=synth.seed_for(4, rank), bound="hbm", flags=1 if mode == "swap" else 2)
+    raise SystemExit("unknown workload %r" % name)
+
+
+def host_inputs(w: Workload):
+    """Seeded FP8 codes (numpy) for one instance of the workload."""
+    import numpy as np
+    import synth
+    if w.kind == "dense":
+        if w.dist == "uniform":
+            A = synth.uniform_fp8((w.M, w.K), w.seed, -2.0, 2.0, w.fa)
+            B = synth.uniform_fp8((w.N, w.K), w.seed + 100, -2.0, 2.0, w.fb)
+        else:
+            A = synth.normal_fp8((w.M, w.K), w.seed, 0.0, w.std, w.fa)
+            B = synth.normal_fp8((w.N, w.K), w.seed + 100, 0.0, w.std, w.fb)
+        return {"A": A, "B": B}
+    A = synth.normal_fp8((w.G, w.M_max, w.K), w.seed, 0.0, w.std, w.fa)
+    B = synth.normal_fp8((w.G, w.N, w.K), w.seed + 100, 0.0, w.std, w.fb)
+    mm = synth.uniform_int(w.G, w.seed + 200, 0, 32).astype(np.int32)
+    return {"A": A, "B": B, "masked_m": mm}
+
+
+# ---------------------------------------------------------------------------
+# measurement helpers
+# ---------------------------------------------------------------------------
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("kernels.cu", "ptx.cuh", "kernels.cuh", "api.cu"):
+        with open(os.path.join(ROOT, "fp8_tensor_core_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """Per-launch DRAM bytes (read + write) of the dominant kernel from the
+    committed ncu summary, valid only while the kernel sources are unchanged
+    since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    cur = kernel_source_hash()
+    with open(path) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            parts = line.split()
+            if len(parts) >= 3 and parts[0] == workload and parts[1] == cur:
+                return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples, timestamped on arrival."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [s.strip() for s in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        def parse(rows):
+            sm = [float(r[0]) for _, r in rows if r and r[0].replace(".", "", 1).isdigit()]
+            mx = [float(r[1]) for _, r in rows if len(r) > 1 and r[1].replace(".", "", 1).isdigit()]
+            reasons = set()
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for _, r in rows:
+                for i, n in enumerate(names):
+                    if len(r) > 4 + i and r[4 + i].lower().startswith("active"):
+                        reasons.add(n)
+            return sm, mx, sorted(reasons)
+        inside = [s for s in self.samples if t0 <= s[0] <= t1 + 0.15]
+        window = "timed"
+        if len(inside) < 2:
+            inside = [s for s in self.samples if s[0] <= t1 + 0.15]
+            window = "warmup+timed"
+        sm, mx, reasons = parse(inside)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(sm), "window": window}
+
+
+def dist_setup():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle, as it stands, on a bounded sample
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w: Workload, inp, budget_s: float, min_rows: int = 1):
+    """Time the oracle on whole output rows of the workload until about
+    `budget_s` seconds have been spent.  Returns (flops, seconds, cores,
+    description)."""
+    import numpy as np
+    import oracle
+    cores = oracle.default_threads()
+    flops = 0.0
+    t_start = time.perf_counter()
+    if w.kind == "dense":
+        A, B = inp["A"], inp["B"]
+        rows, r0 = max(min_rows, 8), 0
+        while r0 < w.M:
+            r1 = min(w.M, r0 + rows)
+            t = time.perf_counter()
+            oracle.gemm_nt(A[r0:r1], B, w.fa, w.fb)
+            dt = time.perf_counter() - t
+            flops += 2.0 * (r1 - r0) * w.N * w.K
+            r0 = r1
+            if time.perf_counter() - t_start >= budget_s:
+                break
+            rows = max(rows, int(rows * min(4.0, 0.5 * budget_s / max(dt, 1e-3))))
+        secs = time.perf_counter() - t_start
+        desc = "rows 0..%d of D (%d of %d rows, all N=%d columns, K=%d)" % (r0 - 1, r0, w.M, w.N, w.K)
+        return flops, secs, cores, desc
+    A, B, mm = inp["A"], inp["B"], inp["masked_m"]
+    D0 = np.zeros((1, w.M_max, w.N), np.uint16)
+    g_done = 0
+    for g in range(w.G):
+        if mm[g] == 0:
+            g_done += 1
+            continue
+        oracle.gemm_grouped_masked(A[g:g + 1], B[g:g + 1], mm[g:g + 1], D0, w.fa, w.fb)
+        flops += 2.0 * int(mm[g]) * w.N * w.K
+        g_done += 1
+        if time.perf_counter() - t_start >= budget_s:
+            break
+    secs = time.perf_counter() - t_start
+    return flops, secs, cores, "groups 0..%d of %d (all their valid rows)" % (g_done - 1, w.G)
+
+
+def run_reference(args, w: Workload):
+    """--impl reference: the CPU oracle timed on the host cores, each step a
+    bounded sample (a block of output rows) of the workload."""
+    rank, world, _ = dist_setup()
+    if rank != 0:
+        return 0
+    import oracle
+    inp = host_inputs(w)
+    oracle.build()
+    per_step_budget = max(0.05, min(2.0, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, inp, per_step_budget * 0.25)
+    flops = secs = 0.0
+    desc = ""
+    cores = oracle.default_threads()
+    for _ in range(args.steps):
+        f, s, cores, desc = oracle_sample(w, inp, per_step_budget)
+        flops += f
+        secs += s
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.desc, "name": w.name},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "per step: " + desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, w: Workload):
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_setup()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", rank=rank, world_size=world, device_id=device)
+
+    import fp8_tensor_core_gb300 as fp8g
+    fp8g._lib.load()          # fails loudly if the CUDA library is not built
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 129 * 2**20)
+
+    inp = host_inputs(w)
+    stream = torch.cuda.current_stream(device)
+
+    # Rotating device copies so that consecutive steps do not find their
+    # operands in L2: sets x (inputs + output) >= 3 x L2.
+    if w.kind == "dense":
+        set_bytes = w.M * w.K + w.N * w.K + 2 * w.M * w.N
+    else:
+        set_bytes = w.G * w.M_max * w.K + w.G * w.N * w.K + 2 * w.G * w.M_max * w.N
+    n_sets = max(1, math.ceil(3 * l2 / set_bytes))
+    n_sets = min(n_sets, 64)
+    sets = []
+    A_h = torch.from_numpy(inp["A"]).pin_memory()
+    B_h = torch.from_numpy(inp["B"]).pin_memory()
+    for _ in range(n_sets):
+        s = {"A": A_h.to(device), "B": B_h.to(device)}
+        if w.kind == "dense":
+            s["D"] = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device)
+        else:
+            s["mm"] = torch.from_numpy(inp["masked_m"]).to(device)
+            s["D"] = torch.zeros((w.G, w.M_max, w.N), dtype=torch.bfloat16, device=device)
+        sets.append(s)
+    torch.cuda.synchronize(device)
+
+    def step(i):
+        s = sets[i % n_sets]
+        if w.kind == "dense":
+            fp8g.fp8_gemm_nt(s["A"], s["B"], s["D"], a_dtype=w.fa, b_dtype=w.fb, flags=w.flags,
+                             stream=stream)
+        else:
+            fp8g.fp8_gemm_grouped_masked(s["A"], s["B"], s["mm"], s["D"], max_m_hint=w.hint,
+                                         a_dtype=w.fa, b_dtype=w.fb, flags=w.flags, stream=stream)
+
+    sampler = ClockSampler("GPU-" + str(props.uuid)) if rank == 0 else None
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(device)
+    st = fp8g.fp8g_get_device_status(stream)
+    if st[0] != fp8g.OK:
+        raise SystemExit("device status after warm-up: %s" % (st,))
+
+    # ---- timed region: exactly K steps --------------------------------------
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step(args.warmup + i)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world, device)
+    t_wall1 = time.time()
+    total_ms = ev[0][0].elapsed_time(ev[-1][1])
+    per_launch_ms = [a.elapsed_time(b) for a, b in ev]
+    kernel_ms = sum(per_launch_ms) / len(per_launch_ms)
+    st = fp8g.fp8g_get_device_status(stream)
+    if st[0] != fp8g.OK:
+        raise SystemExit("device status after timed region: %s" % (st,))
+    total_ms_max = max_over_ranks(total_ms, world, device)
+    kernel_ms_max = max_over_ranks(kernel_ms, world, device)
+    if sampler:
+        sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+
+    mm = inp.get("masked_m")
+    flops = w.flops(mm)
+    algo_bytes = w.bytes(mm)
+    value = world * args.steps * flops / (total_ms_max * 1e-3) / 1e12
+
+    # ---- end to end through the public API, host buffers ---------------------
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+        s0 = sets[0]
+        D_h = torch.empty(s0["D"].shape, dtype=torch.bfloat16).pin_memory()
+        mm_h = torch.from_numpy(inp["masked_m"]).pin_memory() if mm is not None else None
+
+        def e2e_step():
+            s0["A"].copy_(A_h, non_blocking=True)
+            s0["B"].copy_(B_h, non_blocking=True)
+            if mm_h is not None:
+                s0["mm"].copy_(mm_h, non_blocking=True)
+                fp8g.fp8_gemm_grouped_masked(s0["A"], s0["B"], s0["mm"], s0["D"], max_m_hint=w.hint,
+                                             a_dtype=w.fa, b_dtype=w.fb, flags=w.flags, stream=stream)
+            else:
+                fp8g.fp8_gemm_nt(s0["A"], s0["B"], s0["D"], a_dtype=w.fa, b_dtype=w.fb,
+                                 flags=w.flags, stream=stream)
+            D_h.copy_(s0["D"], non_blocking=True)
+
+        for _ in range(min(3, e2e_steps)):
+            e2e_step()
+        torch.cuda.synchronize(device)
+        barrier(world, device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
+        h2d = A_h.numel() + B_h.numel() + (mm_h.numel() * 4 if mm_h is not None else 0)
+        d2h = D_h.numel() * 2
+        e2e = {"value": world * e2e_steps * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps}
+
+    # ---- roofline of the dominant kernel -----------------------------------------
+    peaks, peak_src = load_peaks()
+    if w.bound == "tensor":
+        peak = FP8_PER_BF16 * peaks["bf16_tflops_sustained"]
+        achieved = flops / (kernel_ms_max * 1e-3) / 1e12
+        unit = "TFLOP/s"
+        basis = ("FP8 = %g x %s BF16 sustained (%.1f TF/s; kernel timed back to back in a long loop)"
+                 % (FP8_PER_BF16, peak_src, peaks["bf16_tflops_sustained"]))
+    else:
+        peak = peaks["hbm_gbs"]
+        achieved = algo_bytes / (kernel_ms_max * 1e-3) / 1e9
+        unit = "GB/s"
+        basis = "%s HBM copy bandwidth" % peak_src
+    traffic = profiled_traffic(w.name)
+    kernel_name = "k_gemm_swap" if (w.flags & 3) == 1 or (w.kind == "masked") else "k_gemm_mn"
+    roof = {"bound": w.bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": traffic, "kernel": kernel_name,
+            "peak_basis": basis, "algorithmic_flop": flops, "algorithmic_bytes": algo_bytes,
+            "kernel_ms": kernel_ms_max}
+    if w.bound == "tensor":
+        roof["frac_of_nominal_4500"] = achieved / 4500.0
+    else:
+        roof["frac_of_nominal_8000"] = achieved / 8000.0
+
+    # ---- CPU baseline (rank 0, N = 1 only) ----------------------------------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        f, s, cores, desc = oracle_sample(w, inp, args.cpu_budget)
+        cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": desc + "; %.1f s" % s}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp8_e4m3" if w.fb == 0 else "fp8_e4m3xe5m2", "data": "synthetic",
+            "config": {"workload": w.desc, "name": w.name,
+                       "l2": "%d rotating input+output sets of %.1f MB (>= 3x the %d MB L2)"
+                             % (n_sets, set_bytes / 1e6, l2 >> 20),
+                       "parallelism": "independent shard per GPU" if world > 1 else "single GPU"},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+        }
+        if w.kind == "masked":
+            line["config"]["sum_masked_m"] = int(sum(mm))
+            line["config"]["empty_groups"] = int(sum(1 for m in mm if m == 0))
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="dense4096")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    rank, _, _ = dist_setup()
+    w = make_workload(args.workload, rank)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

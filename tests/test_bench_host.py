@@ -1,0 +1,155 @@
+"""Host logic of bench.py: workload arithmetic, roofline inputs, and the
+multi-rank path (max over ranks, barrier, per-rank shards) on world-size-2
+gloo process groups on CPU."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+import __graft_entry__  # noqa: F401
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "page_arithmetic.txt")
+
+
+def golden():
+    vals = {}
+    for line in open(GOLDEN):
+        line = line.split("#")[0].strip()
+        if line:
+            k, v = line.split()
+            vals[k] = float(int(v, 16)) if v.startswith("0x") else float(v)
+    return vals
+
+
+def test_page_roofline_arithmetic():
+    """Square GEMM intensity 2n/3 and the ridge point, as printed on the
+    DeepGEMM page §2.2, from the bench's own FLOP and byte counts (bytes as
+    the page counts them: one byte per element of A, B and C)."""
+    g = golden()
+    n = int(g["square_n"])
+    w = bench.Workload("sq", "dense", "", M=n, N=n, K=n)
+    flops = w.flops()
+    page_bytes = 3.0 * n * n
+    assert flops == 2.0 * n ** 3
+    assert abs(flops / page_bytes - g["square_intensity_approx"]) < 5
+    ridge = g["ridge_tflops"] * 1e12 / (g["ridge_tbs"] * 1e12)
+    assert abs(ridge - g["ridge_approx"]) < 5
+
+
+def test_page_tile_bytes():
+    g = golden()
+    assert 128 * 32 == g["tile_a_bytes"]
+    assert 32 * 256 == g["tile_b_bytes"]
+    assert 2 * (128 * 32 + 32 * 256) == g["double_buffer_bytes"]
+
+
+def test_page_64bit_offset_example():
+    """MLS page, Bug 1: the carry of a 64-bit add must not be lost."""
+    g = golden()
+    base, off = int(g["base"]), int(g["offset"])
+    assert base + off == int(g["correct"])
+    low_only = (base & ~0xFFFFFFFF) | ((base + off) & 0xFFFFFFFF)
+    assert low_only == int(g["low_word_only"])
+    assert int(g["correct"]) - low_only == int(g["delta"])
+
+
+def test_page_m_utilisation():
+    g = golden()
+    assert g["natural_m"] / g["instr_m"] == g["utilisation"]
+
+
+def test_workload_bytes_and_flops():
+    w = bench.make_workload("masked")
+    mm = [0, 5, 32, 0, 1]
+    w.G = len(mm)
+    assert w.flops(mm) == 2.0 * 38 * 4096 * 7168
+    live = 3
+    assert w.bytes(mm) == live * 4096 * 7168 + 38 * 7168 + 2 * 38 * 4096
+    d = bench.make_workload("dense4096")
+    assert d.bytes() == 4096 * 4096 * 4
+    s = bench.make_workload("smallm:8:7168:16384:noswap")
+    assert s.flags == 2 and s.M == 8
+    p = bench.make_workload("proj:7168:18432:e5m2")
+    assert p.fb == 1 and p.M == 8192
+
+
+def test_shards_differ_per_rank():
+    a = bench.make_workload("dense4096", rank=0)
+    b = bench.make_workload("dense4096", rank=1)
+    assert a.seed != b.seed
+
+
+def test_traffic_lookup_tracks_kernel_sources(tmp_path, monkeypatch):
+    h = bench.kernel_source_hash()
+    assert len(h) == 16
+    t = bench.profiled_traffic("dense4096")
+    # valid only for the hash it was captured with
+    lines = open(os.path.join(ROOT, "profiles", "traffic.txt")).read()
+    if h in lines:
+        assert t is not None
+    else:
+        assert t is None
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+_WORKER = r"""
+import os, sys, json
+sys.path.insert(0, %(root)r)
+import torch.distributed as dist
+import bench
+dist.init_process_group("gloo", init_method="tcp://127.0.0.1:%(port)d",
+                        rank=int(sys.argv[1]), world_size=2)
+r = dist.get_rank()
+bench.barrier(2)
+m = bench.max_over_ranks(1.0 + 10.0 * r, 2)
+w = bench.make_workload("dense4096", rank=r)
+print(json.dumps({"rank": r, "max": m, "seed": w.seed}))
+dist.destroy_process_group()
+"""
+
+
+def test_two_rank_gloo_max_and_barrier(tmp_path):
+    port = _free_port()
+    script = tmp_path / "w.py"
+    script.write_text(_WORKER % {"root": ROOT, "port": port})
+    procs = [subprocess.Popen([sys.executable, str(script), str(r)], stdout=subprocess.PIPE,
+                              stderr=subprocess.PIPE, text=True) for r in range(2)]
+    outs = [p.communicate(timeout=120) for p in procs]
+    for p, (o, e) in zip(procs, outs):
+        assert p.returncode == 0, e
+    res = [json.loads(o.strip().splitlines()[-1]) for o, _ in outs]
+    assert all(r["max"] == 11.0 for r in res)
+    assert res[0]["seed"] != res[1]["seed"]
+
+
+def test_reference_arm_rank1_does_no_work():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    p = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3"], env=env, capture_output=True,
+                       text=True, timeout=120)
+    assert p.returncode == 0
+    assert p.stdout.strip() == ""
+
+
+def test_reference_arm_line(tmp_path):
+    p = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "cube256", "--steps", "2", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=300)
+    assert p.returncode == 0, p.stderr
+    line = json.loads(p.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+    assert line["unit"] == "TFLOP/s" and line["higher_is_better"] is True
