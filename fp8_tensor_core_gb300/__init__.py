@@ -149,3 +149,26 @@ def fp8_gemm_grouped_masked(A, B, masked_m, D=None, max_m_hint: int = 0, a_dtype
     if rc != OK:
         raise Fp8gError(rc, "fp8_gemm_grouped_masked")
     return D
+
+
+def fp8_gemm_nt_noalloc(A, B, D, a_dtype=None, b_dtype=None, stream=None):
+    """D[M,N] = A[M,K] . B[N,K]^T for M <= 256 tokens without any device
+    allocation by the library: split-K scratch lives in a fixed 32 MiB device
+    array inside the library (for callers whose allocator must own all
+    device memory, or that cannot take cudaMalloc's synchronisation).  D
+    must be given.  Calls on unordered streams race on the shared scratch."""
+    import torch
+    _check_operand(A, "A", 2)
+    _check_operand(B, "B", 2)
+    _check_operand(D, "D", 2)
+    fa, fb = _fp8_code(A, a_dtype), _fp8_code(B, b_dtype)
+    M, K = A.shape
+    N, K2 = B.shape
+    if K != K2 or D.dtype != torch.bfloat16 or tuple(D.shape) != (M, N):
+        raise ValueError("shapes: A [M,K], B [N,K], D bf16 [M,N]")
+    with torch.cuda.device(A.device):
+        rc = _lib.load().fp8_gemm_nt_noalloc(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K,
+                                             fa, fb, _stream_handle(stream))
+    if rc != OK:
+        raise Fp8gError(rc, "fp8_gemm_nt_noalloc")
+    return D

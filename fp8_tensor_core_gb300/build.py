@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libfp8g.so")
-SOURCES = ["kernels.cu", "api.cu"]
+SOURCES = ["kernels.cu", "api.cu", "noalloc.cu"]
 HEADERS = ["kernels.cuh", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

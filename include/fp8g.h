@@ -140,6 +140,40 @@ int fp8g_get_device_status(int32_t *info, cudaStream_t stream);
  */
 uint64_t fp8g_set_wait_timeout_ns(uint64_t ns);
 
+/*
+ * fp8_gemm_nt_noalloc -- dense D = A . B^T for small token counts that
+ * allocates no device memory.  (Not from the pages: they have no
+ * counterpart.)
+ *
+ * For callers that cannot have a library call cudaMalloc: a framework whose
+ * caching allocator must own every device byte, a serving loop that cannot
+ * take cudaMalloc's device-wide synchronisation, code recording launches into
+ * a CUDA graph (allocation is not allowed while capturing).  fp8_gemm_nt may
+ * allocate its split-K workspace on first use; this call instead keeps that
+ * scratch in one fixed device array of FP8G_NOALLOC_SCRATCH_BYTES (32 MiB)
+ * inside the library, which every GPU that loads the library holds until the
+ * process exits.  It runs the same SwapAB split-K kernel with the same tiling
+ * choices as fp8_gemm_nt's small-token path.
+ *
+ *   A [M, K], B [N, K], D [M, N] and the dtypes: as fp8_gemm_nt.
+ *   M  1..256 tokens, else FP8G_ERR_UNSUPPORTED.
+ *   A problem whose partial tiles and counters need more than the fixed
+ *   scratch (about tiles(N/128) x splits x 128 x round16(M) x 4 bytes)
+ *   returns FP8G_ERR_UNSUPPORTED before anything is enqueued.
+ *   No cudaMalloc, cudaFree or allocating library routine is called.  The
+ *   first call on a device looks up the array's device address and the
+ *   device limits (once per device, with that device current): make that
+ *   first call before any stream capture.  Each call clears the scratch's
+ *   arrival counters with cudaMemsetAsync on `stream` before its launch.
+ *   All calls on a device share the array: calls that overlap on the GPU
+ *   (unordered streams) race on it and give wrong results.
+ *   Bounded waits use the default 2 s limit.
+ * Returns FP8G_OK or an error code; on error nothing is enqueued.
+ */
+#define FP8G_NOALLOC_SCRATCH_BYTES (32u << 20)
+int fp8_gemm_nt_noalloc(const void *A, const void *B, void *D, int64_t M, int64_t N,
+                        int64_t K, int a_dtype, int b_dtype, cudaStream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char *fp8g_status_string(int code);
 
