@@ -362,14 +362,17 @@ def run_ours(args, w: Workload):
         sets.append(s)
     torch.cuda.synchronize(device)
 
-    def step(i):
+    def step_on(i, strm):
         s = sets[i % n_sets]
         if w.kind == "dense":
             fp8g.fp8_gemm_nt(s["A"], s["B"], s["D"], a_dtype=w.fa, b_dtype=w.fb, flags=w.flags,
-                             stream=stream)
+                             stream=strm)
         else:
             fp8g.fp8_gemm_grouped_masked(s["A"], s["B"], s["mm"], s["D"], max_m_hint=w.hint,
-                                         a_dtype=w.fa, b_dtype=w.fb, flags=w.flags, stream=stream)
+                                         a_dtype=w.fa, b_dtype=w.fb, flags=w.flags, stream=strm)
+
+    def step(i):
+        step_on(i, stream)
 
     sampler = ClockSampler("GPU-" + str(props.uuid)) if rank == 0 else None
 
@@ -381,21 +384,48 @@ def run_ours(args, w: Workload):
         raise SystemExit("device status after warm-up: %s" % (st,))
 
     # ---- timed region: exactly K steps --------------------------------------
+    # Direct launches are timed per launch with events; small launch-bound
+    # kernels are captured K at a time into one CUDA graph (the launches are
+    # the same C-ABI calls) and the graph replay is timed.
+    use_graph = args.graph == "on" or (args.graph == "auto" and w.bound == "hbm")
+    graph = None
+    if use_graph:
+        gs = torch.cuda.Stream(device)
+        gs.wait_stream(stream)
+        with torch.cuda.stream(gs):
+            for i in range(2):            # warm the side stream too
+                step_on(i, gs)
+        gs.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=gs):
+            for i in range(args.steps):
+                step_on(args.warmup + i, gs)
+        torch.cuda.synchronize(device)
+        graph.replay()                    # upload / first replay, untimed
+        torch.cuda.synchronize(device)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+          for _ in range(1 if use_graph else args.steps)]
     barrier(world, device)
     torch.cuda.synchronize(device)
     t_wall0 = time.time()
-    for i in range(args.steps):
-        ev[i][0].record(stream)
-        step(args.warmup + i)
-        ev[i][1].record(stream)
+    if use_graph:
+        ev[0][0].record(stream)
+        graph.replay()
+        ev[0][1].record(stream)
+    else:
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step(args.warmup + i)
+            ev[i][1].record(stream)
     torch.cuda.synchronize(device)
     barrier(world, device)
     t_wall1 = time.time()
     total_ms = ev[0][0].elapsed_time(ev[-1][1])
-    per_launch_ms = [a.elapsed_time(b) for a, b in ev]
-    kernel_ms = sum(per_launch_ms) / len(per_launch_ms)
+    if use_graph:
+        kernel_ms = total_ms / args.steps
+    else:
+        per_launch_ms = [a.elapsed_time(b) for a, b in ev]
+        kernel_ms = sum(per_launch_ms) / len(per_launch_ms)
     st = fp8g.fp8g_get_device_status(stream)
     if st[0] != fp8g.OK:
         raise SystemExit("device status after timed region: %s" % (st,))
@@ -483,7 +513,7 @@ def run_ours(args, w: Workload):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "fp8_e4m3" if w.fb == 0 else "fp8_e4m3xe5m2", "data": "synthetic",
-            "config": {"workload": w.desc, "name": w.name,
+            "config": {"workload": w.desc, "name": w.name, "flags": hex(w.flags),
                        "l2": "%d rotating input+output sets of %.1f MB (>= 3x the %d MB L2)"
                              % (n_sets, set_bytes / 1e6, l2 >> 20),
                        "parallelism": "independent shard per GPU" if world > 1 else "single GPU"},
@@ -491,6 +521,7 @@ def run_ours(args, w: Workload):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": args.steps,
+            "timing": "one CUDA graph of K launches" if use_graph else "K direct launches, events per launch",
             "clocks": clocks,
         }
         if w.kind == "masked":
@@ -510,6 +541,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="dense4096")
+    ap.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
+                    help="capture the K timed launches in a CUDA graph (auto: HBM-bound workloads)")
+    ap.add_argument("--extra-flags", type=lambda v: int(v, 0), default=0,
+                    help="tuning-override flag bits OR-ed into the call (FP8G_WHOLE_TILES 0x100, FP8G_TILE_N)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -519,6 +554,7 @@ def main(argv=None):
         raise SystemExit("--warmup must be >= 3")
     rank, _, _ = dist_setup()
     w = make_workload(args.workload, rank)
+    w.flags |= args.extra_flags
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

@@ -20,6 +20,17 @@ SWAP_AUTO = 0
 SWAP_ON = 1
 SWAP_OFF = 2
 DEBUG_ONE_STAGE = 0x10
+
+
+WHOLE_TILES = 0x100   # SwapAB kernel: whole tiles per CTA instead of stream-K ranges
+
+
+def TILE_N(n: int) -> int:
+    """Flag bits forcing an N tile of n (multiple of 32, <= 256) in the
+    non-swapped kernel."""
+    return ((int(n) // 32) & 15) << 16
+
+
 DEBUG_DROP_FIRST_LOAD = 0x20
 
 OK = 0
@@ -60,6 +71,25 @@ def fp8g_get_device_status(stream=None):
     if rc != OK:
         raise Fp8gError(rc, "fp8g_get_device_status")
     return tuple(int(v) for v in info)
+
+
+class _NoSwitch:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        return False
+
+
+_NO_SWITCH = _NoSwitch()
+
+
+def _on_device(device):
+    """Make `device` current for the call (a no-op when it already is)."""
+    import torch
+    if device.index is None or device.index == torch.cuda.current_device():
+        return _NO_SWITCH
+    return torch.cuda.device(device)
 
 
 def _stream_handle(stream):
@@ -112,7 +142,7 @@ def fp8_gemm_nt(A, B, D=None, a_dtype=None, b_dtype=None, flags: int = 0, stream
         _check_operand(D, "D", 2)
         if D.dtype != torch.bfloat16 or tuple(D.shape) != (M, N) or D.device != A.device:
             raise ValueError("D must be a contiguous bf16 [M, N] tensor on A's device")
-    with torch.cuda.device(A.device):
+    with _on_device(A.device):
         rc = _lib.load().fp8_gemm_nt(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K,
                                      fa, fb, int(flags), _stream_handle(stream))
     if rc != OK:
@@ -142,7 +172,7 @@ def fp8_gemm_grouped_masked(A, B, masked_m, D=None, max_m_hint: int = 0, a_dtype
         _check_operand(D, "D", 3)
         if D.dtype != torch.bfloat16 or tuple(D.shape) != (G, M_max, N):
             raise ValueError("D must be a contiguous bf16 [G, M_max, N] tensor")
-    with torch.cuda.device(A.device):
+    with _on_device(A.device):
         rc = _lib.load().fp8_gemm_grouped_masked(
             A.data_ptr(), B.data_ptr(), D.data_ptr(), masked_m.data_ptr(), G, M_max, N, K,
             int(max_m_hint), fa, fb, int(flags), _stream_handle(stream))
@@ -153,7 +183,7 @@ def fp8_gemm_grouped_masked(A, B, masked_m, D=None, max_m_hint: int = 0, a_dtype
 
 def fp8_gemm_nt_noalloc(A, B, D, a_dtype=None, b_dtype=None, stream=None):
     """D[M,N] = A[M,K] . B[N,K]^T for M <= 256 tokens without any device
-    allocation by the library: split-K scratch lives in a fixed 32 MiB device
+    allocation by the library: stream-K scratch lives in a fixed 32 MiB device
     array inside the library (for callers whose allocator must own all
     device memory, or that cannot take cudaMalloc's synchronisation).  D
     must be given.  Calls on unordered streams race on the shared scratch."""
@@ -166,7 +196,7 @@ def fp8_gemm_nt_noalloc(A, B, D, a_dtype=None, b_dtype=None, stream=None):
     N, K2 = B.shape
     if K != K2 or D.dtype != torch.bfloat16 or tuple(D.shape) != (M, N):
         raise ValueError("shapes: A [M,K], B [N,K], D bf16 [M,N]")
-    with torch.cuda.device(A.device):
+    with _on_device(A.device):
         rc = _lib.load().fp8_gemm_nt_noalloc(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K,
                                              fa, fb, _stream_handle(stream))
     if rc != OK:

@@ -1,5 +1,5 @@
 // Host side of the C ABI declared in include/fp8g.h: argument validation,
-// variant selection (SwapAB or not, tile sizes, pipeline depth, split-K),
+// variant selection (SwapAB or not, tile sizes, pipeline depth, stream-K),
 // TMA tensor-map encoding and kernel launch.
 //
 // Sources: "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践"
@@ -205,24 +205,6 @@ int pick_tile_n(int64_t m_tiles_total, int64_t N, int sms)
     return best;
 }
 
-// K partitions for the swap kernel: fewest k-block-equivalents over whole
-// waves, each unit charged one extra k-block for its epilogue.
-int pick_k_splits(int64_t tiles, int num_kb, int sms)
-{
-    int best = 1;
-    double best_cost = 1e300;
-    const int max_ks = std::min(16, num_kb);
-    for (int ks = 1; ks <= max_ks; ++ks) {
-        const int64_t waves = cdiv(tiles * ks, sms);
-        const double cost = static_cast<double>(waves) * (static_cast<double>(cdiv(num_kb, ks)) + 1.0);
-        if (cost < best_cost - 1e-9) {
-            best_cost = cost;
-            best = ks;
-        }
-    }
-    return best;
-}
-
 struct Problem {
     const void *A, *B;
     void *D;
@@ -269,35 +251,36 @@ int launch(const Problem &p, cudaStream_t stream)
         const int64_t chunks = cdiv(p.rows_a, cap);
         const int64_t n_tiles = cdiv(p.N, kTileM);
         const int64_t tiles_upper = p.G * chunks * n_tiles;
-        // Dense problems: the tile count is exact, so split K to fill the SMs.
-        int ks = 1;
-        if (!p.masked_m)
-            ks = pick_k_splits(tiles_upper, num_kb, info.sms);
-        if (tiles_upper * ks > kMaxDim)
+        if (tiles_upper > kMaxDim || tiles_upper * num_kb > (int64_t(1) << 53))
             return FP8G_ERR_UNSUPPORTED;
+        // Stream-K over all (tile, k-block) pairs unless whole tiles are asked for.
+        const bool whole_tiles = (p.flags & FP8G_WHOLE_TILES) != 0;
+        int grid = static_cast<int>(std::min<int64_t>(info.sms, whole_tiles ? tiles_upper
+                                                                            : tiles_upper * num_kb));
+        if (grid <= 0)
+            return FP8G_OK;
         args.tile_n = static_cast<int32_t>(cap);
         args.stage_bytes = static_cast<int32_t>(kTileM * kBlockK + cap * kBlockK);
         args.stages = pick_stages(info, args.stage_bytes, p.flags);
-        args.k_splits = ks;
-        if (ks > 1) {
-            const size_t ws_bytes = static_cast<size_t>(tiles_upper) * ks * kTileM * cap * sizeof(float);
-            const size_t cnt_bytes = static_cast<size_t>(tiles_upper) * 4 * sizeof(int32_t);
-            st = ensure_workspace(dev, ws_bytes, cnt_bytes, &args.workspace, &args.counters);
+        args.k_splits = whole_tiles ? 1 : 0;
+        if (!whole_tiles) {
+            st = ensure_workspace(dev, swap_partials_bytes(grid, static_cast<int>(cap)),
+                                  swap_counter_bytes(tiles_upper), &args.workspace, &args.counters);
             if (st != FP8G_OK)
                 return st;
         }
         if (!make_map(&tm0, p.B, p.K, p.N, p.G, kTileM) || !make_map(&tm1, p.A, p.K, p.rows_a, p.G, 16))
             return FP8G_ERR_CUDA;
-        const int grid = static_cast<int>(std::min<int64_t>(tiles_upper * ks, info.sms));
-        if (grid <= 0)
-            return FP8G_OK;
         return launch_gemm_swap(tm0, tm1, args, grid, static_cast<size_t>(info.smem_optin), stream) == cudaSuccess
                    ? FP8G_OK
                    : FP8G_ERR_CUDA;
     }
 
     const int64_t m_tiles = cdiv(p.rows_a, kTileM);
-    const int tile_n = pick_tile_n(p.G * m_tiles, p.N, info.sms);
+    int tile_n = pick_tile_n(p.G * m_tiles, p.N, info.sms);
+    const int tn_override = static_cast<int>((p.flags >> 16) & 15u);
+    if (tn_override >= 1 && tn_override <= 8)
+        tile_n = 32 * tn_override;
     const int64_t units_upper = p.G * m_tiles * cdiv(p.N, tile_n);
     if (units_upper > kMaxDim)
         return FP8G_ERR_UNSUPPORTED;
@@ -378,7 +361,7 @@ extern "C" int fp8g_get_device_status(int32_t *info, cudaStream_t stream)
     if (read_and_clear_status(info) != cudaSuccess)
         return FP8G_ERR_CUDA;
     if (info[0] == FP8G_ERR_TIMEOUT) {
-        // An aborted split-K launch can leave arrival counts behind.
+        // An aborted stream-K launch can leave arrival counts behind.
         std::lock_guard<std::mutex> lk(g_mu);
         Workspace &w = g_ws[dev];
         if (w.counters && cudaMemset(w.counters, 0, w.counter_bytes) != cudaSuccess)

@@ -15,8 +15,9 @@
 //              per group.
 // k_gemm_swap  SwapAB: weights (B) on the M side (128 weight rows), tokens
 //              (A) on N with a per-unit runtime N = valid tokens rounded up
-//              to 16, written into the instruction descriptor.  Optional
-//              split-K with a deterministic fixed-order reduction.
+//              to 16, written into the instruction descriptor.  Stream-K
+//              work split with a deterministic K-ordered reduction of the
+//              partial tiles.
 //
 // Sources: "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践"
 // (sheratonhq.com/news/187119) §3.3 (producer/consumer warp roles), §4.3
@@ -444,7 +445,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // =====================================================================================
 // k_gemm_swap: SwapAB.  Weights (B) on M, tokens (A) on a runtime N.
+//
+// Work is a list of output tiles (group, token chunk, 128 weight rows), each
+// needing num_kb K blocks.  Stream-K: the tiles' K blocks are laid end to end
+// and every CTA takes an equal contiguous range, so all SMs stream the same
+// number of weight bytes.  A range covers whole tiles plus at most two
+// partial ones (its first and last segment); a partial segment publishes an
+// FP32 partial tile, and the contributor whose arrival completes the tile
+// sums all contributions in K order and writes BF16.  Whole-tile mode (one
+// tile per unit, no partials) is kept for comparison.
 // =====================================================================================
+struct SwapSeg {
+    int g, tok0, n_tok, n_mma, w0, kb0, kb1, tile;
+    int kind;   // 0: first segment of this CTA's range, 1: a later segment
+};
+
+struct SwapWalker {
+    // stream-K: k-block positions [pos, end) of the linearised (tile, kb) space
+    long long pos, end;
+    // whole-tile mode: tile index u, stepping by the grid
+    int u;
+    bool first;
+};
+
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_swap(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_t,
                 const GemmArgs a)
@@ -456,7 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int n_tiles = ceil_div(a.n, kTileM);   // 128 weight rows per tile
     const int cap = a.tile_n;                    // tokens per chunk
-    const int ks_n = a.k_splits;
+    const int num_kb = a.num_kb;
+    const bool stream_k = a.k_splits != 1;       // 1 = whole tiles only
     const uint32_t w_bytes = kTileM * kBlockK;   // 16 KB weight box
     constexpr int kTokBox = 16;                  // token rows per TMA box
     constexpr uint32_t kTokBoxBytes = kTokBox * kBlockK;
@@ -464,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0)
         init_barriers(ctl, a.stages);
     if (warp == 0)
-        build_group_table(ctl, a, [&](int m) { return ceil_div(m, cap) * n_tiles * ks_n; });
+        build_group_table(ctl, a, [&](int m) { return ceil_div(m, cap) * n_tiles; });
     if (warp == 1) {
         tmem_alloc(smem_addr(&ctl.tmem_base), kTmemCols);
         tmem_relinquish();
@@ -473,30 +497,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = ctl.tmem_base;
-    const int total = ctl.units_total;
+    const int total_tiles = ctl.units_total;
+    const long long T = static_cast<long long>(total_tiles) * num_kb;
+    // Partition count: never more ranges than k-blocks, so every range that
+    // meets a tile is non-empty and arrives on the tile's counter.  CTAs
+    // beyond it get no stream-K work.
+    const long long P = T < static_cast<long long>(gridDim.x) ? T : static_cast<long long>(gridDim.x);
 
-    // Unit u -> group, token chunk, weight tile, K split (split fastest, so
-    // the parts of one output tile run close together in time).
-    struct U {
-        int g, tok0, n_tok, n_mma, w0, ks, kb0, kb1, tile;
+    // CTA whose stream-K range contains k-block position x.
+    auto cta_of = [&](long long x) { return static_cast<int>(((x + 1) * P - 1) / T); };
+    auto range_begin = [&](long long b) { return b * T / P; };
+
+    auto make_walker = [&]() {
+        SwapWalker w;
+        if (static_cast<long long>(blockIdx.x) < P) {
+            w.pos = range_begin(blockIdx.x);
+            w.end = range_begin(static_cast<long long>(blockIdx.x) + 1);
+        } else {
+            w.pos = w.end = 0;
+        }
+        w.u = blockIdx.x;
+        w.first = true;
+        return w;
     };
-    auto decode = [&](int u) {
-        U x;
-        x.g = find_group(ctl, a.groups, u);
-        const int local = u - ctl.group_prefix[x.g];
-        x.ks = local % ks_n;
-        const int rest = local / ks_n;
-        const int nt = rest % n_tiles;
-        const int chunk = rest / n_tiles;
+    // Next segment of this CTA's work; false when done.
+    auto next_seg = [&](SwapWalker &w, SwapSeg &x) {
+        int tile;
+        if (stream_k) {
+            if (w.pos >= w.end)
+                return false;
+            tile = static_cast<int>(w.pos / num_kb);
+            x.kb0 = static_cast<int>(w.pos - static_cast<long long>(tile) * num_kb);
+            const long long left = w.end - w.pos;
+            x.kb1 = left < num_kb - x.kb0 ? x.kb0 + static_cast<int>(left) : num_kb;
+            w.pos += x.kb1 - x.kb0;
+        } else {
+            if (w.u >= total_tiles)
+                return false;
+            tile = w.u;
+            x.kb0 = 0;
+            x.kb1 = num_kb;
+            w.u += gridDim.x;
+        }
+        x.tile = tile;
+        x.kind = w.first ? 0 : 1;
+        w.first = false;
+        x.g = find_group(ctl, a.groups, tile);
+        const int local = tile - ctl.group_prefix[x.g];
+        const int nt = local % n_tiles;
+        const int chunk = local / n_tiles;
         x.tok0 = chunk * cap;
-        const int left = ctl.group_m[x.g] - x.tok0;
-        x.n_tok = left < cap ? left : cap;
+        const int left_tok = ctl.group_m[x.g] - x.tok0;
+        x.n_tok = left_tok < cap ? left_tok : cap;
         x.n_mma = (x.n_tok + 15) & ~15;
         x.w0 = nt * kTileM;
-        x.kb0 = static_cast<int>((static_cast<long long>(x.ks) * a.num_kb) / ks_n);
-        x.kb1 = static_cast<int>((static_cast<long long>(x.ks + 1) * a.num_kb) / ks_n);
-        x.tile = u / ks_n;
-        return x;
+        return true;
     };
 
     if (warp == 0) {
@@ -511,8 +566,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool aborted = false;
         const bool drop = (a.flags & FP8G_DEBUG_DROP_FIRST_LOAD) && blockIdx.x == 0;
         const uint64_t w_policy = policy_evict_first();   // weights are read once
-        for (int u = blockIdx.x; u < total && !aborted; u += gridDim.x) {
-            const U x = decode(u);
+        SwapWalker wk = make_walker();
+        SwapSeg x;
+        while (!aborted && next_seg(wk, x)) {
             const uint32_t tx = w_bytes + static_cast<uint32_t>(x.n_mma) * kBlockK;
             for (int kb = x.kb0; kb < x.kb1; ++kb) {
                 if (!warp_wait(smem_addr(&ctl.empty[stage]), phase ^ 1u, ctl, a.timeout_ns,
@@ -547,8 +603,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         bool issued_any = false;
-        for (int u = blockIdx.x; u < total; u += gridDim.x) {
-            const U x = decode(u);
+        SwapWalker wk = make_walker();
+        SwapSeg x;
+        while (next_seg(wk, x)) {
             const uint32_t idesc = make_idesc(a.b_fmt, a.a_fmt, kTileM, static_cast<uint32_t>(x.n_mma));
             if (!warp_wait(smem_addr(&ctl.tempty[acc]), acc_phase ^ 1u, ctl, a.timeout_ns, kRoleMma,
                            100 + acc))
@@ -596,35 +653,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Thread = weight row n (TMEM lane), registers = tokens (TMEM columns).
         // For a fixed token the 32 lanes of a warp write 32 consecutive n.
         const int q = warp & 3;
+        const int row = q * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
         __nv_bfloat16 *dout = static_cast<__nv_bfloat16 *>(a.d);
-        for (int u = blockIdx.x; u < total; u += gridDim.x) {
-            const U x = decode(u);
+        // Partial tiles: slot (cta, kind) of [cap/4 token groups][128 weight
+        // rows][4 tokens] FP32.  A thread owns one weight row and moves 4 tokens
+        // per 16-byte access; a warp touches 512 consecutive bytes.
+        const int64_t part_stride4 = kTileM * static_cast<int64_t>(cap) / 4;
+        float4 *slots = reinterpret_cast<float4 *>(a.workspace);
+        SwapWalker wk = make_walker();
+        SwapSeg x;
+        while (next_seg(wk, x)) {
             if (!warp_wait(smem_addr(&ctl.tfull[acc]), acc_phase, ctl, a.timeout_ns, kRoleEpilogue,
                            200 + acc))
                 break;
             tc_fence_after();
-            const int nrow = x.w0 + q * 32 + lane;
+            const int nrow = x.w0 + row;
             const bool n_ok = nrow < a.n;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * kAccStride);
             __nv_bfloat16 *dcol = dout + static_cast<int64_t>(x.g) * a.rows_a * static_cast<int64_t>(a.n) +
                                   nrow;
-            bool last = true;
-            if (ks_n > 1) {
-                // Publish this split's partial tile, then count arrivals for
-                // this (tile, quadrant); the last of the ks_n arrivals reduces
-                // all partials in split order.
-                float *ws = a.workspace +
-                            (static_cast<int64_t>(x.tile) * ks_n + x.ks) * (kTileM * static_cast<int64_t>(cap));
+            const bool whole = x.kb0 == 0 && x.kb1 == num_kb;
+            if (whole) {
+                for (int c = 0; c < x.n_mma; c += 16) {
+                    uint32_t r[16];
+                    tmem_ld_32x32b_x16(t_row + static_cast<uint32_t>(c), r);
+                    if (n_ok) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            if (c + j < x.n_tok)
+                                dcol[static_cast<int64_t>(x.tok0 + c + j) * a.n] =
+                                    __float2bfloat16_rn(__uint_as_float(r[j]));
+                        }
+                    }
+                }
+            } else {
+                // Contributors of this tile: the CTAs whose ranges meet it,
+                // in K order.
+                const long long t0 = static_cast<long long>(x.tile) * num_kb;
+                const int first = cta_of(t0);
+                const int n_contrib = cta_of(t0 + num_kb - 1) - first + 1;
+                float4 *mine = slots + (static_cast<int64_t>(blockIdx.x) * 2 + x.kind) * part_stride4;
                 for (int c = 0; c < x.n_mma; c += 16) {
                     uint32_t r[16];
                     tmem_ld_32x32b_x16(t_row + static_cast<uint32_t>(c), r);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (c + j < x.n_tok)
-                            ws[(c + j) * kTileM + q * 32 + lane] = __uint_as_float(r[j]);
+                    for (int v = 0; v < 4; ++v)
+                        mine[(c / 4 + v) * kTileM + row] =
+                            make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                        __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
                 }
                 __threadfence();
                 __syncwarp();
@@ -632,44 +711,57 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0)
                     prev = atomicAdd(a.counters + static_cast<int64_t>(x.tile) * 4 + q, 1);
                 prev = __shfl_sync(0xffffffffu, prev, 0);
-                last = (prev == ks_n - 1);
-                if (last) {
+                if (prev == n_contrib - 1) {
+                    // The tile is complete: sum the contributions in K order
+                    // (this segment's own from memory too), 16 tokens of four
+                    // contributors per batch, every load unconditional.
                     __threadfence();
                     if (lane == 0)
-                        a.counters[static_cast<int64_t>(x.tile) * 4 + q] = 0;  // ready for the next launch
-                }
-            }
-            if (last) {
-                for (int c = 0; c < x.n_mma; c += 16) {
-                    uint32_t r[16];
-                    tmem_ld_32x32b_x16(t_row + static_cast<uint32_t>(c), r);
-                    float v[16];
+                        a.counters[static_cast<int64_t>(x.tile) * 4 + q] = 0;   // ready for the next launch
+                    for (int c = 0; c < x.n_mma; c += 16) {
+                        float acc_v[16];
+                        for (int p0 = 0; p0 < n_contrib; p0 += 4) {
+                            float4 buf[4][4];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        v[j] = __uint_as_float(r[j]);
-                    if (ks_n > 1) {
-                        const float *base = a.workspace +
-                                            static_cast<int64_t>(x.tile) * ks_n * (kTileM * static_cast<int64_t>(cap));
+                            for (int i = 0; i < 4; ++i) {
+                                const int ci = (p0 + i < n_contrib) ? p0 + i : 0;
+                                const int cta = first + ci;
+                                const int kind =
+                                    (range_begin(cta) / num_kb == static_cast<long long>(x.tile)) ? 0 : 1;
+                                const float4 *src = slots + (static_cast<int64_t>(cta) * 2 + kind) * part_stride4 +
+                                                    (c / 4) * kTileM + row;
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            if (c + j >= x.n_tok)
-                                continue;
-                            float s = 0.0f;
-                            for (int p = 0; p < ks_n; ++p) {
-                                const float t = (p == x.ks)
-                                                    ? v[j]
-                                                    : __ldcg(base + static_cast<int64_t>(p) * kTileM * cap +
-                                                             (c + j) * kTileM + q * 32 + lane);
-                                s = (p == 0) ? t : s + t;
+                                for (int w = 0; w < 4; ++w)
+                                    buf[i][w] = __ldcg(src + w * kTileM);
                             }
-                            v[j] = s;
-                        }
-                    }
-                    if (n_ok) {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            if (c + j < x.n_tok)
-                                dcol[static_cast<int64_t>(x.tok0 + c + j) * a.n] = __float2bfloat16_rn(v[j]);
+                            for (int i = 0; i < 4; ++i) {
+                                if (p0 + i >= n_contrib)
+                                    break;
+#pragma unroll
+                                for (int w = 0; w < 4; ++w) {
+                                    const float4 f = buf[i][w];
+                                    if (p0 + i == 0) {
+                                        acc_v[4 * w] = f.x;
+                                        acc_v[4 * w + 1] = f.y;
+                                        acc_v[4 * w + 2] = f.z;
+                                        acc_v[4 * w + 3] = f.w;
+                                    } else {
+                                        acc_v[4 * w] += f.x;
+                                        acc_v[4 * w + 1] += f.y;
+                                        acc_v[4 * w + 2] += f.z;
+                                        acc_v[4 * w + 3] += f.w;
+                                    }
+                                }
+                            }
+                        }
+                        if (n_ok) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                if (c + j < x.n_tok)
+                                    dcol[static_cast<int64_t>(x.tok0 + c + j) * a.n] =
+                                        __float2bfloat16_rn(acc_v[j]);
+                            }
                         }
                     }
                 }

@@ -36,13 +36,16 @@ struct GemmArgs {
                                // swap kernel: token chunk (16..256, multiple of 16)
     int32_t stages;            // pipeline depth (1..kMaxStages)
     int32_t stage_bytes;       // bytes per stage (multiple of 1024)
-    int32_t k_splits;          // swap kernel: K partitions per output tile (1 = none)
+    int32_t k_splits;          // swap kernel: 1 = whole tiles per unit; otherwise stream-K
+                               // (equal k-block ranges per CTA, partial tiles reduced)
     int32_t raster_band;       // mn kernel: M tiles per rasterisation band
     uint32_t a_fmt, b_fmt;     // 0 = E4M3, 1 = E5M2 (of A and B as passed by the caller)
     uint32_t flags;            // FP8G_DEBUG_* bits
     uint64_t timeout_ns;       // limit of every barrier wait
-    float *workspace;          // swap kernel, k_splits > 1: FP32 partial tiles
-    int32_t *counters;         // swap kernel, k_splits > 1: arrivals per (tile, warp)
+    float *workspace;          // swap kernel, stream-K: 2 FP32 partial tiles per CTA
+                               // (128 x tile_n floats each)
+    int32_t *counters;         // swap kernel, stream-K: arrivals per (tile, epilogue warp),
+                               // zero at rest
 };
 
 // Shared-memory footprint of a launch (stages + control block + alignment).
@@ -58,6 +61,13 @@ cudaError_t launch_gemm_mn(const CUtensorMap &tm_a, const CUtensorMap &tm_b, con
                            int grid, size_t smem, cudaStream_t stream);
 cudaError_t launch_gemm_swap(const CUtensorMap &tm_w, const CUtensorMap &tm_t,
                              const GemmArgs &args, int grid, size_t smem, cudaStream_t stream);
+
+// Scratch a swap-kernel launch needs: partial tiles (2 per CTA) and counters.
+inline size_t swap_partials_bytes(int grid, int tile_n)
+{
+    return static_cast<size_t>(grid) * 2 * kTileM * static_cast<size_t>(tile_n) * sizeof(float);
+}
+inline size_t swap_counter_bytes(long long tiles) { return static_cast<size_t>(tiles) * 4 * sizeof(int32_t); }
 
 // Status word of the current device: read it, then clear it.
 cudaError_t read_and_clear_status(int32_t info[4]);

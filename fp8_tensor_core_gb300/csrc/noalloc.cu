@@ -1,4 +1,4 @@
-// fp8_gemm_nt_noalloc: the small-token SwapAB split-K GEMM with its scratch
+// fp8_gemm_nt_noalloc: the small-token SwapAB stream-K GEMM with its scratch
 // in a fixed, file-scope device array instead of library-allocated memory.
 //
 // Some callers cannot let a library call cudaMalloc: a framework whose
@@ -6,10 +6,10 @@
 // reuses memory and would be bypassed), a serving loop that must not take
 // cudaMalloc's implicit device-wide synchronisation on its latency path, or
 // code that records its launches into a CUDA graph, where allocation calls
-// are not allowed while capturing.  fp8_gemm_nt may allocate its split-K
+// are not allowed while capturing.  fp8_gemm_nt may allocate its stream-K
 // workspace on first use; this entry point never allocates.  It launches the
 // same k_gemm_swap kernel as fp8_gemm_nt's SwapAB path with the same tiling
-// choices, pointing the kernel's split-K partial tiles and arrival counters
+// choices, pointing the kernel's stream-K partial tiles and arrival counters
 // at g_noalloc_scratch.
 //
 // The scratch array is FP8G_NOALLOC_SCRATCH_BYTES long and every GPU that
@@ -114,24 +114,6 @@ bool encode(CUtensorMap *m, const void *base, int64_t k, int64_t rows, uint32_t 
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Same rule as the allocating entry point: fewest k-block-equivalents over
-// whole waves, one extra k-block per unit for its epilogue.
-int k_splits_for(int64_t tiles, int num_kb, int sms)
-{
-    int best = 1;
-    double best_cost = 1e300;
-    const int max_ks = std::min(16, num_kb);
-    for (int ks = 1; ks <= max_ks; ++ks) {
-        const double cost = static_cast<double>(cdiv(tiles * ks, sms)) *
-                            (static_cast<double>(cdiv(num_kb, ks)) + 1.0);
-        if (cost < best_cost - 1e-9) {
-            best_cost = cost;
-            best = ks;
-        }
-    }
-    return best;
-}
-
 }  // namespace
 }  // namespace fp8g
 
@@ -169,11 +151,12 @@ extern "C" int fp8_gemm_nt_noalloc(const void *A, const void *B, void *D, int64_
     const int num_kb = static_cast<int>(cdiv(K, kBlockK));
     const int64_t cap = cdiv(M, 16) * 16;             // tokens per chunk (M <= 256: one chunk)
     const int64_t tiles = cdiv(N, kTileM);
-    const int ks = k_splits_for(tiles, num_kb, sms);
-    // Scratch layout: arrival counters (4 per tile), then FP32 partial tiles.
-    const size_t counter_bytes = static_cast<size_t>(tiles) * 4 * sizeof(int32_t);
+    const int grid = static_cast<int>(std::min<int64_t>(sms, tiles * num_kb));
+    // Scratch layout: arrival counters (4 per tile), then the stream-K
+    // partial tiles (2 per CTA).
+    const size_t counter_bytes = swap_counter_bytes(tiles);
     const size_t counter_span = (counter_bytes + 255) & ~static_cast<size_t>(255);
-    const size_t ws_bytes = ks > 1 ? static_cast<size_t>(tiles) * ks * kTileM * cap * sizeof(float) : 0;
+    const size_t ws_bytes = swap_partials_bytes(grid, static_cast<int>(cap));
     if (counter_span + ws_bytes > static_cast<size_t>(FP8G_NOALLOC_SCRATCH_BYTES))
         return FP8G_ERR_UNSUPPORTED;                  // needs more scratch than the fixed array holds
 
@@ -190,7 +173,7 @@ extern "C" int fp8_gemm_nt_noalloc(const void *A, const void *B, void *D, int64_
     args.stage_bytes = static_cast<int32_t>(kTileM * kBlockK + cap * kBlockK);
     const int budget = smem - kCtlBytes - kSmemAlignPad;
     args.stages = std::max(1, std::min(kMaxStages, budget / args.stage_bytes));
-    args.k_splits = ks;
+    args.k_splits = 0;                                // stream-K, as fp8_gemm_nt's SwapAB path
     args.raster_band = 1;
     args.a_fmt = static_cast<uint32_t>(a_dtype);
     args.b_fmt = static_cast<uint32_t>(b_dtype);
@@ -198,14 +181,13 @@ extern "C" int fp8_gemm_nt_noalloc(const void *A, const void *B, void *D, int64_
     args.timeout_ns = kWaitLimitNs;
     unsigned char *base = static_cast<unsigned char *>(scratch);
     args.counters = reinterpret_cast<int32_t *>(base);
-    args.workspace = ks > 1 ? reinterpret_cast<float *>(base + counter_span) : nullptr;
+    args.workspace = reinterpret_cast<float *>(base + counter_span);
 
     CUtensorMap tm_w, tm_t;
     if (!encode(&tm_w, B, K, N, kTileM) || !encode(&tm_t, A, K, M, 16))
         return FP8G_ERR_CUDA;
-    if (ks > 1 && cudaMemsetAsync(args.counters, 0, counter_bytes, stream) != cudaSuccess)
+    if (cudaMemsetAsync(args.counters, 0, counter_bytes, stream) != cudaSuccess)
         return FP8G_ERR_CUDA;
-    const int grid = static_cast<int>(std::min<int64_t>(tiles * ks, sms));
     return launch_gemm_swap(tm_w, tm_t, args, grid, static_cast<size_t>(smem), stream) == cudaSuccess
                ? FP8G_OK
                : FP8G_ERR_CUDA;

@@ -72,6 +72,13 @@ typedef enum {
 #define FP8G_SWAP_ON 1u    /* weights (B) on the MMA M side, tokens (A) on N       */
 #define FP8G_SWAP_OFF 2u   /* tokens (A) on the MMA M side, weights (B) on N       */
 #define FP8G_SWAP_MASK 3u
+/* Tuning overrides (0 = the library's choice).  Results stay correct for
+ * every value; only speed (and the last bits of rounding) change.
+ *   FP8G_WHOLE_TILES  SwapAB kernel: each CTA takes whole output tiles in
+ *                     turn instead of an equal stream-K range of K blocks
+ *   FP8G_TILE_N(n)    non-swapped kernel: N tile of n (32..256, multiple of 32) */
+#define FP8G_WHOLE_TILES 0x100u
+#define FP8G_TILE_N(n) (((((uint32_t)(n)) / 32u) & 15u) << 16)
 /* Debug bits (bench and tests only; never needed for correct results). */
 #define FP8G_DEBUG_ONE_STAGE 0x10u       /* one shared-memory stage: load,
                                             compute, load ... (isolates races
@@ -149,17 +156,18 @@ uint64_t fp8g_set_wait_timeout_ns(uint64_t ns);
  * caching allocator must own every device byte, a serving loop that cannot
  * take cudaMalloc's device-wide synchronisation, code recording launches into
  * a CUDA graph (allocation is not allowed while capturing).  fp8_gemm_nt may
- * allocate its split-K workspace on first use; this call instead keeps that
+ * allocate its stream-K workspace on first use; this call instead keeps that
  * scratch in one fixed device array of FP8G_NOALLOC_SCRATCH_BYTES (32 MiB)
  * inside the library, which every GPU that loads the library holds until the
- * process exits.  It runs the same SwapAB split-K kernel with the same tiling
- * choices as fp8_gemm_nt's small-token path.
+ * process exits.  It runs the same SwapAB stream-K kernel with the same
+ * tiling choices as fp8_gemm_nt's small-token path.
  *
  *   A [M, K], B [N, K], D [M, N] and the dtypes: as fp8_gemm_nt.
  *   M  1..256 tokens, else FP8G_ERR_UNSUPPORTED.
  *   A problem whose partial tiles and counters need more than the fixed
- *   scratch (about tiles(N/128) x splits x 128 x round16(M) x 4 bytes)
- *   returns FP8G_ERR_UNSUPPORTED before anything is enqueued.
+ *   scratch (2 x SMs x 128 x round16(M) x 4 bytes plus 16 bytes per 128
+ *   rows of N; tokens up to about 192 fit on 152 SMs) returns
+ *   FP8G_ERR_UNSUPPORTED before anything is enqueued.
  *   No cudaMalloc, cudaFree or allocating library routine is called.  The
  *   first call on a device looks up the array's device address and the
  *   device limits (once per device, with that device current): make that

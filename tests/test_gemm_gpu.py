@@ -171,7 +171,7 @@ def test_accumulator_keeps_small_terms():
 
 
 def test_deterministic_repeat():
-    A, B = dense_inputs(64, 7168, 4096, E4, E4, 29)      # small M: split-K path
+    A, B = dense_inputs(64, 7168, 4096, E4, E4, 29)      # small M: stream-K path
     Ad, Bd = dev(A), dev(B)
     D1 = fp8g.fp8_gemm_nt(Ad, Bd, a_dtype=E4, b_dtype=E4, flags=ON)
     D2 = fp8g.fp8_gemm_nt(Ad, Bd, a_dtype=E4, b_dtype=E4, flags=ON)
@@ -263,3 +263,32 @@ def test_grouped_masked_m_out_of_range_is_clamped_and_flagged():
 
 def test_grouped_mixed_formats():
     grouped_case(3, 40, 256, 384, [40, 9, 25], ON, 40, seed=151, fb=E5)
+
+
+# ---- stream-K partition edge cases (SwapAB kernel) -------------------------------
+
+@pytest.mark.parametrize("M,N,K", [
+    (16, 128, 128 * 200),     # one tile whose 200 K blocks span every CTA
+    (5, 1280, 128 * 16),      # 160 K blocks over 152 CTAs: ~15 contributors per tile
+    (33, 384, 128 * 3),       # fewer K blocks (9) than SMs: partition shrinks
+    (64, 24576, 1536),        # the small-M streaming shape, every element
+    (1, 7168, 16384),
+])
+def test_stream_k_partitions(M, N, K):
+    check_dense(M, N, K, flags=ON, seed=7 * M + N + K)
+
+
+def test_whole_tiles_mode_matches_stream_k():
+    A, B = dense_inputs(40, 2048, 2048, E4, E4, 41)
+    sk = run_dense(A, B, E4, E4, ON)
+    wt = run_dense(A, B, E4, E4, ON | fp8g.WHOLE_TILES)
+    ref, absdot = oracle.gemm_nt(A, B)
+    for got in (sk, wt):
+        ok, rep = oracle.check_bf16(got, ref, absdot)
+        assert ok, rep
+
+
+def test_grouped_stream_k_many_groups():
+    mm = [0, 3, 0, 128, 1, 77, 0, 16, 128, 5, 31, 0]
+    grouped_case(len(mm), 128, 384, 1024, mm, ON, 0, seed=161)
+    grouped_case(len(mm), 128, 384, 1024, mm, ON | fp8g.WHOLE_TILES, 0, seed=162)

@@ -1,7 +1,7 @@
 """fp8_gemm_nt_noalloc, the entry point that allocates no device memory
 (for callers whose own allocator must own every device byte, or that cannot
 take cudaMalloc's synchronisation or call it during graph capture).  Its
-split-K scratch is a fixed device array inside the library, shared by every
+stream-K scratch is a fixed device array inside the library, shared by every
 call, so two calls in a row must both agree with the allocating entry point.
 
 Kept in a file of its own that pytest collects last."""
