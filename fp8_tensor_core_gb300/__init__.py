@@ -23,6 +23,7 @@ DEBUG_ONE_STAGE = 0x10
 
 
 WHOLE_TILES = 0x100   # SwapAB kernel: whole tiles per CTA instead of stream-K ranges
+SINGLE_SM_TILES = 0x200   # dense non-swapped: one SM per 128-row tile instead of SM pairs
 
 
 def TILE_N(n: int) -> int:

@@ -276,6 +276,33 @@ int launch(const Problem &p, cudaStream_t stream)
                    : FP8G_ERR_CUDA;
     }
 
+    // Dense problems with more than one 128-row token tile: two SMs per
+    // 256-row tile (cta_group::2), unless single-SM tiles are asked for.
+    if (!p.masked_m && p.G == 1 && p.rows_a > kTileM && !(p.flags & FP8G_SINGLE_SM_TILES)) {
+        const int64_t m_tiles2 = cdiv(p.rows_a, 2 * kTileM);
+        const int pairs = info.sms / 2;
+        int tile_n = pick_tile_n(m_tiles2, p.N, pairs);
+        const int tn_override = static_cast<int>((p.flags >> 16) & 15u);
+        if (tn_override >= 1 && tn_override <= 8)
+            tile_n = 32 * tn_override;
+        const int64_t units = m_tiles2 * cdiv(p.N, tile_n);
+        if (units > kMaxDim)
+            return FP8G_ERR_UNSUPPORTED;
+        args.tile_n = tile_n;
+        args.stage_bytes = kTileM * kBlockK + (tile_n / 2) * kBlockK;
+        args.stages = pick_stages(info, args.stage_bytes, p.flags);
+        const int64_t band = (48ll << 20) / (2 * kTileM * p.K);
+        args.raster_band = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(band, m_tiles2)));
+        if (!make_map(&tm0, p.A, p.K, p.rows_a, 1, kTileM) ||
+            !make_map(&tm1, p.B, p.K, p.N, 1, static_cast<uint32_t>(tile_n / 2)))
+            return FP8G_ERR_CUDA;
+        const int grid = 2 * static_cast<int>(std::min<int64_t>(units, pairs));
+        return launch_gemm_mn2(tm0, tm1, args, grid, static_cast<size_t>(info.smem_optin), stream) ==
+                       cudaSuccess
+                   ? FP8G_OK
+                   : FP8G_ERR_CUDA;
+    }
+
     const int64_t m_tiles = cdiv(p.rows_a, kTileM);
     int tile_n = pick_tile_n(p.G * m_tiles, p.N, info.sms);
     const int tn_override = static_cast<int>((p.flags >> 16) & 15u);

@@ -60,6 +60,7 @@ struct alignas(16) SmemCtl {
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
+    uint64_t pair_exit;   // CTA-pair kernel: the peer's "done" arrival
     uint32_t tmem_base;
     volatile int32_t abort;
     int32_t units_total;
@@ -444,6 +445,281 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // =====================================================================================
+// k_gemm_mn2: dense, tokens on M, two SMs per tile (tcgen05 cta_group::2).
+//
+// A cluster of two CTAs computes a 256 x tile_n output tile.  Each CTA loads
+// its own 128 token rows and half of the tile's weight rows into its shared
+// memory; the even CTA issues one 256-row MMA that reads A from both CTAs and
+// B from both halves, so each weight byte is read from shared memory once
+// for two SMs' worth of tensor-core work.  Each CTA's TMEM holds its own 128
+// output rows and its own epilogue writes them.
+//
+// Barriers: full[s] lives in the even CTA (both CTAs' copies complete on it,
+// the even CTA's producer posts the byte count for both); empty[s] and
+// tfull[b] receive multicast commits in both CTAs; tempty[b] (even CTA)
+// counts the four epilogue warps of both CTAs.
+// =====================================================================================
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    k_gemm_mn2(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+               const GemmArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const Smem sm = carve(smem_raw, a);
+    SmemCtl &ctl = *sm.ctl;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int half_n = a.tile_n / 2;
+    const int n_tiles = ceil_div(a.n, a.tile_n);
+    const int m_tiles = ceil_div(a.rows_a, 2 * kTileM);
+    const int total = m_tiles * n_tiles;
+    const uint32_t a_bytes = kTileM * kBlockK;                          // own 128 token rows
+    const uint32_t tx_pair = 2u * (a_bytes + static_cast<uint32_t>(half_n) * kBlockK);
+    const int cid = blockIdx.x >> 1;
+    const int ncl = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(smem_addr(&ctl.full[s]), 1);
+            mbar_init(smem_addr(&ctl.empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_addr(&ctl.tfull[b]), 1);
+            mbar_init(smem_addr(&ctl.tempty[b]), 2 * 4);
+        }
+        mbar_init(smem_addr(&ctl.drain), 1);
+        mbar_init(smem_addr(&ctl.pair_exit), 1);
+        ctl.abort = 0;
+        fence_mbar_init();
+    }
+    // Both CTAs' barriers must exist before any copy, commit or arrive
+    // crosses the pair.
+    cluster_sync_all();
+    if (warp == 1) {
+        tmem_alloc_pair(smem_addr(&ctl.tmem_base), kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ctl.tmem_base;
+
+    // Tile u -> first row of this CTA's half, first column of the tile.
+    auto decode = [&](int u, int &m0, int &n0) {
+        const int band_units = a.raster_band * n_tiles;
+        const int band = u / band_units;
+        const int in_band = u - band * band_units;
+        const int rows_left = m_tiles - band * a.raster_band;
+        const int gm = rows_left < a.raster_band ? rows_left : a.raster_band;
+        m0 = (band * a.raster_band + in_band % gm) * (2 * kTileM) + static_cast<int>(rank) * kTileM;
+        n0 = (in_band / gm) * a.tile_n;
+    };
+
+    bool aborted = false;
+    if (warp == 0) {
+        // ------------------------------- loader -------------------------------
+        if (lane == 0) {
+            tma_prefetch_map(&tm_a);
+            tma_prefetch_map(&tm_b);
+        }
+        int stage = 0;
+        uint32_t phase = 0;
+        long long issued = 0;
+        const bool drop = (a.flags & FP8G_DEBUG_DROP_FIRST_LOAD) && blockIdx.x == 0;
+        for (int u = cid; u < total && !aborted; u += ncl) {
+            int m0, n0;
+            decode(u, m0, n0);
+            for (int kb = 0; kb < a.num_kb; ++kb) {
+                if (!warp_wait(smem_addr(&ctl.empty[stage]), phase ^ 1u, ctl, a.timeout_ns,
+                               kRoleLoader, stage)) {
+                    aborted = true;
+                    break;
+                }
+                if (lane == 0 && !(drop && issued == 0)) {
+                    uint8_t *sa = sm.stages + static_cast<size_t>(stage) * a.stage_bytes;
+                    if (leader)
+                        mbar_arrive_expect_tx(smem_addr(&ctl.full[stage]), tx_pair);
+                    const uint32_t fb = mapa_shared(smem_addr(&ctl.full[stage]), 0);
+                    tma_load_3d_pair(smem_addr(sa), &tm_a, fb, kb * kBlockK, m0, 0);
+                    tma_load_3d_pair(smem_addr(sa + a_bytes), &tm_b, fb, kb * kBlockK,
+                                     n0 + static_cast<int>(rank) * half_n, 0);
+                }
+                __syncwarp();
+                ++issued;
+                if (++stage == a.stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!aborted) {
+            // Wait until the pair MMA has released every stage this CTA filled.
+            for (int i = 0; i < a.stages; ++i) {
+                if (!warp_wait(smem_addr(&ctl.empty[stage]), phase ^ 1u, ctl, a.timeout_ns,
+                               kRoleLoader, stage)) {
+                    aborted = true;
+                    break;
+                }
+                if (++stage == a.stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (aborted && leader) {
+            // The even CTA's full barriers count both CTAs' copies: wait for
+            // the fills it posted.
+            for (int s = 0; s < a.stages; ++s) {
+                if (issued < a.stages && s >= issued)
+                    continue;
+                if (drop && issued <= a.stages && s == 0)
+                    continue;
+                const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
+                warp_wait_drain(smem_addr(&ctl.full[s]), par, a.timeout_ns);
+            }
+        }
+    } else if (warp == 1) {
+        // ----------------------------- MMA issuer -----------------------------
+        if (leader) {
+            const uint32_t idesc = make_idesc(a.a_fmt, a.b_fmt, 2 * kTileM, a.tile_n);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool issued_any = false;
+            for (int u = cid; u < total && !aborted; u += ncl) {
+                if (!warp_wait(smem_addr(&ctl.tempty[acc]), acc_phase ^ 1u, ctl, a.timeout_ns, kRoleMma,
+                               100 + acc)) {
+                    aborted = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccStride);
+                for (int kb = 0; kb < a.num_kb; ++kb) {
+                    if (!warp_wait(smem_addr(&ctl.full[stage]), phase, ctl, a.timeout_ns, kRoleMma,
+                                   stage)) {
+                        aborted = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t sa = smem_addr(sm.stages + static_cast<size_t>(stage) * a.stage_bytes);
+                        const uint64_t adesc = smem_desc_k_sw128(sa);
+                        const uint64_t bdesc = smem_desc_k_sw128(sa + a_bytes);
+#pragma unroll
+                        for (int k = 0; k < kBlockK / 32; ++k)
+                            mma_f8f6f4_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc,
+                                            (kb | k) != 0 ? 1u : 0u);
+                        mma_commit_pair_mc(smem_addr(&ctl.empty[stage]), 0x3);
+                    }
+                    __syncwarp();
+                    issued_any = true;
+                    if (++stage == a.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (aborted)
+                    break;
+                if (lane == 0)
+                    mma_commit_pair_mc(smem_addr(&ctl.tfull[acc]), 0x3);
+                __syncwarp();
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            // Both CTAs' epilogues must be done with every accumulator (their
+            // arrivals on this CTA's tempty have all landed) before TMEM goes.
+            for (int i = 0; i < 2 && !aborted; ++i) {
+                if (!warp_wait(smem_addr(&ctl.tempty[acc]), acc_phase ^ 1u, ctl, a.timeout_ns, kRoleMma,
+                               100 + acc))
+                    aborted = true;
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            if (issued_any) {
+                if (lane == 0)
+                    mma_commit_pair(smem_addr(&ctl.drain));
+                __syncwarp();
+                warp_wait_drain(smem_addr(&ctl.drain), 0, a.timeout_ns);
+            }
+        }
+    } else {
+        // ------------------------------ epilogue ------------------------------
+        const int q = warp & 3;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        __nv_bfloat16 *dout = static_cast<__nv_bfloat16 *>(a.d);
+        for (int u = cid; u < total; u += ncl) {
+            int m0, n0;
+            decode(u, m0, n0);
+            if (!warp_wait(smem_addr(&ctl.tfull[acc]), acc_phase, ctl, a.timeout_ns, kRoleEpilogue,
+                           200 + acc)) {
+                aborted = true;
+                break;
+            }
+            tc_fence_after();
+            const int row = m0 + q * 32 + lane;
+            const bool row_ok = row < a.rows_a;
+            __nv_bfloat16 *drow = dout + static_cast<int64_t>(row) * static_cast<int64_t>(a.n);
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(acc * kAccStride);
+            for (int c = 0; c < a.tile_n; c += 32) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c), r);
+                if (row_ok) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int col = n0 + c + 8 * j;
+                        if (col < a.n) {
+                            uint4 v;
+                            v.x = pack_bf16x2(r[8 * j + 0], r[8 * j + 1]);
+                            v.y = pack_bf16x2(r[8 * j + 2], r[8 * j + 3]);
+                            v.z = pack_bf16x2(r[8 * j + 4], r[8 * j + 5]);
+                            v.w = pack_bf16x2(r[8 * j + 6], r[8 * j + 7]);
+                            *reinterpret_cast<uint4 *>(drow + col) = v;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_cluster(mapa_shared(smem_addr(&ctl.tempty[acc]), 0));
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    // Pair exit: neither CTA leaves while the other may still touch its
+    // shared memory or barriers.  On an abort, also give copies still in
+    // flight time to land.
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0)
+        mbar_arrive_cluster(mapa_shared(smem_addr(&ctl.pair_exit), rank ^ 1u));
+    if (warp == 0) {
+        warp_wait_drain(smem_addr(&ctl.pair_exit), 0, 4 * a.timeout_ns);
+        if (ctl.abort) {
+            const uint64_t t0 = globaltimer_ns();
+            while (globaltimer_ns() - t0 < 50000ull) {
+            }
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
+// =====================================================================================
 // k_gemm_swap: SwapAB.  Weights (B) on M, tokens (A) on a runtime N.
 //
 // Work is a list of output tiles (group, token chunk, 128 weight rows), each
@@ -796,6 +1072,20 @@ cudaError_t launch_gemm_mn(const CUtensorMap &tm_a, const CUtensorMap &tm_b, con
     if (e != cudaSuccess)
         return e;
     k_gemm_mn<<<grid, kThreads, smem, stream>>>(tm_a, tm_b, args);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_mn2(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const GemmArgs &args,
+                            int grid, size_t smem, cudaStream_t stream)
+{
+    if (smem < smem_bytes_for(args.stages, args.stage_bytes) || (grid & 1) || args.groups != 1 ||
+        args.masked_m != nullptr)
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_mn2, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess)
+        return e;
+    k_gemm_mn2<<<grid, kThreads, smem, stream>>>(tm_a, tm_b, args);
     return cudaGetLastError();
 }
 

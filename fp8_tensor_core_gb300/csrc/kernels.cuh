@@ -59,6 +59,9 @@ inline size_t smem_bytes_for(int stages, int stage_bytes)
 // 512-column TMEM allocation) is resident per SM.
 cudaError_t launch_gemm_mn(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const GemmArgs &args,
                            int grid, size_t smem, cudaStream_t stream);
+// Dense only: clusters of two CTAs, 256 x tile_n tiles, B box of tile_n/2 rows.
+cudaError_t launch_gemm_mn2(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const GemmArgs &args,
+                            int grid, size_t smem, cudaStream_t stream);
 cudaError_t launch_gemm_swap(const CUtensorMap &tm_w, const CUtensorMap &tm_t,
                              const GemmArgs &args, int grid, size_t smem, cudaStream_t stream);
 

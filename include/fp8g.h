@@ -78,6 +78,9 @@ typedef enum {
  *                     turn instead of an equal stream-K range of K blocks
  *   FP8G_TILE_N(n)    non-swapped kernel: N tile of n (32..256, multiple of 32) */
 #define FP8G_WHOLE_TILES 0x100u
+/*   FP8G_SINGLE_SM_TILES  non-swapped dense kernel: 128-row tiles on one SM
+ *                     each instead of 256-row tiles on a pair of SMs         */
+#define FP8G_SINGLE_SM_TILES 0x200u
 #define FP8G_TILE_N(n) (((((uint32_t)(n)) / 32u) & 15u) << 16)
 /* Debug bits (bench and tests only; never needed for correct results). */
 #define FP8G_DEBUG_ONE_STAGE 0x10u       /* one shared-memory stage: load,

@@ -292,3 +292,39 @@ def test_grouped_stream_k_many_groups():
     mm = [0, 3, 0, 128, 1, 77, 0, 16, 128, 5, 31, 0]
     grouped_case(len(mm), 128, 384, 1024, mm, ON, 0, seed=161)
     grouped_case(len(mm), 128, 384, 1024, mm, ON | fp8g.WHOLE_TILES, 0, seed=162)
+
+
+# ---- SM-pair (cta_group::2) dense kernel --------------------------------------------
+
+@pytest.mark.parametrize("M,N,K", [
+    (256, 256, 128),          # one 256 x 256 tile
+    (257, 224, 384),          # second 256-row tile has one valid row
+    (512, 1000, 640),         # ragged N tile
+    (384, 96, 1280),          # N narrower than half a tile
+    (1024, 2048, 1024),
+])
+def test_pair_kernel_shapes(M, N, K):
+    check_dense(M, N, K, flags=OFF, seed=3 * M + N + K)
+
+
+def test_pair_matches_single_sm_tiles_bitwise_on_exact_data():
+    """Integer-valued data: both kernels are exact, so bit-identical."""
+    rng = np.random.default_rng(8)
+    enc = {-2: 0xC0, -1: 0xB8, 0: 0x00, 1: 0x38, 2: 0x40}
+    M, N, K = 600, 736, 64
+    A = np.vectorize(enc.get)(rng.choice([-2, -1, 0, 1, 2], (M, K))).astype(np.uint8)
+    B = np.vectorize(enc.get)(rng.choice([-2, -1, 0, 1, 2], (N, K))).astype(np.uint8)
+    pair = run_dense(A, B, E4, E4, OFF)
+    single = run_dense(A, B, E4, E4, OFF | fp8g.SINGLE_SM_TILES)
+    ref, _ = oracle.gemm_nt(A, B)
+    assert np.array_equal(pair, ref) and np.array_equal(single, ref)
+
+
+def test_pair_one_stage_and_tile_overrides():
+    A, B = dense_inputs(300, 520, 768, E4, E4, 47)
+    ref, absdot = oracle.gemm_nt(A, B)
+    for flags in (OFF | fp8g.DEBUG_ONE_STAGE, OFF | fp8g.TILE_N(128), OFF | fp8g.TILE_N(256),
+                  OFF | fp8g.TILE_N(160)):
+        got = run_dense(A, B, E4, E4, flags)
+        ok, rep = oracle.check_bf16(got, ref, absdot)
+        assert ok, (hex(flags), rep)
