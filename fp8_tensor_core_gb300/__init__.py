@@ -24,6 +24,12 @@ DEBUG_ONE_STAGE = 0x10
 
 WHOLE_TILES = 0x100   # SwapAB kernel: whole tiles per CTA instead of stream-K ranges
 SINGLE_SM_TILES = 0x200   # dense non-swapped: one SM per 128-row tile instead of SM pairs
+NO_PDL = 0x400            # launch without programmatic dependent launch
+
+
+def STAGES(n: int) -> int:
+    """Flag bits capping the shared-memory pipeline at n stages (1..15)."""
+    return (int(n) & 15) << 20
 
 
 def TILE_N(n: int) -> int:

@@ -125,17 +125,18 @@ bool make_map(CUtensorMap *m, const void *base, int64_t k, int64_t rows, int64_t
     return r == CUDA_SUCCESS;
 }
 
-int stage_budget(const DeviceInfo &d)
-{
-    return d.smem_optin - kCtlBytes - kSmemAlignPad;
-}
-
-int pick_stages(const DeviceInfo &d, int stage_bytes, uint32_t flags)
+// Stages that fit the per-block shared-memory budget beside the control
+// block (FP8G_STAGES(n) caps it; the one-stage debug mode forces 1).
+int pick_stages(const DeviceInfo &d, int stage_bytes, int groups, uint32_t flags)
 {
     if (flags & FP8G_DEBUG_ONE_STAGE)
         return 1;
-    const int s = stage_budget(d) / stage_bytes;
-    return std::max(1, std::min(kMaxStages, s));
+    const int budget = d.smem_optin - ctl_bytes_for(groups) - kSmemAlignPad;
+    int s = std::max(1, std::min(kMaxStages, budget / stage_bytes));
+    const int cap = static_cast<int>((flags >> 20) & 15u);
+    if (cap > 0)
+        s = std::min(s, cap);
+    return s;
 }
 
 // Split-K workspace of the current device, grown on demand (the first call
@@ -261,7 +262,7 @@ int launch(const Problem &p, cudaStream_t stream)
             return FP8G_OK;
         args.tile_n = static_cast<int32_t>(cap);
         args.stage_bytes = static_cast<int32_t>(kTileM * kBlockK + cap * kBlockK);
-        args.stages = pick_stages(info, args.stage_bytes, p.flags);
+        args.stages = pick_stages(info, args.stage_bytes, static_cast<int>(p.G), p.flags);
         args.k_splits = whole_tiles ? 1 : 0;
         if (!whole_tiles) {
             st = ensure_workspace(dev, swap_partials_bytes(grid, static_cast<int>(cap)),
@@ -290,7 +291,7 @@ int launch(const Problem &p, cudaStream_t stream)
             return FP8G_ERR_UNSUPPORTED;
         args.tile_n = tile_n;
         args.stage_bytes = kTileM * kBlockK + (tile_n / 2) * kBlockK;
-        args.stages = pick_stages(info, args.stage_bytes, p.flags);
+        args.stages = pick_stages(info, args.stage_bytes, static_cast<int>(p.G), p.flags);
         const int64_t band = (48ll << 20) / (2 * kTileM * p.K);
         args.raster_band = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(band, m_tiles2)));
         if (!make_map(&tm0, p.A, p.K, p.rows_a, 1, kTileM) ||
@@ -313,7 +314,7 @@ int launch(const Problem &p, cudaStream_t stream)
         return FP8G_ERR_UNSUPPORTED;
     args.tile_n = tile_n;
     args.stage_bytes = kTileM * kBlockK + tile_n * kBlockK;
-    args.stages = pick_stages(info, args.stage_bytes, p.flags);
+    args.stages = pick_stages(info, args.stage_bytes, static_cast<int>(p.G), p.flags);
     // Bands of M tiles whose token rows total about 48 MB stay resident in L2
     // while the weight tiles stream past them.
     const int64_t band = (48ll << 20) / (kTileM * p.K);

@@ -65,10 +65,10 @@ struct alignas(16) SmemCtl {
     volatile int32_t abort;
     int32_t units_total;
     int32_t pad_;
-    int32_t group_prefix[kMaxGroups + 1];  // work units before group g
-    int32_t group_m[kMaxGroups];           // valid token rows of group g (clamped)
+    int32_t *group_prefix;   // [groups + 1] work units before group g (after this struct)
+    int32_t *group_m;        // [groups] valid token rows of group g, clamped
 };
-static_assert(sizeof(SmemCtl) <= kCtlBytes, "control block too large");
+static_assert(sizeof(SmemCtl) <= kCtlFixedBytes, "control block too large");
 
 // Warp-uniform bounded wait on an mbarrier phase.  Returns false when the
 // block is aborting (another role timed out) or this wait ran out.
@@ -186,6 +186,9 @@ __device__ __forceinline__ Smem carve(uint8_t *raw, const GemmArgs &a)
     Smem s;
     s.stages = raw + pad;
     s.ctl = reinterpret_cast<SmemCtl *>(s.stages + static_cast<size_t>(a.stages) * a.stage_bytes);
+    int32_t *tables = reinterpret_cast<int32_t *>(reinterpret_cast<uint8_t *>(s.ctl) + kCtlFixedBytes);
+    s.ctl->group_prefix = tables;
+    s.ctl->group_m = tables + a.groups + 1;
     return s;
 }
 
@@ -273,8 +276,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0)
         init_barriers(ctl, a.stages);
-    if (warp == 0)
+    if (warp == 0) {
+        grid_dep_wait();   // inputs may come from the previous launch in the stream
         build_group_table(ctl, a, [&](int m) { return ceil_div(m, kTileM) * n_tiles; });
+    }
     if (warp == 1) {
         tmem_alloc(smem_addr(&ctl.tmem_base), kTmemCols);
         tmem_relinquish();
@@ -282,6 +287,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    grid_dep_wait();
+    if (threadIdx.x == 0)
+        grid_dep_launch_dependents();
     const uint32_t tmem_base = ctl.tmem_base;
     const int total = ctl.units_total;
 
@@ -503,6 +511,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    grid_dep_wait();   // inputs may come from the previous launch in the stream
+    if (threadIdx.x == 0)
+        grid_dep_launch_dependents();
     const uint32_t tmem_base = ctl.tmem_base;
 
     // Tile u -> first row of this CTA's half, first column of the tile.
@@ -763,8 +774,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0)
         init_barriers(ctl, a.stages);
-    if (warp == 0)
+    if (warp == 0) {
+        grid_dep_wait();   // inputs may come from the previous launch in the stream
         build_group_table(ctl, a, [&](int m) { return ceil_div(m, cap) * n_tiles; });
+    }
     if (warp == 1) {
         tmem_alloc(smem_addr(&ctl.tmem_base), kTmemCols);
         tmem_relinquish();
@@ -772,6 +785,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    grid_dep_wait();
+    if (threadIdx.x == 0)
+        grid_dep_launch_dependents();
     const uint32_t tmem_base = ctl.tmem_base;
     const int total_tiles = ctl.units_total;
     const long long T = static_cast<long long>(total_tiles) * num_kb;
@@ -1062,44 +1078,64 @@ __global__ void __launch_bounds__(kThreads, 1)
 // =====================================================================================
 // Launchers
 // =====================================================================================
+// Launch with programmatic stream serialisation (unless FP8G_NO_PDL): the
+// kernel may start while the previous launch in the stream finishes; it
+// waits (griddepcontrol.wait) before touching global memory.
+template <typename Kernel>
+static cudaError_t launch_pdl(Kernel kernel, int grid, size_t smem, cudaStream_t stream,
+                              const GemmArgs &args, const CUtensorMap &m0, const CUtensorMap &m1)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = (args.flags & FP8G_NO_PDL) ? 0 : 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, m0, m1, args);
+    if (e != cudaSuccess)
+        return e;
+    return cudaGetLastError();
+}
+
 cudaError_t launch_gemm_mn(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const GemmArgs &args,
                            int grid, size_t smem, cudaStream_t stream)
 {
-    if (smem < smem_bytes_for(args.stages, args.stage_bytes))
+    if (smem < smem_bytes_for(args.stages, args.stage_bytes, args.groups))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_gemm_mn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
-    k_gemm_mn<<<grid, kThreads, smem, stream>>>(tm_a, tm_b, args);
-    return cudaGetLastError();
+    return launch_pdl(k_gemm_mn, grid, smem, stream, args, tm_a, tm_b);
 }
 
 cudaError_t launch_gemm_mn2(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const GemmArgs &args,
                             int grid, size_t smem, cudaStream_t stream)
 {
-    if (smem < smem_bytes_for(args.stages, args.stage_bytes) || (grid & 1) || args.groups != 1 ||
+    if (smem < smem_bytes_for(args.stages, args.stage_bytes, args.groups) || (grid & 1) || args.groups != 1 ||
         args.masked_m != nullptr)
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_gemm_mn2, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
-    k_gemm_mn2<<<grid, kThreads, smem, stream>>>(tm_a, tm_b, args);
-    return cudaGetLastError();
+    return launch_pdl(k_gemm_mn2, grid, smem, stream, args, tm_a, tm_b);
 }
 
 cudaError_t launch_gemm_swap(const CUtensorMap &tm_w, const CUtensorMap &tm_t,
                              const GemmArgs &args, int grid, size_t smem, cudaStream_t stream)
 {
-    if (smem < smem_bytes_for(args.stages, args.stage_bytes))
+    if (smem < smem_bytes_for(args.stages, args.stage_bytes, args.groups))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_gemm_swap, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
-    k_gemm_swap<<<grid, kThreads, smem, stream>>>(tm_w, tm_t, args);
-    return cudaGetLastError();
+    return launch_pdl(k_gemm_swap, grid, smem, stream, args, tm_w, tm_t);
 }
 
 cudaError_t read_and_clear_status(int32_t info[4])

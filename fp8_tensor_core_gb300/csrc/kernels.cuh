@@ -15,8 +15,16 @@ constexpr int kMaxGroups = 1024;
 constexpr int kThreads = 192;        // warp 0 loader, warp 1 MMA issuer, warps 2-5 epilogue
 constexpr int kTmemCols = 512;       // two accumulators of up to 256 columns
 constexpr int kAccStride = 256;
-constexpr int kCtlBytes = 10240;     // barriers, TMEM slot, per-group tables
+constexpr int kCtlFixedBytes = 512;  // barriers, TMEM slot, flags
 constexpr int kSmemAlignPad = 1024;  // dynamic smem base rounded up to 1024 B
+
+// Control block: fixed part plus two int32 tables per group (unit prefix,
+// valid rows), rounded up to 128 bytes.
+inline int ctl_bytes_for(int groups)
+{
+    const int b = kCtlFixedBytes + 4 * (2 * groups + 1);
+    return (b + 127) & ~127;
+}
 
 // Roles recorded in the device status word.
 enum Role : int { kRoleLoader = 0, kRoleMma = 1, kRoleEpilogue = 2, kRoleScheduler = 3 };
@@ -49,12 +57,12 @@ struct GemmArgs {
 };
 
 // Shared-memory footprint of a launch (stages + control block + alignment).
-inline size_t smem_bytes_for(int stages, int stage_bytes)
+inline size_t smem_bytes_for(int stages, int stage_bytes, int groups)
 {
-    return static_cast<size_t>(stages) * stage_bytes + kCtlBytes + kSmemAlignPad;
+    return static_cast<size_t>(stages) * stage_bytes + ctl_bytes_for(groups) + kSmemAlignPad;
 }
 
-// `smem` must be at least smem_bytes_for(args.stages, args.stage_bytes); the
+// `smem` must be at least smem_bytes_for(stages, stage_bytes, groups); the
 // host passes the whole per-block budget so that exactly one CTA (and one
 // 512-column TMEM allocation) is resident per SM.
 cudaError_t launch_gemm_mn(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const GemmArgs &args,

@@ -171,7 +171,7 @@ extern "C" int fp8_gemm_nt_noalloc(const void *A, const void *B, void *D, int64_
     args.d = D;
     args.tile_n = static_cast<int32_t>(cap);
     args.stage_bytes = static_cast<int32_t>(kTileM * kBlockK + cap * kBlockK);
-    const int budget = smem - kCtlBytes - kSmemAlignPad;
+    const int budget = smem - ctl_bytes_for(1) - kSmemAlignPad;
     args.stages = std::max(1, std::min(kMaxStages, budget / args.stage_bytes));
     args.k_splits = 0;                                // stream-K, as fp8_gemm_nt's SwapAB path
     args.raster_band = 1;

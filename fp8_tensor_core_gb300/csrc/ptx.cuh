@@ -191,6 +191,21 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
                  : "memory");
 }
 
+// ---- programmatic dependent launch --------------------------------------------------
+
+// Wait until every grid this launch depends on has completed and its memory
+// is visible (a no-op without such a dependency).
+__device__ __forceinline__ void grid_dep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Let the next launch in the stream be scheduled while this grid finishes.
+__device__ __forceinline__ void grid_dep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- CTA pairs (cluster of 2, tcgen05 cta_group::2) ----------------------------------
 
 __device__ __forceinline__ uint32_t cluster_ctarank()

@@ -81,6 +81,13 @@ typedef enum {
 /*   FP8G_SINGLE_SM_TILES  non-swapped dense kernel: 128-row tiles on one SM
  *                     each instead of 256-row tiles on a pair of SMs         */
 #define FP8G_SINGLE_SM_TILES 0x200u
+/*   FP8G_NO_PDL       launch without programmatic dependent launch (by
+ *                     default a launch may begin its set-up while the
+ *                     previous launch in the stream finishes; it waits for
+ *                     that launch before touching global memory)           */
+#define FP8G_NO_PDL 0x400u
+/*   FP8G_STAGES(n)    at most n shared-memory pipeline stages (1..15)       */
+#define FP8G_STAGES(n) ((((uint32_t)(n)) & 15u) << 20)
 #define FP8G_TILE_N(n) (((((uint32_t)(n)) / 32u) & 15u) << 16)
 /* Debug bits (bench and tests only; never needed for correct results). */
 #define FP8G_DEBUG_ONE_STAGE 0x10u       /* one shared-memory stage: load,
