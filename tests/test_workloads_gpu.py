@@ -1,0 +1,107 @@
+"""Parity at the benchmark workloads' full sizes, with the bench's own input
+recipes and launch flags: every element where the oracle finishes in
+seconds (4096^3, the masked MoE-decode workload, every small-M case), and
+for the M=8192 projections whole sampled rows plus random elements, corners
+and the ragged last tile."""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import __graft_entry__  # noqa: F401
+import bench
+import fp8_tensor_core_gb300 as fp8g
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def device():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from fp8_tensor_core_gb300 import build as cuda_build
+    cuda_build.build()
+    torch.cuda.set_device(0)
+    fp8g.fp8g_get_device_status()
+    yield
+
+
+def bits(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def run_dense_workload(w):
+    inp = bench.host_inputs(w)
+    A = torch.from_numpy(inp["A"]).cuda()
+    B = torch.from_numpy(inp["B"]).cuda()
+    D = fp8g.fp8_gemm_nt(A, B, a_dtype=w.fa, b_dtype=w.fb, flags=w.flags)
+    torch.cuda.synchronize()
+    st = fp8g.fp8g_get_device_status()
+    assert st[0] == fp8g.OK, st
+    return inp, bits(D)
+
+
+def test_dense4096_every_element():
+    w = bench.make_workload("dense4096")
+    inp, got = run_dense_workload(w)
+    ref, absdot = oracle.gemm_nt(inp["A"], inp["B"], w.fa, w.fb)
+    ok, rep = oracle.check_bf16(got, ref, absdot)
+    assert ok, rep
+
+
+PROJ = ["proj:7168:2048", "proj:4096:7168", "proj:18432:7168", "proj:7168:18432"]
+
+
+@pytest.mark.parametrize("name", PROJ + [p + ":e5m2" for p in PROJ])
+def test_projection_sampled(name):
+    w = bench.make_workload(name)
+    inp, got = run_dense_workload(w)
+    M, N = w.M, w.N
+    rng = np.random.default_rng(zlib.crc32(name.encode()))
+    rows = np.unique(np.concatenate([[0, 255, 256, M - 1], rng.integers(0, M, 4)]))
+    ms = np.repeat(rows, N)
+    ns = np.tile(np.arange(N), rows.size)
+    rm = rng.integers(0, M, 4096)
+    rn = rng.integers(0, N, 4096)
+    corners_m = np.array([0, 0, M - 1, M - 1])
+    corners_n = np.array([0, N - 1, 0, N - 1])
+    ms = np.concatenate([ms, rm, corners_m])
+    ns = np.concatenate([ns, rn, corners_n])
+    ref, absdot, _ = oracle.gemm_nt_entries(inp["A"], inp["B"], ms, ns, w.fa, w.fb)
+    ok, rep = oracle.check_bf16(got[ms, ns], ref, absdot)
+    assert ok, rep
+
+
+def test_masked_moe_decode_every_valid_row_and_untouched_padding():
+    w = bench.make_workload("masked")
+    inp = bench.host_inputs(w)
+    mm = inp["masked_m"]
+    D0 = np.full((w.G, w.M_max, w.N), 0x7FC3, np.uint16)      # NaN canaries everywhere
+    Dt = torch.from_numpy(D0.view(np.int16)).cuda().view(torch.bfloat16)
+    fp8g.fp8_gemm_grouped_masked(torch.from_numpy(inp["A"]).cuda(), torch.from_numpy(inp["B"]).cuda(),
+                                 torch.from_numpy(mm).cuda(), D=Dt, max_m_hint=w.hint,
+                                 a_dtype=w.fa, b_dtype=w.fb, flags=w.flags)
+    torch.cuda.synchronize()
+    st = fp8g.fp8g_get_device_status()
+    assert st[0] == fp8g.OK, st
+    got = bits(Dt)
+    ref, absdot = oracle.gemm_grouped_masked(inp["A"], inp["B"], mm, D0, w.fa, w.fb)
+    for g in range(w.G):
+        m = int(mm[g])
+        ok, rep = oracle.check_bf16(got[g, :m], ref[g, :m], absdot[g, :m])
+        assert ok, (g, rep)
+        assert np.array_equal(got[g, m:], D0[g, m:]), "padding rows of group %d written" % g
+
+
+SMALLM = ["smallm:%d:%s:%s" % (m, nk, mode) for nk in ("24576:1536", "7168:16384")
+          for m in (1, 8, 16, 32, 64) for mode in ("swap", "noswap")]
+
+
+@pytest.mark.parametrize("name", SMALLM)
+def test_small_m_every_element(name):
+    w = bench.make_workload(name)
+    inp, got = run_dense_workload(w)
+    ref, absdot = oracle.gemm_nt(inp["A"], inp["B"], w.fa, w.fb)
+    ok, rep = oracle.check_bf16(got, ref, absdot)
+    assert ok, rep
