@@ -91,11 +91,13 @@ def make_workload(name: str, rank: int = 0) -> Workload:
         # smallm:M:N:K[:swap|noswap]
         parts = name.split(":")
         M, N, K = int(parts[1]), int(parts[2]), int(parts[3])
-        mode = parts[4] if len(parts) > 4 else "swap"
+        mode = parts[4] if len(parts) > 4 else "auto"
+        label = {"swap": "SwapAB", "noswap": "non-swapped", "auto": "library's choice"}[mode]
         return Workload(name, "dense", "small-M weight-streaming GEMM M=%d N=%d K=%d, E4M3 N(0,1), %s"
-                        % (M, N, K, "SwapAB" if mode == "swap" else "non-swapped"),
+                        % (M, N, K, label),
                         M=M, N=N, K=K, fa=synth.E4M3, fb=synth.E4M3, dist="normal", std=1.0,
-                        seed=synth.seed_for(4, rank), bound="hbm", flags=1 if mode == "swap" else 2)
+                        seed=synth.seed_for(4, rank), bound="hbm",
+                        flags={"swap": 1, "noswap": 2, "auto": 0}[mode])
     raise SystemExit("unknown workload %r" % name)
 
 
@@ -490,7 +492,8 @@ def run_ours(args, w: Workload):
         unit = "GB/s"
         basis = "%s HBM copy bandwidth" % peak_src
     traffic = profiled_traffic(w.name)
-    kernel_name = "k_gemm_swap" if (w.flags & 3) == 1 or (w.kind == "masked") else "k_gemm_mn"
+    kernel_name = "k_gemm_swap" if (w.flags & 3) == 1 or (w.kind == "masked") else \
+        ("k_gemm_mn2" if w.kind == "dense" and w.M > 128 and not (w.flags & 0x200) else "k_gemm_mn/k_gemm_swap (auto)")
     roof = {"bound": w.bound, "achieved": achieved, "peak": peak, "unit": unit,
             "frac": achieved / peak, "traffic": traffic, "kernel": kernel_name,
             "peak_basis": basis, "algorithmic_flop": flops, "algorithmic_bytes": algo_bytes,

@@ -206,6 +206,69 @@ int pick_tile_n(int64_t m_tiles_total, int64_t N, int sms)
     return best;
 }
 
+// Pair-kernel plan: N tile and work split, from a cost model in units of
+// "one K block of a 256-wide tile".  Narrower tiles move more operand bytes
+// per multiply (measured: 224 wide ~7 %, 192 wide ~18 % slower per K block);
+// whole tiles pay for the last partial wave of pairs.  Stream-K for the last
+// wave is only used when FP8G_STREAM_K asks for it: reducing 256-wide FP32
+// partial tiles (128 KB per CTA per contributor) is latency-bound and cost
+// more than the wave it saves on every shape measured.
+struct PairPlan {
+    int tile_n;
+    bool stream_k;
+};
+
+PairPlan plan_pair(int64_t m_tiles2, int64_t N, int num_kb, int pairs, uint32_t flags)
+{
+    static const int cands[] = {256, 224, 192, 160, 128};
+    static const double cost_per_kb[] = {1.0, 1.07, 1.18, 1.30, 1.45};
+    PairPlan best{256, false};
+    double best_cost = 1e300;
+    const int tn_override = static_cast<int>((flags >> 16) & 15u);
+    for (int i = 0; i < 5; ++i) {
+        const int tn = cands[i];
+        if (tn_override >= 1 && tn_override <= 8 && tn != 32 * tn_override)
+            continue;
+        const int64_t units = m_tiles2 * cdiv(N, tn);
+        const double width = static_cast<double>(tn) / 256.0;
+        const double dp = static_cast<double>(cdiv(units, pairs)) * num_kb * cost_per_kb[i] * width;
+        if (dp < best_cost - 1e-9) {
+            best_cost = dp;
+            best = {tn, false};
+        }
+        if ((flags & FP8G_STREAM_K) && units % pairs != 0) {
+            // complete waves of whole tiles, then the last wave's tiles split evenly
+            const double sk = (static_cast<double>(units / pairs) * num_kb +
+                               static_cast<double>(units % pairs) * num_kb / pairs + 3.0) *
+                              cost_per_kb[i] * width;
+            if (sk < best_cost - 1e-9) {
+                best_cost = sk;
+                best = {tn, true};
+            }
+        }
+    }
+    if (tn_override >= 1 && tn_override <= 8 && best.tile_n != 32 * tn_override)
+        best = {32 * tn_override, false};
+    return best;
+}
+
+// Dense problems with few tokens stream the weights once either way.  SwapAB
+// with stream-K keeps every SM streaming but pays a partial-tile reduction;
+// 128-row token tiles need no reduction but only one CTA per N tile, and a
+// single SM streams at most ~55 GB/s.  Estimated times (measured constants on
+// GB300: 6.7 TB/s HBM, ~5 us and ~8 us fixed costs) pick the faster.
+bool swap_beats_token_tiles(int64_t M, int64_t N, int64_t K, int sms)
+{
+    const double bytes = static_cast<double>(N) * K + static_cast<double>(M) * K + 2.0 * M * N;
+    const double hbm = 6.7e12, per_sm = 55e9;
+    const int tn = pick_tile_n(1, N, sms);
+    const int64_t tiles = cdiv(N, tn);
+    const double per_cta = static_cast<double>(tn) * K;
+    const double t_tiles = std::max(bytes / hbm, per_cta * static_cast<double>(cdiv(tiles, sms)) / per_sm) + 5e-6;
+    const double t_swap = bytes / hbm + 8e-6;
+    return t_swap < t_tiles;
+}
+
 struct Problem {
     const void *A, *B;
     void *D;
@@ -227,7 +290,9 @@ int launch(const Problem &p, cudaStream_t stream)
     const uint32_t mode = p.flags & FP8G_SWAP_MASK;
     if (mode == 3u)
         return FP8G_ERR_INVALID_ARG;
-    const bool swap = mode == FP8G_SWAP_ON || (mode == FP8G_SWAP_AUTO && p.token_hint <= kSwapAutoMaxTokens);
+    bool swap = mode == FP8G_SWAP_ON || (mode == FP8G_SWAP_AUTO && p.token_hint <= kSwapAutoMaxTokens);
+    if (swap && mode == FP8G_SWAP_AUTO && !p.masked_m)
+        swap = swap_beats_token_tiles(p.rows_a, p.N, p.K, info.sms);
     const int num_kb = static_cast<int>(cdiv(p.K, kBlockK));
 
     GemmArgs args;
@@ -282,14 +347,13 @@ int launch(const Problem &p, cudaStream_t stream)
     if (!p.masked_m && p.G == 1 && p.rows_a > kTileM && !(p.flags & FP8G_SINGLE_SM_TILES)) {
         const int64_t m_tiles2 = cdiv(p.rows_a, 2 * kTileM);
         const int pairs = info.sms / 2;
-        int tile_n = pick_tile_n(m_tiles2, p.N, pairs);
-        const int tn_override = static_cast<int>((p.flags >> 16) & 15u);
-        if (tn_override >= 1 && tn_override <= 8)
-            tile_n = 32 * tn_override;
+        const PairPlan plan = plan_pair(m_tiles2, p.N, num_kb, pairs, p.flags);
+        const int tile_n = plan.tile_n;
         const int64_t units = m_tiles2 * cdiv(p.N, tile_n);
-        if (units > kMaxDim)
+        if (units > kMaxDim || units * num_kb > (int64_t(1) << 53))
             return FP8G_ERR_UNSUPPORTED;
         args.tile_n = tile_n;
+        args.k_splits = plan.stream_k ? 0 : 1;
         args.stage_bytes = kTileM * kBlockK + (tile_n / 2) * kBlockK;
         args.stages = pick_stages(info, args.stage_bytes, static_cast<int>(p.G), p.flags);
         const int64_t band = (48ll << 20) / (2 * kTileM * p.K);
@@ -297,7 +361,16 @@ int launch(const Problem &p, cudaStream_t stream)
         if (!make_map(&tm0, p.A, p.K, p.rows_a, 1, kTileM) ||
             !make_map(&tm1, p.B, p.K, p.N, 1, static_cast<uint32_t>(tile_n / 2)))
             return FP8G_ERR_CUDA;
-        const int grid = 2 * static_cast<int>(std::min<int64_t>(units, pairs));
+        const int grid = 2 * static_cast<int>(std::min<int64_t>(plan.stream_k ? units * num_kb : units, pairs));
+        // (stream-K implies units is not a multiple of the pairs, so every
+        // pair of the grid exists for the remainder's partition)
+        if (plan.stream_k) {
+            st = ensure_workspace(dev, static_cast<size_t>(grid) * 2 * kTileM * tile_n * sizeof(float),
+                                  static_cast<size_t>(units) * 8 * sizeof(int32_t), &args.workspace,
+                                  &args.counters);
+            if (st != FP8G_OK)
+                return st;
+        }
         return launch_gemm_mn2(tm0, tm1, args, grid, static_cast<size_t>(info.smem_optin), stream) ==
                        cudaSuccess
                    ? FP8G_OK

@@ -455,18 +455,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 // =====================================================================================
 // k_gemm_mn2: dense, tokens on M, two SMs per tile (tcgen05 cta_group::2).
 //
-// A cluster of two CTAs computes a 256 x tile_n output tile.  Each CTA loads
+// A cluster of two CTAs computes 256 x tile_n output tiles.  Each CTA loads
 // its own 128 token rows and half of the tile's weight rows into its shared
 // memory; the even CTA issues one 256-row MMA that reads A from both CTAs and
 // B from both halves, so each weight byte is read from shared memory once
 // for two SMs' worth of tensor-core work.  Each CTA's TMEM holds its own 128
 // output rows and its own epilogue writes them.
 //
+// Work split: whole tiles round-robin over the pairs (so concurrent pairs
+// work on neighbouring tiles and share operands in L2).  With k_splits != 1
+// only the complete waves go that way; the tiles of the last, partial wave
+// are split stream-K: their K blocks are laid end to end and every pair
+// takes an equal contiguous range.  A partial segment publishes FP32
+// partials (each CTA its own 128 rows) and the contributor completing a tile
+// sums them in K order and writes BF16.
+//
 // Barriers: full[s] lives in the even CTA (both CTAs' copies complete on it,
 // the even CTA's producer posts the byte count for both); empty[s] and
 // tfull[b] receive multicast commits in both CTAs; tempty[b] (even CTA)
 // counts the four epilogue warps of both CTAs.
 // =====================================================================================
+struct PairSeg {
+    int tile, m0, n0, kb0, kb1;
+    int kind;   // 0: first segment of the pair's range, 1: a later one
+};
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     k_gemm_mn2(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                const GemmArgs a)
@@ -482,10 +495,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int n_tiles = ceil_div(a.n, a.tile_n);
     const int m_tiles = ceil_div(a.rows_a, 2 * kTileM);
     const int total = m_tiles * n_tiles;
+    const int num_kb = a.num_kb;
+    const bool stream_k = a.k_splits != 1;
     const uint32_t a_bytes = kTileM * kBlockK;                          // own 128 token rows
     const uint32_t tx_pair = 2u * (a_bytes + static_cast<uint32_t>(half_n) * kBlockK);
     const int cid = blockIdx.x >> 1;
     const int ncl = gridDim.x >> 1;
+    // Whole-tile waves, then the stream-K remainder [sk0, sk0 + T).
+    const int dp_tiles = stream_k ? (total / ncl) * ncl : total;
+    const long long sk0 = static_cast<long long>(dp_tiles) * num_kb;
+    const long long T = static_cast<long long>(total - dp_tiles) * num_kb;
+    const long long P = T < static_cast<long long>(ncl) ? T : static_cast<long long>(ncl);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; ++s) {
@@ -516,15 +536,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         grid_dep_launch_dependents();
     const uint32_t tmem_base = ctl.tmem_base;
 
-    // Tile u -> first row of this CTA's half, first column of the tile.
-    auto decode = [&](int u, int &m0, int &n0) {
+    // Only called when T > 0 (a stream-K segment exists).
+    auto range_begin = [&](long long c) { return sk0 + c * T / P; };
+    auto pair_of = [&](long long x) { return static_cast<int>(((x - sk0 + 1) * P - 1) / T); };
+    struct Walker {
+        long long pos, end;
+        int u;
+        bool first;
+    };
+    auto make_walker = [&]() {
+        Walker w;
+        w.u = cid;
+        w.first = true;
+        if (T > 0 && cid < P) {
+            w.pos = range_begin(cid);
+            w.end = range_begin(static_cast<long long>(cid) + 1);
+        } else {
+            w.pos = w.end = 0;
+        }
+        return w;
+    };
+    // Next segment: tile (rasterised in bands of raster_band 256-row tiles,
+    // M fastest), this CTA's first row and the tile's first column.
+    auto next_seg = [&](Walker &w, PairSeg &x) {
+        int u;
+        if (w.u < dp_tiles) {
+            u = w.u;
+            x.kb0 = 0;
+            x.kb1 = num_kb;
+            x.kind = 0;
+            w.u += ncl;
+        } else {
+            if (w.pos >= w.end)
+                return false;
+            u = static_cast<int>(w.pos / num_kb);
+            x.kb0 = static_cast<int>(w.pos - static_cast<long long>(u) * num_kb);
+            const long long left = w.end - w.pos;
+            x.kb1 = left < num_kb - x.kb0 ? x.kb0 + static_cast<int>(left) : num_kb;
+            w.pos += x.kb1 - x.kb0;
+            x.kind = w.first ? 0 : 1;
+            w.first = false;
+        }
+        x.tile = u;
         const int band_units = a.raster_band * n_tiles;
         const int band = u / band_units;
         const int in_band = u - band * band_units;
         const int rows_left = m_tiles - band * a.raster_band;
         const int gm = rows_left < a.raster_band ? rows_left : a.raster_band;
-        m0 = (band * a.raster_band + in_band % gm) * (2 * kTileM) + static_cast<int>(rank) * kTileM;
-        n0 = (in_band / gm) * a.tile_n;
+        x.m0 = (band * a.raster_band + in_band % gm) * (2 * kTileM) + static_cast<int>(rank) * kTileM;
+        x.n0 = (in_band / gm) * a.tile_n;
+        return true;
     };
 
     bool aborted = false;
@@ -538,10 +599,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t phase = 0;
         long long issued = 0;
         const bool drop = (a.flags & FP8G_DEBUG_DROP_FIRST_LOAD) && blockIdx.x == 0;
-        for (int u = cid; u < total && !aborted; u += ncl) {
-            int m0, n0;
-            decode(u, m0, n0);
-            for (int kb = 0; kb < a.num_kb; ++kb) {
+        Walker wk = make_walker();
+        PairSeg x;
+        while (!aborted && next_seg(wk, x)) {
+            for (int kb = x.kb0; kb < x.kb1; ++kb) {
                 if (!warp_wait(smem_addr(&ctl.empty[stage]), phase ^ 1u, ctl, a.timeout_ns,
                                kRoleLoader, stage)) {
                     aborted = true;
@@ -552,9 +613,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (leader)
                         mbar_arrive_expect_tx(smem_addr(&ctl.full[stage]), tx_pair);
                     const uint32_t fb = mapa_shared(smem_addr(&ctl.full[stage]), 0);
-                    tma_load_3d_pair(smem_addr(sa), &tm_a, fb, kb * kBlockK, m0, 0);
+                    tma_load_3d_pair(smem_addr(sa), &tm_a, fb, kb * kBlockK, x.m0, 0);
                     tma_load_3d_pair(smem_addr(sa + a_bytes), &tm_b, fb, kb * kBlockK,
-                                     n0 + static_cast<int>(rank) * half_n, 0);
+                                     x.n0 + static_cast<int>(rank) * half_n, 0);
                 }
                 __syncwarp();
                 ++issued;
@@ -599,7 +660,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool issued_any = false;
-            for (int u = cid; u < total && !aborted; u += ncl) {
+            Walker wk = make_walker();
+            PairSeg x;
+            while (!aborted && next_seg(wk, x)) {
                 if (!warp_wait(smem_addr(&ctl.tempty[acc]), acc_phase ^ 1u, ctl, a.timeout_ns, kRoleMma,
                                100 + acc)) {
                     aborted = true;
@@ -607,7 +670,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccStride);
-                for (int kb = 0; kb < a.num_kb; ++kb) {
+                for (int kb = x.kb0; kb < x.kb1; ++kb) {
                     if (!warp_wait(smem_addr(&ctl.full[stage]), phase, ctl, a.timeout_ns, kRoleMma,
                                    stage)) {
                         aborted = true;
@@ -621,7 +684,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int k = 0; k < kBlockK / 32; ++k)
                             mma_f8f6f4_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc,
-                                            (kb | k) != 0 ? 1u : 0u);
+                                            (kb != x.kb0 || k != 0) ? 1u : 0u);
                         mma_commit_pair_mc(smem_addr(&ctl.empty[stage]), 0x3);
                     }
                     __syncwarp();
@@ -662,38 +725,119 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------ epilogue ------------------------------
         const int q = warp & 3;
+        const int row = q * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
         __nv_bfloat16 *dout = static_cast<__nv_bfloat16 *>(a.d);
-        for (int u = cid; u < total; u += ncl) {
-            int m0, n0;
-            decode(u, m0, n0);
+        // Stream-K partial tiles: slot (CTA, kind) of [tile_n/4 column groups]
+        // [128 rows][4 columns] FP32; a warp access covers 512 contiguous bytes.
+        const int64_t part4 = kTileM * static_cast<int64_t>(a.tile_n) / 4;
+        float4 *slots = reinterpret_cast<float4 *>(a.workspace);
+        Walker wk = make_walker();
+        PairSeg x;
+        while (next_seg(wk, x)) {
             if (!warp_wait(smem_addr(&ctl.tfull[acc]), acc_phase, ctl, a.timeout_ns, kRoleEpilogue,
                            200 + acc)) {
                 aborted = true;
                 break;
             }
             tc_fence_after();
-            const int row = m0 + q * 32 + lane;
-            const bool row_ok = row < a.rows_a;
-            __nv_bfloat16 *drow = dout + static_cast<int64_t>(row) * static_cast<int64_t>(a.n);
+            const int grow = x.m0 + row;
+            const bool row_ok = grow < a.rows_a;
+            __nv_bfloat16 *drow = dout + static_cast<int64_t>(grow) * static_cast<int64_t>(a.n);
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * kAccStride);
-            for (int c = 0; c < a.tile_n; c += 32) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c), r);
-                if (row_ok) {
+            // Eight FP32 values (as bits) -> eight BF16 at column col of this row.
+            auto store8 = [&](int col, const uint32_t *v) {
+                if (row_ok && col < a.n) {
+                    uint4 o;
+                    o.x = pack_bf16x2(v[0], v[1]);
+                    o.y = pack_bf16x2(v[2], v[3]);
+                    o.z = pack_bf16x2(v[4], v[5]);
+                    o.w = pack_bf16x2(v[6], v[7]);
+                    *reinterpret_cast<uint4 *>(drow + col) = o;
+                }
+            };
+            if (x.kb0 == 0 && x.kb1 == num_kb) {
+                for (int c = 0; c < a.tile_n; c += 32) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c), r);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int col = n0 + c + 8 * j;
-                        if (col < a.n) {
-                            uint4 v;
-                            v.x = pack_bf16x2(r[8 * j + 0], r[8 * j + 1]);
-                            v.y = pack_bf16x2(r[8 * j + 2], r[8 * j + 3]);
-                            v.z = pack_bf16x2(r[8 * j + 4], r[8 * j + 5]);
-                            v.w = pack_bf16x2(r[8 * j + 6], r[8 * j + 7]);
-                            *reinterpret_cast<uint4 *>(drow + col) = v;
+                    for (int j = 0; j < 4; ++j)
+                        store8(x.n0 + c + 8 * j, r + 8 * j);
+                }
+            } else {
+                float4 *mine = slots + (static_cast<int64_t>(blockIdx.x) * 2 + x.kind) * part4;
+                for (int c = 0; c < a.tile_n; c += 32) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c), r);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        mine[(c / 4 + v) * kTileM + row] =
+                            make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                        __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                }
+                __threadfence();
+                __syncwarp();
+                const int64_t cnt = (static_cast<int64_t>(x.tile) * 2 + rank) * 4 + q;
+                int prev = 0;
+                if (lane == 0)
+                    prev = atomicAdd(a.counters + cnt, 1);
+                prev = __shfl_sync(0xffffffffu, prev, 0);
+                const long long t0 = static_cast<long long>(x.tile) * num_kb;
+                const int first = pair_of(t0);
+                const int n_contrib = pair_of(t0 + num_kb - 1) - first + 1;
+                if (prev == n_contrib - 1) {
+                    // Tile complete: sum the contributions in K order, two
+                    // contributors' 32 columns per batch (unconditional loads).
+                    __threadfence();
+                    if (lane == 0)
+                        a.counters[cnt] = 0;   // ready for the next launch
+                    for (int c = 0; c < a.tile_n; c += 32) {
+                        float acc_v[32];
+                        for (int p0 = 0; p0 < n_contrib; p0 += 2) {
+                            float4 buf[2][8];
+#pragma unroll
+                            for (int i = 0; i < 2; ++i) {
+                                const int ci = (p0 + i < n_contrib) ? p0 + i : 0;
+                                const int pr = first + ci;
+                                const int kind =
+                                    (range_begin(pr) / num_kb == static_cast<long long>(x.tile)) ? 0 : 1;
+                                const float4 *src = slots +
+                                                    ((static_cast<int64_t>(2 * pr) + rank) * 2 + kind) * part4 +
+                                                    (c / 4) * kTileM + row;
+#pragma unroll
+                                for (int v = 0; v < 8; ++v)
+                                    buf[i][v] = __ldcg(src + v * kTileM);
+                            }
+#pragma unroll
+                            for (int i = 0; i < 2; ++i) {
+                                if (p0 + i >= n_contrib)
+                                    break;
+#pragma unroll
+                                for (int v = 0; v < 8; ++v) {
+                                    const float4 f = buf[i][v];
+                                    if (p0 + i == 0) {
+                                        acc_v[4 * v] = f.x;
+                                        acc_v[4 * v + 1] = f.y;
+                                        acc_v[4 * v + 2] = f.z;
+                                        acc_v[4 * v + 3] = f.w;
+                                    } else {
+                                        acc_v[4 * v] += f.x;
+                                        acc_v[4 * v + 1] += f.y;
+                                        acc_v[4 * v + 2] += f.z;
+                                        acc_v[4 * v + 3] += f.w;
+                                    }
+                                }
+                            }
                         }
+                        uint32_t bits_v[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            bits_v[j] = __float_as_uint(acc_v[j]);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            store8(x.n0 + c + 8 * j, bits_v + 8 * j);
                     }
                 }
             }

@@ -76,8 +76,12 @@ typedef enum {
  * every value; only speed (and the last bits of rounding) change.
  *   FP8G_WHOLE_TILES  SwapAB kernel: each CTA takes whole output tiles in
  *                     turn instead of an equal stream-K range of K blocks
+ *   FP8G_STREAM_K     SM-pair dense kernel: split the tiles of the last,
+ *                     partial wave stream-K over all pairs (default: whole
+ *                     tiles round-robin)
  *   FP8G_TILE_N(n)    non-swapped kernel: N tile of n (32..256, multiple of 32) */
 #define FP8G_WHOLE_TILES 0x100u
+#define FP8G_STREAM_K 0x800u
 /*   FP8G_SINGLE_SM_TILES  non-swapped dense kernel: 128-row tiles on one SM
  *                     each instead of 256-row tiles on a pair of SMs         */
 #define FP8G_SINGLE_SM_TILES 0x200u

@@ -328,3 +328,22 @@ def test_pair_one_stage_and_tile_overrides():
         got = run_dense(A, B, E4, E4, flags)
         ok, rep = oracle.check_bf16(got, ref, absdot)
         assert ok, (hex(flags), rep)
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (256, 256, 128 * 40),     # one tile, 40 K blocks over 76 pairs: 40 contributors
+    (512, 512, 128 * 3),      # 4 tiles x 3 K blocks < 76 pairs: partition shrinks
+    (1000, 1032, 2000),       # ragged everywhere (K tail of 80 bytes)
+])
+def test_pair_stream_k_partitions(M, N, K):
+    check_dense(M, N, K, flags=OFF | fp8g.STREAM_K, seed=5 * M + N + K)
+
+
+def test_pair_whole_tiles_and_stream_k_agree():
+    A, B = dense_inputs(768, 1280, 1536, E4, E4, 53)
+    ref, absdot = oracle.gemm_nt(A, B)
+    for flags in (OFF, OFF | fp8g.STREAM_K, OFF | fp8g.STREAM_K | fp8g.TILE_N(256),
+                  OFF | fp8g.TILE_N(224)):
+        got = run_dense(A, B, E4, E4, flags)
+        ok, rep = oracle.check_bf16(got, ref, absdot)
+        assert ok, (hex(flags), rep)
