@@ -327,7 +327,27 @@ int launch(const Problem &p, cudaStream_t stream)
             return FP8G_OK;
         args.tile_n = static_cast<int32_t>(cap);
         args.stage_bytes = static_cast<int32_t>(kTileM * kBlockK + cap * kBlockK);
-        args.stages = pick_stages(info, args.stage_bytes, static_cast<int>(p.G), p.flags);
+        // Co-residency: with at most 128 tokens per chunk the accumulators fit
+        // 256 TMEM columns; capping shared memory at half the SM lets the next
+        // launch's CTAs become resident (and finish their set-up) while this
+        // one drains.
+        const bool share_sm = (p.flags & FP8G_SHARE_SM) && cap <= 128;
+        size_t smem_request = static_cast<size_t>(info.smem_optin);
+        if (share_sm) {
+            const int half = info.smem_optin / 2 - 1024;   // leave room for two CTAs' reserved smem
+            const int s_half = (half - ctl_bytes_for(static_cast<int>(p.G)) - kSmemAlignPad) / args.stage_bytes;
+            args.stages = std::max(1, std::min(kMaxStages, s_half));
+            const uint32_t cap_st = (p.flags >> 20) & 15u;
+            if (cap_st > 0)
+                args.stages = std::min<int>(args.stages, static_cast<int>(cap_st));
+            if (p.flags & FP8G_DEBUG_ONE_STAGE)
+                args.stages = 1;
+            args.tmem_cols = 256;
+            smem_request = smem_bytes_for(args.stages, args.stage_bytes, static_cast<int>(p.G));
+        } else {
+            args.stages = pick_stages(info, args.stage_bytes, static_cast<int>(p.G), p.flags);
+            args.tmem_cols = 512;
+        }
         args.k_splits = whole_tiles ? 1 : 0;
         if (!whole_tiles) {
             st = ensure_workspace(dev, swap_partials_bytes(grid, static_cast<int>(cap)),
@@ -337,7 +357,7 @@ int launch(const Problem &p, cudaStream_t stream)
         }
         if (!make_map(&tm0, p.B, p.K, p.N, p.G, kTileM) || !make_map(&tm1, p.A, p.K, p.rows_a, p.G, 16))
             return FP8G_ERR_CUDA;
-        return launch_gemm_swap(tm0, tm1, args, grid, static_cast<size_t>(info.smem_optin), stream) == cudaSuccess
+        return launch_gemm_swap(tm0, tm1, args, grid, smem_request, stream) == cudaSuccess
                    ? FP8G_OK
                    : FP8G_ERR_CUDA;
     }

@@ -913,6 +913,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int num_kb = a.num_kb;
     const bool stream_k = a.k_splits != 1;       // 1 = whole tiles only
     const uint32_t w_bytes = kTileM * kBlockK;   // 16 KB weight box
+    // Accumulators: two of 256 columns, or two of 128 (tile_n <= 128) so
+    // that two CTAs -- this launch's and the next one's -- fit in TMEM.
+    const uint32_t tmem_cols = a.tmem_cols == 256 ? 256u : static_cast<uint32_t>(kTmemCols);
+    const int acc_stride = static_cast<int>(tmem_cols / 2);
     constexpr int kTokBox = 16;                  // token rows per TMA box
     constexpr uint32_t kTokBoxBytes = kTokBox * kBlockK;
 
@@ -923,7 +927,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         build_group_table(ctl, a, [&](int m) { return ceil_div(m, cap) * n_tiles; });
     }
     if (warp == 1) {
-        tmem_alloc(smem_addr(&ctl.tmem_base), kTmemCols);
+        tmem_alloc(smem_addr(&ctl.tmem_base), tmem_cols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -1047,7 +1051,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            100 + acc))
                 break;
             tc_fence_after();
-            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccStride);
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * acc_stride);
             bool ok = true;
             for (int kb = x.kb0; kb < x.kb1; ++kb) {
                 if (!warp_wait(smem_addr(&ctl.full[stage]), phase, ctl, a.timeout_ns, kRoleMma,
@@ -1108,7 +1112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nrow = x.w0 + row;
             const bool n_ok = nrow < a.n;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                   static_cast<uint32_t>(acc * kAccStride);
+                                   static_cast<uint32_t>(acc * acc_stride);
             __nv_bfloat16 *dcol = dout + static_cast<int64_t>(x.g) * a.rows_a * static_cast<int64_t>(a.n) +
                                   nrow;
             const bool whole = x.kb0 == 0 && x.kb1 == num_kb;
@@ -1215,7 +1219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        tmem_dealloc(tmem_base, tmem_cols);
     }
 }
 

@@ -47,6 +47,8 @@ struct GemmArgs {
     int32_t k_splits;          // swap kernel: 1 = whole tiles per unit; otherwise stream-K
                                // (equal k-block ranges per CTA, partial tiles reduced)
     int32_t raster_band;       // mn kernel: M tiles per rasterisation band
+    int32_t tmem_cols;         // swap kernel: 256 (two 128-column accumulators, two CTAs
+                               // may share an SM) or 512 (default)
     uint32_t a_fmt, b_fmt;     // 0 = E4M3, 1 = E5M2 (of A and B as passed by the caller)
     uint32_t flags;            // FP8G_DEBUG_* bits
     uint64_t timeout_ns;       // limit of every barrier wait

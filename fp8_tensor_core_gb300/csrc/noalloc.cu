@@ -174,6 +174,7 @@ extern "C" int fp8_gemm_nt_noalloc(const void *A, const void *B, void *D, int64_
     const int budget = smem - ctl_bytes_for(1) - kSmemAlignPad;
     args.stages = std::max(1, std::min(kMaxStages, budget / args.stage_bytes));
     args.k_splits = 0;                                // stream-K, as fp8_gemm_nt's SwapAB path
+    args.tmem_cols = 512;
     args.raster_band = 1;
     args.a_fmt = static_cast<uint32_t>(a_dtype);
     args.b_fmt = static_cast<uint32_t>(b_dtype);

@@ -92,6 +92,10 @@ typedef enum {
 #define FP8G_NO_PDL 0x400u
 /*   FP8G_STAGES(n)    at most n shared-memory pipeline stages (1..15)       */
 #define FP8G_STAGES(n) ((((uint32_t)(n)) & 15u) << 20)
+/*   FP8G_SHARE_SM     SwapAB kernel with <= 128 tokens per chunk: half the
+ *                     shared memory and TMEM per CTA, so the next launch's
+ *                     CTAs can become resident while this one drains        */
+#define FP8G_SHARE_SM 0x1000u
 #define FP8G_TILE_N(n) (((((uint32_t)(n)) / 32u) & 15u) << 16)
 /* Debug bits (bench and tests only; never needed for correct results). */
 #define FP8G_DEBUG_ONE_STAGE 0x10u       /* one shared-memory stage: load,

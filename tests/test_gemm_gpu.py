@@ -347,3 +347,13 @@ def test_pair_whole_tiles_and_stream_k_agree():
         got = run_dense(A, B, E4, E4, flags)
         ok, rep = oracle.check_bf16(got, ref, absdot)
         assert ok, (hex(flags), rep)
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 2048, 4096), (128, 1024, 1536), (1, 7168, 2048)])
+def test_share_sm_mode_dense(M, N, K):
+    check_dense(M, N, K, flags=ON | fp8g.SHARE_SM, seed=11 * M + N + K)
+
+
+def test_share_sm_mode_grouped():
+    mm = [0, 5, 32, 17, 1, 64]
+    grouped_case(len(mm), 64, 512, 1024, mm, ON | fp8g.SHARE_SM, 32, seed=171)
