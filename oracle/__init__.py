@@ -18,6 +18,9 @@ What it computes, with its sources:
 * ``gemm_grouped_masked`` -- the masked grouped variant: only rows
   m < masked_m[g] of each group are computed or written ("一次“转置”，半张
   算力：DeepSeek SwapAB 漂流史", §3.1 and §3.3, valid_m).
+* ``gemm_nt_scaled`` / ``gemm_grouped_masked_scaled`` -- the same products
+  multiplied back by per-tensor or per-channel FP32 scales before the one
+  rounding (DeepGEMM page §3.1 and §5.2).
 * ``check_bf16`` -- the acceptance rule for a GPU result:
   |gpu - oracle| <= ulp_bf16(oracle) + 1e-6 * sum_k |a_k b_k| per element.
 
@@ -96,6 +99,15 @@ def _load():
         lib.oracle_gemm_grouped_masked.argtypes = [
             _u8p, _u8p, _i32p, _i64, _i64, _i64, _i64, ctypes.c_int,
             ctypes.c_int, _u16p, _f64p, ctypes.c_int]
+        _f32p = ctypes.POINTER(ctypes.c_float)
+        lib.oracle_gemm_nt_scaled.restype = None
+        lib.oracle_gemm_nt_scaled.argtypes = [_u8p, _u8p, _i64, _i64, _i64, ctypes.c_int,
+                                              ctypes.c_int, _f32p, _i64, _f32p, _i64, _u16p,
+                                              _f64p, ctypes.c_int]
+        lib.oracle_gemm_grouped_masked_scaled.restype = None
+        lib.oracle_gemm_grouped_masked_scaled.argtypes = [
+            _u8p, _u8p, _i32p, _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _f32p, _i64,
+            _f32p, _i64, _u16p, _f64p, ctypes.c_int]
         _lib = lib
         return lib
 
@@ -209,6 +221,52 @@ def gemm_grouped_masked(A: np.ndarray, B: np.ndarray, masked_m: np.ndarray,
                                        _ptr(mm, _i32p), G, M_max, N, K, fa, fb,
                                        _ptr(D, _u16p), _ptr(absdot, _f64p),
                                        int(nthreads))
+    return D, absdot
+
+
+def gemm_nt_scaled(A: np.ndarray, B: np.ndarray, scale_a: np.ndarray, scale_b: np.ndarray,
+                   fa: int = E4M3, fb: int = E4M3, nthreads: int = 0):
+    """Scaled dense oracle: D[m,n] = bf16(sa(m) sb(n) sum_k a b) with FP32
+    scales of length 1 (per tensor) or M / N (per row / per column).
+    Returns (D_bf16, absdot_scaled)."""
+    A = np.ascontiguousarray(A, np.uint8)
+    B = np.ascontiguousarray(B, np.uint8)
+    M, K = A.shape
+    N, K2 = B.shape
+    assert K == K2
+    sa = np.ascontiguousarray(scale_a, np.float32).ravel()
+    sb = np.ascontiguousarray(scale_b, np.float32).ravel()
+    assert sa.size in (1, M) and sb.size in (1, N)
+    D = np.empty((M, N), np.uint16)
+    absdot = np.empty((M, N), np.float64)
+    f32p = ctypes.POINTER(ctypes.c_float)
+    _load().oracle_gemm_nt_scaled(_ptr(A, _u8p), _ptr(B, _u8p), M, N, K, fa, fb,
+                                  _ptr(sa, f32p), sa.size, _ptr(sb, f32p), sb.size,
+                                  _ptr(D, _u16p), _ptr(absdot, _f64p), int(nthreads))
+    return D, absdot
+
+
+def gemm_grouped_masked_scaled(A: np.ndarray, B: np.ndarray, masked_m: np.ndarray,
+                               scale_a: np.ndarray, scale_b: np.ndarray, D_init: np.ndarray,
+                               fa: int = E4M3, fb: int = E4M3, nthreads: int = 0):
+    """Scaled masked grouped oracle; scale_a has G or G*M_max entries,
+    scale_b G or G*N.  Rows m >= masked_m[g] keep D_init's bits."""
+    A = np.ascontiguousarray(A, np.uint8)
+    B = np.ascontiguousarray(B, np.uint8)
+    G, M_max, K = A.shape
+    G2, N, K2 = B.shape
+    assert G == G2 and K == K2
+    mm = np.ascontiguousarray(masked_m, np.int32)
+    sa = np.ascontiguousarray(scale_a, np.float32).ravel()
+    sb = np.ascontiguousarray(scale_b, np.float32).ravel()
+    assert sa.size in (G, G * M_max) and sb.size in (G, G * N)
+    D = np.array(D_init, np.uint16, copy=True, order="C")
+    absdot = np.zeros((G, M_max, N), np.float64)
+    f32p = ctypes.POINTER(ctypes.c_float)
+    _load().oracle_gemm_grouped_masked_scaled(_ptr(A, _u8p), _ptr(B, _u8p), _ptr(mm, _i32p), G,
+                                              M_max, N, K, fa, fb, _ptr(sa, f32p), sa.size,
+                                              _ptr(sb, f32p), sb.size, _ptr(D, _u16p),
+                                              _ptr(absdot, _f64p), int(nthreads))
     return D, absdot
 
 

@@ -8,6 +8,8 @@
  *   dense   D[m,n]   = bf16_rne( sum_k dec(A[m,k]) * dec(B[n,k]) )
  *   masked  D[g,m,n] = bf16_rne( sum_k dec(A[g,m,k]) * dec(B[g,n,k]) )
  *                       for m < masked_m[g]; other rows of D untouched.
+ *   scaled  the same with the exact sum multiplied by per-tensor or
+ *           per-channel FP32 scales sa * sb before the one rounding.
  *
  * Sources:
  *  - "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践"
@@ -340,4 +342,67 @@ void oracle_gemm_grouped_masked(const uint8_t *A, const uint8_t *B,
     c.D = D;
     c.absdot = absdot;
     run_rows(grouped_row, &c, G * M_max, nthreads);
+}
+
+/* ---- scaled variants ------------------------------------------------------
+ * "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践" §3.1: the
+ * scale is computed beforehand and multiplied back at the output; §5.2: the
+ * scale may be per tensor or per channel.  Here
+ *     D[m,n] = bf16_rne( sa(m) * sb(n) * sum_k dec(A[m,k]) * dec(B[n,k]) )
+ * with sa(m) = scale_a[0] (sa_len == 1) or scale_a[m] (sa_len == M), and
+ * sb(n) = scale_b[0] or scale_b[n].  The product is formed in double and
+ * rounded once.  absdot (if given) receives |sa(m) sb(n)| * sum_k |a_k b_k|. */
+void oracle_gemm_nt_scaled(const uint8_t *A, const uint8_t *B, int64_t M, int64_t N,
+                           int64_t K, int fa, int fb, const float *scale_a,
+                           int64_t sa_len, const float *scale_b, int64_t sb_len,
+                           uint16_t *D, double *absdot, int nthreads)
+{
+    double *exact = (double *)malloc(sizeof(double) * (size_t)(M * N));
+    double *ad = (double *)malloc(sizeof(double) * (size_t)(M * N));
+    oracle_gemm_nt(A, B, M, N, K, fa, fb, NULL, exact, ad, nthreads);
+    for (int64_t m = 0; m < M; ++m) {
+        double sa = (double)scale_a[sa_len == 1 ? 0 : m];
+        for (int64_t n = 0; n < N; ++n) {
+            double sb = (double)scale_b[sb_len == 1 ? 0 : n];
+            int64_t o = m * N + n;
+            D[o] = oracle_round_bf16(sa * sb * exact[o]);
+            if (absdot)
+                absdot[o] = fabs(sa * sb) * ad[o];
+        }
+    }
+    free(exact);
+    free(ad);
+}
+
+/* Masked grouped, scaled: sa(g,m) = scale_a[g] (sa_len == G) or
+ * scale_a[g*M_max + m] (sa_len == G*M_max); sb(g,n) = scale_b[g] or
+ * scale_b[g*N + n].  Rows m >= masked_m[g] are left untouched. */
+void oracle_gemm_grouped_masked_scaled(const uint8_t *A, const uint8_t *B,
+                                       const int32_t *masked_m, int64_t G,
+                                       int64_t M_max, int64_t N, int64_t K, int fa,
+                                       int fb, const float *scale_a, int64_t sa_len,
+                                       const float *scale_b, int64_t sb_len,
+                                       uint16_t *D, double *absdot, int nthreads)
+{
+    for (int64_t g = 0; g < G; ++g) {
+        int64_t m_g = masked_m[g];
+        if (m_g <= 0)
+            continue;
+        double *exact = (double *)malloc(sizeof(double) * (size_t)(m_g * N));
+        double *ad = (double *)malloc(sizeof(double) * (size_t)(m_g * N));
+        oracle_gemm_nt(A + g * M_max * K, B + g * N * K, m_g, N, K, fa, fb, NULL, exact, ad,
+                       nthreads);
+        for (int64_t m = 0; m < m_g; ++m) {
+            double sa = (double)scale_a[sa_len == G ? g : g * M_max + m];
+            for (int64_t n = 0; n < N; ++n) {
+                double sb = (double)scale_b[sb_len == G ? g : g * N + n];
+                int64_t o = (g * M_max + m) * N + n;
+                D[o] = oracle_round_bf16(sa * sb * exact[m * N + n]);
+                if (absdot)
+                    absdot[o] = fabs(sa * sb) * ad[m * N + n];
+            }
+        }
+        free(exact);
+        free(ad);
+    }
 }

@@ -354,3 +354,69 @@ def test_planted_sign_mistake_is_caught():
     D, _ = oracle.gemm_nt(A, B)
     Dneg, _ = oracle.gemm_nt(A ^ 0x80, B)           # planted: flipped sign bits
     assert not np.array_equal(D, Dneg)
+
+
+# ---- scaled variants --------------------------------------------------------------
+
+def test_scaled_power_of_two_scales_shift_exponents_exactly():
+    """Per-row/per-column scales 2^e multiply the exact sum exactly, so the
+    BF16 result is the unscaled one with its exponent shifted."""
+    A = _rand_codes((24, 96), 201, oracle.E4M3)
+    B = _rand_codes((40, 96), 202, oracle.E4M3)
+    ea = np.random.default_rng(1).integers(-6, 7, 24)
+    eb = np.random.default_rng(2).integers(-6, 7, 40)
+    sa = np.ldexp(1.0, ea).astype(np.float32)
+    sb = np.ldexp(1.0, eb).astype(np.float32)
+    D, absdot = oracle.gemm_nt_scaled(A, B, sa, sb)
+    D0, absdot0 = oracle.gemm_nt(A, B)
+    want = oracle.bf16_bits_to_f64(D0) * np.ldexp(1.0, ea[:, None] + eb[None, :])
+    assert np.array_equal(oracle.bf16_bits_to_f64(D), want)
+    assert np.allclose(absdot, absdot0 * np.ldexp(1.0, ea[:, None] + eb[None, :]), rtol=0, atol=0)
+
+
+def test_scaled_unit_and_per_tensor_scales():
+    A = _rand_codes((16, 64), 203, oracle.E5M2)
+    B = _rand_codes((24, 64), 204, oracle.E4M3)
+    D0, _ = oracle.gemm_nt(A, B, 1, 0)
+    D1, _ = oracle.gemm_nt_scaled(A, B, np.ones(1, np.float32), np.ones(24, np.float32), 1, 0)
+    assert np.array_equal(D0, D1)
+    Dt, _ = oracle.gemm_nt_scaled(A, B, np.array([0.375], np.float32), np.array([-3.0], np.float32), 1, 0)
+    Dr, _ = oracle.gemm_nt_scaled(A, B, np.full(16, 0.375, np.float32), np.full(24, -3.0, np.float32), 1, 0)
+    assert np.array_equal(Dt, Dr)
+
+
+def test_scaled_matches_numpy_reference():
+    """Against numpy float64 products of torch-decoded operands and the
+    scales; BF16 codes within one ulp (numpy's path rounds through float32)."""
+    A = _rand_codes((37, 200), 205, oracle.E4M3)
+    B = _rand_codes((29, 200), 206, oracle.E4M3)
+    rng = np.random.default_rng(3)
+    sa = rng.uniform(0.01, 4.0, 37).astype(np.float32)
+    sb = rng.uniform(-2.0, 2.0, 29).astype(np.float32)
+    D, _ = oracle.gemm_nt_scaled(A, B, sa, sb)
+    ref = (sa.astype(np.float64)[:, None] * sb.astype(np.float64)[None, :]
+           * (torch_decode(A, 0) @ torch_decode(B, 0).T))
+    ref_bits = torch.from_numpy(ref.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    d = np.abs(D.astype(np.int64) - ref_bits.astype(np.int64))
+    assert d.max() <= 1 and np.mean(d == 0) > 0.98
+
+
+def test_grouped_scaled_per_group_and_per_row():
+    G, M_max, N, K = 4, 16, 24, 64
+    A = _rand_codes((G, M_max, K), 207, oracle.E4M3)
+    B = _rand_codes((G, N, K), 208, oracle.E4M3)
+    mm = np.array([3, 0, 16, 9], np.int32)
+    sa_g = np.array([0.5, 2.0, 1.25, -1.0], np.float32)
+    sb_gn = np.random.default_rng(4).uniform(0.5, 2.0, G * N).astype(np.float32)
+    D0 = synth.u16_pattern((G, M_max, N), 209)
+    D, _ = oracle.gemm_grouped_masked_scaled(A, B, mm, sa_g, sb_gn, D0)
+    for g in range(G):
+        m = mm[g]
+        ref, _ = oracle.gemm_nt_scaled(A[g, :m], B[g], sa_g[g:g + 1], sb_gn[g * N:(g + 1) * N])
+        assert np.array_equal(D[g, :m], ref)
+        assert np.array_equal(D[g, m:], D0[g, m:])
+    sa_r = np.random.default_rng(5).uniform(0.5, 2.0, G * M_max).astype(np.float32)
+    D2, _ = oracle.gemm_grouped_masked_scaled(A, B, mm, sa_r, sa_g, D0)
+    g = 2
+    ref, _ = oracle.gemm_nt_scaled(A[g], B[g], sa_r[g * M_max:(g + 1) * M_max], sa_g[g:g + 1])
+    assert np.array_equal(D2[g], ref)
