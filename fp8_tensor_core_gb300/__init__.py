@@ -211,3 +211,70 @@ def fp8_gemm_nt_noalloc(A, B, D, a_dtype=None, b_dtype=None, stream=None):
     if rc != OK:
         raise Fp8gError(rc, "fp8_gemm_nt_noalloc")
     return D
+
+
+def _check_scale(t, name, lengths):
+    import torch
+    if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous() or t.numel() not in lengths:
+        raise ValueError("%s must be a contiguous float32 CUDA tensor with %s entries"
+                         % (name, " or ".join(str(v) for v in sorted(set(lengths)))))
+
+
+def fp8_gemm_nt_scaled(A, B, scale_a, scale_b, D=None, a_dtype=None, b_dtype=None, flags: int = 0,
+                       stream=None):
+    """D[m,n] = bf16(sa(m) * sb(n) * sum_k A[m,k] B[n,k]) with float32 CUDA
+    scales: scale_a of 1 (per tensor) or M (per row) entries, scale_b of 1
+    or N (per output channel)."""
+    import torch
+    _check_operand(A, "A", 2)
+    _check_operand(B, "B", 2)
+    fa, fb = _fp8_code(A, a_dtype), _fp8_code(B, b_dtype)
+    M, K = A.shape
+    N, K2 = B.shape
+    if K != K2:
+        raise ValueError("K mismatch: A has %d, B has %d" % (K, K2))
+    _check_scale(scale_a, "scale_a", (1, M))
+    _check_scale(scale_b, "scale_b", (1, N))
+    if D is None:
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    else:
+        _check_operand(D, "D", 2)
+        if D.dtype != torch.bfloat16 or tuple(D.shape) != (M, N):
+            raise ValueError("D must be a contiguous bf16 [M, N] tensor")
+    with _on_device(A.device):
+        rc = _lib.load().fp8_gemm_nt_scaled(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, fa, fb,
+                                            scale_a.data_ptr(), scale_a.numel(), scale_b.data_ptr(),
+                                            scale_b.numel(), int(flags), _stream_handle(stream))
+    if rc != OK:
+        raise Fp8gError(rc, "fp8_gemm_nt_scaled")
+    return D
+
+
+def fp8_gemm_grouped_masked_scaled(A, B, masked_m, scale_a, scale_b, D=None, max_m_hint: int = 0,
+                                   a_dtype=None, b_dtype=None, flags: int = 0, stream=None):
+    """Masked grouped GEMM times scales: scale_a of G (per group) or G*M_max
+    (per token row) entries, scale_b of G or G*N (per output channel)."""
+    import torch
+    _check_operand(A, "A", 3)
+    _check_operand(B, "B", 3)
+    fa, fb = _fp8_code(A, a_dtype), _fp8_code(B, b_dtype)
+    G, M_max, K = A.shape
+    G2, N, K2 = B.shape
+    if G != G2 or K != K2:
+        raise ValueError("shape mismatch: A %s, B %s" % (tuple(A.shape), tuple(B.shape)))
+    if not masked_m.is_cuda or masked_m.dtype != torch.int32 or tuple(masked_m.shape) != (G,):
+        raise ValueError("masked_m must be a contiguous int32 CUDA tensor of shape [G]")
+    _check_scale(scale_a, "scale_a", (G, G * M_max))
+    _check_scale(scale_b, "scale_b", (G, G * N))
+    if D is None:
+        D = torch.empty((G, M_max, N), dtype=torch.bfloat16, device=A.device)
+    else:
+        _check_operand(D, "D", 3)
+    with _on_device(A.device):
+        rc = _lib.load().fp8_gemm_grouped_masked_scaled(
+            A.data_ptr(), B.data_ptr(), D.data_ptr(), masked_m.data_ptr(), G, M_max, N, K,
+            int(max_m_hint), fa, fb, scale_a.data_ptr(), scale_a.numel(), scale_b.data_ptr(),
+            scale_b.numel(), int(flags), _stream_handle(stream))
+    if rc != OK:
+        raise Fp8gError(rc, "fp8_gemm_grouped_masked_scaled")
+    return D

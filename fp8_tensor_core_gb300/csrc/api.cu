@@ -277,7 +277,30 @@ struct Problem {
     int64_t token_hint;   // expected valid tokens per group (<= rows_a)
     int a_dtype, b_dtype;
     uint32_t flags;
+    const float *scale_a = nullptr;   // see GemmArgs
+    const float *scale_b = nullptr;
+    bool sa_per_row = false, sb_per_col = false;
 };
+
+// Scale arguments: both pointers given (16-byte aligned device memory), each
+// with one entry per group or one per row (A) / column (B) of every group.
+int check_scales(const float *sa, int64_t sa_len, const float *sb, int64_t sb_len, int64_t G,
+                 int64_t rows, int64_t N, Problem &p)
+{
+    if (!sa || !sb)
+        return FP8G_ERR_INVALID_ARG;
+    if (!aligned16(sa) || !aligned16(sb))
+        return FP8G_ERR_MISALIGNED;
+    if (sa_len != G && sa_len != G * rows)
+        return FP8G_ERR_INVALID_ARG;
+    if (sb_len != G && sb_len != G * N)
+        return FP8G_ERR_INVALID_ARG;
+    p.scale_a = sa;
+    p.scale_b = sb;
+    p.sa_per_row = sa_len == G * rows && rows != 1;
+    p.sb_per_col = sb_len == G * N && N != 1;
+    return FP8G_OK;
+}
 
 int launch(const Problem &p, cudaStream_t stream)
 {
@@ -308,6 +331,10 @@ int launch(const Problem &p, cudaStream_t stream)
     args.b_fmt = static_cast<uint32_t>(p.b_dtype);
     args.flags = p.flags;
     args.timeout_ns = g_timeout_ns.load();
+    args.scale_a = p.scale_a;
+    args.scale_b = p.scale_b;
+    args.sa_per_row = p.sa_per_row ? 1 : 0;
+    args.sb_per_col = p.sb_per_col ? 1 : 0;
     args.k_splits = 1;
     args.raster_band = 1;
 
@@ -467,6 +494,58 @@ extern "C" int fp8_gemm_grouped_masked(const void *A, const void *B, void *D, co
         return FP8G_ERR_INVALID_ARG;
     const int64_t hint = max_m_hint > 0 ? max_m_hint : M_max;
     Problem p{A, B, D, masked_m, G, M_max, N, K, hint, a_dtype, b_dtype, flags};
+    return launch(p, stream);
+}
+
+extern "C" int fp8_gemm_nt_scaled(const void *A, const void *B, void *D, int64_t M, int64_t N,
+                                  int64_t K, int a_dtype, int b_dtype, const float *scale_a,
+                                  int64_t scale_a_len, const float *scale_b, int64_t scale_b_len,
+                                  uint32_t flags, cudaStream_t stream)
+{
+    int st = check_common(A, B, D, N, K, a_dtype, b_dtype);
+    if (st != FP8G_OK)
+        return st;
+    if (M <= 0 || M > kMaxDim)
+        return FP8G_ERR_INVALID_ARG;
+    Problem p{A, B, D, nullptr, 1, M, N, K, M, a_dtype, b_dtype, flags};
+    st = check_scales(scale_a, scale_a_len, scale_b, scale_b_len, 1, M, N, p);
+    if (st != FP8G_OK)
+        return st;
+    return launch(p, stream);
+}
+
+extern "C" int fp8_gemm_grouped_masked_scaled(const void *A, const void *B, void *D,
+                                              const int32_t *masked_m, int64_t G, int64_t M_max,
+                                              int64_t N, int64_t K, int64_t max_m_hint, int a_dtype,
+                                              int b_dtype, const float *scale_a, int64_t scale_a_len,
+                                              const float *scale_b, int64_t scale_b_len, uint32_t flags,
+                                              cudaStream_t stream)
+{
+    int st = check_common(A, B, D, N, K, a_dtype, b_dtype);
+    if (st != FP8G_OK)
+        return st;
+    if (!masked_m)
+        return FP8G_ERR_INVALID_ARG;
+    if (G <= 0 || M_max <= 0 || M_max > kMaxDim || max_m_hint < 0 || max_m_hint > M_max)
+        return FP8G_ERR_INVALID_ARG;
+    if (G > kMaxGroups)
+        return FP8G_ERR_UNSUPPORTED;
+    if (G * M_max > kMaxDim || G * N > kMaxDim)
+        return FP8G_ERR_UNSUPPORTED;
+    if (!aligned16(masked_m))
+        return FP8G_ERR_MISALIGNED;
+    const int64_t hint = max_m_hint > 0 ? max_m_hint : M_max;
+    Problem p{A, B, D, masked_m, G, M_max, N, K, hint, a_dtype, b_dtype, flags};
+    st = check_scales(scale_a, scale_a_len, scale_b, scale_b_len, G, M_max, N, p);
+    if (st != FP8G_OK)
+        return st;
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, masked_m) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8G_ERR_INVALID_ARG;
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+        return FP8G_ERR_INVALID_ARG;
     return launch(p, stream);
 }
 

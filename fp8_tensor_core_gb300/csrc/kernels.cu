@@ -119,6 +119,69 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_bits, uint32_t hi_bi
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// ---- output scales -------------------------------------------------------------
+// D = bf16(sa * sb * acc): "the scale is computed beforehand and multiplied
+// back at the output" (DeepGEMM page, §3.1), per tensor or per channel
+// (§5.2).  In FP32: (acc * row_factor) * column_factor.
+
+// Factor that is constant along an output row of the token operand (row m of
+// group g): sa(g, m), times sb(g) when B's scale is per tensor.
+__device__ __forceinline__ float row_factor(const GemmArgs &a, int g, int m)
+{
+    float f = 1.0f;
+    if (a.scale_a)
+        f = __ldg(a.scale_a + (a.sa_per_row ? static_cast<int64_t>(g) * a.rows_a + m : g));
+    if (a.scale_b && !a.sb_per_col)
+        f *= __ldg(a.scale_b + g);
+    return f;
+}
+
+// Eight accumulator values (bits) of columns col..col+7, times `rf` and, with
+// per-column B scales, times sb(g, col + i); packed to eight BF16.
+__device__ __forceinline__ uint4 scale_pack8(const GemmArgs &a, const uint32_t *v, float rf, int g, int col)
+{
+    float f[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        f[i] = __uint_as_float(v[i]) * rf;
+    if (a.scale_b && a.sb_per_col) {
+        const float4 *p = reinterpret_cast<const float4 *>(a.scale_b + static_cast<int64_t>(g) * a.n + col);
+        const float4 x = __ldg(p), y = __ldg(p + 1);
+        f[0] *= x.x;
+        f[1] *= x.y;
+        f[2] *= x.z;
+        f[3] *= x.w;
+        f[4] *= y.x;
+        f[5] *= y.y;
+        f[6] *= y.z;
+        f[7] *= y.w;
+    }
+    uint4 o;
+    o.x = pack_bf16x2(__float_as_uint(f[0]), __float_as_uint(f[1]));
+    o.y = pack_bf16x2(__float_as_uint(f[2]), __float_as_uint(f[3]));
+    o.z = pack_bf16x2(__float_as_uint(f[4]), __float_as_uint(f[5]));
+    o.w = pack_bf16x2(__float_as_uint(f[6]), __float_as_uint(f[7]));
+    return o;
+}
+
+// SwapAB epilogue: thread = output column n (weight row), registers = tokens.
+// Column factor sb(g, n) (times sa(g) when A's scale is per tensor).
+__device__ __forceinline__ float col_factor(const GemmArgs &a, int g, int n)
+{
+    float f = 1.0f;
+    if (a.scale_b)
+        f = __ldg(a.scale_b + (a.sb_per_col ? static_cast<int64_t>(g) * a.n + n : g));
+    if (a.scale_a && !a.sa_per_row)
+        f *= __ldg(a.scale_a + g);
+    return f;
+}
+
+// Per-token factor sa(g, m) when A's scale is per row, else 1.
+__device__ __forceinline__ float token_factor(const GemmArgs &a, int g, int m)
+{
+    return (a.scale_a && a.sa_per_row) ? __ldg(a.scale_a + static_cast<int64_t>(g) * a.rows_a + m) : 1.0f;
+}
+
 // Group table: valid rows per group (clamped to [0, rows_a]) and the
 // exclusive prefix of work units.  Run by one warp.
 template <typename UnitsFn>
@@ -417,6 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dout + (static_cast<int64_t>(g) * a.rows_a + row) * static_cast<int64_t>(a.n);
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * kAccStride);
+            const float rf = row_ok ? row_factor(a, g, row) : 1.0f;
             for (int c = 0; c < a.tile_n; c += 32) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c), r);
@@ -424,14 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const int col = n0 + c + 8 * j;
-                        if (col < a.n) {
-                            uint4 v;
-                            v.x = pack_bf16x2(r[8 * j + 0], r[8 * j + 1]);
-                            v.y = pack_bf16x2(r[8 * j + 2], r[8 * j + 3]);
-                            v.z = pack_bf16x2(r[8 * j + 4], r[8 * j + 5]);
-                            v.w = pack_bf16x2(r[8 * j + 6], r[8 * j + 7]);
-                            *reinterpret_cast<uint4 *>(drow + col) = v;
-                        }
+                        if (col < a.n)
+                            *reinterpret_cast<uint4 *>(drow + col) = scale_pack8(a, r + 8 * j, rf, g, col);
                     }
                 }
             }
@@ -747,16 +805,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             __nv_bfloat16 *drow = dout + static_cast<int64_t>(grow) * static_cast<int64_t>(a.n);
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * kAccStride);
-            // Eight FP32 values (as bits) -> eight BF16 at column col of this row.
+            // Eight FP32 values (as bits) -> eight scaled BF16 at column col.
+            const float rf = row_ok ? row_factor(a, 0, grow) : 1.0f;
             auto store8 = [&](int col, const uint32_t *v) {
-                if (row_ok && col < a.n) {
-                    uint4 o;
-                    o.x = pack_bf16x2(v[0], v[1]);
-                    o.y = pack_bf16x2(v[2], v[3]);
-                    o.z = pack_bf16x2(v[4], v[5]);
-                    o.w = pack_bf16x2(v[6], v[7]);
-                    *reinterpret_cast<uint4 *>(drow + col) = o;
-                }
+                if (row_ok && col < a.n)
+                    *reinterpret_cast<uint4 *>(drow + col) = scale_pack8(a, v, rf, 0, col);
             };
             if (x.kb0 == 0 && x.kb1 == num_kb) {
                 for (int c = 0; c < a.tile_n; c += 32) {
@@ -1116,6 +1169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __nv_bfloat16 *dcol = dout + static_cast<int64_t>(x.g) * a.rows_a * static_cast<int64_t>(a.n) +
                                   nrow;
             const bool whole = x.kb0 == 0 && x.kb1 == num_kb;
+            const float cf = n_ok ? col_factor(a, x.g, nrow) : 1.0f;
             if (whole) {
                 for (int c = 0; c < x.n_mma; c += 16) {
                     uint32_t r[16];
@@ -1124,8 +1178,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             if (c + j < x.n_tok)
-                                dcol[static_cast<int64_t>(x.tok0 + c + j) * a.n] =
-                                    __float2bfloat16_rn(__uint_as_float(r[j]));
+                                dcol[static_cast<int64_t>(x.tok0 + c + j) * a.n] = __float2bfloat16_rn(
+                                    __uint_as_float(r[j]) * cf * token_factor(a, x.g, x.tok0 + c + j));
                         }
                     }
                 }
@@ -1199,8 +1253,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int j = 0; j < 16; ++j) {
                                 if (c + j < x.n_tok)
-                                    dcol[static_cast<int64_t>(x.tok0 + c + j) * a.n] =
-                                        __float2bfloat16_rn(acc_v[j]);
+                                    dcol[static_cast<int64_t>(x.tok0 + c + j) * a.n] = __float2bfloat16_rn(
+                                        acc_v[j] * cf * token_factor(a, x.g, x.tok0 + c + j));
                             }
                         }
                     }

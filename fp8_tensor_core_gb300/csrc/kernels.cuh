@@ -52,6 +52,13 @@ struct GemmArgs {
     uint32_t a_fmt, b_fmt;     // 0 = E4M3, 1 = E5M2 (of A and B as passed by the caller)
     uint32_t flags;            // FP8G_DEBUG_* bits
     uint64_t timeout_ns;       // limit of every barrier wait
+    // Output scales (nullptr: none).  D = bf16(sa * sb * sum):
+    //   sa = scale_a[g * rows_a + m] if sa_per_row, else scale_a[g];
+    //   sb = scale_b[g * n + col]    if sb_per_col, else scale_b[g].
+    const float *scale_a;
+    const float *scale_b;
+    int32_t sa_per_row;
+    int32_t sb_per_col;
     float *workspace;          // swap kernel, stream-K: 2 FP32 partial tiles per CTA
                                // (128 x tile_n floats each)
     int32_t *counters;         // swap kernel, stream-K: arrivals per (tile, epilogue warp),

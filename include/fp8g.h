@@ -1,10 +1,12 @@
 /*
  * fp8g.h -- C ABI of the GB300 (sm_103a) FP8 GEMM library.
  *
- * Two compute entry points:
+ * Compute entry points:
  *
  *   fp8_gemm_nt              D[M,N] = A[M,K] . B[N,K]^T
  *   fp8_gemm_grouped_masked  D[g,m,n] = A[g,m,:] . B[g,n,:]  for m < masked_m[g]
+ *   ..._scaled               the same times per-tensor / per-channel scales
+ *   fp8_gemm_nt_noalloc      dense small-token form that allocates nothing
  *
  * A and B hold FP8 codes (E4M3 or E5M2, chosen per operand), products are
  * accumulated in FP32 by the tensor cores, and D is BF16 (round to nearest
@@ -145,6 +147,33 @@ int fp8_gemm_grouped_masked(const void *A, const void *B, void *D,
                             int64_t N, int64_t K, int64_t max_m_hint,
                             int a_dtype, int b_dtype, uint32_t flags,
                             cudaStream_t stream);
+
+/*
+ * fp8_gemm_nt_scaled / fp8_gemm_grouped_masked_scaled -- the same products
+ * multiplied back by FP32 scales before the BF16 rounding:
+ *   D[m,n]   = bf16( sa(m) * sb(n) * sum_k A[m,k] B[n,k] )            (dense)
+ *   D[g,m,n] = bf16( sa(g,m) * sb(g,n) * sum_k A[g,m,k] B[g,n,k] )    (grouped)
+ * Source: "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践"
+ * §3.1 (the scale is computed beforehand and multiplied back at the
+ * output) and §5.2 (per-tensor or per-channel scales).
+ *   scale_a  DEVICE float array: scale_a_len == G (one per tensor / group)
+ *            or G*rows (rows = M dense, M_max grouped: one per token row).
+ *   scale_b  DEVICE float array: scale_b_len == G or G*N (one per output
+ *            channel).  Dense problems have G = 1.
+ *   Both 16-byte aligned.  Computed in FP32 as (acc * sa) * sb, or with the
+ *   per-tensor factor folded first.  Other arguments, layouts and errors as
+ *   the unscaled calls.
+ */
+int fp8_gemm_nt_scaled(const void *A, const void *B, void *D, int64_t M, int64_t N,
+                       int64_t K, int a_dtype, int b_dtype, const float *scale_a,
+                       int64_t scale_a_len, const float *scale_b, int64_t scale_b_len,
+                       uint32_t flags, cudaStream_t stream);
+int fp8_gemm_grouped_masked_scaled(const void *A, const void *B, void *D,
+                                   const int32_t *masked_m, int64_t G, int64_t M_max,
+                                   int64_t N, int64_t K, int64_t max_m_hint, int a_dtype,
+                                   int b_dtype, const float *scale_a, int64_t scale_a_len,
+                                   const float *scale_b, int64_t scale_b_len,
+                                   uint32_t flags, cudaStream_t stream);
 
 /*
  * fp8g_get_device_status -- synchronise `stream`, then read and clear the
