@@ -18,6 +18,10 @@ What it computes, with its sources:
 * ``gemm_grouped_masked`` -- the masked grouped variant: only rows
   m < masked_m[g] of each group are computed or written ("一次“转置”，半张
   算力：DeepSeek SwapAB 漂流史", §3.1 and §3.3, valid_m).
+* ``gemm_blockscaled`` -- every product scaled by the UE8M0 factors of its
+  K group (32 or 128 elements) for its A row and B row, then summed and
+  rounded once (DeepGEMM page §5.2 per-128-element groups, UE8M0 scales in
+  its SM100 timeline; SwapAB page §3.4, scale factors in the Blackwell MMA).
 * ``gemm_nt_scaled`` / ``gemm_grouped_masked_scaled`` -- the same products
   multiplied back by per-tensor or per-channel FP32 scales before the one
   rounding (DeepGEMM page §3.1 and §5.2).
@@ -108,6 +112,10 @@ def _load():
         lib.oracle_gemm_grouped_masked_scaled.argtypes = [
             _u8p, _u8p, _i32p, _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _f32p, _i64,
             _f32p, _i64, _u16p, _f64p, ctypes.c_int]
+        lib.oracle_gemm_blockscaled.restype = None
+        lib.oracle_gemm_blockscaled.argtypes = [
+            _u8p, _u8p, _i32p, _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _u8p, _i64,
+            _u8p, _i64, _i64, _u16p, _f64p, ctypes.c_int]
         _lib = lib
         return lib
 
@@ -267,6 +275,44 @@ def gemm_grouped_masked_scaled(A: np.ndarray, B: np.ndarray, masked_m: np.ndarra
                                               M_max, N, K, fa, fb, _ptr(sa, f32p), sa.size,
                                               _ptr(sb, f32p), sb.size, _ptr(D, _u16p),
                                               _ptr(absdot, _f64p), int(nthreads))
+    return D, absdot
+
+
+def gemm_blockscaled(A: np.ndarray, B: np.ndarray, sfa: np.ndarray, sfb: np.ndarray,
+                     gran: int = 128, masked_m=None, D_init=None, fa: int = E4M3, fb: int = E4M3,
+                     nthreads: int = 0):
+    """Block-scaled oracle.  Dense: A [M,K], B [N,K], sfa [KS,lda], sfb
+    [KS,ldb] uint8 UE8M0 codes (KS = ceil(K/gran), row m of A scaled by
+    sfa[k // gran, m]).  Grouped: A [G,M_max,K], B [G,N,K], sfa [G,KS,lda],
+    sfb [G,KS,ldb], masked_m [G] (rows m >= masked_m[g] keep D_init's bits).
+    Returns (D_bf16, absdot)."""
+    dense = np.ndim(A) == 2
+    A3 = np.ascontiguousarray(A, np.uint8).reshape((1,) + np.shape(A) if dense else np.shape(A))
+    B3 = np.ascontiguousarray(B, np.uint8).reshape((1,) + np.shape(B) if dense else np.shape(B))
+    G, M_max, K = A3.shape
+    G2, N, K2 = B3.shape
+    assert G == G2 and K == K2 and gran in (32, 128)
+    KS = -(-K // gran)
+    SA = np.ascontiguousarray(sfa, np.uint8).reshape(G, KS, -1)
+    SB = np.ascontiguousarray(sfb, np.uint8).reshape(G, KS, -1)
+    lda, ldb = SA.shape[2], SB.shape[2]
+    assert lda >= M_max and ldb >= N
+    if masked_m is not None:
+        mm = np.ascontiguousarray(masked_m, np.int32)
+        assert mm.shape == (G,) and (mm.size == 0 or (mm.min() >= 0 and mm.max() <= M_max))
+        mm_p = _ptr(mm, _i32p)
+    else:
+        mm_p = None
+    if D_init is None:
+        D = np.zeros((G, M_max, N), np.uint16)
+    else:
+        D = np.array(D_init, np.uint16, copy=True, order="C").reshape(G, M_max, N)
+    absdot = np.zeros((G, M_max, N), np.float64)
+    _load().oracle_gemm_blockscaled(_ptr(A3, _u8p), _ptr(B3, _u8p), mm_p, G, M_max, N, K, fa, fb,
+                                    _ptr(SA, _u8p), lda, _ptr(SB, _u8p), ldb, gran, _ptr(D, _u16p),
+                                    _ptr(absdot, _f64p), int(nthreads))
+    if dense:
+        return D[0], absdot[0]
     return D, absdot
 
 

@@ -10,6 +10,9 @@
  *                       for m < masked_m[g]; other rows of D untouched.
  *   scaled  the same with the exact sum multiplied by per-tensor or
  *           per-channel FP32 scales sa * sb before the one rounding.
+ *   block-scaled  every product a_k b_k multiplied by the UE8M0 scales of
+ *           the K group (of 32 or 128 elements) that k falls in, for its
+ *           row of A and its row of B, before the sum.
  *
  * Sources:
  *  - "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践"
@@ -405,4 +408,87 @@ void oracle_gemm_grouped_masked_scaled(const uint8_t *A, const uint8_t *B,
         free(exact);
         free(ad);
     }
+}
+
+/* ---- block-scaled variant ---------------------------------------------------
+ * "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践" §5.2: scales
+ * may be kept per group of 128 elements; the same page's timeline gives the
+ * SM100 form as UE8M0 ("packed") scale factors, and "一次“转置”，半张算力：
+ * DeepSeek SwapAB 漂流史" §3.4 shows the Blackwell MMA consuming A- and
+ * B-side scale factors.  Reading: with gran in {32, 128} and KS = ceil(K/gran),
+ *     D[g,m,n] = bf16_rne( sum_k dec(A[g,m,k]) dec(B[g,n,k])
+ *                          * 2^(SA[g][k/gran][m] - 127) * 2^(SB[g][k/gran][n] - 127) )
+ * SA is [G][KS][lda] bytes (row m of A at byte m of each K group's vector),
+ * SB is [G][KS][ldb].  A UE8M0 code is a power of two 2^(e-127); code 255 is
+ * NaN (OCP microscaling formats).  Every product is exact in double; the sum
+ * is taken in ascending k and rounded once.  absdot receives
+ * sum_k |a_k b_k| * scales. */
+static double ue8m0_value(uint8_t e)
+{
+    return e == 255 ? NAN : ldexp(1.0, (int)e - 127);
+}
+
+typedef struct {
+    const uint8_t *A, *B, *SA, *SB;
+    const int32_t *masked_m;   /* NULL: every row */
+    int64_t G, M_max, N, K, lda, ldb, gran, KS;
+    double ta[256], tb[256];
+    uint16_t *D;
+    double *absdot;
+} bs_ctx;
+
+static void blockscaled_row(void *vctx, int64_t gm)
+{
+    bs_ctx *c = (bs_ctx *)vctx;
+    int64_t g = gm / c->M_max, m = gm % c->M_max;
+    if (c->masked_m && m >= (int64_t)c->masked_m[g])
+        return;
+    const uint8_t *a = c->A + (g * c->M_max + m) * c->K;
+    const uint8_t *sa = c->SA + g * c->KS * c->lda + m;
+    for (int64_t n = 0; n < c->N; ++n) {
+        const uint8_t *b = c->B + (g * c->N + n) * c->K;
+        const uint8_t *sb = c->SB + g * c->KS * c->ldb + n;
+        double s = 0.0, ad = 0.0;
+        for (int64_t kg = 0; kg < c->KS; ++kg) {
+            double f = ue8m0_value(sa[kg * c->lda]) * ue8m0_value(sb[kg * c->ldb]);
+            int64_t k1 = (kg + 1) * c->gran < c->K ? (kg + 1) * c->gran : c->K;
+            for (int64_t k = kg * c->gran; k < k1; ++k) {
+                double p = c->ta[a[k]] * c->tb[b[k]] * f;
+                s += p;
+                ad += fabs(p);
+            }
+        }
+        int64_t o = (g * c->M_max + m) * c->N + n;
+        c->D[o] = oracle_round_bf16(s);
+        if (c->absdot)
+            c->absdot[o] = ad;
+    }
+}
+
+/* Grouped form; dense is G = 1, masked_m = NULL.  A[G,M_max,K],
+ * B[G,N,K], D[G,M_max,N]; rows m >= masked_m[g] of D are left untouched. */
+void oracle_gemm_blockscaled(const uint8_t *A, const uint8_t *B, const int32_t *masked_m,
+                             int64_t G, int64_t M_max, int64_t N, int64_t K, int fa, int fb,
+                             const uint8_t *SA, int64_t lda, const uint8_t *SB, int64_t ldb,
+                             int64_t gran, uint16_t *D, double *absdot, int nthreads)
+{
+    bs_ctx c;
+    c.A = A;
+    c.B = B;
+    c.SA = SA;
+    c.SB = SB;
+    c.masked_m = masked_m;
+    c.G = G;
+    c.M_max = M_max;
+    c.N = N;
+    c.K = K;
+    c.lda = lda;
+    c.ldb = ldb;
+    c.gran = gran;
+    c.KS = (K + gran - 1) / gran;
+    oracle_decode_table(fa, c.ta);
+    oracle_decode_table(fb, c.tb);
+    c.D = D;
+    c.absdot = absdot;
+    run_rows(blockscaled_row, &c, G * M_max, nthreads);
 }

@@ -420,3 +420,113 @@ def test_grouped_scaled_per_group_and_per_row():
     g = 2
     ref, _ = oracle.gemm_nt_scaled(A[g], B[g], sa_r[g * M_max:(g + 1) * M_max], sa_g[g:g + 1])
     assert np.array_equal(D2[g], ref)
+
+
+# ---- block-scaled variant -----------------------------------------------------------
+
+def _ue8m0(shape, seed, lo=124, hi=130):
+    return np.random.default_rng(seed).integers(lo, hi + 1, shape).astype(np.uint8)
+
+
+@pytest.mark.parametrize("M,N,K,gran", [(3, 4, 40, 32), (5, 2, 130, 128), (2, 3, 96, 32), (4, 4, 17, 128)])
+def test_blockscaled_exact_rational_bruteforce(M, N, K, gran):
+    """Exact rational sum of a_k b_k 2^(ea-127) 2^(eb-127) over k, rounded
+    exactly to BF16, equals the oracle bit for bit."""
+    A = _rand_codes((M, K), 301 + K, 0)
+    B = _rand_codes((N, K), 302 + K, 1)
+    KS = -(-K // gran)
+    sfa = _ue8m0((KS, M + 3), 303 + K)             # ld > M: padding bytes unused
+    sfb = _ue8m0((KS, N), 304 + K)
+    D, absdot = oracle.gemm_blockscaled(A, B, sfa, sfb, gran, fa=0, fb=1)
+    da, db = torch_decode(A, 0), torch_decode(B, 1)
+    for m in range(M):
+        for n in range(N):
+            terms = [Fraction(da[m, k]) * Fraction(db[n, k])
+                     * Fraction(2) ** (int(sfa[k // gran, m]) - 127)
+                     * Fraction(2) ** (int(sfb[k // gran, n]) - 127) for k in range(K)]
+            assert D[m, n] == _rne_fraction_to_bf16(sum(terms, Fraction(0))), (m, n)
+            assert absdot[m, n] == float(sum(abs(t) for t in terms))
+
+
+@pytest.mark.parametrize("gran", [32, 128])
+def test_blockscaled_unit_scales_equal_unscaled(gran):
+    A = _rand_codes((20, 200), 311, 0)
+    B = _rand_codes((12, 200), 312, 0)
+    KS = -(-200 // gran)
+    D, _ = oracle.gemm_blockscaled(A, B, np.full((KS, 20), 127, np.uint8), np.full((KS, 16), 127, np.uint8), gran)
+    D0, _ = oracle.gemm_nt(A, B)
+    assert np.array_equal(D, D0)
+
+
+def test_blockscaled_constant_row_scales_shift_exponents():
+    """Scales constant along K act as per-row / per-column powers of two:
+    the unscaled result with its exponent shifted, exactly."""
+    A = _rand_codes((24, 384), 313, 0)
+    B = _rand_codes((16, 384), 314, 0)
+    ea = np.random.default_rng(6).integers(110, 145, 24)
+    eb = np.random.default_rng(7).integers(110, 145, 16)
+    sfa = np.tile(ea.astype(np.uint8), (3, 1))
+    sfb = np.tile(eb.astype(np.uint8), (3, 1))
+    D, _ = oracle.gemm_blockscaled(A, B, sfa, sfb, 128)
+    D0, _ = oracle.gemm_nt(A, B)
+    want = oracle.bf16_bits_to_f64(D0) * np.ldexp(1.0, (ea - 127)[:, None] + (eb - 127)[None, :])
+    assert np.array_equal(oracle.bf16_bits_to_f64(D), want)
+
+
+@pytest.mark.parametrize("gran", [32, 128])
+def test_blockscaled_isolates_each_k_group(gran):
+    """Scale 1 on one K group and 2^-127 on the others leaves (up to a
+    leak below 2^-90) the unscaled product of that group's K slice alone --
+    so a transposed or mis-strided scale index fails here."""
+    M, N, K = 9, 7, 200
+    A = _rand_codes((M, K), 315, 0)
+    B = _rand_codes((N, K), 316, 0)
+    KS = -(-K // gran)
+    for j in range(KS):
+        sfa = np.zeros((KS, M), np.uint8)
+        sfa[j] = 127
+        sfb = np.full((KS, N), 127, np.uint8)
+        D, _ = oracle.gemm_blockscaled(A, B, sfa, sfb, gran)
+        lo, hi = j * gran, min(K, (j + 1) * gran)
+        _, _, exact = oracle.gemm_nt(A[:, lo:hi].copy(), B[:, lo:hi].copy(), want_exact=True)
+        got = oracle.bf16_bits_to_f64(D)
+        ref = oracle.bf16_bits_to_f64(np.array([[oracle.round_bf16(v) for v in r] for r in exact], np.uint16))
+        assert np.all(np.abs(got - ref) <= 2.0 ** -90), j
+
+
+def test_blockscaled_gran32_replicated_equals_gran128():
+    A = _rand_codes((10, 300), 317, 0)
+    B = _rand_codes((6, 300), 318, 1)
+    s128a, s128b = _ue8m0((3, 10), 319), _ue8m0((3, 6), 320)
+    s32a = np.repeat(s128a, 4, axis=0)[:10]        # ceil(300/32) = 10 groups
+    s32b = np.repeat(s128b, 4, axis=0)[:10]
+    D128, _ = oracle.gemm_blockscaled(A, B, s128a, s128b, 128, fb=1)
+    D32, _ = oracle.gemm_blockscaled(A, B, s32a, s32b, 32, fb=1)
+    assert np.array_equal(D128, D32)
+
+
+def test_blockscaled_nan_code_poisons_its_rows_only():
+    A = _rand_codes((6, 256), 321, 0)
+    B = _rand_codes((5, 256), 322, 0)
+    sfa = np.full((2, 6), 127, np.uint8)
+    sfb = np.full((2, 5), 127, np.uint8)
+    sfa[1, 4] = 255
+    D, _ = oracle.gemm_blockscaled(A, B, sfa, sfb, 128)
+    vals = oracle.bf16_bits_to_f64(D)
+    assert np.all(np.isnan(vals[4])) and not np.any(np.isnan(np.delete(vals, 4, axis=0)))
+
+
+def test_blockscaled_grouped_matches_dense_and_keeps_padding():
+    G, M_max, N, K = 3, 8, 10, 160
+    A = _rand_codes((G, M_max, K), 323, 0)
+    B = _rand_codes((G, N, K), 324, 0)
+    sfa = _ue8m0((G, 2, 16), 325)
+    sfb = _ue8m0((G, 2, N), 326)
+    mm = np.array([5, 0, 8], np.int32)
+    D0 = synth.u16_pattern((G, M_max, N), 327)
+    D, _ = oracle.gemm_blockscaled(A, B, sfa, sfb, 128, masked_m=mm, D_init=D0)
+    for g in range(G):
+        ref, _ = oracle.gemm_blockscaled(A[g], B[g], sfa[g], sfb[g], 128)
+        m = mm[g]
+        assert np.array_equal(D[g, :m], ref[:m])
+        assert np.array_equal(D[g, m:], D0[g, m:])
