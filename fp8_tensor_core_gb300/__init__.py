@@ -278,3 +278,81 @@ def fp8_gemm_grouped_masked_scaled(A, B, masked_m, scale_a, scale_b, D=None, max
     if rc != OK:
         raise Fp8gError(rc, "fp8_gemm_grouped_masked_scaled")
     return D
+
+
+def _check_sf(t, name, groups, ks, rows):
+    import torch
+    if (not t.is_cuda or t.dtype != torch.uint8 or not t.is_contiguous() or t.dim() != 3
+            or t.shape[0] != groups or t.shape[1] != ks or t.shape[2] < rows or t.shape[2] % 16 != 0):
+        raise ValueError("%s must be a contiguous uint8 CUDA tensor [%d, %d, ld] with ld >= %d, ld %% 16 == 0"
+                         % (name, groups, ks, rows))
+
+
+def fp8_gemm_nt_blockscaled(A, B, sf_a, sf_b, D=None, sf_group_k: int = 128, a_dtype=None, b_dtype=None,
+                            flags: int = 0, stream=None):
+    """Block-scaled D[m,n] = bf16(sum_k A[m,k] B[n,k] 2^(sf_a[k/gs, m]-127)
+    2^(sf_b[k/gs, n]-127)).  sf_a: uint8 [ks, lda] (or [1, ks, lda]), sf_b:
+    uint8 [ks, ldb]; ks = ceil(K / sf_group_k), lda >= M and ldb >= N
+    multiples of 16."""
+    import torch
+    _check_operand(A, "A", 2)
+    _check_operand(B, "B", 2)
+    fa, fb = _fp8_code(A, a_dtype), _fp8_code(B, b_dtype)
+    M, K = A.shape
+    N, K2 = B.shape
+    if K != K2:
+        raise ValueError("K mismatch: A has %d, B has %d" % (K, K2))
+    if sf_group_k not in (32, 128):
+        raise ValueError("sf_group_k must be 32 or 128")
+    ks = -(-K // sf_group_k)
+    sa = sf_a if sf_a.dim() == 3 else sf_a.unsqueeze(0)
+    sb = sf_b if sf_b.dim() == 3 else sf_b.unsqueeze(0)
+    _check_sf(sa, "sf_a", 1, ks, M)
+    _check_sf(sb, "sf_b", 1, ks, N)
+    if D is None:
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    else:
+        _check_operand(D, "D", 2)
+        if D.dtype != torch.bfloat16 or tuple(D.shape) != (M, N):
+            raise ValueError("D must be a contiguous bf16 [M, N] tensor")
+    with _on_device(A.device):
+        rc = _lib.load().fp8_gemm_nt_blockscaled(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, fa, fb,
+                                                 sa.data_ptr(), sa.shape[2], sb.data_ptr(), sb.shape[2],
+                                                 int(sf_group_k), int(flags), _stream_handle(stream))
+    if rc != OK:
+        raise Fp8gError(rc, "fp8_gemm_nt_blockscaled")
+    return D
+
+
+def fp8_gemm_grouped_masked_blockscaled(A, B, masked_m, sf_a, sf_b, D=None, max_m_hint: int = 0,
+                                        sf_group_k: int = 128, a_dtype=None, b_dtype=None, flags: int = 0,
+                                        stream=None):
+    """Masked grouped GEMM with block scales: sf_a uint8 [G, ks, lda]
+    (lda >= M_max), sf_b uint8 [G, ks, ldb] (ldb >= N)."""
+    import torch
+    _check_operand(A, "A", 3)
+    _check_operand(B, "B", 3)
+    fa, fb = _fp8_code(A, a_dtype), _fp8_code(B, b_dtype)
+    G, M_max, K = A.shape
+    G2, N, K2 = B.shape
+    if G != G2 or K != K2:
+        raise ValueError("shape mismatch: A %s, B %s" % (tuple(A.shape), tuple(B.shape)))
+    if not masked_m.is_cuda or masked_m.dtype != torch.int32 or tuple(masked_m.shape) != (G,):
+        raise ValueError("masked_m must be a contiguous int32 CUDA tensor of shape [G]")
+    if sf_group_k not in (32, 128):
+        raise ValueError("sf_group_k must be 32 or 128")
+    ks = -(-K // sf_group_k)
+    _check_sf(sf_a, "sf_a", G, ks, M_max)
+    _check_sf(sf_b, "sf_b", G, ks, N)
+    if D is None:
+        D = torch.empty((G, M_max, N), dtype=torch.bfloat16, device=A.device)
+    else:
+        _check_operand(D, "D", 3)
+    with _on_device(A.device):
+        rc = _lib.load().fp8_gemm_grouped_masked_blockscaled(
+            A.data_ptr(), B.data_ptr(), D.data_ptr(), masked_m.data_ptr(), G, M_max, N, K, int(max_m_hint),
+            fa, fb, sf_a.data_ptr(), sf_a.shape[2], sf_b.data_ptr(), sf_b.shape[2], int(sf_group_k),
+            int(flags), _stream_handle(stream))
+    if rc != OK:
+        raise Fp8gError(rc, "fp8_gemm_grouped_masked_blockscaled")
+    return D

@@ -27,6 +27,14 @@ SIGNATURES = {
                                                       _i64, _i64, _i64, _i64, _i64, ctypes.c_int,
                                                       ctypes.c_int, _c_void_p, _i64, _c_void_p, _i64,
                                                       ctypes.c_uint32, _c_void_p]),
+    "fp8_gemm_nt_blockscaled": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _i64, _i64,
+                                               ctypes.c_int, ctypes.c_int, _c_void_p, _i64, _c_void_p,
+                                               _i64, ctypes.c_int, ctypes.c_uint32, _c_void_p]),
+    "fp8_gemm_grouped_masked_blockscaled": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                                           _i64, _i64, _i64, _i64, _i64, ctypes.c_int,
+                                                           ctypes.c_int, _c_void_p, _i64, _c_void_p,
+                                                           _i64, ctypes.c_int, ctypes.c_uint32,
+                                                           _c_void_p]),
     "fp8_gemm_nt_noalloc": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _i64, _i64,
                                            ctypes.c_int, ctypes.c_int, _c_void_p]),
     "fp8g_get_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), _c_void_p]),

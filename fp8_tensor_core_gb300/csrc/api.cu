@@ -125,6 +125,28 @@ bool make_map(CUtensorMap *m, const void *base, int64_t k, int64_t rows, int64_t
     return r == CUDA_SUCCESS;
 }
 
+// 3-D map over block scales [groups, ks, ld] bytes (row r of K group j at
+// byte r of that group's vector), box {box_rows, box_k, 1}, no swizzle,
+// rows >= `rows` and groups >= ks read as zero.
+bool make_sf_map(CUtensorMap *m, const void *base, int64_t rows, int64_t ks, int64_t groups, int64_t ld,
+                 uint32_t box_rows, uint32_t box_k)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(ks),
+                                static_cast<cuuint64_t>(groups)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld),
+                                   static_cast<cuuint64_t>(ks) * static_cast<cuuint64_t>(ld)};
+    const cuuint32_t box[3] = {box_rows, box_k, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    std::memset(m, 0, sizeof(*m));
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Stages that fit the per-block shared-memory budget beside the control
 // block (FP8G_STAGES(n) caps it; the one-stage debug mode forces 1).
 int pick_stages(const DeviceInfo &d, int stage_bytes, int groups, uint32_t flags)
@@ -189,12 +211,14 @@ int check_common(const void *A, const void *B, void *D, int64_t N, int64_t K, in
 
 // N tile of the non-swapped kernel: the candidate with the fewest tile
 // column-equivalents over whole waves of SMs.
-int pick_tile_n(int64_t m_tiles_total, int64_t N, int sms)
+int pick_tile_n(int64_t m_tiles_total, int64_t N, int sms, int max_tn = 256)
 {
     static const int cands[] = {256, 224, 192, 160, 128};
-    int best = 256;
+    int best = 128;
     double best_cost = 1e300;
     for (int tn : cands) {
+        if (tn > max_tn)
+            continue;
         const int64_t units = m_tiles_total * cdiv(N, tn);
         const int64_t waves = cdiv(units, sms);
         const double cost = static_cast<double>(waves) * (tn + 32);
@@ -280,7 +304,47 @@ struct Problem {
     const float *scale_a = nullptr;   // see GemmArgs
     const float *scale_b = nullptr;
     bool sa_per_row = false, sb_per_col = false;
+    // Block scales: [G][ks][ld] UE8M0 bytes; sf_k = 128 / group size (0: none).
+    const uint8_t *sf_a = nullptr, *sf_b = nullptr;
+    int64_t sf_a_ld = 0, sf_b_ld = 0;
+    int sf_k = 0;
 };
+
+// Largest tile (token chunk, or N tile) whose two accumulators leave TMEM
+// room for at least two stages' scale sets.
+constexpr int kMaxBlockScaledTile = 224;
+
+int check_blockscales(const uint8_t *sf_a, int64_t sf_a_ld, const uint8_t *sf_b, int64_t sf_b_ld,
+                      int group_k, int64_t rows, int64_t N, Problem &p)
+{
+    if (!sf_a || !sf_b)
+        return FP8G_ERR_INVALID_ARG;
+    if (group_k != 32 && group_k != 128)
+        return FP8G_ERR_INVALID_ARG;
+    if (sf_a_ld < rows || sf_b_ld < N || sf_a_ld > kMaxDim || sf_b_ld > kMaxDim)
+        return FP8G_ERR_INVALID_ARG;
+    if (sf_a_ld % 16 != 0 || sf_b_ld % 16 != 0 || !aligned16(sf_a) || !aligned16(sf_b))
+        return FP8G_ERR_MISALIGNED;
+    p.sf_a = sf_a;
+    p.sf_b = sf_b;
+    p.sf_a_ld = sf_a_ld;
+    p.sf_b_ld = sf_b_ld;
+    p.sf_k = kBlockK / group_k;
+    return FP8G_OK;
+}
+
+// Stage size and TMEM-limited depth of a block-scaled launch whose MMA B side
+// has box_b rows: operand tiles, then the scale area (at args.sf_off), the
+// whole rounded up to 1024 bytes; scale sets after two accumulators of
+// box_b columns.
+void plan_blockscaled(GemmArgs &args, const DeviceInfo &info, int box_b, int groups, uint32_t flags)
+{
+    args.sf_off = kTileM * kBlockK + box_b * kBlockK;
+    args.stage_bytes = (args.sf_off + sf_stage_bytes(args.sf_k, box_b) + 1023) & ~1023;
+    args.sf_col0 = 2 * box_b;
+    args.stages = pick_stages(info, args.stage_bytes, groups, flags);
+    args.stages = std::min(args.stages, (kTmemCols - 2 * box_b) / sf_set_cols(box_b));
+}
 
 // Scale arguments: both pointers given (16-byte aligned device memory), each
 // with one entry per group or one per row (A) / column (B) of every group.
@@ -337,10 +401,13 @@ int launch(const Problem &p, cudaStream_t stream)
     args.sb_per_col = p.sb_per_col ? 1 : 0;
     args.k_splits = 1;
     args.raster_band = 1;
+    args.sf_k = p.sf_k;
+    const int64_t ks = p.sf_k ? cdiv(p.K, kBlockK / p.sf_k) : 0;
 
-    CUtensorMap tm0, tm1;
+    CUtensorMap tm0, tm1, tm2, tm3;
     if (swap) {
-        const int64_t cap = std::min<int64_t>(256, cdiv(std::max<int64_t>(p.token_hint, 1), 16) * 16);
+        const int64_t cap = std::min<int64_t>(p.sf_k ? kMaxBlockScaledTile : 256,
+                                              cdiv(std::max<int64_t>(p.token_hint, 1), 16) * 16);
         const int64_t chunks = cdiv(p.rows_a, cap);
         const int64_t n_tiles = cdiv(p.N, kTileM);
         const int64_t tiles_upper = p.G * chunks * n_tiles;
@@ -358,7 +425,7 @@ int launch(const Problem &p, cudaStream_t stream)
         // 256 TMEM columns; capping shared memory at half the SM lets the next
         // launch's CTAs become resident (and finish their set-up) while this
         // one drains.
-        const bool share_sm = (p.flags & FP8G_SHARE_SM) && cap <= 128;
+        const bool share_sm = (p.flags & FP8G_SHARE_SM) && cap <= 128 && !p.sf_k;
         size_t smem_request = static_cast<size_t>(info.smem_optin);
         if (share_sm) {
             const int half = info.smem_optin / 2 - 1024;   // leave room for two CTAs' reserved smem
@@ -371,6 +438,9 @@ int launch(const Problem &p, cudaStream_t stream)
                 args.stages = 1;
             args.tmem_cols = 256;
             smem_request = smem_bytes_for(args.stages, args.stage_bytes, static_cast<int>(p.G));
+        } else if (p.sf_k) {
+            plan_blockscaled(args, info, static_cast<int>(cap), static_cast<int>(p.G), p.flags);
+            args.tmem_cols = 512;
         } else {
             args.stages = pick_stages(info, args.stage_bytes, static_cast<int>(p.G), p.flags);
             args.tmem_cols = 512;
@@ -384,14 +454,24 @@ int launch(const Problem &p, cudaStream_t stream)
         }
         if (!make_map(&tm0, p.B, p.K, p.N, p.G, kTileM) || !make_map(&tm1, p.A, p.K, p.rows_a, p.G, 16))
             return FP8G_ERR_CUDA;
-        return launch_gemm_swap(tm0, tm1, args, grid, smem_request, stream) == cudaSuccess
+        if (p.sf_k) {
+            // MMA side A = weights (B's scales), side B = tokens (A's scales).
+            if (!make_sf_map(&tm2, p.sf_b, p.N, ks, p.G, p.sf_b_ld, kTileM, static_cast<uint32_t>(p.sf_k)) ||
+                !make_sf_map(&tm3, p.sf_a, p.rows_a, ks, p.G, p.sf_a_ld, static_cast<uint32_t>(cap),
+                             static_cast<uint32_t>(p.sf_k)))
+                return FP8G_ERR_CUDA;
+        } else {
+            tm2 = tm0;
+            tm3 = tm1;
+        }
+        return launch_gemm_swap(tm0, tm1, tm2, tm3, args, grid, smem_request, stream) == cudaSuccess
                    ? FP8G_OK
                    : FP8G_ERR_CUDA;
     }
 
     // Dense problems with more than one 128-row token tile: two SMs per
     // 256-row tile (cta_group::2), unless single-SM tiles are asked for.
-    if (!p.masked_m && p.G == 1 && p.rows_a > kTileM && !(p.flags & FP8G_SINGLE_SM_TILES)) {
+    if (!p.masked_m && p.G == 1 && p.rows_a > kTileM && !(p.flags & FP8G_SINGLE_SM_TILES) && !p.sf_k) {
         const int64_t m_tiles2 = cdiv(p.rows_a, 2 * kTileM);
         const int pairs = info.sms / 2;
         const PairPlan plan = plan_pair(m_tiles2, p.N, num_kb, pairs, p.flags);
@@ -425,16 +505,21 @@ int launch(const Problem &p, cudaStream_t stream)
     }
 
     const int64_t m_tiles = cdiv(p.rows_a, kTileM);
-    int tile_n = pick_tile_n(p.G * m_tiles, p.N, info.sms);
+    const int max_tn = p.sf_k ? kMaxBlockScaledTile : 256;
+    int tile_n = pick_tile_n(p.G * m_tiles, p.N, info.sms, max_tn);
     const int tn_override = static_cast<int>((p.flags >> 16) & 15u);
     if (tn_override >= 1 && tn_override <= 8)
-        tile_n = 32 * tn_override;
+        tile_n = std::min(32 * tn_override, max_tn);
     const int64_t units_upper = p.G * m_tiles * cdiv(p.N, tile_n);
     if (units_upper > kMaxDim)
         return FP8G_ERR_UNSUPPORTED;
     args.tile_n = tile_n;
-    args.stage_bytes = kTileM * kBlockK + tile_n * kBlockK;
-    args.stages = pick_stages(info, args.stage_bytes, static_cast<int>(p.G), p.flags);
+    if (p.sf_k) {
+        plan_blockscaled(args, info, tile_n, static_cast<int>(p.G), p.flags);
+    } else {
+        args.stage_bytes = kTileM * kBlockK + tile_n * kBlockK;
+        args.stages = pick_stages(info, args.stage_bytes, static_cast<int>(p.G), p.flags);
+    }
     // Bands of M tiles whose token rows total about 48 MB stay resident in L2
     // while the weight tiles stream past them.
     const int64_t band = (48ll << 20) / (kTileM * p.K);
@@ -442,10 +527,20 @@ int launch(const Problem &p, cudaStream_t stream)
     if (!make_map(&tm0, p.A, p.K, p.rows_a, p.G, kTileM) ||
         !make_map(&tm1, p.B, p.K, p.N, p.G, static_cast<uint32_t>(tile_n)))
         return FP8G_ERR_CUDA;
+    if (p.sf_k) {
+        if (!make_sf_map(&tm2, p.sf_a, p.rows_a, ks, p.G, p.sf_a_ld, kTileM, static_cast<uint32_t>(p.sf_k)) ||
+            !make_sf_map(&tm3, p.sf_b, p.N, ks, p.G, p.sf_b_ld, static_cast<uint32_t>(tile_n),
+                         static_cast<uint32_t>(p.sf_k)))
+            return FP8G_ERR_CUDA;
+    } else {
+        tm2 = tm0;
+        tm3 = tm1;
+    }
     const int grid = static_cast<int>(std::min<int64_t>(units_upper, info.sms));
     if (grid <= 0)
         return FP8G_OK;
-    return launch_gemm_mn(tm0, tm1, args, grid, static_cast<size_t>(info.smem_optin), stream) == cudaSuccess
+    return launch_gemm_mn(tm0, tm1, tm2, tm3, args, grid, static_cast<size_t>(info.smem_optin), stream) ==
+                   cudaSuccess
                ? FP8G_OK
                : FP8G_ERR_CUDA;
 }
@@ -537,6 +632,58 @@ extern "C" int fp8_gemm_grouped_masked_scaled(const void *A, const void *B, void
     const int64_t hint = max_m_hint > 0 ? max_m_hint : M_max;
     Problem p{A, B, D, masked_m, G, M_max, N, K, hint, a_dtype, b_dtype, flags};
     st = check_scales(scale_a, scale_a_len, scale_b, scale_b_len, G, M_max, N, p);
+    if (st != FP8G_OK)
+        return st;
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, masked_m) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8G_ERR_INVALID_ARG;
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+        return FP8G_ERR_INVALID_ARG;
+    return launch(p, stream);
+}
+
+extern "C" int fp8_gemm_nt_blockscaled(const void *A, const void *B, void *D, int64_t M, int64_t N,
+                                       int64_t K, int a_dtype, int b_dtype, const uint8_t *sf_a,
+                                       int64_t sf_a_ld, const uint8_t *sf_b, int64_t sf_b_ld,
+                                       int sf_group_k, uint32_t flags, cudaStream_t stream)
+{
+    int st = check_common(A, B, D, N, K, a_dtype, b_dtype);
+    if (st != FP8G_OK)
+        return st;
+    if (M <= 0 || M > kMaxDim)
+        return FP8G_ERR_INVALID_ARG;
+    Problem p{A, B, D, nullptr, 1, M, N, K, M, a_dtype, b_dtype, flags};
+    st = check_blockscales(sf_a, sf_a_ld, sf_b, sf_b_ld, sf_group_k, M, N, p);
+    if (st != FP8G_OK)
+        return st;
+    return launch(p, stream);
+}
+
+extern "C" int fp8_gemm_grouped_masked_blockscaled(const void *A, const void *B, void *D,
+                                                   const int32_t *masked_m, int64_t G, int64_t M_max,
+                                                   int64_t N, int64_t K, int64_t max_m_hint, int a_dtype,
+                                                   int b_dtype, const uint8_t *sf_a, int64_t sf_a_ld,
+                                                   const uint8_t *sf_b, int64_t sf_b_ld, int sf_group_k,
+                                                   uint32_t flags, cudaStream_t stream)
+{
+    int st = check_common(A, B, D, N, K, a_dtype, b_dtype);
+    if (st != FP8G_OK)
+        return st;
+    if (!masked_m)
+        return FP8G_ERR_INVALID_ARG;
+    if (G <= 0 || M_max <= 0 || M_max > kMaxDim || max_m_hint < 0 || max_m_hint > M_max)
+        return FP8G_ERR_INVALID_ARG;
+    if (G > kMaxGroups)
+        return FP8G_ERR_UNSUPPORTED;
+    if (G * M_max > kMaxDim || G * N > kMaxDim)
+        return FP8G_ERR_UNSUPPORTED;
+    if (!aligned16(masked_m))
+        return FP8G_ERR_MISALIGNED;
+    const int64_t hint = max_m_hint > 0 ? max_m_hint : M_max;
+    Problem p{A, B, D, masked_m, G, M_max, N, K, hint, a_dtype, b_dtype, flags};
+    st = check_blockscales(sf_a, sf_a_ld, sf_b, sf_b_ld, sf_group_k, M_max, N, p);
     if (st != FP8G_OK)
         return st;
     cudaPointerAttributes attr;

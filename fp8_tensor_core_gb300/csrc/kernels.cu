@@ -182,6 +182,58 @@ __device__ __forceinline__ float token_factor(const GemmArgs &a, int g, int m)
     return (a.scale_a && a.sa_per_row) ? __ldg(a.scale_a + static_cast<int64_t>(g) * a.rows_a + m) : 1.0f;
 }
 
+// ---- block scales --------------------------------------------------------------
+// Per-group scales of the K dimension ("DeepGEMM：基于 Hopper Tensor Core 的 FP8
+// 矩阵乘法内核优化实践" §5.2, groups of 128 elements; UE8M0 scale factors in its
+// SM100 timeline) applied by the tensor core itself: kind::mxf8f6f4 with one
+// scale factor per row per 32 K elements, read from TMEM ("一次“转置”，半张算力：
+// DeepSeek SwapAB 漂流史" §3.4 shows the A- and B-side scale-factor columns).
+
+// Scale word of row `row` of a raw [sf_k][box] byte block as TMA wrote it:
+// byte i is the row's scale for K elements 32i..32i+31 of the 128-wide block
+// (one 128-element group: the same byte four times).
+__device__ __forceinline__ uint32_t sf_word(const uint8_t *raw, int sf_k, int box, int row)
+{
+    if (sf_k == 1)
+        return static_cast<uint32_t>(raw[row]) * 0x01010101u;
+    return static_cast<uint32_t>(raw[row]) | (static_cast<uint32_t>(raw[box + row]) << 8) |
+           (static_cast<uint32_t>(raw[2 * box + row]) << 16) | (static_cast<uint32_t>(raw[3 * box + row]) << 24);
+}
+
+// MMA warp, all lanes, after the stage's full barrier: rearrange the raw
+// scale bytes into tcgen05.cp sources (per 128 rows, 16-byte row r % 32,
+// word r / 32), then lane 0 copies them into the stage's TMEM scale set:
+// side A at set_tmem, side B at set_tmem + 4 (+4 per further 128 rows).
+// The copies are ordered before the MMAs lane 0 issues next.
+__device__ __forceinline__ void stage_scales(uint8_t *stage, const GemmArgs &a, int box_b, uint32_t set_tmem)
+{
+    const int lane = threadIdx.x & 31;
+    const int sk = a.sf_k;
+    const uint8_t *raw_a = stage + a.sf_off;
+    const uint8_t *raw_b = raw_a + sk * kTileM;
+    uint8_t *src = stage + a.sf_off + sk * (kTileM + box_b);
+    *reinterpret_cast<uint4 *>(src + 16 * lane) =
+        make_uint4(sf_word(raw_a, sk, kTileM, lane), sf_word(raw_a, sk, kTileM, 32 + lane),
+                   sf_word(raw_a, sk, kTileM, 64 + lane), sf_word(raw_a, sk, kTileM, 96 + lane));
+    const int nch = (box_b + 127) >> 7;
+    for (int h = 0; h < nch; ++h) {
+        uint32_t v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int r = 128 * h + 32 * j + lane;
+            v[j] = r < box_b ? sf_word(raw_b, sk, box_b, r) : 0u;
+        }
+        *reinterpret_cast<uint4 *>(src + 512 * (1 + h) + 16 * lane) = make_uint4(v[0], v[1], v[2], v[3]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tmem_cp_32x128b_warpx4(set_tmem, smem_desc_rows16(smem_addr(src)));
+        for (int h = 0; h < nch; ++h)
+            tmem_cp_32x128b_warpx4(set_tmem + 4u + 4u * h, smem_desc_rows16(smem_addr(src + 512 * (1 + h))));
+    }
+}
+
 // Group table: valid rows per group (clamped to [0, rows_a]) and the
 // exclusive prefix of work units.  Run by one warp.
 template <typename UnitsFn>
@@ -326,6 +378,7 @@ __device__ __forceinline__ void mma_drain(SmemCtl &ctl, const GemmArgs &a, bool 
 // =====================================================================================
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_mn(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+              const __grid_constant__ CUtensorMap tm_sa, const __grid_constant__ CUtensorMap tm_sb,
               const GemmArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -335,7 +388,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int n_tiles = ceil_div(a.n, a.tile_n);
     const uint32_t a_bytes = kTileM * kBlockK;                  // 16 KB A box
-    const uint32_t tx_bytes = a_bytes + static_cast<uint32_t>(a.tile_n) * kBlockK;
+    const uint32_t tx_bytes = a_bytes + static_cast<uint32_t>(a.tile_n) * kBlockK +
+                              static_cast<uint32_t>(a.sf_k * (kTileM + a.tile_n));
+    // Accumulator spacing in TMEM: 256 columns, or tile_n when the per-stage
+    // scale sets follow the two accumulators.
+    const int acc_stride = a.sf_k ? a.tile_n : kAccStride;
+    const int set_cols = sf_set_cols(a.tile_n);
 
     if (threadIdx.x == 0)
         init_barriers(ctl, a.stages);
@@ -378,6 +436,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             tma_prefetch_map(&tm_a);
             tma_prefetch_map(&tm_b);
+            if (a.sf_k) {
+                tma_prefetch_map(&tm_sa);
+                tma_prefetch_map(&tm_sb);
+            }
         }
         int stage = 0;
         uint32_t phase = 0;
@@ -399,6 +461,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(fb, tx_bytes);
                     tma_load_3d(smem_addr(sa), &tm_a, fb, kb * kBlockK, m0, g);
                     tma_load_3d(smem_addr(sa + a_bytes), &tm_b, fb, kb * kBlockK, n0, g);
+                    if (a.sf_k) {
+                        tma_load_3d(smem_addr(sa + a.sf_off), &tm_sa, fb, m0, kb * a.sf_k, g);
+                        tma_load_3d(smem_addr(sa + a.sf_off + a.sf_k * kTileM), &tm_sb, fb, n0,
+                                    kb * a.sf_k, g);
+                    }
                 }
                 __syncwarp();
                 ++issued;
@@ -412,6 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ----------------------------- MMA issuer -----------------------------
         const uint32_t idesc = make_idesc(a.a_fmt, a.b_fmt, kTileM, a.tile_n);
+        const uint32_t idesc_bs = make_idesc_bs(a.a_fmt, a.b_fmt, kTileM, a.tile_n, 0);
         int stage = 0;
         uint32_t phase = 0;
         int acc = 0;
@@ -422,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            100 + acc))
                 break;
             tc_fence_after();
-            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccStride);
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * acc_stride);
             bool ok = true;
             for (int kb = 0; kb < a.num_kb; ++kb) {
                 if (!warp_wait(smem_addr(&ctl.full[stage]), phase, ctl, a.timeout_ns, kRoleMma,
@@ -431,7 +499,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                if (lane == 0) {
+                if (a.sf_k) {
+                    uint8_t *sp = sm.stages + static_cast<size_t>(stage) * a.stage_bytes;
+                    const uint32_t set = tmem_base + static_cast<uint32_t>(a.sf_col0 + stage * set_cols);
+                    stage_scales(sp, a, a.tile_n, set);
+                    if (lane == 0) {
+                        const uint64_t adesc = smem_desc_k_sw128(smem_addr(sp));
+                        const uint64_t bdesc = smem_desc_k_sw128(smem_addr(sp) + a_bytes);
+#pragma unroll
+                        for (int k = 0; k < kBlockK / 32; ++k)
+                            mma_f8f6f4_bs(d_tmem, adesc + 2u * k, bdesc + 2u * k,
+                                          idesc_bs | (static_cast<uint32_t>(k) << 4) |
+                                              (static_cast<uint32_t>(k) << 29),
+                                          set, set + 4u, (kb | k) != 0 ? 1u : 0u);
+                        mma_commit(smem_addr(&ctl.empty[stage]));
+                    }
+                } else if (lane == 0) {
                     const uint32_t sa = smem_addr(sm.stages + static_cast<size_t>(stage) * a.stage_bytes);
                     const uint64_t adesc = smem_desc_k_sw128(sa);
                     const uint64_t bdesc = smem_desc_k_sw128(sa + a_bytes);
@@ -479,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __nv_bfloat16 *drow =
                 dout + (static_cast<int64_t>(g) * a.rows_a + row) * static_cast<int64_t>(a.n);
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                   static_cast<uint32_t>(acc * kAccStride);
+                                   static_cast<uint32_t>(acc * acc_stride);
             const float rf = row_ok ? row_factor(a, g, row) : 1.0f;
             for (int c = 0; c < a.tile_n; c += 32) {
                 uint32_t r[32];
@@ -954,6 +1037,7 @@ struct SwapWalker {
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_swap(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_t,
+                const __grid_constant__ CUtensorMap tm_sw, const __grid_constant__ CUtensorMap tm_st,
                 const GemmArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -968,8 +1052,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t w_bytes = kTileM * kBlockK;   // 16 KB weight box
     // Accumulators: two of 256 columns, or two of 128 (tile_n <= 128) so
     // that two CTAs -- this launch's and the next one's -- fit in TMEM.
-    const uint32_t tmem_cols = a.tmem_cols == 256 ? 256u : static_cast<uint32_t>(kTmemCols);
-    const int acc_stride = static_cast<int>(tmem_cols / 2);
+    // With block scales: two accumulators of `cap` columns, then the
+    // per-stage scale sets.
+    const uint32_t tmem_cols = (a.tmem_cols == 256 && !a.sf_k) ? 256u : static_cast<uint32_t>(kTmemCols);
+    const int acc_stride = a.sf_k ? cap : static_cast<int>(tmem_cols / 2);
+    const int set_cols = sf_set_cols(cap);
     constexpr int kTokBox = 16;                  // token rows per TMA box
     constexpr uint32_t kTokBoxBytes = kTokBox * kBlockK;
 
@@ -1052,6 +1139,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             tma_prefetch_map(&tm_w);
             tma_prefetch_map(&tm_t);
+            if (a.sf_k) {
+                tma_prefetch_map(&tm_sw);
+                tma_prefetch_map(&tm_st);
+            }
         }
         int stage = 0;
         uint32_t phase = 0;
@@ -1062,7 +1153,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         SwapWalker wk = make_walker();
         SwapSeg x;
         while (!aborted && next_seg(wk, x)) {
-            const uint32_t tx = w_bytes + static_cast<uint32_t>(x.n_mma) * kBlockK;
+            const uint32_t tx = w_bytes + static_cast<uint32_t>(x.n_mma) * kBlockK +
+                                static_cast<uint32_t>(a.sf_k * (kTileM + cap));
             for (int kb = x.kb0; kb < x.kb1; ++kb) {
                 if (!warp_wait(smem_addr(&ctl.empty[stage]), phase ^ 1u, ctl, a.timeout_ns,
                                kRoleLoader, stage)) {
@@ -1077,6 +1169,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int r = 0; r < x.n_mma; r += kTokBox)
                         tma_load_3d(smem_addr(sw + w_bytes + (r / kTokBox) * kTokBoxBytes), &tm_t, fb,
                                     kb * kBlockK, x.tok0 + r, x.g);
+                    if (a.sf_k) {
+                        tma_load_3d_hint(smem_addr(sw + a.sf_off), &tm_sw, fb, x.w0, kb * a.sf_k, x.g,
+                                         w_policy);
+                        tma_load_3d(smem_addr(sw + a.sf_off + a.sf_k * kTileM), &tm_st, fb, x.tok0,
+                                    kb * a.sf_k, x.g);
+                    }
                 }
                 __syncwarp();
                 ++issued;
@@ -1100,6 +1198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         SwapSeg x;
         while (next_seg(wk, x)) {
             const uint32_t idesc = make_idesc(a.b_fmt, a.a_fmt, kTileM, static_cast<uint32_t>(x.n_mma));
+            const uint32_t idesc_bs = make_idesc_bs(a.b_fmt, a.a_fmt, kTileM, static_cast<uint32_t>(x.n_mma), 0);
             if (!warp_wait(smem_addr(&ctl.tempty[acc]), acc_phase ^ 1u, ctl, a.timeout_ns, kRoleMma,
                            100 + acc))
                 break;
@@ -1113,7 +1212,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                if (lane == 0) {
+                if (a.sf_k) {
+                    uint8_t *sp = sm.stages + static_cast<size_t>(stage) * a.stage_bytes;
+                    const uint32_t set = tmem_base + static_cast<uint32_t>(a.sf_col0 + stage * set_cols);
+                    stage_scales(sp, a, cap, set);
+                    if (lane == 0) {
+                        const uint64_t wdesc = smem_desc_k_sw128(smem_addr(sp));
+                        const uint64_t tdesc = smem_desc_k_sw128(smem_addr(sp) + w_bytes);
+#pragma unroll
+                        for (int k = 0; k < kBlockK / 32; ++k)
+                            mma_f8f6f4_bs(d_tmem, wdesc + 2u * k, tdesc + 2u * k,
+                                          idesc_bs | (static_cast<uint32_t>(k) << 4) |
+                                              (static_cast<uint32_t>(k) << 29),
+                                          set, set + 4u, (kb != x.kb0 || k != 0) ? 1u : 0u);
+                        mma_commit(smem_addr(&ctl.empty[stage]));
+                    }
+                } else if (lane == 0) {
                     const uint32_t sw = smem_addr(sm.stages + static_cast<size_t>(stage) * a.stage_bytes);
                     const uint64_t wdesc = smem_desc_k_sw128(sw);
                     const uint64_t tdesc = smem_desc_k_sw128(sw + w_bytes);
@@ -1283,9 +1397,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Launch with programmatic stream serialisation (unless FP8G_NO_PDL): the
 // kernel may start while the previous launch in the stream finishes; it
 // waits (griddepcontrol.wait) before touching global memory.
-template <typename Kernel>
+template <typename Kernel, typename... Maps>
 static cudaError_t launch_pdl(Kernel kernel, int grid, size_t smem, cudaStream_t stream,
-                              const GemmArgs &args, const CUtensorMap &m0, const CUtensorMap &m1)
+                              const GemmArgs &args, const Maps &...maps)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
@@ -1297,14 +1411,15 @@ static cudaError_t launch_pdl(Kernel kernel, int grid, size_t smem, cudaStream_t
     attr[0].val.programmaticStreamSerializationAllowed = (args.flags & FP8G_NO_PDL) ? 0 : 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, m0, m1, args);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, maps..., args);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
 }
 
-cudaError_t launch_gemm_mn(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const GemmArgs &args,
-                           int grid, size_t smem, cudaStream_t stream)
+cudaError_t launch_gemm_mn(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const CUtensorMap &tm_sa,
+                           const CUtensorMap &tm_sb, const GemmArgs &args, int grid, size_t smem,
+                           cudaStream_t stream)
 {
     if (smem < smem_bytes_for(args.stages, args.stage_bytes, args.groups))
         return cudaErrorInvalidValue;
@@ -1312,7 +1427,7 @@ cudaError_t launch_gemm_mn(const CUtensorMap &tm_a, const CUtensorMap &tm_b, con
                                          static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(k_gemm_mn, grid, smem, stream, args, tm_a, tm_b);
+    return launch_pdl(k_gemm_mn, grid, smem, stream, args, tm_a, tm_b, tm_sa, tm_sb);
 }
 
 cudaError_t launch_gemm_mn2(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const GemmArgs &args,
@@ -1328,8 +1443,9 @@ cudaError_t launch_gemm_mn2(const CUtensorMap &tm_a, const CUtensorMap &tm_b, co
     return launch_pdl(k_gemm_mn2, grid, smem, stream, args, tm_a, tm_b);
 }
 
-cudaError_t launch_gemm_swap(const CUtensorMap &tm_w, const CUtensorMap &tm_t,
-                             const GemmArgs &args, int grid, size_t smem, cudaStream_t stream)
+cudaError_t launch_gemm_swap(const CUtensorMap &tm_w, const CUtensorMap &tm_t, const CUtensorMap &tm_sw,
+                             const CUtensorMap &tm_st, const GemmArgs &args, int grid, size_t smem,
+                             cudaStream_t stream)
 {
     if (smem < smem_bytes_for(args.stages, args.stage_bytes, args.groups))
         return cudaErrorInvalidValue;
@@ -1337,7 +1453,7 @@ cudaError_t launch_gemm_swap(const CUtensorMap &tm_w, const CUtensorMap &tm_t,
                                          static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(k_gemm_swap, grid, smem, stream, args, tm_w, tm_t);
+    return launch_pdl(k_gemm_swap, grid, smem, stream, args, tm_w, tm_t, tm_sw, tm_st);
 }
 
 cudaError_t read_and_clear_status(int32_t info[4])

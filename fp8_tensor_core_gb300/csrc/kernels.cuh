@@ -59,11 +59,28 @@ struct GemmArgs {
     const float *scale_b;
     int32_t sa_per_row;
     int32_t sb_per_col;
+    // Block scales (UE8M0, one byte per row per K group), loaded by TMA with
+    // each stage.  sf_k = 0: none; else scale bytes per row per 128-wide K
+    // block (1: groups of 128 elements, 4: groups of 32).
+    int32_t sf_k;
+    int32_t sf_off;            // byte offset of the scale area inside a stage
+    int32_t sf_col0;           // first TMEM column of the per-stage scale sets
     float *workspace;          // swap kernel, stream-K: 2 FP32 partial tiles per CTA
                                // (128 x tile_n floats each)
     int32_t *counters;         // swap kernel, stream-K: arrivals per (tile, epilogue warp),
                                // zero at rest
 };
+
+// Block-scaled stage layout.  After the two operand tiles (MMA side A: 128
+// rows; side B: box_b rows) a stage holds the raw scale bytes as TMA writes
+// them ([sf_k][128] then [sf_k][box_b]) and the tcgen05.cp sources built
+// from them (512 bytes per 128 rows).  In TMEM each stage owns a scale set
+// of 4 columns for side A and 4 per 128 rows of side B.
+inline int sf_stage_bytes(int sf_k, int box_b)
+{
+    return sf_k * (kTileM + box_b) + 512 * (1 + (box_b + 127) / 128);
+}
+__host__ __device__ inline int sf_set_cols(int box_b) { return 4 + 4 * ((box_b + 127) / 128); }
 
 // Shared-memory footprint of a launch (stages + control block + alignment).
 inline size_t smem_bytes_for(int stages, int stage_bytes, int groups)
@@ -74,13 +91,17 @@ inline size_t smem_bytes_for(int stages, int stage_bytes, int groups)
 // `smem` must be at least smem_bytes_for(stages, stage_bytes, groups); the
 // host passes the whole per-block budget so that exactly one CTA (and one
 // 512-column TMEM allocation) is resident per SM.
-cudaError_t launch_gemm_mn(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const GemmArgs &args,
-                           int grid, size_t smem, cudaStream_t stream);
+// tm_sa / tm_sb: block-scale maps of the MMA's A and B sides (read only when
+// args.sf_k != 0; any valid map otherwise).
+cudaError_t launch_gemm_mn(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const CUtensorMap &tm_sa,
+                           const CUtensorMap &tm_sb, const GemmArgs &args, int grid, size_t smem,
+                           cudaStream_t stream);
 // Dense only: clusters of two CTAs, 256 x tile_n tiles, B box of tile_n/2 rows.
 cudaError_t launch_gemm_mn2(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const GemmArgs &args,
                             int grid, size_t smem, cudaStream_t stream);
-cudaError_t launch_gemm_swap(const CUtensorMap &tm_w, const CUtensorMap &tm_t,
-                             const GemmArgs &args, int grid, size_t smem, cudaStream_t stream);
+cudaError_t launch_gemm_swap(const CUtensorMap &tm_w, const CUtensorMap &tm_t, const CUtensorMap &tm_sw,
+                             const CUtensorMap &tm_st, const GemmArgs &args, int grid, size_t smem,
+                             cudaStream_t stream);
 
 // Scratch a swap-kernel launch needs: partial tiles (2 per CTA) and counters.
 inline size_t swap_partials_bytes(int grid, int tile_n)

@@ -189,7 +189,7 @@ extern "C" int fp8_gemm_nt_noalloc(const void *A, const void *B, void *D, int64_
         return FP8G_ERR_CUDA;
     if (cudaMemsetAsync(args.counters, 0, counter_bytes, stream) != cudaSuccess)
         return FP8G_ERR_CUDA;
-    return launch_gemm_swap(tm_w, tm_t, args, grid, static_cast<size_t>(smem), stream) == cudaSuccess
+    return launch_gemm_swap(tm_w, tm_t, tm_w, tm_t, args, grid, static_cast<size_t>(smem), stream) == cudaSuccess
                ? FP8G_OK
                : FP8G_ERR_CUDA;
 }

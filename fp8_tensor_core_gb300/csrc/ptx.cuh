@@ -147,6 +147,40 @@ __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, uin
                  : "memory");
 }
 
+// Block-scaled form (kind::mxf8f6f4 with UE8M0 scale factors, one per 32
+// K elements of each row): each row of A and of B is multiplied by the
+// scale factor read from TMEM at sfa_tmem / sfb_tmem.  Scale-factor layout
+// in TMEM (four columns per 128 rows): row r at lane r % 32 of every lane
+// quadrant, column r / 32; the instruction descriptor picks the byte.
+__device__ __forceinline__ void mma_f8f6f4_bs(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                              uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %6, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+                 "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+                 : "memory");
+}
+
+// Shared memory -> TMEM copy of 32 rows x 16 bytes, replicated into all four
+// lane quadrants: source row l lands in lanes l, 32 + l, 64 + l, 96 + l,
+// its four 32-bit words in columns taddr.col .. +3.  Ordered before the
+// tcgen05.mma instructions this thread issues after it.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+}
+
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy reads (TMA, tcgen05.cp) of the same bytes.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation issued so far by this
 // thread has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar)
@@ -317,6 +351,30 @@ __device__ __forceinline__ uint64_t smem_desc_k_sw128(uint32_t saddr)
     d |= static_cast<uint64_t>(1u) << 46;
     d |= static_cast<uint64_t>(2u) << 61;
     return d;
+}
+
+// Descriptor of a tcgen05.cp source: 32 rows of 16 bytes at a 16-byte
+// pitch (no swizzle; 8-row core matrices 128 bytes apart).
+__device__ __forceinline__ uint64_t smem_desc_rows16(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(128u >> 4) << 16;
+    d |= static_cast<uint64_t>(128u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    return d;
+}
+
+// Instruction descriptor for tcgen05.mma kind::mxf8f6f4.block_scale, FP32 D,
+// K-major operands, UE8M0 scale factors:
+//   bits 4-5 byte of the B scale-factor word, 7-9 A format, 10-12 B format,
+//   17-22 N >> 3, 23 scale format (1 = UE8M0), 24-28 M >> 4, 29-30 byte of
+//   the A scale-factor word.
+__host__ __device__ __forceinline__ constexpr uint32_t make_idesc_bs(uint32_t a_fmt, uint32_t b_fmt,
+                                                                      uint32_t m, uint32_t n, uint32_t sf_id)
+{
+    return (sf_id << 4) | (a_fmt << 7) | (b_fmt << 10) | ((n >> 3) << 17) | (1u << 23) | ((m >> 4) << 24) |
+           (sf_id << 29);
 }
 
 // Instruction descriptor for tcgen05.mma kind::f8f6f4, dense, FP32 D,

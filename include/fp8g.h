@@ -6,6 +6,7 @@
  *   fp8_gemm_nt              D[M,N] = A[M,K] . B[N,K]^T
  *   fp8_gemm_grouped_masked  D[g,m,n] = A[g,m,:] . B[g,n,:]  for m < masked_m[g]
  *   ..._scaled               the same times per-tensor / per-channel scales
+ *   ..._blockscaled          UE8M0 scales per row per 32/128-element K group
  *   fp8_gemm_nt_noalloc      dense small-token form that allocates nothing
  *
  * A and B hold FP8 codes (E4M3 or E5M2, chosen per operand), products are
@@ -174,6 +175,40 @@ int fp8_gemm_grouped_masked_scaled(const void *A, const void *B, void *D,
                                    int b_dtype, const float *scale_a, int64_t scale_a_len,
                                    const float *scale_b, int64_t scale_b_len,
                                    uint32_t flags, cudaStream_t stream);
+
+/*
+ * fp8_gemm_nt_blockscaled / fp8_gemm_grouped_masked_blockscaled -- block-
+ * scaled products: every K group of `sf_group_k` (32 or 128) elements of
+ * each row of A and of B carries its own UE8M0 scale (2^(e-127); e = 255 is
+ * NaN), applied to the products before they are summed:
+ *   D[g,m,n] = bf16( sum_k A[g,m,k] B[g,n,k]
+ *                    * 2^(sf_a[g][k/gs][m] - 127) * 2^(sf_b[g][k/gs][n] - 127) )
+ * Source: "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践"
+ * §5.2 (scales per group of 128 elements) and its SM100 timeline (UE8M0
+ * scales); "一次“转置”，半张算力：DeepSeek SwapAB 漂流史" §3.4 (the
+ * Blackwell MMA takes A- and B-side scale factors).  The tensor core applies
+ * the scales (tcgen05.mma kind::mxf8f6f4.block_scale).
+ *   sf_a   DEVICE bytes [G][ceil(K/gs)][sf_a_ld]: the scale of row m of A
+ *          (token row) for K group j at sf_a[(g*ks + j)*sf_a_ld + m];
+ *          sf_a_ld >= M (dense) or M_max (grouped), a multiple of 16.
+ *   sf_b   DEVICE bytes [G][ceil(K/gs)][sf_b_ld], row n of B likewise;
+ *          sf_b_ld >= N, a multiple of 16.  128x128 weight blocks are
+ *          expressed by repeating a block's scale over its 128 rows.
+ *   Both 16-byte aligned; padding bytes past M / N are never read.
+ * The SM-pair dense kernel has no block-scaled form: dense problems run on
+ * single-SM tiles (N tile <= 224) or SwapAB (token chunks <= 224).  Other
+ * arguments, layouts and errors as the unscaled calls.
+ */
+int fp8_gemm_nt_blockscaled(const void *A, const void *B, void *D, int64_t M, int64_t N,
+                            int64_t K, int a_dtype, int b_dtype, const uint8_t *sf_a,
+                            int64_t sf_a_ld, const uint8_t *sf_b, int64_t sf_b_ld,
+                            int sf_group_k, uint32_t flags, cudaStream_t stream);
+int fp8_gemm_grouped_masked_blockscaled(const void *A, const void *B, void *D,
+                                        const int32_t *masked_m, int64_t G, int64_t M_max,
+                                        int64_t N, int64_t K, int64_t max_m_hint, int a_dtype,
+                                        int b_dtype, const uint8_t *sf_a, int64_t sf_a_ld,
+                                        const uint8_t *sf_b, int64_t sf_b_ld, int sf_group_k,
+                                        uint32_t flags, cudaStream_t stream);
 
 /*
  * fp8g_get_device_status -- synchronise `stream`, then read and clear the

@@ -1,0 +1,231 @@
+"""GPU parity of the block-scaled entry points (UE8M0 scale per row per 32- or
+128-element K group, applied by tcgen05.mma kind::mxf8f6f4.block_scale)
+against the oracle's block-scaled definition: the single-SM tile kernel at
+every tile width, SwapAB (stream-K and whole tiles), the masked grouped form
+with poisoned padding, ragged tails, both FP8 formats, and the host-side
+argument checks.  Sources: "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法
+内核优化实践" §5.2 (per-128-element groups) and "一次“转置”，半张算力：DeepSeek
+SwapAB 漂流史" §3.4 (scale factors in the Blackwell MMA)."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import __graft_entry__  # noqa: F401
+import fp8_tensor_core_gb300 as fp8g
+from fp8_tensor_core_gb300 import _lib
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+E4, E5 = synth.E4M3, synth.E5M2
+OFF, ON, AUTO = fp8g.SWAP_OFF, fp8g.SWAP_ON, fp8g.SWAP_AUTO
+
+
+@pytest.fixture(scope="module", autouse=True)
+def device():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from fp8_tensor_core_gb300 import build as cuda_build
+    cuda_build.build()
+    torch.cuda.set_device(0)
+    fp8g.fp8g_get_device_status()
+    yield
+
+
+def dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).to("cuda:0")
+
+
+def bits(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def assert_status_ok():
+    st = fp8g.fp8g_get_device_status()
+    assert st[0] == fp8g.OK, "device status %s" % (st,)
+
+
+def ld16(n):
+    return -(-n // 16) * 16
+
+
+def ue8m0(shape, seed, lo=117, hi=137):
+    """Seeded UE8M0 codes in [lo, hi] (2^-10 .. 2^10 by default)."""
+    return np.random.default_rng(seed).integers(lo, hi + 1, shape).astype(np.uint8)
+
+
+def check_dense_bs(M, N, K, gran, flags, seed, fa=E4, fb=E4, pad=16):
+    A = synth.normal_fp8((M, K), seed, 0.0, 1.0, fa)
+    B = synth.normal_fp8((N, K), seed + 1, 0.0, 1.0, fb)
+    ks = -(-K // gran)
+    sfa = ue8m0((ks, ld16(M) + pad), seed + 2)
+    sfb = ue8m0((ks, ld16(N) + pad), seed + 3)
+    D = fp8g.fp8_gemm_nt_blockscaled(dev(A), dev(B), dev(sfa), dev(sfb), sf_group_k=gran, a_dtype=fa,
+                                     b_dtype=fb, flags=flags)
+    torch.cuda.synchronize()
+    assert_status_ok()
+    ref, absdot = oracle.gemm_blockscaled(A, B, sfa, sfb, gran, fa=fa, fb=fb)
+    ok, rep = oracle.check_bf16(bits(D), ref, absdot)
+    assert ok, rep
+    return rep
+
+
+# ---- single-SM tiles (tokens on M) ---------------------------------------------------
+
+@pytest.mark.parametrize("gran", [128, 32])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (300, 520, 1040), (129, 232, 2064), (640, 896, 512)])
+def test_dense_tiles(M, N, K, gran):
+    check_dense_bs(M, N, K, gran, OFF, seed=500 + M + N + K + gran)
+
+
+@pytest.mark.parametrize("tn", [4, 5, 6, 7, 8])
+def test_dense_every_tile_width(tn):
+    """FP8G_TILE_N(8) (256 columns) is clamped to the widest block-scaled tile."""
+    check_dense_bs(256, 480, 768, 128, OFF | fp8g.TILE_N(tn), seed=520 + tn)
+
+
+@pytest.mark.parametrize("fa,fb", [(E5, E4), (E4, E5), (E5, E5)])
+def test_dense_mixed_formats(fa, fb):
+    check_dense_bs(200, 272, 640, 32, OFF, seed=530 + 2 * fa + fb, fa=fa, fb=fb)
+
+
+def test_dense_one_stage_pipeline():
+    check_dense_bs(256, 384, 1024, 128, OFF | fp8g.DEBUG_ONE_STAGE, seed=535)
+
+
+def test_exact_data_is_bit_exact():
+    """Small-integer operands and power-of-two scales: every partial sum is
+    exact in FP32, so the result must equal the oracle bit for bit."""
+    M, N, K = 256, 320, 512
+    rng = np.random.default_rng(540)
+    vals = np.array([-2.0, -1.0, 0.0, 1.0, 2.0])
+    A = synth.encode_fp8_array(vals[rng.integers(0, 5, (M, K))], E4)
+    B = synth.encode_fp8_array(vals[rng.integers(0, 5, (N, K))], E4)
+    for gran in (128, 32):
+        ks = K // gran
+        sfa = ue8m0((ks, M), 541 + gran, 124, 130)
+        sfb = ue8m0((ks, N), 542 + gran, 124, 130)
+        for flags in (OFF, ON):
+            D = fp8g.fp8_gemm_nt_blockscaled(dev(A), dev(B), dev(sfa), dev(sfb), sf_group_k=gran,
+                                             a_dtype=E4, b_dtype=E4, flags=flags)
+            torch.cuda.synchronize()
+            assert_status_ok()
+            ref, _ = oracle.gemm_blockscaled(A, B, sfa, sfb, gran)
+            assert np.array_equal(bits(D), ref), (gran, flags)
+
+
+def test_scales_reach_the_right_k_group():
+    """One K group scaled 2^20 above the rest: the result is (to BF16
+    precision) that group's product alone, for every group position."""
+    M, N, K = 128, 256, 640
+    A = synth.normal_fp8((M, K), 545, 0.0, 1.0, E4)
+    B = synth.normal_fp8((N, K), 546, 0.0, 1.0, E4)
+    for gran in (128, 32):
+        ks = K // gran
+        for j in (0, 1, ks - 1):
+            sfa = np.full((ks, M), 107, np.uint8)
+            sfa[j] = 127
+            sfb = np.full((ks, N), 127, np.uint8)
+            for flags in (OFF, ON):
+                D = fp8g.fp8_gemm_nt_blockscaled(dev(A), dev(B), dev(sfa), dev(sfb), sf_group_k=gran,
+                                                 a_dtype=E4, b_dtype=E4, flags=flags)
+                torch.cuda.synchronize()
+                assert_status_ok()
+                ref, absdot = oracle.gemm_blockscaled(A, B, sfa, sfb, gran)
+                ok, rep = oracle.check_bf16(bits(D), ref, absdot)
+                assert ok, (gran, j, flags, rep)
+
+
+# ---- SwapAB (weights on M, tokens on the runtime N) -----------------------------------
+
+@pytest.mark.parametrize("gran", [128, 32])
+@pytest.mark.parametrize("flags", [ON, ON | fp8g.WHOLE_TILES])
+@pytest.mark.parametrize("M,N,K", [(1, 256, 512), (40, 640, 1536), (100, 384, 4112), (224, 512, 1024)])
+def test_swap(M, N, K, flags, gran):
+    check_dense_bs(M, N, K, gran, flags, seed=550 + M + N + gran)
+
+
+@pytest.mark.parametrize("M", [1, 16, 33, 64, 130])
+def test_auto_small_m(M):
+    check_dense_bs(M, 2048, 1024, 128, AUTO, seed=560 + M)
+
+
+# ---- masked grouped -------------------------------------------------------------------
+
+def grouped_bs_case(G, M_max, N, K, mm, gran, flags, hint, seed, fa=E4, fb=E4):
+    A = synth.normal_fp8((G, M_max, K), seed, 0.0, 0.5, fa)
+    B = synth.normal_fp8((G, N, K), seed + 1, 0.0, 0.5, fb)
+    mm = np.asarray(mm, np.int32)
+    ks = -(-K // gran)
+    sfa = ue8m0((G, ks, ld16(M_max)), seed + 2)
+    sfb = ue8m0((G, ks, ld16(N)), seed + 3)
+    for g in range(G):                      # padding tokens: NaN data and NaN scales
+        A[g, mm[g]:] = 0x7F
+        sfa[g, :, mm[g]:] = 255
+    D0 = synth.u16_pattern((G, M_max, N), seed + 4)
+    D0[..., ::89] = 0x7FC1
+    Dt = dev(D0.view(np.int16)).view(torch.bfloat16)
+    fp8g.fp8_gemm_grouped_masked_blockscaled(dev(A), dev(B), dev(mm), dev(sfa), dev(sfb), D=Dt,
+                                             max_m_hint=hint, sf_group_k=gran, a_dtype=fa, b_dtype=fb,
+                                             flags=flags)
+    torch.cuda.synchronize()
+    assert_status_ok()
+    got = bits(Dt)
+    ref, absdot = oracle.gemm_blockscaled(A, B, sfa, sfb, gran, masked_m=mm, D_init=D0, fa=fa, fb=fb)
+    for g in range(G):
+        m = mm[g]
+        ok, rep = oracle.check_bf16(got[g, :m], ref[g, :m], absdot[g, :m])
+        assert ok, (g, rep)
+        assert np.array_equal(got[g, m:], D0[g, m:]), "padding rows of group %d written" % g
+
+
+@pytest.mark.parametrize("gran", [128, 32])
+@pytest.mark.parametrize("flags,hint", [(ON, 32), (ON | fp8g.WHOLE_TILES, 64), (OFF, 0), (AUTO, 0)])
+def test_grouped(flags, hint, gran):
+    mm = [0, 1, 9, 16, 17, 32, 5, 64]
+    grouped_bs_case(len(mm), 64, 384, 640, mm, gran, flags, hint, seed=600 + gran)
+
+
+def test_grouped_mixed_formats():
+    grouped_bs_case(3, 48, 256, 512, [48, 7, 0], 128, ON, 48, seed=610, fa=E5, fb=E4)
+
+
+def test_grouped_moe_decode_shape():
+    G, M_max, N, K = 8, 128, 4096, 7168
+    mm = [3, 64, 0, 17, 40, 1, 8, 128]
+    grouped_bs_case(G, M_max, N, K, mm, 128, AUTO, 0, seed=620)
+
+
+# ---- host-side argument checks (no kernel runs) -------------------------------------
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def test_argument_errors():
+    lib = _lib.load()
+    A = torch.zeros((64, 256), dtype=torch.uint8, device="cuda")
+    B = torch.zeros((48, 256), dtype=torch.uint8, device="cuda")
+    D = torch.zeros((64, 48), dtype=torch.bfloat16, device="cuda")
+    s = torch.full((4096,), 127, dtype=torch.uint8, device="cuda")
+
+    def call(sa, lda, sb, ldb, gran):
+        return lib.fp8_gemm_nt_blockscaled(_ptr(A), _ptr(B), _ptr(D), 64, 48, 256, 0, 0, sa, lda, sb, ldb,
+                                           gran, 0, None)
+    assert call(_ptr(s), 64, _ptr(s), 48, 128) == fp8g.OK
+    assert call(_ptr(s), 64, _ptr(s), 48, 32) == fp8g.OK
+    assert call(None, 64, _ptr(s), 48, 128) == fp8g.ERR_INVALID_ARG
+    assert call(_ptr(s), 64, None, 48, 128) == fp8g.ERR_INVALID_ARG
+    assert call(_ptr(s), 64, _ptr(s), 48, 64) == fp8g.ERR_INVALID_ARG
+    assert call(_ptr(s), 48, _ptr(s), 48, 128) == fp8g.ERR_INVALID_ARG      # lda < M
+    assert call(_ptr(s), 64, _ptr(s), 32, 128) == fp8g.ERR_INVALID_ARG      # ldb < N
+    assert call(_ptr(s), 72, _ptr(s), 48, 128) == fp8g.ERR_MISALIGNED       # lda % 16
+    off = ctypes.c_void_p(s.data_ptr() + 8)
+    assert call(off, 64, _ptr(s), 48, 128) == fp8g.ERR_MISALIGNED
+    torch.cuda.synchronize()
+    assert_status_ok()
+    with pytest.raises(ValueError):
+        fp8g.fp8_gemm_nt_blockscaled(A, B, s[:128].view(2, 64), s[:96].view(2, 48), a_dtype=E4, b_dtype=E4,
+                                     sf_group_k=32)
