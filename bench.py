@@ -57,13 +57,33 @@ class Workload:
         return 2.0 * float(sum(masked_m)) * self.N * self.K
 
     def bytes(self, masked_m=None):
+        ks = -(-self.K // self.gran) if self.gran else 0      # block-scale bytes per row
         if self.kind == "dense":
-            return float(self.M * self.K + self.N * self.K + 2 * self.M * self.N)
+            return float(self.M * (self.K + ks) + self.N * (self.K + ks) + 2 * self.M * self.N)
         live = [m for m in masked_m if m > 0]
-        return float(len(live) * self.N * self.K + sum(live) * self.K + 2 * sum(live) * self.N)
+        return float(len(live) * self.N * (self.K + ks) + sum(live) * (self.K + ks) + 2 * sum(live) * self.N)
 
 
 def make_workload(name: str, rank: int = 0) -> Workload:
+    """A workload by name; a trailing ":bs" (":bs32") adds UE8M0 block scales
+    per row per 128 (32) K elements: per-token scales for A, 128x128-block
+    weight scales for B (each block's scale repeated over its rows)."""
+    gran = 0
+    if name.endswith(":bs") or name.endswith(":bs32"):
+        base, tag = name.rsplit(":", 1)
+        gran = 128 if tag == "bs" else 32
+        w = _make_base_workload(base, rank)
+        w.name, w.gran = name, gran
+        w.desc += ", block-scaled (UE8M0, 1x%d tokens, %s weights)" % (gran, "128x128" if gran == 128 else "1x32")
+        if w.kind == "dense" and w.M > 128 and (w.flags & 3) != 1:
+            w.kernel = "k_gemm_mn"
+        return w
+    w = _make_base_workload(name, rank)
+    w.gran = gran
+    return w
+
+
+def _make_base_workload(name: str, rank: int = 0) -> Workload:
     import synth
     if name == "dense4096":
         return Workload(name, "dense", "dense GEMM M=N=K=4096, A,B E4M3 from N(0,1), FP32 accumulate, BF16 out",
@@ -112,11 +132,36 @@ def host_inputs(w: Workload):
         else:
             A = synth.normal_fp8((w.M, w.K), w.seed, 0.0, w.std, w.fa)
             B = synth.normal_fp8((w.N, w.K), w.seed + 100, 0.0, w.std, w.fb)
-        return {"A": A, "B": B}
-    A = synth.normal_fp8((w.G, w.M_max, w.K), w.seed, 0.0, w.std, w.fa)
-    B = synth.normal_fp8((w.G, w.N, w.K), w.seed + 100, 0.0, w.std, w.fb)
-    mm = synth.uniform_int(w.G, w.seed + 200, 0, 32).astype(np.int32)
-    return {"A": A, "B": B, "masked_m": mm}
+        out = {"A": A, "B": B}
+    else:
+        A = synth.normal_fp8((w.G, w.M_max, w.K), w.seed, 0.0, w.std, w.fa)
+        B = synth.normal_fp8((w.G, w.N, w.K), w.seed + 100, 0.0, w.std, w.fb)
+        mm = synth.uniform_int(w.G, w.seed + 200, 0, 32).astype(np.int32)
+        out = {"A": A, "B": B, "masked_m": mm}
+    if w.gran:
+        out.update(block_scales(w))
+    return out
+
+
+def block_scales(w: Workload):
+    """Seeded UE8M0 codes in [120, 134]: sf_a [G, ks, lda] one per token row
+    per K group; sf_b [G, ks, ldb] one per 128x128 weight block (gran 128) or
+    per row per 32 K elements (gran 32), repeated over the block's rows."""
+    import numpy as np
+    import synth
+    G = 1 if w.kind == "dense" else w.G
+    rows = w.M if w.kind == "dense" else w.M_max
+    ks = -(-w.K // w.gran)
+    lda, ldb = -(-rows // 16) * 16, -(-w.N // 16) * 16
+    sfa = synth.uniform_int(G * ks * lda, w.seed + 300, 120, 134).astype(np.uint8).reshape(G, ks, lda)
+    if w.gran == 128:
+        nb = -(-w.N // 128)
+        blk = synth.uniform_int(G * ks * nb, w.seed + 301, 120, 134).astype(np.uint8).reshape(G, ks, nb)
+        sfb = np.zeros((G, ks, ldb), np.uint8)
+        sfb[:, :, :w.N] = np.repeat(blk, 128, axis=2)[:, :, :w.N]
+    else:
+        sfb = synth.uniform_int(G * ks * ldb, w.seed + 301, 120, 134).astype(np.uint8).reshape(G, ks, ldb)
+    return {"sf_a": sfa, "sf_b": sfb}
 
 
 # ---------------------------------------------------------------------------
@@ -260,7 +305,11 @@ def oracle_sample(w: Workload, inp, budget_s: float, min_rows: int = 1):
         while r0 < w.M:
             r1 = min(w.M, r0 + rows)
             t = time.perf_counter()
-            oracle.gemm_nt(A[r0:r1], B, w.fa, w.fb)
+            if w.gran:
+                oracle.gemm_blockscaled(A[r0:r1], B, inp["sf_a"][0][:, r0:r1].copy(), inp["sf_b"][0], w.gran,
+                                        fa=w.fa, fb=w.fb)
+            else:
+                oracle.gemm_nt(A[r0:r1], B, w.fa, w.fb)
             dt = time.perf_counter() - t
             flops += 2.0 * (r1 - r0) * w.N * w.K
             r0 = r1
@@ -277,7 +326,11 @@ def oracle_sample(w: Workload, inp, budget_s: float, min_rows: int = 1):
         if mm[g] == 0:
             g_done += 1
             continue
-        oracle.gemm_grouped_masked(A[g:g + 1], B[g:g + 1], mm[g:g + 1], D0, w.fa, w.fb)
+        if w.gran:
+            oracle.gemm_blockscaled(A[g:g + 1], B[g:g + 1], inp["sf_a"][g:g + 1], inp["sf_b"][g:g + 1], w.gran,
+                                    masked_m=mm[g:g + 1], D_init=D0, fa=w.fa, fb=w.fb)
+        else:
+            oracle.gemm_grouped_masked(A[g:g + 1], B[g:g + 1], mm[g:g + 1], D0, w.fa, w.fb)
         flops += 2.0 * int(mm[g]) * w.N * w.K
         g_done += 1
         if time.perf_counter() - t_start >= budget_s:
@@ -354,8 +407,12 @@ def run_ours(args, w: Workload):
     sets = []
     A_h = torch.from_numpy(inp["A"]).pin_memory()
     B_h = torch.from_numpy(inp["B"]).pin_memory()
+    sfa_h = torch.from_numpy(inp["sf_a"]).pin_memory() if w.gran else None
+    sfb_h = torch.from_numpy(inp["sf_b"]).pin_memory() if w.gran else None
     for _ in range(n_sets):
         s = {"A": A_h.to(device), "B": B_h.to(device)}
+        if w.gran:
+            s["sfa"], s["sfb"] = sfa_h.to(device), sfb_h.to(device)
         if w.kind == "dense":
             s["D"] = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device)
         else:
@@ -364,14 +421,23 @@ def run_ours(args, w: Workload):
         sets.append(s)
     torch.cuda.synchronize(device)
 
-    def step_on(i, strm):
-        s = sets[i % n_sets]
-        if w.kind == "dense":
+    def call(s, strm):
+        if w.kind == "dense" and w.gran:
+            fp8g.fp8_gemm_nt_blockscaled(s["A"], s["B"], s["sfa"], s["sfb"], s["D"], sf_group_k=w.gran,
+                                         a_dtype=w.fa, b_dtype=w.fb, flags=w.flags, stream=strm)
+        elif w.kind == "dense":
             fp8g.fp8_gemm_nt(s["A"], s["B"], s["D"], a_dtype=w.fa, b_dtype=w.fb, flags=w.flags,
                              stream=strm)
+        elif w.gran:
+            fp8g.fp8_gemm_grouped_masked_blockscaled(s["A"], s["B"], s["mm"], s["sfa"], s["sfb"], s["D"],
+                                                     max_m_hint=w.hint, sf_group_k=w.gran, a_dtype=w.fa,
+                                                     b_dtype=w.fb, flags=w.flags, stream=strm)
         else:
             fp8g.fp8_gemm_grouped_masked(s["A"], s["B"], s["mm"], s["D"], max_m_hint=w.hint,
                                          a_dtype=w.fa, b_dtype=w.fb, flags=w.flags, stream=strm)
+
+    def step_on(i, strm):
+        call(sets[i % n_sets], strm)
 
     def step(i):
         step_on(i, stream)
@@ -453,13 +519,12 @@ def run_ours(args, w: Workload):
         def e2e_step():
             s0["A"].copy_(A_h, non_blocking=True)
             s0["B"].copy_(B_h, non_blocking=True)
+            if w.gran:
+                s0["sfa"].copy_(sfa_h, non_blocking=True)
+                s0["sfb"].copy_(sfb_h, non_blocking=True)
             if mm_h is not None:
                 s0["mm"].copy_(mm_h, non_blocking=True)
-                fp8g.fp8_gemm_grouped_masked(s0["A"], s0["B"], s0["mm"], s0["D"], max_m_hint=w.hint,
-                                             a_dtype=w.fa, b_dtype=w.fb, flags=w.flags, stream=stream)
-            else:
-                fp8g.fp8_gemm_nt(s0["A"], s0["B"], s0["D"], a_dtype=w.fa, b_dtype=w.fb,
-                                 flags=w.flags, stream=stream)
+            call(s0, stream)
             D_h.copy_(s0["D"], non_blocking=True)
 
         for _ in range(min(3, e2e_steps)):
@@ -474,6 +539,8 @@ def run_ours(args, w: Workload):
         torch.cuda.synchronize(device)
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
         h2d = A_h.numel() + B_h.numel() + (mm_h.numel() * 4 if mm_h is not None else 0)
+        if w.gran:
+            h2d += sfa_h.numel() + sfb_h.numel()
         d2h = D_h.numel() * 2
         e2e = {"value": world * e2e_steps * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps}
@@ -494,6 +561,7 @@ def run_ours(args, w: Workload):
     traffic = profiled_traffic(w.name)
     kernel_name = "k_gemm_swap" if (w.flags & 3) == 1 or (w.kind == "masked") else \
         ("k_gemm_mn2" if w.kind == "dense" and w.M > 128 and not (w.flags & 0x200) else "k_gemm_mn/k_gemm_swap (auto)")
+    kernel_name = getattr(w, "kernel", kernel_name)
     roof = {"bound": w.bound, "achieved": achieved, "peak": peak, "unit": unit,
             "frac": achieved / peak, "traffic": traffic, "kernel": kernel_name,
             "peak_basis": basis, "algorithmic_flop": flops, "algorithmic_bytes": algo_bytes,

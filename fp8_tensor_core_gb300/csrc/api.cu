@@ -333,17 +333,17 @@ int check_blockscales(const uint8_t *sf_a, int64_t sf_a_ld, const uint8_t *sf_b,
     return FP8G_OK;
 }
 
-// Stage size and TMEM-limited depth of a block-scaled launch whose MMA B side
-// has box_b rows: operand tiles, then the scale area (at args.sf_off), the
-// whole rounded up to 1024 bytes; scale sets after two accumulators of
-// box_b columns.
+// Stage layout of a block-scaled launch whose MMA B side has box_b rows:
+// operand tiles, then the scale area (at args.sf_off), the whole rounded up to
+// 1024 bytes.  TMEM: two accumulators of box_b columns, then as many scale
+// sets (up to kMaxSfSets) as the remaining columns hold.
 void plan_blockscaled(GemmArgs &args, const DeviceInfo &info, int box_b, int groups, uint32_t flags)
 {
     args.sf_off = kTileM * kBlockK + box_b * kBlockK;
-    args.stage_bytes = (args.sf_off + sf_stage_bytes(args.sf_k, box_b) + 1023) & ~1023;
+    args.stage_bytes = (args.sf_off + sf_stage_bytes(box_b) + 1023) & ~1023;
     args.sf_col0 = 2 * box_b;
+    args.sf_sets = std::min(kMaxSfSets, (kTmemCols - 2 * box_b) / sf_set_cols(box_b));
     args.stages = pick_stages(info, args.stage_bytes, groups, flags);
-    args.stages = std::min(args.stages, (kTmemCols - 2 * box_b) / sf_set_cols(box_b));
 }
 
 // Scale arguments: both pointers given (16-byte aligned device memory), each
@@ -456,9 +456,8 @@ int launch(const Problem &p, cudaStream_t stream)
             return FP8G_ERR_CUDA;
         if (p.sf_k) {
             // MMA side A = weights (B's scales), side B = tokens (A's scales).
-            if (!make_sf_map(&tm2, p.sf_b, p.N, ks, p.G, p.sf_b_ld, kTileM, static_cast<uint32_t>(p.sf_k)) ||
-                !make_sf_map(&tm3, p.sf_a, p.rows_a, ks, p.G, p.sf_a_ld, static_cast<uint32_t>(cap),
-                             static_cast<uint32_t>(p.sf_k)))
+            if (!make_sf_map(&tm2, p.sf_b, p.N, ks, p.G, p.sf_b_ld, kTileM, 4) ||
+                !make_sf_map(&tm3, p.sf_a, p.rows_a, ks, p.G, p.sf_a_ld, static_cast<uint32_t>(cap), 4))
                 return FP8G_ERR_CUDA;
         } else {
             tm2 = tm0;
@@ -528,9 +527,8 @@ int launch(const Problem &p, cudaStream_t stream)
         !make_map(&tm1, p.B, p.K, p.N, p.G, static_cast<uint32_t>(tile_n)))
         return FP8G_ERR_CUDA;
     if (p.sf_k) {
-        if (!make_sf_map(&tm2, p.sf_a, p.rows_a, ks, p.G, p.sf_a_ld, kTileM, static_cast<uint32_t>(p.sf_k)) ||
-            !make_sf_map(&tm3, p.sf_b, p.N, ks, p.G, p.sf_b_ld, static_cast<uint32_t>(tile_n),
-                         static_cast<uint32_t>(p.sf_k)))
+        if (!make_sf_map(&tm2, p.sf_a, p.rows_a, ks, p.G, p.sf_a_ld, kTileM, 4) ||
+            !make_sf_map(&tm3, p.sf_b, p.N, ks, p.G, p.sf_b_ld, static_cast<uint32_t>(tile_n), 4))
             return FP8G_ERR_CUDA;
     } else {
         tm2 = tm0;

@@ -61,6 +61,8 @@ struct alignas(16) SmemCtl {
     uint64_t tempty[2];
     uint64_t drain;
     uint64_t pair_exit;   // CTA-pair kernel: the peer's "done" arrival
+    uint64_t sfready[kMaxStages];   // block scales of stage s staged for tcgen05.cp
+    uint64_t sffree[kMaxSfSets];    // TMEM scale set no longer read by any MMA
     uint32_t tmem_base;
     volatile int32_t abort;
     int32_t units_total;
@@ -189,49 +191,89 @@ __device__ __forceinline__ float token_factor(const GemmArgs &a, int g, int m)
 // scale factor per row per 32 K elements, read from TMEM ("一次“转置”，半张算力：
 // DeepSeek SwapAB 漂流史" §3.4 shows the A- and B-side scale-factor columns).
 
-// Scale word of row `row` of a raw [sf_k][box] byte block as TMA wrote it:
-// byte i is the row's scale for K elements 32i..32i+31 of the 128-wide block
-// (one 128-element group: the same byte four times).
-__device__ __forceinline__ uint32_t sf_word(const uint8_t *raw, int sf_k, int box, int row)
+// A scale load brings four K groups per row (TMA box {rows, 4}), as bytes
+// [group][row].  With 128-element groups (sf_k = 1) one load serves four K
+// blocks: it rides with the stage of K block kb when kb is a multiple of 4 or
+// the first block of a run, and covers groups (kb & ~3) .. +3; the MMA of
+// block kb picks byte kb & 3.  With 32-element groups (sf_k = 4) every K block
+// loads groups 4kb .. 4kb+3 and its k-th MMA picks byte k.
+__device__ __forceinline__ bool sf_load_at(int kb, int kb_first, int sf_k)
 {
-    if (sf_k == 1)
-        return static_cast<uint32_t>(raw[row]) * 0x01010101u;
-    return static_cast<uint32_t>(raw[row]) | (static_cast<uint32_t>(raw[box + row]) << 8) |
-           (static_cast<uint32_t>(raw[2 * box + row]) << 16) | (static_cast<uint32_t>(raw[3 * box + row]) << 24);
+    return kb == kb_first || sf_k == 4 || (kb & 3) == 0;
 }
+__device__ __forceinline__ int sf_first_group(int kb, int sf_k) { return sf_k == 1 ? (kb & ~3) : 4 * kb; }
 
-// MMA warp, all lanes, after the stage's full barrier: rearrange the raw
-// scale bytes into tcgen05.cp sources (per 128 rows, 16-byte row r % 32,
-// word r / 32), then lane 0 copies them into the stage's TMEM scale set:
-// side A at set_tmem, side B at set_tmem + 4 (+4 per further 128 rows).
-// The copies are ordered before the MMAs lane 0 issues next.
-__device__ __forceinline__ void stage_scales(uint8_t *stage, const GemmArgs &a, int box_b, uint32_t set_tmem)
+// Scale-staging warp, all lanes, once the stage's full barrier has passed:
+// rearrange the raw bytes into tcgen05.cp sources -- per 128 rows, 16-byte
+// row r % 32, 32-bit word r / 32 holding the row's four K-group bytes.
+__device__ __forceinline__ void sf_transpose(uint8_t *stage, const GemmArgs &a, int box_b)
 {
     const int lane = threadIdx.x & 31;
-    const int sk = a.sf_k;
-    const uint8_t *raw_a = stage + a.sf_off;
-    const uint8_t *raw_b = raw_a + sk * kTileM;
-    uint8_t *src = stage + a.sf_off + sk * (kTileM + box_b);
-    *reinterpret_cast<uint4 *>(src + 16 * lane) =
-        make_uint4(sf_word(raw_a, sk, kTileM, lane), sf_word(raw_a, sk, kTileM, 32 + lane),
-                   sf_word(raw_a, sk, kTileM, 64 + lane), sf_word(raw_a, sk, kTileM, 96 + lane));
+    const uint8_t *raw_a = stage + a.sf_off;            // [4][128]
+    const uint8_t *raw_b = raw_a + 4 * kTileM;          // [4][box_b]
+    uint8_t *src = stage + a.sf_off + 4 * (kTileM + box_b);
+    auto word = [](const uint8_t *raw, int box, int r) {
+        return static_cast<uint32_t>(raw[r]) | (static_cast<uint32_t>(raw[box + r]) << 8) |
+               (static_cast<uint32_t>(raw[2 * box + r]) << 16) | (static_cast<uint32_t>(raw[3 * box + r]) << 24);
+    };
+    *reinterpret_cast<uint4 *>(src + 16 * lane) = make_uint4(
+        word(raw_a, kTileM, lane), word(raw_a, kTileM, 32 + lane), word(raw_a, kTileM, 64 + lane),
+        word(raw_a, kTileM, 96 + lane));
     const int nch = (box_b + 127) >> 7;
     for (int h = 0; h < nch; ++h) {
         uint32_t v[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int r = 128 * h + 32 * j + lane;
-            v[j] = r < box_b ? sf_word(raw_b, sk, box_b, r) : 0u;
+            v[j] = r < box_b ? word(raw_b, box_b, r) : 0u;
         }
         *reinterpret_cast<uint4 *>(src + 512 * (1 + h) + 16 * lane) = make_uint4(v[0], v[1], v[2], v[3]);
     }
     fence_proxy_async_smem();
     __syncwarp();
+}
+
+// MMA warp, all lanes, at a K block that carries scales: wait until the
+// staging warp has built this stage's copy sources, retire the previous TMEM
+// scale set (its last MMA is already issued), take the next one once its
+// previous use has completed, and (lane 0) copy the sources into it: side A
+// at the set's first column, side B 4 columns on (4 more per 128 rows).  The
+// copies are ordered before the MMAs lane 0 issues next.  Returns false when
+// a wait gave up.
+struct SfState {
+    int j;              // scale loads consumed so far - 1
+    uint32_t ready_par; // parity bit per stage of sfready
+};
+
+__device__ __forceinline__ bool sf_take(SmemCtl &ctl, const GemmArgs &a, SfState &st, int stage,
+                                        const uint8_t *stage_ptr, int box_b, uint32_t sets_tmem, int set_cols,
+                                        uint32_t &set_tmem)
+{
+    const int lane = threadIdx.x & 31;
+    if (!warp_wait(smem_addr(&ctl.sfready[stage]), (st.ready_par >> stage) & 1u, ctl, a.timeout_ns, kRoleMma,
+                   300 + stage))
+        return false;
+    st.ready_par ^= 1u << stage;
+    const int R = a.sf_sets;
+    if (st.j >= 0 && lane == 0)
+        mma_commit(smem_addr(&ctl.sffree[st.j % R]));
+    __syncwarp();
+    ++st.j;
+    const int set = st.j % R;
+    if (st.j >= R &&
+        !warp_wait(smem_addr(&ctl.sffree[set]), static_cast<uint32_t>((st.j / R - 1) & 1), ctl, a.timeout_ns,
+                   kRoleMma, 400 + set))
+        return false;
+    tc_fence_after();
+    set_tmem = sets_tmem + static_cast<uint32_t>(set * set_cols);
     if (lane == 0) {
+        const uint8_t *src = stage_ptr + a.sf_off + 4 * (kTileM + box_b);
         tmem_cp_32x128b_warpx4(set_tmem, smem_desc_rows16(smem_addr(src)));
+        const int nch = (box_b + 127) >> 7;
         for (int h = 0; h < nch; ++h)
             tmem_cp_32x128b_warpx4(set_tmem + 4u + 4u * h, smem_desc_rows16(smem_addr(src + 512 * (1 + h))));
     }
+    return true;
 }
 
 // Group table: valid rows per group (clamped to [0, rows_a]) and the
@@ -318,6 +360,10 @@ __device__ __forceinline__ void init_barriers(SmemCtl &ctl, int stages)
         mbar_init(smem_addr(&ctl.tempty[b]), 4 * 32);
     }
     mbar_init(smem_addr(&ctl.drain), 1);
+    for (int s = 0; s < stages; ++s)
+        mbar_init(smem_addr(&ctl.sfready[s]), 1);
+    for (int i = 0; i < kMaxSfSets; ++i)
+        mbar_init(smem_addr(&ctl.sffree[i]), 1);
     ctl.abort = 0;
     fence_mbar_init();
 }
@@ -376,7 +422,7 @@ __device__ __forceinline__ void mma_drain(SmemCtl &ctl, const GemmArgs &a, bool 
 // =====================================================================================
 // k_gemm_mn: tokens on M, weights on N.
 // =====================================================================================
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsScaled, 1)
     k_gemm_mn(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
               const __grid_constant__ CUtensorMap tm_sa, const __grid_constant__ CUtensorMap tm_sb,
               const GemmArgs a)
@@ -388,10 +434,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int n_tiles = ceil_div(a.n, a.tile_n);
     const uint32_t a_bytes = kTileM * kBlockK;                  // 16 KB A box
-    const uint32_t tx_bytes = a_bytes + static_cast<uint32_t>(a.tile_n) * kBlockK +
-                              static_cast<uint32_t>(a.sf_k * (kTileM + a.tile_n));
-    // Accumulator spacing in TMEM: 256 columns, or tile_n when the per-stage
-    // scale sets follow the two accumulators.
+    const uint32_t tx_bytes = a_bytes + static_cast<uint32_t>(a.tile_n) * kBlockK;
+    const uint32_t sf_bytes = 4u * static_cast<uint32_t>(kTileM + a.tile_n);
+    // Accumulator spacing in TMEM: 256 columns, or tile_n when the block-scale
+    // sets follow the two accumulators.
     const int acc_stride = a.sf_k ? a.tile_n : kAccStride;
     const int set_cols = sf_set_cols(a.tile_n);
 
@@ -458,13 +504,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0 && !(drop && issued == 0)) {
                     uint8_t *sa = sm.stages + static_cast<size_t>(stage) * a.stage_bytes;
                     const uint32_t fb = smem_addr(&ctl.full[stage]);
-                    mbar_arrive_expect_tx(fb, tx_bytes);
+                    const bool sf = a.sf_k && sf_load_at(kb, 0, a.sf_k);
+                    mbar_arrive_expect_tx(fb, tx_bytes + (sf ? sf_bytes : 0u));
                     tma_load_3d(smem_addr(sa), &tm_a, fb, kb * kBlockK, m0, g);
                     tma_load_3d(smem_addr(sa + a_bytes), &tm_b, fb, kb * kBlockK, n0, g);
-                    if (a.sf_k) {
-                        tma_load_3d(smem_addr(sa + a.sf_off), &tm_sa, fb, m0, kb * a.sf_k, g);
-                        tma_load_3d(smem_addr(sa + a.sf_off + a.sf_k * kTileM), &tm_sb, fb, n0,
-                                    kb * a.sf_k, g);
+                    if (sf) {
+                        const int y = sf_first_group(kb, a.sf_k);
+                        tma_load_3d(smem_addr(sa + a.sf_off), &tm_sa, fb, m0, y, g);
+                        tma_load_3d(smem_addr(sa + a.sf_off + 4 * kTileM), &tm_sb, fb, n0, y, g);
                     }
                 }
                 __syncwarp();
@@ -480,6 +527,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ----------------------------- MMA issuer -----------------------------
         const uint32_t idesc = make_idesc(a.a_fmt, a.b_fmt, kTileM, a.tile_n);
         const uint32_t idesc_bs = make_idesc_bs(a.a_fmt, a.b_fmt, kTileM, a.tile_n, 0);
+        const uint32_t sets_tmem = tmem_base + static_cast<uint32_t>(a.sf_col0);
+        SfState sfs{-1, 0u};
+        uint32_t set_tmem = sets_tmem;
         int stage = 0;
         uint32_t phase = 0;
         int acc = 0;
@@ -500,18 +550,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 if (a.sf_k) {
-                    uint8_t *sp = sm.stages + static_cast<size_t>(stage) * a.stage_bytes;
-                    const uint32_t set = tmem_base + static_cast<uint32_t>(a.sf_col0 + stage * set_cols);
-                    stage_scales(sp, a, a.tile_n, set);
+                    const uint8_t *sp = sm.stages + static_cast<size_t>(stage) * a.stage_bytes;
+                    if (sf_load_at(kb, 0, a.sf_k) &&
+                        !sf_take(ctl, a, sfs, stage, sp, a.tile_n, sets_tmem, set_cols, set_tmem)) {
+                        ok = false;
+                        break;
+                    }
                     if (lane == 0) {
                         const uint64_t adesc = smem_desc_k_sw128(smem_addr(sp));
                         const uint64_t bdesc = smem_desc_k_sw128(smem_addr(sp) + a_bytes);
 #pragma unroll
-                        for (int k = 0; k < kBlockK / 32; ++k)
-                            mma_f8f6f4_bs(d_tmem, adesc + 2u * k, bdesc + 2u * k,
-                                          idesc_bs | (static_cast<uint32_t>(k) << 4) |
-                                              (static_cast<uint32_t>(k) << 29),
-                                          set, set + 4u, (kb | k) != 0 ? 1u : 0u);
+                        for (int k = 0; k < kBlockK / 32; ++k) {
+                            const uint32_t id = a.sf_k == 1 ? static_cast<uint32_t>(kb & 3) : static_cast<uint32_t>(k);
+                            mma_f8f6f4_bs(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc_bs | (id << 4) | (id << 29),
+                                          set_tmem, set_tmem + 4u, (kb | k) != 0 ? 1u : 0u);
+                        }
                         mma_commit(smem_addr(&ctl.empty[stage]));
                     }
                 } else if (lane == 0) {
@@ -544,6 +597,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         mma_drain(ctl, a, issued_any);
+    } else if (warp == 6) {
+        // ------------------------- block-scale staging -------------------------
+        if (a.sf_k) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool stop = false;
+            for (int u = blockIdx.x; u < total && !stop; u += gridDim.x) {
+                for (int kb = 0; kb < a.num_kb; ++kb) {
+                    if (!warp_wait(smem_addr(&ctl.full[stage]), phase, ctl, a.timeout_ns, kRoleScales, stage)) {
+                        stop = true;
+                        break;
+                    }
+                    if (sf_load_at(kb, 0, a.sf_k)) {
+                        sf_transpose(sm.stages + static_cast<size_t>(stage) * a.stage_bytes, a, a.tile_n);
+                        if (lane == 0)
+                            mbar_arrive(smem_addr(&ctl.sfready[stage]));
+                    }
+                    if (++stage == a.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
     } else {
         // ------------------------------ epilogue ------------------------------
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
@@ -1035,7 +1112,7 @@ struct SwapWalker {
     bool first;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsScaled, 1)
     k_gemm_swap(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_t,
                 const __grid_constant__ CUtensorMap tm_sw, const __grid_constant__ CUtensorMap tm_st,
                 const GemmArgs a)
@@ -1153,8 +1230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         SwapWalker wk = make_walker();
         SwapSeg x;
         while (!aborted && next_seg(wk, x)) {
-            const uint32_t tx = w_bytes + static_cast<uint32_t>(x.n_mma) * kBlockK +
-                                static_cast<uint32_t>(a.sf_k * (kTileM + cap));
+            const uint32_t tx = w_bytes + static_cast<uint32_t>(x.n_mma) * kBlockK;
             for (int kb = x.kb0; kb < x.kb1; ++kb) {
                 if (!warp_wait(smem_addr(&ctl.empty[stage]), phase ^ 1u, ctl, a.timeout_ns,
                                kRoleLoader, stage)) {
@@ -1164,16 +1240,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0 && !(drop && issued == 0)) {
                     uint8_t *sw = sm.stages + static_cast<size_t>(stage) * a.stage_bytes;
                     const uint32_t fb = smem_addr(&ctl.full[stage]);
-                    mbar_arrive_expect_tx(fb, tx);
+                    const bool sf = a.sf_k && sf_load_at(kb, x.kb0, a.sf_k);
+                    mbar_arrive_expect_tx(fb, tx + (sf ? 4u * static_cast<uint32_t>(kTileM + cap) : 0u));
                     tma_load_3d_hint(smem_addr(sw), &tm_w, fb, kb * kBlockK, x.w0, x.g, w_policy);
                     for (int r = 0; r < x.n_mma; r += kTokBox)
                         tma_load_3d(smem_addr(sw + w_bytes + (r / kTokBox) * kTokBoxBytes), &tm_t, fb,
                                     kb * kBlockK, x.tok0 + r, x.g);
-                    if (a.sf_k) {
-                        tma_load_3d_hint(smem_addr(sw + a.sf_off), &tm_sw, fb, x.w0, kb * a.sf_k, x.g,
-                                         w_policy);
-                        tma_load_3d(smem_addr(sw + a.sf_off + a.sf_k * kTileM), &tm_st, fb, x.tok0,
-                                    kb * a.sf_k, x.g);
+                    if (sf) {
+                        const int y = sf_first_group(kb, a.sf_k);
+                        tma_load_3d_hint(smem_addr(sw + a.sf_off), &tm_sw, fb, x.w0, y, x.g, w_policy);
+                        tma_load_3d(smem_addr(sw + a.sf_off + 4 * kTileM), &tm_st, fb, x.tok0, y, x.g);
                     }
                 }
                 __syncwarp();
@@ -1194,6 +1270,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         bool issued_any = false;
+        const uint32_t sets_tmem = tmem_base + static_cast<uint32_t>(a.sf_col0);
+        SfState sfs{-1, 0u};
+        uint32_t set_tmem = sets_tmem;
         SwapWalker wk = make_walker();
         SwapSeg x;
         while (next_seg(wk, x)) {
@@ -1213,18 +1292,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 if (a.sf_k) {
-                    uint8_t *sp = sm.stages + static_cast<size_t>(stage) * a.stage_bytes;
-                    const uint32_t set = tmem_base + static_cast<uint32_t>(a.sf_col0 + stage * set_cols);
-                    stage_scales(sp, a, cap, set);
+                    const uint8_t *sp = sm.stages + static_cast<size_t>(stage) * a.stage_bytes;
+                    if (sf_load_at(kb, x.kb0, a.sf_k) &&
+                        !sf_take(ctl, a, sfs, stage, sp, cap, sets_tmem, set_cols, set_tmem)) {
+                        ok = false;
+                        break;
+                    }
                     if (lane == 0) {
                         const uint64_t wdesc = smem_desc_k_sw128(smem_addr(sp));
                         const uint64_t tdesc = smem_desc_k_sw128(smem_addr(sp) + w_bytes);
 #pragma unroll
-                        for (int k = 0; k < kBlockK / 32; ++k)
-                            mma_f8f6f4_bs(d_tmem, wdesc + 2u * k, tdesc + 2u * k,
-                                          idesc_bs | (static_cast<uint32_t>(k) << 4) |
-                                              (static_cast<uint32_t>(k) << 29),
-                                          set, set + 4u, (kb != x.kb0 || k != 0) ? 1u : 0u);
+                        for (int k = 0; k < kBlockK / 32; ++k) {
+                            const uint32_t id = a.sf_k == 1 ? static_cast<uint32_t>(kb & 3) : static_cast<uint32_t>(k);
+                            mma_f8f6f4_bs(d_tmem, wdesc + 2u * k, tdesc + 2u * k, idesc_bs | (id << 4) | (id << 29),
+                                          set_tmem, set_tmem + 4u, (kb != x.kb0 || k != 0) ? 1u : 0u);
+                        }
                         mma_commit(smem_addr(&ctl.empty[stage]));
                     }
                 } else if (lane == 0) {
@@ -1255,6 +1337,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         mma_drain(ctl, a, issued_any);
+    } else if (warp == 6) {
+        // ------------------------- block-scale staging -------------------------
+        if (a.sf_k) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool stop = false;
+            SwapWalker wk = make_walker();
+            SwapSeg x;
+            while (!stop && next_seg(wk, x)) {
+                for (int kb = x.kb0; kb < x.kb1; ++kb) {
+                    if (!warp_wait(smem_addr(&ctl.full[stage]), phase, ctl, a.timeout_ns, kRoleScales, stage)) {
+                        stop = true;
+                        break;
+                    }
+                    if (sf_load_at(kb, x.kb0, a.sf_k)) {
+                        sf_transpose(sm.stages + static_cast<size_t>(stage) * a.stage_bytes, a, cap);
+                        if (lane == 0)
+                            mbar_arrive(smem_addr(&ctl.sfready[stage]));
+                    }
+                    if (++stage == a.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
     } else {
         // ------------------------------ epilogue ------------------------------
         // Thread = weight row n (TMEM lane), registers = tokens (TMEM columns).
@@ -1398,12 +1506,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // kernel may start while the previous launch in the stream finishes; it
 // waits (griddepcontrol.wait) before touching global memory.
 template <typename Kernel, typename... Maps>
-static cudaError_t launch_pdl(Kernel kernel, int grid, size_t smem, cudaStream_t stream,
+static cudaError_t launch_pdl(Kernel kernel, int threads, int grid, size_t smem, cudaStream_t stream,
                               const GemmArgs &args, const Maps &...maps)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1427,7 +1535,7 @@ cudaError_t launch_gemm_mn(const CUtensorMap &tm_a, const CUtensorMap &tm_b, con
                                          static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(k_gemm_mn, grid, smem, stream, args, tm_a, tm_b, tm_sa, tm_sb);
+    return launch_pdl(k_gemm_mn, kThreadsScaled, grid, smem, stream, args, tm_a, tm_b, tm_sa, tm_sb);
 }
 
 cudaError_t launch_gemm_mn2(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const GemmArgs &args,
@@ -1440,7 +1548,7 @@ cudaError_t launch_gemm_mn2(const CUtensorMap &tm_a, const CUtensorMap &tm_b, co
                                          static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(k_gemm_mn2, grid, smem, stream, args, tm_a, tm_b);
+    return launch_pdl(k_gemm_mn2, kThreads, grid, smem, stream, args, tm_a, tm_b);
 }
 
 cudaError_t launch_gemm_swap(const CUtensorMap &tm_w, const CUtensorMap &tm_t, const CUtensorMap &tm_sw,
@@ -1453,7 +1561,7 @@ cudaError_t launch_gemm_swap(const CUtensorMap &tm_w, const CUtensorMap &tm_t, c
                                          static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(k_gemm_swap, grid, smem, stream, args, tm_w, tm_t, tm_sw, tm_st);
+    return launch_pdl(k_gemm_swap, kThreadsScaled, grid, smem, stream, args, tm_w, tm_t, tm_sw, tm_st);
 }
 
 cudaError_t read_and_clear_status(int32_t info[4])

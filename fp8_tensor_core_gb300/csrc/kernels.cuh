@@ -13,9 +13,11 @@ constexpr int kTileM = 128;          // MMA M: rows of the operand on the M side
 constexpr int kMaxStages = 16;
 constexpr int kMaxGroups = 1024;
 constexpr int kThreads = 192;        // warp 0 loader, warp 1 MMA issuer, warps 2-5 epilogue
+constexpr int kThreadsScaled = 224;  // single-SM and SwapAB kernels: + warp 6, block-scale staging
+constexpr int kMaxSfSets = 4;        // TMEM block-scale sets in flight
 constexpr int kTmemCols = 512;       // two accumulators of up to 256 columns
 constexpr int kAccStride = 256;
-constexpr int kCtlFixedBytes = 512;  // barriers, TMEM slot, flags
+constexpr int kCtlFixedBytes = 768;  // barriers, TMEM slot, flags
 constexpr int kSmemAlignPad = 1024;  // dynamic smem base rounded up to 1024 B
 
 // Control block: fixed part plus two int32 tables per group (unit prefix,
@@ -27,7 +29,7 @@ inline int ctl_bytes_for(int groups)
 }
 
 // Roles recorded in the device status word.
-enum Role : int { kRoleLoader = 0, kRoleMma = 1, kRoleEpilogue = 2, kRoleScheduler = 3 };
+enum Role : int { kRoleLoader = 0, kRoleMma = 1, kRoleEpilogue = 2, kRoleScheduler = 3, kRoleScales = 4 };
 
 struct GemmArgs {
     // Problem.  Token operand A is [groups, rows_a, k]; weight operand B is
@@ -59,12 +61,14 @@ struct GemmArgs {
     const float *scale_b;
     int32_t sa_per_row;
     int32_t sb_per_col;
-    // Block scales (UE8M0, one byte per row per K group), loaded by TMA with
-    // each stage.  sf_k = 0: none; else scale bytes per row per 128-wide K
-    // block (1: groups of 128 elements, 4: groups of 32).
+    // Block scales (UE8M0, one byte per row per K group).  sf_k = 0: none;
+    // else K groups per 128-wide K block (1: groups of 128 elements, 4:
+    // groups of 32).  Every load brings 4 groups per row (4 K blocks' worth
+    // for sf_k = 1, one K block's for sf_k = 4) into the stage it rides with.
     int32_t sf_k;
     int32_t sf_off;            // byte offset of the scale area inside a stage
-    int32_t sf_col0;           // first TMEM column of the per-stage scale sets
+    int32_t sf_col0;           // first TMEM column of the block-scale sets
+    int32_t sf_sets;           // TMEM block-scale sets (2..kMaxSfSets)
     float *workspace;          // swap kernel, stream-K: 2 FP32 partial tiles per CTA
                                // (128 x tile_n floats each)
     int32_t *counters;         // swap kernel, stream-K: arrivals per (tile, epilogue warp),
@@ -73,12 +77,12 @@ struct GemmArgs {
 
 // Block-scaled stage layout.  After the two operand tiles (MMA side A: 128
 // rows; side B: box_b rows) a stage holds the raw scale bytes as TMA writes
-// them ([sf_k][128] then [sf_k][box_b]) and the tcgen05.cp sources built
-// from them (512 bytes per 128 rows).  In TMEM each stage owns a scale set
-// of 4 columns for side A and 4 per 128 rows of side B.
-inline int sf_stage_bytes(int sf_k, int box_b)
+// them ([4][128] then [4][box_b]: four K groups per row) and the tcgen05.cp
+// sources built from them (512 bytes per 128 rows).  A TMEM scale set has 4
+// columns for side A and 4 per 128 rows of side B.
+inline int sf_stage_bytes(int box_b)
 {
-    return sf_k * (kTileM + box_b) + 512 * (1 + (box_b + 127) / 128);
+    return 4 * (kTileM + box_b) + 512 * (1 + (box_b + 127) / 128);
 }
 __host__ __device__ inline int sf_set_cols(int box_b) { return 4 + 4 * ((box_b + 127) / 128); }
 

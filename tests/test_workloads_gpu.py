@@ -105,3 +105,54 @@ def test_small_m_every_element(name):
     ref, absdot = oracle.gemm_nt(inp["A"], inp["B"], w.fa, w.fb)
     ok, rep = oracle.check_bf16(got, ref, absdot)
     assert ok, rep
+
+
+BLOCKSCALED = ["dense4096:bs", "masked:bs", "masked:bs32", "smallm:16:7168:16384:auto:bs",
+               "smallm:64:24576:1536:auto:bs32", "proj:7168:2048:bs"]
+
+
+@pytest.mark.parametrize("name", BLOCKSCALED)
+def test_blockscaled_workload(name):
+    """Block-scaled workloads with the bench's recipes and flags: every
+    element (sampled rows and elements for the M=8192 projection), padding
+    rows of the masked output untouched."""
+    w = bench.make_workload(name)
+    inp = bench.host_inputs(w)
+    sfa, sfb = torch.from_numpy(inp["sf_a"]).cuda(), torch.from_numpy(inp["sf_b"]).cuda()
+    A, B = torch.from_numpy(inp["A"]).cuda(), torch.from_numpy(inp["B"]).cuda()
+    if w.kind == "dense":
+        D = fp8g.fp8_gemm_nt_blockscaled(A, B, sfa, sfb, sf_group_k=w.gran, a_dtype=w.fa, b_dtype=w.fb,
+                                         flags=w.flags)
+        torch.cuda.synchronize()
+        st = fp8g.fp8g_get_device_status()
+        assert st[0] == fp8g.OK, st
+        got = bits(D)
+        if w.M > 4096:
+            rng = np.random.default_rng(zlib.crc32(name.encode()))
+            rows = np.unique(np.concatenate([[0, 127, 128, w.M - 1], rng.integers(0, w.M, 3)]))
+            ref, absdot = oracle.gemm_blockscaled(inp["A"][rows], inp["B"], inp["sf_a"][0][:, rows].copy(),
+                                                  inp["sf_b"][0], w.gran, fa=w.fa, fb=w.fb)
+            got = got[rows]
+        else:
+            ref, absdot = oracle.gemm_blockscaled(inp["A"], inp["B"], inp["sf_a"][0], inp["sf_b"][0], w.gran,
+                                                  fa=w.fa, fb=w.fb)
+        ok, rep = oracle.check_bf16(got, ref, absdot)
+        assert ok, rep
+        return
+    mm = inp["masked_m"]
+    D0 = np.full((w.G, w.M_max, w.N), 0x7FC3, np.uint16)
+    Dt = torch.from_numpy(D0.view(np.int16)).cuda().view(torch.bfloat16)
+    fp8g.fp8_gemm_grouped_masked_blockscaled(A, B, torch.from_numpy(mm).cuda(), sfa, sfb, D=Dt,
+                                             max_m_hint=w.hint, sf_group_k=w.gran, a_dtype=w.fa, b_dtype=w.fb,
+                                             flags=w.flags)
+    torch.cuda.synchronize()
+    st = fp8g.fp8g_get_device_status()
+    assert st[0] == fp8g.OK, st
+    got = bits(Dt)
+    ref, absdot = oracle.gemm_blockscaled(inp["A"], inp["B"], inp["sf_a"], inp["sf_b"], w.gran, masked_m=mm,
+                                          D_init=D0, fa=w.fa, fb=w.fb)
+    for g in range(w.G):
+        m = int(mm[g])
+        ok, rep = oracle.check_bf16(got[g, :m], ref[g, :m], absdot[g, :m])
+        assert ok, (g, rep)
+        assert np.array_equal(got[g, m:], D0[g, m:]), "padding rows of group %d written" % g
