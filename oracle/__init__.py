@@ -18,6 +18,9 @@ What it computes, with its sources:
 * ``gemm_grouped_masked`` -- the masked grouped variant: only rows
   m < masked_m[g] of each group are computed or written ("一次“转置”，半张
   算力：DeepSeek SwapAB 漂流史", §3.1 and §3.3, valid_m).
+* ``epilogue`` -- round_mode(act(alpha*S + beta*C + bias)) of exact sums S,
+  BF16 rounding to nearest even / toward zero / toward +inf / toward -inf
+  (DeepGEMM page §3.3: fused alpha, beta, bias, ReLU and rounding mode).
 * ``gemm_blockscaled`` -- every product scaled by the UE8M0 factors of its
   K group (32 or 128 elements) for its A row and B row, then summed and
   rounded once (DeepGEMM page §5.2 per-128-element groups, UE8M0 scales in
@@ -115,7 +118,13 @@ def _load():
         lib.oracle_gemm_blockscaled.restype = None
         lib.oracle_gemm_blockscaled.argtypes = [
             _u8p, _u8p, _i32p, _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _u8p, _i64,
-            _u8p, _i64, _i64, _u16p, _f64p, ctypes.c_int]
+            _u8p, _i64, _i64, _u16p, _f64p, _f64p, ctypes.c_int]
+        lib.oracle_round_bf16_mode.restype = ctypes.c_uint16
+        lib.oracle_round_bf16_mode.argtypes = [ctypes.c_double, ctypes.c_int]
+        lib.oracle_epilogue.restype = None
+        lib.oracle_epilogue.argtypes = [_f64p, _f64p, _i64, _i64, _i64, _i32p, ctypes.c_double,
+                                        ctypes.c_double, _u16p, _f32p, ctypes.c_int, ctypes.c_int,
+                                        _u16p, _f64p]
         _lib = lib
         return lib
 
@@ -280,12 +289,12 @@ def gemm_grouped_masked_scaled(A: np.ndarray, B: np.ndarray, masked_m: np.ndarra
 
 def gemm_blockscaled(A: np.ndarray, B: np.ndarray, sfa: np.ndarray, sfb: np.ndarray,
                      gran: int = 128, masked_m=None, D_init=None, fa: int = E4M3, fb: int = E4M3,
-                     nthreads: int = 0):
+                     nthreads: int = 0, want_exact: bool = False):
     """Block-scaled oracle.  Dense: A [M,K], B [N,K], sfa [KS,lda], sfb
     [KS,ldb] uint8 UE8M0 codes (KS = ceil(K/gran), row m of A scaled by
     sfa[k // gran, m]).  Grouped: A [G,M_max,K], B [G,N,K], sfa [G,KS,lda],
     sfb [G,KS,ldb], masked_m [G] (rows m >= masked_m[g] keep D_init's bits).
-    Returns (D_bf16, absdot)."""
+    Returns (D_bf16, absdot[, exact sums])."""
     dense = np.ndim(A) == 2
     A3 = np.ascontiguousarray(A, np.uint8).reshape((1,) + np.shape(A) if dense else np.shape(A))
     B3 = np.ascontiguousarray(B, np.uint8).reshape((1,) + np.shape(B) if dense else np.shape(B))
@@ -308,12 +317,47 @@ def gemm_blockscaled(A: np.ndarray, B: np.ndarray, sfa: np.ndarray, sfb: np.ndar
     else:
         D = np.array(D_init, np.uint16, copy=True, order="C").reshape(G, M_max, N)
     absdot = np.zeros((G, M_max, N), np.float64)
+    exact = np.zeros((G, M_max, N), np.float64)
     _load().oracle_gemm_blockscaled(_ptr(A3, _u8p), _ptr(B3, _u8p), mm_p, G, M_max, N, K, fa, fb,
                                     _ptr(SA, _u8p), lda, _ptr(SB, _u8p), ldb, gran, _ptr(D, _u16p),
-                                    _ptr(absdot, _f64p), int(nthreads))
+                                    _ptr(exact, _f64p), _ptr(absdot, _f64p), int(nthreads))
+    out = (D, absdot, exact)
     if dense:
-        return D[0], absdot[0]
-    return D, absdot
+        out = tuple(x[0] for x in out)
+    return out if want_exact else out[:2]
+
+
+ROUND_RN, ROUND_RZ, ROUND_RU, ROUND_RD = 0, 1, 2, 3
+
+
+def round_bf16_mode(x: float, mode: int) -> int:
+    """BF16 code of x rounded in direction `mode` (0 nearest-even, 1 toward
+    zero, 2 toward +inf, 3 toward -inf)."""
+    return int(_load().oracle_round_bf16_mode(float(x), int(mode)))
+
+
+def epilogue(S: np.ndarray, absS: np.ndarray, alpha: float = 1.0, beta: float = 0.0, C=None, bias=None,
+             relu: bool = False, mode: int = ROUND_RN, masked_m=None, D_init=None):
+    """Fused-epilogue oracle: round_mode(act(alpha*S + beta*C + bias[g, n]))
+    per element.  S, absS: exact sums and sum|terms| shaped [M,N] or
+    [G,M_max,N]; C: BF16 codes shaped like S (or None); bias: float32 [N] or
+    [G,N] (or None); masked rows keep D_init's bits.  Returns (D, absdot)."""
+    S = np.ascontiguousarray(S, np.float64)
+    absS = np.ascontiguousarray(absS, np.float64)
+    shape = S.shape
+    S3 = S.reshape((1,) + shape if S.ndim == 2 else shape)
+    G, M_max, N = S3.shape
+    Cc = None if C is None else np.ascontiguousarray(C, np.uint16).reshape(S3.shape)
+    bb = None if bias is None else np.ascontiguousarray(bias, np.float32).reshape(G, N)
+    mm = None if masked_m is None else np.ascontiguousarray(masked_m, np.int32)
+    D = (np.zeros(S3.shape, np.uint16) if D_init is None
+         else np.array(D_init, np.uint16, copy=True, order="C").reshape(S3.shape))
+    absdot = np.zeros(S3.shape, np.float64)
+    _load().oracle_epilogue(_ptr(S3, _f64p), _ptr(absS.reshape(S3.shape), _f64p), G * M_max, M_max, N,
+                            _ptr(mm, _i32p), float(alpha), float(beta), _ptr(Cc, _u16p),
+                            _ptr(bb, ctypes.POINTER(ctypes.c_float)), 1 if relu else 0, int(mode),
+                            _ptr(D, _u16p), _ptr(absdot, _f64p))
+    return D.reshape(shape), absdot.reshape(shape)
 
 
 # ---- acceptance rule -------------------------------------------------------

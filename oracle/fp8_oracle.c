@@ -13,6 +13,9 @@
  *   block-scaled  every product a_k b_k multiplied by the UE8M0 scales of
  *           the K group (of 32 or 128 elements) that k falls in, for its
  *           row of A and its row of B, before the sum.
+ *   epilogue  round_mode(act(alpha * S + beta * C + bias)) of any of the
+ *           above sums S, with BF16 rounding to nearest even, toward zero,
+ *           toward +infinity or toward -infinity.
  *
  * Sources:
  *  - "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践"
@@ -124,6 +127,50 @@ uint16_t oracle_round_bf16(double x)
         return sign | (uint16_t)f;
     if (E > 127)
         return sign | 0x7F80;     /* overflow                            */
+    return sign | (uint16_t)(((E + 127) << 7) | ((int)f - 128));
+}
+
+/* Round a double to BF16 with a given rounding direction: 0 nearest-even
+ * (as above), 1 toward zero, 2 toward +infinity, 3 toward -infinity.  Same
+ * construction: the quotient by the binade's spacing is truncated, then
+ * bumped by one unit when the direction asks for it; a finite value beyond
+ * the largest BF16 goes to infinity only when rounding away from zero in its
+ * direction, otherwise to the largest finite value (IEEE 754 directed
+ * rounding). */
+uint16_t oracle_round_bf16_mode(double x, int mode)
+{
+    if (mode == 0)
+        return oracle_round_bf16(x);
+    if (isnan(x))
+        return 0x7FC0;
+    int neg = signbit(x) ? 1 : 0;
+    uint16_t sign = neg ? 0x8000 : 0;
+    double a = fabs(x);
+    if (a == 0.0)
+        return sign;
+    if (isinf(a))
+        return sign | 0x7F80;
+    int e2;
+    (void)frexp(a, &e2);
+    int E = e2 - 1;
+    if (E < -126)
+        E = -126;
+    double spacing = ldexp(1.0, E - 7);
+    double q = a / spacing;
+    double f = floor(q);
+    int inexact = (q - f) != 0.0;
+    /* away from zero: toward +inf for positives, toward -inf for negatives */
+    int away = (mode == 2 && !neg) || (mode == 3 && neg);
+    if (inexact && away)
+        f += 1.0;
+    if (f >= 256.0) {
+        f = 128.0;
+        E += 1;
+    }
+    if (f < 128.0)
+        return sign | (uint16_t)f;
+    if (E > 127)
+        return away ? (uint16_t)(sign | 0x7F80) : (uint16_t)(sign | 0x7F7F);
     return sign | (uint16_t)(((E + 127) << 7) | ((int)f - 128));
 }
 
@@ -434,6 +481,7 @@ typedef struct {
     int64_t G, M_max, N, K, lda, ldb, gran, KS;
     double ta[256], tb[256];
     uint16_t *D;
+    double *exact;     /* sums before rounding, may be NULL */
     double *absdot;
 } bs_ctx;
 
@@ -460,6 +508,8 @@ static void blockscaled_row(void *vctx, int64_t gm)
         }
         int64_t o = (g * c->M_max + m) * c->N + n;
         c->D[o] = oracle_round_bf16(s);
+        if (c->exact)
+            c->exact[o] = s;
         if (c->absdot)
             c->absdot[o] = ad;
     }
@@ -470,7 +520,7 @@ static void blockscaled_row(void *vctx, int64_t gm)
 void oracle_gemm_blockscaled(const uint8_t *A, const uint8_t *B, const int32_t *masked_m,
                              int64_t G, int64_t M_max, int64_t N, int64_t K, int fa, int fb,
                              const uint8_t *SA, int64_t lda, const uint8_t *SB, int64_t ldb,
-                             int64_t gran, uint16_t *D, double *absdot, int nthreads)
+                             int64_t gran, uint16_t *D, double *exact, double *absdot, int nthreads)
 {
     bs_ctx c;
     c.A = A;
@@ -489,6 +539,43 @@ void oracle_gemm_blockscaled(const uint8_t *A, const uint8_t *B, const int32_t *
     oracle_decode_table(fa, c.ta);
     oracle_decode_table(fb, c.tb);
     c.D = D;
+    c.exact = exact;
     c.absdot = absdot;
     run_rows(blockscaled_row, &c, G * M_max, nthreads);
+}
+
+/* ---- fused epilogue ----------------------------------------------------------
+ * "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践" §3.3: the
+ * epilogue computes C = alpha * A B + beta * C + bias (bias per output
+ * channel) with an optional ReLU inside the GEMM, and the final rounding may
+ * be to nearest even, toward zero or toward +infinity.  Reading: for each
+ * output element with product value S (the exact sum, already multiplied by
+ * any output or block scales),
+ *     out = round_mode( act( alpha * S + beta * C[row, n] + bias[group, n] ) )
+ * with C a BF16 array shaped like D (NULL: the term is absent), bias FP32
+ * [groups][N] (NULL: absent), act 0 = none, 1 = ReLU (x < 0 becomes +0; NaN
+ * stays NaN), evaluated in double and rounded once.  Row r belongs to group
+ * r / rows_per_group; with masked_m (NULL: every row) rows at or beyond
+ * masked_m[group] keep D's bits.  absdot receives
+ * |alpha| * absS + |beta * C| + |bias|. */
+void oracle_epilogue(const double *S, const double *absS, int64_t rows, int64_t rows_per_group,
+                     int64_t N, const int32_t *masked_m, double alpha, double beta, const uint16_t *C,
+                     const float *bias, int act, int mode, uint16_t *D, double *absdot)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t g = r / rows_per_group;
+        if (masked_m && (r % rows_per_group) >= (int64_t)masked_m[g])
+            continue;
+        for (int64_t n = 0; n < N; ++n) {
+            int64_t o = r * N + n;
+            double c = C ? oracle_bf16_to_double(C[o]) : 0.0;
+            double b = bias ? (double)bias[g * N + n] : 0.0;
+            double v = alpha * S[o] + beta * c + b;
+            if (act == 1 && v < 0.0)
+                v = 0.0;
+            D[o] = oracle_round_bf16_mode(v, mode);
+            if (absdot)
+                absdot[o] = fabs(alpha) * absS[o] + fabs(beta * c) + fabs(b);
+        }
+    }
 }

@@ -530,3 +530,125 @@ def test_blockscaled_grouped_matches_dense_and_keeps_padding():
         m = mm[g]
         assert np.array_equal(D[g, :m], ref[:m])
         assert np.array_equal(D[g, m:], D0[g, m:])
+
+
+# ---- directed BF16 rounding and the fused epilogue ------------------------------------
+
+def _round_fraction_to_bf16(x: Fraction, mode: int) -> int:
+    """Exact directed rounding of a rational to BF16 by choosing between the
+    two representable neighbours (no floating point)."""
+    if mode == 0:
+        return _rne_fraction_to_bf16(x)
+    if x == 0:
+        return 0
+    neg = x < 0
+    a = abs(x)
+    k = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** k > a:
+        k -= 1
+    while Fraction(2) ** (k + 1) <= a:
+        k += 1
+    k = max(k, -126)
+    sp = Fraction(2) ** (k - 7)
+    lo = (a / sp).__floor__()
+    away = (mode == 2 and not neg) or (mode == 3 and neg)
+    mag = lo + 1 if (away and lo * sp != a) else lo
+    val = mag * sp
+    biggest = (2 - Fraction(1, 128)) * Fraction(2) ** 127
+    if val > biggest:
+        return (0x8000 if neg else 0) | (0x7F80 if away else 0x7F7F)
+    code = _rne_fraction_to_bf16(val)          # val is representable: exact encode
+    return code | (0x8000 if neg else 0)
+
+
+def _specials():
+    vals = [1.0, -1.0, 1.5, 3.0e38, -3.3e38, 3.4e38, 1e-40, -1e-40, 2.0 ** -133, 2.0 ** -134 * 3,
+            9.2e-39, 1.0 + 2.0 ** -8, 1.0 + 2.0 ** -9, -(1.0 + 2.0 ** -7 + 2.0 ** -30), 7.0e-45]
+    rng = np.random.default_rng(11)
+    vals += list(rng.standard_normal(300) * np.exp2(rng.uniform(-140, 130, 300)))
+    return vals
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+def test_round_bf16_modes_exact_rational(mode):
+    for v in _specials():
+        assert oracle.round_bf16_mode(v, mode) == _round_fraction_to_bf16(Fraction(v), mode), (v, mode)
+
+
+def test_round_bf16_modes_float32_bit_rule():
+    """For a float32 input BF16 is its top half: toward zero drops the low 16
+    bits; away from zero in the value's direction adds one unit when any
+    dropped bit is set (a carry may reach infinity)."""
+    rng = np.random.default_rng(12)
+    bits = rng.integers(0, 2 ** 32, 20000, dtype=np.uint64).astype(np.uint32)
+    f = bits.view(np.float32)
+    keep = np.isfinite(f)
+    bits, f = bits[keep], f[keep]
+    top = (bits >> 16).astype(np.uint16)
+    low = (bits & 0xFFFF) != 0
+    neg = (bits >> 31) == 1
+    for i in range(0, bits.size, 37):
+        v = float(f[i])
+        assert oracle.round_bf16_mode(v, 1) == top[i]
+        up = top[i] + (1 if (low[i] and not neg[i]) else 0)
+        dn = top[i] + (1 if (low[i] and neg[i]) else 0)
+        assert oracle.round_bf16_mode(v, 2) == up, v
+        assert oracle.round_bf16_mode(v, 3) == dn, v
+
+
+def test_round_bf16_modes_order_and_symmetry():
+    for v in _specials():
+        rd = oracle.bf16_to_double(oracle.round_bf16_mode(v, 3))
+        ru = oracle.bf16_to_double(oracle.round_bf16_mode(v, 2))
+        rn = oracle.bf16_to_double(oracle.round_bf16_mode(v, 0))
+        rz = oracle.bf16_to_double(oracle.round_bf16_mode(v, 1))
+        assert rd <= v <= ru and rn in (rd, ru)
+        assert rz == (rd if v >= 0 else ru)
+        assert oracle.round_bf16_mode(-v, 3) == oracle.round_bf16_mode(v, 2) ^ 0x8000
+
+
+def test_epilogue_identity_bias_c_alpha():
+    A = _rand_codes((12, 96), 401, 0)
+    B = _rand_codes((20, 96), 402, 0)
+    D0, absd, S = oracle.gemm_nt(A, B, want_exact=True)
+    D1, _ = oracle.epilogue(S, absd)                              # alpha 1, nothing else
+    assert np.array_equal(D0, D1)
+    bias = np.random.default_rng(13).standard_normal(20).astype(np.float32)
+    Db, _ = oracle.epilogue(np.zeros_like(S), np.zeros_like(S), bias=bias)
+    assert np.array_equal(Db, np.tile(oracle.round_bf16_array(bias.astype(np.float64)), (12, 1)))
+    C = synth.u16_pattern((12, 20), 403) & 0x7F7F                 # finite codes of both signs
+    for mode in range(4):
+        Dc, _ = oracle.epilogue(S, absd, alpha=0.0, beta=1.0, C=C, mode=mode)
+        assert np.array_equal(oracle.bf16_bits_to_f64(Dc), oracle.bf16_bits_to_f64(C)), mode
+    D4, _ = oracle.epilogue(S, absd, alpha=4.0)
+    assert np.array_equal(oracle.bf16_bits_to_f64(D4), 4 * oracle.bf16_bits_to_f64(D0))
+
+
+def test_epilogue_relu_and_modes_bracket():
+    A = _rand_codes((16, 64), 404, 0)
+    B = _rand_codes((16, 64), 405, 1)
+    _, absd, S = oracle.gemm_nt(A, B, 0, 1, want_exact=True)
+    bias = np.linspace(-3, 3, 16).astype(np.float32)
+    C = synth.u16_pattern((16, 16), 406) & 0x3FFF
+    plain, _ = oracle.epilogue(S, absd, 0.5, -2.0, C, bias)
+    relu, _ = oracle.epilogue(S, absd, 0.5, -2.0, C, bias, relu=True)
+    pv, rv = oracle.bf16_bits_to_f64(plain), oracle.bf16_bits_to_f64(relu)
+    assert np.array_equal(rv, np.maximum(pv, 0.0))
+    v = 0.5 * S - 2.0 * oracle.bf16_bits_to_f64(C) + bias[None, :].astype(np.float64)
+    dn = oracle.bf16_bits_to_f64(oracle.epilogue(S, absd, 0.5, -2.0, C, bias, mode=3)[0])
+    up = oracle.bf16_bits_to_f64(oracle.epilogue(S, absd, 0.5, -2.0, C, bias, mode=2)[0])
+    assert np.all(dn <= v) and np.all(v <= up)
+    assert np.all((pv == dn) | (pv == up))
+
+
+def test_epilogue_grouped_masked_rows_untouched():
+    G, M_max, N = 3, 5, 8
+    S = np.random.default_rng(14).standard_normal((G, M_max, N))
+    D0 = synth.u16_pattern((G, M_max, N), 407)
+    mm = np.array([2, 0, 5], np.int32)
+    bias = np.random.default_rng(15).standard_normal((G, N)).astype(np.float32)
+    D, _ = oracle.epilogue(S, np.abs(S), bias=bias, masked_m=mm, D_init=D0)
+    for g in range(G):
+        assert np.array_equal(D[g, mm[g]:], D0[g, mm[g]:])
+        want = oracle.round_bf16_array(S[g, :mm[g]] + bias[g][None, :].astype(np.float64))
+        assert np.array_equal(D[g, :mm[g]], want)
