@@ -356,3 +356,113 @@ def fp8_gemm_grouped_masked_blockscaled(A, B, masked_m, sf_a, sf_b, D=None, max_
     if rc != OK:
         raise Fp8gError(rc, "fp8_gemm_grouped_masked_blockscaled")
     return D
+
+
+ACT_NONE, ACT_RELU = 0, 1
+ROUND_RN, ROUND_RZ, ROUND_RU, ROUND_RD = 0, 1, 2, 3
+
+
+def _ex_structs(groups, rows, N, K, scale_a, scale_b, sf_a, sf_b, sf_group_k, epilogue):
+    import torch
+    sc = None
+    if scale_a is not None or scale_b is not None or sf_a is not None or sf_b is not None:
+        sc = _lib.Scales()
+        if scale_a is not None or scale_b is not None:
+            if scale_a is None or scale_b is None:
+                raise ValueError("output scales need both scale_a and scale_b")
+            _check_scale(scale_a, "scale_a", (groups, groups * rows))
+            _check_scale(scale_b, "scale_b", (groups, groups * N))
+            sc.out_a, sc.out_a_len = scale_a.data_ptr(), scale_a.numel()
+            sc.out_b, sc.out_b_len = scale_b.data_ptr(), scale_b.numel()
+        if sf_a is not None or sf_b is not None:
+            if sf_a is None or sf_b is None:
+                raise ValueError("block scales need both sf_a and sf_b")
+            if sf_group_k not in (32, 128):
+                raise ValueError("sf_group_k must be 32 or 128")
+            ks = -(-K // sf_group_k)
+            sa = sf_a if sf_a.dim() == 3 else sf_a.unsqueeze(0)
+            sb = sf_b if sf_b.dim() == 3 else sf_b.unsqueeze(0)
+            _check_sf(sa, "sf_a", groups, ks, rows)
+            _check_sf(sb, "sf_b", groups, ks, N)
+            sc.block_a, sc.block_a_ld = sa.data_ptr(), sa.shape[2]
+            sc.block_b, sc.block_b_ld = sb.data_ptr(), sb.shape[2]
+            sc.block_k = int(sf_group_k)
+    ep = None
+    if epilogue is not None:
+        e = dict(epilogue)
+        ep = _lib.Epilogue()
+        ep.alpha = float(e.get("alpha", 1.0))
+        ep.beta = float(e.get("beta", 0.0))
+        C, bias = e.get("C"), e.get("bias")
+        if C is not None:
+            if not C.is_cuda or C.dtype != torch.bfloat16 or not C.is_contiguous() or C.numel() != groups * rows * N:
+                raise ValueError("epilogue C must be a contiguous bf16 CUDA tensor shaped like D")
+            ep.c = C.data_ptr()
+        if bias is not None:
+            if not bias.is_cuda or bias.dtype != torch.float32 or not bias.is_contiguous() or bias.numel() != groups * N:
+                raise ValueError("epilogue bias must be a contiguous float32 CUDA tensor of %d entries" % (groups * N))
+            ep.bias = bias.data_ptr()
+        ep.activation = ACT_RELU if e.get("relu", False) else ACT_NONE
+        ep.round_mode = int(e.get("round_mode", ROUND_RN))
+    return sc, ep
+
+
+def fp8_gemm_nt_ex(A, B, D=None, scale_a=None, scale_b=None, sf_a=None, sf_b=None, sf_group_k: int = 128,
+                   epilogue=None, a_dtype=None, b_dtype=None, flags: int = 0, stream=None):
+    """General dense form: optional output scales (scale_a/scale_b), block
+    scales (sf_a/sf_b, sf_group_k) and a fused epilogue given as a dict with
+    keys alpha, beta, C (bf16 like D), bias (float32 [N]), relu, round_mode:
+    D = round(act(alpha * value + beta * C + bias))."""
+    import torch
+    _check_operand(A, "A", 2)
+    _check_operand(B, "B", 2)
+    fa, fb = _fp8_code(A, a_dtype), _fp8_code(B, b_dtype)
+    M, K = A.shape
+    N, K2 = B.shape
+    if K != K2:
+        raise ValueError("K mismatch: A has %d, B has %d" % (K, K2))
+    sc, ep = _ex_structs(1, M, N, K, scale_a, scale_b, sf_a, sf_b, sf_group_k, epilogue)
+    if D is None:
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    else:
+        _check_operand(D, "D", 2)
+        if D.dtype != torch.bfloat16 or tuple(D.shape) != (M, N):
+            raise ValueError("D must be a contiguous bf16 [M, N] tensor")
+    with _on_device(A.device):
+        rc = _lib.load().fp8_gemm_nt_ex(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, fa, fb,
+                                        None if sc is None else ctypes.byref(sc),
+                                        None if ep is None else ctypes.byref(ep), int(flags),
+                                        _stream_handle(stream))
+    if rc != OK:
+        raise Fp8gError(rc, "fp8_gemm_nt_ex")
+    return D
+
+
+def fp8_gemm_grouped_masked_ex(A, B, masked_m, D=None, max_m_hint: int = 0, scale_a=None, scale_b=None,
+                               sf_a=None, sf_b=None, sf_group_k: int = 128, epilogue=None, a_dtype=None,
+                               b_dtype=None, flags: int = 0, stream=None):
+    """General masked grouped form (see fp8_gemm_nt_ex); epilogue bias is
+    float32 [G, N], C bf16 [G, M_max, N]."""
+    import torch
+    _check_operand(A, "A", 3)
+    _check_operand(B, "B", 3)
+    fa, fb = _fp8_code(A, a_dtype), _fp8_code(B, b_dtype)
+    G, M_max, K = A.shape
+    G2, N, K2 = B.shape
+    if G != G2 or K != K2:
+        raise ValueError("shape mismatch: A %s, B %s" % (tuple(A.shape), tuple(B.shape)))
+    if not masked_m.is_cuda or masked_m.dtype != torch.int32 or tuple(masked_m.shape) != (G,):
+        raise ValueError("masked_m must be a contiguous int32 CUDA tensor of shape [G]")
+    sc, ep = _ex_structs(G, M_max, N, K, scale_a, scale_b, sf_a, sf_b, sf_group_k, epilogue)
+    if D is None:
+        D = torch.empty((G, M_max, N), dtype=torch.bfloat16, device=A.device)
+    else:
+        _check_operand(D, "D", 3)
+    with _on_device(A.device):
+        rc = _lib.load().fp8_gemm_grouped_masked_ex(
+            A.data_ptr(), B.data_ptr(), D.data_ptr(), masked_m.data_ptr(), G, M_max, N, K, int(max_m_hint), fa, fb,
+            None if sc is None else ctypes.byref(sc), None if ep is None else ctypes.byref(ep), int(flags),
+            _stream_handle(stream))
+    if rc != OK:
+        raise Fp8gError(rc, "fp8_gemm_grouped_masked_ex")
+    return D

@@ -14,6 +14,25 @@ LIB_PATH = os.path.join(HERE, "_build", "libfp8g.so")
 # Symbols declared in include/fp8g.h, with their ctypes signatures.
 _c_void_p = ctypes.c_void_p
 _i64 = ctypes.c_int64
+
+
+class Scales(ctypes.Structure):
+    """fp8g_scales: output scales and block scales (NULL pointers: absent)."""
+    _fields_ = [("out_a", ctypes.c_void_p), ("out_a_len", ctypes.c_int64),
+                ("out_b", ctypes.c_void_p), ("out_b_len", ctypes.c_int64),
+                ("block_a", ctypes.c_void_p), ("block_a_ld", ctypes.c_int64),
+                ("block_b", ctypes.c_void_p), ("block_b_ld", ctypes.c_int64),
+                ("block_k", ctypes.c_int32)]
+
+
+class Epilogue(ctypes.Structure):
+    """fp8g_epilogue: D = round(act(alpha * value + beta * C + bias))."""
+    _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("c", ctypes.c_void_p),
+                ("bias", ctypes.c_void_p), ("activation", ctypes.c_int32), ("round_mode", ctypes.c_int32)]
+
+
+_scales_p = ctypes.POINTER(Scales)
+_epi_p = ctypes.POINTER(Epilogue)
 SIGNATURES = {
     "fp8_gemm_nt": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _i64, _i64,
                                    ctypes.c_int, ctypes.c_int, ctypes.c_uint32, _c_void_p]),
@@ -35,6 +54,11 @@ SIGNATURES = {
                                                            ctypes.c_int, _c_void_p, _i64, _c_void_p,
                                                            _i64, ctypes.c_int, ctypes.c_uint32,
                                                            _c_void_p]),
+    "fp8_gemm_nt_ex": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _i64, _i64, ctypes.c_int,
+                                      ctypes.c_int, _scales_p, _epi_p, ctypes.c_uint32, _c_void_p]),
+    "fp8_gemm_grouped_masked_ex": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _i64, _i64, _i64,
+                                                  _i64, _i64, ctypes.c_int, ctypes.c_int, _scales_p, _epi_p,
+                                                  ctypes.c_uint32, _c_void_p]),
     "fp8_gemm_nt_noalloc": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _i64, _i64,
                                            ctypes.c_int, ctypes.c_int, _c_void_p]),
     "fp8g_get_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), _c_void_p]),

@@ -308,7 +308,33 @@ struct Problem {
     const uint8_t *sf_a = nullptr, *sf_b = nullptr;
     int64_t sf_a_ld = 0, sf_b_ld = 0;
     int sf_k = 0;
+    // Fused epilogue (see GemmArgs).
+    bool epi = false;
+    float alpha = 1.0f, beta = 0.0f;
+    const void *c_in = nullptr;
+    const float *bias = nullptr;
+    int relu = 0, round_mode = 0;
 };
+
+int check_epilogue(const fp8g_epilogue *e, Problem &p)
+{
+    if (!e)
+        return FP8G_OK;
+    if (e->activation != FP8G_ACT_NONE && e->activation != FP8G_ACT_RELU)
+        return FP8G_ERR_INVALID_ARG;
+    if (e->round_mode < FP8G_ROUND_RN || e->round_mode > FP8G_ROUND_RD)
+        return FP8G_ERR_INVALID_ARG;
+    if ((e->c && !aligned16(e->c)) || (e->bias && !aligned16(e->bias)))
+        return FP8G_ERR_MISALIGNED;
+    p.epi = true;
+    p.alpha = e->alpha;
+    p.beta = e->beta;
+    p.c_in = e->c;
+    p.bias = e->bias;
+    p.relu = e->activation == FP8G_ACT_RELU ? 1 : 0;
+    p.round_mode = e->round_mode;
+    return FP8G_OK;
+}
 
 // Largest tile (token chunk, or N tile) whose two accumulators leave TMEM
 // room for at least two stages' scale sets.
@@ -403,6 +429,13 @@ int launch(const Problem &p, cudaStream_t stream)
     args.raster_band = 1;
     args.sf_k = p.sf_k;
     const int64_t ks = p.sf_k ? cdiv(p.K, kBlockK / p.sf_k) : 0;
+    args.epi = p.epi ? 1 : 0;
+    args.alpha = p.alpha;
+    args.beta = p.beta;
+    args.c_in = p.c_in;
+    args.bias = p.bias;
+    args.relu = p.relu;
+    args.round_mode = p.round_mode;
 
     CUtensorMap tm0, tm1, tm2, tm3;
     if (swap) {
@@ -548,8 +581,26 @@ int launch(const Problem &p, cudaStream_t stream)
 
 using namespace fp8g;
 
-extern "C" int fp8_gemm_nt(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K,
-                           int a_dtype, int b_dtype, uint32_t flags, cudaStream_t stream)
+namespace fp8g {
+namespace {
+
+int apply_scales(const fp8g_scales *sc, int64_t G, int64_t rows, int64_t N, Problem &p)
+{
+    if (!sc)
+        return FP8G_OK;
+    int st = FP8G_OK;
+    if (sc->out_a || sc->out_b) {
+        st = check_scales(sc->out_a, sc->out_a_len, sc->out_b, sc->out_b_len, G, rows, N, p);
+        if (st != FP8G_OK)
+            return st;
+    }
+    if (sc->block_a || sc->block_b)
+        st = check_blockscales(sc->block_a, sc->block_a_ld, sc->block_b, sc->block_b_ld, sc->block_k, rows, N, p);
+    return st;
+}
+
+int dense_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, int a_dtype, int b_dtype,
+             const fp8g_scales *sc, const fp8g_epilogue *epi, uint32_t flags, cudaStream_t stream)
 {
     int st = check_common(A, B, D, N, K, a_dtype, b_dtype);
     if (st != FP8G_OK)
@@ -557,13 +608,14 @@ extern "C" int fp8_gemm_nt(const void *A, const void *B, void *D, int64_t M, int
     if (M <= 0 || M > kMaxDim)
         return FP8G_ERR_INVALID_ARG;
     Problem p{A, B, D, nullptr, 1, M, N, K, M, a_dtype, b_dtype, flags};
+    if ((st = apply_scales(sc, 1, M, N, p)) != FP8G_OK || (st = check_epilogue(epi, p)) != FP8G_OK)
+        return st;
     return launch(p, stream);
 }
 
-extern "C" int fp8_gemm_grouped_masked(const void *A, const void *B, void *D, const int32_t *masked_m,
-                                       int64_t G, int64_t M_max, int64_t N, int64_t K,
-                                       int64_t max_m_hint, int a_dtype, int b_dtype, uint32_t flags,
-                                       cudaStream_t stream)
+int grouped_ex(const void *A, const void *B, void *D, const int32_t *masked_m, int64_t G, int64_t M_max, int64_t N,
+               int64_t K, int64_t max_m_hint, int a_dtype, int b_dtype, const fp8g_scales *sc,
+               const fp8g_epilogue *epi, uint32_t flags, cudaStream_t stream)
 {
     int st = check_common(A, B, D, N, K, a_dtype, b_dtype);
     if (st != FP8G_OK)
@@ -578,6 +630,10 @@ extern "C" int fp8_gemm_grouped_masked(const void *A, const void *B, void *D, co
         return FP8G_ERR_UNSUPPORTED;
     if (!aligned16(masked_m))
         return FP8G_ERR_MISALIGNED;
+    const int64_t hint = max_m_hint > 0 ? max_m_hint : M_max;
+    Problem p{A, B, D, masked_m, G, M_max, N, K, hint, a_dtype, b_dtype, flags};
+    if ((st = apply_scales(sc, G, M_max, N, p)) != FP8G_OK || (st = check_epilogue(epi, p)) != FP8G_OK)
+        return st;
     cudaPointerAttributes attr;
     if (cudaPointerGetAttributes(&attr, masked_m) != cudaSuccess) {
         cudaGetLastError();
@@ -585,9 +641,40 @@ extern "C" int fp8_gemm_grouped_masked(const void *A, const void *B, void *D, co
     }
     if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
         return FP8G_ERR_INVALID_ARG;
-    const int64_t hint = max_m_hint > 0 ? max_m_hint : M_max;
-    Problem p{A, B, D, masked_m, G, M_max, N, K, hint, a_dtype, b_dtype, flags};
     return launch(p, stream);
+}
+
+}  // namespace
+}  // namespace fp8g
+
+extern "C" int fp8_gemm_nt(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K,
+                           int a_dtype, int b_dtype, uint32_t flags, cudaStream_t stream)
+{
+    return dense_ex(A, B, D, M, N, K, a_dtype, b_dtype, nullptr, nullptr, flags, stream);
+}
+
+extern "C" int fp8_gemm_grouped_masked(const void *A, const void *B, void *D, const int32_t *masked_m,
+                                       int64_t G, int64_t M_max, int64_t N, int64_t K, int64_t max_m_hint,
+                                       int a_dtype, int b_dtype, uint32_t flags, cudaStream_t stream)
+{
+    return grouped_ex(A, B, D, masked_m, G, M_max, N, K, max_m_hint, a_dtype, b_dtype, nullptr, nullptr, flags,
+                      stream);
+}
+
+extern "C" int fp8_gemm_nt_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K,
+                              int a_dtype, int b_dtype, const fp8g_scales *scales, const fp8g_epilogue *epilogue,
+                              uint32_t flags, cudaStream_t stream)
+{
+    return dense_ex(A, B, D, M, N, K, a_dtype, b_dtype, scales, epilogue, flags, stream);
+}
+
+extern "C" int fp8_gemm_grouped_masked_ex(const void *A, const void *B, void *D, const int32_t *masked_m,
+                                          int64_t G, int64_t M_max, int64_t N, int64_t K, int64_t max_m_hint,
+                                          int a_dtype, int b_dtype, const fp8g_scales *scales,
+                                          const fp8g_epilogue *epilogue, uint32_t flags, cudaStream_t stream)
+{
+    return grouped_ex(A, B, D, masked_m, G, M_max, N, K, max_m_hint, a_dtype, b_dtype, scales, epilogue, flags,
+                      stream);
 }
 
 extern "C" int fp8_gemm_nt_scaled(const void *A, const void *B, void *D, int64_t M, int64_t N,
@@ -595,16 +682,10 @@ extern "C" int fp8_gemm_nt_scaled(const void *A, const void *B, void *D, int64_t
                                   int64_t scale_a_len, const float *scale_b, int64_t scale_b_len,
                                   uint32_t flags, cudaStream_t stream)
 {
-    int st = check_common(A, B, D, N, K, a_dtype, b_dtype);
-    if (st != FP8G_OK)
-        return st;
-    if (M <= 0 || M > kMaxDim)
+    if (!scale_a || !scale_b)
         return FP8G_ERR_INVALID_ARG;
-    Problem p{A, B, D, nullptr, 1, M, N, K, M, a_dtype, b_dtype, flags};
-    st = check_scales(scale_a, scale_a_len, scale_b, scale_b_len, 1, M, N, p);
-    if (st != FP8G_OK)
-        return st;
-    return launch(p, stream);
+    const fp8g_scales sc{scale_a, scale_a_len, scale_b, scale_b_len, nullptr, 0, nullptr, 0, 0};
+    return dense_ex(A, B, D, M, N, K, a_dtype, b_dtype, &sc, nullptr, flags, stream);
 }
 
 extern "C" int fp8_gemm_grouped_masked_scaled(const void *A, const void *B, void *D,
@@ -614,32 +695,11 @@ extern "C" int fp8_gemm_grouped_masked_scaled(const void *A, const void *B, void
                                               const float *scale_b, int64_t scale_b_len, uint32_t flags,
                                               cudaStream_t stream)
 {
-    int st = check_common(A, B, D, N, K, a_dtype, b_dtype);
-    if (st != FP8G_OK)
-        return st;
-    if (!masked_m)
+    if (!scale_a || !scale_b)
         return FP8G_ERR_INVALID_ARG;
-    if (G <= 0 || M_max <= 0 || M_max > kMaxDim || max_m_hint < 0 || max_m_hint > M_max)
-        return FP8G_ERR_INVALID_ARG;
-    if (G > kMaxGroups)
-        return FP8G_ERR_UNSUPPORTED;
-    if (G * M_max > kMaxDim || G * N > kMaxDim)
-        return FP8G_ERR_UNSUPPORTED;
-    if (!aligned16(masked_m))
-        return FP8G_ERR_MISALIGNED;
-    const int64_t hint = max_m_hint > 0 ? max_m_hint : M_max;
-    Problem p{A, B, D, masked_m, G, M_max, N, K, hint, a_dtype, b_dtype, flags};
-    st = check_scales(scale_a, scale_a_len, scale_b, scale_b_len, G, M_max, N, p);
-    if (st != FP8G_OK)
-        return st;
-    cudaPointerAttributes attr;
-    if (cudaPointerGetAttributes(&attr, masked_m) != cudaSuccess) {
-        cudaGetLastError();
-        return FP8G_ERR_INVALID_ARG;
-    }
-    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
-        return FP8G_ERR_INVALID_ARG;
-    return launch(p, stream);
+    const fp8g_scales sc{scale_a, scale_a_len, scale_b, scale_b_len, nullptr, 0, nullptr, 0, 0};
+    return grouped_ex(A, B, D, masked_m, G, M_max, N, K, max_m_hint, a_dtype, b_dtype, &sc, nullptr, flags,
+                      stream);
 }
 
 extern "C" int fp8_gemm_nt_blockscaled(const void *A, const void *B, void *D, int64_t M, int64_t N,
@@ -647,16 +707,10 @@ extern "C" int fp8_gemm_nt_blockscaled(const void *A, const void *B, void *D, in
                                        int64_t sf_a_ld, const uint8_t *sf_b, int64_t sf_b_ld,
                                        int sf_group_k, uint32_t flags, cudaStream_t stream)
 {
-    int st = check_common(A, B, D, N, K, a_dtype, b_dtype);
-    if (st != FP8G_OK)
-        return st;
-    if (M <= 0 || M > kMaxDim)
+    if (!sf_a || !sf_b)
         return FP8G_ERR_INVALID_ARG;
-    Problem p{A, B, D, nullptr, 1, M, N, K, M, a_dtype, b_dtype, flags};
-    st = check_blockscales(sf_a, sf_a_ld, sf_b, sf_b_ld, sf_group_k, M, N, p);
-    if (st != FP8G_OK)
-        return st;
-    return launch(p, stream);
+    const fp8g_scales sc{nullptr, 0, nullptr, 0, sf_a, sf_a_ld, sf_b, sf_b_ld, sf_group_k};
+    return dense_ex(A, B, D, M, N, K, a_dtype, b_dtype, &sc, nullptr, flags, stream);
 }
 
 extern "C" int fp8_gemm_grouped_masked_blockscaled(const void *A, const void *B, void *D,
@@ -666,32 +720,11 @@ extern "C" int fp8_gemm_grouped_masked_blockscaled(const void *A, const void *B,
                                                    const uint8_t *sf_b, int64_t sf_b_ld, int sf_group_k,
                                                    uint32_t flags, cudaStream_t stream)
 {
-    int st = check_common(A, B, D, N, K, a_dtype, b_dtype);
-    if (st != FP8G_OK)
-        return st;
-    if (!masked_m)
+    if (!sf_a || !sf_b)
         return FP8G_ERR_INVALID_ARG;
-    if (G <= 0 || M_max <= 0 || M_max > kMaxDim || max_m_hint < 0 || max_m_hint > M_max)
-        return FP8G_ERR_INVALID_ARG;
-    if (G > kMaxGroups)
-        return FP8G_ERR_UNSUPPORTED;
-    if (G * M_max > kMaxDim || G * N > kMaxDim)
-        return FP8G_ERR_UNSUPPORTED;
-    if (!aligned16(masked_m))
-        return FP8G_ERR_MISALIGNED;
-    const int64_t hint = max_m_hint > 0 ? max_m_hint : M_max;
-    Problem p{A, B, D, masked_m, G, M_max, N, K, hint, a_dtype, b_dtype, flags};
-    st = check_blockscales(sf_a, sf_a_ld, sf_b, sf_b_ld, sf_group_k, M_max, N, p);
-    if (st != FP8G_OK)
-        return st;
-    cudaPointerAttributes attr;
-    if (cudaPointerGetAttributes(&attr, masked_m) != cudaSuccess) {
-        cudaGetLastError();
-        return FP8G_ERR_INVALID_ARG;
-    }
-    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
-        return FP8G_ERR_INVALID_ARG;
-    return launch(p, stream);
+    const fp8g_scales sc{nullptr, 0, nullptr, 0, sf_a, sf_a_ld, sf_b, sf_b_ld, sf_group_k};
+    return grouped_ex(A, B, D, masked_m, G, M_max, N, K, max_m_hint, a_dtype, b_dtype, &sc, nullptr, flags,
+                      stream);
 }
 
 extern "C" int fp8g_get_device_status(int32_t *info, cudaStream_t stream)

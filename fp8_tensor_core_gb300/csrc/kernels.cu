@@ -166,6 +166,103 @@ __device__ __forceinline__ uint4 scale_pack8(const GemmArgs &a, const uint32_t *
     return o;
 }
 
+// ---- fused epilogue ---------------------------------------------------------------
+// "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践" §3.3: alpha * AB
+// + beta * C + per-channel bias and an optional ReLU inside the GEMM's
+// epilogue, with a choice of rounding for the final conversion.
+
+__device__ __forceinline__ uint16_t bf16_bits_rounded(float x, int mode)
+{
+    __nv_bfloat16 h;
+    switch (mode) {
+    case 1: h = __float2bfloat16_rz(x); break;
+    case 2: h = __float2bfloat16_ru(x); break;
+    case 3: h = __float2bfloat16_rd(x); break;
+    default: h = __float2bfloat16_rn(x); break;
+    }
+    return __bfloat16_as_ushort(h);
+}
+
+__device__ __forceinline__ float epi_value(const GemmArgs &a, float v, float c, float b)
+{
+    float x = fmaf(a.alpha, v, fmaf(a.beta, c, b));
+    if (a.relu && x < 0.0f)
+        x = 0.0f;
+    return x;
+}
+
+// Eight scaled products of output row `row` (row of the [groups * rows_a]
+// output), columns col..col+7 of group g, through the fused epilogue.
+__device__ __forceinline__ uint4 epi_pack8(const GemmArgs &a, const float *f, int g, int64_t row, int col)
+{
+    float c[8], b[8];
+    if (a.c_in) {
+        const uint4 cv = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.c_in) +
+                                                          row * a.n + col);
+        const uint32_t w[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            c[2 * i] = __uint_as_float(w[i] << 16);
+            c[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            c[i] = 0.0f;
+    }
+    if (a.bias) {
+        const float4 *p = reinterpret_cast<const float4 *>(a.bias + static_cast<int64_t>(g) * a.n + col);
+        const float4 x = __ldg(p), y = __ldg(p + 1);
+        b[0] = x.x; b[1] = x.y; b[2] = x.z; b[3] = x.w;
+        b[4] = y.x; b[5] = y.y; b[6] = y.z; b[7] = y.w;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            b[i] = 0.0f;
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        o[i] = static_cast<uint32_t>(bf16_bits_rounded(epi_value(a, f[2 * i], c[2 * i], b[2 * i]), a.round_mode)) |
+               (static_cast<uint32_t>(bf16_bits_rounded(epi_value(a, f[2 * i + 1], c[2 * i + 1], b[2 * i + 1]),
+                                                        a.round_mode))
+                << 16);
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Output of eight accumulator values (bits) of row `row` of group g at
+// columns col..col+7: output scales, then the fused epilogue or a plain
+// round-to-nearest-even.
+__device__ __forceinline__ uint4 out_pack8(const GemmArgs &a, const uint32_t *v, float rf, int g, int64_t row,
+                                           int col)
+{
+    if (!a.epi)
+        return scale_pack8(a, v, rf, g, col);
+    float f[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        f[i] = __uint_as_float(v[i]) * rf;
+    if (a.scale_b && a.sb_per_col) {
+        const float4 *p = reinterpret_cast<const float4 *>(a.scale_b + static_cast<int64_t>(g) * a.n + col);
+        const float4 x = __ldg(p), y = __ldg(p + 1);
+        f[0] *= x.x; f[1] *= x.y; f[2] *= x.z; f[3] *= x.w;
+        f[4] *= y.x; f[5] *= y.y; f[6] *= y.z; f[7] *= y.w;
+    }
+    return epi_pack8(a, f, g, static_cast<int64_t>(g) * a.rows_a + row, col);
+}
+
+// One SwapAB output element (token `tok` of group g, column n), value v
+// already scaled.
+__device__ __forceinline__ __nv_bfloat16 out_one(const GemmArgs &a, float v, int g, int tok, int n)
+{
+    if (!a.epi)
+        return __float2bfloat16_rn(v);
+    const int64_t idx = (static_cast<int64_t>(g) * a.rows_a + tok) * a.n + n;
+    const float c = a.c_in ? __bfloat162float(static_cast<const __nv_bfloat16 *>(a.c_in)[idx]) : 0.0f;
+    const float b = a.bias ? __ldg(a.bias + static_cast<int64_t>(g) * a.n + n) : 0.0f;
+    return __ushort_as_bfloat16(bf16_bits_rounded(epi_value(a, v, c, b), a.round_mode));
+}
+
 // SwapAB epilogue: thread = output column n (weight row), registers = tokens.
 // Column factor sb(g, n) (times sa(g) when A's scale is per tensor).
 __device__ __forceinline__ float col_factor(const GemmArgs &a, int g, int n)
@@ -649,7 +746,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
                     for (int j = 0; j < 4; ++j) {
                         const int col = n0 + c + 8 * j;
                         if (col < a.n)
-                            *reinterpret_cast<uint4 *>(drow + col) = scale_pack8(a, r + 8 * j, rf, g, col);
+                            *reinterpret_cast<uint4 *>(drow + col) = out_pack8(a, r + 8 * j, rf, g, row, col);
                     }
                 }
             }
@@ -969,7 +1066,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const float rf = row_ok ? row_factor(a, 0, grow) : 1.0f;
             auto store8 = [&](int col, const uint32_t *v) {
                 if (row_ok && col < a.n)
-                    *reinterpret_cast<uint4 *>(drow + col) = scale_pack8(a, v, rf, 0, col);
+                    *reinterpret_cast<uint4 *>(drow + col) = out_pack8(a, v, rf, 0, grow, col);
             };
             if (x.kb0 == 0 && x.kb1 == num_kb) {
                 for (int c = 0; c < a.tile_n; c += 32) {
@@ -1400,8 +1497,9 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             if (c + j < x.n_tok)
-                                dcol[static_cast<int64_t>(x.tok0 + c + j) * a.n] = __float2bfloat16_rn(
-                                    __uint_as_float(r[j]) * cf * token_factor(a, x.g, x.tok0 + c + j));
+                                dcol[static_cast<int64_t>(x.tok0 + c + j) * a.n] =
+                                    out_one(a, __uint_as_float(r[j]) * cf * token_factor(a, x.g, x.tok0 + c + j),
+                                            x.g, x.tok0 + c + j, nrow);
                         }
                     }
                 }
@@ -1475,8 +1573,9 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
 #pragma unroll
                             for (int j = 0; j < 16; ++j) {
                                 if (c + j < x.n_tok)
-                                    dcol[static_cast<int64_t>(x.tok0 + c + j) * a.n] = __float2bfloat16_rn(
-                                        acc_v[j] * cf * token_factor(a, x.g, x.tok0 + c + j));
+                                    dcol[static_cast<int64_t>(x.tok0 + c + j) * a.n] =
+                                        out_one(a, acc_v[j] * cf * token_factor(a, x.g, x.tok0 + c + j), x.g,
+                                                x.tok0 + c + j, nrow);
                             }
                         }
                     }

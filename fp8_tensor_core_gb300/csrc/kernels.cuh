@@ -69,6 +69,17 @@ struct GemmArgs {
     int32_t sf_off;            // byte offset of the scale area inside a stage
     int32_t sf_col0;           // first TMEM column of the block-scale sets
     int32_t sf_sets;           // TMEM block-scale sets (2..kMaxSfSets)
+    // Fused epilogue (epi != 0): out = round(act(alpha * v + beta * c_in + bias)),
+    // v the (scaled) product; c_in BF16 shaped like D or nullptr; bias FP32
+    // [groups][n] or nullptr; act ReLU when relu != 0; round_mode 0 nearest
+    // even, 1 toward zero, 2 toward +inf, 3 toward -inf.
+    int32_t epi;
+    int32_t relu;
+    int32_t round_mode;
+    float alpha;
+    float beta;
+    const void *c_in;
+    const float *bias;
     float *workspace;          // swap kernel, stream-K: 2 FP32 partial tiles per CTA
                                // (128 x tile_n floats each)
     int32_t *counters;         // swap kernel, stream-K: arrivals per (tile, epilogue warp),

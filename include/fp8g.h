@@ -7,6 +7,8 @@
  *   fp8_gemm_grouped_masked  D[g,m,n] = A[g,m,:] . B[g,n,:]  for m < masked_m[g]
  *   ..._scaled               the same times per-tensor / per-channel scales
  *   ..._blockscaled          UE8M0 scales per row per 32/128-element K group
+ *   ..._ex                   any of those plus a fused epilogue (alpha, beta*C,
+ *                            bias, ReLU, rounding mode)
  *   fp8_gemm_nt_noalloc      dense small-token form that allocates nothing
  *
  * A and B hold FP8 codes (E4M3 or E5M2, chosen per operand), products are
@@ -209,6 +211,70 @@ int fp8_gemm_grouped_masked_blockscaled(const void *A, const void *B, void *D,
                                         int b_dtype, const uint8_t *sf_a, int64_t sf_a_ld,
                                         const uint8_t *sf_b, int64_t sf_b_ld, int sf_group_k,
                                         uint32_t flags, cudaStream_t stream);
+
+/*
+ * fp8_gemm_nt_ex / fp8_gemm_grouped_masked_ex -- the general forms: any
+ * combination of output scales, block scales and a fused epilogue.
+ *
+ *   value  = sum_k A B (* block scales)  * sa * sb  (output scales)
+ *   D      = round( act( alpha * value + beta * C + bias[g][n] ) )
+ *
+ * The fused epilogue follows "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法
+ * 内核优化实践" §3.3: alpha * AB + beta * C + per-channel bias and ReLU inside
+ * the GEMM (no extra pass over HBM), with a choice of rounding for the final
+ * conversion (nearest even, toward zero, toward +inf; toward -inf added for
+ * symmetry).  Evaluated in FP32 as fma(alpha, value, fma(beta, C, bias)).
+ *
+ * `scales` (NULL: none) -- out_a/out_b as in the ..._scaled calls (both or
+ * neither), block_a/block_b as in the ..._blockscaled calls (both or
+ * neither, with block_k 32 or 128).
+ * `epilogue` (NULL: D = round-to-nearest-even(value)) --
+ *   alpha, beta  FP32 multipliers;
+ *   c            DEVICE BF16 shaped like D (may be D itself), or NULL (no
+ *                beta term);
+ *   bias         DEVICE FP32 [G][N] (dense: [N]), or NULL;
+ *   activation   FP8G_ACT_NONE or FP8G_ACT_RELU (negative results become
+ *                +0, NaN stays NaN);
+ *   round_mode   FP8G_ROUND_RN / _RZ / _RU / _RD.
+ *   c and bias must be 16-byte aligned.  Masked-out rows of the grouped
+ *   form are neither read from c nor written.
+ */
+typedef struct {
+    const float *out_a;
+    int64_t out_a_len;
+    const float *out_b;
+    int64_t out_b_len;
+    const uint8_t *block_a;
+    int64_t block_a_ld;
+    const uint8_t *block_b;
+    int64_t block_b_ld;
+    int32_t block_k;
+} fp8g_scales;
+
+#define FP8G_ACT_NONE 0
+#define FP8G_ACT_RELU 1
+#define FP8G_ROUND_RN 0 /* to nearest, ties to even  */
+#define FP8G_ROUND_RZ 1 /* toward zero               */
+#define FP8G_ROUND_RU 2 /* toward +infinity          */
+#define FP8G_ROUND_RD 3 /* toward -infinity          */
+
+typedef struct {
+    float alpha;
+    float beta;
+    const void *c;
+    const float *bias;
+    int32_t activation;
+    int32_t round_mode;
+} fp8g_epilogue;
+
+int fp8_gemm_nt_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K,
+                   int a_dtype, int b_dtype, const fp8g_scales *scales,
+                   const fp8g_epilogue *epilogue, uint32_t flags, cudaStream_t stream);
+int fp8_gemm_grouped_masked_ex(const void *A, const void *B, void *D, const int32_t *masked_m,
+                               int64_t G, int64_t M_max, int64_t N, int64_t K,
+                               int64_t max_m_hint, int a_dtype, int b_dtype,
+                               const fp8g_scales *scales, const fp8g_epilogue *epilogue,
+                               uint32_t flags, cudaStream_t stream);
 
 /*
  * fp8g_get_device_status -- synchronise `stream`, then read and clear the
