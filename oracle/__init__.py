@@ -18,6 +18,8 @@ What it computes, with its sources:
 * ``gemm_grouped_masked`` -- the masked grouped variant: only rows
   m < masked_m[g] of each group are computed or written ("一次“转置”，半张
   算力：DeepSeek SwapAB 漂流史", §3.1 and §3.3, valid_m).
+* ``gemm_grouped_contiguous`` -- groups' token rows concatenated along M,
+  group g owning rows offsets[g]..offsets[g+1]-1 and multiplying B[g].
 * ``epilogue`` -- round_mode(act(alpha*S + beta*C + bias)) of exact sums S,
   BF16 rounding to nearest even / toward zero / toward +inf / toward -inf
   (DeepGEMM page §3.3: fused alpha, beta, bias, ReLU and rounding mode).
@@ -119,6 +121,9 @@ def _load():
         lib.oracle_gemm_blockscaled.argtypes = [
             _u8p, _u8p, _i32p, _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _u8p, _i64,
             _u8p, _i64, _i64, _u16p, _f64p, _f64p, ctypes.c_int]
+        lib.oracle_gemm_grouped_contiguous.restype = None
+        lib.oracle_gemm_grouped_contiguous.argtypes = [_u8p, _u8p, _i32p, _i64, _i64, _i64, _i64, ctypes.c_int,
+                                                       ctypes.c_int, _u16p, _f64p, _f64p, ctypes.c_int]
         lib.oracle_round_bf16_mode.restype = ctypes.c_uint16
         lib.oracle_round_bf16_mode.argtypes = [ctypes.c_double, ctypes.c_int]
         lib.oracle_epilogue.restype = None
@@ -325,6 +330,28 @@ def gemm_blockscaled(A: np.ndarray, B: np.ndarray, sfa: np.ndarray, sfb: np.ndar
     if dense:
         out = tuple(x[0] for x in out)
     return out if want_exact else out[:2]
+
+
+def gemm_grouped_contiguous(A: np.ndarray, B: np.ndarray, offsets: np.ndarray, D_init=None, fa: int = E4M3,
+                            fb: int = E4M3, nthreads: int = 0, want_exact: bool = False):
+    """Contiguous grouped oracle: A uint8 [M_total, K] (groups' token rows
+    concatenated), B uint8 [G, N, K], offsets int32 [G+1] (group g owns rows
+    offsets[g] .. offsets[g+1]-1).  Rows outside every group keep D_init's
+    bits.  Returns (D, absdot[, exact])."""
+    A = np.ascontiguousarray(A, np.uint8)
+    B = np.ascontiguousarray(B, np.uint8)
+    M_total, K = A.shape
+    G, N, K2 = B.shape
+    assert K == K2
+    off = np.ascontiguousarray(offsets, np.int32)
+    assert off.shape == (G + 1,) and np.all(np.diff(off) >= 0) and off[0] >= 0 and off[-1] <= M_total
+    D = np.zeros((M_total, N), np.uint16) if D_init is None else np.array(D_init, np.uint16, copy=True, order="C")
+    exact = np.zeros((M_total, N), np.float64)
+    absdot = np.zeros((M_total, N), np.float64)
+    _load().oracle_gemm_grouped_contiguous(_ptr(A, _u8p), _ptr(B, _u8p), _ptr(off, _i32p), G, M_total, N, K, fa,
+                                           fb, _ptr(D, _u16p), _ptr(exact, _f64p), _ptr(absdot, _f64p),
+                                           int(nthreads))
+    return (D, absdot, exact) if want_exact else (D, absdot)
 
 
 ROUND_RN, ROUND_RZ, ROUND_RU, ROUND_RD = 0, 1, 2, 3

@@ -13,6 +13,8 @@
  *   block-scaled  every product a_k b_k multiplied by the UE8M0 scales of
  *           the K group (of 32 or 128 elements) that k falls in, for its
  *           row of A and its row of B, before the sum.
+ *   contiguous  D[r,n] = bf16_rne( sum_k dec(A[r,k]) * dec(B[g,n,k]) ) for the
+ *           rows r of group g in a concatenated [M_total, K] token array.
  *   epilogue  round_mode(act(alpha * S + beta * C + bias)) of any of the
  *           above sums S, with BF16 rounding to nearest even, toward zero,
  *           toward +infinity or toward -infinity.
@@ -578,4 +580,67 @@ void oracle_epilogue(const double *S, const double *absS, int64_t rows, int64_t 
                 absdot[o] = fabs(alpha) * absS[o] + fabs(beta * c) + fabs(b);
         }
     }
+}
+
+/* ---- contiguous grouped layout ------------------------------------------------
+ * "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践" lists grouped
+ * GEMM layouts beside the masked one ("一次“转置”，半张算力：DeepSeek SwapAB
+ * 漂流史" §3.1 names the masked form; the SM100 timeline counts four
+ * layouts).  Reading for the contiguous form: the token rows of all groups
+ * are concatenated along M in group order, group g owning rows
+ * offsets[g] .. offsets[g+1]-1 of A [M_total, K] and of D [M_total, N], and
+ * multiplying B[g] [N, K]:
+ *     D[r, n] = bf16_rne( sum_k dec(A[r, k]) * dec(B[g, n, k]) ),  offsets[g] <= r < offsets[g+1]
+ * Rows outside every group keep D's bits.  offsets is nondecreasing with
+ * 0 <= offsets[0] and offsets[G] <= M_total. */
+typedef struct {
+    const uint8_t *A, *B;
+    const int32_t *offsets;
+    int64_t G, N, K;
+    double ta[256], tb[256];
+    uint16_t *D;
+    double *exact, *absdot;
+} contig_ctx;
+
+static void contig_row(void *vctx, int64_t r)
+{
+    contig_ctx *c = (contig_ctx *)vctx;
+    int64_t g = -1;
+    for (int64_t i = 0; i < c->G; ++i)
+        if (r >= (int64_t)c->offsets[i] && r < (int64_t)c->offsets[i + 1]) {
+            g = i;
+            break;
+        }
+    if (g < 0)
+        return;
+    const uint8_t *a = c->A + r * c->K;
+    for (int64_t n = 0; n < c->N; ++n) {
+        double ad;
+        double s = dot_row(a, c->B + (g * c->N + n) * c->K, c->K, c->ta, c->tb, &ad);
+        int64_t o = r * c->N + n;
+        c->D[o] = oracle_round_bf16(s);
+        if (c->exact)
+            c->exact[o] = s;
+        if (c->absdot)
+            c->absdot[o] = ad;
+    }
+}
+
+void oracle_gemm_grouped_contiguous(const uint8_t *A, const uint8_t *B, const int32_t *offsets, int64_t G,
+                                    int64_t M_total, int64_t N, int64_t K, int fa, int fb, uint16_t *D,
+                                    double *exact, double *absdot, int nthreads)
+{
+    contig_ctx c;
+    c.A = A;
+    c.B = B;
+    c.offsets = offsets;
+    c.G = G;
+    c.N = N;
+    c.K = K;
+    oracle_decode_table(fa, c.ta);
+    oracle_decode_table(fb, c.tb);
+    c.D = D;
+    c.exact = exact;
+    c.absdot = absdot;
+    run_rows(contig_row, &c, M_total, nthreads);
 }

@@ -652,3 +652,48 @@ def test_epilogue_grouped_masked_rows_untouched():
         assert np.array_equal(D[g, mm[g]:], D0[g, mm[g]:])
         want = oracle.round_bf16_array(S[g, :mm[g]] + bias[g][None, :].astype(np.float64))
         assert np.array_equal(D[g, :mm[g]], want)
+
+
+# ---- contiguous grouped layout -------------------------------------------------------
+
+def test_contiguous_equals_per_group_dense_and_keeps_other_rows():
+    G, N, K = 4, 24, 80
+    off = np.array([3, 3, 10, 27, 40], np.int32)          # an empty group, rows 0-2 and 40+ outside
+    M_total = 45
+    A = _rand_codes((M_total, K), 501, 0)
+    B = _rand_codes((G, N, K), 502, 1)
+    D0 = synth.u16_pattern((M_total, N), 503)
+    D, absd = oracle.gemm_grouped_contiguous(A, B, off, D0, 0, 1)
+    for g in range(G):
+        r0, r1 = off[g], off[g + 1]
+        if r1 > r0:
+            ref, ad = oracle.gemm_nt(A[r0:r1], B[g], 0, 1)
+            assert np.array_equal(D[r0:r1], ref) and np.array_equal(absd[r0:r1], ad)
+    assert np.array_equal(D[:3], D0[:3]) and np.array_equal(D[40:], D0[40:])
+
+
+def test_contiguous_equals_masked_layout_rows():
+    """Packing each masked group's valid rows back to back gives the same
+    products as the masked layout (the two layouts hold the same problem)."""
+    G, M_max, N, K = 5, 12, 16, 64
+    A = _rand_codes((G, M_max, K), 504, 0)
+    B = _rand_codes((G, N, K), 505, 0)
+    mm = np.array([4, 0, 12, 7, 1], np.int32)
+    Dm, _ = oracle.gemm_grouped_masked(A, B, mm, np.zeros((G, M_max, N), np.uint16))
+    off = np.concatenate([[0], np.cumsum(mm)]).astype(np.int32)
+    Ac = np.concatenate([A[g, :mm[g]] for g in range(G)])
+    Dc, _ = oracle.gemm_grouped_contiguous(Ac, B, off)
+    assert np.array_equal(Dc, np.concatenate([Dm[g, :mm[g]] for g in range(G)]))
+
+
+def test_contiguous_swapped_weights_move_outputs():
+    """Exchanging two groups' weights exchanges exactly their outputs (a
+    wrong group lookup fails here)."""
+    G, N, K = 3, 8, 32
+    off = np.array([0, 5, 9, 16], np.int32)
+    A = _rand_codes((16, K), 506, 0)
+    B = _rand_codes((G, N, K), 507, 0)
+    D, _ = oracle.gemm_grouped_contiguous(A, B, off)
+    D2, _ = oracle.gemm_grouped_contiguous(A, B[[1, 0, 2]], off)
+    ref, _ = oracle.gemm_nt(A[0:5], B[1])
+    assert np.array_equal(D2[0:5], ref) and np.array_equal(D2[9:], D[9:])
