@@ -107,6 +107,17 @@ def _make_base_workload(name: str, rank: int = 0) -> Workload:
                         "E4M3 N(0,0.5), SwapAB", G=32, M_max=128, N=4096, K=7168, fa=synth.E4M3,
                         fb=synth.E4M3, dist="normal", std=0.5, seed=synth.seed_for(3, rank), bound="hbm",
                         hint=32, flags=1)
+    if name.startswith("grouped:"):
+        # grouped:G:m:N:K[:swap|noswap|auto] -- masked grouped GEMM whose G groups
+        # all hold m valid tokens (the aligned-M grouped benchmark shape)
+        parts = name.split(":")
+        G, m, N, K = int(parts[1]), int(parts[2]), int(parts[3]), int(parts[4])
+        mode = parts[5] if len(parts) > 5 else "auto"
+        label = {"swap": "SwapAB", "noswap": "non-swapped", "auto": "library's choice"}[mode]
+        return Workload(name, "masked", "masked grouped GEMM G=%d, m=%d tokens in every group, N=%d K=%d, "
+                        "E4M3 N(0,0.5), %s" % (G, m, N, K, label), G=G, M_max=m, N=N, K=K, fa=synth.E4M3,
+                        fb=synth.E4M3, dist="normal", std=0.5, seed=synth.seed_for(5, rank), bound="hbm",
+                        hint=m, flags={"swap": 1, "noswap": 2, "auto": 0}[mode], m_fixed=m)
     if name.startswith("smallm"):
         # smallm:M:N:K[:swap|noswap]
         parts = name.split(":")
@@ -136,7 +147,10 @@ def host_inputs(w: Workload):
     else:
         A = synth.normal_fp8((w.G, w.M_max, w.K), w.seed, 0.0, w.std, w.fa)
         B = synth.normal_fp8((w.G, w.N, w.K), w.seed + 100, 0.0, w.std, w.fb)
-        mm = synth.uniform_int(w.G, w.seed + 200, 0, 32).astype(np.int32)
+        if getattr(w, "m_fixed", None) is not None:
+            mm = np.full(w.G, w.m_fixed, np.int32)
+        else:
+            mm = synth.uniform_int(w.G, w.seed + 200, 0, 32).astype(np.int32)
         out = {"A": A, "B": B, "masked_m": mm}
     if w.gran:
         out.update(block_scales(w))

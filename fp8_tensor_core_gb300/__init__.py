@@ -362,15 +362,16 @@ ACT_NONE, ACT_RELU = 0, 1
 ROUND_RN, ROUND_RZ, ROUND_RU, ROUND_RD = 0, 1, 2, 3
 
 
-def _ex_structs(groups, rows, N, K, scale_a, scale_b, sf_a, sf_b, sf_group_k, epilogue):
+def _ex_structs(groups, rows, N, K, scale_a, scale_b, sf_a, sf_b, sf_group_k, epilogue, d_rows=None):
     import torch
+    d_rows = groups * rows if d_rows is None else d_rows      # output rows in all
     sc = None
     if scale_a is not None or scale_b is not None or sf_a is not None or sf_b is not None:
         sc = _lib.Scales()
         if scale_a is not None or scale_b is not None:
             if scale_a is None or scale_b is None:
                 raise ValueError("output scales need both scale_a and scale_b")
-            _check_scale(scale_a, "scale_a", (groups, groups * rows))
+            _check_scale(scale_a, "scale_a", (groups, d_rows))
             _check_scale(scale_b, "scale_b", (groups, groups * N))
             sc.out_a, sc.out_a_len = scale_a.data_ptr(), scale_a.numel()
             sc.out_b, sc.out_b_len = scale_b.data_ptr(), scale_b.numel()
@@ -395,7 +396,7 @@ def _ex_structs(groups, rows, N, K, scale_a, scale_b, sf_a, sf_b, sf_group_k, ep
         ep.beta = float(e.get("beta", 0.0))
         C, bias = e.get("C"), e.get("bias")
         if C is not None:
-            if not C.is_cuda or C.dtype != torch.bfloat16 or not C.is_contiguous() or C.numel() != groups * rows * N:
+            if not C.is_cuda or C.dtype != torch.bfloat16 or not C.is_contiguous() or C.numel() != d_rows * N:
                 raise ValueError("epilogue C must be a contiguous bf16 CUDA tensor shaped like D")
             ep.c = C.data_ptr()
         if bias is not None:
@@ -465,4 +466,39 @@ def fp8_gemm_grouped_masked_ex(A, B, masked_m, D=None, max_m_hint: int = 0, scal
             _stream_handle(stream))
     if rc != OK:
         raise Fp8gError(rc, "fp8_gemm_grouped_masked_ex")
+    return D
+
+
+def fp8_gemm_grouped_contiguous(A, B, group_offsets, D=None, max_m_hint: int = 0, scale_a=None, scale_b=None,
+                                epilogue=None, a_dtype=None, b_dtype=None, flags: int = 0, stream=None):
+    """Contiguous grouped GEMM: A [M_total, K] holds the groups' token rows
+    back to back, group g owning rows group_offsets[g] .. group_offsets[g+1]-1
+    (int32 CUDA tensor [G+1]); B [G, N, K]; D [M_total, N] (rows outside every
+    group untouched).  Optional output scales (scale_a: G or M_total entries,
+    scale_b: G or G*N) and fused epilogue (bias [G, N], C like D)."""
+    import torch
+    _check_operand(A, "A", 2)
+    _check_operand(B, "B", 3)
+    fa, fb = _fp8_code(A, a_dtype), _fp8_code(B, b_dtype)
+    M_total, K = A.shape
+    G, N, K2 = B.shape
+    if K != K2:
+        raise ValueError("K mismatch: A has %d, B has %d" % (K, K2))
+    off = group_offsets
+    if not off.is_cuda or off.dtype != torch.int32 or not off.is_contiguous() or tuple(off.shape) != (G + 1,):
+        raise ValueError("group_offsets must be a contiguous int32 CUDA tensor of shape [G + 1]")
+    sc, ep = _ex_structs(G, M_total, N, K, scale_a, scale_b, None, None, 128, epilogue, d_rows=M_total)
+    if D is None:
+        D = torch.empty((M_total, N), dtype=torch.bfloat16, device=A.device)
+    else:
+        _check_operand(D, "D", 2)
+        if D.dtype != torch.bfloat16 or tuple(D.shape) != (M_total, N):
+            raise ValueError("D must be a contiguous bf16 [M_total, N] tensor")
+    with _on_device(A.device):
+        rc = _lib.load().fp8_gemm_grouped_contiguous_ex(
+            A.data_ptr(), B.data_ptr(), D.data_ptr(), off.data_ptr(), G, M_total, N, K, int(max_m_hint), fa, fb,
+            None if sc is None else ctypes.byref(sc), None if ep is None else ctypes.byref(ep), int(flags),
+            _stream_handle(stream))
+    if rc != OK:
+        raise Fp8gError(rc, "fp8_gemm_grouped_contiguous")
     return D

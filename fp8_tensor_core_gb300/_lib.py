@@ -59,6 +59,12 @@ SIGNATURES = {
     "fp8_gemm_grouped_masked_ex": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _i64, _i64, _i64,
                                                   _i64, _i64, ctypes.c_int, ctypes.c_int, _scales_p, _epi_p,
                                                   ctypes.c_uint32, _c_void_p]),
+    "fp8_gemm_grouped_contiguous": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _i64, _i64, _i64,
+                                                   _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_uint32,
+                                                   _c_void_p]),
+    "fp8_gemm_grouped_contiguous_ex": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _i64, _i64, _i64,
+                                                      _i64, _i64, ctypes.c_int, ctypes.c_int, _scales_p, _epi_p,
+                                                      ctypes.c_uint32, _c_void_p]),
     "fp8_gemm_nt_noalloc": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _i64, _i64,
                                            ctypes.c_int, ctypes.c_int, _c_void_p]),
     "fp8g_get_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), _c_void_p]),

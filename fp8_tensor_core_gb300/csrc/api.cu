@@ -297,6 +297,7 @@ struct Problem {
     const void *A, *B;
     void *D;
     const int32_t *masked_m;
+    const int32_t *group_offsets;   // contiguous layout (rows_a = M_total), else nullptr
     int64_t G, rows_a, N, K;
     int64_t token_hint;   // expected valid tokens per group (<= rows_a)
     int a_dtype, b_dtype;
@@ -373,21 +374,22 @@ void plan_blockscaled(GemmArgs &args, const DeviceInfo &info, int box_b, int gro
 }
 
 // Scale arguments: both pointers given (16-byte aligned device memory), each
-// with one entry per group or one per row (A) / column (B) of every group.
+// with one entry per group or one per output row (A: `row_len` rows in all)
+// / per column of every group (B).
 int check_scales(const float *sa, int64_t sa_len, const float *sb, int64_t sb_len, int64_t G,
-                 int64_t rows, int64_t N, Problem &p)
+                 int64_t row_len, int64_t N, Problem &p)
 {
     if (!sa || !sb)
         return FP8G_ERR_INVALID_ARG;
     if (!aligned16(sa) || !aligned16(sb))
         return FP8G_ERR_MISALIGNED;
-    if (sa_len != G && sa_len != G * rows)
+    if (sa_len != G && sa_len != row_len)
         return FP8G_ERR_INVALID_ARG;
     if (sb_len != G && sb_len != G * N)
         return FP8G_ERR_INVALID_ARG;
     p.scale_a = sa;
     p.scale_b = sb;
-    p.sa_per_row = sa_len == G * rows && rows != 1;
+    p.sa_per_row = sa_len == row_len && row_len != G;
     p.sb_per_col = sb_len == G * N && N != 1;
     return FP8G_OK;
 }
@@ -404,7 +406,7 @@ int launch(const Problem &p, cudaStream_t stream)
     if (mode == 3u)
         return FP8G_ERR_INVALID_ARG;
     bool swap = mode == FP8G_SWAP_ON || (mode == FP8G_SWAP_AUTO && p.token_hint <= kSwapAutoMaxTokens);
-    if (swap && mode == FP8G_SWAP_AUTO && !p.masked_m)
+    if (swap && mode == FP8G_SWAP_AUTO && !p.masked_m && !p.group_offsets)
         swap = swap_beats_token_tiles(p.rows_a, p.N, p.K, info.sms);
     const int num_kb = static_cast<int>(cdiv(p.K, kBlockK));
 
@@ -416,6 +418,7 @@ int launch(const Problem &p, cudaStream_t stream)
     args.groups = static_cast<int32_t>(p.G);
     args.num_kb = num_kb;
     args.masked_m = p.masked_m;
+    args.group_offsets = p.group_offsets;
     args.d = p.D;
     args.a_fmt = static_cast<uint32_t>(p.a_dtype);
     args.b_fmt = static_cast<uint32_t>(p.b_dtype);
@@ -485,7 +488,8 @@ int launch(const Problem &p, cudaStream_t stream)
             if (st != FP8G_OK)
                 return st;
         }
-        if (!make_map(&tm0, p.B, p.K, p.N, p.G, kTileM) || !make_map(&tm1, p.A, p.K, p.rows_a, p.G, 16))
+        if (!make_map(&tm0, p.B, p.K, p.N, p.G, kTileM) ||
+            !make_map(&tm1, p.A, p.K, p.rows_a, p.group_offsets ? 1 : p.G, 16))
             return FP8G_ERR_CUDA;
         if (p.sf_k) {
             // MMA side A = weights (B's scales), side B = tokens (A's scales).
@@ -503,7 +507,8 @@ int launch(const Problem &p, cudaStream_t stream)
 
     // Dense problems with more than one 128-row token tile: two SMs per
     // 256-row tile (cta_group::2), unless single-SM tiles are asked for.
-    if (!p.masked_m && p.G == 1 && p.rows_a > kTileM && !(p.flags & FP8G_SINGLE_SM_TILES) && !p.sf_k) {
+    if (!p.masked_m && !p.group_offsets && p.G == 1 && p.rows_a > kTileM && !(p.flags & FP8G_SINGLE_SM_TILES) &&
+        !p.sf_k) {
         const int64_t m_tiles2 = cdiv(p.rows_a, 2 * kTileM);
         const int pairs = info.sms / 2;
         const PairPlan plan = plan_pair(m_tiles2, p.N, num_kb, pairs, p.flags);
@@ -556,7 +561,7 @@ int launch(const Problem &p, cudaStream_t stream)
     // while the weight tiles stream past them.
     const int64_t band = (48ll << 20) / (kTileM * p.K);
     args.raster_band = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(band, m_tiles)));
-    if (!make_map(&tm0, p.A, p.K, p.rows_a, p.G, kTileM) ||
+    if (!make_map(&tm0, p.A, p.K, p.rows_a, p.group_offsets ? 1 : p.G, kTileM) ||
         !make_map(&tm1, p.B, p.K, p.N, p.G, static_cast<uint32_t>(tile_n)))
         return FP8G_ERR_CUDA;
     if (p.sf_k) {
@@ -590,12 +595,17 @@ int apply_scales(const fp8g_scales *sc, int64_t G, int64_t rows, int64_t N, Prob
         return FP8G_OK;
     int st = FP8G_OK;
     if (sc->out_a || sc->out_b) {
-        st = check_scales(sc->out_a, sc->out_a_len, sc->out_b, sc->out_b_len, G, rows, N, p);
+        st = check_scales(sc->out_a, sc->out_a_len, sc->out_b, sc->out_b_len, G, p.group_offsets ? rows : G * rows,
+                          N, p);
         if (st != FP8G_OK)
             return st;
     }
-    if (sc->block_a || sc->block_b)
+    if (sc->block_a || sc->block_b) {
+        // The A-side scale map's row coordinate would need 16-aligned group offsets.
+        if (p.group_offsets)
+            return FP8G_ERR_UNSUPPORTED;
         st = check_blockscales(sc->block_a, sc->block_a_ld, sc->block_b, sc->block_b_ld, sc->block_k, rows, N, p);
+    }
     return st;
 }
 
@@ -607,7 +617,7 @@ int dense_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_
         return st;
     if (M <= 0 || M > kMaxDim)
         return FP8G_ERR_INVALID_ARG;
-    Problem p{A, B, D, nullptr, 1, M, N, K, M, a_dtype, b_dtype, flags};
+    Problem p{A, B, D, nullptr, nullptr, 1, M, N, K, M, a_dtype, b_dtype, flags};
     if ((st = apply_scales(sc, 1, M, N, p)) != FP8G_OK || (st = check_epilogue(epi, p)) != FP8G_OK)
         return st;
     return launch(p, stream);
@@ -631,7 +641,7 @@ int grouped_ex(const void *A, const void *B, void *D, const int32_t *masked_m, i
     if (!aligned16(masked_m))
         return FP8G_ERR_MISALIGNED;
     const int64_t hint = max_m_hint > 0 ? max_m_hint : M_max;
-    Problem p{A, B, D, masked_m, G, M_max, N, K, hint, a_dtype, b_dtype, flags};
+    Problem p{A, B, D, masked_m, nullptr, G, M_max, N, K, hint, a_dtype, b_dtype, flags};
     if ((st = apply_scales(sc, G, M_max, N, p)) != FP8G_OK || (st = check_epilogue(epi, p)) != FP8G_OK)
         return st;
     cudaPointerAttributes attr;
@@ -644,8 +654,54 @@ int grouped_ex(const void *A, const void *B, void *D, const int32_t *masked_m, i
     return launch(p, stream);
 }
 
+int contiguous_ex(const void *A, const void *B, void *D, const int32_t *offsets, int64_t G, int64_t M_total,
+                  int64_t N, int64_t K, int64_t max_m_hint, int a_dtype, int b_dtype, const fp8g_scales *sc,
+                  const fp8g_epilogue *epi, uint32_t flags, cudaStream_t stream)
+{
+    int st = check_common(A, B, D, N, K, a_dtype, b_dtype);
+    if (st != FP8G_OK)
+        return st;
+    if (!offsets || G <= 0 || M_total <= 0 || M_total > kMaxDim || max_m_hint < 0 || max_m_hint > M_total)
+        return FP8G_ERR_INVALID_ARG;
+    if (G > kMaxGroups)
+        return FP8G_ERR_UNSUPPORTED;
+    if (G * N > kMaxDim)
+        return FP8G_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(offsets) & 3u) != 0)
+        return FP8G_ERR_MISALIGNED;
+    const int64_t hint = max_m_hint > 0 ? max_m_hint : M_total;
+    Problem p{A, B, D, nullptr, offsets, G, M_total, N, K, hint, a_dtype, b_dtype, flags};
+    if ((st = apply_scales(sc, G, M_total, N, p)) != FP8G_OK || (st = check_epilogue(epi, p)) != FP8G_OK)
+        return st;
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, offsets) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8G_ERR_INVALID_ARG;
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+        return FP8G_ERR_INVALID_ARG;
+    return launch(p, stream);
+}
+
 }  // namespace
 }  // namespace fp8g
+
+extern "C" int fp8_gemm_grouped_contiguous(const void *A, const void *B, void *D, const int32_t *group_offsets,
+                                           int64_t G, int64_t M_total, int64_t N, int64_t K, int64_t max_m_hint,
+                                           int a_dtype, int b_dtype, uint32_t flags, cudaStream_t stream)
+{
+    return contiguous_ex(A, B, D, group_offsets, G, M_total, N, K, max_m_hint, a_dtype, b_dtype, nullptr, nullptr,
+                         flags, stream);
+}
+
+extern "C" int fp8_gemm_grouped_contiguous_ex(const void *A, const void *B, void *D, const int32_t *group_offsets,
+                                              int64_t G, int64_t M_total, int64_t N, int64_t K, int64_t max_m_hint,
+                                              int a_dtype, int b_dtype, const fp8g_scales *scales,
+                                              const fp8g_epilogue *epilogue, uint32_t flags, cudaStream_t stream)
+{
+    return contiguous_ex(A, B, D, group_offsets, G, M_total, N, K, max_m_hint, a_dtype, b_dtype, scales, epilogue,
+                         flags, stream);
+}
 
 extern "C" int fp8_gemm_nt(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K,
                            int a_dtype, int b_dtype, uint32_t flags, cudaStream_t stream)

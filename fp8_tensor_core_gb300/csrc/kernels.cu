@@ -69,6 +69,7 @@ struct alignas(16) SmemCtl {
     int32_t pad_;
     int32_t *group_prefix;   // [groups + 1] work units before group g (after this struct)
     int32_t *group_m;        // [groups] valid token rows of group g, clamped
+    int32_t *group_row0;     // [groups] output row of group g's first token row
 };
 static_assert(sizeof(SmemCtl) <= kCtlFixedBytes, "control block too large");
 
@@ -126,13 +127,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_bits, uint32_t hi_bi
 // back at the output" (DeepGEMM page, §3.1), per tensor or per channel
 // (§5.2).  In FP32: (acc * row_factor) * column_factor.
 
-// Factor that is constant along an output row of the token operand (row m of
-// group g): sa(g, m), times sb(g) when B's scale is per tensor.
-__device__ __forceinline__ float row_factor(const GemmArgs &a, int g, int m)
+// Factor that is constant along an output row of the token operand (output
+// row grow, in group g): sa(grow) or sa(g), times sb(g) when B's scale is per
+// tensor.
+__device__ __forceinline__ float row_factor(const GemmArgs &a, int g, int64_t grow)
 {
     float f = 1.0f;
     if (a.scale_a)
-        f = __ldg(a.scale_a + (a.sa_per_row ? static_cast<int64_t>(g) * a.rows_a + m : g));
+        f = __ldg(a.scale_a + (a.sa_per_row ? grow : static_cast<int64_t>(g)));
     if (a.scale_b && !a.sb_per_col)
         f *= __ldg(a.scale_b + g);
     return f;
@@ -230,10 +232,10 @@ __device__ __forceinline__ uint4 epi_pack8(const GemmArgs &a, const float *f, in
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// Output of eight accumulator values (bits) of row `row` of group g at
+// Output of eight accumulator values (bits) of output row `grow` (group g) at
 // columns col..col+7: output scales, then the fused epilogue or a plain
 // round-to-nearest-even.
-__device__ __forceinline__ uint4 out_pack8(const GemmArgs &a, const uint32_t *v, float rf, int g, int64_t row,
+__device__ __forceinline__ uint4 out_pack8(const GemmArgs &a, const uint32_t *v, float rf, int g, int64_t grow,
                                            int col)
 {
     if (!a.epi)
@@ -248,16 +250,16 @@ __device__ __forceinline__ uint4 out_pack8(const GemmArgs &a, const uint32_t *v,
         f[0] *= x.x; f[1] *= x.y; f[2] *= x.z; f[3] *= x.w;
         f[4] *= y.x; f[5] *= y.y; f[6] *= y.z; f[7] *= y.w;
     }
-    return epi_pack8(a, f, g, static_cast<int64_t>(g) * a.rows_a + row, col);
+    return epi_pack8(a, f, g, grow, col);
 }
 
-// One SwapAB output element (token `tok` of group g, column n), value v
-// already scaled.
-__device__ __forceinline__ __nv_bfloat16 out_one(const GemmArgs &a, float v, int g, int tok, int n)
+// One SwapAB output element (output row `grow` of group g, column n), value
+// v already scaled.
+__device__ __forceinline__ __nv_bfloat16 out_one(const GemmArgs &a, float v, int g, int64_t grow, int n)
 {
     if (!a.epi)
         return __float2bfloat16_rn(v);
-    const int64_t idx = (static_cast<int64_t>(g) * a.rows_a + tok) * a.n + n;
+    const int64_t idx = grow * a.n + n;
     const float c = a.c_in ? __bfloat162float(static_cast<const __nv_bfloat16 *>(a.c_in)[idx]) : 0.0f;
     const float b = a.bias ? __ldg(a.bias + static_cast<int64_t>(g) * a.n + n) : 0.0f;
     return __ushort_as_bfloat16(bf16_bits_rounded(epi_value(a, v, c, b), a.round_mode));
@@ -275,18 +277,18 @@ __device__ __forceinline__ float col_factor(const GemmArgs &a, int g, int n)
     return f;
 }
 
-// Per-token factor sa(g, m) when A's scale is per row, else 1.
-__device__ __forceinline__ float token_factor(const GemmArgs &a, int g, int m)
+// Per-token factor sa(grow) when A's scale is per row, else 1.
+__device__ __forceinline__ float token_factor(const GemmArgs &a, int64_t grow)
 {
-    return (a.scale_a && a.sa_per_row) ? __ldg(a.scale_a + static_cast<int64_t>(g) * a.rows_a + m) : 1.0f;
+    return (a.scale_a && a.sa_per_row) ? __ldg(a.scale_a + grow) : 1.0f;
 }
 
 // ---- block scales --------------------------------------------------------------
 // Per-group scales of the K dimension ("DeepGEMM：基于 Hopper Tensor Core 的 FP8
-// 矩阵乘法内核优化实践" §5.2, groups of 128 elements; UE8M0 scale factors in its
-// SM100 timeline) applied by the tensor core itself: kind::mxf8f6f4 with one
-// scale factor per row per 32 K elements, read from TMEM ("一次“转置”，半张算力：
-// DeepSeek SwapAB 漂流史" §3.4 shows the A- and B-side scale-factor columns).
+// 矩阵乘法内核优化实践" §5.2, groups of 128 elements) applied by the tensor core
+// itself: kind::mxf8f6f4 with one UE8M0 scale factor per row per 32 K
+// elements, read from TMEM ("一次“转置”，半张算力：DeepSeek SwapAB 漂流史" §5:
+// UE8M0 scales on SM100; §3.4: the A- and B-side scale-factor columns).
 
 // A scale load brings four K groups per row (TMA box {rows, 4}), as bytes
 // [group][row].  With 128-element groups (sf_k = 1) one load serves four K
@@ -384,13 +386,31 @@ __device__ void build_group_table(SmemCtl &ctl, const GemmArgs &a, UnitsFn units
         const int g = base + lane;
         int cnt = 0;
         if (g < a.groups) {
-            int m = a.masked_m ? __ldg(a.masked_m + g) : a.rows_a;
-            if (m < 0 || m > a.rows_a) {
-                if (blockIdx.x == 0)
-                    record_status(FP8G_ERR_MASKED_M_RANGE, kRoleScheduler, g);
-                m = m < 0 ? 0 : a.rows_a;
+            int m, r0;
+            if (a.group_offsets) {
+                // Contiguous layout: rows offsets[g] .. offsets[g+1]-1; a group
+                // whose extent is not inside [0, rows_a] is flagged and skipped.
+                const int lo = __ldg(a.group_offsets + g), hi = __ldg(a.group_offsets + g + 1);
+                if (lo < 0 || hi < lo || hi > a.rows_a) {
+                    if (blockIdx.x == 0)
+                        record_status(FP8G_ERR_MASKED_M_RANGE, kRoleScheduler, g);
+                    m = 0;
+                    r0 = 0;
+                } else {
+                    m = hi - lo;
+                    r0 = lo;
+                }
+            } else {
+                m = a.masked_m ? __ldg(a.masked_m + g) : a.rows_a;
+                if (m < 0 || m > a.rows_a) {
+                    if (blockIdx.x == 0)
+                        record_status(FP8G_ERR_MASKED_M_RANGE, kRoleScheduler, g);
+                    m = m < 0 ? 0 : a.rows_a;
+                }
+                r0 = g * a.rows_a;
             }
             ctl.group_m[g] = m;
+            ctl.group_row0[g] = r0;
             cnt = units_of(m);
         }
         int x = cnt;
@@ -409,6 +429,14 @@ __device__ void build_group_table(SmemCtl &ctl, const GemmArgs &a, UnitsFn units
         ctl.units_total = running;
     }
 }
+
+// TMA coordinates (row, group) of token row m of group g in A: the 3-D
+// [groups, rows_a, k] map, or the contiguous layout's [1, rows_a, k] map.
+__device__ __forceinline__ int a_row(const GemmArgs &a, const SmemCtl &ctl, int g, int m)
+{
+    return a.group_offsets ? ctl.group_row0[g] + m : m;
+}
+__device__ __forceinline__ int a_grp(const GemmArgs &a, int g) { return a.group_offsets ? 0 : g; }
 
 // Group g with prefix[g] <= u < prefix[g+1].
 __device__ __forceinline__ int find_group(const SmemCtl &ctl, int groups, int u)
@@ -443,6 +471,7 @@ __device__ __forceinline__ Smem carve(uint8_t *raw, const GemmArgs &a)
     int32_t *tables = reinterpret_cast<int32_t *>(reinterpret_cast<uint8_t *>(s.ctl) + kCtlFixedBytes);
     s.ctl->group_prefix = tables;
     s.ctl->group_m = tables + a.groups + 1;
+    s.ctl->group_row0 = tables + 2 * a.groups + 1;
     return s;
 }
 
@@ -603,7 +632,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
                     const uint32_t fb = smem_addr(&ctl.full[stage]);
                     const bool sf = a.sf_k && sf_load_at(kb, 0, a.sf_k);
                     mbar_arrive_expect_tx(fb, tx_bytes + (sf ? sf_bytes : 0u));
-                    tma_load_3d(smem_addr(sa), &tm_a, fb, kb * kBlockK, m0, g);
+                    tma_load_3d(smem_addr(sa), &tm_a, fb, kb * kBlockK, a_row(a, ctl, g, m0), a_grp(a, g));
                     tma_load_3d(smem_addr(sa + a_bytes), &tm_b, fb, kb * kBlockK, n0, g);
                     if (sf) {
                         const int y = sf_first_group(kb, a.sf_k);
@@ -733,11 +762,11 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
             tc_fence_after();
             const int row = m0 + q * 32 + lane;
             const bool row_ok = row < mv;
-            __nv_bfloat16 *drow =
-                dout + (static_cast<int64_t>(g) * a.rows_a + row) * static_cast<int64_t>(a.n);
+            const int64_t grow = static_cast<int64_t>(ctl.group_row0[g]) + row;
+            __nv_bfloat16 *drow = dout + grow * static_cast<int64_t>(a.n);
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * acc_stride);
-            const float rf = row_ok ? row_factor(a, g, row) : 1.0f;
+            const float rf = row_ok ? row_factor(a, g, grow) : 1.0f;
             for (int c = 0; c < a.tile_n; c += 32) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c), r);
@@ -746,7 +775,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
                     for (int j = 0; j < 4; ++j) {
                         const int col = n0 + c + 8 * j;
                         if (col < a.n)
-                            *reinterpret_cast<uint4 *>(drow + col) = out_pack8(a, r + 8 * j, rf, g, row, col);
+                            *reinterpret_cast<uint4 *>(drow + col) = out_pack8(a, r + 8 * j, rf, g, grow, col);
                     }
                 }
             }
@@ -1342,7 +1371,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
                     tma_load_3d_hint(smem_addr(sw), &tm_w, fb, kb * kBlockK, x.w0, x.g, w_policy);
                     for (int r = 0; r < x.n_mma; r += kTokBox)
                         tma_load_3d(smem_addr(sw + w_bytes + (r / kTokBox) * kTokBoxBytes), &tm_t, fb,
-                                    kb * kBlockK, x.tok0 + r, x.g);
+                                    kb * kBlockK, a_row(a, ctl, x.g, x.tok0 + r), a_grp(a, x.g));
                     if (sf) {
                         const int y = sf_first_group(kb, a.sf_k);
                         tma_load_3d_hint(smem_addr(sw + a.sf_off), &tm_sw, fb, x.w0, y, x.g, w_policy);
@@ -1485,8 +1514,8 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
             const bool n_ok = nrow < a.n;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * acc_stride);
-            __nv_bfloat16 *dcol = dout + static_cast<int64_t>(x.g) * a.rows_a * static_cast<int64_t>(a.n) +
-                                  nrow;
+            const int64_t grow0 = static_cast<int64_t>(ctl.group_row0[x.g]) + x.tok0;   // output row of token 0
+            __nv_bfloat16 *dcol = dout + grow0 * static_cast<int64_t>(a.n) + nrow;
             const bool whole = x.kb0 == 0 && x.kb1 == num_kb;
             const float cf = n_ok ? col_factor(a, x.g, nrow) : 1.0f;
             if (whole) {
@@ -1497,9 +1526,9 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             if (c + j < x.n_tok)
-                                dcol[static_cast<int64_t>(x.tok0 + c + j) * a.n] =
-                                    out_one(a, __uint_as_float(r[j]) * cf * token_factor(a, x.g, x.tok0 + c + j),
-                                            x.g, x.tok0 + c + j, nrow);
+                                dcol[static_cast<int64_t>(c + j) * a.n] =
+                                    out_one(a, __uint_as_float(r[j]) * cf * token_factor(a, grow0 + c + j), x.g,
+                                            grow0 + c + j, nrow);
                         }
                     }
                 }
@@ -1573,9 +1602,9 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
 #pragma unroll
                             for (int j = 0; j < 16; ++j) {
                                 if (c + j < x.n_tok)
-                                    dcol[static_cast<int64_t>(x.tok0 + c + j) * a.n] =
-                                        out_one(a, acc_v[j] * cf * token_factor(a, x.g, x.tok0 + c + j), x.g,
-                                                x.tok0 + c + j, nrow);
+                                    dcol[static_cast<int64_t>(c + j) * a.n] =
+                                        out_one(a, acc_v[j] * cf * token_factor(a, grow0 + c + j), x.g,
+                                                grow0 + c + j, nrow);
                             }
                         }
                     }

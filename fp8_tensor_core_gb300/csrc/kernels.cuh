@@ -20,11 +20,11 @@ constexpr int kAccStride = 256;
 constexpr int kCtlFixedBytes = 768;  // barriers, TMEM slot, flags
 constexpr int kSmemAlignPad = 1024;  // dynamic smem base rounded up to 1024 B
 
-// Control block: fixed part plus two int32 tables per group (unit prefix,
-// valid rows), rounded up to 128 bytes.
+// Control block: fixed part plus three int32 tables per group (unit prefix,
+// valid rows, first output row), rounded up to 128 bytes.
 inline int ctl_bytes_for(int groups)
 {
-    const int b = kCtlFixedBytes + 4 * (2 * groups + 1);
+    const int b = kCtlFixedBytes + 4 * (3 * groups + 1);
     return (b + 127) & ~127;
 }
 
@@ -40,6 +40,9 @@ struct GemmArgs {
     int32_t groups;
     int32_t num_kb;            // ceil(k / kBlockK)
     const int32_t *masked_m;   // device [groups] or nullptr (all rows valid)
+    const int32_t *group_offsets;  // contiguous layout: device [groups + 1]; group g owns rows
+                               // offsets[g] .. offsets[g+1]-1 of A [rows_a, k] and D [rows_a, n]
+                               // (rows_a = M_total); nullptr: the [groups, rows_a] layouts
     void *d;
     // Tiling.
     int32_t tile_n;            // mn kernel: N tile (32..256, multiple of 32)

@@ -9,6 +9,7 @@
  *   ..._blockscaled          UE8M0 scales per row per 32/128-element K group
  *   ..._ex                   any of those plus a fused epilogue (alpha, beta*C,
  *                            bias, ReLU, rounding mode)
+ *   fp8_gemm_grouped_contiguous  groups' token rows concatenated along M
  *   fp8_gemm_nt_noalloc      dense small-token form that allocates nothing
  *
  * A and B hold FP8 codes (E4M3 or E5M2, chosen per operand), products are
@@ -186,9 +187,9 @@ int fp8_gemm_grouped_masked_scaled(const void *A, const void *B, void *D,
  *   D[g,m,n] = bf16( sum_k A[g,m,k] B[g,n,k]
  *                    * 2^(sf_a[g][k/gs][m] - 127) * 2^(sf_b[g][k/gs][n] - 127) )
  * Source: "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践"
- * §5.2 (scales per group of 128 elements) and its SM100 timeline (UE8M0
- * scales); "一次“转置”，半张算力：DeepSeek SwapAB 漂流史" §3.4 (the
- * Blackwell MMA takes A- and B-side scale factors).  The tensor core applies
+ * §5.2 (scales per group of 128 elements); "一次“转置”，半张算力：DeepSeek
+ * SwapAB 漂流史" §5 (UE8M0 scales on SM100) and §3.4 (the Blackwell MMA
+ * takes A- and B-side scale factors).  The tensor core applies
  * the scales (tcgen05.mma kind::mxf8f6f4.block_scale).
  *   sf_a   DEVICE bytes [G][ceil(K/gs)][sf_a_ld]: the scale of row m of A
  *          (token row) for K group j at sf_a[(g*ks + j)*sf_a_ld + m];
@@ -275,6 +276,35 @@ int fp8_gemm_grouped_masked_ex(const void *A, const void *B, void *D, const int3
                                int64_t max_m_hint, int a_dtype, int b_dtype,
                                const fp8g_scales *scales, const fp8g_epilogue *epilogue,
                                uint32_t flags, cudaStream_t stream);
+
+/*
+ * fp8_gemm_grouped_contiguous / _ex -- grouped GEMM with the groups' token
+ * rows concatenated along M (the MoE prefill form, beside the masked decode
+ * form; "一次“转置”，半张算力：DeepSeek SwapAB 漂流史" §5 counts four grouped
+ * layouts on SM100 without describing them -- this is the plainest reading):
+ *   D[r, n] = sum_k A[r, k] * B[g, n, k]   for group_offsets[g] <= r < group_offsets[g+1]
+ *   A              [M_total, K] FP8 codes, row-major.
+ *   B              [G, N, K] FP8 codes.
+ *   D              [M_total, N] BF16; rows outside every group are not written.
+ *   group_offsets  DEVICE int32 [G+1], nondecreasing, 0 <= offsets[0],
+ *                  offsets[G] <= M_total; group boundaries need no alignment.
+ *                  A group whose extent breaks this is skipped and reported as
+ *                  FP8G_ERR_MASKED_M_RANGE by fp8g_get_device_status().
+ *   max_m_hint     expected largest group (0: M_total); picks SwapAB under AUTO.
+ * Output scales (out_a: G or M_total entries, out_b: G or G*N) and the fused
+ * epilogue (bias [G][N], C shaped like D) as in the _ex calls; block scales
+ * are not supported with this layout (FP8G_ERR_UNSUPPORTED).
+ */
+int fp8_gemm_grouped_contiguous(const void *A, const void *B, void *D,
+                                const int32_t *group_offsets, int64_t G, int64_t M_total,
+                                int64_t N, int64_t K, int64_t max_m_hint, int a_dtype,
+                                int b_dtype, uint32_t flags, cudaStream_t stream);
+int fp8_gemm_grouped_contiguous_ex(const void *A, const void *B, void *D,
+                                   const int32_t *group_offsets, int64_t G, int64_t M_total,
+                                   int64_t N, int64_t K, int64_t max_m_hint, int a_dtype,
+                                   int b_dtype, const fp8g_scales *scales,
+                                   const fp8g_epilogue *epilogue, uint32_t flags,
+                                   cudaStream_t stream);
 
 /*
  * fp8g_get_device_status -- synchronise `stream`, then read and clear the

@@ -25,8 +25,8 @@ What it computes, with its sources:
   (DeepGEMM page §3.3: fused alpha, beta, bias, ReLU and rounding mode).
 * ``gemm_blockscaled`` -- every product scaled by the UE8M0 factors of its
   K group (32 or 128 elements) for its A row and B row, then summed and
-  rounded once (DeepGEMM page §5.2 per-128-element groups, UE8M0 scales in
-  its SM100 timeline; SwapAB page §3.4, scale factors in the Blackwell MMA).
+  rounded once (DeepGEMM page §5.2 per-128-element groups; SwapAB page §5,
+  UE8M0 scales on SM100, and §3.4, scale factors in the Blackwell MMA).
 * ``gemm_nt_scaled`` / ``gemm_grouped_masked_scaled`` -- the same products
   multiplied back by per-tensor or per-channel FP32 scales before the one
   rounding (DeepGEMM page §3.1 and §5.2).

@@ -461,10 +461,10 @@ void oracle_gemm_grouped_masked_scaled(const uint8_t *A, const uint8_t *B,
 
 /* ---- block-scaled variant ---------------------------------------------------
  * "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践" §5.2: scales
- * may be kept per group of 128 elements; the same page's timeline gives the
- * SM100 form as UE8M0 ("packed") scale factors, and "一次“转置”，半张算力：
- * DeepSeek SwapAB 漂流史" §3.4 shows the Blackwell MMA consuming A- and
- * B-side scale factors.  Reading: with gran in {32, 128} and KS = ceil(K/gran),
+ * may be kept per group of 128 elements; "一次“转置”，半张算力：DeepSeek SwapAB
+ * 漂流史" §5 (timeline) gives the SM100 form as UE8M0 ("packed") scale
+ * factors and §3.4 shows the Blackwell MMA consuming A- and B-side scale
+ * factors.  Reading: with gran in {32, 128} and KS = ceil(K/gran),
  *     D[g,m,n] = bf16_rne( sum_k dec(A[g,m,k]) dec(B[g,n,k])
  *                          * 2^(SA[g][k/gran][m] - 127) * 2^(SB[g][k/gran][n] - 127) )
  * SA is [G][KS][lda] bytes (row m of A at byte m of each K group's vector),
@@ -583,10 +583,9 @@ void oracle_epilogue(const double *S, const double *absS, int64_t rows, int64_t 
 }
 
 /* ---- contiguous grouped layout ------------------------------------------------
- * "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践" lists grouped
- * GEMM layouts beside the masked one ("一次“转置”，半张算力：DeepSeek SwapAB
- * 漂流史" §3.1 names the masked form; the SM100 timeline counts four
- * layouts).  Reading for the contiguous form: the token rows of all groups
+ * "一次“转置”，半张算力：DeepSeek SwapAB 漂流史" §3.1 names the masked grouped
+ * form and its §5 timeline counts four grouped layouts on SM100 without
+ * describing the others.  Reading for the contiguous form: the token rows of all groups
  * are concatenated along M in group order, group g owning rows
  * offsets[g] .. offsets[g+1]-1 of A [M_total, K] and of D [M_total, N], and
  * multiplying B[g] [N, K]:
