@@ -102,11 +102,14 @@ def _make_base_workload(name: str, rank: int = 0) -> Workload:
                         % (N, K, "E5M2" if fb else "E4M3"),
                         M=8192, N=N, K=K, fa=synth.E4M3, fb=fb, dist="normal", std=0.5,
                         seed=synth.seed_for(2, rank), bound="tensor", flags=0)
-    if name == "masked":
+    if name == "masked" or name.startswith("masked:"):
+        # masked[:swap|noswap|auto] -- the MoE-decode workload (SwapAB unless asked otherwise)
+        mode = name.split(":")[1] if ":" in name else "swap"
+        label = {"swap": "SwapAB", "noswap": "non-swapped", "auto": "library's choice"}[mode]
         return Workload(name, "masked", "masked grouped GEMM G=32 M_max=128 N=4096 K=7168, m_g~U{0..32}, "
-                        "E4M3 N(0,0.5), SwapAB", G=32, M_max=128, N=4096, K=7168, fa=synth.E4M3,
+                        "E4M3 N(0,0.5), %s" % label, G=32, M_max=128, N=4096, K=7168, fa=synth.E4M3,
                         fb=synth.E4M3, dist="normal", std=0.5, seed=synth.seed_for(3, rank), bound="hbm",
-                        hint=32, flags=1)
+                        hint=32, flags={"swap": 1, "noswap": 2, "auto": 0}[mode])
     if name.startswith("grouped:"):
         # grouped:G:m:N:K[:swap|noswap|auto] -- masked grouped GEMM whose G groups
         # all hold m valid tokens (the aligned-M grouped benchmark shape)

@@ -276,20 +276,31 @@ PairPlan plan_pair(int64_t m_tiles2, int64_t N, int num_kb, int pairs, uint32_t 
     return best;
 }
 
-// Dense problems with few tokens stream the weights once either way.  SwapAB
-// with stream-K keeps every SM streaming but pays a partial-tile reduction;
-// 128-row token tiles need no reduction but only one CTA per N tile, and a
-// single SM streams at most ~55 GB/s.  Estimated times (measured constants on
-// GB300: 6.7 TB/s HBM, ~5 us and ~8 us fixed costs) pick the faster.
-bool swap_beats_token_tiles(int64_t M, int64_t N, int64_t K, int sms)
+// SwapAB or 128-row token tiles, for G groups of (up to) M tokens each.
+// Both stream every weight byte once.  Token tiles: one CTA per weight tile,
+// so few tiles leave SMs idle and one SM streams at most ~55 GB/s; no
+// reduction.  SwapAB with stream-K keeps every SM streaming but pays a
+// partial-tile reduction, and its per-K-block MMA work grows with the tokens
+// (measured ~9.8 ns per K block per token on GB300).  Estimated times
+// (measured constants: 6.7 TB/s HBM, ~5 us and ~8 us fixed costs) pick the
+// faster.  Measured on GB300 for grouped shapes (16 or 32 experts, N x K of
+// 4096 x 7168 or 7168 x 2048): token tiles won at every token count from 8
+// to 256; SwapAB wins when the tiles are too few to fill the GPU (dense
+// small-M, few groups).
+bool swap_beats_token_tiles(int64_t G, int64_t M, int64_t N, int64_t K, int sms)
 {
-    const double bytes = static_cast<double>(N) * K + static_cast<double>(M) * K + 2.0 * M * N;
+    const double bytes = static_cast<double>(G) * (static_cast<double>(N) * K + static_cast<double>(M) * K +
+                                                   2.0 * M * N);
     const double hbm = 6.7e12, per_sm = 55e9;
-    const int tn = pick_tile_n(1, N, sms);
-    const int64_t tiles = cdiv(N, tn);
+    const int64_t m_tiles = G * cdiv(M, kTileM);
+    const int tn = pick_tile_n(m_tiles, N, sms);
+    const int64_t tiles = m_tiles * cdiv(N, tn);
     const double per_cta = static_cast<double>(tn) * K;
-    const double t_tiles = std::max(bytes / hbm, per_cta * static_cast<double>(cdiv(tiles, sms)) / per_sm) + 5e-6;
-    const double t_swap = bytes / hbm + 8e-6;
+    const double t_tiles =
+        std::max(bytes / hbm, per_cta * static_cast<double>(cdiv(tiles, sms)) / per_sm) + 5e-6;
+    const double kblocks = static_cast<double>(G) * cdiv(N, kTileM) * cdiv(K, kBlockK);
+    const double t_mma = kblocks * static_cast<double>(cdiv(M, 16) * 16) * 9.8e-9 / sms;
+    const double t_swap = std::max(bytes / hbm, t_mma) + 8e-6;
     return t_swap < t_tiles;
 }
 
@@ -406,8 +417,8 @@ int launch(const Problem &p, cudaStream_t stream)
     if (mode == 3u)
         return FP8G_ERR_INVALID_ARG;
     bool swap = mode == FP8G_SWAP_ON || (mode == FP8G_SWAP_AUTO && p.token_hint <= kSwapAutoMaxTokens);
-    if (swap && mode == FP8G_SWAP_AUTO && !p.masked_m && !p.group_offsets)
-        swap = swap_beats_token_tiles(p.rows_a, p.N, p.K, info.sms);
+    if (swap && mode == FP8G_SWAP_AUTO)
+        swap = swap_beats_token_tiles(p.G, p.token_hint, p.N, p.K, info.sms);
     const int num_kb = static_cast<int>(cdiv(p.K, kBlockK));
 
     GemmArgs args;
