@@ -253,34 +253,60 @@ __device__ __forceinline__ uint4 out_pack8(const GemmArgs &a, const uint32_t *v,
     return epi_pack8(a, f, g, grow, col);
 }
 
-// One SwapAB output element (output row `grow` of group g, column n), value
-// v already scaled.
-__device__ __forceinline__ __nv_bfloat16 out_one(const GemmArgs &a, float v, int g, int64_t grow, int n)
+// Transpose the 8x8 blocks held by each group of 8 lanes: lane 8g+t holds
+// x[i] = row t, column i of its group's block on entry and x[i] = row i,
+// column t on return.  Three butterfly stages of shuffles, each exchanging
+// the off-diagonal halves at one bit of the lane index.
+__device__ __forceinline__ void transpose8x8(uint32_t (&x)[8])
 {
-    if (!a.epi)
-        return __float2bfloat16_rn(v);
-    const int64_t idx = grow * a.n + n;
-    const float c = a.c_in ? __bfloat162float(static_cast<const __nv_bfloat16 *>(a.c_in)[idx]) : 0.0f;
-    const float b = a.bias ? __ldg(a.bias + static_cast<int64_t>(g) * a.n + n) : 0.0f;
-    return __ushort_as_bfloat16(bf16_bits_rounded(epi_value(a, v, c, b), a.round_mode));
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int m = 4; m >= 1; m >>= 1) {
+        const bool hi = (lane & m) != 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if ((i & m) == 0) {
+                const uint32_t send = hi ? x[i] : x[i | m];
+                const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, m);
+                if (hi)
+                    x[i] = recv;
+                else
+                    x[i | m] = recv;
+            }
+        }
+    }
 }
 
-// SwapAB epilogue: thread = output column n (weight row), registers = tokens.
-// Column factor sb(g, n) (times sa(g) when A's scale is per tensor).
-__device__ __forceinline__ float col_factor(const GemmArgs &a, int g, int n)
+// SwapAB output of 16 tokens: on entry lane `lane` of the warp holds
+// accumulator values (bits) v[j] of weight row (= output column) col_base +
+// lane for tokens tok0+j, j < 16.  Two in-warp 8x8 transposes give lane 8g+t
+// the columns col_base + 8g .. +7 of tokens tok0 + t and tok0 + 8 + t, which
+// it writes as two 16-byte stores through out_pack8 (scales, fused
+// epilogue): 2 store instructions per lane instead of 16 scalar ones.
+__device__ __forceinline__ void swap_store16(const GemmArgs &a, __nv_bfloat16 *dout, const uint32_t (&v)[16],
+                                             int g, int64_t grow_tok0, int n_valid, int col_base)
 {
-    float f = 1.0f;
-    if (a.scale_b)
-        f = __ldg(a.scale_b + (a.sb_per_col ? static_cast<int64_t>(g) * a.n + n : g));
-    if (a.scale_a && !a.sa_per_row)
-        f *= __ldg(a.scale_a + g);
-    return f;
-}
-
-// Per-token factor sa(grow) when A's scale is per row, else 1.
-__device__ __forceinline__ float token_factor(const GemmArgs &a, int64_t grow)
-{
-    return (a.scale_a && a.sa_per_row) ? __ldg(a.scale_a + grow) : 1.0f;
+    const int lane = threadIdx.x & 31;
+    const int t = lane & 7;
+    const int col = col_base + 8 * (lane >> 3);
+    uint32_t lo[8], hi[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        lo[i] = v[i];
+        hi[i] = v[8 + i];
+    }
+    transpose8x8(lo);
+    transpose8x8(hi);
+    if (col < a.n) {
+        if (t < n_valid) {
+            const int64_t grow = grow_tok0 + t;
+            *reinterpret_cast<uint4 *>(dout + grow * a.n + col) = out_pack8(a, lo, row_factor(a, g, grow), g, grow, col);
+        }
+        if (8 + t < n_valid) {
+            const int64_t grow = grow_tok0 + 8 + t;
+            *reinterpret_cast<uint4 *>(dout + grow * a.n + col) = out_pack8(a, hi, row_factor(a, g, grow), g, grow, col);
+        }
+    }
 }
 
 // ---- block scales --------------------------------------------------------------
@@ -1126,6 +1152,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const long long t0 = static_cast<long long>(x.tile) * num_kb;
                 const int first = pair_of(t0);
                 const int n_contrib = pair_of(t0 + num_kb - 1) - first + 1;
+                // Pairs after the first start their range inside this tile
+                // (slot kind 0); only the first pair's range may have begun
+                // in an earlier tile.
+                const int kind_first = range_begin(first) >= t0 ? 0 : 1;
                 if (prev == n_contrib - 1) {
                     // Tile complete: sum the contributions in K order, two
                     // contributors' 32 columns per batch (unconditional loads).
@@ -1140,8 +1170,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             for (int i = 0; i < 2; ++i) {
                                 const int ci = (p0 + i < n_contrib) ? p0 + i : 0;
                                 const int pr = first + ci;
-                                const int kind =
-                                    (range_begin(pr) / num_kb == static_cast<long long>(x.tile)) ? 0 : 1;
+                                const int kind = ci == 0 ? kind_first : 0;
                                 const float4 *src = slots +
                                                     ((static_cast<int64_t>(2 * pr) + rank) * 2 + kind) * part4 +
                                                     (c / 4) * kTileM + row;
@@ -1510,27 +1539,16 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
                            200 + acc))
                 break;
             tc_fence_after();
-            const int nrow = x.w0 + row;
-            const bool n_ok = nrow < a.n;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * acc_stride);
             const int64_t grow0 = static_cast<int64_t>(ctl.group_row0[x.g]) + x.tok0;   // output row of token 0
-            __nv_bfloat16 *dcol = dout + grow0 * static_cast<int64_t>(a.n) + nrow;
+            const int col_base = x.w0 + q * 32;                                         // this warp's 32 columns
             const bool whole = x.kb0 == 0 && x.kb1 == num_kb;
-            const float cf = n_ok ? col_factor(a, x.g, nrow) : 1.0f;
             if (whole) {
                 for (int c = 0; c < x.n_mma; c += 16) {
                     uint32_t r[16];
                     tmem_ld_32x32b_x16(t_row + static_cast<uint32_t>(c), r);
-                    if (n_ok) {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            if (c + j < x.n_tok)
-                                dcol[static_cast<int64_t>(c + j) * a.n] =
-                                    out_one(a, __uint_as_float(r[j]) * cf * token_factor(a, grow0 + c + j), x.g,
-                                            grow0 + c + j, nrow);
-                        }
-                    }
+                    swap_store16(a, dout, r, x.g, grow0 + c, x.n_tok - c, col_base);
                 }
             } else {
                 // Contributors of this tile: the CTAs whose ranges meet it,
@@ -1538,6 +1556,11 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
                 const long long t0 = static_cast<long long>(x.tile) * num_kb;
                 const int first = cta_of(t0);
                 const int n_contrib = cta_of(t0 + num_kb - 1) - first + 1;
+                // Every contributor after the first starts its range inside
+                // this tile, so the tile is its first segment (slot kind 0);
+                // the first contributor's range may have begun in an earlier
+                // tile.  (No division inside the reduction loop.)
+                const int kind_first = range_begin(first) >= t0 ? 0 : 1;
                 float4 *mine = slots + (static_cast<int64_t>(blockIdx.x) * 2 + x.kind) * part_stride4;
                 for (int c = 0; c < x.n_mma; c += 16) {
                     uint32_t r[16];
@@ -1569,8 +1592,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
                             for (int i = 0; i < 4; ++i) {
                                 const int ci = (p0 + i < n_contrib) ? p0 + i : 0;
                                 const int cta = first + ci;
-                                const int kind =
-                                    (range_begin(cta) / num_kb == static_cast<long long>(x.tile)) ? 0 : 1;
+                                const int kind = ci == 0 ? kind_first : 0;
                                 const float4 *src = slots + (static_cast<int64_t>(cta) * 2 + kind) * part_stride4 +
                                                     (c / 4) * kTileM + row;
 #pragma unroll
@@ -1598,15 +1620,11 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
                                 }
                             }
                         }
-                        if (n_ok) {
+                        uint32_t bits_v[16];
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                if (c + j < x.n_tok)
-                                    dcol[static_cast<int64_t>(c + j) * a.n] =
-                                        out_one(a, acc_v[j] * cf * token_factor(a, grow0 + c + j), x.g,
-                                                grow0 + c + j, nrow);
-                            }
-                        }
+                        for (int j = 0; j < 16; ++j)
+                            bits_v[j] = __float_as_uint(acc_v[j]);
+                        swap_store16(a, dout, bits_v, x.g, grow0 + c, x.n_tok - c, col_base);
                     }
                 }
             }
