@@ -253,6 +253,25 @@ __device__ __forceinline__ uint4 out_pack8(const GemmArgs &a, const uint32_t *v,
     return epi_pack8(a, f, g, grow, col);
 }
 
+// Eight FP32 accumulator values (bits) rounded to nearest even and packed.
+__device__ __forceinline__ uint4 plain_pack8(const uint32_t *v)
+{
+    return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                      pack_bf16x2(v[6], v[7]));
+}
+
+// Kernels are instantiated with and without the scale / fused-epilogue store
+// path, so that the plain GEMM carries none of its code.
+template <bool kEpi>
+__device__ __forceinline__ uint4 store_pack8(const GemmArgs &a, const uint32_t *v, float rf, int g, int64_t grow,
+                                             int col)
+{
+    if constexpr (kEpi)
+        return out_pack8(a, v, rf, g, grow, col);
+    else
+        return plain_pack8(v);
+}
+
 // Transpose the 8x8 blocks held by each group of 8 lanes: lane 8g+t holds
 // x[i] = row t, column i of its group's block on entry and x[i] = row i,
 // column t on return.  Three butterfly stages of shuffles, each exchanging
@@ -283,6 +302,7 @@ __device__ __forceinline__ void transpose8x8(uint32_t (&x)[8])
 // the columns col_base + 8g .. +7 of tokens tok0 + t and tok0 + 8 + t, which
 // it writes as two 16-byte stores through out_pack8 (scales, fused
 // epilogue): 2 store instructions per lane instead of 16 scalar ones.
+template <bool kEpi>
 __device__ __forceinline__ void swap_store16(const GemmArgs &a, __nv_bfloat16 *dout, const uint32_t (&v)[16],
                                              int g, int64_t grow_tok0, int n_valid, int col_base)
 {
@@ -300,11 +320,13 @@ __device__ __forceinline__ void swap_store16(const GemmArgs &a, __nv_bfloat16 *d
     if (col < a.n) {
         if (t < n_valid) {
             const int64_t grow = grow_tok0 + t;
-            *reinterpret_cast<uint4 *>(dout + grow * a.n + col) = out_pack8(a, lo, row_factor(a, g, grow), g, grow, col);
+            *reinterpret_cast<uint4 *>(dout + grow * a.n + col) =
+                store_pack8<kEpi>(a, lo, kEpi ? row_factor(a, g, grow) : 1.0f, g, grow, col);
         }
         if (8 + t < n_valid) {
             const int64_t grow = grow_tok0 + 8 + t;
-            *reinterpret_cast<uint4 *>(dout + grow * a.n + col) = out_pack8(a, hi, row_factor(a, g, grow), g, grow, col);
+            *reinterpret_cast<uint4 *>(dout + grow * a.n + col) =
+                store_pack8<kEpi>(a, hi, kEpi ? row_factor(a, g, grow) : 1.0f, g, grow, col);
         }
     }
 }
@@ -574,6 +596,7 @@ __device__ __forceinline__ void mma_drain(SmemCtl &ctl, const GemmArgs &a, bool 
 // =====================================================================================
 // k_gemm_mn: tokens on M, weights on N.
 // =====================================================================================
+template <bool kBS, bool kEpi>
 __global__ void __launch_bounds__(kThreadsScaled, 1)
     k_gemm_mn(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
               const __grid_constant__ CUtensorMap tm_sa, const __grid_constant__ CUtensorMap tm_sb,
@@ -590,7 +613,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
     const uint32_t sf_bytes = 4u * static_cast<uint32_t>(kTileM + a.tile_n);
     // Accumulator spacing in TMEM: 256 columns, or tile_n when the block-scale
     // sets follow the two accumulators.
-    const int acc_stride = a.sf_k ? a.tile_n : kAccStride;
+    const int acc_stride = kBS ? a.tile_n : kAccStride;
     const int set_cols = sf_set_cols(a.tile_n);
 
     if (threadIdx.x == 0)
@@ -634,7 +657,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
         if (lane == 0) {
             tma_prefetch_map(&tm_a);
             tma_prefetch_map(&tm_b);
-            if (a.sf_k) {
+            if constexpr (kBS) {
                 tma_prefetch_map(&tm_sa);
                 tma_prefetch_map(&tm_sb);
             }
@@ -656,7 +679,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
                 if (lane == 0 && !(drop && issued == 0)) {
                     uint8_t *sa = sm.stages + static_cast<size_t>(stage) * a.stage_bytes;
                     const uint32_t fb = smem_addr(&ctl.full[stage]);
-                    const bool sf = a.sf_k && sf_load_at(kb, 0, a.sf_k);
+                    const bool sf = kBS && sf_load_at(kb, 0, a.sf_k);
                     mbar_arrive_expect_tx(fb, tx_bytes + (sf ? sf_bytes : 0u));
                     tma_load_3d(smem_addr(sa), &tm_a, fb, kb * kBlockK, a_row(a, ctl, g, m0), a_grp(a, g));
                     tma_load_3d(smem_addr(sa + a_bytes), &tm_b, fb, kb * kBlockK, n0, g);
@@ -701,7 +724,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
                     break;
                 }
                 tc_fence_after();
-                if (a.sf_k) {
+                if constexpr (kBS) {
                     const uint8_t *sp = sm.stages + static_cast<size_t>(stage) * a.stage_bytes;
                     if (sf_load_at(kb, 0, a.sf_k) &&
                         !sf_take(ctl, a, sfs, stage, sp, a.tile_n, sets_tmem, set_cols, set_tmem)) {
@@ -751,7 +774,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
         mma_drain(ctl, a, issued_any);
     } else if (warp == 6) {
         // ------------------------- block-scale staging -------------------------
-        if (a.sf_k) {
+        if constexpr (kBS) {
             int stage = 0;
             uint32_t phase = 0;
             bool stop = false;
@@ -792,7 +815,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
             __nv_bfloat16 *drow = dout + grow * static_cast<int64_t>(a.n);
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * acc_stride);
-            const float rf = row_ok ? row_factor(a, g, grow) : 1.0f;
+            const float rf = (kEpi && row_ok) ? row_factor(a, g, grow) : 1.0f;
             for (int c = 0; c < a.tile_n; c += 32) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c), r);
@@ -801,7 +824,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
                     for (int j = 0; j < 4; ++j) {
                         const int col = n0 + c + 8 * j;
                         if (col < a.n)
-                            *reinterpret_cast<uint4 *>(drow + col) = out_pack8(a, r + 8 * j, rf, g, grow, col);
+                            *reinterpret_cast<uint4 *>(drow + col) = store_pack8<kEpi>(a, r + 8 * j, rf, g, grow, col);
                     }
                 }
             }
@@ -850,6 +873,7 @@ struct PairSeg {
     int kind;   // 0: first segment of the pair's range, 1: a later one
 };
 
+template <bool kEpi>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     k_gemm_mn2(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                const GemmArgs a)
@@ -1118,10 +1142,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * kAccStride);
             // Eight FP32 values (as bits) -> eight scaled BF16 at column col.
-            const float rf = row_ok ? row_factor(a, 0, grow) : 1.0f;
+            const float rf = (kEpi && row_ok) ? row_factor(a, 0, grow) : 1.0f;
             auto store8 = [&](int col, const uint32_t *v) {
                 if (row_ok && col < a.n)
-                    *reinterpret_cast<uint4 *>(drow + col) = out_pack8(a, v, rf, 0, grow, col);
+                    *reinterpret_cast<uint4 *>(drow + col) = store_pack8<kEpi>(a, v, rf, 0, grow, col);
             };
             if (x.kb0 == 0 && x.kb1 == num_kb) {
                 for (int c = 0; c < a.tile_n; c += 32) {
@@ -1267,6 +1291,7 @@ struct SwapWalker {
     bool first;
 };
 
+template <bool kBS, bool kEpi>
 __global__ void __launch_bounds__(kThreadsScaled, 1)
     k_gemm_swap(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_t,
                 const __grid_constant__ CUtensorMap tm_sw, const __grid_constant__ CUtensorMap tm_st,
@@ -1286,8 +1311,8 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
     // that two CTAs -- this launch's and the next one's -- fit in TMEM.
     // With block scales: two accumulators of `cap` columns, then the
     // per-stage scale sets.
-    const uint32_t tmem_cols = (a.tmem_cols == 256 && !a.sf_k) ? 256u : static_cast<uint32_t>(kTmemCols);
-    const int acc_stride = a.sf_k ? cap : static_cast<int>(tmem_cols / 2);
+    const uint32_t tmem_cols = (a.tmem_cols == 256 && !kBS) ? 256u : static_cast<uint32_t>(kTmemCols);
+    const int acc_stride = kBS ? cap : static_cast<int>(tmem_cols / 2);
     const int set_cols = sf_set_cols(cap);
     constexpr int kTokBox = 16;                  // token rows per TMA box
     constexpr uint32_t kTokBoxBytes = kTokBox * kBlockK;
@@ -1371,7 +1396,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
         if (lane == 0) {
             tma_prefetch_map(&tm_w);
             tma_prefetch_map(&tm_t);
-            if (a.sf_k) {
+            if constexpr (kBS) {
                 tma_prefetch_map(&tm_sw);
                 tma_prefetch_map(&tm_st);
             }
@@ -1395,7 +1420,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
                 if (lane == 0 && !(drop && issued == 0)) {
                     uint8_t *sw = sm.stages + static_cast<size_t>(stage) * a.stage_bytes;
                     const uint32_t fb = smem_addr(&ctl.full[stage]);
-                    const bool sf = a.sf_k && sf_load_at(kb, x.kb0, a.sf_k);
+                    const bool sf = kBS && sf_load_at(kb, x.kb0, a.sf_k);
                     mbar_arrive_expect_tx(fb, tx + (sf ? 4u * static_cast<uint32_t>(kTileM + cap) : 0u));
                     tma_load_3d_hint(smem_addr(sw), &tm_w, fb, kb * kBlockK, x.w0, x.g, w_policy);
                     for (int r = 0; r < x.n_mma; r += kTokBox)
@@ -1446,7 +1471,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
                     break;
                 }
                 tc_fence_after();
-                if (a.sf_k) {
+                if constexpr (kBS) {
                     const uint8_t *sp = sm.stages + static_cast<size_t>(stage) * a.stage_bytes;
                     if (sf_load_at(kb, x.kb0, a.sf_k) &&
                         !sf_take(ctl, a, sfs, stage, sp, cap, sets_tmem, set_cols, set_tmem)) {
@@ -1494,7 +1519,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
         mma_drain(ctl, a, issued_any);
     } else if (warp == 6) {
         // ------------------------- block-scale staging -------------------------
-        if (a.sf_k) {
+        if constexpr (kBS) {
             int stage = 0;
             uint32_t phase = 0;
             bool stop = false;
@@ -1548,7 +1573,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
                 for (int c = 0; c < x.n_mma; c += 16) {
                     uint32_t r[16];
                     tmem_ld_32x32b_x16(t_row + static_cast<uint32_t>(c), r);
-                    swap_store16(a, dout, r, x.g, grow0 + c, x.n_tok - c, col_base);
+                    swap_store16<kEpi>(a, dout, r, x.g, grow0 + c, x.n_tok - c, col_base);
                 }
             } else {
                 // Contributors of this tile: the CTAs whose ranges meet it,
@@ -1624,7 +1649,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
                             bits_v[j] = __float_as_uint(acc_v[j]);
-                        swap_store16(a, dout, bits_v, x.g, grow0 + c, x.n_tok - c, col_base);
+                        swap_store16<kEpi>(a, dout, bits_v, x.g, grow0 + c, x.n_tok - c, col_base);
                     }
                 }
             }
@@ -1671,30 +1696,68 @@ static cudaError_t launch_pdl(Kernel kernel, int threads, int grid, size_t smem,
     return cudaGetLastError();
 }
 
+template <bool kBS, bool kEpi>
+static cudaError_t launch_mn_t(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const CUtensorMap &tm_sa,
+                               const CUtensorMap &tm_sb, const GemmArgs &args, int grid, size_t smem,
+                               cudaStream_t stream)
+{
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_mn<kBS, kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess)
+        return e;
+    return launch_pdl(k_gemm_mn<kBS, kEpi>, kBS ? kThreadsScaled : kThreads, grid, smem, stream, args, tm_a, tm_b,
+                      tm_sa, tm_sb);
+}
+
+// Output scales or a fused epilogue select the kernels' full store path.
+static bool wants_epi(const GemmArgs &args) { return args.epi || args.scale_a || args.scale_b; }
+
 cudaError_t launch_gemm_mn(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const CUtensorMap &tm_sa,
                            const CUtensorMap &tm_sb, const GemmArgs &args, int grid, size_t smem,
                            cudaStream_t stream)
 {
     if (smem < smem_bytes_for(args.stages, args.stage_bytes, args.groups))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_mn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const bool epi = wants_epi(args);
+    if (args.sf_k)
+        return epi ? launch_mn_t<true, true>(tm_a, tm_b, tm_sa, tm_sb, args, grid, smem, stream)
+                   : launch_mn_t<true, false>(tm_a, tm_b, tm_sa, tm_sb, args, grid, smem, stream);
+    return epi ? launch_mn_t<false, true>(tm_a, tm_b, tm_sa, tm_sb, args, grid, smem, stream)
+               : launch_mn_t<false, false>(tm_a, tm_b, tm_sa, tm_sb, args, grid, smem, stream);
+}
+
+template <bool kEpi>
+static cudaError_t launch_mn2_t(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const GemmArgs &args, int grid,
+                                size_t smem, cudaStream_t stream)
+{
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_mn2<kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(k_gemm_mn, kThreadsScaled, grid, smem, stream, args, tm_a, tm_b, tm_sa, tm_sb);
+    return launch_pdl(k_gemm_mn2<kEpi>, kThreads, grid, smem, stream, args, tm_a, tm_b);
 }
 
 cudaError_t launch_gemm_mn2(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const GemmArgs &args,
                             int grid, size_t smem, cudaStream_t stream)
 {
     if (smem < smem_bytes_for(args.stages, args.stage_bytes, args.groups) || (grid & 1) || args.groups != 1 ||
-        args.masked_m != nullptr)
+        args.masked_m != nullptr || args.sf_k)
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_mn2, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return wants_epi(args) ? launch_mn2_t<true>(tm_a, tm_b, args, grid, smem, stream)
+                           : launch_mn2_t<false>(tm_a, tm_b, args, grid, smem, stream);
+}
+
+template <bool kBS, bool kEpi>
+static cudaError_t launch_swap_t(const CUtensorMap &tm_w, const CUtensorMap &tm_t, const CUtensorMap &tm_sw,
+                                 const CUtensorMap &tm_st, const GemmArgs &args, int grid, size_t smem,
+                                 cudaStream_t stream)
+{
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_swap<kBS, kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(k_gemm_mn2, kThreads, grid, smem, stream, args, tm_a, tm_b);
+    return launch_pdl(k_gemm_swap<kBS, kEpi>, kBS ? kThreadsScaled : kThreads, grid, smem, stream, args, tm_w, tm_t,
+                      tm_sw, tm_st);
 }
 
 cudaError_t launch_gemm_swap(const CUtensorMap &tm_w, const CUtensorMap &tm_t, const CUtensorMap &tm_sw,
@@ -1703,11 +1766,12 @@ cudaError_t launch_gemm_swap(const CUtensorMap &tm_w, const CUtensorMap &tm_t, c
 {
     if (smem < smem_bytes_for(args.stages, args.stage_bytes, args.groups))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_swap, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess)
-        return e;
-    return launch_pdl(k_gemm_swap, kThreadsScaled, grid, smem, stream, args, tm_w, tm_t, tm_sw, tm_st);
+    const bool epi = wants_epi(args);
+    if (args.sf_k)
+        return epi ? launch_swap_t<true, true>(tm_w, tm_t, tm_sw, tm_st, args, grid, smem, stream)
+                   : launch_swap_t<true, false>(tm_w, tm_t, tm_sw, tm_st, args, grid, smem, stream);
+    return epi ? launch_swap_t<false, true>(tm_w, tm_t, tm_sw, tm_st, args, grid, smem, stream)
+               : launch_swap_t<false, false>(tm_w, tm_t, tm_sw, tm_st, args, grid, smem, stream);
 }
 
 cudaError_t read_and_clear_status(int32_t info[4])
