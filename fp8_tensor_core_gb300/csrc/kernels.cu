@@ -101,6 +101,21 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, SmemCtl
     }
 }
 
+// Single thread: poll a global counter (acquire) until it reaches `target`;
+// false if that takes longer than timeout_ns.
+__device__ __forceinline__ bool wait_count_at_least(const int32_t *p, int target, uint64_t timeout_ns)
+{
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+        if (v >= target)
+            return true;
+        if (globaltimer_ns() - t0 > timeout_ns)
+            return false;
+    }
+}
+
 // Bounded wait that ignores the abort flag (used while draining).
 __device__ __forceinline__ bool warp_wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns)
 {
@@ -1586,32 +1601,53 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
                 // the first contributor's range may have begun in an earlier
                 // tile.  (No division inside the reduction loop.)
                 const int kind_first = range_begin(first) >= t0 ? 0 : 1;
-                float4 *mine = slots + (static_cast<int64_t>(blockIdx.x) * 2 + x.kind) * part_stride4;
-                for (int c = 0; c < x.n_mma; c += 16) {
-                    uint32_t r[16];
-                    tmem_ld_32x32b_x16(t_row + static_cast<uint32_t>(c), r);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        mine[(c / 4 + v) * kTileM + row] =
-                            make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                        __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-                }
-                __threadfence();
-                __syncwarp();
+                // Per (tile, epilogue warp): {arrived, published}.  Every
+                // contributor arrives first; all but the last then publish
+                // their FP32 partial tile and count it as published.  The
+                // last arriver publishes nothing: it waits (bounded) until
+                // the others' partials are out and sums them with its own,
+                // still in TMEM, in K order.
+                int32_t *cnt = a.counters + (static_cast<int64_t>(x.tile) * 4 + q) * 2;
                 int prev = 0;
                 if (lane == 0)
-                    prev = atomicAdd(a.counters + static_cast<int64_t>(x.tile) * 4 + q, 1);
+                    prev = atomicAdd(cnt, 1);
                 prev = __shfl_sync(0xffffffffu, prev, 0);
-                if (prev == n_contrib - 1) {
-                    // The tile is complete: sum the contributions in K order
-                    // (this segment's own from memory too), 16 tokens of four
-                    // contributors per batch, every load unconditional.
-                    __threadfence();
-                    if (lane == 0)
-                        a.counters[static_cast<int64_t>(x.tile) * 4 + q] = 0;   // ready for the next launch
+                if (prev != n_contrib - 1) {
+                    float4 *mine = slots + (static_cast<int64_t>(blockIdx.x) * 2 + x.kind) * part_stride4;
                     for (int c = 0; c < x.n_mma; c += 16) {
+                        uint32_t r[16];
+                        tmem_ld_32x32b_x16(t_row + static_cast<uint32_t>(c), r);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            mine[(c / 4 + v) * kTileM + row] =
+                                make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                            __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                    }
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0)
+                        atomicAdd(cnt + 1, 1);
+                } else {
+                    int ok = 1;
+                    if (lane == 0) {
+                        ok = wait_count_at_least(cnt + 1, n_contrib - 1, a.timeout_ns) ? 1 : 0;
+                        if (!ok) {
+                            ctl.abort = 1;
+                            record_status(FP8G_ERR_TIMEOUT, kRoleEpilogue, 500 + q);
+                        }
+                        cnt[0] = 0;   // ready for the next launch
+                        cnt[1] = 0;
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    __threadfence();
+                    const int me = static_cast<int>(blockIdx.x) - first;   // this CTA's place in K order
+                    for (int c = 0; c < x.n_mma && ok; c += 16) {
+                        uint32_t own[16];
+                        tmem_ld_32x32b_x16(t_row + static_cast<uint32_t>(c), own);
                         float acc_v[16];
                         for (int p0 = 0; p0 < n_contrib; p0 += 4) {
+                            // four contributors' 16 tokens per batch, every load
+                            // unconditional (this CTA's own slot is read but unused)
                             float4 buf[4][4];
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
@@ -1628,21 +1664,23 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
                             for (int i = 0; i < 4; ++i) {
                                 if (p0 + i >= n_contrib)
                                     break;
+                                float part[16];
+                                if (p0 + i == me) {
 #pragma unroll
-                                for (int w = 0; w < 4; ++w) {
-                                    const float4 f = buf[i][w];
-                                    if (p0 + i == 0) {
-                                        acc_v[4 * w] = f.x;
-                                        acc_v[4 * w + 1] = f.y;
-                                        acc_v[4 * w + 2] = f.z;
-                                        acc_v[4 * w + 3] = f.w;
-                                    } else {
-                                        acc_v[4 * w] += f.x;
-                                        acc_v[4 * w + 1] += f.y;
-                                        acc_v[4 * w + 2] += f.z;
-                                        acc_v[4 * w + 3] += f.w;
+                                    for (int j = 0; j < 16; ++j)
+                                        part[j] = __uint_as_float(own[j]);
+                                } else {
+#pragma unroll
+                                    for (int w = 0; w < 4; ++w) {
+                                        part[4 * w] = buf[i][w].x;
+                                        part[4 * w + 1] = buf[i][w].y;
+                                        part[4 * w + 2] = buf[i][w].z;
+                                        part[4 * w + 3] = buf[i][w].w;
                                     }
                                 }
+#pragma unroll
+                                for (int j = 0; j < 16; ++j)
+                                    acc_v[j] = (p0 + i == 0) ? part[j] : acc_v[j] + part[j];
                             }
                         }
                         uint32_t bits_v[16];

@@ -85,8 +85,8 @@ struct GemmArgs {
     const float *bias;
     float *workspace;          // swap kernel, stream-K: 2 FP32 partial tiles per CTA
                                // (128 x tile_n floats each)
-    int32_t *counters;         // swap kernel, stream-K: arrivals per (tile, epilogue warp),
-                               // zero at rest
+    int32_t *counters;         // stream-K: per (tile, epilogue warp) counters, zero at rest
+                               // (SwapAB: arrived and published; SM pair: arrivals)
 };
 
 // Block-scaled stage layout.  After the two operand tiles (MMA side A: 128
@@ -126,7 +126,8 @@ inline size_t swap_partials_bytes(int grid, int tile_n)
 {
     return static_cast<size_t>(grid) * 2 * kTileM * static_cast<size_t>(tile_n) * sizeof(float);
 }
-inline size_t swap_counter_bytes(long long tiles) { return static_cast<size_t>(tiles) * 4 * sizeof(int32_t); }
+// Two counters (arrived, published) per (tile, epilogue warp).
+inline size_t swap_counter_bytes(long long tiles) { return static_cast<size_t>(tiles) * 8 * sizeof(int32_t); }
 
 // Status word of the current device: read it, then clear it.
 cudaError_t read_and_clear_status(int32_t info[4]);
