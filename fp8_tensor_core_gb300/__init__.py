@@ -26,6 +26,7 @@ WHOLE_TILES = 0x100   # SwapAB kernel: whole tiles per CTA instead of stream-K r
 STREAM_K = 0x800      # SM-pair dense kernel: stream-K split of the last partial wave
 SINGLE_SM_TILES = 0x200   # dense non-swapped: one SM per 128-row tile instead of SM pairs
 NO_PDL = 0x400            # launch without programmatic dependent launch
+PAIR_TILES = 0x4000       # dense: always SM-pair tiles when M > 128
 SHARE_SM = 0x1000         # SwapAB kernel: half an SM per CTA (next launch overlaps the drain)
 
 

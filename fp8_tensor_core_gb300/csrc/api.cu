@@ -242,16 +242,18 @@ struct PairPlan {
     bool stream_k;
 };
 
-PairPlan plan_pair(int64_t m_tiles2, int64_t N, int num_kb, int pairs, uint32_t flags)
+PairPlan plan_pair(int64_t m_tiles2, int64_t N, int num_kb, int pairs, uint32_t flags, int max_tn = 256)
 {
     static const int cands[] = {256, 224, 192, 160, 128};
     static const double cost_per_kb[] = {1.0, 1.07, 1.18, 1.30, 1.45};
-    PairPlan best{256, false};
+    PairPlan best{max_tn, false};
     double best_cost = 1e300;
     const int tn_override = static_cast<int>((flags >> 16) & 15u);
     for (int i = 0; i < 5; ++i) {
         const int tn = cands[i];
-        if (tn_override >= 1 && tn_override <= 8 && tn != 32 * tn_override)
+        if (tn > max_tn)
+            continue;
+        if (tn_override >= 1 && tn_override <= 8 && tn != std::min(32 * tn_override, max_tn))
             continue;
         const int64_t units = m_tiles2 * cdiv(N, tn);
         const double width = static_cast<double>(tn) / 256.0;
@@ -271,8 +273,8 @@ PairPlan plan_pair(int64_t m_tiles2, int64_t N, int num_kb, int pairs, uint32_t 
             }
         }
     }
-    if (tn_override >= 1 && tn_override <= 8 && best.tile_n != 32 * tn_override)
-        best = {32 * tn_override, false};
+    if (tn_override >= 1 && tn_override <= 8 && best.tile_n != std::min(32 * tn_override, max_tn))
+        best = {std::min(32 * tn_override, max_tn), false};
     return best;
 }
 
@@ -518,24 +520,47 @@ int launch(const Problem &p, cudaStream_t stream)
 
     // Dense problems with more than one 128-row token tile: two SMs per
     // 256-row tile (cta_group::2), unless single-SM tiles are asked for.
+    // Block scales: the pair kernel only pays for 128-element groups and long K
+    // (measured on GB300: 2-6 % faster at K >= 7168, even at K = 4096, 7-13 %
+    // slower at K = 2048 or with 32-element groups, whose per-K-block scale
+    // copies weigh more in the pair's longer K block).
+    const bool pair_ok = !p.sf_k || (p.sf_k == 1 && p.K > 4096) || (p.flags & FP8G_PAIR_TILES);
     if (!p.masked_m && !p.group_offsets && p.G == 1 && p.rows_a > kTileM && !(p.flags & FP8G_SINGLE_SM_TILES) &&
-        !p.sf_k) {
+        pair_ok) {
         const int64_t m_tiles2 = cdiv(p.rows_a, 2 * kTileM);
         const int pairs = info.sms / 2;
-        const PairPlan plan = plan_pair(m_tiles2, p.N, num_kb, pairs, p.flags);
+        const PairPlan plan =
+            plan_pair(m_tiles2, p.N, num_kb, pairs, p.flags, p.sf_k ? kMaxBlockScaledTile : 256);
         const int tile_n = plan.tile_n;
         const int64_t units = m_tiles2 * cdiv(p.N, tile_n);
         if (units > kMaxDim || units * num_kb > (int64_t(1) << 53))
             return FP8G_ERR_UNSUPPORTED;
         args.tile_n = tile_n;
         args.k_splits = plan.stream_k ? 0 : 1;
-        args.stage_bytes = kTileM * kBlockK + (tile_n / 2) * kBlockK;
+        if (p.sf_k) {
+            // Operand tiles (own 128 A rows, half of the B rows), then the scale
+            // area for 128 A rows and the whole tile's tile_n B rows.
+            args.sf_off = kTileM * kBlockK + (tile_n / 2) * kBlockK;
+            args.stage_bytes = (args.sf_off + sf_stage_bytes(tile_n) + 1023) & ~1023;
+            args.sf_col0 = 2 * tile_n;
+            args.sf_sets = std::min(kMaxSfSets, (kTmemCols - 2 * tile_n) / sf_set_cols(tile_n));
+        } else {
+            args.stage_bytes = kTileM * kBlockK + (tile_n / 2) * kBlockK;
+        }
         args.stages = pick_stages(info, args.stage_bytes, static_cast<int>(p.G), p.flags);
         const int64_t band = (48ll << 20) / (2 * kTileM * p.K);
         args.raster_band = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(band, m_tiles2)));
         if (!make_map(&tm0, p.A, p.K, p.rows_a, 1, kTileM) ||
             !make_map(&tm1, p.B, p.K, p.N, 1, static_cast<uint32_t>(tile_n / 2)))
             return FP8G_ERR_CUDA;
+        if (p.sf_k) {
+            if (!make_sf_map(&tm2, p.sf_a, p.rows_a, ks, 1, p.sf_a_ld, kTileM, 4) ||
+                !make_sf_map(&tm3, p.sf_b, p.N, ks, 1, p.sf_b_ld, static_cast<uint32_t>(tile_n), 4))
+                return FP8G_ERR_CUDA;
+        } else {
+            tm2 = tm0;
+            tm3 = tm1;
+        }
         const int grid = 2 * static_cast<int>(std::min<int64_t>(plan.stream_k ? units * num_kb : units, pairs));
         // (stream-K implies units is not a multiple of the pairs, so every
         // pair of the grid exists for the remainder's partition)
@@ -546,7 +571,7 @@ int launch(const Problem &p, cudaStream_t stream)
             if (st != FP8G_OK)
                 return st;
         }
-        return launch_gemm_mn2(tm0, tm1, args, grid, static_cast<size_t>(info.smem_optin), stream) ==
+        return launch_gemm_mn2(tm0, tm1, tm2, tm3, args, grid, static_cast<size_t>(info.smem_optin), stream) ==
                        cudaSuccess
                    ? FP8G_OK
                    : FP8G_ERR_CUDA;

@@ -62,6 +62,7 @@ struct alignas(16) SmemCtl {
     uint64_t drain;
     uint64_t pair_exit;   // CTA-pair kernel: the peer's "done" arrival
     uint64_t sfready[kMaxStages];   // block scales of stage s staged for tcgen05.cp
+    uint64_t sffull[kMaxStages];    // SM-pair kernel: this CTA's scale bytes of stage s landed
     uint64_t sffree[kMaxSfSets];    // TMEM scale set no longer read by any MMA
     uint32_t tmem_base;
     volatile int32_t abort;
@@ -407,6 +408,9 @@ struct SfState {
     uint32_t ready_par; // parity bit per stage of sfready
 };
 
+// kPair: the SM-pair kernel's even CTA, whose commits and copies act on
+// both CTAs (each CTA's own copy sources, at the same offsets).
+template <bool kPair = false>
 __device__ __forceinline__ bool sf_take(SmemCtl &ctl, const GemmArgs &a, SfState &st, int stage,
                                         const uint8_t *stage_ptr, int box_b, uint32_t sets_tmem, int set_cols,
                                         uint32_t &set_tmem)
@@ -417,8 +421,12 @@ __device__ __forceinline__ bool sf_take(SmemCtl &ctl, const GemmArgs &a, SfState
         return false;
     st.ready_par ^= 1u << stage;
     const int R = a.sf_sets;
-    if (st.j >= 0 && lane == 0)
-        mma_commit(smem_addr(&ctl.sffree[st.j % R]));
+    if (st.j >= 0 && lane == 0) {
+        if constexpr (kPair)
+            mma_commit_pair(smem_addr(&ctl.sffree[st.j % R]));
+        else
+            mma_commit(smem_addr(&ctl.sffree[st.j % R]));
+    }
     __syncwarp();
     ++st.j;
     const int set = st.j % R;
@@ -430,10 +438,17 @@ __device__ __forceinline__ bool sf_take(SmemCtl &ctl, const GemmArgs &a, SfState
     set_tmem = sets_tmem + static_cast<uint32_t>(set * set_cols);
     if (lane == 0) {
         const uint8_t *src = stage_ptr + a.sf_off + 4 * (kTileM + box_b);
-        tmem_cp_32x128b_warpx4(set_tmem, smem_desc_rows16(smem_addr(src)));
         const int nch = (box_b + 127) >> 7;
-        for (int h = 0; h < nch; ++h)
-            tmem_cp_32x128b_warpx4(set_tmem + 4u + 4u * h, smem_desc_rows16(smem_addr(src + 512 * (1 + h))));
+        if constexpr (kPair) {
+            tmem_cp_32x128b_warpx4_pair(set_tmem, smem_desc_rows16(smem_addr(src)));
+            for (int h = 0; h < nch; ++h)
+                tmem_cp_32x128b_warpx4_pair(set_tmem + 4u + 4u * h,
+                                            smem_desc_rows16(smem_addr(src + 512 * (1 + h))));
+        } else {
+            tmem_cp_32x128b_warpx4(set_tmem, smem_desc_rows16(smem_addr(src)));
+            for (int h = 0; h < nch; ++h)
+                tmem_cp_32x128b_warpx4(set_tmem + 4u + 4u * h, smem_desc_rows16(smem_addr(src + 512 * (1 + h))));
+        }
     }
     return true;
 }
@@ -888,9 +903,10 @@ struct PairSeg {
     int kind;   // 0: first segment of the pair's range, 1: a later one
 };
 
-template <bool kEpi>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+template <bool kBS, bool kEpi>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsScaled, 1)
     k_gemm_mn2(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+               const __grid_constant__ CUtensorMap tm_sa, const __grid_constant__ CUtensorMap tm_sb,
                const GemmArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -908,6 +924,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const bool stream_k = a.k_splits != 1;
     const uint32_t a_bytes = kTileM * kBlockK;                          // own 128 token rows
     const uint32_t tx_pair = 2u * (a_bytes + static_cast<uint32_t>(half_n) * kBlockK);
+    // Block scales: each CTA loads its own 128 rows' A-side scales and the
+    // whole tile's B-side scales (each CTA's tensor core scales all N
+    // columns), completing on its own sffull barrier.  Accumulators are then
+    // tile_n columns apart, followed by the scale sets.
+    const uint32_t sf_bytes = 4u * static_cast<uint32_t>(kTileM + a.tile_n);
+    const int acc_stride = kBS ? a.tile_n : kAccStride;
+    const int set_cols = sf_set_cols(a.tile_n);
     const int cid = blockIdx.x >> 1;
     const int ncl = gridDim.x >> 1;
     // Whole-tile waves, then the stream-K remainder [sk0, sk0 + T).
@@ -927,6 +950,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         mbar_init(smem_addr(&ctl.drain), 1);
         mbar_init(smem_addr(&ctl.pair_exit), 1);
+        if constexpr (kBS) {
+            for (int s = 0; s < a.stages; ++s) {
+                mbar_init(smem_addr(&ctl.sffull[s]), 1);
+                mbar_init(smem_addr(&ctl.sfready[s]), 2);   // both CTAs' staging warps
+            }
+            for (int i = 0; i < kMaxSfSets; ++i)
+                mbar_init(smem_addr(&ctl.sffree[i]), 1);
+        }
         ctl.abort = 0;
         fence_mbar_init();
     }
@@ -1003,6 +1034,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             tma_prefetch_map(&tm_a);
             tma_prefetch_map(&tm_b);
+            if constexpr (kBS) {
+                tma_prefetch_map(&tm_sa);
+                tma_prefetch_map(&tm_sb);
+            }
         }
         int stage = 0;
         uint32_t phase = 0;
@@ -1025,6 +1060,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tma_load_3d_pair(smem_addr(sa), &tm_a, fb, kb * kBlockK, x.m0, 0);
                     tma_load_3d_pair(smem_addr(sa + a_bytes), &tm_b, fb, kb * kBlockK,
                                      x.n0 + static_cast<int>(rank) * half_n, 0);
+                    if constexpr (kBS) {
+                        if (sf_load_at(kb, x.kb0, a.sf_k)) {
+                            const uint32_t sb = smem_addr(&ctl.sffull[stage]);
+                            const int y = sf_first_group(kb, a.sf_k);
+                            mbar_arrive_expect_tx(sb, sf_bytes);
+                            tma_load_3d(smem_addr(sa + a.sf_off), &tm_sa, sb, x.m0, y, 0);
+                            tma_load_3d(smem_addr(sa + a.sf_off + 4 * kTileM), &tm_sb, sb, x.n0, y, 0);
+                        }
+                    }
                 }
                 __syncwarp();
                 ++issued;
@@ -1064,6 +1108,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ----------------------------- MMA issuer -----------------------------
         if (leader) {
             const uint32_t idesc = make_idesc(a.a_fmt, a.b_fmt, 2 * kTileM, a.tile_n);
+            const uint32_t idesc_bs = make_idesc_bs(a.a_fmt, a.b_fmt, 2 * kTileM, a.tile_n, 0);
+            const uint32_t sets_tmem = tmem_base + static_cast<uint32_t>(a.sf_col0);
+            SfState sfs{-1, 0u};
+            uint32_t set_tmem = sets_tmem;
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -1078,7 +1126,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccStride);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * acc_stride);
                 for (int kb = x.kb0; kb < x.kb1; ++kb) {
                     if (!warp_wait(smem_addr(&ctl.full[stage]), phase, ctl, a.timeout_ns, kRoleMma,
                                    stage)) {
@@ -1086,7 +1134,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    if (lane == 0) {
+                    if constexpr (kBS) {
+                        const uint8_t *sp = sm.stages + static_cast<size_t>(stage) * a.stage_bytes;
+                        if (sf_load_at(kb, x.kb0, a.sf_k) &&
+                            !sf_take<true>(ctl, a, sfs, stage, sp, a.tile_n, sets_tmem, set_cols, set_tmem)) {
+                            aborted = true;
+                            break;
+                        }
+                        if (lane == 0) {
+                            const uint64_t adesc = smem_desc_k_sw128(smem_addr(sp));
+                            const uint64_t bdesc = smem_desc_k_sw128(smem_addr(sp) + a_bytes);
+#pragma unroll
+                            for (int k = 0; k < kBlockK / 32; ++k) {
+                                const uint32_t id =
+                                    a.sf_k == 1 ? static_cast<uint32_t>(kb & 3) : static_cast<uint32_t>(k);
+                                mma_f8f6f4_bs_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k,
+                                                   idesc_bs | (id << 4) | (id << 29), set_tmem, set_tmem + 4u,
+                                                   (kb != x.kb0 || k != 0) ? 1u : 0u);
+                            }
+                            mma_commit_pair_mc(smem_addr(&ctl.empty[stage]), 0x3);
+                        }
+                    } else if (lane == 0) {
                         const uint32_t sa = smem_addr(sm.stages + static_cast<size_t>(stage) * a.stage_bytes);
                         const uint64_t adesc = smem_desc_k_sw128(sa);
                         const uint64_t bdesc = smem_desc_k_sw128(sa + a_bytes);
@@ -1131,6 +1199,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 warp_wait_drain(smem_addr(&ctl.drain), 0, a.timeout_ns);
             }
         }
+    } else if (warp == 6) {
+        // ------------------------- block-scale staging -------------------------
+        // Each CTA waits for its own scale bytes of a stage (sffull, one
+        // completion per scale load of that stage), builds the copy sources
+        // and tells the even CTA (sfready counts both CTAs).
+        if constexpr (kBS) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t sf_par = 0;   // parity bit per stage of sffull
+            const uint32_t ready_leader0 = mapa_shared(smem_addr(&ctl.sfready[0]), 0);
+            Walker wk = make_walker();
+            PairSeg x;
+            while (!aborted && next_seg(wk, x)) {
+                for (int kb = x.kb0; kb < x.kb1; ++kb) {
+                    if (sf_load_at(kb, x.kb0, a.sf_k)) {
+                        if (!warp_wait(smem_addr(&ctl.sffull[stage]), (sf_par >> stage) & 1u, ctl, a.timeout_ns,
+                                       kRoleScales, stage)) {
+                            aborted = true;
+                            break;
+                        }
+                        sf_par ^= 1u << stage;
+                        sf_transpose(sm.stages + static_cast<size_t>(stage) * a.stage_bytes, a, a.tile_n);
+                        if (lane == 0)
+                            mbar_arrive_cluster(ready_leader0 + static_cast<uint32_t>(stage) * 8u);
+                    }
+                    if (++stage == a.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            (void)phase;
+        }
     } else {
         // ------------------------------ epilogue ------------------------------
         const int q = warp & 3;
@@ -1155,7 +1256,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const bool row_ok = grow < a.rows_a;
             __nv_bfloat16 *drow = dout + static_cast<int64_t>(grow) * static_cast<int64_t>(a.n);
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                   static_cast<uint32_t>(acc * kAccStride);
+                                   static_cast<uint32_t>(acc * acc_stride);
             // Eight FP32 values (as bits) -> eight scaled BF16 at column col.
             const float rf = (kEpi && row_ok) ? row_factor(a, 0, grow) : 1.0f;
             auto store8 = [&](int col, const uint32_t *v) {
@@ -1764,25 +1865,32 @@ cudaError_t launch_gemm_mn(const CUtensorMap &tm_a, const CUtensorMap &tm_b, con
                : launch_mn_t<false, false>(tm_a, tm_b, tm_sa, tm_sb, args, grid, smem, stream);
 }
 
-template <bool kEpi>
-static cudaError_t launch_mn2_t(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const GemmArgs &args, int grid,
-                                size_t smem, cudaStream_t stream)
+template <bool kBS, bool kEpi>
+static cudaError_t launch_mn2_t(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const CUtensorMap &tm_sa,
+                                const CUtensorMap &tm_sb, const GemmArgs &args, int grid, size_t smem,
+                                cudaStream_t stream)
 {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_mn2<kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_mn2<kBS, kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(k_gemm_mn2<kEpi>, kThreads, grid, smem, stream, args, tm_a, tm_b);
+    return launch_pdl(k_gemm_mn2<kBS, kEpi>, kBS ? kThreadsScaled : kThreads, grid, smem, stream, args, tm_a, tm_b,
+                      tm_sa, tm_sb);
 }
 
-cudaError_t launch_gemm_mn2(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const GemmArgs &args,
-                            int grid, size_t smem, cudaStream_t stream)
+cudaError_t launch_gemm_mn2(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const CUtensorMap &tm_sa,
+                            const CUtensorMap &tm_sb, const GemmArgs &args, int grid, size_t smem,
+                            cudaStream_t stream)
 {
     if (smem < smem_bytes_for(args.stages, args.stage_bytes, args.groups) || (grid & 1) || args.groups != 1 ||
-        args.masked_m != nullptr || args.sf_k)
+        args.masked_m != nullptr || args.group_offsets != nullptr)
         return cudaErrorInvalidValue;
-    return wants_epi(args) ? launch_mn2_t<true>(tm_a, tm_b, args, grid, smem, stream)
-                           : launch_mn2_t<false>(tm_a, tm_b, args, grid, smem, stream);
+    const bool epi = wants_epi(args);
+    if (args.sf_k)
+        return epi ? launch_mn2_t<true, true>(tm_a, tm_b, tm_sa, tm_sb, args, grid, smem, stream)
+                   : launch_mn2_t<true, false>(tm_a, tm_b, tm_sa, tm_sb, args, grid, smem, stream);
+    return epi ? launch_mn2_t<false, true>(tm_a, tm_b, tm_sa, tm_sb, args, grid, smem, stream)
+               : launch_mn2_t<false, false>(tm_a, tm_b, tm_sa, tm_sb, args, grid, smem, stream);
 }
 
 template <bool kBS, bool kEpi>

@@ -115,8 +115,11 @@ cudaError_t launch_gemm_mn(const CUtensorMap &tm_a, const CUtensorMap &tm_b, con
                            const CUtensorMap &tm_sb, const GemmArgs &args, int grid, size_t smem,
                            cudaStream_t stream);
 // Dense only: clusters of two CTAs, 256 x tile_n tiles, B box of tile_n/2 rows.
-cudaError_t launch_gemm_mn2(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const GemmArgs &args,
-                            int grid, size_t smem, cudaStream_t stream);
+// With block scales tm_sa covers A's scales (box 128 rows) and tm_sb B's
+// (box tile_n rows: each CTA loads the whole tile's).
+cudaError_t launch_gemm_mn2(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const CUtensorMap &tm_sa,
+                            const CUtensorMap &tm_sb, const GemmArgs &args, int grid, size_t smem,
+                            cudaStream_t stream);
 cudaError_t launch_gemm_swap(const CUtensorMap &tm_w, const CUtensorMap &tm_t, const CUtensorMap &tm_sw,
                              const CUtensorMap &tm_st, const GemmArgs &args, int grid, size_t smem,
                              cudaStream_t stream);

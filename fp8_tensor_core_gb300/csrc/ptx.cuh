@@ -314,6 +314,28 @@ __device__ __forceinline__ void mma_f8f6f4_pair(uint32_t d_tmem, uint64_t a_desc
                  : "memory");
 }
 
+// Pair form of the block-scaled MMA: each CTA's TMEM holds the A-side scale
+// factors of its own 128 rows and the B-side ones of all N columns (same
+// layout as the single-CTA form, same TMEM addresses in both CTAs).
+__device__ __forceinline__ void mma_f8f6f4_bs_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                   uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                   uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %6, 0;\n\t"
+                 "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X "
+                 "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+                 : "memory");
+}
+
+// Pair form of the scale-factor copy (issued by the even CTA): each CTA's
+// shared memory at this offset goes to its own TMEM at taddr.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4_pair(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Arrive once, on the mbarrier at this shared-memory offset in every CTA of
 // `cta_mask`, when the pair MMAs issued so far have completed.
 __device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t cta_mask)

@@ -96,6 +96,11 @@ typedef enum {
  *                     previous launch in the stream finishes; it waits for
  *                     that launch before touching global memory)           */
 #define FP8G_NO_PDL 0x400u
+/*   FP8G_PAIR_TILES   dense problems with more than 128 token rows: always use
+ *                     SM-pair tiles (the automatic choice skips them for
+ *                     block-scaled problems with short K or 32-element
+ *                     groups, where single-SM tiles measured faster). */
+#define FP8G_PAIR_TILES 0x4000u
 /*   FP8G_STAGES(n)    at most n shared-memory pipeline stages (1..15)       */
 #define FP8G_STAGES(n) ((((uint32_t)(n)) & 15u) << 20)
 /*   FP8G_SHARE_SM     SwapAB kernel with <= 128 tokens per chunk: half the
@@ -198,9 +203,9 @@ int fp8_gemm_grouped_masked_scaled(const void *A, const void *B, void *D,
  *          sf_b_ld >= N, a multiple of 16.  128x128 weight blocks are
  *          expressed by repeating a block's scale over its 128 rows.
  *   Both 16-byte aligned; padding bytes past M / N are never read.
- * The SM-pair dense kernel has no block-scaled form: dense problems run on
- * single-SM tiles (N tile <= 224) or SwapAB (token chunks <= 224).  Other
- * arguments, layouts and errors as the unscaled calls.
+ * Dense problems run on SM-pair tiles (128-element groups, K > 4096, or with
+ * FP8G_PAIR_TILES) or single-SM tiles, N tile <= 224, or SwapAB with token
+ * chunks <= 224.  Other arguments, layouts and errors as the unscaled calls.
  */
 int fp8_gemm_nt_blockscaled(const void *A, const void *B, void *D, int64_t M, int64_t N,
                             int64_t K, int a_dtype, int b_dtype, const uint8_t *sf_a,

@@ -1,7 +1,7 @@
 """GPU parity of the block-scaled entry points (UE8M0 scale per row per 32- or
 128-element K group, applied by tcgen05.mma kind::mxf8f6f4.block_scale)
-against the oracle's block-scaled definition: the single-SM tile kernel at
-every tile width, SwapAB (stream-K and whole tiles), the masked grouped form
+against the oracle's block-scaled definition: the SM-pair and single-SM tile
+kernels at every tile width, SwapAB (stream-K and whole tiles), the masked grouped form
 with poisoned padding, ragged tails, both FP8 formats, and the host-side
 argument checks.  Sources: "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法
 内核优化实践" §5.2 (per-128-element groups) and "一次“转置”，半张算力：DeepSeek
@@ -72,18 +72,31 @@ def check_dense_bs(M, N, K, gran, flags, seed, fa=E4, fb=E4, pad=16):
     return rep
 
 
-# ---- single-SM tiles (tokens on M) ---------------------------------------------------
+# ---- token tiles: SM pairs and single SMs (tokens on M) -------------------------------
 
+DENSE_KERNELS = {"pair": OFF | fp8g.PAIR_TILES, "single_sm": OFF | fp8g.SINGLE_SM_TILES,
+                 "pair_stream_k": OFF | fp8g.PAIR_TILES | fp8g.STREAM_K, "auto": OFF}
+
+
+@pytest.mark.parametrize("kernel", sorted(DENSE_KERNELS))
 @pytest.mark.parametrize("gran", [128, 32])
 @pytest.mark.parametrize("M,N,K", [(128, 128, 128), (300, 520, 1040), (129, 232, 2064), (640, 896, 512)])
-def test_dense_tiles(M, N, K, gran):
-    check_dense_bs(M, N, K, gran, OFF, seed=500 + M + N + K + gran)
+def test_dense_tiles(M, N, K, gran, kernel):
+    check_dense_bs(M, N, K, gran, DENSE_KERNELS[kernel], seed=500 + M + N + K + gran)
 
 
+@pytest.mark.parametrize("kernel", ["pair", "single_sm"])
 @pytest.mark.parametrize("tn", [4, 5, 6, 7, 8])
-def test_dense_every_tile_width(tn):
+def test_dense_every_tile_width(tn, kernel):
     """FP8G_TILE_N(8) (256 columns) is clamped to the widest block-scaled tile."""
-    check_dense_bs(256, 480, 768, 128, OFF | fp8g.TILE_N(tn), seed=520 + tn)
+    check_dense_bs(256, 480, 768, 128, DENSE_KERNELS[kernel] | fp8g.TILE_N(tn), seed=520 + tn)
+
+
+@pytest.mark.parametrize("gran", [128, 32])
+def test_dense_pair_many_tiles_and_k_blocks(gran):
+    """Several whole waves of SM-pair tiles and a K of 33 blocks (the scale
+    ring wraps many times, 128-element groups span K-block quadruples)."""
+    check_dense_bs(1024, 1792, 4224, gran, OFF | fp8g.PAIR_TILES, seed=530 + gran)
 
 
 @pytest.mark.parametrize("fa,fb", [(E5, E4), (E4, E5), (E5, E5)])
@@ -91,8 +104,9 @@ def test_dense_mixed_formats(fa, fb):
     check_dense_bs(200, 272, 640, 32, OFF, seed=530 + 2 * fa + fb, fa=fa, fb=fb)
 
 
-def test_dense_one_stage_pipeline():
-    check_dense_bs(256, 384, 1024, 128, OFF | fp8g.DEBUG_ONE_STAGE, seed=535)
+@pytest.mark.parametrize("kernel", ["pair", "single_sm"])
+def test_dense_one_stage_pipeline(kernel):
+    check_dense_bs(256, 384, 1024, 128, DENSE_KERNELS[kernel] | fp8g.DEBUG_ONE_STAGE, seed=535)
 
 
 def test_exact_data_is_bit_exact():
@@ -107,7 +121,7 @@ def test_exact_data_is_bit_exact():
         ks = K // gran
         sfa = ue8m0((ks, M), 541 + gran, 124, 130)
         sfb = ue8m0((ks, N), 542 + gran, 124, 130)
-        for flags in (OFF, ON):
+        for flags in (OFF | fp8g.PAIR_TILES, OFF | fp8g.SINGLE_SM_TILES, ON):
             D = fp8g.fp8_gemm_nt_blockscaled(dev(A), dev(B), dev(sfa), dev(sfb), sf_group_k=gran,
                                              a_dtype=E4, b_dtype=E4, flags=flags)
             torch.cuda.synchronize()
@@ -128,7 +142,7 @@ def test_scales_reach_the_right_k_group():
             sfa = np.full((ks, M), 107, np.uint8)
             sfa[j] = 127
             sfb = np.full((ks, N), 127, np.uint8)
-            for flags in (OFF, ON):
+            for flags in (OFF | fp8g.PAIR_TILES, OFF | fp8g.SINGLE_SM_TILES, ON):
                 D = fp8g.fp8_gemm_nt_blockscaled(dev(A), dev(B), dev(sfa), dev(sfb), sf_group_k=gran,
                                                  a_dtype=E4, b_dtype=E4, flags=flags)
                 torch.cuda.synchronize()
