@@ -153,3 +153,39 @@ def test_reference_arm_line(tmp_path):
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0
     assert line["unit"] == "TFLOP/s" and line["higher_is_better"] is True
+
+
+def test_workload_variants_parse():
+    """masked:mode, grouped:G:m:N:K[:mode] and the :bs / :bs32 block-scale
+    suffix give the documented shapes, flags, scale granularity and bytes."""
+    m = bench.make_workload("masked:noswap")
+    assert m.flags == 2 and m.G == 32 and m.hint == 32 and m.gran == 0
+    assert bench.make_workload("masked").flags == 1 and bench.make_workload("masked:auto").flags == 0
+    g = bench.make_workload("grouped:16:96:4096:7168:swap")
+    assert (g.G, g.M_max, g.N, g.K, g.flags, g.hint) == (16, 96, 4096, 7168, 1, 96)
+    inp = bench.host_inputs(g)
+    assert inp["masked_m"].tolist() == [96] * 16
+    b = bench.make_workload("dense4096:bs")
+    assert b.gran == 128 and b.kernel == "k_gemm_mn" and b.name == "dense4096:bs"
+    ks = 4096 // 128
+    assert b.bytes() == 4096 * (4096 + ks) * 2 + 2 * 4096 * 4096
+    b32 = bench.make_workload("smallm:16:7168:16384:swap:bs32")
+    assert b32.gran == 32 and b32.M == 16 and b32.flags == 1
+
+
+def test_block_scale_recipe():
+    """Per-token scales vary per row; weight scales are constant over each
+    128x128 block (gran 128); all codes in [120, 134]; ld is padded to 16."""
+    import numpy as np
+    w = bench.make_workload("masked:bs")
+    w.G = 3                                  # a small instance of the same recipe
+    sc = bench.block_scales(w)
+    sfa, sfb = sc["sf_a"], sc["sf_b"]
+    assert sfa.shape == (3, 7168 // 128, 128) and sfb.shape == (3, 7168 // 128, 4096)
+    assert sfa.min() >= 120 and sfa.max() <= 134 and sfb.min() >= 120 and sfb.max() <= 134
+    blocks = sfb.reshape(3, 56, 32, 128)
+    assert np.all(blocks == blocks[..., :1])          # one code per 128 rows
+    assert len(np.unique(sfa[0, 0])) > 1
+    w32 = bench.make_workload("smallm:1:7168:16384:bs32")
+    sc32 = bench.block_scales(w32)
+    assert sc32["sf_a"].shape == (1, 16384 // 32, 16) and sc32["sf_b"].shape == (1, 512, 7168)
