@@ -490,6 +490,15 @@ int launch(const Problem &p, cudaStream_t stream)
         } else if (p.sf_k) {
             plan_blockscaled(args, info, static_cast<int>(cap), static_cast<int>(p.G), p.flags);
             args.tmem_cols = 512;
+            // Two MMA issuers when four accumulators of the chunk and at
+            // least two scale sets fit in TMEM.
+            const int set_cols = sf_set_cols(static_cast<int>(cap));
+            const int sets_dual = std::min<int>(kMaxSfSets, (kTmemCols - 4 * static_cast<int>(cap)) / set_cols);
+            if (sets_dual >= 2 && !(p.flags & FP8G_ONE_MMA_ISSUER)) {
+                args.dual_mma = 1;
+                args.sf_col0 = static_cast<int32_t>(4 * cap);
+                args.sf_sets = sets_dual;
+            }
         } else {
             args.stages = pick_stages(info, args.stage_bytes, static_cast<int>(p.G), p.flags);
             args.tmem_cols = 512;

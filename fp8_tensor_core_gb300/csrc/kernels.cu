@@ -64,6 +64,8 @@ struct alignas(16) SmemCtl {
     uint64_t sfready[kMaxStages];   // block scales of stage s staged for tcgen05.cp
     uint64_t sffull[kMaxStages];    // SM-pair kernel: this CTA's scale bytes of stage s landed
     uint64_t sffree[kMaxSfSets];    // TMEM scale set no longer read by any MMA
+    uint64_t sfset_ready[kMaxSfSets];   // SwapAB: scale set written into TMEM by the staging warps
+    uint64_t drain2;                // SwapAB: completion of the second issuer's tensor-core work
     uint32_t tmem_base;
     volatile int32_t abort;
     int32_t units_total;
@@ -553,21 +555,25 @@ __device__ __forceinline__ Smem carve(uint8_t *raw, const GemmArgs &a)
     return s;
 }
 
-__device__ __forceinline__ void init_barriers(SmemCtl &ctl, int stages)
+// `issuers`: MMA-issuing threads that each commit to tfull and sffree (1 or 2).
+__device__ __forceinline__ void init_barriers(SmemCtl &ctl, int stages, uint32_t issuers = 1)
 {
     for (int s = 0; s < stages; ++s) {
         mbar_init(smem_addr(&ctl.full[s]), 1);
         mbar_init(smem_addr(&ctl.empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
-        mbar_init(smem_addr(&ctl.tfull[b]), 1);
+        mbar_init(smem_addr(&ctl.tfull[b]), issuers);
         mbar_init(smem_addr(&ctl.tempty[b]), 4 * 32);
     }
     mbar_init(smem_addr(&ctl.drain), 1);
+    mbar_init(smem_addr(&ctl.drain2), 1);
     for (int s = 0; s < stages; ++s)
         mbar_init(smem_addr(&ctl.sfready[s]), 1);
-    for (int i = 0; i < kMaxSfSets; ++i)
-        mbar_init(smem_addr(&ctl.sffree[i]), 1);
+    for (int i = 0; i < kMaxSfSets; ++i) {
+        mbar_init(smem_addr(&ctl.sffree[i]), issuers);
+        mbar_init(smem_addr(&ctl.sfset_ready[i]), 4);   // one arrival per staging warp
+    }
     ctl.abort = 0;
     fence_mbar_init();
 }
@@ -613,14 +619,16 @@ __device__ __forceinline__ void loader_tail(SmemCtl &ctl, const GemmArgs &a, int
 
 // MMA issuer tail: wait until every tensor-core operation it issued has
 // completed, so TMEM can be freed.
-__device__ __forceinline__ void mma_drain(SmemCtl &ctl, const GemmArgs &a, bool issued_any)
+__device__ __forceinline__ void mma_drain(SmemCtl &ctl, const GemmArgs &a, bool issued_any,
+                                          uint64_t *bar = nullptr)
 {
     if (!issued_any)
         return;
+    const uint32_t b = smem_addr(bar ? bar : &ctl.drain);
     if ((threadIdx.x & 31) == 0)
-        mma_commit(smem_addr(&ctl.drain));
+        mma_commit(b);
     __syncwarp();
-    warp_wait_drain(smem_addr(&ctl.drain), 0, a.timeout_ns);
+    warp_wait_drain(b, 0, a.timeout_ns);
 }
 
 // =====================================================================================
@@ -1408,7 +1416,7 @@ struct SwapWalker {
 };
 
 template <bool kBS, bool kEpi>
-__global__ void __launch_bounds__(kThreadsScaled, 1)
+__global__ void __launch_bounds__(kBS ? kThreadsSwapScaled : kThreads, 1)
     k_gemm_swap(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_t,
                 const __grid_constant__ CUtensorMap tm_sw, const __grid_constant__ CUtensorMap tm_st,
                 const GemmArgs a)
@@ -1425,16 +1433,18 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
     const uint32_t w_bytes = kTileM * kBlockK;   // 16 KB weight box
     // Accumulators: two of 256 columns, or two of 128 (tile_n <= 128) so
     // that two CTAs -- this launch's and the next one's -- fit in TMEM.
-    // With block scales: two accumulators of `cap` columns, then the
-    // per-stage scale sets.
+    // With block scales: two accumulators of `cap` columns per MMA issuer
+    // (issuer i's accumulator of buffer b at column (2b + i) * cap with two
+    // issuers), then the TMEM scale sets.
     const uint32_t tmem_cols = (a.tmem_cols == 256 && !kBS) ? 256u : static_cast<uint32_t>(kTmemCols);
     const int acc_stride = kBS ? cap : static_cast<int>(tmem_cols / 2);
+    const int acc_step = (kBS && a.dual_mma) ? 2 : 1;
     const int set_cols = sf_set_cols(cap);
     constexpr int kTokBox = 16;                  // token rows per TMA box
     constexpr uint32_t kTokBoxBytes = kTokBox * kBlockK;
 
     if (threadIdx.x == 0)
-        init_barriers(ctl, a.stages);
+        init_barriers(ctl, a.stages, static_cast<uint32_t>(acc_step));
     if (warp == 0) {
         grid_dep_wait();   // inputs may come from the previous launch in the stream
         build_group_table(ctl, a, [&](int m) { return ceil_div(m, cap) * n_tiles; });
@@ -1557,7 +1567,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
             }
         }
         loader_tail(ctl, a, stage, phase, issued, aborted, drop);
-    } else if (warp == 1) {
+    } else if (warp == 1 && !kBS) {
         // ----------------------------- MMA issuer -----------------------------
         // MMA operand A = weight tile (format of B), operand B = token tile
         // (format of A).
@@ -1566,14 +1576,10 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         bool issued_any = false;
-        const uint32_t sets_tmem = tmem_base + static_cast<uint32_t>(a.sf_col0);
-        SfState sfs{-1, 0u};
-        uint32_t set_tmem = sets_tmem;
         SwapWalker wk = make_walker();
         SwapSeg x;
         while (next_seg(wk, x)) {
             const uint32_t idesc = make_idesc(a.b_fmt, a.a_fmt, kTileM, static_cast<uint32_t>(x.n_mma));
-            const uint32_t idesc_bs = make_idesc_bs(a.b_fmt, a.a_fmt, kTileM, static_cast<uint32_t>(x.n_mma), 0);
             if (!warp_wait(smem_addr(&ctl.tempty[acc]), acc_phase ^ 1u, ctl, a.timeout_ns, kRoleMma,
                            100 + acc))
                 break;
@@ -1587,25 +1593,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
                     break;
                 }
                 tc_fence_after();
-                if constexpr (kBS) {
-                    const uint8_t *sp = sm.stages + static_cast<size_t>(stage) * a.stage_bytes;
-                    if (sf_load_at(kb, x.kb0, a.sf_k) &&
-                        !sf_take(ctl, a, sfs, stage, sp, cap, sets_tmem, set_cols, set_tmem)) {
-                        ok = false;
-                        break;
-                    }
-                    if (lane == 0) {
-                        const uint64_t wdesc = smem_desc_k_sw128(smem_addr(sp));
-                        const uint64_t tdesc = smem_desc_k_sw128(smem_addr(sp) + w_bytes);
-#pragma unroll
-                        for (int k = 0; k < kBlockK / 32; ++k) {
-                            const uint32_t id = a.sf_k == 1 ? static_cast<uint32_t>(kb & 3) : static_cast<uint32_t>(k);
-                            mma_f8f6f4_bs(d_tmem, wdesc + 2u * k, tdesc + 2u * k, idesc_bs | (id << 4) | (id << 29),
-                                          set_tmem, set_tmem + 4u, (kb != x.kb0 || k != 0) ? 1u : 0u);
-                        }
-                        mma_commit(smem_addr(&ctl.empty[stage]));
-                    }
-                } else if (lane == 0) {
+                if (lane == 0) {
                     const uint32_t sw = smem_addr(sm.stages + static_cast<size_t>(stage) * a.stage_bytes);
                     const uint64_t wdesc = smem_desc_k_sw128(sw);
                     const uint64_t tdesc = smem_desc_k_sw128(sw + w_bytes);
@@ -1633,24 +1621,153 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
             }
         }
         mma_drain(ctl, a, issued_any);
-    } else if (warp == 6) {
-        // ------------------------- block-scale staging -------------------------
+    } else if (kBS && (warp == 1 || (warp == 6 && a.dual_mma))) {
+        // ---------------------- MMA issuers, block-scaled ----------------------
+        // One block-scaled MMA costs an issuing thread far more time than a
+        // plain one, so with room in TMEM two threads issue (warps 1 and 6):
+        // issuer i takes the K blocks whose running index in this CTA is
+        // i mod 2, into its own accumulator; the epilogue adds the two.  Both
+        // walk every K block to follow the stage ring and the scale sets,
+        // which the staging warps write into TMEM.  At each scale load an
+        // issuer retires the previous set (a commit on sffree, counted once
+        // per issuer) and waits for the next one.
+        const int me = warp == 1 ? 0 : 1;
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t par = 0;   // running K-block index mod 2
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool issued_any = false;
+        const uint32_t sets_tmem = tmem_base + static_cast<uint32_t>(a.sf_col0);
+        const int R = a.sf_sets;
+        int j = -1;   // scale loads passed
+        uint32_t set_tmem = sets_tmem;
+        bool ok = true;
+        SwapWalker wk = make_walker();
+        SwapSeg x;
+        while (ok && next_seg(wk, x)) {
+            const uint32_t idesc_bs = make_idesc_bs(a.b_fmt, a.a_fmt, kTileM, static_cast<uint32_t>(x.n_mma), 0);
+            if (!warp_wait(smem_addr(&ctl.tempty[acc]), acc_phase ^ 1u, ctl, a.timeout_ns, kRoleMma,
+                           100 + acc))
+                break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>((acc * acc_step + me) * acc_stride);
+            bool first = true;
+            for (int kb = x.kb0; kb < x.kb1; ++kb) {
+                if (sf_load_at(kb, x.kb0, a.sf_k)) {
+                    if (j >= 0 && lane == 0)
+                        mma_commit(smem_addr(&ctl.sffree[j % R]));
+                    __syncwarp();
+                    ++j;
+                    const int set = j % R;
+                    if (!warp_wait(smem_addr(&ctl.sfset_ready[set]), static_cast<uint32_t>((j / R) & 1), ctl,
+                                   a.timeout_ns, kRoleMma, 300 + set)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    set_tmem = sets_tmem + static_cast<uint32_t>(set * set_cols);
+                }
+                if (acc_step == 1 || static_cast<int>(par) == me) {
+                    if (!warp_wait(smem_addr(&ctl.full[stage]), phase, ctl, a.timeout_ns, kRoleMma, stage)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t sw = smem_addr(sm.stages + static_cast<size_t>(stage) * a.stage_bytes);
+                        const uint64_t wdesc = smem_desc_k_sw128(sw);
+                        const uint64_t tdesc = smem_desc_k_sw128(sw + w_bytes);
+#pragma unroll
+                        for (int k = 0; k < kBlockK / 32; ++k) {
+                            const uint32_t id = a.sf_k == 1 ? static_cast<uint32_t>(kb & 3) : static_cast<uint32_t>(k);
+                            mma_f8f6f4_bs(d_tmem, wdesc + 2u * k, tdesc + 2u * k, idesc_bs | (id << 4) | (id << 29),
+                                          set_tmem, set_tmem + 4u, (!first || k != 0) ? 1u : 0u);
+                        }
+                        mma_commit(smem_addr(&ctl.empty[stage]));
+                    }
+                    __syncwarp();
+                    first = false;
+                    issued_any = true;
+                }
+                par ^= 1u;
+                if (++stage == a.stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok)
+                break;
+            // Both issuers arrive, whether or not this one had a K block of
+            // the segment (the epilogue knows which accumulators hold data).
+            if (lane == 0)
+                mma_commit(smem_addr(&ctl.tfull[acc]));
+            __syncwarp();
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+        mma_drain(ctl, a, issued_any, me == 0 ? &ctl.drain : &ctl.drain2);
+    } else if (kBS && warp >= 7) {
+        // --------------------- block-scale staging into TMEM ---------------------
+        // Warps 7-10, one per TMEM lane quadrant.  For each scale load: wait
+        // for its stage, rearrange the raw bytes ([4 K groups][rows]) into
+        // one 32-bit word per row (byte g = K group g), wait until both
+        // issuers have retired the TMEM set's previous contents, write the
+        // set -- row r of either side at lane r % 32 of every quadrant,
+        // column r / 32 (side B from column 4) -- and arrive on sfset_ready.
         if constexpr (kBS) {
+            const int q = warp & 3;
+            const int R = a.sf_sets;
+            const uint32_t sets_q = tmem_base + static_cast<uint32_t>(a.sf_col0) + (static_cast<uint32_t>(q * 32) << 16);
+            const int nch = (cap + 127) >> 7;   // 1 or 2 (cap <= 224)
+            auto word = [](const uint8_t *raw, int box, int r) {
+                return static_cast<uint32_t>(raw[r]) | (static_cast<uint32_t>(raw[box + r]) << 8) |
+                       (static_cast<uint32_t>(raw[2 * box + r]) << 16) |
+                       (static_cast<uint32_t>(raw[3 * box + r]) << 24);
+            };
             int stage = 0;
             uint32_t phase = 0;
+            int j = -1;
             bool stop = false;
             SwapWalker wk = make_walker();
             SwapSeg x;
             while (!stop && next_seg(wk, x)) {
                 for (int kb = x.kb0; kb < x.kb1; ++kb) {
-                    if (!warp_wait(smem_addr(&ctl.full[stage]), phase, ctl, a.timeout_ns, kRoleScales, stage)) {
-                        stop = true;
-                        break;
-                    }
                     if (sf_load_at(kb, x.kb0, a.sf_k)) {
-                        sf_transpose(sm.stages + static_cast<size_t>(stage) * a.stage_bytes, a, cap);
+                        ++j;
+                        const int set = j % R;
+                        if (!warp_wait(smem_addr(&ctl.full[stage]), phase, ctl, a.timeout_ns, kRoleScales, stage)) {
+                            stop = true;
+                            break;
+                        }
+                        const uint8_t *raw_a = sm.stages + static_cast<size_t>(stage) * a.stage_bytes + a.sf_off;
+                        const uint8_t *raw_b = raw_a + 4 * kTileM;
+                        uint32_t wa[4], wb[8];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            wa[c] = word(raw_a, kTileM, 32 * c + lane);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const int r = 32 * c + lane;
+                            wb[c] = r < cap ? word(raw_b, cap, r) : 0u;
+                        }
+                        if (j >= R && !warp_wait(smem_addr(&ctl.sffree[set]), static_cast<uint32_t>((j / R - 1) & 1),
+                                                 ctl, a.timeout_ns, kRoleScales, 400 + set)) {
+                            stop = true;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t t = sets_q + static_cast<uint32_t>(set * set_cols);
+                        tmem_st_32x32b_x4(t, wa[0], wa[1], wa[2], wa[3]);
+                        tmem_st_32x32b_x4(t + 4u, wb[0], wb[1], wb[2], wb[3]);
+                        if (nch > 1)
+                            tmem_st_32x32b_x4(t + 8u, wb[4], wb[5], wb[6], wb[7]);
+                        tc_fence_before();
+                        __syncwarp();
                         if (lane == 0)
-                            mbar_arrive(smem_addr(&ctl.sfready[stage]));
+                            mbar_arrive(smem_addr(&ctl.sfset_ready[set]));
                     }
                     if (++stage == a.stages) {
                         stage = 0;
@@ -1659,7 +1776,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
                 }
             }
         }
-    } else {
+    } else if (warp >= 2 && warp <= 5) {
         // ------------------------------ epilogue ------------------------------
         // Thread = weight row n (TMEM lane), registers = tokens (TMEM columns).
         // For a fixed token the 32 lanes of a warp write 32 consecutive n.
@@ -1673,6 +1790,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
         // per 16-byte access; a warp touches 512 consecutive bytes.
         const int64_t part_stride4 = kTileM * static_cast<int64_t>(cap) / 4;
         float4 *slots = reinterpret_cast<float4 *>(a.workspace);
+        uint32_t par = 0;   // running K-block index mod 2 (which issuer took a segment's first K block)
         SwapWalker wk = make_walker();
         SwapSeg x;
         while (next_seg(wk, x)) {
@@ -1681,14 +1799,35 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
                 break;
             tc_fence_after();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                   static_cast<uint32_t>(acc * acc_stride);
+                                   static_cast<uint32_t>(acc * acc_step * acc_stride);
+            // With two issuers: the one that took the segment's first K block
+            // always has data; the other one only if the segment has two or
+            // more K blocks.
+            const uint32_t t_first = t_row + par * static_cast<uint32_t>(acc_stride);
+            const uint32_t t_second = t_row + (par ^ 1u) * static_cast<uint32_t>(acc_stride);
+            const bool both = acc_step == 2 && x.kb1 - x.kb0 >= 2;
+            if (acc_step == 2)
+                par ^= static_cast<uint32_t>((x.kb1 - x.kb0) & 1);
+            // 16 accumulator columns of this thread's row, summed over issuers.
+            auto ld16 = [&](int c, uint32_t (&r)[16]) {
+                tmem_ld_32x32b_x16(t_first + static_cast<uint32_t>(c), r);
+                if constexpr (kBS) {
+                    if (both) {
+                        uint32_t r2[16];
+                        tmem_ld_32x32b_x16(t_second + static_cast<uint32_t>(c), r2);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
+                    }
+                }
+            };
             const int64_t grow0 = static_cast<int64_t>(ctl.group_row0[x.g]) + x.tok0;   // output row of token 0
             const int col_base = x.w0 + q * 32;                                         // this warp's 32 columns
             const bool whole = x.kb0 == 0 && x.kb1 == num_kb;
             if (whole) {
                 for (int c = 0; c < x.n_mma; c += 16) {
                     uint32_t r[16];
-                    tmem_ld_32x32b_x16(t_row + static_cast<uint32_t>(c), r);
+                    ld16(c, r);
                     swap_store16<kEpi>(a, dout, r, x.g, grow0 + c, x.n_tok - c, col_base);
                 }
             } else {
@@ -1717,7 +1856,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
                     float4 *mine = slots + (static_cast<int64_t>(blockIdx.x) * 2 + x.kind) * part_stride4;
                     for (int c = 0; c < x.n_mma; c += 16) {
                         uint32_t r[16];
-                        tmem_ld_32x32b_x16(t_row + static_cast<uint32_t>(c), r);
+                        ld16(c, r);
 #pragma unroll
                         for (int v = 0; v < 4; ++v)
                             mine[(c / 4 + v) * kTileM + row] =
@@ -1744,7 +1883,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
                     const int me = static_cast<int>(blockIdx.x) - first;   // this CTA's place in K order
                     for (int c = 0; c < x.n_mma && ok; c += 16) {
                         uint32_t own[16];
-                        tmem_ld_32x32b_x16(t_row + static_cast<uint32_t>(c), own);
+                        ld16(c, own);
                         float acc_v[16];
                         for (int p0 = 0; p0 < n_contrib; p0 += 4) {
                             // four contributors' 16 tokens per batch, every load
@@ -1902,7 +2041,7 @@ static cudaError_t launch_swap_t(const CUtensorMap &tm_w, const CUtensorMap &tm_
                                          static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(k_gemm_swap<kBS, kEpi>, kBS ? kThreadsScaled : kThreads, grid, smem, stream, args, tm_w, tm_t,
+    return launch_pdl(k_gemm_swap<kBS, kEpi>, kBS ? kThreadsSwapScaled : kThreads, grid, smem, stream, args, tm_w, tm_t,
                       tm_sw, tm_st);
 }
 

@@ -225,6 +225,22 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
                  : "memory");
 }
 
+// ---- tcgen05: registers -> TMEM ------------------------------------------------------
+
+// Warp-wide: lane l of the warp writes TMEM lane (taddr.lane + l), 4
+// consecutive 32-bit columns from taddr.col, and waits until the writes are
+// done (a later tcgen05.fence::before_thread_sync then orders them before a
+// barrier arrive that another thread's MMAs wait on).  A warp may touch only
+// its own 32-lane quadrant (warp index mod 4).
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2,
+                                                  uint32_t v3)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};\n\t"
+                 "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+                 "r"(v0), "r"(v1), "r"(v2), "r"(v3)
+                 : "memory");
+}
+
 // ---- programmatic dependent launch --------------------------------------------------
 
 // Wait until every grid this launch depends on has completed and its memory

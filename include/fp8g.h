@@ -101,6 +101,11 @@ typedef enum {
  *                     block-scaled problems with short K or 32-element
  *                     groups, where single-SM tiles measured faster). */
 #define FP8G_PAIR_TILES 0x4000u
+/*   FP8G_ONE_MMA_ISSUER  block-scaled SwapAB kernel: one thread issues every
+ *                     MMA (default: two threads alternate K blocks, each
+ *                     into its own accumulator, when TMEM holds four
+ *                     accumulators of the token chunk, i.e. up to 112 tokens) */
+#define FP8G_ONE_MMA_ISSUER 0x8000u
 /*   FP8G_STAGES(n)    at most n shared-memory pipeline stages (1..15)       */
 #define FP8G_STAGES(n) ((((uint32_t)(n)) & 15u) << 20)
 /*   FP8G_SHARE_SM     SwapAB kernel with <= 128 tokens per chunk: half the

@@ -107,3 +107,18 @@ def test_binding_refuses_cpu_tensors():
     a = torch.zeros((16, 16), dtype=torch.uint8)
     with pytest.raises(ValueError):
         fp8g.fp8_gemm_nt(a, a, a_dtype=0, b_dtype=0)
+
+
+def test_python_flag_constants_match_the_header():
+    """Every flag the binding exports has the value the C header defines."""
+    import re
+    import fp8_tensor_core_gb300 as fp8g
+    with open(os.path.join(ROOT, "include", "fp8g.h")) as f:
+        defs = dict(re.findall(r"#define FP8G_([A-Z0-9_]+) (0x[0-9a-fA-F]+|[0-9]+)u?\b", f.read()))
+    checked = 0
+    for name in ("SWAP_AUTO", "SWAP_ON", "SWAP_OFF", "DEBUG_ONE_STAGE", "WHOLE_TILES", "STREAM_K", "SINGLE_SM_TILES",
+                 "NO_PDL", "PAIR_TILES", "ONE_MMA_ISSUER", "SHARE_SM"):
+        assert name in defs, name
+        assert getattr(fp8g, name) == int(defs[name], 0), name
+        checked += 1
+    assert checked == 11

@@ -155,9 +155,12 @@ def test_scales_reach_the_right_k_group():
 # ---- SwapAB (weights on M, tokens on the runtime N) -----------------------------------
 
 @pytest.mark.parametrize("gran", [128, 32])
-@pytest.mark.parametrize("flags", [ON, ON | fp8g.WHOLE_TILES])
+@pytest.mark.parametrize("flags", [ON, ON | fp8g.WHOLE_TILES, ON | fp8g.ONE_MMA_ISSUER])
 @pytest.mark.parametrize("M,N,K", [(1, 256, 512), (40, 640, 1536), (100, 384, 4112), (224, 512, 1024)])
 def test_swap(M, N, K, flags, gran):
+    # Token chunks of 16, 48 and 112 take two MMA issuers (alternate K blocks,
+    # two accumulators); 224 takes one.  (1, 256, 512): eight CTAs of one K
+    # block each, so a segment's second accumulator is often empty.
     check_dense_bs(M, N, K, gran, flags, seed=550 + M + N + gran)
 
 
@@ -196,7 +199,8 @@ def grouped_bs_case(G, M_max, N, K, mm, gran, flags, hint, seed, fa=E4, fb=E4):
 
 
 @pytest.mark.parametrize("gran", [128, 32])
-@pytest.mark.parametrize("flags,hint", [(ON, 32), (ON | fp8g.WHOLE_TILES, 64), (OFF, 0), (AUTO, 0)])
+@pytest.mark.parametrize("flags,hint", [(ON, 32), (ON | fp8g.WHOLE_TILES, 64), (ON | fp8g.ONE_MMA_ISSUER, 32),
+                                        (OFF, 0), (AUTO, 0)])
 def test_grouped(flags, hint, gran):
     mm = [0, 1, 9, 16, 17, 32, 5, 64]
     grouped_bs_case(len(mm), 64, 384, 640, mm, gran, flags, hint, seed=600 + gran)
