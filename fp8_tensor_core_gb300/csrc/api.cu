@@ -494,10 +494,13 @@ int launch(const Problem &p, cudaStream_t stream)
             // least two scale sets fit in TMEM.
             const int set_cols = sf_set_cols(static_cast<int>(cap));
             const int sets_dual = std::min<int>(kMaxSfSets, (kTmemCols - 4 * static_cast<int>(cap)) / set_cols);
-            if (sets_dual >= 2 && !(p.flags & FP8G_ONE_MMA_ISSUER)) {
+            // (An even stage count keeps each stage with one issuer, whose
+            // parity waits on it then never skip a phase.)
+            if (sets_dual >= 2 && !(p.flags & FP8G_ONE_MMA_ISSUER) && args.stages >= 2) {
                 args.dual_mma = 1;
                 args.sf_col0 = static_cast<int32_t>(4 * cap);
                 args.sf_sets = sets_dual;
+                args.stages &= ~1;
             }
         } else {
             args.stages = pick_stages(info, args.stage_bytes, static_cast<int>(p.G), p.flags);
@@ -533,7 +536,7 @@ int launch(const Problem &p, cudaStream_t stream)
     // (measured on GB300: 2-6 % faster at K >= 7168, even at K = 4096, 7-13 %
     // slower at K = 2048 or with 32-element groups, whose per-K-block scale
     // copies weigh more in the pair's longer K block).
-    const bool pair_ok = !p.sf_k || (p.sf_k == 1 && p.K > 4096) || (p.flags & FP8G_PAIR_TILES);
+    const bool pair_ok = !p.sf_k || (p.flags & FP8G_PAIR_TILES);
     if (!p.masked_m && !p.group_offsets && p.G == 1 && p.rows_a > kTileM && !(p.flags & FP8G_SINGLE_SM_TILES) &&
         pair_ok) {
         const int64_t m_tiles2 = cdiv(p.rows_a, 2 * kTileM);
@@ -598,6 +601,24 @@ int launch(const Problem &p, cudaStream_t stream)
     args.tile_n = tile_n;
     if (p.sf_k) {
         plan_blockscaled(args, info, tile_n, static_cast<int>(p.G), p.flags);
+        // Two MMA issuers (alternate K blocks, one accumulator each): with
+        // two accumulator buffers per issuer when four tiles and two scale
+        // sets fit in TMEM; with one (the epilogue then holds the issuers
+        // back at every tile) only for 32-element groups, where it measured
+        // faster than one issuer -- with 128-element groups it was slower.
+        // (An even stage count keeps each stage with one issuer.)
+        if (!(p.flags & FP8G_ONE_MMA_ISSUER) && args.stages >= 2) {
+            const int set_cols = sf_set_cols(tile_n);
+            const int sets2 = std::min(kMaxSfSets, (kTmemCols - 4 * tile_n) / set_cols);
+            const int sets1 = std::min(kMaxSfSets, (kTmemCols - 2 * tile_n) / set_cols);
+            if (sets2 >= 2 || (sets1 >= 2 && (p.sf_k == 4 || (p.flags & FP8G_TWO_MMA_ISSUERS)))) {
+                args.dual_mma = 1;
+                args.acc_bufs = sets2 >= 2 ? 2 : 1;
+                args.sf_col0 = args.acc_bufs * 2 * tile_n;
+                args.sf_sets = sets2 >= 2 ? sets2 : sets1;
+                args.stages &= ~1;
+            }
+        }
     } else {
         args.stage_bytes = kTileM * kBlockK + tile_n * kBlockK;
         args.stages = pick_stages(info, args.stage_bytes, static_cast<int>(p.G), p.flags);

@@ -455,6 +455,76 @@ __device__ __forceinline__ bool sf_take(SmemCtl &ctl, const GemmArgs &a, SfState
     return true;
 }
 
+// ---- block scales written into TMEM by staging warps ---------------------------------
+// (SwapAB and single-SM kernels.)  A copy of scale factors into TMEM issued
+// by the MMA thread costs it ~100 ns and a block-scaled MMA ~95 ns, so the
+// scale sets are written by four staging warps instead (tcgen05.st, one
+// TMEM lane quadrant each) and announced on sfset_ready[set] (four
+// arrivals); the MMA issuers only wait for a set and retire it.
+
+// Staging warp, all lanes, for scale load j (the raw bytes of stage_ptr,
+// whose full barrier has passed): build one 32-bit word per row (byte g =
+// K group g of the load), wait until every issuer has retired the set's
+// previous contents, write the set into this warp's lane quadrant -- row r
+// of side A at lane r % 32, column r / 32; side B from column 4 likewise --
+// and arrive.  box_b <= 256.  Returns false when a wait gave up.
+__device__ __forceinline__ bool sf_stage_tmem(SmemCtl &ctl, const GemmArgs &a, const uint8_t *stage_ptr, int box_b,
+                                              int j, uint32_t sets_q, int set_cols)
+{
+    const int lane = threadIdx.x & 31;
+    const int R = a.sf_sets;
+    const int set = j % R;
+    auto word = [](const uint8_t *raw, int box, int r) {
+        return static_cast<uint32_t>(raw[r]) | (static_cast<uint32_t>(raw[box + r]) << 8) |
+               (static_cast<uint32_t>(raw[2 * box + r]) << 16) | (static_cast<uint32_t>(raw[3 * box + r]) << 24);
+    };
+    const uint8_t *raw_a = stage_ptr + a.sf_off;   // [4][128]
+    const uint8_t *raw_b = raw_a + 4 * kTileM;      // [4][box_b]
+    uint32_t wa[4], wb[8];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        wa[c] = word(raw_a, kTileM, 32 * c + lane);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const int r = 32 * c + lane;
+        wb[c] = r < box_b ? word(raw_b, box_b, r) : 0u;
+    }
+    if (j >= R && !warp_wait(smem_addr(&ctl.sffree[set]), static_cast<uint32_t>((j / R - 1) & 1), ctl, a.timeout_ns,
+                             kRoleScales, 400 + set))
+        return false;
+    tc_fence_after();
+    const uint32_t t = sets_q + static_cast<uint32_t>(set * set_cols);
+    tmem_st_32x32b_x4(t, wa[0], wa[1], wa[2], wa[3]);
+    tmem_st_32x32b_x4(t + 4u, wb[0], wb[1], wb[2], wb[3]);
+    if (box_b > 128)
+        tmem_st_32x32b_x4(t + 8u, wb[4], wb[5], wb[6], wb[7]);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0)
+        mbar_arrive(smem_addr(&ctl.sfset_ready[set]));
+    return true;
+}
+
+// MMA issuer warp, all lanes, at scale load j + 1: retire set j (a commit
+// that arrives once this thread's MMAs so far are done), wait for set j + 1
+// and point set_tmem at it.  Returns false when the wait gave up.
+__device__ __forceinline__ bool sf_next_set(SmemCtl &ctl, const GemmArgs &a, int &j, uint32_t sets_tmem,
+                                            int set_cols, uint32_t &set_tmem)
+{
+    const int R = a.sf_sets;
+    if (j >= 0 && (threadIdx.x & 31) == 0)
+        mma_commit(smem_addr(&ctl.sffree[j % R]));
+    __syncwarp();
+    ++j;
+    const int set = j % R;
+    if (!warp_wait(smem_addr(&ctl.sfset_ready[set]), static_cast<uint32_t>((j / R) & 1), ctl, a.timeout_ns, kRoleMma,
+                   300 + set))
+        return false;
+    tc_fence_after();
+    set_tmem = sets_tmem + static_cast<uint32_t>(set * set_cols);
+    return true;
+}
+
 // Group table: valid rows per group (clamped to [0, rows_a]) and the
 // exclusive prefix of work units.  Run by one warp.
 template <typename UnitsFn>
@@ -568,8 +638,10 @@ __device__ __forceinline__ void init_barriers(SmemCtl &ctl, int stages, uint32_t
     }
     mbar_init(smem_addr(&ctl.drain), 1);
     mbar_init(smem_addr(&ctl.drain2), 1);
-    for (int s = 0; s < stages; ++s)
+    for (int s = 0; s < stages; ++s) {
         mbar_init(smem_addr(&ctl.sfready[s]), 1);
+        mbar_init(smem_addr(&ctl.sffull[s]), 1);
+    }
     for (int i = 0; i < kMaxSfSets; ++i) {
         mbar_init(smem_addr(&ctl.sffree[i]), issuers);
         mbar_init(smem_addr(&ctl.sfset_ready[i]), 4);   // one arrival per staging warp
@@ -617,6 +689,18 @@ __device__ __forceinline__ void loader_tail(SmemCtl &ctl, const GemmArgs &a, int
     }
 }
 
+// Loader (all lanes), block-scaled single-SM and SwapAB kernels: the scale
+// bytes of a stage complete on their own barrier sffull[s].  `par` holds,
+// per stage, the parity of the number of scale fills posted, `used` which
+// stages ever had one; wait (bounded) until the last fill of each has
+// landed.  Without an abort they all have (the staging warps consumed them).
+__device__ __forceinline__ void sf_loader_drain(SmemCtl &ctl, const GemmArgs &a, uint32_t par, uint32_t used)
+{
+    for (int s = 0; s < a.stages; ++s)
+        if ((used >> s) & 1u)
+            warp_wait_drain(smem_addr(&ctl.sffull[s]), ((par >> s) & 1u) ^ 1u, a.timeout_ns);
+}
+
 // MMA issuer tail: wait until every tensor-core operation it issued has
 // completed, so TMEM can be freed.
 __device__ __forceinline__ void mma_drain(SmemCtl &ctl, const GemmArgs &a, bool issued_any,
@@ -635,7 +719,7 @@ __device__ __forceinline__ void mma_drain(SmemCtl &ctl, const GemmArgs &a, bool 
 // k_gemm_mn: tokens on M, weights on N.
 // =====================================================================================
 template <bool kBS, bool kEpi>
-__global__ void __launch_bounds__(kThreadsScaled, 1)
+__global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
     k_gemm_mn(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
               const __grid_constant__ CUtensorMap tm_sa, const __grid_constant__ CUtensorMap tm_sb,
               const GemmArgs a)
@@ -650,12 +734,17 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
     const uint32_t tx_bytes = a_bytes + static_cast<uint32_t>(a.tile_n) * kBlockK;
     const uint32_t sf_bytes = 4u * static_cast<uint32_t>(kTileM + a.tile_n);
     // Accumulator spacing in TMEM: 256 columns, or tile_n when the block-scale
-    // sets follow the two accumulators.
+    // sets follow the accumulators.  With block scales and two MMA issuers,
+    // issuer i's accumulator of buffer b sits at column (acc_step * b + i) *
+    // tile_n, with one buffer per issuer when four do not fit (the epilogue
+    // of a tile then holds the issuers back until it has read it).
     const int acc_stride = kBS ? a.tile_n : kAccStride;
+    const int acc_step = (kBS && a.dual_mma) ? 2 : 1;
+    const int n_bufs = (kBS && a.dual_mma && a.acc_bufs == 1) ? 1 : 2;
     const int set_cols = sf_set_cols(a.tile_n);
 
     if (threadIdx.x == 0)
-        init_barriers(ctl, a.stages);
+        init_barriers(ctl, a.stages, static_cast<uint32_t>(acc_step));
     if (warp == 0) {
         grid_dep_wait();   // inputs may come from the previous launch in the stream
         build_group_table(ctl, a, [&](int m) { return ceil_div(m, kTileM) * n_tiles; });
@@ -705,6 +794,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
         long long issued = 0;
         bool aborted = false;
         const bool drop = (a.flags & FP8G_DEBUG_DROP_FIRST_LOAD) && blockIdx.x == 0;
+        uint32_t sf_par = 0, sf_used = 0;   // per stage: parity of scale fills posted, any posted
         for (int u = blockIdx.x; u < total && !aborted; u += gridDim.x) {
             int g, m0, n0, mv;
             decode(u, g, m0, n0, mv);
@@ -714,18 +804,24 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
                     aborted = true;
                     break;
                 }
+                const bool sf = kBS && sf_load_at(kb, 0, a.sf_k) && !(drop && issued == 0);
                 if (lane == 0 && !(drop && issued == 0)) {
                     uint8_t *sa = sm.stages + static_cast<size_t>(stage) * a.stage_bytes;
                     const uint32_t fb = smem_addr(&ctl.full[stage]);
-                    const bool sf = kBS && sf_load_at(kb, 0, a.sf_k);
-                    mbar_arrive_expect_tx(fb, tx_bytes + (sf ? sf_bytes : 0u));
+                    mbar_arrive_expect_tx(fb, tx_bytes);
                     tma_load_3d(smem_addr(sa), &tm_a, fb, kb * kBlockK, a_row(a, ctl, g, m0), a_grp(a, g));
                     tma_load_3d(smem_addr(sa + a_bytes), &tm_b, fb, kb * kBlockK, n0, g);
                     if (sf) {
+                        const uint32_t sb = smem_addr(&ctl.sffull[stage]);
                         const int y = sf_first_group(kb, a.sf_k);
-                        tma_load_3d(smem_addr(sa + a.sf_off), &tm_sa, fb, m0, y, g);
-                        tma_load_3d(smem_addr(sa + a.sf_off + 4 * kTileM), &tm_sb, fb, n0, y, g);
+                        mbar_arrive_expect_tx(sb, sf_bytes);
+                        tma_load_3d(smem_addr(sa + a.sf_off), &tm_sa, sb, m0, y, g);
+                        tma_load_3d(smem_addr(sa + a.sf_off + 4 * kTileM), &tm_sb, sb, n0, y, g);
                     }
+                }
+                if (sf) {
+                    sf_par ^= 1u << stage;
+                    sf_used |= 1u << stage;
                 }
                 __syncwarp();
                 ++issued;
@@ -736,13 +832,11 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
             }
         }
         loader_tail(ctl, a, stage, phase, issued, aborted, drop);
-    } else if (warp == 1) {
+        if constexpr (kBS)
+            sf_loader_drain(ctl, a, sf_par, sf_used);
+    } else if (warp == 1 && !kBS) {
         // ----------------------------- MMA issuer -----------------------------
         const uint32_t idesc = make_idesc(a.a_fmt, a.b_fmt, kTileM, a.tile_n);
-        const uint32_t idesc_bs = make_idesc_bs(a.a_fmt, a.b_fmt, kTileM, a.tile_n, 0);
-        const uint32_t sets_tmem = tmem_base + static_cast<uint32_t>(a.sf_col0);
-        SfState sfs{-1, 0u};
-        uint32_t set_tmem = sets_tmem;
         int stage = 0;
         uint32_t phase = 0;
         int acc = 0;
@@ -762,25 +856,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
                     break;
                 }
                 tc_fence_after();
-                if constexpr (kBS) {
-                    const uint8_t *sp = sm.stages + static_cast<size_t>(stage) * a.stage_bytes;
-                    if (sf_load_at(kb, 0, a.sf_k) &&
-                        !sf_take(ctl, a, sfs, stage, sp, a.tile_n, sets_tmem, set_cols, set_tmem)) {
-                        ok = false;
-                        break;
-                    }
-                    if (lane == 0) {
-                        const uint64_t adesc = smem_desc_k_sw128(smem_addr(sp));
-                        const uint64_t bdesc = smem_desc_k_sw128(smem_addr(sp) + a_bytes);
-#pragma unroll
-                        for (int k = 0; k < kBlockK / 32; ++k) {
-                            const uint32_t id = a.sf_k == 1 ? static_cast<uint32_t>(kb & 3) : static_cast<uint32_t>(k);
-                            mma_f8f6f4_bs(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc_bs | (id << 4) | (id << 29),
-                                          set_tmem, set_tmem + 4u, (kb | k) != 0 ? 1u : 0u);
-                        }
-                        mma_commit(smem_addr(&ctl.empty[stage]));
-                    }
-                } else if (lane == 0) {
+                if (lane == 0) {
                     const uint32_t sa = smem_addr(sm.stages + static_cast<size_t>(stage) * a.stage_bytes);
                     const uint64_t adesc = smem_desc_k_sw128(sa);
                     const uint64_t bdesc = smem_desc_k_sw128(sa + a_bytes);
@@ -810,35 +886,108 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
             }
         }
         mma_drain(ctl, a, issued_any);
-    } else if (warp == 6) {
-        // ------------------------- block-scale staging -------------------------
+    } else if (kBS && (warp == 1 || (warp == 6 && a.dual_mma))) {
+        // ---------------------- MMA issuers, block-scaled ----------------------
+        // As in the SwapAB kernel: one or two issuing threads (warps 1 and
+        // 6); with two, issuer i takes the K blocks whose running index in
+        // this CTA is i mod 2, into its own accumulator, and the epilogue
+        // adds the two.  Scale sets come from the staging warps.
+        const int me = warp == 1 ? 0 : 1;
+        const uint32_t idesc_bs = make_idesc_bs(a.a_fmt, a.b_fmt, kTileM, a.tile_n, 0);
+        const uint32_t sets_tmem = tmem_base + static_cast<uint32_t>(a.sf_col0);
+        uint32_t set_tmem = sets_tmem;
+        int j = -1;   // scale loads passed
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t par = 0;   // running K-block index mod 2
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool issued_any = false;
+        bool ok = true;
+        for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+            if (!warp_wait(smem_addr(&ctl.tempty[acc]), acc_phase ^ 1u, ctl, a.timeout_ns, kRoleMma,
+                           100 + acc))
+                break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>((acc * acc_step + me) * acc_stride);
+            bool first = true;
+            for (int kb = 0; kb < a.num_kb; ++kb) {
+                if (sf_load_at(kb, 0, a.sf_k) && !sf_next_set(ctl, a, j, sets_tmem, set_cols, set_tmem)) {
+                    ok = false;
+                    break;
+                }
+                if (acc_step == 1 || static_cast<int>(par) == me) {
+                    if (!warp_wait(smem_addr(&ctl.full[stage]), phase, ctl, a.timeout_ns, kRoleMma, stage)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t sa = smem_addr(sm.stages + static_cast<size_t>(stage) * a.stage_bytes);
+                        const uint64_t adesc = smem_desc_k_sw128(sa);
+                        const uint64_t bdesc = smem_desc_k_sw128(sa + a_bytes);
+#pragma unroll
+                        for (int k = 0; k < kBlockK / 32; ++k) {
+                            const uint32_t id = a.sf_k == 1 ? static_cast<uint32_t>(kb & 3) : static_cast<uint32_t>(k);
+                            mma_f8f6f4_bs(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc_bs | (id << 4) | (id << 29),
+                                          set_tmem, set_tmem + 4u, (!first || k != 0) ? 1u : 0u);
+                        }
+                        mma_commit(smem_addr(&ctl.empty[stage]));
+                    }
+                    __syncwarp();
+                    first = false;
+                    issued_any = true;
+                }
+                par ^= 1u;
+                if (++stage == a.stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok)
+                break;
+            if (lane == 0)
+                mma_commit(smem_addr(&ctl.tfull[acc]));
+            __syncwarp();
+            if (++acc == n_bufs) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+        mma_drain(ctl, a, issued_any, me == 0 ? &ctl.drain : &ctl.drain2);
+    } else if (kBS && warp >= 7) {
+        // --------------------- block-scale staging into TMEM ---------------------
         if constexpr (kBS) {
+            const uint32_t sets_q = tmem_base + static_cast<uint32_t>(a.sf_col0) +
+                                    (static_cast<uint32_t>((warp & 3) * 32) << 16);
             int stage = 0;
-            uint32_t phase = 0;
+            uint32_t sf_par = 0;   // per stage: parity of the next scale fill to wait for
+            int j = -1;
             bool stop = false;
             for (int u = blockIdx.x; u < total && !stop; u += gridDim.x) {
                 for (int kb = 0; kb < a.num_kb; ++kb) {
-                    if (!warp_wait(smem_addr(&ctl.full[stage]), phase, ctl, a.timeout_ns, kRoleScales, stage)) {
-                        stop = true;
-                        break;
-                    }
                     if (sf_load_at(kb, 0, a.sf_k)) {
-                        sf_transpose(sm.stages + static_cast<size_t>(stage) * a.stage_bytes, a, a.tile_n);
-                        if (lane == 0)
-                            mbar_arrive(smem_addr(&ctl.sfready[stage]));
+                        ++j;
+                        if (!warp_wait(smem_addr(&ctl.sffull[stage]), (sf_par >> stage) & 1u, ctl, a.timeout_ns,
+                                       kRoleScales, stage) ||
+                            !sf_stage_tmem(ctl, a, sm.stages + static_cast<size_t>(stage) * a.stage_bytes, a.tile_n,
+                                           j, sets_q, set_cols)) {
+                            stop = true;
+                            break;
+                        }
+                        sf_par ^= 1u << stage;
                     }
-                    if (++stage == a.stages) {
+                    if (++stage == a.stages)
                         stage = 0;
-                        phase ^= 1u;
-                    }
                 }
             }
         }
-    } else {
+    } else if (warp >= 2 && warp <= 5) {
         // ------------------------------ epilogue ------------------------------
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
         int acc = 0;
         uint32_t acc_phase = 0;
+        uint32_t par = 0;   // running K-block index mod 2 (which issuer took a tile's first K block)
         __nv_bfloat16 *dout = static_cast<__nv_bfloat16 *>(a.d);
         for (int u = blockIdx.x; u < total; u += gridDim.x) {
             int g, m0, n0, mv;
@@ -852,11 +1001,25 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
             const int64_t grow = static_cast<int64_t>(ctl.group_row0[g]) + row;
             __nv_bfloat16 *drow = dout + grow * static_cast<int64_t>(a.n);
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                   static_cast<uint32_t>(acc * acc_stride);
+                                   static_cast<uint32_t>(acc * acc_step * acc_stride);
+            const uint32_t t_first = t_row + par * static_cast<uint32_t>(acc_stride);
+            const uint32_t t_second = t_row + (par ^ 1u) * static_cast<uint32_t>(acc_stride);
+            const bool both = acc_step == 2 && a.num_kb >= 2;
+            if (acc_step == 2)
+                par ^= static_cast<uint32_t>(a.num_kb & 1);
             const float rf = (kEpi && row_ok) ? row_factor(a, g, grow) : 1.0f;
             for (int c = 0; c < a.tile_n; c += 32) {
                 uint32_t r[32];
-                tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c), r);
+                tmem_ld_32x32b_x32(t_first + static_cast<uint32_t>(c), r);
+                if constexpr (kBS) {
+                    if (both) {
+                        uint32_t r2[32];
+                        tmem_ld_32x32b_x32(t_second + static_cast<uint32_t>(c), r2);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
+                    }
+                }
                 if (row_ok) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -868,7 +1031,7 @@ __global__ void __launch_bounds__(kThreadsScaled, 1)
             }
             tc_fence_before();
             mbar_arrive(smem_addr(&ctl.tempty[acc]));
-            if (++acc == 2) {
+            if (++acc == n_bufs) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
@@ -1416,7 +1579,7 @@ struct SwapWalker {
 };
 
 template <bool kBS, bool kEpi>
-__global__ void __launch_bounds__(kBS ? kThreadsSwapScaled : kThreads, 1)
+__global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
     k_gemm_swap(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_t,
                 const __grid_constant__ CUtensorMap tm_sw, const __grid_constant__ CUtensorMap tm_st,
                 const GemmArgs a)
@@ -1533,6 +1696,7 @@ __global__ void __launch_bounds__(kBS ? kThreadsSwapScaled : kThreads, 1)
         bool aborted = false;
         const bool drop = (a.flags & FP8G_DEBUG_DROP_FIRST_LOAD) && blockIdx.x == 0;
         const uint64_t w_policy = policy_evict_first();   // weights are read once
+        uint32_t sf_par = 0, sf_used = 0;   // per stage: parity of scale fills posted, any posted
         SwapWalker wk = make_walker();
         SwapSeg x;
         while (!aborted && next_seg(wk, x)) {
@@ -1543,20 +1707,26 @@ __global__ void __launch_bounds__(kBS ? kThreadsSwapScaled : kThreads, 1)
                     aborted = true;
                     break;
                 }
+                const bool sf = kBS && sf_load_at(kb, x.kb0, a.sf_k) && !(drop && issued == 0);
                 if (lane == 0 && !(drop && issued == 0)) {
                     uint8_t *sw = sm.stages + static_cast<size_t>(stage) * a.stage_bytes;
                     const uint32_t fb = smem_addr(&ctl.full[stage]);
-                    const bool sf = kBS && sf_load_at(kb, x.kb0, a.sf_k);
-                    mbar_arrive_expect_tx(fb, tx + (sf ? 4u * static_cast<uint32_t>(kTileM + cap) : 0u));
+                    mbar_arrive_expect_tx(fb, tx);
                     tma_load_3d_hint(smem_addr(sw), &tm_w, fb, kb * kBlockK, x.w0, x.g, w_policy);
                     for (int r = 0; r < x.n_mma; r += kTokBox)
                         tma_load_3d(smem_addr(sw + w_bytes + (r / kTokBox) * kTokBoxBytes), &tm_t, fb,
                                     kb * kBlockK, a_row(a, ctl, x.g, x.tok0 + r), a_grp(a, x.g));
                     if (sf) {
+                        const uint32_t sb = smem_addr(&ctl.sffull[stage]);
                         const int y = sf_first_group(kb, a.sf_k);
-                        tma_load_3d_hint(smem_addr(sw + a.sf_off), &tm_sw, fb, x.w0, y, x.g, w_policy);
-                        tma_load_3d(smem_addr(sw + a.sf_off + 4 * kTileM), &tm_st, fb, x.tok0, y, x.g);
+                        mbar_arrive_expect_tx(sb, 4u * static_cast<uint32_t>(kTileM + cap));
+                        tma_load_3d_hint(smem_addr(sw + a.sf_off), &tm_sw, sb, x.w0, y, x.g, w_policy);
+                        tma_load_3d(smem_addr(sw + a.sf_off + 4 * kTileM), &tm_st, sb, x.tok0, y, x.g);
                     }
+                }
+                if (sf) {
+                    sf_par ^= 1u << stage;
+                    sf_used |= 1u << stage;
                 }
                 __syncwarp();
                 ++issued;
@@ -1567,6 +1737,8 @@ __global__ void __launch_bounds__(kBS ? kThreadsSwapScaled : kThreads, 1)
             }
         }
         loader_tail(ctl, a, stage, phase, issued, aborted, drop);
+        if constexpr (kBS)
+            sf_loader_drain(ctl, a, sf_par, sf_used);
     } else if (warp == 1 && !kBS) {
         // ----------------------------- MMA issuer -----------------------------
         // MMA operand A = weight tile (format of B), operand B = token tile
@@ -1639,7 +1811,6 @@ __global__ void __launch_bounds__(kBS ? kThreadsSwapScaled : kThreads, 1)
         uint32_t acc_phase = 0;
         bool issued_any = false;
         const uint32_t sets_tmem = tmem_base + static_cast<uint32_t>(a.sf_col0);
-        const int R = a.sf_sets;
         int j = -1;   // scale loads passed
         uint32_t set_tmem = sets_tmem;
         bool ok = true;
@@ -1654,19 +1825,9 @@ __global__ void __launch_bounds__(kBS ? kThreadsSwapScaled : kThreads, 1)
             const uint32_t d_tmem = tmem_base + static_cast<uint32_t>((acc * acc_step + me) * acc_stride);
             bool first = true;
             for (int kb = x.kb0; kb < x.kb1; ++kb) {
-                if (sf_load_at(kb, x.kb0, a.sf_k)) {
-                    if (j >= 0 && lane == 0)
-                        mma_commit(smem_addr(&ctl.sffree[j % R]));
-                    __syncwarp();
-                    ++j;
-                    const int set = j % R;
-                    if (!warp_wait(smem_addr(&ctl.sfset_ready[set]), static_cast<uint32_t>((j / R) & 1), ctl,
-                                   a.timeout_ns, kRoleMma, 300 + set)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    set_tmem = sets_tmem + static_cast<uint32_t>(set * set_cols);
+                if (sf_load_at(kb, x.kb0, a.sf_k) && !sf_next_set(ctl, a, j, sets_tmem, set_cols, set_tmem)) {
+                    ok = false;
+                    break;
                 }
                 if (acc_step == 1 || static_cast<int>(par) == me) {
                     if (!warp_wait(smem_addr(&ctl.full[stage]), phase, ctl, a.timeout_ns, kRoleMma, stage)) {
@@ -1711,24 +1872,13 @@ __global__ void __launch_bounds__(kBS ? kThreadsSwapScaled : kThreads, 1)
         mma_drain(ctl, a, issued_any, me == 0 ? &ctl.drain : &ctl.drain2);
     } else if (kBS && warp >= 7) {
         // --------------------- block-scale staging into TMEM ---------------------
-        // Warps 7-10, one per TMEM lane quadrant.  For each scale load: wait
-        // for its stage, rearrange the raw bytes ([4 K groups][rows]) into
-        // one 32-bit word per row (byte g = K group g), wait until both
-        // issuers have retired the TMEM set's previous contents, write the
-        // set -- row r of either side at lane r % 32 of every quadrant,
-        // column r / 32 (side B from column 4) -- and arrive on sfset_ready.
+        // Warps 7-10, one per TMEM lane quadrant: for each scale load, wait
+        // for its stage and write the TMEM scale set (sf_stage_tmem).
         if constexpr (kBS) {
-            const int q = warp & 3;
-            const int R = a.sf_sets;
-            const uint32_t sets_q = tmem_base + static_cast<uint32_t>(a.sf_col0) + (static_cast<uint32_t>(q * 32) << 16);
-            const int nch = (cap + 127) >> 7;   // 1 or 2 (cap <= 224)
-            auto word = [](const uint8_t *raw, int box, int r) {
-                return static_cast<uint32_t>(raw[r]) | (static_cast<uint32_t>(raw[box + r]) << 8) |
-                       (static_cast<uint32_t>(raw[2 * box + r]) << 16) |
-                       (static_cast<uint32_t>(raw[3 * box + r]) << 24);
-            };
+            const uint32_t sets_q = tmem_base + static_cast<uint32_t>(a.sf_col0) +
+                                    (static_cast<uint32_t>((warp & 3) * 32) << 16);
             int stage = 0;
-            uint32_t phase = 0;
+            uint32_t sf_par = 0;   // per stage: parity of the next scale fill to wait for
             int j = -1;
             bool stop = false;
             SwapWalker wk = make_walker();
@@ -1737,42 +1887,17 @@ __global__ void __launch_bounds__(kBS ? kThreadsSwapScaled : kThreads, 1)
                 for (int kb = x.kb0; kb < x.kb1; ++kb) {
                     if (sf_load_at(kb, x.kb0, a.sf_k)) {
                         ++j;
-                        const int set = j % R;
-                        if (!warp_wait(smem_addr(&ctl.full[stage]), phase, ctl, a.timeout_ns, kRoleScales, stage)) {
+                        if (!warp_wait(smem_addr(&ctl.sffull[stage]), (sf_par >> stage) & 1u, ctl, a.timeout_ns,
+                                       kRoleScales, stage) ||
+                            !sf_stage_tmem(ctl, a, sm.stages + static_cast<size_t>(stage) * a.stage_bytes, cap, j,
+                                           sets_q, set_cols)) {
                             stop = true;
                             break;
                         }
-                        const uint8_t *raw_a = sm.stages + static_cast<size_t>(stage) * a.stage_bytes + a.sf_off;
-                        const uint8_t *raw_b = raw_a + 4 * kTileM;
-                        uint32_t wa[4], wb[8];
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            wa[c] = word(raw_a, kTileM, 32 * c + lane);
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const int r = 32 * c + lane;
-                            wb[c] = r < cap ? word(raw_b, cap, r) : 0u;
-                        }
-                        if (j >= R && !warp_wait(smem_addr(&ctl.sffree[set]), static_cast<uint32_t>((j / R - 1) & 1),
-                                                 ctl, a.timeout_ns, kRoleScales, 400 + set)) {
-                            stop = true;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t t = sets_q + static_cast<uint32_t>(set * set_cols);
-                        tmem_st_32x32b_x4(t, wa[0], wa[1], wa[2], wa[3]);
-                        tmem_st_32x32b_x4(t + 4u, wb[0], wb[1], wb[2], wb[3]);
-                        if (nch > 1)
-                            tmem_st_32x32b_x4(t + 8u, wb[4], wb[5], wb[6], wb[7]);
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0)
-                            mbar_arrive(smem_addr(&ctl.sfset_ready[set]));
+                        sf_par ^= 1u << stage;
                     }
-                    if (++stage == a.stages) {
+                    if (++stage == a.stages)
                         stage = 0;
-                        phase ^= 1u;
-                    }
                 }
             }
         }
@@ -1983,18 +2108,25 @@ static cudaError_t launch_mn_t(const CUtensorMap &tm_a, const CUtensorMap &tm_b,
                                          static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(k_gemm_mn<kBS, kEpi>, kBS ? kThreadsScaled : kThreads, grid, smem, stream, args, tm_a, tm_b,
+    return launch_pdl(k_gemm_mn<kBS, kEpi>, kBS ? kThreadsTmemScaled : kThreads, grid, smem, stream, args, tm_a, tm_b,
                       tm_sa, tm_sb);
 }
 
 // Output scales or a fused epilogue select the kernels' full store path.
 static bool wants_epi(const GemmArgs &args) { return args.epi || args.scale_a || args.scale_b; }
 
+// Two MMA issuers need an even number of stages (>= 2): each stage then
+// always feeds the same issuer, so no parity wait on it can skip a phase.
+static bool dual_ok(const GemmArgs &args)
+{
+    return !args.dual_mma || (args.sf_k && args.stages >= 2 && (args.stages & 1) == 0);
+}
+
 cudaError_t launch_gemm_mn(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const CUtensorMap &tm_sa,
                            const CUtensorMap &tm_sb, const GemmArgs &args, int grid, size_t smem,
                            cudaStream_t stream)
 {
-    if (smem < smem_bytes_for(args.stages, args.stage_bytes, args.groups))
+    if (smem < smem_bytes_for(args.stages, args.stage_bytes, args.groups) || !dual_ok(args))
         return cudaErrorInvalidValue;
     const bool epi = wants_epi(args);
     if (args.sf_k)
@@ -2022,7 +2154,7 @@ cudaError_t launch_gemm_mn2(const CUtensorMap &tm_a, const CUtensorMap &tm_b, co
                             cudaStream_t stream)
 {
     if (smem < smem_bytes_for(args.stages, args.stage_bytes, args.groups) || (grid & 1) || args.groups != 1 ||
-        args.masked_m != nullptr || args.group_offsets != nullptr)
+        args.masked_m != nullptr || args.group_offsets != nullptr || args.dual_mma)
         return cudaErrorInvalidValue;
     const bool epi = wants_epi(args);
     if (args.sf_k)
@@ -2041,7 +2173,7 @@ static cudaError_t launch_swap_t(const CUtensorMap &tm_w, const CUtensorMap &tm_
                                          static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(k_gemm_swap<kBS, kEpi>, kBS ? kThreadsSwapScaled : kThreads, grid, smem, stream, args, tm_w, tm_t,
+    return launch_pdl(k_gemm_swap<kBS, kEpi>, kBS ? kThreadsTmemScaled : kThreads, grid, smem, stream, args, tm_w, tm_t,
                       tm_sw, tm_st);
 }
 
@@ -2049,7 +2181,7 @@ cudaError_t launch_gemm_swap(const CUtensorMap &tm_w, const CUtensorMap &tm_t, c
                              const CUtensorMap &tm_st, const GemmArgs &args, int grid, size_t smem,
                              cudaStream_t stream)
 {
-    if (smem < smem_bytes_for(args.stages, args.stage_bytes, args.groups))
+    if (smem < smem_bytes_for(args.stages, args.stage_bytes, args.groups) || !dual_ok(args))
         return cudaErrorInvalidValue;
     const bool epi = wants_epi(args);
     if (args.sf_k)

@@ -13,9 +13,9 @@ constexpr int kTileM = 128;          // MMA M: rows of the operand on the M side
 constexpr int kMaxStages = 16;
 constexpr int kMaxGroups = 1024;
 constexpr int kThreads = 192;        // warp 0 loader, warp 1 MMA issuer, warps 2-5 epilogue
-constexpr int kThreadsScaled = 224;  // single-SM and SM-pair kernels: + warp 6, block-scale staging
-constexpr int kThreadsSwapScaled = 352;  // block-scaled SwapAB: + warp 6, second MMA issuer, and
-                                         // warps 7-10, block-scale staging into TMEM
+constexpr int kThreadsScaled = 224;  // SM-pair kernel with block scales: + warp 6, scale staging
+constexpr int kThreadsTmemScaled = 352;  // SwapAB and single-SM kernels with block scales: + warp 6,
+                                         // second MMA issuer, and warps 7-10, scale sets into TMEM
 constexpr int kMaxSfSets = 4;        // TMEM block-scale sets in flight
 constexpr int kTmemCols = 512;       // two accumulators of up to 256 columns
 constexpr int kAccStride = 256;
@@ -74,8 +74,10 @@ struct GemmArgs {
     int32_t sf_off;            // byte offset of the scale area inside a stage
     int32_t sf_col0;           // first TMEM column of the block-scale sets
     int32_t sf_sets;           // TMEM block-scale sets (2..kMaxSfSets)
-    int32_t dual_mma;          // block-scaled SwapAB: two MMA-issuing threads, each with its own
-                               // accumulators (4 x tile_n TMEM columns), alternating K blocks
+    int32_t dual_mma;          // block-scaled SwapAB / single-SM kernels: two MMA-issuing threads,
+                               // each with its own accumulators, alternating K blocks
+    int32_t acc_bufs;          // single-SM kernel with two issuers: accumulator buffers per issuer
+                               // (2, or 1 when four tile_n-wide accumulators do not fit in TMEM)
     // Fused epilogue (epi != 0): out = round(act(alpha * v + beta * c_in + bias)),
     // v the (scaled) product; c_in BF16 shaped like D or nullptr; bias FP32
     // [groups][n] or nullptr; act ReLU when relu != 0; round_mode 0 nearest

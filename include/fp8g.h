@@ -98,14 +98,19 @@ typedef enum {
 #define FP8G_NO_PDL 0x400u
 /*   FP8G_PAIR_TILES   dense problems with more than 128 token rows: always use
  *                     SM-pair tiles (the automatic choice skips them for
- *                     block-scaled problems with short K or 32-element
- *                     groups, where single-SM tiles measured faster). */
+ *                     block-scaled problems, where single-SM tiles measured
+ *                     faster). */
 #define FP8G_PAIR_TILES 0x4000u
-/*   FP8G_ONE_MMA_ISSUER  block-scaled SwapAB kernel: one thread issues every
- *                     MMA (default: two threads alternate K blocks, each
- *                     into its own accumulator, when TMEM holds four
- *                     accumulators of the token chunk, i.e. up to 112 tokens) */
+/*   FP8G_ONE_MMA_ISSUER  block-scaled SwapAB and single-SM tile kernels: one
+ *                     thread issues every MMA (default: two threads alternate
+ *                     K blocks, each into its own accumulator, when each has
+ *                     two accumulator buffers in TMEM -- token chunks or
+ *                     tiles up to 112 wide -- and, single-SM tiles with
+ *                     32-element groups, also with one buffer each) */
 #define FP8G_ONE_MMA_ISSUER 0x8000u
+/*   FP8G_TWO_MMA_ISSUERS  block-scaled single-SM tiles: two issuers even when
+ *                     each has only one accumulator buffer */
+#define FP8G_TWO_MMA_ISSUERS 0x2000u
 /*   FP8G_STAGES(n)    at most n shared-memory pipeline stages (1..15)       */
 #define FP8G_STAGES(n) ((((uint32_t)(n)) & 15u) << 20)
 /*   FP8G_SHARE_SM     SwapAB kernel with <= 128 tokens per chunk: half the

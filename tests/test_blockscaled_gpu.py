@@ -75,6 +75,7 @@ def check_dense_bs(M, N, K, gran, flags, seed, fa=E4, fb=E4, pad=16):
 # ---- token tiles: SM pairs and single SMs (tokens on M) -------------------------------
 
 DENSE_KERNELS = {"pair": OFF | fp8g.PAIR_TILES, "single_sm": OFF | fp8g.SINGLE_SM_TILES,
+                 "single_sm_two_issuers": OFF | fp8g.SINGLE_SM_TILES | fp8g.TWO_MMA_ISSUERS,
                  "pair_stream_k": OFF | fp8g.PAIR_TILES | fp8g.STREAM_K, "auto": OFF}
 
 
@@ -93,6 +94,15 @@ def test_dense_every_tile_width(tn, kernel):
 
 
 @pytest.mark.parametrize("gran", [128, 32])
+@pytest.mark.parametrize("tn", [1, 2, 3])
+def test_single_sm_narrow_tiles_two_issuers(tn, gran):
+    """Tiles of 32..96 columns: two MMA issuers with two accumulator buffers each."""
+    check_dense_bs(300, 416, 1664, gran, OFF | fp8g.SINGLE_SM_TILES | fp8g.TILE_N(tn), seed=527 + tn + gran)
+    check_dense_bs(300, 416, 1664, gran, OFF | fp8g.SINGLE_SM_TILES | fp8g.TILE_N(tn) | fp8g.ONE_MMA_ISSUER,
+                   seed=527 + tn + gran)
+
+
+@pytest.mark.parametrize("gran", [128, 32])
 def test_dense_pair_many_tiles_and_k_blocks(gran):
     """Several whole waves of SM-pair tiles and a K of 33 blocks (the scale
     ring wraps many times, 128-element groups span K-block quadruples)."""
@@ -106,7 +116,16 @@ def test_dense_mixed_formats(fa, fb):
 
 @pytest.mark.parametrize("kernel", ["pair", "single_sm"])
 def test_dense_one_stage_pipeline(kernel):
+    # one stage: a single MMA issuer (two need an even stage count)
     check_dense_bs(256, 384, 1024, 128, DENSE_KERNELS[kernel] | fp8g.DEBUG_ONE_STAGE, seed=535)
+
+
+@pytest.mark.parametrize("flags", [OFF | fp8g.SINGLE_SM_TILES, ON])
+@pytest.mark.parametrize("stages", [2, 3, 5])
+def test_short_pipelines(stages, flags):
+    # stage caps: two issuers run on the largest even count below the cap
+    M = 40 if flags == ON else 256
+    check_dense_bs(M, 384, 1536, 128, flags | fp8g.STAGES(stages), seed=536 + stages)
 
 
 def test_exact_data_is_bit_exact():
