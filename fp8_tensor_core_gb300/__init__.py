@@ -27,8 +27,8 @@ STREAM_K = 0x800      # SM-pair dense kernel: stream-K split of the last partial
 SINGLE_SM_TILES = 0x200   # dense non-swapped: one SM per 128-row tile instead of SM pairs
 NO_PDL = 0x400            # launch without programmatic dependent launch
 PAIR_TILES = 0x4000       # dense: always SM-pair tiles when M > 128
-ONE_MMA_ISSUER = 0x8000   # block-scaled SwapAB / single-SM tiles: one MMA-issuing thread
-TWO_MMA_ISSUERS = 0x2000  # block-scaled single-SM tiles: two issuers even with one buffer each
+ONE_MMA_ISSUER = 0x8000   # block-scaled kernels: one MMA-issuing thread
+TWO_MMA_ISSUERS = 0x2000  # block-scaled tile kernels: two issuers even with one buffer each
 SHARE_SM = 0x1000         # SwapAB kernel: half an SM per CTA (next launch overlaps the drain)
 
 

@@ -560,6 +560,19 @@ int launch(const Problem &p, cudaStream_t stream)
             args.stage_bytes = kTileM * kBlockK + (tile_n / 2) * kBlockK;
         }
         args.stages = pick_stages(info, args.stage_bytes, static_cast<int>(p.G), p.flags);
+        if (p.sf_k && !(p.flags & FP8G_ONE_MMA_ISSUER) && args.stages >= 2) {
+            // Two MMA issuers in the even CTA, as for single-SM tiles.
+            const int set_cols = sf_set_cols(tile_n);
+            const int sets2 = std::min(kMaxSfSets, (kTmemCols - 4 * tile_n) / set_cols);
+            if (sets2 >= 2 || ((p.flags & FP8G_TWO_MMA_ISSUERS) && args.sf_sets >= 2)) {
+                args.dual_mma = 1;
+                args.acc_bufs = sets2 >= 2 ? 2 : 1;
+                args.sf_col0 = args.acc_bufs * 2 * tile_n;
+                if (sets2 >= 2)
+                    args.sf_sets = sets2;
+                args.stages &= ~1;
+            }
+        }
         const int64_t band = (48ll << 20) / (2 * kTileM * p.K);
         args.raster_band = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(band, m_tiles2)));
         if (!make_map(&tm0, p.A, p.K, p.rows_a, 1, kTileM) ||

@@ -61,8 +61,7 @@ struct alignas(16) SmemCtl {
     uint64_t tempty[2];
     uint64_t drain;
     uint64_t pair_exit;   // CTA-pair kernel: the peer's "done" arrival
-    uint64_t sfready[kMaxStages];   // block scales of stage s staged for tcgen05.cp
-    uint64_t sffull[kMaxStages];    // SM-pair kernel: this CTA's scale bytes of stage s landed
+    uint64_t sffull[kMaxStages];    // this CTA's scale bytes of stage s landed
     uint64_t sffree[kMaxSfSets];    // TMEM scale set no longer read by any MMA
     uint64_t sfset_ready[kMaxSfSets];   // SwapAB: scale set written into TMEM by the staging warps
     uint64_t drain2;                // SwapAB: completion of the second issuer's tensor-core work
@@ -78,14 +77,17 @@ static_assert(sizeof(SmemCtl) <= kCtlFixedBytes, "control block too large");
 
 // Warp-uniform bounded wait on an mbarrier phase.  Returns false when the
 // block is aborting (another role timed out) or this wait ran out.
+// kCluster: acquire at cluster scope (the phase is completed by the peer CTA).
+template <bool kCluster = false>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, SmemCtl &ctl,
                                           uint64_t timeout_ns, int role, int detail)
 {
-    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity)))
+    auto test = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    if (__all_sync(0xffffffffu, test()))
         return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity)))
+        if (__all_sync(0xffffffffu, test()))
             return true;
         if ((it & 15u) == 0) {
             int stop = 0;
@@ -368,93 +370,6 @@ __device__ __forceinline__ bool sf_load_at(int kb, int kb_first, int sf_k)
 }
 __device__ __forceinline__ int sf_first_group(int kb, int sf_k) { return sf_k == 1 ? (kb & ~3) : 4 * kb; }
 
-// Scale-staging warp, all lanes, once the stage's full barrier has passed:
-// rearrange the raw bytes into tcgen05.cp sources -- per 128 rows, 16-byte
-// row r % 32, 32-bit word r / 32 holding the row's four K-group bytes.
-__device__ __forceinline__ void sf_transpose(uint8_t *stage, const GemmArgs &a, int box_b)
-{
-    const int lane = threadIdx.x & 31;
-    const uint8_t *raw_a = stage + a.sf_off;            // [4][128]
-    const uint8_t *raw_b = raw_a + 4 * kTileM;          // [4][box_b]
-    uint8_t *src = stage + a.sf_off + 4 * (kTileM + box_b);
-    auto word = [](const uint8_t *raw, int box, int r) {
-        return static_cast<uint32_t>(raw[r]) | (static_cast<uint32_t>(raw[box + r]) << 8) |
-               (static_cast<uint32_t>(raw[2 * box + r]) << 16) | (static_cast<uint32_t>(raw[3 * box + r]) << 24);
-    };
-    *reinterpret_cast<uint4 *>(src + 16 * lane) = make_uint4(
-        word(raw_a, kTileM, lane), word(raw_a, kTileM, 32 + lane), word(raw_a, kTileM, 64 + lane),
-        word(raw_a, kTileM, 96 + lane));
-    const int nch = (box_b + 127) >> 7;
-    for (int h = 0; h < nch; ++h) {
-        uint32_t v[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int r = 128 * h + 32 * j + lane;
-            v[j] = r < box_b ? word(raw_b, box_b, r) : 0u;
-        }
-        *reinterpret_cast<uint4 *>(src + 512 * (1 + h) + 16 * lane) = make_uint4(v[0], v[1], v[2], v[3]);
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-}
-
-// MMA warp, all lanes, at a K block that carries scales: wait until the
-// staging warp has built this stage's copy sources, retire the previous TMEM
-// scale set (its last MMA is already issued), take the next one once its
-// previous use has completed, and (lane 0) copy the sources into it: side A
-// at the set's first column, side B 4 columns on (4 more per 128 rows).  The
-// copies are ordered before the MMAs lane 0 issues next.  Returns false when
-// a wait gave up.
-struct SfState {
-    int j;              // scale loads consumed so far - 1
-    uint32_t ready_par; // parity bit per stage of sfready
-};
-
-// kPair: the SM-pair kernel's even CTA, whose commits and copies act on
-// both CTAs (each CTA's own copy sources, at the same offsets).
-template <bool kPair = false>
-__device__ __forceinline__ bool sf_take(SmemCtl &ctl, const GemmArgs &a, SfState &st, int stage,
-                                        const uint8_t *stage_ptr, int box_b, uint32_t sets_tmem, int set_cols,
-                                        uint32_t &set_tmem)
-{
-    const int lane = threadIdx.x & 31;
-    if (!warp_wait(smem_addr(&ctl.sfready[stage]), (st.ready_par >> stage) & 1u, ctl, a.timeout_ns, kRoleMma,
-                   300 + stage))
-        return false;
-    st.ready_par ^= 1u << stage;
-    const int R = a.sf_sets;
-    if (st.j >= 0 && lane == 0) {
-        if constexpr (kPair)
-            mma_commit_pair(smem_addr(&ctl.sffree[st.j % R]));
-        else
-            mma_commit(smem_addr(&ctl.sffree[st.j % R]));
-    }
-    __syncwarp();
-    ++st.j;
-    const int set = st.j % R;
-    if (st.j >= R &&
-        !warp_wait(smem_addr(&ctl.sffree[set]), static_cast<uint32_t>((st.j / R - 1) & 1), ctl, a.timeout_ns,
-                   kRoleMma, 400 + set))
-        return false;
-    tc_fence_after();
-    set_tmem = sets_tmem + static_cast<uint32_t>(set * set_cols);
-    if (lane == 0) {
-        const uint8_t *src = stage_ptr + a.sf_off + 4 * (kTileM + box_b);
-        const int nch = (box_b + 127) >> 7;
-        if constexpr (kPair) {
-            tmem_cp_32x128b_warpx4_pair(set_tmem, smem_desc_rows16(smem_addr(src)));
-            for (int h = 0; h < nch; ++h)
-                tmem_cp_32x128b_warpx4_pair(set_tmem + 4u + 4u * h,
-                                            smem_desc_rows16(smem_addr(src + 512 * (1 + h))));
-        } else {
-            tmem_cp_32x128b_warpx4(set_tmem, smem_desc_rows16(smem_addr(src)));
-            for (int h = 0; h < nch; ++h)
-                tmem_cp_32x128b_warpx4(set_tmem + 4u + 4u * h, smem_desc_rows16(smem_addr(src + 512 * (1 + h))));
-        }
-    }
-    return true;
-}
-
 // ---- block scales written into TMEM by staging warps ---------------------------------
 // (SwapAB and single-SM kernels.)  A copy of scale factors into TMEM issued
 // by the MMA thread costs it ~100 ns and a block-scaled MMA ~95 ns, so the
@@ -467,7 +382,9 @@ __device__ __forceinline__ bool sf_take(SmemCtl &ctl, const GemmArgs &a, SfState
 // K group g of the load), wait until every issuer has retired the set's
 // previous contents, write the set into this warp's lane quadrant -- row r
 // of side A at lane r % 32, column r / 32; side B from column 4 likewise --
-// and arrive.  box_b <= 256.  Returns false when a wait gave up.
+// and arrive (kPair: on the even CTA's barrier, which counts both CTAs'
+// staging warps).  box_b <= 256.  Returns false when a wait gave up.
+template <bool kPair = false>
 __device__ __forceinline__ bool sf_stage_tmem(SmemCtl &ctl, const GemmArgs &a, const uint8_t *stage_ptr, int box_b,
                                               int j, uint32_t sets_q, int set_cols)
 {
@@ -500,25 +417,35 @@ __device__ __forceinline__ bool sf_stage_tmem(SmemCtl &ctl, const GemmArgs &a, c
         tmem_st_32x32b_x4(t + 8u, wb[4], wb[5], wb[6], wb[7]);
     tc_fence_before();
     __syncwarp();
-    if (lane == 0)
-        mbar_arrive(smem_addr(&ctl.sfset_ready[set]));
+    if (lane == 0) {
+        if constexpr (kPair)
+            mbar_arrive_cluster(mapa_shared(smem_addr(&ctl.sfset_ready[set]), 0));
+        else
+            mbar_arrive(smem_addr(&ctl.sfset_ready[set]));
+    }
     return true;
 }
 
 // MMA issuer warp, all lanes, at scale load j + 1: retire set j (a commit
-// that arrives once this thread's MMAs so far are done), wait for set j + 1
-// and point set_tmem at it.  Returns false when the wait gave up.
+// that arrives once this thread's MMAs so far are done; kPair: in both
+// CTAs), wait for set j + 1 and point set_tmem at it.  Returns false when
+// the wait gave up.
+template <bool kPair = false>
 __device__ __forceinline__ bool sf_next_set(SmemCtl &ctl, const GemmArgs &a, int &j, uint32_t sets_tmem,
                                             int set_cols, uint32_t &set_tmem)
 {
     const int R = a.sf_sets;
-    if (j >= 0 && (threadIdx.x & 31) == 0)
-        mma_commit(smem_addr(&ctl.sffree[j % R]));
+    if (j >= 0 && (threadIdx.x & 31) == 0) {
+        if constexpr (kPair)
+            mma_commit_pair_mc(smem_addr(&ctl.sffree[j % R]), 0x3);
+        else
+            mma_commit(smem_addr(&ctl.sffree[j % R]));
+    }
     __syncwarp();
     ++j;
     const int set = j % R;
-    if (!warp_wait(smem_addr(&ctl.sfset_ready[set]), static_cast<uint32_t>((j / R) & 1), ctl, a.timeout_ns, kRoleMma,
-                   300 + set))
+    if (!warp_wait<kPair>(smem_addr(&ctl.sfset_ready[set]), static_cast<uint32_t>((j / R) & 1), ctl, a.timeout_ns,
+                          kRoleMma, 300 + set))
         return false;
     tc_fence_after();
     set_tmem = sets_tmem + static_cast<uint32_t>(set * set_cols);
@@ -638,10 +565,8 @@ __device__ __forceinline__ void init_barriers(SmemCtl &ctl, int stages, uint32_t
     }
     mbar_init(smem_addr(&ctl.drain), 1);
     mbar_init(smem_addr(&ctl.drain2), 1);
-    for (int s = 0; s < stages; ++s) {
-        mbar_init(smem_addr(&ctl.sfready[s]), 1);
+    for (int s = 0; s < stages; ++s)
         mbar_init(smem_addr(&ctl.sffull[s]), 1);
-    }
     for (int i = 0; i < kMaxSfSets; ++i) {
         mbar_init(smem_addr(&ctl.sffree[i]), issuers);
         mbar_init(smem_addr(&ctl.sfset_ready[i]), 4);   // one arrival per staging warp
@@ -1075,7 +1000,7 @@ struct PairSeg {
 };
 
 template <bool kBS, bool kEpi>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsScaled, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemScaled : kThreadsScaled, 1)
     k_gemm_mn2(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                const __grid_constant__ CUtensorMap tm_sa, const __grid_constant__ CUtensorMap tm_sb,
                const GemmArgs a)
@@ -1101,6 +1026,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsScaled, 1)
     // tile_n columns apart, followed by the scale sets.
     const uint32_t sf_bytes = 4u * static_cast<uint32_t>(kTileM + a.tile_n);
     const int acc_stride = kBS ? a.tile_n : kAccStride;
+    // Two MMA issuers in the even CTA (warps 1 and 6, alternate K blocks,
+    // one accumulator each; one buffer each when four do not fit in TMEM).
+    const int acc_step = (kBS && a.dual_mma) ? 2 : 1;
+    const int n_bufs = (kBS && a.dual_mma && a.acc_bufs == 1) ? 1 : 2;
     const int set_cols = sf_set_cols(a.tile_n);
     const int cid = blockIdx.x >> 1;
     const int ncl = gridDim.x >> 1;
@@ -1116,18 +1045,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsScaled, 1)
             mbar_init(smem_addr(&ctl.empty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_addr(&ctl.tfull[b]), 1);
+            mbar_init(smem_addr(&ctl.tfull[b]), static_cast<uint32_t>(acc_step));
             mbar_init(smem_addr(&ctl.tempty[b]), 2 * 4);
         }
         mbar_init(smem_addr(&ctl.drain), 1);
+        mbar_init(smem_addr(&ctl.drain2), 1);
         mbar_init(smem_addr(&ctl.pair_exit), 1);
         if constexpr (kBS) {
-            for (int s = 0; s < a.stages; ++s) {
+            for (int s = 0; s < a.stages; ++s)
                 mbar_init(smem_addr(&ctl.sffull[s]), 1);
-                mbar_init(smem_addr(&ctl.sfready[s]), 2);   // both CTAs' staging warps
+            for (int i = 0; i < kMaxSfSets; ++i) {
+                mbar_init(smem_addr(&ctl.sffree[i]), static_cast<uint32_t>(acc_step));
+                mbar_init(smem_addr(&ctl.sfset_ready[i]), 2 * 4);   // both CTAs' staging warps (even CTA's copy)
             }
-            for (int i = 0; i < kMaxSfSets; ++i)
-                mbar_init(smem_addr(&ctl.sffree[i]), 1);
         }
         ctl.abort = 0;
         fence_mbar_init();
@@ -1275,14 +1205,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsScaled, 1)
                 warp_wait_drain(smem_addr(&ctl.full[s]), par, a.timeout_ns);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 && !kBS) {
         // ----------------------------- MMA issuer -----------------------------
         if (leader) {
             const uint32_t idesc = make_idesc(a.a_fmt, a.b_fmt, 2 * kTileM, a.tile_n);
-            const uint32_t idesc_bs = make_idesc_bs(a.a_fmt, a.b_fmt, 2 * kTileM, a.tile_n, 0);
-            const uint32_t sets_tmem = tmem_base + static_cast<uint32_t>(a.sf_col0);
-            SfState sfs{-1, 0u};
-            uint32_t set_tmem = sets_tmem;
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -1305,27 +1231,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsScaled, 1)
                         break;
                     }
                     tc_fence_after();
-                    if constexpr (kBS) {
-                        const uint8_t *sp = sm.stages + static_cast<size_t>(stage) * a.stage_bytes;
-                        if (sf_load_at(kb, x.kb0, a.sf_k) &&
-                            !sf_take<true>(ctl, a, sfs, stage, sp, a.tile_n, sets_tmem, set_cols, set_tmem)) {
-                            aborted = true;
-                            break;
-                        }
-                        if (lane == 0) {
-                            const uint64_t adesc = smem_desc_k_sw128(smem_addr(sp));
-                            const uint64_t bdesc = smem_desc_k_sw128(smem_addr(sp) + a_bytes);
-#pragma unroll
-                            for (int k = 0; k < kBlockK / 32; ++k) {
-                                const uint32_t id =
-                                    a.sf_k == 1 ? static_cast<uint32_t>(kb & 3) : static_cast<uint32_t>(k);
-                                mma_f8f6f4_bs_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k,
-                                                   idesc_bs | (id << 4) | (id << 29), set_tmem, set_tmem + 4u,
-                                                   (kb != x.kb0 || k != 0) ? 1u : 0u);
-                            }
-                            mma_commit_pair_mc(smem_addr(&ctl.empty[stage]), 0x3);
-                        }
-                    } else if (lane == 0) {
+                    if (lane == 0) {
                         const uint32_t sa = smem_addr(sm.stages + static_cast<size_t>(stage) * a.stage_bytes);
                         const uint64_t adesc = smem_desc_k_sw128(sa);
                         const uint64_t bdesc = smem_desc_k_sw128(sa + a_bytes);
@@ -1370,45 +1276,139 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsScaled, 1)
                 warp_wait_drain(smem_addr(&ctl.drain), 0, a.timeout_ns);
             }
         }
-    } else if (warp == 6) {
-        // ------------------------- block-scale staging -------------------------
-        // Each CTA waits for its own scale bytes of a stage (sffull, one
-        // completion per scale load of that stage), builds the copy sources
-        // and tells the even CTA (sfready counts both CTAs).
-        if constexpr (kBS) {
+    } else if (kBS && (warp == 1 || (warp == 6 && a.dual_mma))) {
+        // ---------------------- MMA issuers, block-scaled ----------------------
+        // Even CTA only: one or two issuing threads (warps 1 and 6).  With
+        // two, issuer i takes the K blocks whose running index in this pair
+        // is i mod 2, into its own accumulator; the epilogues add the two.
+        // Scale sets come from both CTAs' staging warps; a set is retired in
+        // both CTAs by a multicast commit.
+        if (leader) {
+            const int me = warp == 1 ? 0 : 1;
+            const uint32_t idesc_bs = make_idesc_bs(a.a_fmt, a.b_fmt, 2 * kTileM, a.tile_n, 0);
+            const uint32_t sets_tmem = tmem_base + static_cast<uint32_t>(a.sf_col0);
+            uint32_t set_tmem = sets_tmem;
+            int j = -1;   // scale loads passed
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t sf_par = 0;   // parity bit per stage of sffull
-            const uint32_t ready_leader0 = mapa_shared(smem_addr(&ctl.sfready[0]), 0);
+            uint32_t par = 0;   // running K-block index mod 2
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool issued_any = false;
             Walker wk = make_walker();
             PairSeg x;
             while (!aborted && next_seg(wk, x)) {
+                if (!warp_wait(smem_addr(&ctl.tempty[acc]), acc_phase ^ 1u, ctl, a.timeout_ns, kRoleMma,
+                               100 + acc)) {
+                    aborted = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>((acc * acc_step + me) * acc_stride);
+                bool first = true;
                 for (int kb = x.kb0; kb < x.kb1; ++kb) {
-                    if (sf_load_at(kb, x.kb0, a.sf_k)) {
-                        if (!warp_wait(smem_addr(&ctl.sffull[stage]), (sf_par >> stage) & 1u, ctl, a.timeout_ns,
-                                       kRoleScales, stage)) {
+                    if (sf_load_at(kb, x.kb0, a.sf_k) &&
+                        !sf_next_set<true>(ctl, a, j, sets_tmem, set_cols, set_tmem)) {
+                        aborted = true;
+                        break;
+                    }
+                    if (acc_step == 1 || static_cast<int>(par) == me) {
+                        if (!warp_wait(smem_addr(&ctl.full[stage]), phase, ctl, a.timeout_ns, kRoleMma, stage)) {
                             aborted = true;
                             break;
                         }
-                        sf_par ^= 1u << stage;
-                        sf_transpose(sm.stages + static_cast<size_t>(stage) * a.stage_bytes, a, a.tile_n);
-                        if (lane == 0)
-                            mbar_arrive_cluster(ready_leader0 + static_cast<uint32_t>(stage) * 8u);
+                        tc_fence_after();
+                        if (lane == 0) {
+                            const uint32_t sa = smem_addr(sm.stages + static_cast<size_t>(stage) * a.stage_bytes);
+                            const uint64_t adesc = smem_desc_k_sw128(sa);
+                            const uint64_t bdesc = smem_desc_k_sw128(sa + a_bytes);
+#pragma unroll
+                            for (int k = 0; k < kBlockK / 32; ++k) {
+                                const uint32_t id =
+                                    a.sf_k == 1 ? static_cast<uint32_t>(kb & 3) : static_cast<uint32_t>(k);
+                                mma_f8f6f4_bs_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k,
+                                                   idesc_bs | (id << 4) | (id << 29), set_tmem, set_tmem + 4u,
+                                                   (!first || k != 0) ? 1u : 0u);
+                            }
+                            mma_commit_pair_mc(smem_addr(&ctl.empty[stage]), 0x3);
+                        }
+                        __syncwarp();
+                        first = false;
+                        issued_any = true;
                     }
+                    par ^= 1u;
                     if (++stage == a.stages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
+                if (aborted)
+                    break;
+                if (lane == 0)
+                    mma_commit_pair_mc(smem_addr(&ctl.tfull[acc]), 0x3);
+                __syncwarp();
+                if (++acc == n_bufs) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
             }
-            (void)phase;
+            // Issuer 0: both CTAs' epilogues must be done with every
+            // accumulator before TMEM goes.
+            for (int i = 0; i < n_bufs && !aborted && me == 0; ++i) {
+                if (!warp_wait(smem_addr(&ctl.tempty[acc]), acc_phase ^ 1u, ctl, a.timeout_ns, kRoleMma,
+                               100 + acc))
+                    aborted = true;
+                if (++acc == n_bufs) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            if (issued_any) {
+                uint64_t *db = me == 0 ? &ctl.drain : &ctl.drain2;
+                if (lane == 0)
+                    mma_commit_pair(smem_addr(db));
+                __syncwarp();
+                warp_wait_drain(smem_addr(db), 0, a.timeout_ns);
+            }
         }
-    } else {
+    } else if (kBS && warp >= 7) {
+        // --------------------- block-scale staging into TMEM ---------------------
+        // Warps 7-10 of each CTA: its own 128 rows' A-side scales and the
+        // whole tile's B-side scales (each CTA's tensor core scales all N
+        // columns), written into its own TMEM; arrivals go to the even CTA.
+        if constexpr (kBS) {
+            const uint32_t sets_q = tmem_base + static_cast<uint32_t>(a.sf_col0) +
+                                    (static_cast<uint32_t>((warp & 3) * 32) << 16);
+            int stage = 0;
+            uint32_t sf_par = 0;   // per stage: parity of the next scale fill to wait for
+            int j = -1;
+            Walker wk = make_walker();
+            PairSeg x;
+            while (!aborted && next_seg(wk, x)) {
+                for (int kb = x.kb0; kb < x.kb1; ++kb) {
+                    if (sf_load_at(kb, x.kb0, a.sf_k)) {
+                        ++j;
+                        if (!warp_wait(smem_addr(&ctl.sffull[stage]), (sf_par >> stage) & 1u, ctl, a.timeout_ns,
+                                       kRoleScales, stage) ||
+                            !sf_stage_tmem<true>(ctl, a, sm.stages + static_cast<size_t>(stage) * a.stage_bytes,
+                                                 a.tile_n, j, sets_q, set_cols)) {
+                            aborted = true;
+                            break;
+                        }
+                        sf_par ^= 1u << stage;
+                    }
+                    if (++stage == a.stages)
+                        stage = 0;
+                }
+            }
+        }
+    } else if (warp >= 2 && warp <= 5) {
         // ------------------------------ epilogue ------------------------------
         const int q = warp & 3;
         const int row = q * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
+        uint32_t par = 0;   // running K-block index mod 2 (which issuer took a segment's first K block)
         __nv_bfloat16 *dout = static_cast<__nv_bfloat16 *>(a.d);
         // Stream-K partial tiles: slot (CTA, kind) of [tile_n/4 column groups]
         // [128 rows][4 columns] FP32; a warp access covers 512 contiguous bytes.
@@ -1427,7 +1427,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsScaled, 1)
             const bool row_ok = grow < a.rows_a;
             __nv_bfloat16 *drow = dout + static_cast<int64_t>(grow) * static_cast<int64_t>(a.n);
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                   static_cast<uint32_t>(acc * acc_stride);
+                                   static_cast<uint32_t>(acc * acc_step * acc_stride);
+            // With two issuers: the one that took the segment's first K block
+            // always has data, the other one if the segment has two or more.
+            const uint32_t t_first = t_row + par * static_cast<uint32_t>(acc_stride);
+            const uint32_t t_second = t_row + (par ^ 1u) * static_cast<uint32_t>(acc_stride);
+            const bool both = acc_step == 2 && x.kb1 - x.kb0 >= 2;
+            if (acc_step == 2)
+                par ^= static_cast<uint32_t>((x.kb1 - x.kb0) & 1);
+            // 32 accumulator columns of this thread's row, summed over issuers.
+            auto ld32 = [&](int c, uint32_t (&r)[32]) {
+                tmem_ld_32x32b_x32(t_first + static_cast<uint32_t>(c), r);
+                if constexpr (kBS) {
+                    if (both) {
+                        uint32_t r2[32];
+                        tmem_ld_32x32b_x32(t_second + static_cast<uint32_t>(c), r2);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
+                    }
+                }
+            };
             // Eight FP32 values (as bits) -> eight scaled BF16 at column col.
             const float rf = (kEpi && row_ok) ? row_factor(a, 0, grow) : 1.0f;
             auto store8 = [&](int col, const uint32_t *v) {
@@ -1437,7 +1457,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsScaled, 1)
             if (x.kb0 == 0 && x.kb1 == num_kb) {
                 for (int c = 0; c < a.tile_n; c += 32) {
                     uint32_t r[32];
-                    tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c), r);
+                    ld32(c, r);
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
                         store8(x.n0 + c + 8 * j, r + 8 * j);
@@ -1446,7 +1466,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsScaled, 1)
                 float4 *mine = slots + (static_cast<int64_t>(blockIdx.x) * 2 + x.kind) * part4;
                 for (int c = 0; c < a.tile_n; c += 32) {
                     uint32_t r[32];
-                    tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c), r);
+                    ld32(c, r);
 #pragma unroll
                     for (int v = 0; v < 8; ++v)
                         mine[(c / 4 + v) * kTileM + row] =
@@ -1524,7 +1544,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsScaled, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive_cluster(mapa_shared(smem_addr(&ctl.tempty[acc]), 0));
-            if (++acc == 2) {
+            if (++acc == n_bufs) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
@@ -2145,7 +2165,7 @@ static cudaError_t launch_mn2_t(const CUtensorMap &tm_a, const CUtensorMap &tm_b
                                          static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(k_gemm_mn2<kBS, kEpi>, kBS ? kThreadsScaled : kThreads, grid, smem, stream, args, tm_a, tm_b,
+    return launch_pdl(k_gemm_mn2<kBS, kEpi>, kBS ? kThreadsTmemScaled : kThreads, grid, smem, stream, args, tm_a, tm_b,
                       tm_sa, tm_sb);
 }
 
@@ -2154,7 +2174,7 @@ cudaError_t launch_gemm_mn2(const CUtensorMap &tm_a, const CUtensorMap &tm_b, co
                             cudaStream_t stream)
 {
     if (smem < smem_bytes_for(args.stages, args.stage_bytes, args.groups) || (grid & 1) || args.groups != 1 ||
-        args.masked_m != nullptr || args.group_offsets != nullptr || args.dual_mma)
+        args.masked_m != nullptr || args.group_offsets != nullptr || !dual_ok(args))
         return cudaErrorInvalidValue;
     const bool epi = wants_epi(args);
     if (args.sf_k)

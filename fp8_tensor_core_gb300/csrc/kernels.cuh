@@ -97,13 +97,9 @@ struct GemmArgs {
 
 // Block-scaled stage layout.  After the two operand tiles (MMA side A: 128
 // rows; side B: box_b rows) a stage holds the raw scale bytes as TMA writes
-// them ([4][128] then [4][box_b]: four K groups per row) and the tcgen05.cp
-// sources built from them (512 bytes per 128 rows).  A TMEM scale set has 4
-// columns for side A and 4 per 128 rows of side B.
-inline int sf_stage_bytes(int box_b)
-{
-    return 4 * (kTileM + box_b) + 512 * (1 + (box_b + 127) / 128);
-}
+// them ([4][128] then [4][box_b]: four K groups per row).  A TMEM scale set
+// has 4 columns for side A and 4 per 128 rows of side B.
+inline int sf_stage_bytes(int box_b) { return 4 * (kTileM + box_b); }
 __host__ __device__ inline int sf_set_cols(int box_b) { return 4 + 4 * ((box_b + 127) / 128); }
 
 // Shared-memory footprint of a launch (stages + control block + alignment).

@@ -58,6 +58,20 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok;
 }
 
+// The same with cluster-scope acquire: for a phase completed by arrivals
+// from the peer CTA (release.cluster), whose writes the waiter then uses.
+__device__ __forceinline__ uint32_t mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok;
+}
+
 // ---- TMA (bulk tensor copy global -> shared) ---------------------------------
 
 __device__ __forceinline__ void tma_prefetch_map(const void *map)
@@ -162,23 +176,6 @@ __device__ __forceinline__ void mma_f8f6f4_bs(uint32_t d_tmem, uint64_t a_desc, 
                  "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
                  "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
                  : "memory");
-}
-
-// Shared memory -> TMEM copy of 32 rows x 16 bytes, replicated into all four
-// lane quadrants: source row l lands in lanes l, 32 + l, 64 + l, 96 + l,
-// its four 32-bit words in columns taddr.col .. +3.  Ordered before the
-// tcgen05.mma instructions this thread issues after it.
-__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
-                 : "memory");
-}
-
-// Order this thread's generic-proxy shared-memory writes before later
-// async-proxy reads (TMA, tcgen05.cp) of the same bytes.
-__device__ __forceinline__ void fence_proxy_async_smem()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Arrive once on `bar` when every tcgen05 operation issued so far by this
@@ -345,13 +342,6 @@ __device__ __forceinline__ void mma_f8f6f4_bs_pair(uint32_t d_tmem, uint64_t a_d
                  : "memory");
 }
 
-// Pair form of the scale-factor copy (issued by the even CTA): each CTA's
-// shared memory at this offset goes to its own TMEM at taddr.
-__device__ __forceinline__ void tmem_cp_32x128b_warpx4_pair(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
 // Arrive once, on the mbarrier at this shared-memory offset in every CTA of
 // `cta_mask`, when the pair MMAs issued so far have completed.
 __device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t cta_mask)
@@ -388,18 +378,6 @@ __device__ __forceinline__ uint64_t smem_desc_k_sw128(uint32_t saddr)
     d |= static_cast<uint64_t>(1024u >> 4) << 32;
     d |= static_cast<uint64_t>(1u) << 46;
     d |= static_cast<uint64_t>(2u) << 61;
-    return d;
-}
-
-// Descriptor of a tcgen05.cp source: 32 rows of 16 bytes at a 16-byte
-// pitch (no swizzle; 8-row core matrices 128 bytes apart).
-__device__ __forceinline__ uint64_t smem_desc_rows16(uint32_t saddr)
-{
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>(128u >> 4) << 16;
-    d |= static_cast<uint64_t>(128u >> 4) << 32;
-    d |= static_cast<uint64_t>(1u) << 46;
     return d;
 }
 

@@ -101,15 +101,15 @@ typedef enum {
  *                     block-scaled problems, where single-SM tiles measured
  *                     faster). */
 #define FP8G_PAIR_TILES 0x4000u
-/*   FP8G_ONE_MMA_ISSUER  block-scaled SwapAB and single-SM tile kernels: one
+/*   FP8G_ONE_MMA_ISSUER  block-scaled SwapAB, single-SM and SM-pair kernels: one
  *                     thread issues every MMA (default: two threads alternate
  *                     K blocks, each into its own accumulator, when each has
  *                     two accumulator buffers in TMEM -- token chunks or
  *                     tiles up to 112 wide -- and, single-SM tiles with
  *                     32-element groups, also with one buffer each) */
 #define FP8G_ONE_MMA_ISSUER 0x8000u
-/*   FP8G_TWO_MMA_ISSUERS  block-scaled single-SM tiles: two issuers even when
- *                     each has only one accumulator buffer */
+/*   FP8G_TWO_MMA_ISSUERS  block-scaled single-SM and SM-pair tiles: two
+ *                     issuers even when each has only one accumulator buffer */
 #define FP8G_TWO_MMA_ISSUERS 0x2000u
 /*   FP8G_STAGES(n)    at most n shared-memory pipeline stages (1..15)       */
 #define FP8G_STAGES(n) ((((uint32_t)(n)) & 15u) << 20)

@@ -76,6 +76,8 @@ def check_dense_bs(M, N, K, gran, flags, seed, fa=E4, fb=E4, pad=16):
 
 DENSE_KERNELS = {"pair": OFF | fp8g.PAIR_TILES, "single_sm": OFF | fp8g.SINGLE_SM_TILES,
                  "single_sm_two_issuers": OFF | fp8g.SINGLE_SM_TILES | fp8g.TWO_MMA_ISSUERS,
+                 "pair_two_issuers": OFF | fp8g.PAIR_TILES | fp8g.TWO_MMA_ISSUERS,
+                 "pair_stream_k_two_issuers": OFF | fp8g.PAIR_TILES | fp8g.STREAM_K | fp8g.TWO_MMA_ISSUERS,
                  "pair_stream_k": OFF | fp8g.PAIR_TILES | fp8g.STREAM_K, "auto": OFF}
 
 
@@ -103,10 +105,17 @@ def test_single_sm_narrow_tiles_two_issuers(tn, gran):
 
 
 @pytest.mark.parametrize("gran", [128, 32])
-def test_dense_pair_many_tiles_and_k_blocks(gran):
+@pytest.mark.parametrize("issuers", [0, fp8g.TWO_MMA_ISSUERS, fp8g.ONE_MMA_ISSUER])
+def test_dense_pair_many_tiles_and_k_blocks(issuers, gran):
     """Several whole waves of SM-pair tiles and a K of 33 blocks (the scale
     ring wraps many times, 128-element groups span K-block quadruples)."""
-    check_dense_bs(1024, 1792, 4224, gran, OFF | fp8g.PAIR_TILES, seed=530 + gran)
+    check_dense_bs(1024, 1792, 4224, gran, OFF | fp8g.PAIR_TILES | issuers, seed=530 + gran)
+
+
+@pytest.mark.parametrize("tn", [2, 3])
+def test_pair_narrow_tiles_two_issuers(tn):
+    """SM-pair tiles of 64 / 96 columns: two issuers with two buffers each."""
+    check_dense_bs(640, 704, 1536, 128, OFF | fp8g.PAIR_TILES | fp8g.TILE_N(tn), seed=533 + tn)
 
 
 @pytest.mark.parametrize("fa,fb", [(E5, E4), (E4, E5), (E5, E5)])
