@@ -69,6 +69,22 @@ def fp8g_version() -> int:
     return int(_lib.load().fp8g_version())
 
 
+def fp8g_init(max_tiles: int = 0) -> None:
+    """Allocate the stream-K workspace of the current device at its largest
+    size (counters for max_tiles output tiles, 0 = the library default), so
+    that later calls allocate nothing -- e.g. before CUDA graph capture."""
+    rc = _lib.load().fp8g_init(int(max_tiles))
+    if rc != OK:
+        raise Fp8gError(rc, "fp8g_init")
+
+
+def fp8g_shutdown() -> None:
+    """Free the library's stream-K workspace on every device."""
+    rc = _lib.load().fp8g_shutdown()
+    if rc != OK:
+        raise Fp8gError(rc, "fp8g_shutdown")
+
+
 def fp8g_set_wait_timeout_ns(ns: int) -> int:
     return int(_lib.load().fp8g_set_wait_timeout_ns(int(ns)))
 

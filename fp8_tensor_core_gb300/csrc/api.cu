@@ -51,6 +51,7 @@ struct Workspace {
 };
 
 std::mutex g_mu;
+constexpr int64_t kDefaultInitTiles = 65536;   // fp8g_init(0): counters for this many stream-K tiles
 DeviceInfo g_dev[kMaxDevices];
 Workspace g_ws[kMaxDevices];
 
@@ -881,6 +882,52 @@ extern "C" int fp8g_get_device_status(int32_t *info, cudaStream_t stream)
             return FP8G_ERR_CUDA;
     }
     return FP8G_OK;
+}
+
+extern "C" int fp8g_init(int64_t max_tiles)
+{
+    int dev = 0;
+    DeviceInfo info;
+    int st = current_device(&dev, &info);
+    if (st != FP8G_OK)
+        return st;
+    if (max_tiles < 0 || max_tiles > kMaxDim)
+        return FP8G_ERR_INVALID_ARG;
+    const int64_t tiles = max_tiles ? max_tiles : kDefaultInitTiles;
+    // The largest partial-tile area any launch takes: two FP32 tiles of 128
+    // x 256 per CTA, one CTA per SM (SwapAB chunks and SM-pair tiles are at
+    // most 256 wide); one counter pair per (tile, epilogue warp).
+    const size_t ws_bytes = static_cast<size_t>(info.sms) * 2 * kTileM * 256 * sizeof(float);
+    float *ws = nullptr;
+    int32_t *counters = nullptr;
+    return ensure_workspace(dev, ws_bytes, swap_counter_bytes(tiles), &ws, &counters);
+}
+
+extern "C" int fp8g_shutdown(void)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    int prev = 0;
+    const bool have_prev = cudaGetDevice(&prev) == cudaSuccess;
+    int rc = FP8G_OK;
+    for (int d = 0; d < kMaxDevices; ++d) {
+        Workspace &w = g_ws[d];
+        if (!w.ws && !w.counters)
+            continue;
+        if (cudaSetDevice(d) != cudaSuccess) {
+            rc = FP8G_ERR_CUDA;
+            continue;
+        }
+        if (w.ws && cudaFree(w.ws) != cudaSuccess)
+            rc = FP8G_ERR_CUDA;
+        if (w.counters && cudaFree(w.counters) != cudaSuccess)
+            rc = FP8G_ERR_CUDA;
+        w = Workspace{};
+    }
+    if (have_prev)
+        cudaSetDevice(prev);
+    else
+        cudaGetLastError();
+    return rc;
 }
 
 extern "C" uint64_t fp8g_set_wait_timeout_ns(uint64_t ns)

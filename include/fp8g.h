@@ -332,6 +332,29 @@ int fp8_gemm_grouped_contiguous_ex(const void *A, const void *B, void *D,
 int fp8g_get_device_status(int32_t *info, cudaStream_t stream);
 
 /*
+ * fp8g_init -- allocate, on the current device, the library's stream-K
+ * workspace at its largest size: partial tiles for every SM (2 x SMs x
+ * 128 x 256 FP32, 39.8 MB on 152 SMs) and arrival counters for up to
+ * `max_tiles` output tiles of one launch (0 = 65536; 32 bytes a tile).  A
+ * stream-K launch is one with SwapAB (output tiles = groups x token chunks
+ * x ceil(N / 128)) or split SM-pair tiles (ceil(M / 256) x ceil(N / tile)).
+ * The calls allocate that workspace themselves on first need; after
+ * fp8g_init, calls whose launches fit allocate nothing, so they can be
+ * recorded into a CUDA graph from the start.  Idempotent; never shrinks.
+ * Returns FP8G_OK, FP8G_ERR_INVALID_ARG (max_tiles < 0 or > 2^31 - 1),
+ * FP8G_ERR_NO_DEVICE, FP8G_ERR_UNSUPPORTED (not sm_103) or FP8G_ERR_CUDA
+ * (allocation failed).
+ *
+ * fp8g_shutdown -- free the stream-K workspace on every device that has
+ * one (cudaFree waits for the device's work).  Call it with no library
+ * work being enqueued or captured on another thread; later calls allocate
+ * again on first need.  The fixed array of fp8_gemm_nt_noalloc is not
+ * affected.  Returns FP8G_OK or FP8G_ERR_CUDA.
+ */
+int fp8g_init(int64_t max_tiles);
+int fp8g_shutdown(void);
+
+/*
  * fp8g_set_wait_timeout_ns -- limit, in nanoseconds of device time, of every
  * barrier wait inside the kernels launched after this call (default 2e9).
  * A wait that runs out records FP8G_ERR_TIMEOUT, stops the block's pipeline,

@@ -357,3 +357,36 @@ def test_share_sm_mode_dense(M, N, K):
 def test_share_sm_mode_grouped():
     mm = [0, 5, 32, 17, 1, 64]
     grouped_case(len(mm), 64, 512, 1024, mm, ON | fp8g.SHARE_SM, 32, seed=171)
+
+
+def test_init_then_capture_stream_k_in_a_graph():
+    """After fp8g_init a stream-K call allocates nothing, so it can be the
+    first call recorded into a CUDA graph; fp8g_shutdown frees the workspace
+    and later calls allocate it again."""
+    fp8g.fp8g_shutdown()
+    fp8g.fp8g_init(0)
+    M, N, K = 24, 1536, 3072
+    A = synth.normal_fp8((M, K), 181, 0.0, 1.0, E4)
+    B = synth.normal_fp8((N, K), 182, 0.0, 1.0, E4)
+    Ad, Bd = dev(A), dev(B)
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fp8g.fp8_gemm_nt(Ad, Bd, D, a_dtype=E4, b_dtype=E4, flags=ON)
+    g.replay()
+    torch.cuda.synchronize()
+    assert fp8g.fp8g_get_device_status()[0] == fp8g.OK
+    ref, absdot = oracle.gemm_nt(A, B)
+    ok, rep = oracle.check_bf16(bits(D), ref, absdot)
+    assert ok, rep
+    fp8g.fp8g_shutdown()
+    D2 = fp8g.fp8_gemm_nt(Ad, Bd, a_dtype=E4, b_dtype=E4, flags=ON)
+    torch.cuda.synchronize()
+    ok, rep = oracle.check_bf16(bits(D2), ref, absdot)
+    assert ok, rep
+
+
+def test_init_argument_errors():
+    assert fp8g._lib.load().fp8g_init(-1) == fp8g.ERR_INVALID_ARG
+    assert fp8g._lib.load().fp8g_init(1 << 40) == fp8g.ERR_INVALID_ARG
