@@ -316,6 +316,78 @@ __device__ __forceinline__ void transpose8x8(uint32_t (&x)[8])
     }
 }
 
+// Tile epilogue stores.  A warp of the tile kernels holds one output row
+// per lane (TMEM lane = row), so 16-byte stores straight from registers
+// touch 32 rows per instruction.  Instead each lane packs its row's four
+// 8-column groups, and each group of 4 lanes transposes its 4x4 block of
+// 16-byte groups: lane 4h+t then holds column group t of the rows of lanes
+// 4h..4h+3, and one store instruction writes 8 rows x 64 contiguous bytes.
+__device__ __forceinline__ void transpose4x4_u4(uint4 (&x)[4])
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int m = 2; m >= 1; m >>= 1) {
+        const bool hi = (lane & m) != 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if ((i & m) == 0) {
+                const uint4 send = hi ? x[i] : x[i | m];
+                uint4 recv;
+                recv.x = __shfl_xor_sync(0xffffffffu, send.x, m);
+                recv.y = __shfl_xor_sync(0xffffffffu, send.y, m);
+                recv.z = __shfl_xor_sync(0xffffffffu, send.z, m);
+                recv.w = __shfl_xor_sync(0xffffffffu, send.w, m);
+                if (hi)
+                    x[i] = recv;
+                else
+                    x[i | m] = recv;
+            }
+        }
+    }
+}
+
+// Where lane 4h+t stores: the row start (element offset into D) and
+// validity of each row of its group of 4 lanes, gathered once per tile.
+struct RowTargets {
+    int64_t off[4];
+    bool ok[4];
+};
+
+__device__ __forceinline__ RowTargets row_targets(int64_t my_off, bool my_ok)
+{
+    const int base = (threadIdx.x & 31) & ~3;
+    RowTargets t;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        t.off[j] = __shfl_sync(0xffffffffu, static_cast<long long>(my_off), base + j);
+        t.ok[j] = __shfl_sync(0xffffffffu, my_ok ? 1 : 0, base + j) != 0;
+    }
+    return t;
+}
+
+// All lanes: 32 accumulator columns (bits) v of this lane's row `grow`
+// (valid if row_ok), columns col0 .. col0 + 31 of the output.
+template <bool kEpi>
+__device__ __forceinline__ void store_rows32(const GemmArgs &a, __nv_bfloat16 *dout, const uint32_t *v, float rf,
+                                             int g, int64_t grow, bool row_ok, int col0, const RowTargets &t)
+{
+    const int lane = threadIdx.x & 31;
+    uint4 p[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int col = col0 + 8 * j;
+        p[j] = (row_ok && col < a.n) ? store_pack8<kEpi>(a, v + 8 * j, rf, g, grow, col) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    transpose4x4_u4(p);
+    const int col = col0 + 8 * (lane & 3);
+    if (col < a.n) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (t.ok[j])
+                *reinterpret_cast<uint4 *>(dout + t.off[j] + col) = p[j];
+    }
+}
+
 // SwapAB output of 16 tokens: on entry lane `lane` of the warp holds
 // accumulator values (bits) v[j] of weight row (= output column) col_base +
 // lane for tokens tok0+j, j < 16.  Two in-warp 8x8 transposes give lane 8g+t
@@ -924,7 +996,6 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
             const int row = m0 + q * 32 + lane;
             const bool row_ok = row < mv;
             const int64_t grow = static_cast<int64_t>(ctl.group_row0[g]) + row;
-            __nv_bfloat16 *drow = dout + grow * static_cast<int64_t>(a.n);
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * acc_step * acc_stride);
             const uint32_t t_first = t_row + par * static_cast<uint32_t>(acc_stride);
@@ -933,6 +1004,7 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
             if (acc_step == 2)
                 par ^= static_cast<uint32_t>(a.num_kb & 1);
             const float rf = (kEpi && row_ok) ? row_factor(a, g, grow) : 1.0f;
+            const RowTargets tg = row_targets(grow * static_cast<int64_t>(a.n), row_ok);
             for (int c = 0; c < a.tile_n; c += 32) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(t_first + static_cast<uint32_t>(c), r);
@@ -945,14 +1017,7 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
                             r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
                     }
                 }
-                if (row_ok) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int col = n0 + c + 8 * j;
-                        if (col < a.n)
-                            *reinterpret_cast<uint4 *>(drow + col) = store_pack8<kEpi>(a, r + 8 * j, rf, g, grow, col);
-                    }
-                }
+                store_rows32<kEpi>(a, dout, r, rf, g, grow, row_ok, n0 + c, tg);
             }
             tc_fence_before();
             mbar_arrive(smem_addr(&ctl.tempty[acc]));
@@ -1425,7 +1490,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
             tc_fence_after();
             const int grow = x.m0 + row;
             const bool row_ok = grow < a.rows_a;
-            __nv_bfloat16 *drow = dout + static_cast<int64_t>(grow) * static_cast<int64_t>(a.n);
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * acc_step * acc_stride);
             // With two issuers: the one that took the segment's first K block
@@ -1448,19 +1512,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
                     }
                 }
             };
-            // Eight FP32 values (as bits) -> eight scaled BF16 at column col.
             const float rf = (kEpi && row_ok) ? row_factor(a, 0, grow) : 1.0f;
-            auto store8 = [&](int col, const uint32_t *v) {
-                if (row_ok && col < a.n)
-                    *reinterpret_cast<uint4 *>(drow + col) = store_pack8<kEpi>(a, v, rf, 0, grow, col);
-            };
+            const RowTargets tg = row_targets(static_cast<int64_t>(grow) * static_cast<int64_t>(a.n), row_ok);
             if (x.kb0 == 0 && x.kb1 == num_kb) {
                 for (int c = 0; c < a.tile_n; c += 32) {
                     uint32_t r[32];
                     ld32(c, r);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        store8(x.n0 + c + 8 * j, r + 8 * j);
+                    store_rows32<kEpi>(a, dout, r, rf, 0, grow, row_ok, x.n0 + c, tg);
                 }
             } else {
                 float4 *mine = slots + (static_cast<int64_t>(blockIdx.x) * 2 + x.kind) * part4;
@@ -1534,9 +1592,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
                             bits_v[j] = __float_as_uint(acc_v[j]);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            store8(x.n0 + c + 8 * j, bits_v + 8 * j);
+                        store_rows32<kEpi>(a, dout, bits_v, rf, 0, grow, row_ok, x.n0 + c, tg);
                     }
                 }
             }
