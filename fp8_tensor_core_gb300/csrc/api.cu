@@ -353,7 +353,8 @@ int check_epilogue(const fp8g_epilogue *e, Problem &p)
 
 // Largest tile (token chunk, or N tile) whose two accumulators leave TMEM
 // room for at least two stages' scale sets.
-constexpr int kMaxBlockScaledTile = 224;
+constexpr int kMaxBlockScaledTile = 224;   // widest block-scaled tile with two accumulator buffers
+constexpr int kWideBlockScaledKb = 48;     // K blocks from which single-SM block-scaled tiles go 256 wide
 
 int check_blockscales(const uint8_t *sf_a, int64_t sf_a_ld, const uint8_t *sf_b, int64_t sf_b_ld,
                       int group_k, int64_t rows, int64_t N, Problem &p)
@@ -604,9 +605,14 @@ int launch(const Problem &p, cudaStream_t stream)
     }
 
     const int64_t m_tiles = cdiv(p.rows_a, kTileM);
-    const int max_tn = p.sf_k ? kMaxBlockScaledTile : 256;
-    int tile_n = pick_tile_n(p.G * m_tiles, p.N, info.sms, max_tn);
+    // Block scales with long K: 256-wide tiles and one accumulator buffer.
+    // A block-scaled MMA costs its issuing thread the same at N = 256 as at
+    // 224, and the epilogue's hold on the issuer at every tile is small
+    // against a long main loop.  (FP8G_TILE_N(8) asks for it at any K.)
     const int tn_override = static_cast<int>((p.flags >> 16) & 15u);
+    const bool bs_wide = p.sf_k && (num_kb >= kWideBlockScaledKb || tn_override == 8);
+    const int max_tn = p.sf_k && !bs_wide ? kMaxBlockScaledTile : 256;
+    int tile_n = pick_tile_n(p.G * m_tiles, p.N, info.sms, max_tn);
     if (tn_override >= 1 && tn_override <= 8)
         tile_n = std::min(32 * tn_override, max_tn);
     const int64_t units_upper = p.G * m_tiles * cdiv(p.N, tile_n);
@@ -615,6 +621,11 @@ int launch(const Problem &p, cudaStream_t stream)
     args.tile_n = tile_n;
     if (p.sf_k) {
         plan_blockscaled(args, info, tile_n, static_cast<int>(p.G), p.flags);
+        if (tile_n > kMaxBlockScaledTile) {   // one accumulator buffer, then the scale sets
+            args.acc_bufs = 1;
+            args.sf_col0 = tile_n;
+            args.sf_sets = std::min(kMaxSfSets, (kTmemCols - tile_n) / sf_set_cols(tile_n));
+        }
         // Two MMA issuers (alternate K blocks, one accumulator each): with
         // two accumulator buffers per issuer when four tiles and two scale
         // sets fit in TMEM; with one (the epilogue then holds the issuers

@@ -733,11 +733,12 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
     // Accumulator spacing in TMEM: 256 columns, or tile_n when the block-scale
     // sets follow the accumulators.  With block scales and two MMA issuers,
     // issuer i's accumulator of buffer b sits at column (acc_step * b + i) *
-    // tile_n, with one buffer per issuer when four do not fit (the epilogue
-    // of a tile then holds the issuers back until it has read it).
+    // tile_n.  With one buffer per issuer (four do not fit, or 256-wide
+    // block-scaled tiles) the epilogue of a tile holds the issuers back
+    // until it has read it.
     const int acc_stride = kBS ? a.tile_n : kAccStride;
     const int acc_step = (kBS && a.dual_mma) ? 2 : 1;
-    const int n_bufs = (kBS && a.dual_mma && a.acc_bufs == 1) ? 1 : 2;
+    const int n_bufs = (kBS && a.acc_bufs == 1) ? 1 : 2;
     const int set_cols = sf_set_cols(a.tile_n);
 
     if (threadIdx.x == 0)
@@ -1094,7 +1095,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
     // Two MMA issuers in the even CTA (warps 1 and 6, alternate K blocks,
     // one accumulator each; one buffer each when four do not fit in TMEM).
     const int acc_step = (kBS && a.dual_mma) ? 2 : 1;
-    const int n_bufs = (kBS && a.dual_mma && a.acc_bufs == 1) ? 1 : 2;
+    const int n_bufs = (kBS && a.acc_bufs == 1) ? 1 : 2;
     const int set_cols = sf_set_cols(a.tile_n);
     const int cid = blockIdx.x >> 1;
     const int ncl = gridDim.x >> 1;

@@ -76,8 +76,9 @@ struct GemmArgs {
     int32_t sf_sets;           // TMEM block-scale sets (2..kMaxSfSets)
     int32_t dual_mma;          // block-scaled SwapAB / single-SM kernels: two MMA-issuing threads,
                                // each with its own accumulators, alternating K blocks
-    int32_t acc_bufs;          // single-SM kernel with two issuers: accumulator buffers per issuer
-                               // (2, or 1 when four tile_n-wide accumulators do not fit in TMEM)
+    int32_t acc_bufs;          // block-scaled tile kernels: accumulator buffers per issuer (0 or 2:
+                               // two; 1: one, when two issuers' four or a 256-wide tile's two
+                               // accumulators and the scale sets do not fit in TMEM)
     // Fused epilogue (epi != 0): out = round(act(alpha * v + beta * c_in + bias)),
     // v the (scaled) product; c_in BF16 shaped like D or nullptr; bias FP32
     // [groups][n] or nullptr; act ReLU when relu != 0; round_mode 0 nearest

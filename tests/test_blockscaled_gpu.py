@@ -91,8 +91,17 @@ def test_dense_tiles(M, N, K, gran, kernel):
 @pytest.mark.parametrize("kernel", ["pair", "single_sm"])
 @pytest.mark.parametrize("tn", [4, 5, 6, 7, 8])
 def test_dense_every_tile_width(tn, kernel):
-    """FP8G_TILE_N(8) (256 columns) is clamped to the widest block-scaled tile."""
+    """FP8G_TILE_N(8): 256-wide single-SM tiles with one accumulator buffer;
+    SM pairs clamp it to the widest block-scaled tile."""
     check_dense_bs(256, 480, 768, 128, DENSE_KERNELS[kernel] | fp8g.TILE_N(tn), seed=520 + tn)
+
+
+@pytest.mark.parametrize("gran", [128, 32])
+@pytest.mark.parametrize("M,N,K", [(300, 640, 6272), (129, 520, 8208)])
+def test_single_sm_long_k_wide_tiles(M, N, K, gran):
+    """K of 49 / 65 K blocks: 256-wide single-SM tiles with one buffer (the
+    default from 48 K blocks), N tails inside a tile, several tiles per SM."""
+    check_dense_bs(M, N, K, gran, OFF | fp8g.SINGLE_SM_TILES, seed=540 + M + gran)
 
 
 @pytest.mark.parametrize("gran", [128, 32])

@@ -108,7 +108,7 @@ def test_small_m_every_element(name):
 
 
 BLOCKSCALED = ["dense4096:bs", "masked:bs", "masked:bs32", "smallm:16:7168:16384:auto:bs",
-               "smallm:64:24576:1536:auto:bs32", "proj:7168:2048:bs"]
+               "smallm:64:24576:1536:auto:bs32", "proj:7168:2048:bs", "proj:7168:18432:bs"]
 
 
 @pytest.mark.parametrize("name", BLOCKSCALED)
