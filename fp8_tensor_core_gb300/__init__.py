@@ -30,6 +30,7 @@ PAIR_TILES = 0x4000       # dense: always SM-pair tiles when M > 128
 ONE_MMA_ISSUER = 0x8000   # block-scaled kernels: one MMA-issuing thread
 TWO_MMA_ISSUERS = 0x2000  # block-scaled tile kernels: two issuers even with one buffer each
 SHARE_SM = 0x1000         # SwapAB kernel: half an SM per CTA (next launch overlaps the drain)
+NO_SHARE_SM = 0x40        # SwapAB kernel: never share an SM (default shares it for <= 16 tokens)
 
 
 def STAGES(n: int) -> int:

@@ -115,8 +115,11 @@ typedef enum {
 #define FP8G_STAGES(n) ((((uint32_t)(n)) & 15u) << 20)
 /*   FP8G_SHARE_SM     SwapAB kernel with <= 128 tokens per chunk: half the
  *                     shared memory and TMEM per CTA, so the next launch's
- *                     CTAs can become resident while this one drains        */
+ *                     CTAs can become resident while this one drains (the
+ *                     default for dense problems of up to 16 tokens)
+ *   FP8G_NO_SHARE_SM  never share an SM that way                            */
 #define FP8G_SHARE_SM 0x1000u
+#define FP8G_NO_SHARE_SM 0x40u
 #define FP8G_TILE_N(n) (((((uint32_t)(n)) / 32u) & 15u) << 16)
 /* Debug bits (bench and tests only; never needed for correct results). */
 #define FP8G_DEBUG_ONE_STAGE 0x10u       /* one shared-memory stage: load,

@@ -117,8 +117,8 @@ def test_python_flag_constants_match_the_header():
         defs = dict(re.findall(r"#define FP8G_([A-Z0-9_]+) (0x[0-9a-fA-F]+|[0-9]+)u?\b", f.read()))
     checked = 0
     for name in ("SWAP_AUTO", "SWAP_ON", "SWAP_OFF", "DEBUG_ONE_STAGE", "WHOLE_TILES", "STREAM_K", "SINGLE_SM_TILES",
-                 "NO_PDL", "PAIR_TILES", "ONE_MMA_ISSUER", "TWO_MMA_ISSUERS", "SHARE_SM"):
+                 "NO_PDL", "PAIR_TILES", "ONE_MMA_ISSUER", "TWO_MMA_ISSUERS", "SHARE_SM", "NO_SHARE_SM"):
         assert name in defs, name
         assert getattr(fp8g, name) == int(defs[name], 0), name
         checked += 1
-    assert checked == 12
+    assert checked == 13

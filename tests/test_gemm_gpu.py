@@ -354,6 +354,13 @@ def test_share_sm_mode_dense(M, N, K):
     check_dense(M, N, K, flags=ON | fp8g.SHARE_SM, seed=11 * M + N + K)
 
 
+@pytest.mark.parametrize("M", [1, 9, 16])
+def test_dense_up_to_16_tokens_with_and_without_sharing(M):
+    # the default shares the SM for up to 16 tokens; NO_SHARE_SM keeps the whole SM
+    check_dense(M, 3072, 5120, flags=ON, seed=13 * M)
+    check_dense(M, 3072, 5120, flags=ON | fp8g.NO_SHARE_SM, seed=13 * M)
+
+
 def test_share_sm_mode_grouped():
     mm = [0, 5, 32, 17, 1, 64]
     grouped_case(len(mm), 64, 512, 1024, mm, ON | fp8g.SHARE_SM, 32, seed=171)
