@@ -1,18 +1,25 @@
 // FP8 GEMM kernels for sm_103a (GB300).
 //
-// Both kernels are persistent (one CTA per SM, looping over work units) and
-// warp-specialised:
+// All three kernels are persistent (one CTA, or CTA pair, per SM, looping
+// over work units) and warp-specialised:
 //   warp 0      loader: TMA copies of 128-byte K slices into a ring of
 //               shared-memory stages (full/empty mbarrier pairs);
 //   warp 1      MMA issuer: one thread issues tcgen05.mma kind::f8f6f4 into
 //               a TMEM accumulator (two accumulators, so the epilogue of one
 //               unit overlaps the main loop of the next);
 //   warps 2-5   epilogue: tcgen05.ld TMEM -> registers, FP32 -> BF16 (round
-//               to nearest even), stores to D.
+//               to nearest even, or the fused epilogue), stores to D;
+// and, in the block-scaled instantiations (kind::mxf8f6f4 with UE8M0 scale
+// factors in TMEM),
+//   warp 6      a second MMA issuer taking alternate K blocks into its own
+//               accumulator, where TMEM has room;
+//   warps 7-10  scale staging: each writes the scale sets into its TMEM lane
+//               quadrant with tcgen05.st.
 //
 // k_gemm_mn    tokens (A) on the MMA M side (128-row tiles), weights (B) on
 //              N (tile_n columns).  Dense, or grouped with a valid-row count
-//              per group.
+//              per group (masked or contiguous layout).
+// k_gemm_mn2   dense, 256-row tiles on an SM pair (tcgen05 cta_group::2).
 // k_gemm_swap  SwapAB: weights (B) on the M side (128 weight rows), tokens
 //              (A) on N with a per-unit runtime N = valid tokens rounded up
 //              to 16, written into the instruction descriptor.  Stream-K
@@ -1066,7 +1073,7 @@ struct PairSeg {
 };
 
 template <bool kBS, bool kEpi>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemScaled : kThreadsScaled, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
     k_gemm_mn2(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                const __grid_constant__ CUtensorMap tm_sa, const __grid_constant__ CUtensorMap tm_sb,
                const GemmArgs a)

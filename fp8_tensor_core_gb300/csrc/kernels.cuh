@@ -13,9 +13,8 @@ constexpr int kTileM = 128;          // MMA M: rows of the operand on the M side
 constexpr int kMaxStages = 16;
 constexpr int kMaxGroups = 1024;
 constexpr int kThreads = 192;        // warp 0 loader, warp 1 MMA issuer, warps 2-5 epilogue
-constexpr int kThreadsScaled = 224;  // SM-pair kernel with block scales: + warp 6, scale staging
-constexpr int kThreadsTmemScaled = 352;  // SwapAB and single-SM kernels with block scales: + warp 6,
-                                         // second MMA issuer, and warps 7-10, scale sets into TMEM
+constexpr int kThreadsTmemScaled = 352;  // block-scaled instantiations: + warp 6, second MMA issuer,
+                                         // and warps 7-10, scale sets into TMEM
 constexpr int kMaxSfSets = 4;        // TMEM block-scale sets in flight
 constexpr int kTmemCols = 512;       // two accumulators of up to 256 columns
 constexpr int kAccStride = 256;
