@@ -66,3 +66,40 @@ def test_wait_runs_out_then_gpu_still_correct(M, N, K, flags, name):
 
 def test_status_word_is_cleared_by_reading():
     assert fp8g.fp8g_get_device_status()[0] == fp8g.OK
+
+
+@pytest.mark.parametrize("M,N,K,flags,name", [
+    (512, 768, 1024, fp8g.SWAP_OFF | fp8g.PAIR_TILES, "SM-pair kernel"),
+    (256, 512, 1024, fp8g.SWAP_OFF | fp8g.SINGLE_SM_TILES, "single-SM kernel, one issuer"),
+    (256, 512, 1024, fp8g.SWAP_OFF | fp8g.SINGLE_SM_TILES | fp8g.TILE_N(3), "single-SM kernel, two issuers"),
+    (32, 2048, 2048, fp8g.SWAP_ON, "SwapAB kernel, two issuers"),
+])
+def test_block_scaled_wait_runs_out_then_gpu_still_correct(M, N, K, flags, name):
+    """The block-scaled kernels' extra roles (scale-staging warps, a second
+    MMA issuer, the scale barriers the loader drains) leave cleanly too."""
+    A = synth.normal_fp8((M, K), 611 + M, 0.0, 1.0, synth.E4M3)
+    B = synth.normal_fp8((N, K), 612 + N, 0.0, 1.0, synth.E4M3)
+    ks = K // 128
+    rng = np.random.default_rng(613)
+    sfa = rng.integers(124, 131, (1, ks, M)).astype(np.uint8)
+    sfb = rng.integers(124, 131, (1, ks, N)).astype(np.uint8)
+    Ad, Bd = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    sfad, sfbd = torch.from_numpy(sfa).cuda(), torch.from_numpy(sfb).cuda()
+    prev = fp8g.fp8g_set_wait_timeout_ns(LIMIT_NS)
+    try:
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        fp8g.fp8_gemm_nt_blockscaled(Ad, Bd, sfad, sfbd, sf_group_k=128, a_dtype=0, b_dtype=0,
+                                     flags=flags | fp8g.DEBUG_DROP_FIRST_LOAD)
+        st = fp8g.fp8g_get_device_status()
+        elapsed = time.perf_counter() - t0
+    finally:
+        fp8g.fp8g_set_wait_timeout_ns(prev)
+    assert st[0] == fp8g.ERR_TIMEOUT, (name, st)
+    assert elapsed < 5.0, elapsed
+    D = fp8g.fp8_gemm_nt_blockscaled(Ad, Bd, sfad, sfbd, sf_group_k=128, a_dtype=0, b_dtype=0, flags=flags)
+    st2 = fp8g.fp8g_get_device_status()
+    assert st2[0] == fp8g.OK, st2
+    ref, absdot = oracle.gemm_blockscaled(A, B, sfa[0], sfb[0], 128)
+    ok, rep = oracle.check_bf16(bits(D), ref, absdot)
+    assert ok, (name, rep)
