@@ -73,6 +73,8 @@ def make_workload(name: str, rank: int = 0) -> Workload:
         base, tag = name.rsplit(":", 1)
         gran = 128 if tag == "bs" else 32
         w = _make_base_workload(base, rank)
+        if w.kind == "contig":
+            raise SystemExit("block scales are not supported with the contiguous grouped layout")
         w.name, w.gran = name, gran
         w.desc += ", block-scaled (UE8M0, 1x%d tokens, %s weights)" % (gran, "128x128" if gran == 128 else "1x32")
         if w.kind == "dense" and w.M > 128 and (w.flags & 3) != 1:
@@ -117,10 +119,25 @@ def _make_base_workload(name: str, rank: int = 0) -> Workload:
         G, m, N, K = int(parts[1]), int(parts[2]), int(parts[3]), int(parts[4])
         mode = parts[5] if len(parts) > 5 else "auto"
         label = {"swap": "SwapAB", "noswap": "non-swapped", "auto": "library's choice"}[mode]
+        # tensor-bound above the ridge (~500 FLOP per byte), else HBM-bound
+        bound = "tensor" if 2.0 * G * m * N * K / (G * N * K + G * m * K + 2.0 * G * m * N) > 500 else "hbm"
         return Workload(name, "masked", "masked grouped GEMM G=%d, m=%d tokens in every group, N=%d K=%d, "
                         "E4M3 N(0,0.5), %s" % (G, m, N, K, label), G=G, M_max=m, N=N, K=K, fa=synth.E4M3,
-                        fb=synth.E4M3, dist="normal", std=0.5, seed=synth.seed_for(5, rank), bound="hbm",
+                        fb=synth.E4M3, dist="normal", std=0.5, seed=synth.seed_for(5, rank), bound=bound,
                         hint=m, flags={"swap": 1, "noswap": 2, "auto": 0}[mode], m_fixed=m)
+    if name.startswith("contig:"):
+        # contig:G:m:N:K[:swap|noswap|auto] -- contiguous grouped GEMM: the G
+        # groups' m token rows each stored back to back in A [G*m, K]
+        parts = name.split(":")
+        G, m, N, K = int(parts[1]), int(parts[2]), int(parts[3]), int(parts[4])
+        mode = parts[5] if len(parts) > 5 else "auto"
+        label = {"swap": "SwapAB", "noswap": "non-swapped", "auto": "library's choice"}[mode]
+        # tensor-bound above the ridge (~500 FLOP per byte), else HBM-bound
+        bound = "tensor" if 2.0 * G * m * N * K / (G * N * K + G * m * K + 2.0 * G * m * N) > 500 else "hbm"
+        return Workload(name, "contig", "contiguous grouped GEMM G=%d, m=%d token rows per group back to back, "
+                        "N=%d K=%d, E4M3 N(0,0.5), %s" % (G, m, N, K, label), G=G, M_max=m, N=N, K=K,
+                        fa=synth.E4M3, fb=synth.E4M3, dist="normal", std=0.5, seed=synth.seed_for(6, rank),
+                        bound=bound, hint=m, flags={"swap": 1, "noswap": 2, "auto": 0}[mode], m_fixed=m)
     if name.startswith("smallm"):
         # smallm:M:N:K[:swap|noswap]
         parts = name.split(":")
@@ -147,6 +164,12 @@ def host_inputs(w: Workload):
             A = synth.normal_fp8((w.M, w.K), w.seed, 0.0, w.std, w.fa)
             B = synth.normal_fp8((w.N, w.K), w.seed + 100, 0.0, w.std, w.fb)
         out = {"A": A, "B": B}
+    elif w.kind == "contig":
+        A = synth.normal_fp8((w.G * w.M_max, w.K), w.seed, 0.0, w.std, w.fa)
+        B = synth.normal_fp8((w.G, w.N, w.K), w.seed + 100, 0.0, w.std, w.fb)
+        mm = np.full(w.G, w.m_fixed, np.int32)
+        out = {"A": A, "B": B, "masked_m": mm,
+               "offsets": np.concatenate([[0], np.cumsum(mm)]).astype(np.int32)}
     else:
         A = synth.normal_fp8((w.G, w.M_max, w.K), w.seed, 0.0, w.std, w.fa)
         B = synth.normal_fp8((w.G, w.N, w.K), w.seed + 100, 0.0, w.std, w.fb)
@@ -336,6 +359,18 @@ def oracle_sample(w: Workload, inp, budget_s: float, min_rows: int = 1):
         secs = time.perf_counter() - t_start
         desc = "rows 0..%d of D (%d of %d rows, all N=%d columns, K=%d)" % (r0 - 1, r0, w.M, w.N, w.K)
         return flops, secs, cores, desc
+    if w.kind == "contig":
+        A, B, off = inp["A"], inp["B"], inp["offsets"]
+        g_done = 0
+        for g in range(w.G):
+            if off[g + 1] > off[g]:
+                oracle.gemm_nt(A[off[g]:off[g + 1]], B[g], w.fa, w.fb)
+                flops += 2.0 * int(off[g + 1] - off[g]) * w.N * w.K
+            g_done += 1
+            if time.perf_counter() - t_start >= budget_s:
+                break
+        secs = time.perf_counter() - t_start
+        return flops, secs, cores, "groups 0..%d of %d (all their rows)" % (g_done - 1, w.G)
     A, B, mm = inp["A"], inp["B"], inp["masked_m"]
     D0 = np.zeros((1, w.M_max, w.N), np.uint16)
     g_done = 0
@@ -417,6 +452,8 @@ def run_ours(args, w: Workload):
     # operands in L2: sets x (inputs + output) >= 3 x L2.
     if w.kind == "dense":
         set_bytes = w.M * w.K + w.N * w.K + 2 * w.M * w.N
+    elif w.kind == "contig":
+        set_bytes = w.G * w.M_max * w.K + w.G * w.N * w.K + 2 * w.G * w.M_max * w.N
     else:
         set_bytes = w.G * w.M_max * w.K + w.G * w.N * w.K + 2 * w.G * w.M_max * w.N
     n_sets = max(1, math.ceil(3 * l2 / set_bytes))
@@ -432,6 +469,9 @@ def run_ours(args, w: Workload):
             s["sfa"], s["sfb"] = sfa_h.to(device), sfb_h.to(device)
         if w.kind == "dense":
             s["D"] = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device)
+        elif w.kind == "contig":
+            s["off"] = torch.from_numpy(inp["offsets"]).to(device)
+            s["D"] = torch.empty((w.G * w.M_max, w.N), dtype=torch.bfloat16, device=device)
         else:
             s["mm"] = torch.from_numpy(inp["masked_m"]).to(device)
             s["D"] = torch.zeros((w.G, w.M_max, w.N), dtype=torch.bfloat16, device=device)
@@ -445,6 +485,9 @@ def run_ours(args, w: Workload):
         elif w.kind == "dense":
             fp8g.fp8_gemm_nt(s["A"], s["B"], s["D"], a_dtype=w.fa, b_dtype=w.fb, flags=w.flags,
                              stream=strm)
+        elif w.kind == "contig":
+            fp8g.fp8_gemm_grouped_contiguous(s["A"], s["B"], s["off"], D=s["D"], max_m_hint=w.hint, a_dtype=w.fa,
+                                             b_dtype=w.fb, flags=w.flags, stream=strm)
         elif w.gran:
             fp8g.fp8_gemm_grouped_masked_blockscaled(s["A"], s["B"], s["mm"], s["sfa"], s["sfb"], s["D"],
                                                      max_m_hint=w.hint, sf_group_k=w.gran, a_dtype=w.fa,
@@ -535,7 +578,8 @@ def run_ours(args, w: Workload):
     if not args.no_e2e:
         e2e_steps = max(1, min(args.steps, args.e2e_steps))
         n_pipe = max(1, args.e2e_streams)
-        mm_h = torch.from_numpy(inp["masked_m"]).pin_memory() if mm is not None else None
+        mm_h = torch.from_numpy(inp["masked_m"]).pin_memory() if mm is not None and w.kind == "masked" else None
+        off_h = torch.from_numpy(inp["offsets"]).pin_memory() if w.kind == "contig" else None
         pipe = []
         for k in range(n_pipe):
             if k < n_sets:
@@ -556,6 +600,8 @@ def run_ours(args, w: Workload):
                     s_k["sfb"].copy_(sfb_h, non_blocking=True)
                 if mm_h is not None:
                     s_k["mm"].copy_(mm_h, non_blocking=True)
+                if off_h is not None:
+                    s_k["off"].copy_(off_h, non_blocking=True)
                 call(s_k, strm)
                 p["D_h"].copy_(s_k["D"], non_blocking=True)
 
@@ -577,7 +623,8 @@ def run_ours(args, w: Workload):
         if st[0] != fp8g.OK:
             raise SystemExit("device status after the end-to-end run: %s" % (st,))
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
-        h2d = A_h.numel() + B_h.numel() + (mm_h.numel() * 4 if mm_h is not None else 0)
+        h2d = A_h.numel() + B_h.numel() + (mm_h.numel() * 4 if mm_h is not None else 0) + \
+            (off_h.numel() * 4 if off_h is not None else 0)
         if w.gran:
             h2d += sfa_h.numel() + sfb_h.numel()
         d2h = pipe[0]["D_h"].numel() * 2
@@ -599,7 +646,8 @@ def run_ours(args, w: Workload):
         unit = "GB/s"
         basis = "%s HBM copy bandwidth" % peak_src
     traffic = profiled_traffic(w.name)
-    kernel_name = "k_gemm_swap" if (w.flags & 3) == 1 or (w.kind == "masked") else \
+    kernel_name = "k_gemm_swap" if (w.flags & 3) == 1 or (w.kind == "masked" and w.M_max < 256) else \
+        "k_gemm_mn2/k_gemm_mn" if w.kind in ("contig", "masked") else \
         ("k_gemm_mn2" if w.kind == "dense" and w.M > 128 and not (w.flags & 0x200) else "k_gemm_mn/k_gemm_swap (auto)")
     kernel_name = getattr(w, "kernel", kernel_name)
     roof = {"bound": w.bound, "achieved": achieved, "peak": peak, "unit": unit,
@@ -638,6 +686,8 @@ def run_ours(args, w: Workload):
         if w.kind == "masked":
             line["config"]["sum_masked_m"] = int(sum(mm))
             line["config"]["empty_groups"] = int(sum(1 for m in mm if m == 0))
+        if w.kind == "contig":
+            line["config"]["tokens"] = int(sum(mm))
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist

@@ -544,13 +544,24 @@ int launch(const Problem &p, cudaStream_t stream)
     // (measured on GB300: 2-6 % faster at K >= 7168, even at K = 4096, 7-13 %
     // slower at K = 2048 or with 32-element groups, whose per-K-block scale
     // copies weigh more in the pair's longer K block).
-    const bool pair_ok = !p.sf_k || (p.flags & FP8G_PAIR_TILES);
-    if (!p.masked_m && !p.group_offsets && p.G == 1 && p.rows_a > kTileM && !(p.flags & FP8G_SINGLE_SM_TILES) &&
-        pair_ok) {
-        const int64_t m_tiles2 = cdiv(p.rows_a, 2 * kTileM);
+    // SM-pair tiles (256 token rows): dense problems with more than 128 rows;
+    // grouped ones (plain, whole tiles) whose groups hold 256 or more tokens
+    // on average (contiguous layout) or at most (masked layout's hint).
+    const bool grouped = p.masked_m || p.group_offsets || p.G > 1;
+    const int64_t group_tokens = p.group_offsets ? p.rows_a / p.G : p.token_hint;
+    const bool pair_ok = grouped ? (!p.sf_k && (group_tokens >= 2 * kTileM || (p.flags & FP8G_PAIR_TILES)))
+                                 : (p.rows_a > kTileM && (!p.sf_k || (p.flags & FP8G_PAIR_TILES)));
+    if (pair_ok && !(p.flags & FP8G_SINGLE_SM_TILES)) {
+        // 256-row tiles: exact for dense; for groups an upper bound (each
+        // group boundary can add a partial tile) sizes the grid, and the
+        // expected tokens per group the tile width.
+        const int64_t m_tiles2 = grouped ? (p.group_offsets ? cdiv(p.rows_a, 2 * kTileM) + p.G
+                                                            : p.G * cdiv(p.rows_a, 2 * kTileM))
+                                         : cdiv(p.rows_a, 2 * kTileM);
+        const int64_t m_tiles2_plan = grouped ? p.G * cdiv(std::max<int64_t>(group_tokens, 1), 2 * kTileM) : m_tiles2;
         const int pairs = info.sms / 2;
-        const PairPlan plan =
-            plan_pair(m_tiles2, p.N, num_kb, pairs, p.flags, p.sf_k ? kMaxBlockScaledTile : 256);
+        const PairPlan plan = plan_pair(m_tiles2_plan, p.N, num_kb, pairs, grouped ? (p.flags & ~FP8G_STREAM_K) : p.flags,
+                                        p.sf_k ? kMaxBlockScaledTile : 256);
         const int tile_n = plan.tile_n;
         const int64_t units = m_tiles2 * cdiv(p.N, tile_n);
         if (units > kMaxDim || units * num_kb > (int64_t(1) << 53))
@@ -583,8 +594,8 @@ int launch(const Problem &p, cudaStream_t stream)
         }
         const int64_t band = (48ll << 20) / (2 * kTileM * p.K);
         args.raster_band = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(band, m_tiles2)));
-        if (!make_map(&tm0, p.A, p.K, p.rows_a, 1, kTileM) ||
-            !make_map(&tm1, p.B, p.K, p.N, 1, static_cast<uint32_t>(tile_n / 2)))
+        if (!make_map(&tm0, p.A, p.K, p.rows_a, p.group_offsets ? 1 : p.G, kTileM) ||
+            !make_map(&tm1, p.B, p.K, p.N, p.G, static_cast<uint32_t>(tile_n / 2)))
             return FP8G_ERR_CUDA;
         if (p.sf_k) {
             if (!make_sf_map(&tm2, p.sf_a, p.rows_a, ks, 1, p.sf_a_ld, kTileM, 4) ||

@@ -1070,6 +1070,7 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
 struct PairSeg {
     int tile, m0, n0, kb0, kb1;
     int kind;   // 0: first segment of the pair's range, 1: a later one
+    int g, mv;  // group and its valid rows (dense: 0 and M)
 };
 
 template <bool kBS, bool kEpi>
@@ -1088,7 +1089,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
     const int half_n = a.tile_n / 2;
     const int n_tiles = ceil_div(a.n, a.tile_n);
     const int m_tiles = ceil_div(a.rows_a, 2 * kTileM);
-    const int total = m_tiles * n_tiles;
+    // Grouped problems (masked or contiguous layout): 256-row tiles inside
+    // each group, counted by the group table built on the device; whole
+    // tiles only.
+    const bool grouped = a.groups > 1 || a.masked_m != nullptr || a.group_offsets != nullptr;
+    int total = m_tiles * n_tiles;
     const int num_kb = a.num_kb;
     const bool stream_k = a.k_splits != 1;
     const uint32_t a_bytes = kTileM * kBlockK;                          // own 128 token rows
@@ -1106,11 +1111,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
     const int set_cols = sf_set_cols(a.tile_n);
     const int cid = blockIdx.x >> 1;
     const int ncl = gridDim.x >> 1;
-    // Whole-tile waves, then the stream-K remainder [sk0, sk0 + T).
-    const int dp_tiles = stream_k ? (total / ncl) * ncl : total;
-    const long long sk0 = static_cast<long long>(dp_tiles) * num_kb;
-    const long long T = static_cast<long long>(total - dp_tiles) * num_kb;
-    const long long P = T < static_cast<long long>(ncl) ? T : static_cast<long long>(ncl);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; ++s) {
@@ -1149,6 +1149,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
     if (threadIdx.x == 0)
         grid_dep_launch_dependents();
     const uint32_t tmem_base = ctl.tmem_base;
+    if (grouped) {
+        if (warp == 0)
+            build_group_table(ctl, a, [&](int m) { return ceil_div(m, 2 * kTileM) * n_tiles; });
+        __syncthreads();
+        total = ctl.units_total;
+    }
+    // Whole-tile waves, then the stream-K remainder [sk0, sk0 + T).
+    const int dp_tiles = stream_k && !grouped ? (total / ncl) * ncl : total;
+    const long long sk0 = static_cast<long long>(dp_tiles) * num_kb;
+    const long long T = static_cast<long long>(total - dp_tiles) * num_kb;
+    const long long P = T < static_cast<long long>(ncl) ? T : static_cast<long long>(ncl);
 
     // Only called when T > 0 (a stream-K segment exists).
     auto range_begin = [&](long long c) { return sk0 + c * T / P; };
@@ -1192,11 +1203,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
             w.first = false;
         }
         x.tile = u;
+        int local = u, mt = m_tiles;
+        x.g = 0;
+        x.mv = a.rows_a;
+        if (grouped) {
+            x.g = find_group(ctl, a.groups, u);
+            local = u - ctl.group_prefix[x.g];
+            x.mv = ctl.group_m[x.g];
+            mt = ceil_div(x.mv, 2 * kTileM);
+        }
         const int band_units = a.raster_band * n_tiles;
-        const int band = u / band_units;
-        const int in_band = u - band * band_units;
-        const int rows_left = m_tiles - band * a.raster_band;
+        const int band = local / band_units;
+        const int in_band = local - band * band_units;
+        const int rows_left = mt - band * a.raster_band;
         const int gm = rows_left < a.raster_band ? rows_left : a.raster_band;
+        // group-local first row of this CTA's 128 rows
         x.m0 = (band * a.raster_band + in_band % gm) * (2 * kTileM) + static_cast<int>(rank) * kTileM;
         x.n0 = (in_band / gm) * a.tile_n;
         return true;
@@ -1231,9 +1252,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
                     if (leader)
                         mbar_arrive_expect_tx(smem_addr(&ctl.full[stage]), tx_pair);
                     const uint32_t fb = mapa_shared(smem_addr(&ctl.full[stage]), 0);
-                    tma_load_3d_pair(smem_addr(sa), &tm_a, fb, kb * kBlockK, x.m0, 0);
+                    tma_load_3d_pair(smem_addr(sa), &tm_a, fb, kb * kBlockK, a_row(a, ctl, x.g, x.m0),
+                                     a_grp(a, x.g));
                     tma_load_3d_pair(smem_addr(sa + a_bytes), &tm_b, fb, kb * kBlockK,
-                                     x.n0 + static_cast<int>(rank) * half_n, 0);
+                                     x.n0 + static_cast<int>(rank) * half_n, x.g);
                     if constexpr (kBS) {
                         if (sf_load_at(kb, x.kb0, a.sf_k)) {
                             const uint32_t sb = smem_addr(&ctl.sffull[stage]);
@@ -1496,8 +1518,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
                 break;
             }
             tc_fence_after();
-            const int grow = x.m0 + row;
-            const bool row_ok = grow < a.rows_a;
+            const int lrow = x.m0 + row;   // row within the group (dense: within D)
+            const bool row_ok = lrow < x.mv;
+            const int64_t grow = (grouped ? static_cast<int64_t>(ctl.group_row0[x.g]) : int64_t(0)) + lrow;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * acc_step * acc_stride);
             // With two issuers: the one that took the segment's first K block
@@ -1520,13 +1543,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
                     }
                 }
             };
-            const float rf = (kEpi && row_ok) ? row_factor(a, 0, grow) : 1.0f;
-            const RowTargets tg = row_targets(static_cast<int64_t>(grow) * static_cast<int64_t>(a.n), row_ok);
+            const float rf = (kEpi && row_ok) ? row_factor(a, x.g, grow) : 1.0f;
+            const RowTargets tg = row_targets(grow * static_cast<int64_t>(a.n), row_ok);
             if (x.kb0 == 0 && x.kb1 == num_kb) {
                 for (int c = 0; c < a.tile_n; c += 32) {
                     uint32_t r[32];
                     ld32(c, r);
-                    store_rows32<kEpi>(a, dout, r, rf, 0, grow, row_ok, x.n0 + c, tg);
+                    store_rows32<kEpi>(a, dout, r, rf, x.g, grow, row_ok, x.n0 + c, tg);
                 }
             } else {
                 float4 *mine = slots + (static_cast<int64_t>(blockIdx.x) * 2 + x.kind) * part4;
@@ -1600,7 +1623,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
                             bits_v[j] = __float_as_uint(acc_v[j]);
-                        store_rows32<kEpi>(a, dout, bits_v, rf, 0, grow, row_ok, x.n0 + c, tg);
+                        store_rows32<kEpi>(a, dout, bits_v, rf, x.g, grow, row_ok, x.n0 + c, tg);
                     }
                 }
             }
@@ -2237,8 +2260,10 @@ cudaError_t launch_gemm_mn2(const CUtensorMap &tm_a, const CUtensorMap &tm_b, co
                             const CUtensorMap &tm_sb, const GemmArgs &args, int grid, size_t smem,
                             cudaStream_t stream)
 {
-    if (smem < smem_bytes_for(args.stages, args.stage_bytes, args.groups) || (grid & 1) || args.groups != 1 ||
-        args.masked_m != nullptr || args.group_offsets != nullptr || !dual_ok(args))
+    // Grouped problems: plain kernels, whole tiles.
+    const bool grouped = args.groups != 1 || args.masked_m != nullptr || args.group_offsets != nullptr;
+    if (smem < smem_bytes_for(args.stages, args.stage_bytes, args.groups) || (grid & 1) ||
+        (grouped && (args.sf_k || args.k_splits != 1)) || !dual_ok(args))
         return cudaErrorInvalidValue;
     const bool epi = wants_epi(args);
     if (args.sf_k)

@@ -171,6 +171,15 @@ def test_workload_variants_parse():
     assert b.bytes() == 4096 * (4096 + ks) * 2 + 2 * 4096 * 4096
     b32 = bench.make_workload("smallm:16:7168:16384:swap:bs32")
     assert b32.gran == 32 and b32.M == 16 and b32.flags == 1
+    c = bench.make_workload("contig:8:64:512:1024:noswap")
+    assert (c.kind, c.G, c.M_max, c.N, c.K, c.flags, c.hint) == ("contig", 8, 64, 512, 1024, 2, 64)
+    inp = bench.host_inputs(c)
+    assert inp["A"].shape == (8 * 64, 1024) and inp["B"].shape == (8, 512, 1024)
+    assert inp["offsets"].tolist() == [64 * g for g in range(9)]
+    assert c.flops(inp["masked_m"]) == 2.0 * 8 * 64 * 512 * 1024
+    assert c.bytes(inp["masked_m"]) == 8 * 512 * 1024 + 8 * 64 * 1024 + 2 * 8 * 64 * 512
+    with pytest.raises(SystemExit):
+        bench.make_workload("contig:8:64:512:1024:bs")
 
 
 def test_block_scale_recipe():

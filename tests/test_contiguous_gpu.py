@@ -82,6 +82,12 @@ def test_many_small_groups_e5m2(flags):
     run_case(sizes, 256, 512, flags, 24, seed=902, fb=E5)
 
 
+@pytest.mark.parametrize("flags", [OFF, OFF | fp8g.PAIR_TILES, OFF | fp8g.SINGLE_SM_TILES])
+def test_large_groups_pair_tiles(flags):
+    # about 377 tokens per group on average: SM-pair tiles by default
+    run_case([700, 0, 256, 1000, 1, 300], 512, 768, flags, 0, seed=920)
+
+
 def test_single_group_is_dense():
     run_case([700], 512, 768, OFF, 0, seed=903, lead=0, tail=0)
 
@@ -108,9 +114,9 @@ def test_matches_masked_layout():
             assert ok, rep
 
 
-@pytest.mark.parametrize("flags", [OFF, ON])
-def test_scales_and_epilogue(flags):
-    sizes = [40, 0, 129, 7]
+@pytest.mark.parametrize("flags,sizes", [(OFF, [40, 0, 129, 7]), (ON, [40, 0, 129, 7]),
+                                         (OFF | fp8g.PAIR_TILES, [300, 0, 520, 7])])
+def test_scales_and_epilogue(flags, sizes):
     G, N, K = len(sizes), 256, 512
     off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
     M_total = int(off[-1])

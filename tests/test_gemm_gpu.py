@@ -222,6 +222,18 @@ def grouped_case(G, M_max, N, K, mm, flags, hint, seed, nan_padding=False, fa=E4
         assert np.array_equal(got[g, m:], D0[g, m:]), "padding rows of group %d written" % g
 
 
+@pytest.mark.parametrize("flags,hint", [(OFF | fp8g.PAIR_TILES, 0), (OFF, 0), (AUTO, 640), (OFF, 256),
+                                        (OFF | fp8g.PAIR_TILES, 64)])
+def test_grouped_pair_tiles(flags, hint):
+    """Masked groups of up to 640 tokens on SM-pair tiles: full, partial,
+    empty and one-pair-plus-one-row groups, NaN in the padding rows."""
+    grouped_case(4, 640, 512, 1024, [640, 300, 0, 129], flags, hint, seed=191, nan_padding=True)
+
+
+def test_grouped_pair_tiles_mixed_formats_and_narrow_n():
+    grouped_case(3, 512, 136, 640, [512, 257, 1], OFF | fp8g.PAIR_TILES, 0, seed=193, fa=E5, fb=E4)
+
+
 @pytest.mark.parametrize("flags,hint", [(ON, 32), (ON, 0), (OFF, 0), (AUTO, 32), (AUTO, 0)])
 def test_grouped_edge_counts(flags, hint):
     mm = [0, 1, 7, 8, 15, 16, 17, 31, 32, 64]
