@@ -729,6 +729,17 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
               const GemmArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
+    // The tensor maps are kernel parameters, never written by an earlier
+    // launch: fetch their descriptors now, while programmatic dependent
+    // launch may still hold this CTA before griddepcontrol.wait.
+    if (threadIdx.x == 0) {
+        tma_prefetch_map(&tm_a);
+        tma_prefetch_map(&tm_b);
+        if constexpr (kBS) {
+            tma_prefetch_map(&tm_sa);
+            tma_prefetch_map(&tm_sb);
+        }
+    }
     const Smem sm = carve(smem_raw, a);
     SmemCtl &ctl = *sm.ctl;
     const int warp = threadIdx.x >> 5;
@@ -786,14 +797,6 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------- loader -------------------------------
-        if (lane == 0) {
-            tma_prefetch_map(&tm_a);
-            tma_prefetch_map(&tm_b);
-            if constexpr (kBS) {
-                tma_prefetch_map(&tm_sa);
-                tma_prefetch_map(&tm_sb);
-            }
-        }
         int stage = 0;
         uint32_t phase = 0;
         long long issued = 0;
@@ -1080,6 +1083,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
                const GemmArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
+    // The tensor maps are kernel parameters, never written by an earlier
+    // launch: fetch their descriptors now, while programmatic dependent
+    // launch may still hold this CTA before griddepcontrol.wait.
+    if (threadIdx.x == 0) {
+        tma_prefetch_map(&tm_a);
+        tma_prefetch_map(&tm_b);
+        if constexpr (kBS) {
+            tma_prefetch_map(&tm_sa);
+            tma_prefetch_map(&tm_sb);
+        }
+    }
     const Smem sm = carve(smem_raw, a);
     SmemCtl &ctl = *sm.ctl;
     const int warp = threadIdx.x >> 5;
@@ -1226,14 +1240,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
     bool aborted = false;
     if (warp == 0) {
         // ------------------------------- loader -------------------------------
-        if (lane == 0) {
-            tma_prefetch_map(&tm_a);
-            tma_prefetch_map(&tm_b);
-            if constexpr (kBS) {
-                tma_prefetch_map(&tm_sa);
-                tma_prefetch_map(&tm_sb);
-            }
-        }
         int stage = 0;
         uint32_t phase = 0;
         long long issued = 0;
@@ -1692,6 +1698,17 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
                 const GemmArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
+    // The tensor maps are kernel parameters, never written by an earlier
+    // launch: fetch their descriptors now, while programmatic dependent
+    // launch may still hold this CTA before griddepcontrol.wait.
+    if (threadIdx.x == 0) {
+        tma_prefetch_map(&tm_w);
+        tma_prefetch_map(&tm_t);
+        if constexpr (kBS) {
+            tma_prefetch_map(&tm_sw);
+            tma_prefetch_map(&tm_st);
+        }
+    }
     const Smem sm = carve(smem_raw, a);
     SmemCtl &ctl = *sm.ctl;
     const int warp = threadIdx.x >> 5;
@@ -1789,14 +1806,6 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------- loader -------------------------------
-        if (lane == 0) {
-            tma_prefetch_map(&tm_w);
-            tma_prefetch_map(&tm_t);
-            if constexpr (kBS) {
-                tma_prefetch_map(&tm_sw);
-                tma_prefetch_map(&tm_st);
-            }
-        }
         int stage = 0;
         uint32_t phase = 0;
         long long issued = 0;
