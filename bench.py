@@ -571,9 +571,9 @@ def run_ours(args, w: Workload):
     # ---- end to end through the public API, host buffers ---------------------
     # Every step copies its inputs in from pinned host memory, runs the GEMM
     # through the public API and copies the whole of D back.  Consecutive
-    # steps alternate between --e2e-streams streams, each with its own device
-    # and host buffers, so one step's copies overlap the next one's (the
-    # host link moves ~210 GB/s one way, ~340 GB/s both ways at once).
+    # steps rotate over --e2e-streams streams, each with its own device and
+    # host buffers, so one step's copies overlap its neighbours' (the host
+    # link moves ~210 GB/s one way, ~340 GB/s both ways at once).
     e2e = None
     if not args.no_e2e:
         e2e_steps = max(1, min(args.steps, args.e2e_steps))
@@ -709,7 +709,7 @@ def main(argv=None):
                     help="tuning-override flag bits OR-ed into the call (FP8G_WHOLE_TILES 0x100, FP8G_TILE_N)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
-    ap.add_argument("--e2e-streams", type=int, default=2,
+    ap.add_argument("--e2e-streams", type=int, default=3,
                     help="streams the end-to-end steps alternate between (1 = strictly serial steps)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
