@@ -33,6 +33,11 @@ SHARE_SM = 0x1000         # SwapAB kernel: half an SM per CTA (next launch overl
 NO_SHARE_SM = 0x40        # SwapAB kernel: never share an SM (default shares it for <= 16 tokens)
 
 
+def TOKEN_BOX(n: int) -> int:
+    """Flag bits: SwapAB token rows per TMA copy (multiple of 16 dividing the chunk)."""
+    return ((int(n) // 16) & 15) << 24
+
+
 def STAGES(n: int) -> int:
     """Flag bits capping the shared-memory pipeline at n stages (1..15)."""
     return (int(n) & 15) << 20

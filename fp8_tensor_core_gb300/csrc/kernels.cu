@@ -1727,8 +1727,6 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
     const int acc_stride = kBS ? cap : static_cast<int>(tmem_cols / 2);
     const int acc_step = (kBS && a.dual_mma) ? 2 : 1;
     const int set_cols = sf_set_cols(cap);
-    constexpr int kTokBox = 16;                  // token rows per TMA box
-    constexpr uint32_t kTokBoxBytes = kTokBox * kBlockK;
 
     if (threadIdx.x == 0)
         init_barriers(ctl, a.stages, static_cast<uint32_t>(acc_step));
@@ -1816,7 +1814,11 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
         SwapWalker wk = make_walker();
         SwapSeg x;
         while (!aborted && next_seg(wk, x)) {
-            const uint32_t tx = w_bytes + static_cast<uint32_t>(x.n_mma) * kBlockK;
+            // Token rows in TMA boxes of tok_box rows, enough boxes to cover
+            // the MMA's n_mma rows (rows past the valid tokens are loaded and
+            // never used).
+            const int n_load = ((x.n_mma + a.tok_box - 1) / a.tok_box) * a.tok_box;
+            const uint32_t tx = w_bytes + static_cast<uint32_t>(n_load) * kBlockK;
             for (int kb = x.kb0; kb < x.kb1; ++kb) {
                 if (!warp_wait(smem_addr(&ctl.empty[stage]), phase ^ 1u, ctl, a.timeout_ns,
                                kRoleLoader, stage)) {
@@ -1829,8 +1831,8 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
                     const uint32_t fb = smem_addr(&ctl.full[stage]);
                     mbar_arrive_expect_tx(fb, tx);
                     tma_load_3d_hint(smem_addr(sw), &tm_w, fb, kb * kBlockK, x.w0, x.g, w_policy);
-                    for (int r = 0; r < x.n_mma; r += kTokBox)
-                        tma_load_3d(smem_addr(sw + w_bytes + (r / kTokBox) * kTokBoxBytes), &tm_t, fb,
+                    for (int r = 0; r < n_load; r += a.tok_box)
+                        tma_load_3d(smem_addr(sw + w_bytes + static_cast<uint32_t>(r) * kBlockK), &tm_t, fb,
                                     kb * kBlockK, a_row(a, ctl, x.g, x.tok0 + r), a_grp(a, x.g));
                     if (sf) {
                         const uint32_t sb = smem_addr(&ctl.sffull[stage]);

@@ -75,6 +75,8 @@ struct GemmArgs {
     int32_t sf_sets;           // TMEM block-scale sets (2..kMaxSfSets)
     int32_t dual_mma;          // block-scaled SwapAB / single-SM kernels: two MMA-issuing threads,
                                // each with its own accumulators, alternating K blocks
+    int32_t tok_box;           // swap kernel: token rows per TMA box of a chunk (a multiple of 16
+                               // dividing tile_n; the host encodes the token map with this box)
     int32_t acc_bufs;          // block-scaled tile kernels: accumulator buffers per issuer (0 or 2:
                                // two; 1: one, when two issuers' four or a 256-wide tile's two
                                // accumulators and the scale sets do not fit in TMEM)

@@ -121,6 +121,10 @@ typedef enum {
 #define FP8G_SHARE_SM 0x1000u
 #define FP8G_NO_SHARE_SM 0x40u
 #define FP8G_TILE_N(n) (((((uint32_t)(n)) / 32u) & 15u) << 16)
+/*   FP8G_TOKEN_BOX(n) SwapAB kernel: n token rows per TMA copy of a chunk (a
+ *                     multiple of 16 up to 240 that divides the chunk; other
+ *                     values are ignored)                                   */
+#define FP8G_TOKEN_BOX(n) (((((uint32_t)(n)) / 16u) & 15u) << 24)
 /* Debug bits (bench and tests only; never needed for correct results). */
 #define FP8G_DEBUG_ONE_STAGE 0x10u       /* one shared-memory stage: load,
                                             compute, load ... (isolates races

@@ -122,3 +122,20 @@ def test_python_flag_constants_match_the_header():
         assert getattr(fp8g, name) == int(defs[name], 0), name
         checked += 1
     assert checked == 13
+
+
+def test_field_flags_do_not_overlap_the_single_bit_flags():
+    """STAGES, TILE_N and TOKEN_BOX fill their own bit fields and leave every
+    single-bit flag alone."""
+    import fp8_tensor_core_gb300 as fp8g
+    singles = 0
+    for name in ("SWAP_ON", "SWAP_OFF", "DEBUG_ONE_STAGE", "WHOLE_TILES", "STREAM_K", "SINGLE_SM_TILES", "NO_PDL",
+                 "PAIR_TILES", "ONE_MMA_ISSUER", "TWO_MMA_ISSUERS", "SHARE_SM", "NO_SHARE_SM"):
+        singles |= getattr(fp8g, name)
+    fields = [fp8g.STAGES(15), fp8g.TILE_N(15 * 32), fp8g.TOKEN_BOX(15 * 16)]
+    for i, f in enumerate(fields):
+        assert f & singles == 0
+        for g in fields[i + 1:]:
+            assert f & g == 0
+    assert fp8g.TOKEN_BOX(48) == 3 << 24 and fp8g.TOKEN_BOX(0) == 0
+

@@ -237,7 +237,7 @@ def grouped_bs_case(G, M_max, N, K, mm, gran, flags, hint, seed, fa=E4, fb=E4):
 
 @pytest.mark.parametrize("gran", [128, 32])
 @pytest.mark.parametrize("flags,hint", [(ON, 32), (ON | fp8g.WHOLE_TILES, 64), (ON | fp8g.ONE_MMA_ISSUER, 32),
-                                        (OFF, 0), (AUTO, 0)])
+                                        (ON | fp8g.TOKEN_BOX(16), 32), (OFF, 0), (AUTO, 0)])
 def test_grouped(flags, hint, gran):
     mm = [0, 1, 9, 16, 17, 32, 5, 64]
     grouped_bs_case(len(mm), 64, 384, 640, mm, gran, flags, hint, seed=600 + gran)

@@ -373,6 +373,13 @@ def test_dense_up_to_16_tokens_with_and_without_sharing(M):
     check_dense(M, 3072, 5120, flags=ON | fp8g.NO_SHARE_SM, seed=13 * M)
 
 
+@pytest.mark.parametrize("box", [16, 32, 64, 128])
+def test_swap_token_box_sizes(box):
+    # one 128-token chunk loaded as 128 / box TMA copies per K block
+    check_dense(128, 1536, 1024, flags=ON | fp8g.NO_SHARE_SM | fp8g.TOKEN_BOX(box), seed=700 + box)
+    check_dense(101, 1536, 1024, flags=ON | fp8g.NO_SHARE_SM | fp8g.TOKEN_BOX(box), seed=800 + box)
+
+
 def test_share_sm_mode_grouped():
     mm = [0, 5, 32, 17, 1, 64]
     grouped_case(len(mm), 64, 512, 1024, mm, ON | fp8g.SHARE_SM, 32, seed=171)
