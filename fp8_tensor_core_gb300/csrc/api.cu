@@ -440,6 +440,7 @@ int launch(const Problem &p, cudaStream_t stream)
     if (swap && mode == FP8G_SWAP_AUTO)
         swap = swap_beats_token_tiles(p.G, p.token_hint, p.N, p.K, info.sms);
     const int num_kb = static_cast<int>(cdiv(p.K, kBlockK));
+    const bool dense = p.G == 1 && !p.masked_m && !p.group_offsets;
 
     GemmArgs args;
     std::memset(&args, 0, sizeof(args));
@@ -497,7 +498,7 @@ int launch(const Problem &p, cudaStream_t stream)
         // next launch's set-up then overlaps this one's drain (measured
         // 26.1 -> 24.8 us at N = 7168, K = 16384; no gain at 32 or more
         // tokens, a loss for the masked grouped decode).
-        const bool share_auto = !(p.flags & FP8G_NO_SHARE_SM) && p.G == 1 && !p.masked_m && !p.group_offsets &&
+        const bool share_auto = !(p.flags & FP8G_NO_SHARE_SM) && dense &&
                                 cap <= 16;
         const bool share_sm = ((p.flags & FP8G_SHARE_SM) || share_auto) && cap <= 128 && !p.sf_k;
         size_t smem_request = static_cast<size_t>(info.smem_optin);
@@ -550,6 +551,7 @@ int launch(const Problem &p, cudaStream_t stream)
             tm2 = tm0;
             tm3 = tm1;
         }
+        args.prefetch_kb = dense ? early_prefetch_kb(kTileM * kBlockK, share_sm) : 0;
         return launch_gemm_swap(tm0, tm1, tm2, tm3, args, grid, smem_request, stream) == cudaSuccess
                    ? FP8G_OK
                    : FP8G_ERR_CUDA;
@@ -700,6 +702,7 @@ int launch(const Problem &p, cudaStream_t stream)
     const int grid = static_cast<int>(std::min<int64_t>(units_upper, info.sms));
     if (grid <= 0)
         return FP8G_OK;
+    args.prefetch_kb = dense ? early_prefetch_kb(static_cast<int>(tile_n) * kBlockK, false) : 0;
     return launch_gemm_mn(tm0, tm1, tm2, tm3, args, grid, static_cast<size_t>(info.smem_optin), stream) ==
                    cudaSuccess
                ? FP8G_OK

@@ -762,7 +762,9 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
     if (threadIdx.x == 0)
         init_barriers(ctl, a.stages, static_cast<uint32_t>(acc_step));
     if (warp == 0) {
-        grid_dep_wait();   // inputs may come from the previous launch in the stream
+        // A dense problem's table reads nothing from global memory.
+        if (a.prefetch_kb == 0)
+            grid_dep_wait();
         build_group_table(ctl, a, [&](int m) { return ceil_div(m, kTileM) * n_tiles; });
     }
     if (warp == 1) {
@@ -772,9 +774,6 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    grid_dep_wait();
-    if (threadIdx.x == 0)
-        grid_dep_launch_dependents();
     const uint32_t tmem_base = ctl.tmem_base;
     const int total = ctl.units_total;
 
@@ -794,6 +793,21 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
         m0 = (band * a.raster_band + in_band % gm) * kTileM;
         n0 = (in_band / gm) * a.tile_n;
     };
+
+    // Dense problems: fetch the first prefetch_kb K blocks of this CTA's
+    // weight tiles into L2 while the previous launch may still run.
+    if (a.prefetch_kb > 0 && warp == 2 && lane == 0) {
+        int left = a.prefetch_kb;
+        for (int u = blockIdx.x; u < total && left > 0; u += gridDim.x) {
+            int g, m0, n0, mv;
+            decode(u, g, m0, n0, mv);
+            for (int kb = 0; kb < a.num_kb && left > 0; ++kb, --left)
+                tma_prefetch_l2_3d(&tm_b, kb * kBlockK, n0, g);
+        }
+    }
+    grid_dep_wait();   // inputs may come from the previous launch in the stream
+    if (threadIdx.x == 0)
+        grid_dep_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------- loader -------------------------------
@@ -1731,7 +1745,11 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
     if (threadIdx.x == 0)
         init_barriers(ctl, a.stages, static_cast<uint32_t>(acc_step));
     if (warp == 0) {
-        grid_dep_wait();   // inputs may come from the previous launch in the stream
+        // A dense problem's table reads nothing from global memory; a
+        // grouped one reads masked_m or the offsets, which the previous
+        // launch in the stream may write.
+        if (a.prefetch_kb == 0)
+            grid_dep_wait();
         build_group_table(ctl, a, [&](int m) { return ceil_div(m, cap) * n_tiles; });
     }
     if (warp == 1) {
@@ -1741,9 +1759,6 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    grid_dep_wait();
-    if (threadIdx.x == 0)
-        grid_dep_launch_dependents();
     const uint32_t tmem_base = ctl.tmem_base;
     const int total_tiles = ctl.units_total;
     const long long T = static_cast<long long>(total_tiles) * num_kb;
@@ -1801,6 +1816,22 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
         x.w0 = nt * kTileM;
         return true;
     };
+
+    // Dense problems: fetch the first prefetch_kb K blocks of this CTA's
+    // weights into L2 while the previous launch may still run; the loads
+    // after griddepcontrol.wait then find them there.  (The token rows are
+    // shared by every CTA and come from L2 after the first one's load.)
+    if (a.prefetch_kb > 0 && warp == 2 && lane == 0) {
+        SwapWalker wk = make_walker();
+        SwapSeg x;
+        int left = a.prefetch_kb;
+        while (left > 0 && next_seg(wk, x))
+            for (int kb = x.kb0; kb < x.kb1 && left > 0; ++kb, --left)
+                tma_prefetch_l2_3d(&tm_w, kb * kBlockK, x.w0, x.g);
+    }
+    grid_dep_wait();   // inputs may come from the previous launch in the stream
+    if (threadIdx.x == 0)
+        grid_dep_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------- loader -------------------------------

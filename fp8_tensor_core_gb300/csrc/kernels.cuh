@@ -11,6 +11,17 @@ namespace fp8g {
 constexpr int kBlockK = 128;         // K bytes per pipeline stage (one 128-byte swizzle row)
 constexpr int kTileM = 128;          // MMA M: rows of the operand on the M side
 constexpr int kMaxStages = 16;
+// Weight bytes per CTA that a dense launch fetches into L2 before
+// griddepcontrol.wait: 128 KB, or 64 KB when two CTAs share an SM (the
+// next launch's CTAs are then resident from this launch's start, and a
+// larger early fetch competes with this launch's stream).  Measured on the
+// small-M weight-streaming shapes against 32 KB to 1 MB.
+constexpr int kEarlyPrefetchBytes = 128 * 1024;
+inline int early_prefetch_kb(int weight_bytes_per_kb, bool shared_sm)
+{
+    const int kb = (shared_sm ? kEarlyPrefetchBytes / 2 : kEarlyPrefetchBytes) / weight_bytes_per_kb;
+    return kb > 1 ? kb : 1;
+}
 constexpr int kMaxGroups = 1024;
 constexpr int kThreads = 192;        // warp 0 loader, warp 1 MMA issuer, warps 2-5 epilogue
 constexpr int kThreadsTmemScaled = 352;  // block-scaled instantiations: + warp 6, second MMA issuer,
@@ -77,6 +88,9 @@ struct GemmArgs {
                                // each with its own accumulators, alternating K blocks
     int32_t tok_box;           // swap kernel: token rows per TMA box of a chunk (a multiple of 16
                                // dividing tile_n; the host encodes the token map with this box)
+    int32_t prefetch_kb;       // dense problems (one group, no masked_m, no offsets): K blocks of
+                               // this CTA's first work fetched into L2 before griddepcontrol.wait,
+                               // so that they stream while the previous launch drains; 0: none
     int32_t acc_bufs;          // block-scaled tile kernels: accumulator buffers per issuer (0 or 2:
                                // two; 1: one, when two issuers' four or a 256-wide tile's two
                                // accumulators and the scale sets do not fit in TMEM)

@@ -90,6 +90,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, uint3
                  : "memory");
 }
 
+// 3-D tiled prefetch of one box into L2: no shared memory, no completion.
+// L2 is the point of coherence for global memory, so a prefetch issued
+// before griddepcontrol.wait cannot make a later load see stale data.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void *map, int32_t c0, int32_t c1, int32_t c2)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(c0),
+                 "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 // Same, with an L2 eviction-priority policy (createpolicy result).
 __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *map, uint32_t bar,
                                                  int32_t c0, int32_t c1, int32_t c2,

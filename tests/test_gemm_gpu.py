@@ -380,6 +380,35 @@ def test_swap_token_box_sizes(box):
     check_dense(101, 1536, 1024, flags=ON | fp8g.NO_SHARE_SM | fp8g.TOKEN_BOX(box), seed=800 + box)
 
 
+@pytest.mark.parametrize("M2,flags", [(8, AUTO), (64, AUTO), (32, OFF)])
+def test_weights_written_by_the_previous_launch_are_seen(M2, flags):
+    # GEMM 1 writes its BF16 output into the bytes GEMM 2 then reads as FP8
+    # weights, launched right before it on the same stream.  Dense launches
+    # fetch weights into L2 before waiting for the previous launch; the
+    # product must still use what GEMM 1 wrote, never the stale contents.
+    # GEMM 1 gathers finite E4M3 values (one-hot A rows times B1), so D1 is
+    # exact and its bytes are finite E4M3 codes.
+    N2, K2 = 2048, 4096
+    M1, N1, K1 = N2, K2 // 2, 32
+    A1 = np.zeros((M1, K1), np.uint8)
+    A1[np.arange(M1), np.arange(M1) % K1] = 0x38            # 1.0
+    B1 = synth.normal_fp8((N1, K1), 951, 0.0, 1.0, E4)
+    A2 = synth.normal_fp8((M2, K2), 952, 0.0, 1.0, E4)
+    D1 = torch.full((M1, N1), 1.5, dtype=torch.bfloat16, device="cuda:0")   # stale bytes 0x3F, 0xC0
+    a1, b1, a2 = dev(A1), dev(B1), dev(A2)
+    torch.cuda.synchronize()
+    fp8g.fp8_gemm_nt(a1, b1, D=D1, a_dtype=E4, b_dtype=E4)
+    D2 = fp8g.fp8_gemm_nt(a2, D1.view(torch.uint8), a_dtype=E4, b_dtype=E4, flags=flags)
+    torch.cuda.synchronize()
+    assert_status_ok()
+    B2 = D1.view(torch.uint8).cpu().numpy()
+    ref1, _ = oracle.gemm_nt(A1, B1, E4, E4)
+    assert np.array_equal(B2.view(np.uint16), ref1), "GEMM 1 output"
+    ref, absdot = oracle.gemm_nt(A2, B2, E4, E4)
+    ok, rep = oracle.check_bf16(bits(D2), ref, absdot)
+    assert ok, rep
+
+
 def test_share_sm_mode_grouped():
     mm = [0, 5, 32, 17, 1, 64]
     grouped_case(len(mm), 64, 512, 1024, mm, ON | fp8g.SHARE_SM, 32, seed=171)
