@@ -312,12 +312,16 @@ bool swap_beats_token_tiles(int64_t G, int64_t M, int64_t N, int64_t K, int sms)
 // plain chunks of 32 tokens (masked decode 142.0 vs 144.5 us with one
 // 32-row box), one box of the whole chunk for larger chunks (64 tokens,
 // N=7168, K=16384: 32.9 -> 28.4 us) and for block-scaled chunks (masked
-// decode 162.6 -> 141.3 us).
-int swap_token_box(int64_t cap, bool block_scaled, uint32_t flags)
+// decode 162.6 -> 141.3 us).  A dense problem whose tokens fit one chunk
+// (dense_rows > 0) loads exactly its rows in one box: rows of a box past
+// the tensor's end cost the copy engine time to fill.
+int swap_token_box(int64_t cap, bool block_scaled, uint32_t flags, int64_t dense_rows)
 {
     const int override_rows = static_cast<int>((flags >> 24) & 15u) * 16;   // FP8G_TOKEN_BOX(n)
     if (override_rows > 0 && cap % override_rows == 0)
         return override_rows;
+    if (dense_rows > 0 && dense_rows <= cap)
+        return static_cast<int>(dense_rows);
     if (block_scaled || cap > 32)
         return static_cast<int>(cap);
     return 16;
@@ -488,7 +492,7 @@ int launch(const Problem &p, cudaStream_t stream)
         if (grid <= 0)
             return FP8G_OK;
         args.tile_n = static_cast<int32_t>(cap);
-        args.tok_box = swap_token_box(cap, p.sf_k != 0, p.flags);
+        args.tok_box = swap_token_box(cap, p.sf_k != 0, p.flags, dense ? p.rows_a : 0);
         args.stage_bytes = static_cast<int32_t>(kTileM * kBlockK + cap * kBlockK);
         // Co-residency: with at most 128 tokens per chunk the accumulators fit
         // 256 TMEM columns; capping shared memory at half the SM lets the next
@@ -688,7 +692,9 @@ int launch(const Problem &p, cudaStream_t stream)
     // while the weight tiles stream past them.
     const int64_t band = (48ll << 20) / (kTileM * p.K);
     args.raster_band = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(band, m_tiles)));
-    if (!make_map(&tm0, p.A, p.K, p.rows_a, p.group_offsets ? 1 : p.G, kTileM) ||
+    args.a_box_rows = dense && p.rows_a < kTileM ? static_cast<int32_t>(p.rows_a) : 0;
+    if (!make_map(&tm0, p.A, p.K, p.rows_a, p.group_offsets ? 1 : p.G,
+                  args.a_box_rows ? static_cast<uint32_t>(args.a_box_rows) : kTileM) ||
         !make_map(&tm1, p.B, p.K, p.N, p.G, static_cast<uint32_t>(tile_n)))
         return FP8G_ERR_CUDA;
     if (p.sf_k) {

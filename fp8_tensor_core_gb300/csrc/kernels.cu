@@ -746,7 +746,12 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int n_tiles = ceil_div(a.n, a.tile_n);
     const uint32_t a_bytes = kTileM * kBlockK;                  // 16 KB A box
-    const uint32_t tx_bytes = a_bytes + static_cast<uint32_t>(a.tile_n) * kBlockK;
+    // A dense problem of fewer than 128 tokens loads only its rows (a box
+    // reaching past the tensor costs the copy engine time for every row it
+    // fills); the MMA's other A rows read stale stage bytes and feed only
+    // accumulator rows that are never stored.
+    const uint32_t a_box_bytes = a.a_box_rows ? static_cast<uint32_t>(a.a_box_rows) * kBlockK : a_bytes;
+    const uint32_t tx_bytes = a_box_bytes + static_cast<uint32_t>(a.tile_n) * kBlockK;
     const uint32_t sf_bytes = 4u * static_cast<uint32_t>(kTileM + a.tile_n);
     // Accumulator spacing in TMEM: 256 columns, or tile_n when the block-scale
     // sets follow the accumulators.  With block scales and two MMA issuers,
@@ -1846,9 +1851,10 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
         SwapSeg x;
         while (!aborted && next_seg(wk, x)) {
             // Token rows in TMA boxes of tok_box rows, enough boxes to cover
-            // the MMA's n_mma rows (rows past the valid tokens are loaded and
-            // never used).
-            const int n_load = ((x.n_mma + a.tok_box - 1) / a.tok_box) * a.tok_box;
+            // the valid tokens.  Rows past them up to the MMA's n_mma hold
+            // whatever the stage held before; they only reach accumulator
+            // columns that are never stored.
+            const int n_load = ((x.n_tok + a.tok_box - 1) / a.tok_box) * a.tok_box;
             const uint32_t tx = w_bytes + static_cast<uint32_t>(n_load) * kBlockK;
             for (int kb = x.kb0; kb < x.kb1; ++kb) {
                 if (!warp_wait(smem_addr(&ctl.empty[stage]), phase ^ 1u, ctl, a.timeout_ns,

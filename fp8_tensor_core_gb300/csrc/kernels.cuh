@@ -87,10 +87,13 @@ struct GemmArgs {
     int32_t dual_mma;          // block-scaled SwapAB / single-SM kernels: two MMA-issuing threads,
                                // each with its own accumulators, alternating K blocks
     int32_t tok_box;           // swap kernel: token rows per TMA box of a chunk (a multiple of 16
-                               // dividing tile_n; the host encodes the token map with this box)
+                               // dividing tile_n, or a dense problem's whole token count; the host
+                               // encodes the token map with this box)
     int32_t prefetch_kb;       // dense problems (one group, no masked_m, no offsets): K blocks of
                                // this CTA's first work fetched into L2 before griddepcontrol.wait,
                                // so that they stream while the previous launch drains; 0: none
+    int32_t a_box_rows;        // token-tile kernel: A rows per TMA box (the host encodes the A map with
+                               // it); 0: 128.  Fewer only for dense problems of fewer rows
     int32_t acc_bufs;          // block-scaled tile kernels: accumulator buffers per issuer (0 or 2:
                                // two; 1: one, when two issuers' four or a 256-wide tile's two
                                // accumulators and the scale sets do not fit in TMEM)

@@ -185,7 +185,7 @@ extern "C" int fp8_gemm_nt_noalloc(const void *A, const void *B, void *D, int64_
     args.workspace = reinterpret_cast<float *>(base + counter_span);
 
     CUtensorMap tm_w, tm_t;
-    args.tok_box = cap > 32 ? static_cast<int32_t>(cap) : 16;   // as fp8_gemm_nt's SwapAB path
+    args.tok_box = static_cast<int32_t>(M);   // one box of exactly the tokens, as fp8_gemm_nt's SwapAB path
     if (!encode(&tm_w, B, K, N, kTileM) || !encode(&tm_t, A, K, M, static_cast<uint32_t>(args.tok_box)))
         return FP8G_ERR_CUDA;
     args.prefetch_kb = early_prefetch_kb(kTileM * kBlockK, false);
