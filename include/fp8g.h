@@ -94,7 +94,11 @@ typedef enum {
 /*   FP8G_NO_PDL       launch without programmatic dependent launch (by
  *                     default a launch may begin its set-up while the
  *                     previous launch in the stream finishes; it waits for
- *                     that launch before touching global memory)           */
+ *                     that launch before any load or store of its operands.
+ *                     A dense launch may issue L2 prefetches of its first B
+ *                     tiles before that wait: L2 is coherent, so the loads
+ *                     after the wait still see what the previous launch
+ *                     wrote)                                                */
 #define FP8G_NO_PDL 0x400u
 /*   FP8G_PAIR_TILES   dense problems with more than 128 token rows: always use
  *                     SM-pair tiles (the automatic choice skips them for
