@@ -96,6 +96,10 @@ def test_masked_moe_decode_every_valid_row_and_untouched_padding():
 
 SMALLM = ["smallm:%d:%s:%s" % (m, nk, mode) for nk in ("24576:1536", "7168:16384")
           for m in (1, 8, 16, 32, 64) for mode in ("swap", "noswap")]
+# token counts off the 16-row grid (TMA boxes of exactly the rows) and the
+# library's own choice
+SMALLM += ["smallm:17:7168:16384:swap", "smallm:33:24576:1536:noswap", "smallm:100:24576:1536:noswap",
+           "smallm:5:7168:16384", "smallm:64:24576:1536"]
 
 
 @pytest.mark.parametrize("name", SMALLM)
