@@ -232,8 +232,11 @@ int pick_tile_n(int64_t m_tiles_total, int64_t N, int sms, int max_tn = 256)
 }
 
 // Pair-kernel plan: N tile and work split, from a cost model in units of
-// "one K block of a 256-wide tile".  Narrower tiles move more operand bytes
-// per multiply (measured: 224 wide ~7 %, 192 wide ~18 % slower per K block);
+// "one K block of a 256-wide tile".  Narrower tiles pay a fixed cost per MMA
+// instruction over fewer columns (measured per unit of width: 192 wide
+// ~18 % slower per K block; a 224-wide K block takes as long as a 256-wide
+// one -- 4096^3 in four waves of either: 48.2 vs 47.8 us at 2.07 GHz, and
+// 50.2 vs 49.5 us under the sustained power cap);
 // whole tiles pay for the last partial wave of pairs.  Stream-K for the last
 // wave is only used when FP8G_STREAM_K asks for it: reducing 256-wide FP32
 // partial tiles (128 KB per CTA per contributor) is latency-bound and cost
@@ -246,7 +249,7 @@ struct PairPlan {
 PairPlan plan_pair(int64_t m_tiles2, int64_t N, int num_kb, int pairs, uint32_t flags, int max_tn = 256)
 {
     static const int cands[] = {256, 224, 192, 160, 128};
-    static const double cost_per_kb[] = {1.0, 1.07, 1.18, 1.30, 1.45};
+    static const double cost_per_kb[] = {1.0, 1.15, 1.18, 1.30, 1.45};
     PairPlan best{max_tn, false};
     double best_cost = 1e300;
     const int tn_override = static_cast<int>((flags >> 16) & 15u);
