@@ -380,6 +380,23 @@ def test_swap_token_box_sizes(box):
     check_dense(101, 1536, 1024, flags=ON | fp8g.NO_SHARE_SM | fp8g.TOKEN_BOX(box), seed=800 + box)
 
 
+@pytest.mark.parametrize("M,flags", [(5, OFF), (5, ON), (21, ON), (100, OFF)])
+def test_few_tokens_after_nan_padded_launches(M, flags):
+    # Dense problems of few tokens load only their rows; the MMA's remaining
+    # rows read whatever earlier launches left in shared memory.  Fill it
+    # first with NaN token rows (masked padding over every SM), then check
+    # the valid outputs.
+    G, M_max, N, K = 32, 128, 512, 1024
+    A = np.full((G, M_max, K), 0x7F, np.uint8)
+    A[:, 0] = synth.normal_fp8((G, K), 961, 0.0, 0.5, E4)
+    B = synth.normal_fp8((G, N, K), 962, 0.0, 0.5, E4)
+    mm = np.ones(G, np.int32)
+    Dg = torch.empty((G, M_max, N), dtype=torch.bfloat16, device="cuda:0")
+    for mode in (ON, OFF):
+        fp8g.fp8_gemm_grouped_masked(dev(A), dev(B), dev(mm), D=Dg, max_m_hint=M_max, flags=mode | fp8g.WHOLE_TILES)
+    check_dense(M, 3072, 2048, flags=flags, seed=963 + M)
+
+
 @pytest.mark.parametrize("M2,flags", [(8, AUTO), (64, AUTO), (32, OFF)])
 def test_weights_written_by_the_previous_launch_are_seen(M2, flags):
     # GEMM 1 writes its BF16 output into the bytes GEMM 2 then reads as FP8
