@@ -393,7 +393,8 @@ def test_few_tokens_after_nan_padded_launches(M, flags):
     mm = np.ones(G, np.int32)
     Dg = torch.empty((G, M_max, N), dtype=torch.bfloat16, device="cuda:0")
     for mode in (ON, OFF):
-        fp8g.fp8_gemm_grouped_masked(dev(A), dev(B), dev(mm), D=Dg, max_m_hint=M_max, flags=mode | fp8g.WHOLE_TILES)
+        fp8g.fp8_gemm_grouped_masked(dev(A), dev(B), dev(mm), D=Dg, max_m_hint=M_max, a_dtype=E4, b_dtype=E4,
+                                     flags=mode | fp8g.WHOLE_TILES)
     check_dense(M, 3072, 2048, flags=flags, seed=963 + M)
 
 
