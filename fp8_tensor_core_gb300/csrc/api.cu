@@ -28,10 +28,11 @@ namespace {
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 constexpr int kMaxDevices = 64;
-// SwapAB is chosen automatically when a problem has at most this many
-// token rows per group (the weights then fill the 128-row MMA side and the
-// tokens a narrow runtime N).
-constexpr int64_t kSwapAutoMaxTokens = 128;
+// SwapAB is weighed against token tiles (a cost model) when a problem has
+// at most this many token rows per group (the weights then fill the 128-row
+// MMA side and the tokens a narrow runtime N).
+constexpr int64_t kSwapAutoMaxTokens = 128;        // dense and block-scaled problems
+constexpr int64_t kSwapAutoMaxGroupTokens = 255;   // plain grouped problems
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
 std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
@@ -283,30 +284,36 @@ PairPlan plan_pair(int64_t m_tiles2, int64_t N, int num_kb, int pairs, uint32_t 
 }
 
 // SwapAB or 128-row token tiles, for G groups of (up to) M tokens each.
-// Both stream every weight byte once.  Token tiles: one CTA per weight tile,
-// so few tiles leave SMs idle and one SM streams at most ~55 GB/s; no
-// reduction.  SwapAB with stream-K keeps every SM streaming but pays a
-// partial-tile reduction, and its per-K-block MMA work grows with the tokens
-// (measured ~9.8 ns per K block per token on GB300).  Estimated times
-// (measured constants: 6.7 TB/s HBM, ~5 us and ~8 us fixed costs) pick the
-// faster.  Measured on GB300 for grouped shapes (16 or 32 experts, N x K of
-// 4096 x 7168 or 7168 x 2048): token tiles won at every token count from 8
-// to 256; SwapAB wins when the tiles are too few to fill the GPU (dense
-// small-M, few groups).
+// Both stream every weight byte once from HBM.  Token tiles: one CTA per
+// weight tile, so few tiles leave SMs idle and one SM streams at most ~55
+// GB/s (a group's further token tiles find the weights in L2), and every
+// token tile runs 128-row MMAs however few rows are valid.  SwapAB with
+// stream-K keeps every SM streaming; per K block of 128 it pays ~316 ns
+// plus ~0.8 ns per token (rounded to 16) in MMA issue, plus a partial-tile
+// reduction that grows with the tokens and with fewer K blocks per tile.
+// Constants measured on GB300 at 2.07 GHz: groups of 32 / 96 / 160 tokens
+// (16 groups, N x K of 4096 x 7168 and 7168 x 2048), the masked decode and
+// the dense small-M shapes; the estimates pick the faster kernel on all of
+// them (SwapAB at 16 x 160 tokens, N = 4096, K = 7168: 92.3 vs 102.7 us;
+// token tiles at 32 and 96 tokens and at N = 7168, K = 2048).
 bool swap_beats_token_tiles(int64_t G, int64_t M, int64_t N, int64_t K, int sms)
 {
     const double bytes = static_cast<double>(G) * (static_cast<double>(N) * K + static_cast<double>(M) * K +
                                                    2.0 * M * N);
-    const double hbm = 6.7e12, per_sm = 55e9;
+    const double hbm = 6.7e12, per_sm = 55e9, tensor = 2.5e15;
     const int64_t m_tiles = G * cdiv(M, kTileM);
     const int tn = pick_tile_n(m_tiles, N, sms);
-    const int64_t tiles = m_tiles * cdiv(N, tn);
-    const double per_cta = static_cast<double>(tn) * K;
-    const double t_tiles =
-        std::max(bytes / hbm, per_cta * static_cast<double>(cdiv(tiles, sms)) / per_sm) + 5e-6;
-    const double kblocks = static_cast<double>(G) * cdiv(N, kTileM) * cdiv(K, kBlockK);
-    const double t_mma = kblocks * static_cast<double>(cdiv(M, 16) * 16) * 9.8e-9 / sms;
-    const double t_swap = std::max(bytes / hbm, t_mma) + 8e-6;
+    const int64_t weight_tiles = G * cdiv(N, tn);
+    const double t_tiles = std::max({bytes / hbm,
+                                     static_cast<double>(tn) * K * static_cast<double>(cdiv(weight_tiles, sms)) /
+                                         per_sm,
+                                     2.0 * static_cast<double>(m_tiles) * kTileM * N * K / tensor}) +
+                           5e-6;
+    const double tok = static_cast<double>(cdiv(M, 16) * 16);
+    const double num_kb = static_cast<double>(cdiv(K, kBlockK));
+    const double kb_per_sm = static_cast<double>(G) * cdiv(N, kTileM) * num_kb / sms;
+    const double t_swap =
+        std::max(bytes / hbm, kb_per_sm * (316e-9 + 0.8e-9 * tok)) + 8e-6 + 0.06e-6 * tok * 16.0 / num_kb;
     return t_swap < t_tiles;
 }
 
@@ -443,7 +450,14 @@ int launch(const Problem &p, cudaStream_t stream)
     const uint32_t mode = p.flags & FP8G_SWAP_MASK;
     if (mode == 3u)
         return FP8G_ERR_INVALID_ARG;
-    bool swap = mode == FP8G_SWAP_ON || (mode == FP8G_SWAP_AUTO && p.token_hint <= kSwapAutoMaxTokens);
+    // Plain grouped problems of fewer than 256 tokens per group (the SM-pair
+    // kernel's tile) weigh SwapAB against token tiles; dense and block-scaled
+    // ones only up to 128 tokens (above that the SM-pair or token-tile
+    // kernels take them).
+    const bool grouped_problem = p.G > 1 || p.masked_m || p.group_offsets;
+    bool swap = mode == FP8G_SWAP_ON ||
+                (mode == FP8G_SWAP_AUTO &&
+                 p.token_hint <= (grouped_problem && !p.sf_k ? kSwapAutoMaxGroupTokens : kSwapAutoMaxTokens));
     if (swap && mode == FP8G_SWAP_AUTO)
         swap = swap_beats_token_tiles(p.G, p.token_hint, p.N, p.K, info.sms);
     const int num_kb = static_cast<int>(cdiv(p.K, kBlockK));
