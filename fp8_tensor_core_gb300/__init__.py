@@ -84,6 +84,23 @@ def fp8g_init(max_tiles: int = 0) -> None:
         raise Fp8gError(rc, "fp8g_init")
 
 
+KERNEL_TOKEN_TILES, KERNEL_SM_PAIRS, KERNEL_SWAP_AB = 0, 1, 2
+LAYOUT_DENSE, LAYOUT_MASKED, LAYOUT_CONTIGUOUS = 0, 1, 2
+
+
+def fp8g_describe_plan(layout: int, G: int, rows: int, N: int, K: int, token_hint: int = 0,
+                       sf_group_k: int = 0, flags: int = 0, sms: int = 0, smem_optin: int = 0) -> dict:
+    """The launch the library would make for a problem (kernel, tile,
+    stages, split, issuers, SM sharing, token rows per copy, grid), without
+    touching memory; sms / smem_optin 0 plan for the current device."""
+    out = _lib.Plan()
+    rc = _lib.load().fp8g_describe_plan(int(layout), int(G), int(rows), int(N), int(K), int(token_hint),
+                                        int(sf_group_k), int(flags), int(sms), int(smem_optin), ctypes.byref(out))
+    if rc != OK:
+        raise Fp8gError(rc, "fp8g_describe_plan")
+    return {name: int(getattr(out, name)) for name, _ in _lib.Plan._fields_}
+
+
 def fp8g_shutdown() -> None:
     """Free the library's stream-K workspace on every device."""
     rc = _lib.load().fp8g_shutdown()

@@ -31,6 +31,12 @@ class Epilogue(ctypes.Structure):
                 ("bias", ctypes.c_void_p), ("activation", ctypes.c_int32), ("round_mode", ctypes.c_int32)]
 
 
+class Plan(ctypes.Structure):
+    """fp8g_plan: the launch the library would make for a problem."""
+    _fields_ = [(name, ctypes.c_int32) for name in ("kernel", "tile_n", "stages", "stream_k", "mma_issuers",
+                                                     "shared_sm", "token_box", "grid")]
+
+
 _scales_p = ctypes.POINTER(Scales)
 _epi_p = ctypes.POINTER(Epilogue)
 SIGNATURES = {
@@ -69,6 +75,8 @@ SIGNATURES = {
                                            ctypes.c_int, ctypes.c_int, _c_void_p]),
     "fp8g_get_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), _c_void_p]),
     "fp8g_init": (ctypes.c_int, [_i64]),
+    "fp8g_describe_plan": (ctypes.c_int, [ctypes.c_int, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.c_uint32,
+                                          ctypes.c_int, ctypes.c_int, ctypes.POINTER(Plan)]),
     "fp8g_shutdown": (ctypes.c_int, []),
     "fp8g_set_wait_timeout_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
     "fp8g_status_string": (ctypes.c_char_p, [ctypes.c_int]),

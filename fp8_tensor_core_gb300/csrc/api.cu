@@ -439,12 +439,30 @@ int check_scales(const float *sa, int64_t sa_len, const float *sb, int64_t sb_le
     return FP8G_OK;
 }
 
-int launch(const Problem &p, cudaStream_t stream)
+void describe_as(fp8g_plan *out, int kernel, int tile_n, const GemmArgs &args, bool stream_k, bool shared_sm,
+                 int token_box, int grid)
+{
+    out->kernel = kernel;
+    out->tile_n = tile_n;
+    out->stages = args.stages;
+    out->stream_k = stream_k ? 1 : 0;
+    out->mma_issuers = args.dual_mma ? 2 : 1;
+    out->shared_sm = shared_sm ? 1 : 0;
+    out->token_box = token_box;
+    out->grid = grid;
+}
+
+// Plans and enqueues the launch for `p`.  With `forced`, plans for that
+// device instead of the current one; with `describe`, fills it and returns
+// before anything is allocated, encoded or enqueued.
+int launch(const Problem &p, cudaStream_t stream, const DeviceInfo *forced = nullptr, fp8g_plan *describe = nullptr)
 {
     int dev = 0;
     DeviceInfo info;
-    int st = current_device(&dev, &info);
-    if (st != FP8G_OK)
+    int st = FP8G_OK;
+    if (forced)
+        info = *forced;
+    else if ((st = current_device(&dev, &info)) != FP8G_OK)
         return st;
 
     const uint32_t mode = p.flags & FP8G_SWAP_MASK;
@@ -554,6 +572,12 @@ int launch(const Problem &p, cudaStream_t stream)
             args.tmem_cols = 512;
         }
         args.k_splits = whole_tiles ? 1 : 0;
+        args.prefetch_kb = dense ? early_prefetch_kb(kTileM * kBlockK, share_sm) : 0;
+        if (describe) {
+            describe_as(describe, FP8G_KERNEL_SWAP_AB, static_cast<int>(cap), args, !whole_tiles, share_sm,
+                        args.tok_box, grid);
+            return FP8G_OK;
+        }
         if (!whole_tiles) {
             st = ensure_workspace(dev, swap_partials_bytes(grid, static_cast<int>(cap)),
                                   swap_counter_bytes(tiles_upper), &args.workspace, &args.counters);
@@ -572,7 +596,6 @@ int launch(const Problem &p, cudaStream_t stream)
             tm2 = tm0;
             tm3 = tm1;
         }
-        args.prefetch_kb = dense ? early_prefetch_kb(kTileM * kBlockK, share_sm) : 0;
         return launch_gemm_swap(tm0, tm1, tm2, tm3, args, grid, smem_request, stream) == cudaSuccess
                    ? FP8G_OK
                    : FP8G_ERR_CUDA;
@@ -634,6 +657,11 @@ int launch(const Problem &p, cudaStream_t stream)
         }
         const int64_t band = (48ll << 20) / (2 * kTileM * p.K);
         args.raster_band = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(band, m_tiles2)));
+        const int grid = 2 * static_cast<int>(std::min<int64_t>(plan.stream_k ? units * num_kb : units, pairs));
+        if (describe) {
+            describe_as(describe, FP8G_KERNEL_SM_PAIRS, tile_n, args, plan.stream_k, false, kTileM, grid);
+            return FP8G_OK;
+        }
         if (!make_map(&tm0, p.A, p.K, p.rows_a, p.group_offsets ? 1 : p.G, kTileM) ||
             !make_map(&tm1, p.B, p.K, p.N, p.G, static_cast<uint32_t>(tile_n / 2)))
             return FP8G_ERR_CUDA;
@@ -645,7 +673,6 @@ int launch(const Problem &p, cudaStream_t stream)
             tm2 = tm0;
             tm3 = tm1;
         }
-        const int grid = 2 * static_cast<int>(std::min<int64_t>(plan.stream_k ? units * num_kb : units, pairs));
         // (stream-K implies units is not a multiple of the pairs, so every
         // pair of the grid exists for the remainder's partition)
         if (plan.stream_k) {
@@ -710,6 +737,13 @@ int launch(const Problem &p, cudaStream_t stream)
     const int64_t band = (48ll << 20) / (kTileM * p.K);
     args.raster_band = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(band, m_tiles)));
     args.a_box_rows = dense && p.rows_a < kTileM ? static_cast<int32_t>(p.rows_a) : 0;
+    const int grid = static_cast<int>(std::min<int64_t>(units_upper, info.sms));
+    args.prefetch_kb = dense ? early_prefetch_kb(static_cast<int>(tile_n) * kBlockK, false) : 0;
+    if (describe) {
+        describe_as(describe, FP8G_KERNEL_TOKEN_TILES, tile_n, args, false, false,
+                    args.a_box_rows ? args.a_box_rows : kTileM, grid);
+        return FP8G_OK;
+    }
     if (!make_map(&tm0, p.A, p.K, p.rows_a, p.group_offsets ? 1 : p.G,
                   args.a_box_rows ? static_cast<uint32_t>(args.a_box_rows) : kTileM) ||
         !make_map(&tm1, p.B, p.K, p.N, p.G, static_cast<uint32_t>(tile_n)))
@@ -722,10 +756,8 @@ int launch(const Problem &p, cudaStream_t stream)
         tm2 = tm0;
         tm3 = tm1;
     }
-    const int grid = static_cast<int>(std::min<int64_t>(units_upper, info.sms));
     if (grid <= 0)
         return FP8G_OK;
-    args.prefetch_kb = dense ? early_prefetch_kb(static_cast<int>(tile_n) * kBlockK, false) : 0;
     return launch_gemm_mn(tm0, tm1, tm2, tm3, args, grid, static_cast<size_t>(info.smem_optin), stream) ==
                    cudaSuccess
                ? FP8G_OK
@@ -999,6 +1031,41 @@ extern "C" int fp8g_shutdown(void)
     else
         cudaGetLastError();
     return rc;
+}
+
+extern "C" int fp8g_describe_plan(int layout, int64_t G, int64_t rows, int64_t N, int64_t K, int64_t token_hint,
+                                  int sf_group_k, uint32_t flags, int sms, int smem_optin, fp8g_plan *out)
+{
+    if (!out)
+        return FP8G_ERR_INVALID_ARG;
+    std::memset(out, 0, sizeof(*out));
+    if (layout < 0 || layout > 2 || G <= 0 || rows <= 0 || N <= 0 || K <= 0 || rows > kMaxDim || N > kMaxDim ||
+        K > kMaxDim || K % 16 != 0 || N % 8 != 0 || token_hint < 0 || token_hint > rows ||
+        (layout == 0 && G != 1) || sms < 0 || smem_optin < 0 || (sms == 0) != (smem_optin == 0) ||
+        (sf_group_k != 0 && sf_group_k != 32 && sf_group_k != 128))
+        return FP8G_ERR_INVALID_ARG;
+    if (G > kMaxGroups || G * N > kMaxDim || (layout == 1 && G * rows > kMaxDim) || (layout == 2 && sf_group_k))
+        return FP8G_ERR_UNSUPPORTED;
+    // Planning reads no operand: the layout pointers only mark the layout.
+    static const int32_t kLayoutMark[1] = {0};
+    const int64_t hint = layout == 0 ? rows : (token_hint > 0 ? token_hint : rows);
+    Problem p{nullptr, nullptr, nullptr, layout == 1 ? kLayoutMark : nullptr, layout == 2 ? kLayoutMark : nullptr,
+              G, rows, N, K, hint, FP8G_E4M3, FP8G_E4M3, flags};
+    p.sf_k = sf_group_k ? static_cast<int>(kBlockK / sf_group_k) : 0;
+    DeviceInfo info;
+    if (sms > 0) {
+        info.ready = true;
+        info.sms = sms;
+        info.smem_optin = smem_optin;
+        info.cc_major = 10;
+        info.cc_minor = 3;
+    } else {
+        int dev = 0;
+        const int st = current_device(&dev, &info);
+        if (st != FP8G_OK)
+            return st;
+    }
+    return launch(p, nullptr, &info, out);
 }
 
 extern "C" uint64_t fp8g_set_wait_timeout_ns(uint64_t ns)

@@ -409,6 +409,40 @@ uint64_t fp8g_set_wait_timeout_ns(uint64_t ns);
 int fp8_gemm_nt_noalloc(const void *A, const void *B, void *D, int64_t M, int64_t N,
                         int64_t K, int a_dtype, int b_dtype, cudaStream_t stream);
 
+/*
+ * fp8g_describe_plan -- the launch the library would make for a problem,
+ * without touching memory or enqueueing anything (the kernel choice of
+ * FP8G_SWAP_AUTO and of the tile planners, for inspection and tuning).
+ *   layout      0: dense fp8_gemm_nt (G must be 1); 1: masked grouped
+ *               (rows = M_max); 2: contiguous grouped (rows = M_total).
+ *   G, rows, N, K, token_hint, flags: as the corresponding call takes them
+ *               (token_hint: max_m_hint of the masked call, 0 = rows; the
+ *               contiguous layout uses rows / G, the dense one rows).
+ *   sf_group_k  0 (no block scales), 32 or 128: as the block-scaled calls.
+ *   sms, smem_optin: the device to plan for (SM count, opt-in shared memory
+ *               per block in bytes); both 0: the current device.
+ *   out         caller-owned; filled on FP8G_OK.
+ * Returns FP8G_OK, FP8G_ERR_INVALID_ARG (null out, sizes <= 0, bad layout,
+ * flags or group size), FP8G_ERR_UNSUPPORTED, or a device-query error
+ * when sms and smem_optin are 0.  Shape limits of the GEMM calls (K % 16,
+ * N % 8) are checked as they are there.
+ */
+#define FP8G_KERNEL_TOKEN_TILES 0   /* 128-row token tiles on one SM each */
+#define FP8G_KERNEL_SM_PAIRS 1      /* 256-row token tiles on an SM pair (cta_group::2) */
+#define FP8G_KERNEL_SWAP_AB 2       /* weights on the MMA's M side, tokens on a runtime N */
+typedef struct fp8g_plan {
+    int32_t kernel;      /* FP8G_KERNEL_* */
+    int32_t tile_n;      /* N tile (token tiles, SM pairs) or token chunk (SwapAB) */
+    int32_t stages;      /* shared-memory pipeline stages */
+    int32_t stream_k;    /* 1: K blocks split evenly over the CTAs; 0: whole tiles */
+    int32_t mma_issuers; /* threads issuing MMAs per tile: 1 or 2 */
+    int32_t shared_sm;   /* 1: half the shared memory, two CTAs may share an SM */
+    int32_t token_box;   /* token rows per TMA copy (SwapAB; token tiles: A rows) */
+    int32_t grid;        /* CTAs launched */
+} fp8g_plan;
+int fp8g_describe_plan(int layout, int64_t G, int64_t rows, int64_t N, int64_t K, int64_t token_hint,
+                       int sf_group_k, uint32_t flags, int sms, int smem_optin, fp8g_plan *out);
+
 /* Human-readable name of a status code (static string). */
 const char *fp8g_status_string(int code);
 

@@ -139,3 +139,73 @@ def test_field_flags_do_not_overlap_the_single_bit_flags():
             assert f & g == 0
     assert fp8g.TOKEN_BOX(48) == 3 << 24 and fp8g.TOKEN_BOX(0) == 0
 
+
+
+# ---- the plan query (no device needed when the device is described) ------------------
+
+GB300 = dict(sms=152, smem_optin=232448)
+
+
+def _plan(layout, G, rows, N, K, hint=0, sf=0, flags=0):
+    import fp8_tensor_core_gb300 as fp8g
+    return fp8g.fp8g_describe_plan(layout, G, rows, N, K, hint, sf, flags, **GB300)
+
+
+@pytest.mark.parametrize("args,expect", [
+    # dense 4096^3: SM-pair tiles 256 wide, whole tiles
+    ((0, 1, 4096, 4096, 4096), dict(kernel=1, tile_n=256, stream_k=0)),
+    # small-M weight streaming: token tiles at N=24576, K=1536 (A box of the one row) ...
+    ((0, 1, 1, 24576, 1536), dict(kernel=0, tile_n=192, token_box=1, grid=128)),
+    ((0, 1, 33, 24576, 1536), dict(kernel=0, token_box=33)),
+    # ... SwapAB stream-K at N=7168, K=16384, sharing the SM up to 16 tokens
+    ((0, 1, 16, 7168, 16384), dict(kernel=2, tile_n=16, stream_k=1, shared_sm=1, token_box=16, grid=152)),
+    ((0, 1, 5, 7168, 16384), dict(kernel=2, tile_n=16, shared_sm=1, token_box=5)),
+    ((0, 1, 64, 7168, 16384), dict(kernel=2, tile_n=64, shared_sm=0, token_box=64)),
+    # masked MoE decode (32 experts, up to 32 tokens): token tiles; forced SwapAB: 16-row boxes
+    ((1, 32, 128, 4096, 7168, 32), dict(kernel=0)),
+    ((1, 32, 128, 4096, 7168, 32, 0, 1), dict(kernel=2, tile_n=32, token_box=16, stream_k=1)),
+    # 16 experts: SwapAB at 160 tokens for N=4096, K=7168, token tiles at 96 and for N=7168, K=2048
+    ((1, 16, 160, 4096, 7168, 160), dict(kernel=2, tile_n=160, token_box=160)),
+    ((1, 16, 96, 4096, 7168, 96), dict(kernel=0)),
+    ((1, 16, 160, 7168, 2048, 160), dict(kernel=0)),
+    # contiguous groups of 256 tokens: SM pairs
+    ((2, 32, 8192, 4096, 7168), dict(kernel=1, tile_n=256)),
+    # block scales: single-SM tiles 224 wide (256 wide from 48 K blocks); SwapAB with two issuers
+    ((0, 1, 4096, 4096, 4096, 0, 128), dict(kernel=0, tile_n=224, mma_issuers=1)),
+    ((0, 1, 8192, 7168, 18432, 0, 128), dict(kernel=0, tile_n=256)),
+    ((1, 32, 128, 4096, 7168, 32, 128, 1), dict(kernel=2, tile_n=32, token_box=32, mma_issuers=2)),
+])
+def test_describe_plan_pins_the_automatic_choices(args, expect):
+    got = _plan(*args)
+    assert {k: got[k] for k in expect} == expect, got
+    assert got["stages"] >= 1 and 1 <= got["grid"] <= 152
+    if got["mma_issuers"] == 2:
+        assert got["stages"] % 2 == 0
+
+
+def test_describe_plan_follows_the_flags():
+    import fp8_tensor_core_gb300 as fp8g
+    assert _plan(0, 1, 16, 7168, 16384, flags=fp8g.NO_SHARE_SM)["shared_sm"] == 0
+    assert _plan(0, 1, 64, 7168, 16384, flags=fp8g.SWAP_OFF)["kernel"] == 0
+    assert _plan(0, 1, 4096, 4096, 4096, flags=fp8g.SINGLE_SM_TILES)["kernel"] == 0
+    assert _plan(0, 1, 4096, 4096, 4096, flags=fp8g.TILE_N(224))["tile_n"] == 224
+    assert _plan(0, 1, 4096, 4096, 4096, flags=fp8g.STAGES(3))["stages"] == 3
+    assert _plan(0, 1, 128, 4096, 4096, flags=fp8g.SWAP_ON | fp8g.TOKEN_BOX(32))["token_box"] == 32
+    assert _plan(0, 1, 64, 7168, 16384, flags=fp8g.WHOLE_TILES)["stream_k"] == 0
+
+
+@pytest.mark.parametrize("args,code", [
+    ((3, 1, 16, 4096, 4096, 0, 0, 0, 152, 232448), 1),      # no such layout
+    ((0, 2, 16, 4096, 4096, 0, 0, 0, 152, 232448), 1),      # dense takes one group
+    ((0, 1, 16, 4096, 4100, 0, 0, 0, 152, 232448), 1),      # K % 16
+    ((0, 1, 16, 4100, 4096, 0, 0, 0, 152, 232448), 1),      # N % 8
+    ((1, 4, 16, 4096, 4096, 32, 0, 0, 152, 232448), 1),     # hint above rows
+    ((0, 1, 16, 4096, 4096, 0, 64, 0, 152, 232448), 1),     # group size
+    ((0, 1, 16, 4096, 4096, 0, 0, 0, 152, 0), 1),           # half a device description
+    ((0, 1, 16, 4096, 4096, 0, 0, 3, 152, 232448), 1),      # swap mode 3
+    ((2, 4, 64, 4096, 4096, 0, 128, 0, 152, 232448), 3),    # block scales with the contiguous layout
+])
+def test_describe_plan_argument_errors(lib, args, code):
+    out = _lib.Plan()
+    assert lib.fp8g_describe_plan(*args, ctypes.byref(out)) == code
+    assert lib.fp8g_describe_plan(0, 1, 16, 4096, 4096, 0, 0, 0, 152, 232448, None) == 1
