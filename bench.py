@@ -226,6 +226,21 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+KERNEL_NAMES = {0: "k_gemm_mn", 1: "k_gemm_mn2", 2: "k_gemm_swap"}
+
+
+def planned_launch(w: Workload) -> dict:
+    """The launch the library makes for the workload on the current device
+    (kernel, tile, stages, split, issuers, SM sharing, token rows per copy,
+    grid), from its planner."""
+    import fp8_tensor_core_gb300 as fp8g
+    if w.kind == "dense":
+        return fp8g.fp8g_describe_plan(fp8g.LAYOUT_DENSE, 1, w.M, w.N, w.K, 0, w.gran or 0, w.flags)
+    if w.kind == "contig":
+        return fp8g.fp8g_describe_plan(fp8g.LAYOUT_CONTIGUOUS, w.G, w.G * w.M_max, w.N, w.K, w.hint, 0, w.flags)
+    return fp8g.fp8g_describe_plan(fp8g.LAYOUT_MASKED, w.G, w.M_max, w.N, w.K, w.hint, w.gran or 0, w.flags)
+
+
 def profiled_traffic(workload: str):
     """Per-launch DRAM bytes (read + write) of the dominant kernel from the
     committed ncu summary, valid only while the kernel sources are unchanged
@@ -646,12 +661,10 @@ def run_ours(args, w: Workload):
         unit = "GB/s"
         basis = "%s HBM copy bandwidth" % peak_src
     traffic = profiled_traffic(w.name)
-    kernel_name = "k_gemm_swap" if (w.flags & 3) == 1 or (w.kind == "masked" and w.M_max < 256) else \
-        "k_gemm_mn2/k_gemm_mn" if w.kind in ("contig", "masked") else \
-        ("k_gemm_mn2" if w.kind == "dense" and w.M > 128 and not (w.flags & 0x200) else "k_gemm_mn/k_gemm_swap (auto)")
-    kernel_name = getattr(w, "kernel", kernel_name)
+    plan = planned_launch(w)
+    kernel_name = KERNEL_NAMES[plan["kernel"]]
     roof = {"bound": w.bound, "achieved": achieved, "peak": peak, "unit": unit,
-            "frac": achieved / peak, "traffic": traffic, "kernel": kernel_name,
+            "frac": achieved / peak, "traffic": traffic, "kernel": kernel_name, "plan": plan,
             "peak_basis": basis, "algorithmic_flop": flops, "algorithmic_bytes": algo_bytes,
             "kernel_ms": kernel_ms_max}
     if w.bound == "tensor":
