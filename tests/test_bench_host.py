@@ -198,3 +198,20 @@ def test_block_scale_recipe():
     w32 = bench.make_workload("smallm:1:7168:16384:bs32")
     sc32 = bench.block_scales(w32)
     assert sc32["sf_a"].shape == (1, 16384 // 32, 16) and sc32["sf_b"].shape == (1, 512, 7168)
+
+
+def test_planned_launch_names_the_kernel(monkeypatch):
+    """The bench line's kernel comes from the library's planner (here for a
+    described GB300, so no device is needed)."""
+    from fp8_tensor_core_gb300 import build as cuda_build
+    import fp8_tensor_core_gb300 as fp8g
+    cuda_build.build()
+    real = fp8g.fp8g_describe_plan
+    monkeypatch.setattr(fp8g, "fp8g_describe_plan",
+                        lambda *a, **k: real(*a, sms=152, smem_optin=232448))
+    for name, kernel in [("dense4096", "k_gemm_mn2"), ("masked", "k_gemm_swap"), ("masked:noswap", "k_gemm_mn"),
+                         ("smallm:1:24576:1536", "k_gemm_mn"), ("smallm:16:7168:16384", "k_gemm_swap"),
+                         ("contig:32:256:4096:7168", "k_gemm_mn2"), ("dense4096:bs", "k_gemm_mn"),
+                         ("grouped:16:160:4096:7168:auto", "k_gemm_swap")]:
+        plan = bench.planned_launch(bench.make_workload(name))
+        assert bench.KERNEL_NAMES[plan["kernel"]] == kernel, (name, plan)
