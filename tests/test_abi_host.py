@@ -209,3 +209,17 @@ def test_describe_plan_argument_errors(lib, args, code):
     out = _lib.Plan()
     assert lib.fp8g_describe_plan(*args, ctypes.byref(out)) == code
     assert lib.fp8g_describe_plan(0, 1, 16, 4096, 4096, 0, 0, 0, 152, 232448, None) == 1
+
+
+def test_plan_struct_matches_the_header():
+    """The binding's fp8g_plan fields are the header's, in order, all int32."""
+    src = open(HEADER).read()
+    body = re.search(r"typedef struct fp8g_plan \{(.*?)\} fp8g_plan;", src, flags=re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = re.findall(r"int32_t\s+([a-z_]+);", body)
+    assert fields == [name for name, _ in _lib.Plan._fields_]
+    assert ctypes.sizeof(_lib.Plan) == 4 * len(fields)
+    import fp8_tensor_core_gb300 as fp8g
+    defs = dict(re.findall(r"#define FP8G_KERNEL_([A-Z_]+) ([0-9]+)", src))
+    assert (int(defs["TOKEN_TILES"]), int(defs["SM_PAIRS"]), int(defs["SWAP_AB"])) == \
+        (fp8g.KERNEL_TOKEN_TILES, fp8g.KERNEL_SM_PAIRS, fp8g.KERNEL_SWAP_AB)
