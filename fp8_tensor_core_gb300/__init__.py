@@ -75,13 +75,23 @@ def fp8g_version() -> int:
     return int(_lib.load().fp8g_version())
 
 
-def fp8g_init(max_tiles: int = 0) -> None:
-    """Allocate the stream-K workspace of the current device at its largest
-    size (counters for max_tiles output tiles, 0 = the library default), so
-    that later calls allocate nothing -- e.g. before CUDA graph capture."""
-    rc = _lib.load().fp8g_init(int(max_tiles))
+def fp8g_init(max_tiles: int = 0, stream=None) -> None:
+    """Allocate the stream-K workspace of `stream` (default: the current
+    torch stream) on the current device at its largest size (counters for
+    max_tiles output tiles, 0 = the library default), so that later calls
+    on that stream allocate nothing -- e.g. before capturing a CUDA graph
+    from it."""
+    rc = _lib.load().fp8g_init(int(max_tiles), _stream_handle(stream))
     if rc != OK:
         raise Fp8gError(rc, "fp8g_init")
+
+
+def fp8g_release_stream(stream=None) -> None:
+    """Synchronise `stream` (default: the current torch stream) and free its
+    stream-K workspace on the current device."""
+    rc = _lib.load().fp8g_release_stream(_stream_handle(stream))
+    if rc != OK:
+        raise Fp8gError(rc, "fp8g_release_stream")
 
 
 KERNEL_TOKEN_TILES, KERNEL_SM_PAIRS, KERNEL_SWAP_AB = 0, 1, 2
@@ -102,7 +112,7 @@ def fp8g_describe_plan(layout: int, G: int, rows: int, N: int, K: int, token_hin
 
 
 def fp8g_shutdown() -> None:
-    """Free the library's stream-K workspace on every device."""
+    """Free the library's stream-K workspaces (every stream, every device)."""
     rc = _lib.load().fp8g_shutdown()
     if rc != OK:
         raise Fp8gError(rc, "fp8g_shutdown")

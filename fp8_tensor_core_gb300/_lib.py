@@ -74,7 +74,8 @@ SIGNATURES = {
     "fp8_gemm_nt_noalloc": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _i64, _i64,
                                            ctypes.c_int, ctypes.c_int, _c_void_p]),
     "fp8g_get_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), _c_void_p]),
-    "fp8g_init": (ctypes.c_int, [_i64]),
+    "fp8g_init": (ctypes.c_int, [_i64, _c_void_p]),
+    "fp8g_release_stream": (ctypes.c_int, [_c_void_p]),
     "fp8g_describe_plan": (ctypes.c_int, [ctypes.c_int, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.c_uint32,
                                           ctypes.c_int, ctypes.c_int, ctypes.POINTER(Plan)]),
     "fp8g_shutdown": (ctypes.c_int, []),

@@ -16,6 +16,8 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <thread>
+#include <vector>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -44,7 +46,18 @@ struct DeviceInfo {
     int smem_optin = 0;
 };
 
+// Stream-K scratch of one (device, stream): FP32 partial tiles indexed by
+// the CTA and arrival counters indexed by the output tile.  Two launches that
+// shared one such area could run at the same time on unordered streams and
+// overwrite each other's partials and counts, so every stream has its own;
+// launches on one stream are ordered by the stream (a launch's loads and
+// stores all follow griddepcontrol.wait, i.e. the previous launch's end).
+// The per-thread default stream is one stream per host thread, so its
+// entries are told apart by the thread as well.
 struct Workspace {
+    int dev = -1;
+    cudaStream_t stream = nullptr;
+    std::thread::id thread{};
     float *ws = nullptr;
     size_t ws_bytes = 0;
     int32_t *counters = nullptr;
@@ -54,7 +67,7 @@ struct Workspace {
 std::mutex g_mu;
 constexpr int64_t kDefaultInitTiles = 65536;   // fp8g_init(0): counters for this many stream-K tiles
 DeviceInfo g_dev[kMaxDevices];
-Workspace g_ws[kMaxDevices];
+std::vector<Workspace> g_ws;   // one entry per (device, stream[, thread]), under g_mu
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -163,12 +176,48 @@ int pick_stages(const DeviceInfo &d, int stage_bytes, int groups, uint32_t flags
     return s;
 }
 
-// Split-K workspace of the current device, grown on demand (the first call
-// needing a larger one allocates; later calls reuse it).
-int ensure_workspace(int dev, size_t ws_bytes, size_t counter_bytes, float **ws, int32_t **counters)
+// The handle under which a stream's workspace is kept: the legacy default
+// stream has two names (0 and cudaStreamLegacy).
+cudaStream_t stream_key(cudaStream_t s) { return s == cudaStreamLegacy ? nullptr : s; }
+
+// Entry of (dev, stream), created empty if absent.  Caller holds g_mu.
+Workspace &workspace_of(int dev, cudaStream_t stream)
+{
+    stream = stream_key(stream);
+    const std::thread::id th = stream == cudaStreamPerThread ? std::this_thread::get_id() : std::thread::id{};
+    for (Workspace &w : g_ws)
+        if (w.dev == dev && w.stream == stream && w.thread == th)
+            return w;
+    Workspace w;
+    w.dev = dev;
+    w.stream = stream;
+    w.thread = th;
+    g_ws.push_back(w);
+    return g_ws.back();
+}
+
+// Frees an entry's buffers (cudaFree waits for the device's work); the
+// device must be current.
+bool free_workspace(Workspace &w)
+{
+    bool ok = true;
+    if (w.ws && cudaFree(w.ws) != cudaSuccess)
+        ok = false;
+    if (w.counters && cudaFree(w.counters) != cudaSuccess)
+        ok = false;
+    w.ws = nullptr;
+    w.counters = nullptr;
+    w.ws_bytes = w.counter_bytes = 0;
+    return ok;
+}
+
+// Stream-K workspace of (current device, stream), grown on demand (the
+// first call needing a larger one allocates; later calls reuse it).
+int ensure_workspace(int dev, cudaStream_t stream, size_t ws_bytes, size_t counter_bytes, float **ws,
+                     int32_t **counters)
 {
     std::lock_guard<std::mutex> lk(g_mu);
-    Workspace &w = g_ws[dev];
+    Workspace &w = workspace_of(dev, stream);
     if (w.ws_bytes < ws_bytes) {
         if (w.ws)
             cudaFree(w.ws);
@@ -579,7 +628,7 @@ int launch(const Problem &p, cudaStream_t stream, const DeviceInfo *forced = nul
             return FP8G_OK;
         }
         if (!whole_tiles) {
-            st = ensure_workspace(dev, swap_partials_bytes(grid, static_cast<int>(cap)),
+            st = ensure_workspace(dev, stream, swap_partials_bytes(grid, static_cast<int>(cap)),
                                   swap_counter_bytes(tiles_upper), &args.workspace, &args.counters);
             if (st != FP8G_OK)
                 return st;
@@ -676,7 +725,7 @@ int launch(const Problem &p, cudaStream_t stream, const DeviceInfo *forced = nul
         // (stream-K implies units is not a multiple of the pairs, so every
         // pair of the grid exists for the remainder's partition)
         if (plan.stream_k) {
-            st = ensure_workspace(dev, static_cast<size_t>(grid) * 2 * kTileM * tile_n * sizeof(float),
+            st = ensure_workspace(dev, stream, static_cast<size_t>(grid) * 2 * kTileM * tile_n * sizeof(float),
                                   static_cast<size_t>(units) * 8 * sizeof(int32_t), &args.workspace,
                                   &args.counters);
             if (st != FP8G_OK)
@@ -978,16 +1027,22 @@ extern "C" int fp8g_get_device_status(int32_t *info, cudaStream_t stream)
     if (read_and_clear_status(info) != cudaSuccess)
         return FP8G_ERR_CUDA;
     if (info[0] == FP8G_ERR_TIMEOUT) {
-        // An aborted stream-K launch can leave arrival counts behind.
+        // An aborted stream-K launch can leave arrival counts behind, in the
+        // workspace of whichever stream it ran on: once the device is idle,
+        // clear the counters of every stream of this device.
+        if (cudaDeviceSynchronize() != cudaSuccess)
+            return FP8G_ERR_CUDA;
         std::lock_guard<std::mutex> lk(g_mu);
-        Workspace &w = g_ws[dev];
-        if (w.counters && cudaMemset(w.counters, 0, w.counter_bytes) != cudaSuccess)
+        for (Workspace &w : g_ws)
+            if (w.dev == dev && w.counters && cudaMemset(w.counters, 0, w.counter_bytes) != cudaSuccess)
+                return FP8G_ERR_CUDA;
+        if (cudaDeviceSynchronize() != cudaSuccess)
             return FP8G_ERR_CUDA;
     }
     return FP8G_OK;
 }
 
-extern "C" int fp8g_init(int64_t max_tiles)
+extern "C" int fp8g_init(int64_t max_tiles, cudaStream_t stream)
 {
     int dev = 0;
     DeviceInfo info;
@@ -1003,7 +1058,28 @@ extern "C" int fp8g_init(int64_t max_tiles)
     const size_t ws_bytes = static_cast<size_t>(info.sms) * 2 * kTileM * 256 * sizeof(float);
     float *ws = nullptr;
     int32_t *counters = nullptr;
-    return ensure_workspace(dev, ws_bytes, swap_counter_bytes(tiles), &ws, &counters);
+    return ensure_workspace(dev, stream, ws_bytes, swap_counter_bytes(tiles), &ws, &counters);
+}
+
+extern "C" int fp8g_release_stream(cudaStream_t stream)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return FP8G_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    const cudaStream_t key = stream_key(stream);
+    const std::thread::id th = key == cudaStreamPerThread ? std::this_thread::get_id() : std::thread::id{};
+    for (size_t i = 0; i < g_ws.size(); ++i) {
+        Workspace &w = g_ws[i];
+        if (w.dev != dev || w.stream != key || w.thread != th)
+            continue;
+        if (cudaStreamSynchronize(stream) != cudaSuccess)
+            return FP8G_ERR_CUDA;
+        const bool ok = free_workspace(w);
+        g_ws.erase(g_ws.begin() + static_cast<std::ptrdiff_t>(i));
+        return ok ? FP8G_OK : FP8G_ERR_CUDA;
+    }
+    return FP8G_OK;
 }
 
 extern "C" int fp8g_shutdown(void)
@@ -1012,20 +1088,15 @@ extern "C" int fp8g_shutdown(void)
     int prev = 0;
     const bool have_prev = cudaGetDevice(&prev) == cudaSuccess;
     int rc = FP8G_OK;
-    for (int d = 0; d < kMaxDevices; ++d) {
-        Workspace &w = g_ws[d];
-        if (!w.ws && !w.counters)
-            continue;
-        if (cudaSetDevice(d) != cudaSuccess) {
+    for (Workspace &w : g_ws) {
+        if (cudaSetDevice(w.dev) != cudaSuccess) {
             rc = FP8G_ERR_CUDA;
             continue;
         }
-        if (w.ws && cudaFree(w.ws) != cudaSuccess)
+        if (!free_workspace(w))
             rc = FP8G_ERR_CUDA;
-        if (w.counters && cudaFree(w.counters) != cudaSuccess)
-            rc = FP8G_ERR_CUDA;
-        w = Workspace{};
     }
+    g_ws.clear();
     if (have_prev)
         cudaSetDevice(prev);
     else

@@ -8,9 +8,11 @@
 // code that records its launches into a CUDA graph, where allocation calls
 // are not allowed while capturing.  fp8_gemm_nt may allocate its stream-K
 // workspace on first use; this entry point never allocates.  It launches the
-// same k_gemm_swap kernel as fp8_gemm_nt's SwapAB path with the same tiling
-// choices, pointing the kernel's stream-K partial tiles and arrival counters
-// at g_noalloc_scratch.
+// same k_gemm_swap kernel as fp8_gemm_nt's SwapAB path, pointing the
+// kernel's stream-K partial tiles and arrival counters at g_noalloc_scratch.
+// Its configuration differs in one respect: every CTA takes a whole SM (all
+// of its shared memory and 512 TMEM columns), while fp8_gemm_nt lets two
+// launches share an SM for problems of up to 16 tokens.
 //
 // The scratch array is FP8G_NOALLOC_SCRATCH_BYTES long and every GPU that
 // loads this library holds it until the process exits.  All calls on a
@@ -152,8 +154,9 @@ extern "C" int fp8_gemm_nt_noalloc(const void *A, const void *B, void *D, int64_
     const int64_t cap = cdiv(M, 16) * 16;             // tokens per chunk (M <= 256: one chunk)
     const int64_t tiles = cdiv(N, kTileM);
     const int grid = static_cast<int>(std::min<int64_t>(sms, tiles * num_kb));
-    // Scratch layout: arrival counters (4 per tile), then the stream-K
-    // partial tiles (2 per CTA).
+    // Scratch layout: arrival counters (two int32 per epilogue warp, so 8
+    // = 32 bytes per 128-row tile), then the stream-K partial tiles (2 per
+    // CTA).
     const size_t counter_bytes = swap_counter_bytes(tiles);
     const size_t counter_span = (counter_bytes + 255) & ~static_cast<size_t>(255);
     const size_t ws_bytes = swap_partials_bytes(grid, static_cast<int>(cap));

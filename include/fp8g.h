@@ -38,6 +38,21 @@
  *    (a bounded wait that ran out, masked_m out of range) are recorded in a
  *    per-device status word read by fp8g_get_device_status().
  *  - Offsets are computed in 64 bits throughout.
+ *  - Calls on different streams may run at the same time on the GPU.  The
+ *    scratch memory a launch needs beyond its operands (the stream-K
+ *    partial tiles and arrival counters of the SwapAB kernel and of split
+ *    SM-pair tiles; "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践"
+ *    §6.4 on accumulation across CTAs) is kept per (device, stream), so
+ *    launches on unordered streams never share it; launches on one stream
+ *    are ordered by the stream.  A CUDA graph captured from a stream uses
+ *    that stream's scratch: replay it ordered with the stream's other
+ *    library work (on that stream, or after an event on it).  The
+ *    per-thread default stream counts as one stream per host thread.
+ *    Before destroying a stream whose library work may still be running,
+ *    call fp8g_release_stream() on it (or synchronise it): the runtime may
+ *    hand the same handle to a new stream.
+ *  - fp8_gemm_nt_noalloc is the exception: all of its calls on a device
+ *    share one fixed array (see there).
  *  - Not thread-safe for concurrent calls from several host threads on the
  *    same device while fp8g_set_wait_timeout_ns() is being changed.
  */
@@ -147,7 +162,10 @@ typedef enum {
  *            engine);  N % 8 == 0 (16-byte rows of D);  each < 2^31.
  *   a_dtype, b_dtype  fp8g_dtype of A and B (mixed pairs allowed).
  *   flags  FP8G_SWAP_* (plus debug bits).
- *   stream  CUDA stream to enqueue on (0 = legacy default stream).
+ *   stream  CUDA stream to enqueue on (0 = legacy default stream).  A
+ *           SwapAB or split-tile launch uses this stream's own stream-K
+ *           scratch (allocated on the stream's first such call, or by
+ *           fp8g_init), so calls on other streams may overlap with it.
  * Returns FP8G_OK or an error code; on error nothing is enqueued.
  */
 int fp8_gemm_nt(const void *A, const void *B, void *D, int64_t M, int64_t N,
@@ -170,6 +188,9 @@ int fp8_gemm_nt(const void *A, const void *B, void *D, int64_t M, int64_t N,
  *             unknown, taken as M_max).  It only sizes the token tile; groups
  *             above it are still computed correctly.
  *   N % 8 == 0, K % 16 == 0, sizes < 2^31, dtypes and flags as above.
+ *   stream    as fp8_gemm_nt: the SwapAB kernel's stream-K scratch belongs
+ *             to this stream, so grouped calls and dense calls on other
+ *             streams may run at the same time.
  * Returns FP8G_OK or an error code; on error nothing is enqueued.
  */
 int fp8_gemm_grouped_masked(const void *A, const void *B, void *D,
@@ -343,26 +364,33 @@ int fp8_gemm_grouped_contiguous_ex(const void *A, const void *B, void *D,
 int fp8g_get_device_status(int32_t *info, cudaStream_t stream);
 
 /*
- * fp8g_init -- allocate, on the current device, the library's stream-K
- * workspace at its largest size: partial tiles for every SM (2 x SMs x
- * 128 x 256 FP32, 39.8 MB on 152 SMs) and arrival counters for up to
- * `max_tiles` output tiles of one launch (0 = 65536; 32 bytes a tile).  A
- * stream-K launch is one with SwapAB (output tiles = groups x token chunks
- * x ceil(N / 128)) or split SM-pair tiles (ceil(M / 256) x ceil(N / tile)).
- * The calls allocate that workspace themselves on first need; after
- * fp8g_init, calls whose launches fit allocate nothing, so they can be
- * recorded into a CUDA graph from the start.  Idempotent; never shrinks.
+ * fp8g_init -- allocate, on the current device, the stream-K workspace of
+ * `stream` at its largest size: partial tiles for every SM (2 x SMs x 128 x
+ * 256 FP32, 39.8 MB on 152 SMs) and arrival counters for up to `max_tiles`
+ * output tiles of one launch (0 = 65536; 32 bytes a tile).  A stream-K
+ * launch is one with SwapAB (output tiles = groups x token chunks x
+ * ceil(N / 128)) or split SM-pair tiles (ceil(M / 256) x ceil(N / tile)).
+ * The calls allocate a stream's workspace themselves on its first need;
+ * after fp8g_init, calls on that stream whose launches fit allocate
+ * nothing, so they can be recorded into a CUDA graph captured from that
+ * stream from the start.  Idempotent; never shrinks.
  * Returns FP8G_OK, FP8G_ERR_INVALID_ARG (max_tiles < 0 or > 2^31 - 1),
  * FP8G_ERR_NO_DEVICE, FP8G_ERR_UNSUPPORTED (not sm_103) or FP8G_ERR_CUDA
  * (allocation failed).
  *
- * fp8g_shutdown -- free the stream-K workspace on every device that has
- * one (cudaFree waits for the device's work).  Call it with no library
+ * fp8g_release_stream -- synchronise `stream` and free its stream-K
+ * workspace on the current device (nothing to do if it has none).  Call it
+ * before destroying a stream that ran library work.  Returns FP8G_OK or
+ * FP8G_ERR_CUDA.
+ *
+ * fp8g_shutdown -- free the stream-K workspaces of every stream on every
+ * device (cudaFree waits for the device's work).  Call it with no library
  * work being enqueued or captured on another thread; later calls allocate
  * again on first need.  The fixed array of fp8_gemm_nt_noalloc is not
  * affected.  Returns FP8G_OK or FP8G_ERR_CUDA.
  */
-int fp8g_init(int64_t max_tiles);
+int fp8g_init(int64_t max_tiles, cudaStream_t stream);
+int fp8g_release_stream(cudaStream_t stream);
 int fp8g_shutdown(void);
 
 /*
@@ -386,15 +414,21 @@ uint64_t fp8g_set_wait_timeout_ns(uint64_t ns);
  * allocate its stream-K workspace on first use; this call instead keeps that
  * scratch in one fixed device array of FP8G_NOALLOC_SCRATCH_BYTES (32 MiB)
  * inside the library, which every GPU that loads the library holds until the
- * process exits.  It runs the same SwapAB stream-K kernel with the same
- * tiling choices as fp8_gemm_nt's small-token path.
+ * process exits.  It runs the SwapAB stream-K kernel of fp8_gemm_nt's
+ * small-token path, with one difference in configuration: it always gives
+ * each CTA a whole SM (all of its shared memory, 512 TMEM columns), where
+ * fp8_gemm_nt shares an SM between two launches for problems of up to 16
+ * tokens (measured about 5 % slower than that shared-SM form there).
  *
  *   A [M, K], B [N, K], D [M, N] and the dtypes: as fp8_gemm_nt.
  *   M  1..256 tokens, else FP8G_ERR_UNSUPPORTED.
- *   A problem whose partial tiles and counters need more than the fixed
- *   scratch (2 x SMs x 128 x round16(M) x 4 bytes plus 16 bytes per 128
- *   rows of N; tokens up to about 192 fit on 152 SMs) returns
- *   FP8G_ERR_UNSUPPORTED before anything is enqueued.
+ *   Scratch a call needs: its arrival counters, 32 bytes per 128 rows of N
+ *   (rounded up to 256 bytes), then its partial tiles, 2 x grid x 128 x
+ *   round16(M) x 4 bytes, where grid = min(SMs, ceil(N/128) x ceil(K/128)).
+ *   A problem that needs more than FP8G_NOALLOC_SCRATCH_BYTES returns
+ *   FP8G_ERR_UNSUPPORTED before anything is enqueued.  On 152 SMs every
+ *   problem of up to 208 tokens fits (for N up to 4.7 million rows); 209
+ *   to 256 tokens (chunks of 224, 240, 256) fit only launches of fewer CTAs.
  *   No cudaMalloc, cudaFree or allocating library routine is called.  The
  *   first call on a device looks up the array's device address and the
  *   device limits (once per device, with that device current): make that
@@ -403,7 +437,9 @@ uint64_t fp8g_set_wait_timeout_ns(uint64_t ns);
  *   All calls on a device share the array: calls that overlap on the GPU
  *   (unordered streams) race on it and give wrong results.
  *   Bounded waits use the default 2 s limit.
- * Returns FP8G_OK or an error code; on error nothing is enqueued.
+ * Returns FP8G_OK or an error code.  On an argument or size error nothing
+ * is enqueued; FP8G_ERR_CUDA from the launch itself can follow the
+ * counters' clearing memset, which is then harmless.
  */
 #define FP8G_NOALLOC_SCRATCH_BYTES (32u << 20)
 int fp8_gemm_nt_noalloc(const void *A, const void *B, void *D, int64_t M, int64_t N,

@@ -433,17 +433,18 @@ def test_share_sm_mode_grouped():
 
 
 def test_init_then_capture_stream_k_in_a_graph():
-    """After fp8g_init a stream-K call allocates nothing, so it can be the
-    first call recorded into a CUDA graph; fp8g_shutdown frees the workspace
-    and later calls allocate it again."""
+    """After fp8g_init on a stream, a stream-K call on that stream allocates
+    nothing, so it can be the first call recorded into a CUDA graph captured
+    from it; fp8g_shutdown frees the workspaces and later calls allocate
+    them again."""
     fp8g.fp8g_shutdown()
-    fp8g.fp8g_init(0)
     M, N, K = 24, 1536, 3072
     A = synth.normal_fp8((M, K), 181, 0.0, 1.0, E4)
     B = synth.normal_fp8((N, K), 182, 0.0, 1.0, E4)
     Ad, Bd = dev(A), dev(B)
     D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     s = torch.cuda.Stream()
+    fp8g.fp8g_init(0, s)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         fp8g.fp8_gemm_nt(Ad, Bd, D, a_dtype=E4, b_dtype=E4, flags=ON)
@@ -461,5 +462,24 @@ def test_init_then_capture_stream_k_in_a_graph():
 
 
 def test_init_argument_errors():
-    assert fp8g._lib.load().fp8g_init(-1) == fp8g.ERR_INVALID_ARG
-    assert fp8g._lib.load().fp8g_init(1 << 40) == fp8g.ERR_INVALID_ARG
+    assert fp8g._lib.load().fp8g_init(-1, None) == fp8g.ERR_INVALID_ARG
+    assert fp8g._lib.load().fp8g_init(1 << 40, None) == fp8g.ERR_INVALID_ARG
+
+
+def test_release_stream_frees_and_later_calls_allocate_again():
+    """fp8g_release_stream synchronises the stream and frees its workspace;
+    the next stream-K call on it allocates a fresh one and is still right."""
+    M, N, K = 40, 2048, 2048
+    A = synth.normal_fp8((M, K), 191, 0.0, 1.0, E4)
+    B = synth.normal_fp8((N, K), 192, 0.0, 1.0, E4)
+    Ad, Bd = dev(A), dev(B)
+    ref, absdot = oracle.gemm_nt(A, B)
+    s = torch.cuda.Stream()
+    for _ in range(2):
+        with torch.cuda.stream(s):
+            D = fp8g.fp8_gemm_nt(Ad, Bd, a_dtype=E4, b_dtype=E4, flags=ON)
+        fp8g.fp8g_release_stream(s)
+        ok, rep = oracle.check_bf16(bits(D), ref, absdot)
+        assert ok, rep
+    fp8g.fp8g_release_stream(s)          # nothing left to free: still OK
+    assert fp8g.fp8g_get_device_status()[0] == fp8g.OK
