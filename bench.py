@@ -345,14 +345,19 @@ def barrier(world: int, device=None):
 # CPU baseline: the oracle, as it stands, on a bounded sample
 # ---------------------------------------------------------------------------
 
-def oracle_sample(w: Workload, inp, budget_s: float, min_rows: int = 1):
-    """Time the oracle on whole output rows of the workload until about
-    `budget_s` seconds have been spent.  Returns (flops, seconds, cores,
-    description)."""
+def oracle_sample(w: Workload, inp, budget_s: float, min_rows: int = 1, check_against=None):
+    """Time the oracle on whole output rows (groups) of the workload until
+    about `budget_s` seconds have been spent.  Returns (flops, seconds,
+    cores, description, parity): with `check_against` (the device run's D
+    as uint16 bits) every element the oracle computed is compared with it
+    after the clock stops, within the acceptance rule (one BF16 ulp plus
+    1e-6 * sum |a b|; masked padding rows bit for bit); parity is "ok ..."
+    or a description of the first mismatch, None without a device D."""
     import numpy as np
     import oracle
     cores = oracle.default_threads()
     flops = 0.0
+    pieces = []            # (what, reference D, absdot, device slice)
     t_start = time.perf_counter()
     if w.kind == "dense":
         A, B = inp["A"], inp["B"]
@@ -361,11 +366,14 @@ def oracle_sample(w: Workload, inp, budget_s: float, min_rows: int = 1):
             r1 = min(w.M, r0 + rows)
             t = time.perf_counter()
             if w.gran:
-                oracle.gemm_blockscaled(A[r0:r1], B, inp["sf_a"][0][:, r0:r1].copy(), inp["sf_b"][0], w.gran,
-                                        fa=w.fa, fb=w.fb)
+                ref, absd, accb = oracle.gemm_blockscaled(A[r0:r1], B, inp["sf_a"][0][:, r0:r1].copy(),
+                                                          inp["sf_b"][0], w.gran, fa=w.fa, fb=w.fb,
+                                                          want_accbound=True)
             else:
-                oracle.gemm_nt(A[r0:r1], B, w.fa, w.fb)
+                (ref, absd), accb = oracle.gemm_nt(A[r0:r1], B, w.fa, w.fb), None
             dt = time.perf_counter() - t
+            if check_against is not None:
+                pieces.append(("rows %d..%d" % (r0, r1 - 1), ref, absd, check_against[r0:r1], accb))
             flops += 2.0 * (r1 - r0) * w.N * w.K
             r0 = r1
             if time.perf_counter() - t_start >= budget_s:
@@ -373,37 +381,56 @@ def oracle_sample(w: Workload, inp, budget_s: float, min_rows: int = 1):
             rows = max(rows, int(rows * min(4.0, 0.5 * budget_s / max(dt, 1e-3))))
         secs = time.perf_counter() - t_start
         desc = "rows 0..%d of D (%d of %d rows, all N=%d columns, K=%d)" % (r0 - 1, r0, w.M, w.N, w.K)
-        return flops, secs, cores, desc
-    if w.kind == "contig":
+    elif w.kind == "contig":
         A, B, off = inp["A"], inp["B"], inp["offsets"]
         g_done = 0
         for g in range(w.G):
             if off[g + 1] > off[g]:
-                oracle.gemm_nt(A[off[g]:off[g + 1]], B[g], w.fa, w.fb)
+                ref, absd = oracle.gemm_nt(A[off[g]:off[g + 1]], B[g], w.fa, w.fb)
+                if check_against is not None:
+                    pieces.append(("group %d" % g, ref, absd, check_against[off[g]:off[g + 1]], None))
                 flops += 2.0 * int(off[g + 1] - off[g]) * w.N * w.K
             g_done += 1
             if time.perf_counter() - t_start >= budget_s:
                 break
         secs = time.perf_counter() - t_start
-        return flops, secs, cores, "groups 0..%d of %d (all their rows)" % (g_done - 1, w.G)
-    A, B, mm = inp["A"], inp["B"], inp["masked_m"]
-    D0 = np.zeros((1, w.M_max, w.N), np.uint16)
-    g_done = 0
-    for g in range(w.G):
-        if mm[g] == 0:
+        desc = "groups 0..%d of %d (all their rows)" % (g_done - 1, w.G)
+    else:
+        A, B, mm = inp["A"], inp["B"], inp["masked_m"]
+        D0 = np.zeros((1, w.M_max, w.N), np.uint16)
+        g_done = 0
+        for g in range(w.G):
+            if mm[g] == 0:
+                g_done += 1
+                continue
+            if w.gran:
+                ref, absd, accb = oracle.gemm_blockscaled(A[g:g + 1], B[g:g + 1], inp["sf_a"][g:g + 1],
+                                                          inp["sf_b"][g:g + 1], w.gran, masked_m=mm[g:g + 1],
+                                                          D_init=D0, fa=w.fa, fb=w.fb, want_accbound=True)
+            else:
+                (ref, absd), accb = oracle.gemm_grouped_masked(A[g:g + 1], B[g:g + 1], mm[g:g + 1], D0, w.fa,
+                                                               w.fb), None
+            if check_against is not None:
+                m = int(mm[g])
+                pieces.append(("group %d" % g, ref[0, :m], absd[0, :m], check_against[g, :m],
+                               accb[0, :m] if accb is not None else None))
+            flops += 2.0 * int(mm[g]) * w.N * w.K
             g_done += 1
-            continue
-        if w.gran:
-            oracle.gemm_blockscaled(A[g:g + 1], B[g:g + 1], inp["sf_a"][g:g + 1], inp["sf_b"][g:g + 1], w.gran,
-                                    masked_m=mm[g:g + 1], D_init=D0, fa=w.fa, fb=w.fb)
-        else:
-            oracle.gemm_grouped_masked(A[g:g + 1], B[g:g + 1], mm[g:g + 1], D0, w.fa, w.fb)
-        flops += 2.0 * int(mm[g]) * w.N * w.K
-        g_done += 1
-        if time.perf_counter() - t_start >= budget_s:
-            break
-    secs = time.perf_counter() - t_start
-    return flops, secs, cores, "groups 0..%d of %d (all their valid rows)" % (g_done - 1, w.G)
+            if time.perf_counter() - t_start >= budget_s:
+                break
+        secs = time.perf_counter() - t_start
+        desc = "groups 0..%d of %d (all their valid rows)" % (g_done - 1, w.G)
+    parity = None
+    if check_against is not None:
+        n = 0
+        for what, ref, absd, got, accb in pieces:
+            ok, rep = oracle.check_bf16(got, ref, absd, acc_bound=accb)
+            if not ok:
+                return flops, secs, cores, desc, "mismatch in %s: %s" % (what, rep)
+            n += ref.size
+        parity = "ok: %d elements of the device run's D (the sampled %s) match the oracle" % (
+            n, "rows" if w.kind == "dense" else "groups")
+    return flops, secs, cores, desc, parity
 
 
 def run_reference(args, w: Workload):
@@ -422,7 +449,7 @@ def run_reference(args, w: Workload):
     desc = ""
     cores = oracle.default_threads()
     for _ in range(args.steps):
-        f, s, cores, desc = oracle_sample(w, inp, per_step_budget)
+        f, s, cores, desc, _ = oracle_sample(w, inp, per_step_budget)
         flops += f
         secs += s
     value = flops / secs / 1e12
@@ -444,44 +471,43 @@ def run_reference(args, w: Workload):
 # GPU arm
 # ---------------------------------------------------------------------------
 
-def run_ours(args, w: Workload):
-    import numpy as np
-    import torch
+# The pages' configurations, each a bench workload: the per_config array of
+# the JSON line times every one of them (configs 1-5; config 5 through both
+# kernels, SwapAB and the non-swapped token tiles).
+PER_CONFIG = ([("1", "cube256"), ("2", "dense4096")] +
+              [("3", "proj:%s%s" % (nk, fmt)) for nk in ("7168:2048", "4096:7168", "18432:7168", "7168:18432")
+               for fmt in ("", ":e5m2")] +
+              [("4", "masked"), ("4", "masked:noswap")] +
+              [("5", "smallm:%d:%s:%s" % (m, nk, mode)) for nk in ("24576:1536", "7168:16384")
+               for m in (1, 8, 16, 32, 64) for mode in ("swap", "noswap")])
+DEFAULT_WORKLOAD = "proj:18432:7168"      # the largest configuration (M=8192, N=18432, K=7168)
+BURST_REGION_MS = 1000.0                  # timed regions shorter than this are compared with the burst peak
 
-    rank, world, local = dist_setup()
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", rank=rank, world_size=world, device_id=device)
 
-    import fp8_tensor_core_gb300 as fp8g
-    fp8g._lib.load()          # fails loudly if the CUDA library is not built
-    props = torch.cuda.get_device_properties(device)
-    l2 = int(getattr(props, "L2_cache_size", 0) or 129 * 2**20)
-
-    inp = host_inputs(w)
-    stream = torch.cuda.current_stream(device)
-
-    # Rotating device copies so that consecutive steps do not find their
-    # operands in L2: sets x (inputs + output) >= 3 x L2.
+def set_bytes_of(w: Workload) -> int:
     if w.kind == "dense":
-        set_bytes = w.M * w.K + w.N * w.K + 2 * w.M * w.N
-    elif w.kind == "contig":
-        set_bytes = w.G * w.M_max * w.K + w.G * w.N * w.K + 2 * w.G * w.M_max * w.N
-    else:
-        set_bytes = w.G * w.M_max * w.K + w.G * w.N * w.K + 2 * w.G * w.M_max * w.N
-    n_sets = max(1, math.ceil(3 * l2 / set_bytes))
-    n_sets = min(n_sets, 64)
-    sets = []
-    A_h = torch.from_numpy(inp["A"]).pin_memory()
-    B_h = torch.from_numpy(inp["B"]).pin_memory()
-    sfa_h = torch.from_numpy(inp["sf_a"]).pin_memory() if w.gran else None
-    sfb_h = torch.from_numpy(inp["sf_b"]).pin_memory() if w.gran else None
-    for _ in range(n_sets):
-        s = {"A": A_h.to(device), "B": B_h.to(device)}
+        return w.M * w.K + w.N * w.K + 2 * w.M * w.N
+    return w.G * w.M_max * w.K + w.G * w.N * w.K + 2 * w.G * w.M_max * w.N
+
+
+def device_sets(w: Workload, inp, device, l2: int, pinned=None):
+    """Rotating device copies of the inputs and an output each, so that
+    consecutive launches do not find their operands in L2: sets x (inputs +
+    output) >= 3 x L2.  Returns (sets, host tensors)."""
+    import torch
+    n_sets = min(64, max(1, math.ceil(3 * l2 / set_bytes_of(w))))
+    h = pinned or {}
+    if not h:
+        h["A"] = torch.from_numpy(inp["A"]).pin_memory()
+        h["B"] = torch.from_numpy(inp["B"]).pin_memory()
         if w.gran:
-            s["sfa"], s["sfb"] = sfa_h.to(device), sfb_h.to(device)
+            h["sfa"] = torch.from_numpy(inp["sf_a"]).pin_memory()
+            h["sfb"] = torch.from_numpy(inp["sf_b"]).pin_memory()
+    sets = []
+    for _ in range(n_sets):
+        s = {"A": h["A"].to(device), "B": h["B"].to(device)}
+        if w.gran:
+            s["sfa"], s["sfb"] = h["sfa"].to(device), h["sfb"].to(device)
         if w.kind == "dense":
             s["D"] = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device)
         elif w.kind == "contig":
@@ -491,7 +517,12 @@ def run_ours(args, w: Workload):
             s["mm"] = torch.from_numpy(inp["masked_m"]).to(device)
             s["D"] = torch.zeros((w.G, w.M_max, w.N), dtype=torch.bfloat16, device=device)
         sets.append(s)
-    torch.cuda.synchronize(device)
+    return sets, h
+
+
+def make_call(w: Workload):
+    """The public-API call of one step on a device set."""
+    import fp8_tensor_core_gb300 as fp8g
 
     def call(s, strm):
         if w.kind == "dense" and w.gran:
@@ -510,45 +541,46 @@ def run_ours(args, w: Workload):
         else:
             fp8g.fp8_gemm_grouped_masked(s["A"], s["B"], s["mm"], s["D"], max_m_hint=w.hint,
                                          a_dtype=w.fa, b_dtype=w.fb, flags=w.flags, stream=strm)
+    return call
 
-    def step_on(i, strm):
-        call(sets[i % n_sets], strm)
 
-    def step(i):
-        step_on(i, stream)
-
-    sampler = ClockSampler("GPU-" + str(props.uuid)) if rank == 0 else None
-
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize(device)
+def check_status(where: str, stream=None):
+    import fp8_tensor_core_gb300 as fp8g
     st = fp8g.fp8g_get_device_status(stream)
     if st[0] != fp8g.OK:
-        raise SystemExit("device status after warm-up: %s" % (st,))
+        raise SystemExit("device status %s: %s" % (where, st))
 
-    # ---- timed region: exactly K steps --------------------------------------
-    # By default the K launches (the same C-ABI calls) are captured into one
-    # CUDA graph and its replay is timed, so host launch gaps do not count;
-    # --graph off times K direct launches with events around each.
-    use_graph = args.graph != "off"
+
+def timed_launches(call, sets, steps: int, warmup: int, device, stream, use_graph: bool, sync_world=None):
+    """W warm-up launches, then exactly `steps` launches timed on the device
+    with CUDA events on the launching stream: by default captured into one
+    CUDA graph whose replay is timed (host launch gaps do not count), else
+    direct launches with events around each.  Returns (total_ms, per-launch
+    ms, wall-clock start, end)."""
+    import torch
+    for i in range(warmup):
+        call(sets[i % len(sets)], stream)
+    torch.cuda.synchronize(device)
+    check_status("after warm-up", stream)
     graph = None
     if use_graph:
         gs = torch.cuda.Stream(device)
         gs.wait_stream(stream)
         with torch.cuda.stream(gs):
-            for i in range(2):            # warm the side stream too
-                step_on(i, gs)
+            for i in range(2):            # the side stream's own warm-up (its stream-K scratch)
+                call(sets[i % len(sets)], gs)
         gs.synchronize()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=gs):
-            for i in range(args.steps):
-                step_on(args.warmup + i, gs)
+            for i in range(steps):
+                call(sets[(warmup + i) % len(sets)], gs)
         torch.cuda.synchronize(device)
         graph.replay()                    # upload / first replay, untimed
         torch.cuda.synchronize(device)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(1 if use_graph else args.steps)]
-    barrier(world, device)
+          for _ in range(1 if use_graph else steps)]
+    if sync_world:
+        sync_world()
     torch.cuda.synchronize(device)
     t_wall0 = time.time()
     if use_graph:
@@ -556,39 +588,183 @@ def run_ours(args, w: Workload):
         graph.replay()
         ev[0][1].record(stream)
     else:
-        for i in range(args.steps):
+        for i in range(steps):
             ev[i][0].record(stream)
-            step(args.warmup + i)
+            call(sets[(warmup + i) % len(sets)], stream)
             ev[i][1].record(stream)
     torch.cuda.synchronize(device)
-    barrier(world, device)
+    if sync_world:
+        sync_world()
     t_wall1 = time.time()
     total_ms = ev[0][0].elapsed_time(ev[-1][1])
-    if use_graph:
-        kernel_ms = total_ms / args.steps
+    kernel_ms = total_ms / steps if use_graph else sum(a.elapsed_time(b) for a, b in ev) / steps
+    check_status("after the timed launches", stream)
+    return total_ms, kernel_ms, t_wall0, t_wall1
+
+
+def roofline_of(w: Workload, flops: float, algo_bytes: float, kernel_ms: float, region_ms: float, peaks, peak_src):
+    """Achieved rate of the dominant kernel against its roofline: FP8 tensor
+    peak (2 x the measured BF16 rate: the burst figure for timed regions
+    under a second, the sustained one for longer) or the measured HBM copy
+    bandwidth."""
+    if w.bound == "tensor":
+        burst = region_ms < BURST_REGION_MS
+        bf16 = peaks["bf16_tflops"] if burst else peaks["bf16_tflops_sustained"]
+        peak = FP8_PER_BF16 * bf16
+        achieved = flops / (kernel_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_basis": "FP8 = %g x %s BF16 %s (%.1f TF/s; timed region %.1f ms %s 1 s)"
+                              % (FP8_PER_BF16, peak_src, "burst" if burst else "sustained", bf16, region_ms,
+                                 "<" if burst else ">="),
+                "frac_of_nominal_4500": achieved / 4500.0}
     else:
-        per_launch_ms = [a.elapsed_time(b) for a, b in ev]
-        kernel_ms = sum(per_launch_ms) / len(per_launch_ms)
-    st = fp8g.fp8g_get_device_status(stream)
-    if st[0] != fp8g.OK:
-        raise SystemExit("device status after timed region: %s" % (st,))
+        achieved = algo_bytes / (kernel_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "peak_basis": "%s HBM copy bandwidth" % peak_src,
+                "frac_of_nominal_8000": achieved / 8000.0}
+    roof.update({"algorithmic_flop": flops, "algorithmic_bytes": algo_bytes, "kernel_ms": kernel_ms})
+    return roof
+
+
+def host_us_per_call(w: Workload, s, stream, calls: int = 300) -> dict:
+    """Host time of one enqueue through the C ABI (pointers and sizes already
+    marshalled; every call after the first finds its tensor maps in the
+    library's cache), and the floor of a ctypes call into the library."""
+    import ctypes
+    import fp8_tensor_core_gb300 as fp8g
+    lib = fp8g._lib.load()
+    h = ctypes.c_void_p(stream.cuda_stream)
+    if w.kind == "dense" and not w.gran:
+        fn = lib.fp8_gemm_nt
+        args = (s["A"].data_ptr(), s["B"].data_ptr(), s["D"].data_ptr(), w.M, w.N, w.K, w.fa, w.fb, w.flags, h)
+    elif w.kind == "masked" and not w.gran:
+        fn = lib.fp8_gemm_grouped_masked
+        args = (s["A"].data_ptr(), s["B"].data_ptr(), s["D"].data_ptr(), s["mm"].data_ptr(), w.G, w.M_max, w.N, w.K,
+                w.hint, w.fa, w.fb, w.flags, h)
+    else:
+        return {}
+    import torch
+    for _ in range(3):
+        assert fn(*args) == 0
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(calls):
+        fn(*args)
+    t1 = time.perf_counter()
+    torch.cuda.synchronize()
+    check_status("after the host-cost calls", stream)
+    t2 = time.perf_counter()
+    for _ in range(calls):
+        lib.fp8g_version()
+    t3 = time.perf_counter()
+    return {"host_us_per_call": 1e6 * (t1 - t0) / calls, "ctypes_floor_us": 1e6 * (t3 - t2) / calls}
+
+
+def run_per_config(device, stream, l2, peaks, peak_src, sampler, steps_tensor: int, steps_hbm: int,
+                   use_graph: bool, known=None):
+    """Every configuration of the pages through the same timing: kernel ms,
+    achieved rate and roofline fraction (configs 3 in both B formats, config
+    4 through SwapAB and token tiles, config 5 through both kernels with
+    the automatic choice named)."""
+    import torch
+    import fp8_tensor_core_gb300 as fp8g
+    out = []
+    cache = {}
+    for cfg, name in PER_CONFIG:
+        if known and name in known:
+            out.append(dict(known[name], config=cfg))
+            continue
+        w = make_workload(name)
+        key = (w.kind, getattr(w, "M", None), w.N, w.K, w.fa, w.fb, w.seed, w.dist)
+        inp = cache.get(key)
+        if inp is None:
+            inp = host_inputs(w)
+            cache.clear()
+            cache[key] = inp
+        sets, _ = device_sets(w, inp, device, l2)
+        call = make_call(w)
+        steps = steps_tensor if w.bound == "tensor" else steps_hbm
+        total_ms, kernel_ms, t0, t1 = timed_launches(call, sets, steps, 3, device, stream, use_graph)
+        mm = inp.get("masked_m")
+        roof = roofline_of(w, w.flops(mm), w.bytes(mm), kernel_ms, total_ms, peaks, peak_src)
+        plan = planned_launch(w)
+        e = {"config": cfg, "name": name, "kernel": KERNEL_NAMES[plan["kernel"]], "kernel_ms": kernel_ms,
+             "achieved": roof["achieved"], "unit": roof["unit"], "frac": roof["frac"], "bound": roof["bound"],
+             "steps": steps}
+        if w.bound == "tensor":
+            e["frac_of_nominal_4500"] = roof["frac_of_nominal_4500"]
+        else:
+            e["frac_of_nominal_8000"] = roof["frac_of_nominal_8000"]
+            e["tflops"] = w.flops(mm) / (kernel_ms * 1e-3) / 1e12
+        if name.startswith("smallm") or name.startswith("masked"):
+            e.update(host_us_per_call(w, sets[0], stream))
+        if name.startswith("smallm") and name.endswith(":swap"):
+            base = name.rsplit(":", 1)[0]
+            auto = planned_launch(make_workload(base))
+            e["auto_picks"] = KERNEL_NAMES[auto["kernel"]]
+        if sampler:
+            c = sampler.summary(t0, t1)
+            if c["samples"]:
+                e["sm_mhz"] = c["sm_mhz"]
+        out.append(e)
+        del sets
+        torch.cuda.empty_cache()
+    fp8g.fp8g_release_stream(stream)
+    return out
+
+
+def run_ours(args, w: Workload):
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_setup()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", rank=rank, world_size=world, device_id=device)
+
+    import fp8_tensor_core_gb300 as fp8g
+    fp8g._lib.load()          # fails loudly if the CUDA library is not built
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 129 * 2**20)
+    peaks, peak_src = load_peaks()
+
+    inp = host_inputs(w)
+    stream = torch.cuda.current_stream(device)
+    sets, host = device_sets(w, inp, device, l2)
+    n_sets = len(sets)
+    torch.cuda.synchronize(device)
+    call = make_call(w)
+    sampler = ClockSampler("GPU-" + str(props.uuid)) if rank == 0 else None
+
+    # ---- timed region: exactly K steps --------------------------------------
+    use_graph = args.graph != "off"
+    total_ms, kernel_ms, t_wall0, t_wall1 = timed_launches(
+        call, sets, args.steps, args.warmup, device, stream, use_graph,
+        sync_world=lambda: barrier(world, device))
     total_ms_max = max_over_ranks(total_ms, world, device)
     kernel_ms_max = max_over_ranks(kernel_ms, world, device)
-    if sampler:
-        sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
 
     mm = inp.get("masked_m")
     flops = w.flops(mm)
     algo_bytes = w.bytes(mm)
     value = world * args.steps * flops / (total_ms_max * 1e-3) / 1e12
+    # The device-resident run's output (its last timed launch), kept on the
+    # host before anything else writes the sets: the end-to-end output and
+    # the oracle's sampled rows are compared with it.
+    d_dev = sets[(args.warmup + args.steps - 1) % n_sets]["D"].view(torch.int16).cpu().numpy().view(np.uint16)
 
     # ---- end to end through the public API, host buffers ---------------------
     # Every step copies its inputs in from pinned host memory, runs the GEMM
     # through the public API and copies the whole of D back.  Consecutive
     # steps rotate over --e2e-streams streams, each with its own device and
-    # host buffers, so one step's copies overlap its neighbours' (the host
-    # link moves ~210 GB/s one way, ~340 GB/s both ways at once).
+    # host buffers (and its own stream-K scratch in the library), so one
+    # step's copies overlap its neighbours' (the host link moves ~210 GB/s
+    # one way, ~340 GB/s both ways at once).  Afterwards the last step's D,
+    # as copied to the host, must equal the device-resident run's D bit for
+    # bit (same inputs, same deterministic kernel).
     e2e = None
     if not args.no_e2e:
         e2e_steps = max(1, min(args.steps, args.e2e_steps))
@@ -608,11 +784,11 @@ def run_ours(args, w: Workload):
             p = pipe[i % n_pipe]
             s_k, strm = p["set"], p["stream"]
             with torch.cuda.stream(strm):
-                s_k["A"].copy_(A_h, non_blocking=True)
-                s_k["B"].copy_(B_h, non_blocking=True)
+                s_k["A"].copy_(host["A"], non_blocking=True)
+                s_k["B"].copy_(host["B"], non_blocking=True)
                 if w.gran:
-                    s_k["sfa"].copy_(sfa_h, non_blocking=True)
-                    s_k["sfb"].copy_(sfb_h, non_blocking=True)
+                    s_k["sfa"].copy_(host["sfa"], non_blocking=True)
+                    s_k["sfb"].copy_(host["sfb"], non_blocking=True)
                 if mm_h is not None:
                     s_k["mm"].copy_(mm_h, non_blocking=True)
                 if off_h is not None:
@@ -634,50 +810,60 @@ def run_ours(args, w: Workload):
             stream.wait_stream(p["stream"])
         e1.record(stream)
         torch.cuda.synchronize(device)
-        st = fp8g.fp8g_get_device_status(stream)
-        if st[0] != fp8g.OK:
-            raise SystemExit("device status after the end-to-end run: %s" % (st,))
+        check_status("after the end-to-end run", stream)
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
-        h2d = A_h.numel() + B_h.numel() + (mm_h.numel() * 4 if mm_h is not None else 0) + \
+        h2d = host["A"].numel() + host["B"].numel() + (mm_h.numel() * 4 if mm_h is not None else 0) + \
             (off_h.numel() * 4 if off_h is not None else 0)
         if w.gran:
-            h2d += sfa_h.numel() + sfb_h.numel()
+            h2d += host["sfa"].numel() + host["sfb"].numel()
         d2h = pipe[0]["D_h"].numel() * 2
+        # the last step's host copy against the device-resident run's output
+        last = pipe[(e2e_steps - 1) % n_pipe]["D_h"].view(torch.int16).numpy().view(np.uint16)
+        ref_dev = d_dev
+        if w.kind == "masked":
+            same = all(np.array_equal(last[g, :m], ref_dev[g, :m]) for g, m in enumerate(mm))
+        elif w.kind == "contig":
+            off = inp["offsets"]
+            same = all(np.array_equal(last[off[g]:off[g + 1]], ref_dev[off[g]:off[g + 1]]) for g in range(w.G))
+        else:
+            same = np.array_equal(last, ref_dev)
+        if not same:
+            raise SystemExit("end-to-end output differs from the device-resident run's output")
         e2e = {"value": world * e2e_steps * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps,
-               "streams": n_pipe}
+               "streams": n_pipe, "check": "last step's D bit-identical to the device-resident run's D"}
 
     # ---- roofline of the dominant kernel -----------------------------------------
-    peaks, peak_src = load_peaks()
-    if w.bound == "tensor":
-        peak = FP8_PER_BF16 * peaks["bf16_tflops_sustained"]
-        achieved = flops / (kernel_ms_max * 1e-3) / 1e12
-        unit = "TFLOP/s"
-        basis = ("FP8 = %g x %s BF16 sustained (%.1f TF/s; kernel timed back to back in a long loop)"
-                 % (FP8_PER_BF16, peak_src, peaks["bf16_tflops_sustained"]))
-    else:
-        peak = peaks["hbm_gbs"]
-        achieved = algo_bytes / (kernel_ms_max * 1e-3) / 1e9
-        unit = "GB/s"
-        basis = "%s HBM copy bandwidth" % peak_src
-    traffic = profiled_traffic(w.name)
+    roof = roofline_of(w, flops, algo_bytes, kernel_ms_max, total_ms_max, peaks, peak_src)
     plan = planned_launch(w)
-    kernel_name = KERNEL_NAMES[plan["kernel"]]
-    roof = {"bound": w.bound, "achieved": achieved, "peak": peak, "unit": unit,
-            "frac": achieved / peak, "traffic": traffic, "kernel": kernel_name, "plan": plan,
-            "peak_basis": basis, "algorithmic_flop": flops, "algorithmic_bytes": algo_bytes,
-            "kernel_ms": kernel_ms_max}
-    if w.bound == "tensor":
-        roof["frac_of_nominal_4500"] = achieved / 4500.0
-    else:
-        roof["frac_of_nominal_8000"] = achieved / 8000.0
+    roof.update({"traffic": profiled_traffic(w.name), "kernel": KERNEL_NAMES[plan["kernel"]], "plan": plan})
+    roof = {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")} | \
+        {k: v for k, v in roof.items() if k not in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
 
     # ---- CPU baseline (rank 0, N = 1 only) ----------------------------------------
+    # The oracle, as it stands, on a bounded sample of the same workload; the
+    # rows (groups) it computed are then compared with the device run's D.
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        f, s, cores, desc = oracle_sample(w, inp, args.cpu_budget)
+        f, s, cores, desc, parity = oracle_sample(w, inp, args.cpu_budget, check_against=d_dev)
         cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-               "sample": desc + "; %.1f s" % s}
+               "sample": desc + "; %.1f s" % s, "parity": parity}
+        if not parity.startswith("ok"):
+            raise SystemExit("device output differs from the oracle on the sampled rows: " + parity)
+
+    per_config = None
+    if rank == 0 and world == 1 and not args.no_per_config:
+        del sets
+        torch.cuda.empty_cache()
+        known = {w.name: {"name": w.name, "kernel": roof["kernel"], "kernel_ms": kernel_ms_max,
+                          "achieved": roof["achieved"], "unit": roof["unit"], "frac": roof["frac"],
+                          "bound": roof["bound"], "steps": args.steps} |
+                 ({"frac_of_nominal_4500": roof["frac_of_nominal_4500"]} if w.bound == "tensor" else
+                  {"frac_of_nominal_8000": roof["frac_of_nominal_8000"]})}
+        per_config = run_per_config(device, stream, l2, peaks, peak_src, sampler, args.per_config_steps,
+                                    args.per_config_steps_hbm, use_graph, known=known)
+    if sampler:
+        sampler.stop()
 
     if rank == 0:
         line = {
@@ -687,7 +873,7 @@ def run_ours(args, w: Workload):
             "dtype": "fp8_e4m3" if w.fb == 0 else "fp8_e4m3xe5m2", "data": "synthetic",
             "config": {"workload": w.desc, "name": w.name, "flags": hex(w.flags),
                        "l2": "%d rotating input+output sets of %.1f MB (>= 3x the %d MB L2)"
-                             % (n_sets, set_bytes / 1e6, l2 >> 20),
+                             % (n_sets, set_bytes_of(w) / 1e6, l2 >> 20),
                        "parallelism": "independent shard per GPU" if world > 1 else "single GPU"},
             "roofline": roof,
             "cpu_baseline": cpu,
@@ -695,6 +881,7 @@ def run_ours(args, w: Workload):
             "gpu_launches": args.steps,
             "timing": "one CUDA graph of K launches" if use_graph else "K direct launches, events per launch",
             "clocks": clocks,
+            "per_config": per_config,
         }
         if w.kind == "masked":
             line["config"]["sum_masked_m"] = int(sum(mm))
@@ -711,10 +898,10 @@ def run_ours(args, w: Workload):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="dense4096")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--graph", choices=["on", "off"], default="on",
                     help="replay the K timed launches from one CUDA graph (off: K direct launches "
                          "with events around each)")
@@ -725,6 +912,12 @@ def main(argv=None):
     ap.add_argument("--e2e-streams", type=int, default=3,
                     help="streams the end-to-end steps alternate between (1 = strictly serial steps)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per_config array (every configuration of the pages, timed briefly)")
+    ap.add_argument("--per-config-steps", type=int, default=20,
+                    help="timed launches per tensor-bound configuration in per_config")
+    ap.add_argument("--per-config-steps-hbm", type=int, default=100,
+                    help="timed launches per HBM-bound configuration in per_config")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     args = ap.parse_args(argv)
     if args.warmup < 3:

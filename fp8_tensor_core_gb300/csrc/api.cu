@@ -89,12 +89,17 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
+std::atomic<int> g_have_device{0};   // set once a device has been seen (the count cannot drop later)
+
 int current_device(int *dev, DeviceInfo *info)
 {
-    int count = 0;
-    if (cudaGetDeviceCount(&count) != cudaSuccess || count <= 0) {
-        cudaGetLastError();
-        return FP8G_ERR_NO_DEVICE;
+    if (!g_have_device.load(std::memory_order_acquire)) {
+        int count = 0;
+        if (cudaGetDeviceCount(&count) != cudaSuccess || count <= 0) {
+            cudaGetLastError();
+            return FP8G_ERR_NO_DEVICE;
+        }
+        g_have_device.store(1, std::memory_order_release);
     }
     if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices)
         return FP8G_ERR_CUDA;
@@ -119,47 +124,137 @@ int current_device(int *dev, DeviceInfo *info)
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Tensor maps are encoded once per (base address, extents, box) and kept in
+// a small direct-mapped cache: a map is a pure function of those fields, so
+// a hit returns exactly what encoding would (a freed and reallocated buffer
+// at the same address with the same extents gets the same, correct map).
+// Encoding costs the host a driver call per operand; repeated calls with the
+// same buffers -- the serving and graph-building pattern -- skip it.
+struct MapKey {
+    const void *base;
+    uint64_t d0, d1, d2, ld;
+    uint32_t box0, box1;
+    uint32_t kind;   // 1: operand map (SWIZZLE_128B), 2: block-scale map
+    bool operator==(const MapKey &o) const
+    {
+        return base == o.base && d0 == o.d0 && d1 == o.d1 && d2 == o.d2 && ld == o.ld && box0 == o.box0 &&
+               box1 == o.box1 && kind == o.kind;
+    }
+};
+struct MapSlot {
+    MapKey key{};
+    CUtensorMap map;
+    bool used = false;
+};
+constexpr int kMapCacheSlots = 256;
+std::mutex g_map_mu;
+MapSlot g_maps[kMapCacheSlots];
+
+size_t map_slot(const MapKey &k)
+{
+    uint64_t h = reinterpret_cast<uintptr_t>(k.base) * 0x9E3779B97F4A7C15ull;
+    for (uint64_t v : {k.d0, k.d1, k.d2, k.ld, (static_cast<uint64_t>(k.box0) << 32) | k.box1,
+                       static_cast<uint64_t>(k.kind)})
+        h = (h ^ v) * 0x100000001B3ull;
+    return static_cast<size_t>((h ^ (h >> 29)) % kMapCacheSlots);
+}
+
+bool cached_map(CUtensorMap *m, const MapKey &key, bool (*encode)(CUtensorMap *, const MapKey &))
+{
+    const size_t i = map_slot(key);
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        if (g_maps[i].used && g_maps[i].key == key) {
+            *m = g_maps[i].map;
+            return true;
+        }
+    }
+    if (!encode(m, key))
+        return false;
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    g_maps[i].key = key;
+    g_maps[i].map = *m;
+    g_maps[i].used = true;
+    return true;
+}
+
 // 3-D map over a [groups, rows, k] byte tensor, box {128 bytes of K, box_rows, 1},
 // 128-byte swizzle, out-of-bounds elements read as zero.
-bool make_map(CUtensorMap *m, const void *base, int64_t k, int64_t rows, int64_t groups,
-              uint32_t box_rows)
+bool encode_operand(CUtensorMap *m, const MapKey &key)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc)
         return false;
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows),
-                                static_cast<cuuint64_t>(groups)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(k),
-                                   static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(k)};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kBlockK), box_rows, 1};
+    const cuuint64_t dims[3] = {key.d0, key.d1, key.d2};
+    const cuuint64_t strides[2] = {key.d0, key.d1 * key.d0};
+    const cuuint32_t box[3] = {key.box0, key.box1, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     std::memset(m, 0, sizeof(*m));
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(key.base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+bool make_map(CUtensorMap *m, const void *base, int64_t k, int64_t rows, int64_t groups, uint32_t box_rows)
+{
+    const MapKey key{base, static_cast<uint64_t>(k), static_cast<uint64_t>(rows), static_cast<uint64_t>(groups), 0,
+                     static_cast<uint32_t>(kBlockK), box_rows, 1u};
+    return cached_map(m, key, encode_operand);
 }
 
 // 3-D map over block scales [groups, ks, ld] bytes (row r of K group j at
 // byte r of that group's vector), box {box_rows, box_k, 1}, no swizzle,
 // rows >= `rows` and groups >= ks read as zero.
-bool make_sf_map(CUtensorMap *m, const void *base, int64_t rows, int64_t ks, int64_t groups, int64_t ld,
-                 uint32_t box_rows, uint32_t box_k)
+bool encode_scales(CUtensorMap *m, const MapKey &key)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc)
         return false;
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(ks),
-                                static_cast<cuuint64_t>(groups)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld),
-                                   static_cast<cuuint64_t>(ks) * static_cast<cuuint64_t>(ld)};
-    const cuuint32_t box[3] = {box_rows, box_k, 1};
+    const cuuint64_t dims[3] = {key.d0, key.d1, key.d2};
+    const cuuint64_t strides[2] = {key.ld, key.d1 * key.ld};
+    const cuuint32_t box[3] = {key.box0, key.box1, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     std::memset(m, 0, sizeof(*m));
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(key.base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+bool make_sf_map(CUtensorMap *m, const void *base, int64_t rows, int64_t ks, int64_t groups, int64_t ld,
+                 uint32_t box_rows, uint32_t box_k)
+{
+    const MapKey key{base, static_cast<uint64_t>(rows), static_cast<uint64_t>(ks), static_cast<uint64_t>(groups),
+                     static_cast<uint64_t>(ld), box_rows, box_k, 2u};
+    return cached_map(m, key, encode_scales);
+}
+
+// Device pointers already found to be device (or managed) memory: the
+// grouped calls check their masked_m / offsets pointer once per address
+// instead of asking the driver on every call.
+constexpr int kPtrCacheSlots = 64;
+std::mutex g_ptr_mu;
+const void *g_dev_ptrs[kPtrCacheSlots];
+
+bool is_device_pointer(const void *p)
+{
+    const size_t i = (reinterpret_cast<uintptr_t>(p) >> 4) % kPtrCacheSlots;
+    {
+        std::lock_guard<std::mutex> lk(g_ptr_mu);
+        if (g_dev_ptrs[i] == p)
+            return true;
+    }
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+        return false;
+    std::lock_guard<std::mutex> lk(g_ptr_mu);
+    g_dev_ptrs[i] = p;
+    return true;
 }
 
 // Stages that fit the per-block shared-memory budget beside the control
@@ -876,12 +971,7 @@ int grouped_ex(const void *A, const void *B, void *D, const int32_t *masked_m, i
     Problem p{A, B, D, masked_m, nullptr, G, M_max, N, K, hint, a_dtype, b_dtype, flags};
     if ((st = apply_scales(sc, G, M_max, N, p)) != FP8G_OK || (st = check_epilogue(epi, p)) != FP8G_OK)
         return st;
-    cudaPointerAttributes attr;
-    if (cudaPointerGetAttributes(&attr, masked_m) != cudaSuccess) {
-        cudaGetLastError();
-        return FP8G_ERR_INVALID_ARG;
-    }
-    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+    if (!is_device_pointer(masked_m))
         return FP8G_ERR_INVALID_ARG;
     return launch(p, stream);
 }
@@ -905,12 +995,7 @@ int contiguous_ex(const void *A, const void *B, void *D, const int32_t *offsets,
     Problem p{A, B, D, nullptr, offsets, G, M_total, N, K, hint, a_dtype, b_dtype, flags};
     if ((st = apply_scales(sc, G, M_total, N, p)) != FP8G_OK || (st = check_epilogue(epi, p)) != FP8G_OK)
         return st;
-    cudaPointerAttributes attr;
-    if (cudaPointerGetAttributes(&attr, offsets) != cudaSuccess) {
-        cudaGetLastError();
-        return FP8G_ERR_INVALID_ARG;
-    }
-    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+    if (!is_device_pointer(offsets))
         return FP8G_ERR_INVALID_ARG;
     return launch(p, stream);
 }

@@ -40,6 +40,8 @@
 // out the block records FP8G_ERR_TIMEOUT, every role leaves its loop, the
 // loader waits (bounded) for the copies it issued, the MMA issuer waits
 // (bounded) for its tensor-core work, TMEM is freed and the block returns.
+#include <atomic>
+
 #include <cuda_bf16.h>
 
 #include "fp8g.h"
@@ -1215,18 +1217,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
         return w;
     };
     // Next segment: tile (rasterised in bands of raster_band 256-row tiles,
-    // M fastest), this CTA's first row and the tile's first column.
+    // M fastest), this CTA's first row and the tile's first column.  The
+    // pair's stream-K range comes first, then its whole tiles: the partial
+    // tiles are then published early, and the contributor that completes a
+    // tile sums them in its epilogue while its MMA issuer already runs the
+    // next whole tile (with the range last, every reduction would wait for
+    // the end of the kernel and add its latency there).
     auto next_seg = [&](Walker &w, PairSeg &x) {
         int u;
-        if (w.u < dp_tiles) {
-            u = w.u;
-            x.kb0 = 0;
-            x.kb1 = num_kb;
-            x.kind = 0;
-            w.u += ncl;
-        } else {
-            if (w.pos >= w.end)
-                return false;
+        if (w.pos < w.end) {
             u = static_cast<int>(w.pos / num_kb);
             x.kb0 = static_cast<int>(w.pos - static_cast<long long>(u) * num_kb);
             const long long left = w.end - w.pos;
@@ -1234,6 +1233,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
             w.pos += x.kb1 - x.kb0;
             x.kind = w.first ? 0 : 1;
             w.first = false;
+        } else {
+            if (w.u >= dp_tiles)
+                return false;
+            u = w.u;
+            x.kb0 = 0;
+            x.kb1 = num_kb;
+            x.kind = 0;
+            w.u += ncl;
         }
         x.tile = u;
         int local = u, mt = m_tiles;
@@ -2231,6 +2238,8 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
 // =====================================================================================
 // Launchers
 // =====================================================================================
+constexpr int kSmemLimitDevices = 64;
+
 // Launch with programmatic stream serialisation (unless FP8G_NO_PDL): the
 // kernel may start while the previous launch in the stream finishes; it
 // waits (griddepcontrol.wait) before touching global memory.
@@ -2254,13 +2263,36 @@ static cudaError_t launch_pdl(Kernel kernel, int threads, int grid, size_t smem,
     return cudaGetLastError();
 }
 
+// The dynamic shared-memory limit of a kernel is a property of the kernel in
+// the device's context: set it once per device (and whenever a larger size
+// is wanted) instead of on every launch.
+template <typename Kernel>
+static cudaError_t set_smem_limit(Kernel kernel, size_t smem, std::atomic<int> *done)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const int want = static_cast<int>(smem);
+    const bool cached = dev >= 0 && dev < kSmemLimitDevices;
+    if (cached && done[dev].load(std::memory_order_acquire) >= want)
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
+    if (e == cudaSuccess && cached) {
+        int cur = done[dev].load(std::memory_order_relaxed);
+        while (cur < want && !done[dev].compare_exchange_weak(cur, want, std::memory_order_release))
+            ;
+    }
+    return e;
+}
+
 template <bool kBS, bool kEpi>
 static cudaError_t launch_mn_t(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const CUtensorMap &tm_sa,
                                const CUtensorMap &tm_sb, const GemmArgs &args, int grid, size_t smem,
                                cudaStream_t stream)
 {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_mn<kBS, kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    static std::atomic<int> done[kSmemLimitDevices];
+    cudaError_t e = set_smem_limit(k_gemm_mn<kBS, kEpi>, smem, done);
     if (e != cudaSuccess)
         return e;
     return launch_pdl(k_gemm_mn<kBS, kEpi>, kBS ? kThreadsTmemScaled : kThreads, grid, smem, stream, args, tm_a, tm_b,
@@ -2296,8 +2328,8 @@ static cudaError_t launch_mn2_t(const CUtensorMap &tm_a, const CUtensorMap &tm_b
                                 const CUtensorMap &tm_sb, const GemmArgs &args, int grid, size_t smem,
                                 cudaStream_t stream)
 {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_mn2<kBS, kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    static std::atomic<int> done[kSmemLimitDevices];
+    cudaError_t e = set_smem_limit(k_gemm_mn2<kBS, kEpi>, smem, done);
     if (e != cudaSuccess)
         return e;
     return launch_pdl(k_gemm_mn2<kBS, kEpi>, kBS ? kThreadsTmemScaled : kThreads, grid, smem, stream, args, tm_a, tm_b,
@@ -2326,8 +2358,8 @@ static cudaError_t launch_swap_t(const CUtensorMap &tm_w, const CUtensorMap &tm_
                                  const CUtensorMap &tm_st, const GemmArgs &args, int grid, size_t smem,
                                  cudaStream_t stream)
 {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_swap<kBS, kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    static std::atomic<int> done[kSmemLimitDevices];
+    cudaError_t e = set_smem_limit(k_gemm_swap<kBS, kEpi>, smem, done);
     if (e != cudaSuccess)
         return e;
     return launch_pdl(k_gemm_swap<kBS, kEpi>, kBS ? kThreadsTmemScaled : kThreads, grid, smem, stream, args, tm_w, tm_t,

@@ -53,6 +53,11 @@
  *    hand the same handle to a new stream.
  *  - fp8_gemm_nt_noalloc is the exception: all of its calls on a device
  *    share one fixed array (see there).
+ *  - Host cost: the TMA tensor maps of a call are cached by (base address,
+ *    extents, box), so repeated calls on the same buffers encode none; the
+ *    masked_m / group_offsets pointer of the grouped calls is checked to be
+ *    device memory once per address.  A buffer freed and reallocated at the
+ *    same address with the same extents gets the same, still correct map.
  *  - Not thread-safe for concurrent calls from several host threads on the
  *    same device while fp8g_set_wait_timeout_ns() is being changed.
  */

@@ -120,7 +120,7 @@ def _load():
         lib.oracle_gemm_blockscaled.restype = None
         lib.oracle_gemm_blockscaled.argtypes = [
             _u8p, _u8p, _i32p, _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _u8p, _i64,
-            _u8p, _i64, _i64, _u16p, _f64p, _f64p, ctypes.c_int]
+            _u8p, _i64, _i64, _u16p, _f64p, _f64p, _f64p, ctypes.c_int]
         lib.oracle_gemm_grouped_contiguous.restype = None
         lib.oracle_gemm_grouped_contiguous.argtypes = [_u8p, _u8p, _i32p, _i64, _i64, _i64, _i64, ctypes.c_int,
                                                        ctypes.c_int, _u16p, _f64p, _f64p, ctypes.c_int]
@@ -294,12 +294,16 @@ def gemm_grouped_masked_scaled(A: np.ndarray, B: np.ndarray, masked_m: np.ndarra
 
 def gemm_blockscaled(A: np.ndarray, B: np.ndarray, sfa: np.ndarray, sfb: np.ndarray,
                      gran: int = 128, masked_m=None, D_init=None, fa: int = E4M3, fb: int = E4M3,
-                     nthreads: int = 0, want_exact: bool = False):
+                     nthreads: int = 0, want_exact: bool = False, want_accbound: bool = False):
     """Block-scaled oracle.  Dense: A [M,K], B [N,K], sfa [KS,lda], sfb
     [KS,ldb] uint8 UE8M0 codes (KS = ceil(K/gran), row m of A scaled by
     sfa[k // gran, m]).  Grouped: A [G,M_max,K], B [G,N,K], sfa [G,KS,lda],
     sfb [G,KS,ldb], masked_m [G] (rows m >= masked_m[g] keep D_init's bits).
-    Returns (D_bf16, absdot[, exact sums])."""
+    Returns (D_bf16, absdot[, exact sums][, accbound]): accbound = 2^-23 *
+    sum |S_i| over the running sums S_i at the ends of the 32-element K
+    slices, the bound on the error of an FP32 accumulator that adds each
+    tensor-core instruction's result with at most one FP32 ulp of error
+    (the acc_bound term of check_bf16)."""
     dense = np.ndim(A) == 2
     A3 = np.ascontiguousarray(A, np.uint8).reshape((1,) + np.shape(A) if dense else np.shape(A))
     B3 = np.ascontiguousarray(B, np.uint8).reshape((1,) + np.shape(B) if dense else np.shape(B))
@@ -323,13 +327,14 @@ def gemm_blockscaled(A: np.ndarray, B: np.ndarray, sfa: np.ndarray, sfb: np.ndar
         D = np.array(D_init, np.uint16, copy=True, order="C").reshape(G, M_max, N)
     absdot = np.zeros((G, M_max, N), np.float64)
     exact = np.zeros((G, M_max, N), np.float64)
+    accb = np.zeros((G, M_max, N), np.float64)
     _load().oracle_gemm_blockscaled(_ptr(A3, _u8p), _ptr(B3, _u8p), mm_p, G, M_max, N, K, fa, fb,
                                     _ptr(SA, _u8p), lda, _ptr(SB, _u8p), ldb, gran, _ptr(D, _u16p),
-                                    _ptr(exact, _f64p), _ptr(absdot, _f64p), int(nthreads))
-    out = (D, absdot, exact)
+                                    _ptr(exact, _f64p), _ptr(absdot, _f64p), _ptr(accb, _f64p), int(nthreads))
+    out = (D, absdot) + ((exact,) if want_exact else ()) + ((accb,) if want_accbound else ())
     if dense:
         out = tuple(x[0] for x in out)
-    return out if want_exact else out[:2]
+    return out
 
 
 def gemm_grouped_contiguous(A: np.ndarray, B: np.ndarray, offsets: np.ndarray, D_init=None, fa: int = E4M3,
@@ -404,12 +409,16 @@ def ulp_bf16(ref_bits: np.ndarray) -> np.ndarray:
 
 
 def check_bf16(gpu_bits: np.ndarray, ref_bits: np.ndarray,
-               absdot: np.ndarray, rel: float = REL_TOL):
-    """Per-element acceptance: |gpu - ref| <= ulp_bf16(ref) + rel*absdot.
-    NaN or infinity on either side fails.  Returns (ok, report dict)."""
+               absdot: np.ndarray, rel: float = REL_TOL, acc_bound=None):
+    """Per-element acceptance: |gpu - ref| <= ulp_bf16(ref) + rel*absdot
+    (+ acc_bound, the accumulation-order bound gemm_blockscaled returns for
+    block-scaled products).  NaN or infinity on either side fails.  Returns
+    (ok, report dict)."""
     g = bf16_bits_to_f64(gpu_bits)
     r = bf16_bits_to_f64(ref_bits)
     tol = ulp_bf16(ref_bits) + rel * np.asarray(absdot, np.float64)
+    if acc_bound is not None:
+        tol = tol + np.asarray(acc_bound, np.float64)
     diff = np.abs(g - r)
     finite = np.isfinite(g) & np.isfinite(r)
     bad = (~finite) | (diff > tol)

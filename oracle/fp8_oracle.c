@@ -471,7 +471,19 @@ void oracle_gemm_grouped_masked_scaled(const uint8_t *A, const uint8_t *B,
  * SB is [G][KS][ldb].  A UE8M0 code is a power of two 2^(e-127); code 255 is
  * NaN (OCP microscaling formats).  Every product is exact in double; the sum
  * is taken in ascending k and rounded once.  absdot receives
- * sum_k |a_k b_k| * scales. */
+ * sum_k |a_k b_k| * scales.
+ *
+ * accbound (may be NULL) receives 2^-23 * sum_i |S_i|, S_i the running sum
+ * after the i-th slice of 32 consecutive k (the K of one tensor-core MMA
+ * instruction on 8-bit operands, "一次“转置”，半张算力" §1.1; a shorter last
+ * slice counts as one).  It bounds the error of a hardware accumulator that
+ * adds each instruction's result into an FP32 running sum with at most one
+ * FP32 ulp (2^-23 relative) of error per addition, whatever its rounding
+ * direction.  "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践"
+ * §5.1: FP32 accumulation still carries the rounding error of its order,
+ * largest when intermediate sums are much larger than the result, and the
+ * tensor core's accumulation path is fixed in hardware; block scales make
+ * exactly that case (products of one K group up to 2^28 times another's). */
 static double ue8m0_value(uint8_t e)
 {
     return e == 255 ? NAN : ldexp(1.0, (int)e - 127);
@@ -485,6 +497,7 @@ typedef struct {
     uint16_t *D;
     double *exact;     /* sums before rounding, may be NULL */
     double *absdot;
+    double *accbound;  /* 2^-23 * sum of |running sum| at 32-element slice ends, may be NULL */
 } bs_ctx;
 
 static void blockscaled_row(void *vctx, int64_t gm)
@@ -498,7 +511,7 @@ static void blockscaled_row(void *vctx, int64_t gm)
     for (int64_t n = 0; n < c->N; ++n) {
         const uint8_t *b = c->B + (g * c->N + n) * c->K;
         const uint8_t *sb = c->SB + g * c->KS * c->ldb + n;
-        double s = 0.0, ad = 0.0;
+        double s = 0.0, ad = 0.0, runs = 0.0;
         for (int64_t kg = 0; kg < c->KS; ++kg) {
             double f = ue8m0_value(sa[kg * c->lda]) * ue8m0_value(sb[kg * c->ldb]);
             int64_t k1 = (kg + 1) * c->gran < c->K ? (kg + 1) * c->gran : c->K;
@@ -506,6 +519,8 @@ static void blockscaled_row(void *vctx, int64_t gm)
                 double p = c->ta[a[k]] * c->tb[b[k]] * f;
                 s += p;
                 ad += fabs(p);
+                if ((k + 1) % 32 == 0 || k + 1 == c->K)
+                    runs += fabs(s);
             }
         }
         int64_t o = (g * c->M_max + m) * c->N + n;
@@ -514,6 +529,8 @@ static void blockscaled_row(void *vctx, int64_t gm)
             c->exact[o] = s;
         if (c->absdot)
             c->absdot[o] = ad;
+        if (c->accbound)
+            c->accbound[o] = ldexp(runs, -23);
     }
 }
 
@@ -522,7 +539,8 @@ static void blockscaled_row(void *vctx, int64_t gm)
 void oracle_gemm_blockscaled(const uint8_t *A, const uint8_t *B, const int32_t *masked_m,
                              int64_t G, int64_t M_max, int64_t N, int64_t K, int fa, int fb,
                              const uint8_t *SA, int64_t lda, const uint8_t *SB, int64_t ldb,
-                             int64_t gran, uint16_t *D, double *exact, double *absdot, int nthreads)
+                             int64_t gran, uint16_t *D, double *exact, double *absdot, double *accbound,
+                             int nthreads)
 {
     bs_ctx c;
     c.A = A;
@@ -543,6 +561,7 @@ void oracle_gemm_blockscaled(const uint8_t *A, const uint8_t *B, const int32_t *
     c.D = D;
     c.exact = exact;
     c.absdot = absdot;
+    c.accbound = accbound;
     run_rows(blockscaled_row, &c, G * M_max, nthreads);
 }
 

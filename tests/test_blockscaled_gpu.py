@@ -66,8 +66,8 @@ def check_dense_bs(M, N, K, gran, flags, seed, fa=E4, fb=E4, pad=16):
                                      b_dtype=fb, flags=flags)
     torch.cuda.synchronize()
     assert_status_ok()
-    ref, absdot = oracle.gemm_blockscaled(A, B, sfa, sfb, gran, fa=fa, fb=fb)
-    ok, rep = oracle.check_bf16(bits(D), ref, absdot)
+    ref, absdot, accb = oracle.gemm_blockscaled(A, B, sfa, sfb, gran, fa=fa, fb=fb, want_accbound=True)
+    ok, rep = oracle.check_bf16(bits(D), ref, absdot, acc_bound=accb)
     assert ok, rep
     return rep
 
@@ -184,8 +184,8 @@ def test_scales_reach_the_right_k_group():
                                                  a_dtype=E4, b_dtype=E4, flags=flags)
                 torch.cuda.synchronize()
                 assert_status_ok()
-                ref, absdot = oracle.gemm_blockscaled(A, B, sfa, sfb, gran)
-                ok, rep = oracle.check_bf16(bits(D), ref, absdot)
+                ref, absdot, accb = oracle.gemm_blockscaled(A, B, sfa, sfb, gran, want_accbound=True)
+                ok, rep = oracle.check_bf16(bits(D), ref, absdot, acc_bound=accb)
                 assert ok, (gran, j, flags, rep)
 
 
@@ -227,10 +227,11 @@ def grouped_bs_case(G, M_max, N, K, mm, gran, flags, hint, seed, fa=E4, fb=E4):
     torch.cuda.synchronize()
     assert_status_ok()
     got = bits(Dt)
-    ref, absdot = oracle.gemm_blockscaled(A, B, sfa, sfb, gran, masked_m=mm, D_init=D0, fa=fa, fb=fb)
+    ref, absdot, accb = oracle.gemm_blockscaled(A, B, sfa, sfb, gran, masked_m=mm, D_init=D0, fa=fa, fb=fb,
+                                                want_accbound=True)
     for g in range(G):
         m = mm[g]
-        ok, rep = oracle.check_bf16(got[g, :m], ref[g, :m], absdot[g, :m])
+        ok, rep = oracle.check_bf16(got[g, :m], ref[g, :m], absdot[g, :m], acc_bound=accb[g, :m])
         assert ok, (g, rep)
         assert np.array_equal(got[g, m:], D0[g, m:]), "padding rows of group %d written" % g
 

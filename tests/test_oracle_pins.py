@@ -448,6 +448,63 @@ def test_blockscaled_exact_rational_bruteforce(M, N, K, gran):
             assert absdot[m, n] == float(sum(abs(t) for t in terms))
 
 
+@pytest.mark.parametrize("K,slices", [(128, [32, 64, 96, 128]), (80, [32, 64, 80]), (32, [32]), (16, [16])])
+def test_blockscaled_accbound_closed_form(K, slices):
+    """All-ones operands with unit scales: the running sum after each
+    32-element slice is its length, so the bound is 2^-23 times the sum of
+    the slice ends (a shorter last slice counted once)."""
+    A = np.full((2, K), 0x38, np.uint8)        # E4M3 1.0
+    B = np.full((3, K), 0x38, np.uint8)
+    KS = -(-K // 32)
+    one = np.full((KS, 16), 127, np.uint8)
+    D, absdot, accb = oracle.gemm_blockscaled(A, B, one, one, 32, want_accbound=True)
+    assert np.all(absdot == K)
+    assert np.all(accb == math.ldexp(sum(slices), -23))
+
+
+def _fp32_accumulate(parts, mode):
+    """A float32 accumulator that adds each exact slice sum with one rounding,
+    to nearest even or toward zero."""
+    acc = np.zeros(parts.shape[:-1], np.float64)
+    for i in range(parts.shape[-1]):
+        x = acc + parts[..., i]                    # exact: both terms are float32 / short sums
+        r = x.astype(np.float32).astype(np.float64)
+        if mode == "rz":
+            over = np.abs(r) > np.abs(x)
+            r = np.where(over, np.nextafter(r.astype(np.float32), np.float32(0)).astype(np.float64), r)
+        acc = r
+    return acc
+
+
+@pytest.mark.parametrize("gran", [32, 128])
+def test_blockscaled_accbound_bounds_fp32_accumulation(gran):
+    """The bound holds for an FP32 accumulator that adds each 32-element
+    slice's exact sum with one rounding -- toward zero (the worst direction)
+    or to nearest -- on data whose K groups differ by up to 2^28 in scale,
+    and never exceeds the crude bound n * 2^-23 * sum |a b| that ignores the
+    running sums."""
+    M, N, K = 12, 20, 1024
+    A = _rand_codes((M, K), 331, 0)
+    B = _rand_codes((N, K), 332, 0)
+    KS = -(-K // gran)
+    sfa = _ue8m0((KS, M + 4), 333, 113, 141)
+    sfb = _ue8m0((KS, N + 12), 334, 113, 141)
+    D, absdot, exact, accb = oracle.gemm_blockscaled(A, B, sfa, sfb, gran, want_exact=True, want_accbound=True)
+    da, db = torch_decode(A, 0), torch_decode(B, 0)
+    g = np.arange(K) // gran
+    sa = np.ldexp(1.0, sfa[g, :M].T.astype(np.int64) - 127)          # [M, K]
+    sb = np.ldexp(1.0, sfb[g, :N].T.astype(np.int64) - 127)          # [N, K]
+    prod = (da * sa)[:, None, :] * (db * sb)[None, :, :]             # [M, N, K], exact
+    parts = prod.reshape(M, N, K // 32, 32).sum(axis=-1)             # exact: one scale pair per slice
+    worst = 0.0
+    for mode in ("rz", "rn"):
+        err = np.abs(_fp32_accumulate(parts, mode) - exact)
+        assert np.all(err <= accb), mode
+        worst = max(worst, float((err / accb).max()))
+    assert worst > 0.05                              # the bound is not vacuous on this data
+    assert np.all(accb <= (K // 32) * 2.0 ** -23 * absdot * (1 + 1e-12))
+
+
 @pytest.mark.parametrize("gran", [32, 128])
 def test_blockscaled_unit_scales_equal_unscaled(gran):
     A = _rand_codes((20, 200), 311, 0)

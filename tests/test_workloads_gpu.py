@@ -125,10 +125,10 @@ def test_blockscaled_workload(name):
         got = bits(D)
         for r0 in range(0, w.M, ROW_BLOCK):
             r1 = min(w.M, r0 + ROW_BLOCK)
-            ref, absdot = oracle.gemm_blockscaled(inp["A"][r0:r1], inp["B"],
-                                                  np.ascontiguousarray(inp["sf_a"][0][:, r0:r1]), inp["sf_b"][0],
-                                                  w.gran, fa=w.fa, fb=w.fb)
-            ok, rep = oracle.check_bf16(got[r0:r1], ref, absdot)
+            ref, absdot, accb = oracle.gemm_blockscaled(inp["A"][r0:r1], inp["B"],
+                                                        np.ascontiguousarray(inp["sf_a"][0][:, r0:r1]),
+                                                        inp["sf_b"][0], w.gran, fa=w.fa, fb=w.fb, want_accbound=True)
+            ok, rep = oracle.check_bf16(got[r0:r1], ref, absdot, acc_bound=accb)
             assert ok, (r0, rep)
         return
     mm = inp["masked_m"]
@@ -141,10 +141,10 @@ def test_blockscaled_workload(name):
     st = fp8g.fp8g_get_device_status()
     assert st[0] == fp8g.OK, st
     got = bits(Dt)
-    ref, absdot = oracle.gemm_blockscaled(inp["A"], inp["B"], inp["sf_a"], inp["sf_b"], w.gran, masked_m=mm,
-                                          D_init=D0, fa=w.fa, fb=w.fb)
+    ref, absdot, accb = oracle.gemm_blockscaled(inp["A"], inp["B"], inp["sf_a"], inp["sf_b"], w.gran, masked_m=mm,
+                                                D_init=D0, fa=w.fa, fb=w.fb, want_accbound=True)
     for g in range(w.G):
         m = int(mm[g])
-        ok, rep = oracle.check_bf16(got[g, :m], ref[g, :m], absdot[g, :m])
+        ok, rep = oracle.check_bf16(got[g, :m], ref[g, :m], absdot[g, :m], acc_bound=accb[g, :m])
         assert ok, (g, rep)
         assert np.array_equal(got[g, m:], D0[g, m:]), "padding rows of group %d written" % g
