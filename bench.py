@@ -95,6 +95,15 @@ def _make_base_workload(name: str, rank: int = 0) -> Workload:
         return Workload(name, "dense", "dense GEMM M=N=K=256, A,B E4M3 from U[-2,2]",
                         M=256, N=256, K=256, fa=synth.E4M3, fb=synth.E4M3, dist="uniform", std=None,
                         seed=synth.seed_for(0, rank), bound="tensor", flags=0)
+    if name.startswith("dense:"):
+        # dense:M:N:K[:e5m2] -- any dense shape, A and B from N(0,1)
+        parts = name.split(":")
+        M, N, K = int(parts[1]), int(parts[2]), int(parts[3])
+        fb = synth.E5M2 if len(parts) > 4 and parts[4] == "e5m2" else synth.E4M3
+        bound = "tensor" if 2.0 * M * N * K / (M * K + N * K + 2.0 * M * N) > 500 else "hbm"
+        return Workload(name, "dense", "dense GEMM M=%d N=%d K=%d, A E4M3, B %s, N(0,1)"
+                        % (M, N, K, "E5M2" if fb else "E4M3"), M=M, N=N, K=K, fa=synth.E4M3, fb=fb,
+                        dist="normal", std=1.0, seed=synth.seed_for(7, rank), bound=bound, flags=0)
     if name.startswith("proj"):
         # proj:N:K[:e5m2]  -- M=8192 token projection shapes
         parts = name.split(":")

@@ -34,7 +34,7 @@ class Epilogue(ctypes.Structure):
 class Plan(ctypes.Structure):
     """fp8g_plan: the launch the library would make for a problem."""
     _fields_ = [(name, ctypes.c_int32) for name in ("kernel", "tile_n", "stages", "stream_k", "mma_issuers",
-                                                     "shared_sm", "token_box", "grid")]
+                                                     "shared_sm", "token_box", "grid", "k_split")]
 
 
 _scales_p = ctypes.POINTER(Scales)

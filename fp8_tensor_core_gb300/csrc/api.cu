@@ -381,21 +381,31 @@ int pick_tile_n(int64_t m_tiles_total, int64_t N, int sms, int max_tn = 256)
 // instruction over fewer columns (measured per unit of width: 192 wide
 // ~18 % slower per K block; a 224-wide K block takes as long as a 256-wide
 // one -- 4096^3 in four waves of either: 48.2 vs 47.8 us at 2.07 GHz, and
-// 50.2 vs 49.5 us under the sustained power cap);
-// whole tiles pay for the last partial wave of pairs.  Stream-K for the last
-// wave is only used when FP8G_STREAM_K asks for it: reducing 256-wide FP32
-// partial tiles (128 KB per CTA per contributor) is latency-bound and cost
-// more than the wave it saves on every shape measured.
+// 50.2 vs 49.5 us under the sustained power cap).  Whole tiles pay for the
+// last partial wave of pairs.  When that wave holds at most half as many
+// tiles as there are pairs, each of its tiles can instead be split s ways
+// along K (s ranges of num_kb / s K blocks, at least kMinSplitKb each, on
+// s x tail pairs, run before the pairs' whole tiles); the last contributor
+// of a tile adds the others' FP32 partial tiles to its own while its MMA
+// issuer runs the next whole tile, which the model counts as
+// kSplitOverheadKb K blocks.  Stream-K over every pair (FP8G_STREAM_K)
+// spreads the wave over all pairs but leaves ~3 contributors a tile, whose
+// reduction took longer than the whole tile it overlaps (4096^3: 58.7 us
+// against 48.1), so it stays opt-in; FP8G_WHOLE_TILES keeps whole tiles.
+constexpr int kMaxTailSplit = 4;
+constexpr int kMinSplitKb = 8;
+constexpr double kSplitOverheadKb = 2.0;
+
 struct PairPlan {
     int tile_n;
-    bool stream_k;
+    int k_split;   // GemmArgs::k_splits of the SM-pair kernel: 1 whole tiles, 0 stream-K, >= 2 tail split
 };
 
-PairPlan plan_pair(int64_t m_tiles2, int64_t N, int num_kb, int pairs, uint32_t flags, int max_tn = 256)
+PairPlan plan_pair(int64_t m_tiles2, int64_t N, int num_kb, int pairs, uint32_t flags, int max_tn, bool allow_split)
 {
     static const int cands[] = {256, 224, 192, 160, 128};
     static const double cost_per_kb[] = {1.0, 1.15, 1.18, 1.30, 1.45};
-    PairPlan best{max_tn, false};
+    PairPlan best{max_tn, 1};
     double best_cost = 1e300;
     const int tn_override = static_cast<int>((flags >> 16) & 15u);
     for (int i = 0; i < 5; ++i) {
@@ -409,21 +419,35 @@ PairPlan plan_pair(int64_t m_tiles2, int64_t N, int num_kb, int pairs, uint32_t 
         const double dp = static_cast<double>(cdiv(units, pairs)) * num_kb * cost_per_kb[i] * width;
         if (dp < best_cost - 1e-9) {
             best_cost = dp;
-            best = {tn, false};
+            best = {tn, 1};
         }
-        if ((flags & FP8G_STREAM_K) && units % pairs != 0) {
+        const int64_t tail = units % pairs;
+        if (!allow_split || tail == 0 || (flags & FP8G_WHOLE_TILES))
+            continue;
+        if (flags & FP8G_STREAM_K) {
             // complete waves of whole tiles, then the last wave's tiles split evenly
             const double sk = (static_cast<double>(units / pairs) * num_kb +
-                               static_cast<double>(units % pairs) * num_kb / pairs + 3.0) *
+                               static_cast<double>(tail) * num_kb / pairs + 3.0) *
                               cost_per_kb[i] * width;
             if (sk < best_cost - 1e-9) {
                 best_cost = sk;
-                best = {tn, true};
+                best = {tn, 0};
+            }
+            continue;
+        }
+        const int s = static_cast<int>(std::min<int64_t>({kMaxTailSplit, pairs / tail, num_kb / kMinSplitKb}));
+        if (s >= 2) {
+            const double split = (static_cast<double>(units / pairs) * num_kb + static_cast<double>(num_kb) / s +
+                                  kSplitOverheadKb) *
+                                 cost_per_kb[i] * width;
+            if (split < best_cost - 1e-9) {
+                best_cost = split;
+                best = {tn, s};
             }
         }
     }
     if (tn_override >= 1 && tn_override <= 8 && best.tile_n != std::min(32 * tn_override, max_tn))
-        best = {std::min(32 * tn_override, max_tn), false};
+        best = {std::min(32 * tn_override, max_tn), 1};
     return best;
 }
 
@@ -594,6 +618,7 @@ void describe_as(fp8g_plan *out, int kernel, int tile_n, const GemmArgs &args, b
     out->shared_sm = shared_sm ? 1 : 0;
     out->token_box = token_box;
     out->grid = grid;
+    out->k_split = stream_k ? 0 : 1;
 }
 
 // Plans and enqueues the launch for `p`.  With `forced`, plans for that
@@ -767,14 +792,15 @@ int launch(const Problem &p, cudaStream_t stream, const DeviceInfo *forced = nul
                                          : cdiv(p.rows_a, 2 * kTileM);
         const int64_t m_tiles2_plan = grouped ? p.G * cdiv(std::max<int64_t>(group_tokens, 1), 2 * kTileM) : m_tiles2;
         const int pairs = info.sms / 2;
-        const PairPlan plan = plan_pair(m_tiles2_plan, p.N, num_kb, pairs, grouped ? (p.flags & ~FP8G_STREAM_K) : p.flags,
-                                        p.sf_k ? kMaxBlockScaledTile : 256);
+        const PairPlan plan = plan_pair(m_tiles2_plan, p.N, num_kb, pairs, p.flags, p.sf_k ? kMaxBlockScaledTile : 256,
+                                        !grouped);
         const int tile_n = plan.tile_n;
         const int64_t units = m_tiles2 * cdiv(p.N, tile_n);
         if (units > kMaxDim || units * num_kb > (int64_t(1) << 53))
             return FP8G_ERR_UNSUPPORTED;
         args.tile_n = tile_n;
-        args.k_splits = plan.stream_k ? 0 : 1;
+        args.k_splits = plan.k_split;
+        const bool split_k = plan.k_split != 1;
         if (p.sf_k) {
             // Operand tiles (own 128 A rows, half of the B rows), then the scale
             // area for 128 A rows and the whole tile's tile_n B rows.
@@ -801,9 +827,17 @@ int launch(const Problem &p, cudaStream_t stream, const DeviceInfo *forced = nul
         }
         const int64_t band = (48ll << 20) / (2 * kTileM * p.K);
         args.raster_band = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(band, m_tiles2)));
-        const int grid = 2 * static_cast<int>(std::min<int64_t>(plan.stream_k ? units * num_kb : units, pairs));
+        // Pairs with work: every pair for stream-K (or whole tiles beyond one
+        // wave); with a tail split, the pairs of the whole waves or the split
+        // tail's s ranges per tile, whichever is more.
+        const int64_t busy = plan.k_split == 0 ? units * num_kb
+                                               : (plan.k_split >= 2 ? std::max(units - units % pairs,
+                                                                               units % pairs * plan.k_split)
+                                                                    : units);
+        const int grid = 2 * static_cast<int>(std::min<int64_t>(busy, pairs));
         if (describe) {
-            describe_as(describe, FP8G_KERNEL_SM_PAIRS, tile_n, args, plan.stream_k, false, kTileM, grid);
+            describe_as(describe, FP8G_KERNEL_SM_PAIRS, tile_n, args, split_k, false, kTileM, grid);
+            describe->k_split = plan.k_split;
             return FP8G_OK;
         }
         if (!make_map(&tm0, p.A, p.K, p.rows_a, p.group_offsets ? 1 : p.G, kTileM) ||
@@ -817,12 +851,9 @@ int launch(const Problem &p, cudaStream_t stream, const DeviceInfo *forced = nul
             tm2 = tm0;
             tm3 = tm1;
         }
-        // (stream-K implies units is not a multiple of the pairs, so every
-        // pair of the grid exists for the remainder's partition)
-        if (plan.stream_k) {
+        if (split_k) {
             st = ensure_workspace(dev, stream, static_cast<size_t>(grid) * 2 * kTileM * tile_n * sizeof(float),
-                                  static_cast<size_t>(units) * 8 * sizeof(int32_t), &args.workspace,
-                                  &args.counters);
+                                  pair_counter_bytes(units), &args.workspace, &args.counters);
             if (st != FP8G_OK)
                 return st;
         }
@@ -1139,11 +1170,12 @@ extern "C" int fp8g_init(int64_t max_tiles, cudaStream_t stream)
     const int64_t tiles = max_tiles ? max_tiles : kDefaultInitTiles;
     // The largest partial-tile area any launch takes: two FP32 tiles of 128
     // x 256 per CTA, one CTA per SM (SwapAB chunks and SM-pair tiles are at
-    // most 256 wide); one counter pair per (tile, epilogue warp).
+    // most 256 wide); counters as the SM-pair kernel counts them (one pair
+    // per tile, CTA and epilogue warp; the SwapAB kernel needs half that).
     const size_t ws_bytes = static_cast<size_t>(info.sms) * 2 * kTileM * 256 * sizeof(float);
     float *ws = nullptr;
     int32_t *counters = nullptr;
-    return ensure_workspace(dev, stream, ws_bytes, swap_counter_bytes(tiles), &ws, &counters);
+    return ensure_workspace(dev, stream, ws_bytes, pair_counter_bytes(tiles), &ws, &counters);
 }
 
 extern "C" int fp8g_release_stream(cudaStream_t stream)

@@ -1190,11 +1190,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
         __syncthreads();
         total = ctl.units_total;
     }
-    // Whole-tile waves, then the stream-K remainder [sk0, sk0 + T).
+    // Whole-tile waves, and the K blocks of the remaining tiles [sk0, sk0 + T)
+    // split into P equal ranges: over every pair (k_splits == 0, stream-K),
+    // or k_splits ranges per remaining tile (k_splits >= 2: each tile of the
+    // last partial wave is split k_splits ways along K).
     const int dp_tiles = stream_k && !grouped ? (total / ncl) * ncl : total;
     const long long sk0 = static_cast<long long>(dp_tiles) * num_kb;
     const long long T = static_cast<long long>(total - dp_tiles) * num_kb;
-    const long long P = T < static_cast<long long>(ncl) ? T : static_cast<long long>(ncl);
+    long long P = T < static_cast<long long>(ncl) ? T : static_cast<long long>(ncl);
+    if (a.k_splits >= 2) {
+        const long long want = static_cast<long long>(a.k_splits) * (total - dp_tiles);
+        P = want < P ? want : P;
+    }
 
     // Only called when T > 0 (a stream-K segment exists).
     auto range_begin = [&](long long c) { return sk0 + c * T / P; };
@@ -1584,72 +1591,83 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
                     store_rows32<kEpi>(a, dout, r, rf, x.g, grow, row_ok, x.n0 + c, tg);
                 }
             } else {
-                float4 *mine = slots + (static_cast<int64_t>(blockIdx.x) * 2 + x.kind) * part4;
-                for (int c = 0; c < a.tile_n; c += 32) {
-                    uint32_t r[32];
-                    ld32(c, r);
-#pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        mine[(c / 4 + v) * kTileM + row] =
-                            make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                        __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-                }
-                __threadfence();
-                __syncwarp();
-                const int64_t cnt = (static_cast<int64_t>(x.tile) * 2 + rank) * 4 + q;
-                int prev = 0;
-                if (lane == 0)
-                    prev = atomicAdd(a.counters + cnt, 1);
-                prev = __shfl_sync(0xffffffffu, prev, 0);
+                // Contributors of this tile: the pairs whose ranges meet it,
+                // in K order.  Pairs after the first start their range inside
+                // this tile (slot kind 0); only the first pair's range may
+                // have begun in an earlier tile.
                 const long long t0 = static_cast<long long>(x.tile) * num_kb;
                 const int first = pair_of(t0);
                 const int n_contrib = pair_of(t0 + num_kb - 1) - first + 1;
-                // Pairs after the first start their range inside this tile
-                // (slot kind 0); only the first pair's range may have begun
-                // in an earlier tile.
                 const int kind_first = range_begin(first) >= t0 ? 0 : 1;
-                if (prev == n_contrib - 1) {
-                    // Tile complete: sum the contributions in K order, two
-                    // contributors' 32 columns per batch (unconditional loads).
-                    __threadfence();
-                    if (lane == 0)
-                        a.counters[cnt] = 0;   // ready for the next launch
+                // Per (tile, CTA rank, epilogue warp): {arrived, published}.
+                // Every contributor arrives; all but the last then publish
+                // their FP32 partial tile and count it as published.  The
+                // last arriver publishes nothing: it waits (bounded) until the
+                // others' partials are out -- they have all arrived, so none
+                // of them waits on anything -- and sums them with its own,
+                // still in TMEM, in K order.
+                int32_t *cnt = a.counters + ((static_cast<int64_t>(x.tile) * 2 + rank) * 4 + q) * 2;
+                int prev = 0;
+                if (lane == 0)
+                    prev = atomicAdd(cnt, 1);
+                prev = __shfl_sync(0xffffffffu, prev, 0);
+                if (prev != n_contrib - 1) {
+                    float4 *mine = slots + (static_cast<int64_t>(blockIdx.x) * 2 + x.kind) * part4;
                     for (int c = 0; c < a.tile_n; c += 32) {
-                        float acc_v[32];
-                        for (int p0 = 0; p0 < n_contrib; p0 += 2) {
-                            float4 buf[2][8];
+                        uint32_t r[32];
+                        ld32(c, r);
 #pragma unroll
-                            for (int i = 0; i < 2; ++i) {
-                                const int ci = (p0 + i < n_contrib) ? p0 + i : 0;
-                                const int pr = first + ci;
-                                const int kind = ci == 0 ? kind_first : 0;
+                        for (int v = 0; v < 8; ++v)
+                            mine[(c / 4 + v) * kTileM + row] =
+                                make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                            __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                    }
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0)
+                        atomicAdd(cnt + 1, 1);
+                } else {
+                    int ok = 1;
+                    if (lane == 0) {
+                        ok = wait_count_at_least(cnt + 1, n_contrib - 1, a.timeout_ns) ? 1 : 0;
+                        if (!ok) {
+                            ctl.abort = 1;
+                            record_status(FP8G_ERR_TIMEOUT, kRoleEpilogue, 500 + q);
+                        }
+                        cnt[0] = 0;   // ready for the next launch
+                        cnt[1] = 0;
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    __threadfence();
+                    const int me = cid - first;   // this pair's place in K order
+                    for (int c = 0; c < a.tile_n && ok; c += 32) {
+                        uint32_t own[32];
+                        ld32(c, own);
+                        float acc_v[32];
+                        for (int i = 0; i < n_contrib; ++i) {
+                            float part[32];
+                            if (i == me) {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    part[j] = __uint_as_float(own[j]);
+                            } else {
+                                const int kind = i == 0 ? kind_first : 0;
                                 const float4 *src = slots +
-                                                    ((static_cast<int64_t>(2 * pr) + rank) * 2 + kind) * part4 +
+                                                    ((static_cast<int64_t>(2 * (first + i)) + rank) * 2 + kind) *
+                                                        part4 +
                                                     (c / 4) * kTileM + row;
 #pragma unroll
-                                for (int v = 0; v < 8; ++v)
-                                    buf[i][v] = __ldcg(src + v * kTileM);
-                            }
-#pragma unroll
-                            for (int i = 0; i < 2; ++i) {
-                                if (p0 + i >= n_contrib)
-                                    break;
-#pragma unroll
                                 for (int v = 0; v < 8; ++v) {
-                                    const float4 f = buf[i][v];
-                                    if (p0 + i == 0) {
-                                        acc_v[4 * v] = f.x;
-                                        acc_v[4 * v + 1] = f.y;
-                                        acc_v[4 * v + 2] = f.z;
-                                        acc_v[4 * v + 3] = f.w;
-                                    } else {
-                                        acc_v[4 * v] += f.x;
-                                        acc_v[4 * v + 1] += f.y;
-                                        acc_v[4 * v + 2] += f.z;
-                                        acc_v[4 * v + 3] += f.w;
-                                    }
+                                    const float4 f = __ldcg(src + v * kTileM);
+                                    part[4 * v] = f.x;
+                                    part[4 * v + 1] = f.y;
+                                    part[4 * v + 2] = f.z;
+                                    part[4 * v + 3] = f.w;
                                 }
                             }
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                acc_v[j] = i == 0 ? part[j] : acc_v[j] + part[j];
                         }
                         uint32_t bits_v[32];
 #pragma unroll

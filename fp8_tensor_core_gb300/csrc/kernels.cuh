@@ -62,7 +62,10 @@ struct GemmArgs {
     int32_t stages;            // pipeline depth (1..kMaxStages)
     int32_t stage_bytes;       // bytes per stage (multiple of 1024)
     int32_t k_splits;          // swap kernel: 1 = whole tiles per unit; otherwise stream-K
-                               // (equal k-block ranges per CTA, partial tiles reduced)
+                               // (equal k-block ranges per CTA, partial tiles reduced).
+                               // SM-pair kernel: 1 = whole tiles; 0 = the tiles of the last
+                               // partial wave stream-K over every pair; s >= 2 = each of those
+                               // tiles split s ways along K (s ranges per tile)
     int32_t raster_band;       // mn kernel: M tiles per rasterisation band
     int32_t tmem_cols;         // swap kernel: 256 (two 128-column accumulators, two CTAs
                                // may share an SM) or 512 (default)
@@ -110,8 +113,8 @@ struct GemmArgs {
     const float *bias;
     float *workspace;          // swap kernel, stream-K: 2 FP32 partial tiles per CTA
                                // (128 x tile_n floats each)
-    int32_t *counters;         // stream-K: per (tile, epilogue warp) counters, zero at rest
-                               // (SwapAB: arrived and published; SM pair: arrivals)
+    int32_t *counters;         // stream-K: {arrived, published} per (tile, epilogue warp) (SwapAB)
+                               // or per (tile, CTA of the pair, epilogue warp) (SM pair); zero at rest
 };
 
 // Block-scaled stage layout.  After the two operand tiles (MMA side A: 128
@@ -152,6 +155,8 @@ inline size_t swap_partials_bytes(int grid, int tile_n)
 }
 // Two counters (arrived, published) per (tile, epilogue warp).
 inline size_t swap_counter_bytes(long long tiles) { return static_cast<size_t>(tiles) * 8 * sizeof(int32_t); }
+// SM-pair kernel: two counters per (tile, CTA of the pair, epilogue warp).
+inline size_t pair_counter_bytes(long long tiles) { return static_cast<size_t>(tiles) * 16 * sizeof(int32_t); }
 
 // Status word of the current device: read it, then clear it.
 cudaError_t read_and_clear_status(int32_t info[4]);

@@ -372,7 +372,7 @@ int fp8g_get_device_status(int32_t *info, cudaStream_t stream);
  * fp8g_init -- allocate, on the current device, the stream-K workspace of
  * `stream` at its largest size: partial tiles for every SM (2 x SMs x 128 x
  * 256 FP32, 39.8 MB on 152 SMs) and arrival counters for up to `max_tiles`
- * output tiles of one launch (0 = 65536; 32 bytes a tile).  A stream-K
+ * output tiles of one launch (0 = 65536; 64 bytes a tile).  A stream-K
  * launch is one with SwapAB (output tiles = groups x token chunks x
  * ceil(N / 128)) or split SM-pair tiles (ceil(M / 256) x ceil(N / tile)).
  * The calls allocate a stream's workspace themselves on its first need;
@@ -475,11 +475,16 @@ typedef struct fp8g_plan {
     int32_t kernel;      /* FP8G_KERNEL_* */
     int32_t tile_n;      /* N tile (token tiles, SM pairs) or token chunk (SwapAB) */
     int32_t stages;      /* shared-memory pipeline stages */
-    int32_t stream_k;    /* 1: K blocks split evenly over the CTAs; 0: whole tiles */
+    int32_t stream_k;    /* 1: some tiles' K blocks split over several CTAs (stream-K or a
+                            split last wave); 0: whole tiles */
     int32_t mma_issuers; /* threads issuing MMAs per tile: 1 or 2 */
     int32_t shared_sm;   /* 1: half the shared memory, two CTAs may share an SM */
     int32_t token_box;   /* token rows per TMA copy (SwapAB; token tiles: A rows) */
     int32_t grid;        /* CTAs launched */
+    int32_t k_split;     /* SM pairs: 1 whole tiles; s >= 2: each tile of the last partial wave
+                            split s ways along K (run first, summed by its last contributor);
+                            0: that wave stream-K over every pair.  Other kernels: 1, or 0 for
+                            stream-K */
 } fp8g_plan;
 int fp8g_describe_plan(int layout, int64_t G, int64_t rows, int64_t N, int64_t K, int64_t token_hint,
                        int sf_group_k, uint32_t flags, int sms, int smem_optin, fp8g_plan *out);

@@ -152,8 +152,12 @@ def _plan(layout, G, rows, N, K, hint=0, sf=0, flags=0):
 
 
 @pytest.mark.parametrize("args,expect", [
-    # dense 4096^3: SM-pair tiles 256 wide, whole tiles
-    ((0, 1, 4096, 4096, 4096), dict(kernel=1, tile_n=256, stream_k=0)),
+    # dense 4096^3: SM-pair tiles 256 wide, three whole waves and the last 28
+    # tiles split two ways along K; the 8192-row projections: the 18432 x 7168
+    # one splits its last 24 tiles three ways, 7168 x 18432 (60 left) none
+    ((0, 1, 4096, 4096, 4096), dict(kernel=1, tile_n=256, stream_k=1, k_split=2, grid=152)),
+    ((0, 1, 8192, 18432, 7168), dict(kernel=1, tile_n=256, k_split=3)),
+    ((0, 1, 8192, 7168, 18432), dict(kernel=1, tile_n=256, k_split=1, stream_k=0)),
     # small-M weight streaming: token tiles at N=24576, K=1536 (A box of the one row) ...
     ((0, 1, 1, 24576, 1536), dict(kernel=0, tile_n=192, token_box=1, grid=128)),
     ((0, 1, 33, 24576, 1536), dict(kernel=0, token_box=33)),
@@ -192,6 +196,8 @@ def test_describe_plan_follows_the_flags():
     assert _plan(0, 1, 4096, 4096, 4096, flags=fp8g.STAGES(3))["stages"] == 3
     assert _plan(0, 1, 128, 4096, 4096, flags=fp8g.SWAP_ON | fp8g.TOKEN_BOX(32))["token_box"] == 32
     assert _plan(0, 1, 64, 7168, 16384, flags=fp8g.WHOLE_TILES)["stream_k"] == 0
+    assert _plan(0, 1, 4096, 4096, 4096, flags=fp8g.WHOLE_TILES)["k_split"] == 1
+    assert _plan(0, 1, 4096, 4096, 4096, flags=fp8g.STREAM_K)["k_split"] == 0
 
 
 @pytest.mark.parametrize("args,code", [
