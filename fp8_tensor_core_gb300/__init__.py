@@ -24,6 +24,7 @@ DEBUG_ONE_STAGE = 0x10
 
 WHOLE_TILES = 0x100   # SwapAB kernel: whole tiles per CTA instead of stream-K ranges
 STREAM_K = 0x800      # SM-pair dense kernel: stream-K split of the last partial wave
+SPLIT_TAIL = 0x80     # SM-pair dense kernel: split the last wave's tiles along K whenever possible
 SINGLE_SM_TILES = 0x200   # dense non-swapped: one SM per 128-row tile instead of SM pairs
 NO_PDL = 0x400            # launch without programmatic dependent launch
 PAIR_TILES = 0x4000       # dense: always SM-pair tiles when M > 128

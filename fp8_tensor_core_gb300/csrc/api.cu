@@ -383,18 +383,22 @@ int pick_tile_n(int64_t m_tiles_total, int64_t N, int sms, int max_tn = 256)
 // one -- 4096^3 in four waves of either: 48.2 vs 47.8 us at 2.07 GHz, and
 // 50.2 vs 49.5 us under the sustained power cap).  Whole tiles pay for the
 // last partial wave of pairs.  When that wave holds at most half as many
-// tiles as there are pairs, each of its tiles can instead be split s ways
-// along K (s ranges of num_kb / s K blocks, at least kMinSplitKb each, on
-// s x tail pairs, run before the pairs' whole tiles); the last contributor
-// of a tile adds the others' FP32 partial tiles to its own while its MMA
-// issuer runs the next whole tile, which the model counts as
-// kSplitOverheadKb K blocks.  Stream-K over every pair (FP8G_STREAM_K)
-// spreads the wave over all pairs but leaves ~3 contributors a tile, whose
-// reduction took longer than the whole tile it overlaps (4096^3: 58.7 us
-// against 48.1), so it stays opt-in; FP8G_WHOLE_TILES keeps whole tiles.
+// tiles as there are pairs and every pair has a whole tile to run as well,
+// each of its tiles can instead be split s ways along K (s ranges of
+// num_kb / s K blocks, at least kMinSplitKb each, on s x tail pairs): a
+// pair runs the piece that starts a tile first, then a whole tile, then the
+// piece that finishes a tile, whose contributor sums the earlier partial
+// tiles (published long before) while its MMA issuer runs the next whole
+// tile.  The publishing and summing cost the busiest pair about
+// kSplitOverheadKb K blocks per extra contributor (fit on GB300 at 2.07 GHz,
+// same box, split vs whole: 4096^3 45.1 vs 47.4 us, 4096 x 4096 x 3072 36.0
+// vs 37.7 us, 6400 x 2560 x 2048 29.0 vs 28.2 us); with no whole tile to
+// overlap the sum is exposed (1024 x 1024 x 8192: 29.7 vs 23.9 us), so the
+// split needs a whole wave.  Stream-K over every pair (FP8G_STREAM_K) stays
+// opt-in; FP8G_WHOLE_TILES keeps whole tiles.
 constexpr int kMaxTailSplit = 4;
 constexpr int kMinSplitKb = 8;
-constexpr double kSplitOverheadKb = 2.0;
+constexpr double kSplitOverheadKb = 9.0;
 
 struct PairPlan {
     int tile_n;
@@ -408,6 +412,10 @@ PairPlan plan_pair(int64_t m_tiles2, int64_t N, int num_kb, int pairs, uint32_t 
     PairPlan best{max_tn, 1};
     double best_cost = 1e300;
     const int tn_override = static_cast<int>((flags >> 16) & 15u);
+    // FP8G_SPLIT_TAIL: only split plans compete (when some width allows one).
+    const bool force_split = (flags & FP8G_SPLIT_TAIL) && allow_split && !(flags & (FP8G_WHOLE_TILES | FP8G_STREAM_K));
+    PairPlan best_split{0, 1};
+    double best_split_cost = 1e300;
     for (int i = 0; i < 5; ++i) {
         const int tn = cands[i];
         if (tn > max_tn)
@@ -436,16 +444,22 @@ PairPlan plan_pair(int64_t m_tiles2, int64_t N, int num_kb, int pairs, uint32_t 
             continue;
         }
         const int s = static_cast<int>(std::min<int64_t>({kMaxTailSplit, pairs / tail, num_kb / kMinSplitKb}));
-        if (s >= 2) {
+        if (s >= 2 && (units >= pairs || force_split)) {
             const double split = (static_cast<double>(units / pairs) * num_kb + static_cast<double>(num_kb) / s +
-                                  kSplitOverheadKb) *
+                                  kSplitOverheadKb * (s - 1)) *
                                  cost_per_kb[i] * width;
             if (split < best_cost - 1e-9) {
                 best_cost = split;
                 best = {tn, s};
             }
+            if (split < best_split_cost - 1e-9) {
+                best_split_cost = split;
+                best_split = {tn, s};
+            }
         }
     }
+    if (force_split && best_split.tile_n)
+        best = best_split;
     if (tn_override >= 1 && tn_override <= 8 && best.tile_n != std::min(32 * tn_override, max_tn))
         best = {std::min(32 * tn_override, max_tn), 1};
     return best;

@@ -74,6 +74,8 @@ struct alignas(16) SmemCtl {
     uint64_t sffree[kMaxSfSets];    // TMEM scale set no longer read by any MMA
     uint64_t sfset_ready[kMaxSfSets];   // SwapAB: scale set written into TMEM by the staging warps
     uint64_t drain2;                // SwapAB: completion of the second issuer's tensor-core work
+    uint64_t peer_done;             // CTA-pair kernel (even CTA): the odd CTA's loader has stopped
+    volatile int32_t peer_issued;   // ... after issuing this many stage fills
     uint32_t tmem_base;
     volatile int32_t abort;
     int32_t units_total;
@@ -131,11 +133,13 @@ __device__ __forceinline__ bool wait_count_at_least(const int32_t *p, int target
 }
 
 // Bounded wait that ignores the abort flag (used while draining).
+// kCluster: acquire at cluster scope (the phase is completed by the peer CTA).
+template <bool kCluster = false>
 __device__ __forceinline__ bool warp_wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns)
 {
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
-        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity)))
+        if (__all_sync(0xffffffffu, kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)))
             return true;
         int late = 0;
         if ((threadIdx.x & 31) == 0)
@@ -1159,6 +1163,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
         mbar_init(smem_addr(&ctl.drain), 1);
         mbar_init(smem_addr(&ctl.drain2), 1);
         mbar_init(smem_addr(&ctl.pair_exit), 1);
+        mbar_init(smem_addr(&ctl.peer_done), 1);
+        ctl.peer_issued = 0;
         if constexpr (kBS) {
             for (int s = 0; s < a.stages; ++s)
                 mbar_init(smem_addr(&ctl.sffull[s]), 1);
@@ -1206,49 +1212,85 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
     // Only called when T > 0 (a stream-K segment exists).
     auto range_begin = [&](long long c) { return sk0 + c * T / P; };
     auto pair_of = [&](long long x) { return static_cast<int>(((x - sk0 + 1) * P - 1) / T); };
+    // A pair's work: its range [pos0, end) of the split K blocks (empty if
+    // none; at most two pieces, as a range never exceeds a tile's K blocks)
+    // and whole tiles cid, cid + ncl, ... below dp_tiles.  Order: first the
+    // range's piece that ends inside a tile (a tile's K-earlier part: a later
+    // contributor will add it), then one whole tile, then the range's piece
+    // that finishes a tile (its contributor then finds the earlier parts
+    // published long ago and sums them while its MMA issuer runs the next
+    // whole tile), then the remaining whole tiles.  A piece's partial slot
+    // is kind 0 if it starts the range, else kind 1.
     struct Walker {
-        long long pos, end;
-        int u;
-        bool first;
+        long long pos0;          // range start
+        long long pos, lim;      // later pieces of the range, [pos, lim)
+        long long e_lo, e_hi;    // the piece run first, [e_lo, e_hi) (empty if none)
+        int u;                   // next whole tile
+        int state;
     };
     auto make_walker = [&]() {
         Walker w;
         w.u = cid;
-        w.first = true;
+        w.state = 0;
+        w.pos0 = w.pos = w.lim = w.e_lo = w.e_hi = 0;
         if (T > 0 && cid < P) {
-            w.pos = range_begin(cid);
-            w.end = range_begin(static_cast<long long>(cid) + 1);
-        } else {
-            w.pos = w.end = 0;
+            const long long b = range_begin(cid), e = range_begin(static_cast<long long>(cid) + 1);
+            w.pos0 = w.pos = b;
+            w.lim = e;
+            if (e % num_kb != 0) {   // the range ends inside a tile: run that piece first
+                const long long ts = (e - 1) / num_kb * num_kb;
+                w.e_lo = ts > b ? ts : b;
+                w.e_hi = e;
+                w.lim = w.e_lo;
+            }
         }
         return w;
     };
     // Next segment: tile (rasterised in bands of raster_band 256-row tiles,
-    // M fastest), this CTA's first row and the tile's first column.  The
-    // pair's stream-K range comes first, then its whole tiles: the partial
-    // tiles are then published early, and the contributor that completes a
-    // tile sums them in its epilogue while its MMA issuer already runs the
-    // next whole tile (with the range last, every reduction would wait for
-    // the end of the kernel and add its latency there).
+    // M fastest), this CTA's first row and the tile's first column.
     auto next_seg = [&](Walker &w, PairSeg &x) {
-        int u;
-        if (w.pos < w.end) {
-            u = static_cast<int>(w.pos / num_kb);
-            x.kb0 = static_cast<int>(w.pos - static_cast<long long>(u) * num_kb);
-            const long long left = w.end - w.pos;
-            x.kb1 = left < num_kb - x.kb0 ? x.kb0 + static_cast<int>(left) : num_kb;
-            w.pos += x.kb1 - x.kb0;
-            x.kind = w.first ? 0 : 1;
-            w.first = false;
-        } else {
+        int u = 0;
+        bool found = false;
+        auto piece = [&](long long lo, long long hi) {
+            u = static_cast<int>(lo / num_kb);
+            x.kb0 = static_cast<int>(lo - static_cast<long long>(u) * num_kb);
+            x.kb1 = x.kb0 + static_cast<int>(hi - lo);
+            x.kind = lo == w.pos0 ? 0 : 1;
+            found = true;
+        };
+        auto whole = [&]() {
             if (w.u >= dp_tiles)
-                return false;
+                return;
             u = w.u;
             x.kb0 = 0;
             x.kb1 = num_kb;
             x.kind = 0;
             w.u += ncl;
+            found = true;
+        };
+        if (w.state == 0) {
+            w.state = 1;
+            if (w.e_hi > w.e_lo)
+                piece(w.e_lo, w.e_hi);
         }
+        if (!found && w.state == 1) {
+            w.state = 2;
+            whole();
+        }
+        if (!found && w.state == 2) {
+            if (w.pos < w.lim) {
+                const long long tile_end = (w.pos / num_kb + 1) * num_kb;
+                const long long hi = w.lim < tile_end ? w.lim : tile_end;
+                piece(w.pos, hi);
+                w.pos = hi;
+            } else {
+                w.state = 3;
+            }
+        }
+        if (!found && w.state == 3)
+            whole();
+        if (!found)
+            return false;
         x.tile = u;
         int local = u, mt = m_tiles;
         x.g = 0;
@@ -1276,6 +1318,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
         int stage = 0;
         uint32_t phase = 0;
         long long issued = 0;
+        uint32_t sf_par = 0, sf_used = 0;   // per stage: parity of scale fills posted, any posted
         const bool drop = (a.flags & FP8G_DEBUG_DROP_FIRST_LOAD) && blockIdx.x == 0;
         Walker wk = make_walker();
         PairSeg x;
@@ -1285,6 +1328,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
                                kRoleLoader, stage)) {
                     aborted = true;
                     break;
+                }
+                if constexpr (kBS) {
+                    if (sf_load_at(kb, x.kb0, a.sf_k) && !(drop && issued == 0)) {
+                        sf_par ^= 1u << stage;
+                        sf_used |= 1u << stage;
+                    }
                 }
                 if (lane == 0 && !(drop && issued == 0)) {
                     uint8_t *sa = sm.stages + static_cast<size_t>(stage) * a.stage_bytes;
@@ -1327,18 +1376,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
                 }
             }
         }
+        // The odd CTA's copies complete on the even CTA's full barriers, so
+        // only the even CTA can observe them: the odd CTA reports how many
+        // stage fills it issued (it issues none after this).
+        if (!leader) {
+            if (lane == 0) {
+                st_shared_cluster_u32(mapa_shared(smem_addr(const_cast<int32_t *>(&ctl.peer_issued)), 0),
+                                      static_cast<uint32_t>(issued));
+                mbar_arrive_cluster(mapa_shared(smem_addr(&ctl.peer_done), 0));
+            }
+            __syncwarp();
+        }
         if (aborted && leader) {
-            // The even CTA's full barriers count both CTAs' copies: wait for
-            // the fills it posted.
+            // Stage s's barrier is armed by this CTA (one arrival expecting
+            // both CTAs' bytes, its own half copied with it) and filled by the
+            // odd CTA's half.  Either side issues round r + 1 only after the
+            // MMA consumed round r, so the rounds armed and filled differ by at
+            // most one: the pending phase lacks either the odd half (complete
+            // it here) or the arrival (post it, expecting only the odd half).
+            // Waiting (bounded) for that phase then observes every copy of
+            // both CTAs landed.
+            long long peer = issued;
+            if (warp_wait_drain<true>(smem_addr(&ctl.peer_done), 0, 4 * a.timeout_ns))
+                peer = static_cast<long long>(static_cast<uint32_t>(ctl.peer_issued));
+            const uint32_t odd_bytes = tx_pair / 2;
+            auto rounds = [&](long long n, int s) {
+                return n / a.stages + (static_cast<long long>(s) < n % a.stages ? 1 : 0);
+            };
             for (int s = 0; s < a.stages; ++s) {
-                if (issued < a.stages && s >= issued)
+                const long long armed = rounds(issued, s) - ((drop && s == 0 && issued > 0) ? 1 : 0);
+                const long long filled = rounds(peer, s);
+                const long long last = armed > filled ? armed : filled;
+                if (last <= 0)
                     continue;
-                if (drop && issued <= a.stages && s == 0)
-                    continue;
-                const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
-                warp_wait_drain(smem_addr(&ctl.full[s]), par, a.timeout_ns);
+                const uint32_t fb = smem_addr(&ctl.full[s]);
+                if (lane == 0) {
+                    if (armed == filled + 1)
+                        mbar_complete_tx(fb, odd_bytes);
+                    else if (filled == armed + 1)
+                        mbar_arrive_expect_tx(fb, odd_bytes);
+                }
+                __syncwarp();
+                warp_wait_drain(fb, static_cast<uint32_t>((last - 1) & 1), a.timeout_ns);
             }
         }
+        // Scale bytes complete on each CTA's own barriers.
+        if constexpr (kBS)
+            sf_loader_drain(ctl, a, sf_par, sf_used);
     } else if (warp == 1 && !kBS) {
         // ----------------------------- MMA issuer -----------------------------
         if (leader) {
@@ -1640,7 +1724,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     __threadfence();
                     const int me = cid - first;   // this pair's place in K order
-                    for (int c = 0; c < a.tile_n && ok; c += 32) {
+                    // (plain instantiations only: the block-scaled ones, with
+                    // 352 threads, have no registers to spare for it)
+                    const bool two = !kBS && n_contrib == 2;
+                    if (two && ok) {
+                        // One other contributor: its next 32 columns are loaded
+                        // while this 32 are summed (two chunks of loads in flight).
+                        const int other = 1 - me;
+                        const int kind = other == 0 ? kind_first : 0;
+                        const float4 *src = slots + ((static_cast<int64_t>(2 * (first + other)) + rank) * 2 + kind) *
+                                                        part4 + row;
+                        float4 nxt[8];
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            nxt[v] = __ldcg(src + v * kTileM);
+                        for (int c = 0; c < a.tile_n; c += 32) {
+                            float4 cur[8];
+#pragma unroll
+                            for (int v = 0; v < 8; ++v)
+                                cur[v] = nxt[v];
+                            if (c + 32 < a.tile_n) {
+#pragma unroll
+                                for (int v = 0; v < 8; ++v)
+                                    nxt[v] = __ldcg(src + ((c + 32) / 4 + v) * kTileM);
+                            }
+                            uint32_t own[32];
+                            ld32(c, own);
+                            uint32_t bits_v[32];
+#pragma unroll
+                            for (int v = 0; v < 8; ++v) {
+                                const float o[4] = {cur[v].x, cur[v].y, cur[v].z, cur[v].w};
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    const float mine_f = __uint_as_float(own[4 * v + j]);
+                                    bits_v[4 * v + j] = __float_as_uint(me == 0 ? mine_f + o[j] : o[j] + mine_f);
+                                }
+                            }
+                            store_rows32<kEpi>(a, dout, bits_v, rf, x.g, grow, row_ok, x.n0 + c, tg);
+                        }
+                    }
+                    for (int c = 0; c < a.tile_n && ok && !two; c += 32) {
                         uint32_t own[32];
                         ld32(c, own);
                         float acc_v[32];
@@ -1689,20 +1812,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
     }
 
     // Pair exit: neither CTA leaves while the other may still touch its
-    // shared memory or barriers.  On an abort, also give copies still in
-    // flight time to land.
+    // shared memory or barriers.  Every copy into either CTA has been seen
+    // to land by then (the loaders' drains above), and the even CTA's MMA
+    // issuer has waited for its tensor-core work.
     tc_fence_before();
     __syncthreads();
     if (threadIdx.x == 0)
         mbar_arrive_cluster(mapa_shared(smem_addr(&ctl.pair_exit), rank ^ 1u));
-    if (warp == 0) {
-        warp_wait_drain(smem_addr(&ctl.pair_exit), 0, 4 * a.timeout_ns);
-        if (ctl.abort) {
-            const uint64_t t0 = globaltimer_ns();
-            while (globaltimer_ns() - t0 < 50000ull) {
-            }
-        }
-    }
+    if (warp == 0)
+        warp_wait_drain<true>(smem_addr(&ctl.pair_exit), 0, 4 * a.timeout_ns);
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();

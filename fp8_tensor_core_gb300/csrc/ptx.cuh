@@ -287,6 +287,19 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
                  : "memory");
 }
 
+// Count `bytes` of the current phase's expected transactions as done, as a
+// copy of that size completing on the barrier would.
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// 32-bit store to shared memory anywhere in the cluster.
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
 // Whole-cluster execution barrier (all threads of every CTA).
 __device__ __forceinline__ void cluster_sync_all()
 {

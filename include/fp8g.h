@@ -101,13 +101,20 @@ typedef enum {
 /* Tuning overrides (0 = the library's choice).  Results stay correct for
  * every value; only speed (and the last bits of rounding) change.
  *   FP8G_WHOLE_TILES  SwapAB kernel: each CTA takes whole output tiles in
- *                     turn instead of an equal stream-K range of K blocks
+ *                     turn instead of an equal stream-K range of K blocks;
+ *                     SM-pair kernel: never split the last wave's tiles
  *   FP8G_STREAM_K     SM-pair dense kernel: split the tiles of the last,
  *                     partial wave stream-K over all pairs (default: whole
  *                     tiles round-robin)
  *   FP8G_TILE_N(n)    non-swapped kernel: N tile of n (32..256, multiple of 32) */
 #define FP8G_WHOLE_TILES 0x100u
 #define FP8G_STREAM_K 0x800u
+/*   FP8G_SPLIT_TAIL   SM-pair dense kernel: split each tile of the last partial
+ *                     wave 2 to 4 ways along K whenever that is possible (by
+ *                     default the split competes with whole tiles in a cost
+ *                     model and needs a whole wave to overlap its sums).
+ *                     FP8G_WHOLE_TILES also turns the default split off.    */
+#define FP8G_SPLIT_TAIL 0x80u
 /*   FP8G_SINGLE_SM_TILES  non-swapped dense kernel: 128-row tiles on one SM
  *                     each instead of 256-row tiles on a pair of SMs         */
 #define FP8G_SINGLE_SM_TILES 0x200u

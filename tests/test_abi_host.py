@@ -117,11 +117,11 @@ def test_python_flag_constants_match_the_header():
         defs = dict(re.findall(r"#define FP8G_([A-Z0-9_]+) (0x[0-9a-fA-F]+|[0-9]+)u?\b", f.read()))
     checked = 0
     for name in ("SWAP_AUTO", "SWAP_ON", "SWAP_OFF", "DEBUG_ONE_STAGE", "WHOLE_TILES", "STREAM_K", "SINGLE_SM_TILES",
-                 "NO_PDL", "PAIR_TILES", "ONE_MMA_ISSUER", "TWO_MMA_ISSUERS", "SHARE_SM", "NO_SHARE_SM"):
+                 "NO_PDL", "PAIR_TILES", "ONE_MMA_ISSUER", "TWO_MMA_ISSUERS", "SHARE_SM", "NO_SHARE_SM", "SPLIT_TAIL"):
         assert name in defs, name
         assert getattr(fp8g, name) == int(defs[name], 0), name
         checked += 1
-    assert checked == 13
+    assert checked == 14
 
 
 def test_field_flags_do_not_overlap_the_single_bit_flags():
@@ -130,7 +130,8 @@ def test_field_flags_do_not_overlap_the_single_bit_flags():
     import fp8_tensor_core_gb300 as fp8g
     singles = 0
     for name in ("SWAP_ON", "SWAP_OFF", "DEBUG_ONE_STAGE", "WHOLE_TILES", "STREAM_K", "SINGLE_SM_TILES", "NO_PDL",
-                 "PAIR_TILES", "ONE_MMA_ISSUER", "TWO_MMA_ISSUERS", "SHARE_SM", "NO_SHARE_SM"):
+                 "PAIR_TILES", "ONE_MMA_ISSUER", "TWO_MMA_ISSUERS", "SHARE_SM", "NO_SHARE_SM", "SPLIT_TAIL"):
+        assert singles & getattr(fp8g, name) == 0, name
         singles |= getattr(fp8g, name)
     fields = [fp8g.STAGES(15), fp8g.TILE_N(15 * 32), fp8g.TOKEN_BOX(15 * 16)]
     for i, f in enumerate(fields):

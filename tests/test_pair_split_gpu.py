@@ -1,7 +1,7 @@
 """SM-pair tiles with the last partial wave split along K.
 
 When the tiles left after the whole waves of 256-row SM-pair tiles number at
-most half the pairs, each of them is split s ways along K ("DeepGEMM：基于
+most half the pairs, each of them can be split s ways along K ("DeepGEMM：基于
 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践" §1.3: every SM busy on large
 shapes), run before the pairs' whole tiles; the last contributor of a tile
 sums the others' FP32 partial tiles with its own in K order (§6.4: a fixed
@@ -49,17 +49,20 @@ def plan_of(M, N, K, sf=0, flags=0):
     return fp8g.fp8g_describe_plan(fp8g.LAYOUT_DENSE, 1, M, N, K, 0, sf, flags)
 
 
-# (M, N, K, B format, expected split): no whole wave (s = 4, 3, 2), ranges
-# straddling tiles (s = 3 over 32 or 64 K blocks), ragged M/N/K, whole waves
-# plus a split tail (s = 2), 128-wide tiles (s = 4).
-CASES = [(1024, 1024, 4096, E4, 4), (1000, 1016, 4000, E4, 4), (1280, 1024, 4096, E4, 3),
-         (1200, 1000, 8192, E5, 3), (1280, 1024, 2048, E4, 2), (6400, 2560, 2048, E4, 2),
-         (4000, 4088, 4096, E4, 2), (768, 768, 8192, E5, 4)]
+# (M, N, K, B format, flags, expected split).  By default the split needs a
+# whole wave of tiles besides (4096 x 4096 x 3072, 4000 x 4088 x 4096);
+# FP8G_SPLIT_TAIL forces it: without whole waves (s = 2, 3, 4; 128- and
+# 160-wide tiles), ranges that straddle tiles (s = 3 over 64 and 32 K blocks),
+# ragged M, N and K, and whole waves plus a split tail at short K.
+SPLIT = fp8g.SPLIT_TAIL
+CASES = [(4096, 4096, 3072, E4, 0, 2), (4000, 4088, 4096, E4, 0, 2), (1000, 1016, 4000, E4, SPLIT, 2),
+         (1280, 1024, 4096, E4, SPLIT, 2), (512, 1536, 8192, E5, SPLIT, 3), (1024, 4608, 4096, E4, SPLIT, 3),
+         (768, 768, 8192, E5, SPLIT, 4), (6400, 2560, 2048, E4, SPLIT, 2)]
 
 
-@pytest.mark.parametrize("M,N,K,fb,split", CASES)
-def test_split_tail_every_element_twice(M, N, K, fb, split):
-    plan = plan_of(M, N, K)
+@pytest.mark.parametrize("M,N,K,fb,flags,split", CASES)
+def test_split_tail_every_element_twice(M, N, K, fb, flags, split):
+    plan = plan_of(M, N, K, flags=flags)
     assert plan["kernel"] == fp8g.KERNEL_SM_PAIRS and plan["k_split"] == split, plan
     A = synth.normal_fp8((M, K), 901 + M, 0.0, 1.0, E4)
     B = synth.normal_fp8((N, K), 902 + N, 0.0, 1.0, fb)
@@ -67,7 +70,7 @@ def test_split_tail_every_element_twice(M, N, K, fb, split):
     ref, absdot = oracle.gemm_nt(A, B, E4, fb)
     first = None
     for call in range(2):
-        D = fp8g.fp8_gemm_nt(Ad, Bd, a_dtype=E4, b_dtype=fb)
+        D = fp8g.fp8_gemm_nt(Ad, Bd, a_dtype=E4, b_dtype=fb, flags=flags)
         torch.cuda.synchronize()
         st = fp8g.fp8g_get_device_status()
         assert st[0] == fp8g.OK, st
@@ -85,7 +88,8 @@ def test_split_tail_whole_tiles_flag_and_fused_epilogue():
     scales, alpha, beta*C, bias, ReLU, directed rounding) runs on split
     tiles too."""
     M, N, K = 1280, 1024, 4096
-    assert plan_of(M, N, K, flags=fp8g.WHOLE_TILES)["k_split"] == 1
+    assert plan_of(M, N, K, flags=fp8g.SPLIT_TAIL | fp8g.WHOLE_TILES)["k_split"] == 1
+    assert plan_of(M, N, K, flags=fp8g.SPLIT_TAIL)["k_split"] == 2
     rng = np.random.default_rng(911)
     A = synth.normal_fp8((M, K), 912, 0.0, 1.0, E4)
     B = synth.normal_fp8((N, K), 913, 0.0, 1.0, E4)
@@ -98,7 +102,7 @@ def test_split_tail_whole_tiles_flag_and_fused_epilogue():
     _, absS, S = oracle.gemm_nt(A, B, want_exact=True)
     f = sa.astype(np.float64)[:, None] * sb.astype(np.float64)[None, :]
     ref, absdot = oracle.epilogue(S * f, absS * np.abs(f), 0.5, 2.0, Cb, bias, True, 2)
-    for flags in (0, fp8g.WHOLE_TILES):
+    for flags in (fp8g.SPLIT_TAIL, fp8g.WHOLE_TILES):
         out = fp8g.fp8_gemm_nt_ex(dev(A), dev(B), scale_a=dev(sa), scale_b=dev(sb),
                                   epilogue={"alpha": 0.5, "beta": 2.0, "C": Ct, "bias": dev(bias), "relu": True,
                                             "round_mode": 2}, a_dtype=E4, b_dtype=E4, flags=flags)
@@ -112,7 +116,8 @@ def test_split_tail_block_scaled_pair_tiles():
     """Block-scaled SM-pair tiles (FP8G_PAIR_TILES) with a split tail: the
     scale-staging warps follow the same segment order."""
     M, N, K = 1280, 1024, 4096
-    plan = plan_of(M, N, K, sf=128, flags=fp8g.PAIR_TILES)
+    flags = fp8g.PAIR_TILES | fp8g.SPLIT_TAIL
+    plan = plan_of(M, N, K, sf=128, flags=flags)
     assert plan["kernel"] == fp8g.KERNEL_SM_PAIRS and plan["k_split"] >= 2, plan
     rng = np.random.default_rng(921)
     A = synth.normal_fp8((M, K), 922, 0.0, 1.0, E4)
@@ -121,7 +126,7 @@ def test_split_tail_block_scaled_pair_tiles():
     sfa = rng.integers(120, 135, (ks, M)).astype(np.uint8)
     sfb = rng.integers(120, 135, (ks, N)).astype(np.uint8)
     D = fp8g.fp8_gemm_nt_blockscaled(dev(A), dev(B), dev(sfa), dev(sfb), sf_group_k=128, a_dtype=E4, b_dtype=E4,
-                                     flags=fp8g.PAIR_TILES)
+                                     flags=flags)
     torch.cuda.synchronize()
     assert fp8g.fp8g_get_device_status()[0] == fp8g.OK
     ref, absdot, accb = oracle.gemm_blockscaled(A, B, sfa, sfb, 128, want_accbound=True)
