@@ -636,9 +636,13 @@ def roofline_of(w: Workload, flops: float, algo_bytes: float, kernel_ms: float, 
 
 
 def host_us_per_call(w: Workload, s, stream, calls: int = 300) -> dict:
-    """Host time of one enqueue through the C ABI (pointers and sizes already
-    marshalled; every call after the first finds its tensor maps in the
-    library's cache), and the floor of a ctypes call into the library."""
+    """Host time of one enqueue through the C ABI from Python (pointers and
+    sizes already marshalled; every call after the first finds its tensor
+    maps in the library's cache), in a batch short of the launch queue's
+    depth, and the floor of a ctypes call with as many arguments:
+    fp8g_describe_plan (11 arguments, ~0.1 us of planning in C).  Their
+    difference estimates the library's own cost per call, the CUDA launch
+    included."""
     import ctypes
     import fp8_tensor_core_gb300 as fp8g
     lib = fp8g._lib.load()
@@ -662,11 +666,14 @@ def host_us_per_call(w: Workload, s, stream, calls: int = 300) -> dict:
     t1 = time.perf_counter()
     torch.cuda.synchronize()
     check_status("after the host-cost calls", stream)
+    plan = fp8g._lib.Plan()
+    pargs = (0, 1, 1, 256, 256, 0, 0, 0, 152, 232448, ctypes.byref(plan))
     t2 = time.perf_counter()
     for _ in range(calls):
-        lib.fp8g_version()
+        lib.fp8g_describe_plan(*pargs)
     t3 = time.perf_counter()
-    return {"host_us_per_call": 1e6 * (t1 - t0) / calls, "ctypes_floor_us": 1e6 * (t3 - t2) / calls}
+    host, floor = 1e6 * (t1 - t0) / calls, 1e6 * (t3 - t2) / calls
+    return {"host_us_per_call": host, "ctypes_floor_us": floor, "c_abi_us_est": host - floor}
 
 
 def run_per_config(device, stream, l2, peaks, peak_src, sampler, steps_tensor: int, steps_hbm: int,
