@@ -36,6 +36,7 @@ constexpr int kMaxDevices = 64;
 constexpr int64_t kSwapAutoMaxTokens = 128;        // dense and block-scaled problems
 constexpr int64_t kSwapAutoMaxGroupTokens = 255;   // plain grouped problems
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+constexpr int64_t kSpareFetchMaxBytes = int64_t(64) << 20;   // weights fetched by early CTAs: <= half of L2
 
 std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
 
@@ -928,6 +929,14 @@ int launch(const Problem &p, cudaStream_t stream, const DeviceInfo *forced = nul
     args.a_box_rows = dense && p.rows_a < kTileM ? static_cast<int32_t>(p.rows_a) : 0;
     const int grid = static_cast<int>(std::min<int64_t>(units_upper, info.sms));
     args.prefetch_kb = dense ? early_prefetch_kb(static_cast<int>(tile_n) * kBlockK, false) : 0;
+    // Dense launches that leave SMs idle: the CTAs that start there fetch
+    // the whole launch's weights into L2 while the previous launch runs.
+    // Measured on GB300 (same box, graph replay): N=24576, K=1536 token tiles
+    // (128 CTAs) 9.35 -> 8.75 us at M=1, 10.03 -> 8.82 us at M=64; with
+    // weights of 117 MB (N=7168, K=16384) it lost (39.9 -> 46.3 us), so only
+    // weights up to half of L2 are fetched this way.
+    if (dense && grid < info.sms && p.N * p.K <= kSpareFetchMaxBytes)
+        args.spare_ctas = info.sms - grid;
     if (describe) {
         describe_as(describe, FP8G_KERNEL_TOKEN_TILES, tile_n, args, false, false,
                     args.a_box_rows ? args.a_box_rows : kTileM, grid);

@@ -807,7 +807,21 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
 
     // Dense problems: fetch the first prefetch_kb K blocks of this CTA's
     // weight tiles into L2 while the previous launch may still run.
-    if (a.prefetch_kb > 0 && warp == 2 && lane == 0) {
+    if (a.prefetch_kb > 0 && warp == 2 && lane == 0 && static_cast<int>(blockIdx.x) < a.spare_ctas) {
+        // A CTA that may start on an SM this launch leaves idle, while the
+        // previous launch still streams: fetch all K blocks of the weight
+        // tiles of CTAs blockIdx.x, + spare_ctas, ... into L2, so that the
+        // CTAs starting later find their weights there.  (L2 is the point of
+        // coherence: the loads after griddepcontrol.wait still see whatever
+        // the previous launch wrote.)
+        for (int b = blockIdx.x; b < static_cast<int>(gridDim.x); b += a.spare_ctas)
+            for (int u = b; u < total; u += gridDim.x) {
+                int g, m0, n0, mv;
+                decode(u, g, m0, n0, mv);
+                for (int kb = 0; kb < a.num_kb; ++kb)
+                    tma_prefetch_l2_3d(&tm_b, kb * kBlockK, n0, g);
+            }
+    } else if (a.prefetch_kb > 0 && warp == 2 && lane == 0) {
         int left = a.prefetch_kb;
         for (int u = blockIdx.x; u < total && left > 0; u += gridDim.x) {
             int g, m0, n0, mv;

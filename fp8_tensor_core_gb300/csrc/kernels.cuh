@@ -97,6 +97,12 @@ struct GemmArgs {
                                // so that they stream while the previous launch drains; 0: none
     int32_t a_box_rows;        // token-tile kernel: A rows per TMA box (the host encodes the A map with
                                // it); 0: 128.  Fewer only for dense problems of fewer rows
+    int32_t spare_ctas;        // token-tile kernel, dense problems whose weights fit in half of L2:
+                               // the SMs this launch leaves idle.  CTAs 0 .. spare_ctas-1 are the
+                               // ones that start early, on those SMs, while the previous launch
+                               // still runs: before griddepcontrol.wait they fetch the weight
+                               // tiles of every CTA congruent to them modulo spare_ctas into L2
+                               // (0: each CTA fetches its first prefetch_kb K blocks only)
     int32_t acc_bufs;          // block-scaled tile kernels: accumulator buffers per issuer (0 or 2:
                                // two; 1: one, when two issuers' four or a 256-wide tile's two
                                // accumulators and the scale sets do not fit in TMEM)

@@ -123,7 +123,9 @@ typedef enum {
  *                     previous launch in the stream finishes; it waits for
  *                     that launch before any load or store of its operands.
  *                     A dense launch may issue L2 prefetches of its first B
- *                     tiles before that wait: L2 is coherent, so the loads
+ *                     tiles before that wait -- of all of them from the CTAs
+ *                     that start on SMs the launch leaves idle, when the
+ *                     weights fit in half of L2: L2 is coherent, so the loads
  *                     after the wait still see what the previous launch
  *                     wrote)                                                */
 #define FP8G_NO_PDL 0x400u
