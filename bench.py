@@ -282,7 +282,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", gpu_id, "--query-gpu=" + ",".join(self.FIELDS),
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -302,7 +302,11 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self, t0: float, t1: float):
+    def summary(self, t0: float, t1: float, t_warm: float = None):
+        """Clocks in the timed region [t0, t1]; when that holds fewer than two
+        samples (a short region), in [t_warm, t1] -- the warm-up launches of
+        the same kernel and the timed region -- and without t_warm in
+        everything sampled up to t1."""
         def parse(rows):
             sm = [float(r[0]) for _, r in rows if r and r[0].replace(".", "", 1).isdigit()]
             mx = [float(r[1]) for _, r in rows if len(r) > 1 and r[1].replace(".", "", 1).isdigit()]
@@ -313,10 +317,11 @@ class ClockSampler:
                     if len(r) > 4 + i and r[4 + i].lower().startswith("active"):
                         reasons.add(n)
             return sm, mx, sorted(reasons)
-        inside = [s for s in self.samples if t0 <= s[0] <= t1 + 0.15]
+        inside = [s for s in self.samples if t0 <= s[0] <= t1 + 0.05]
         window = "timed"
         if len(inside) < 2:
-            inside = [s for s in self.samples if s[0] <= t1 + 0.15]
+            lo = t_warm if t_warm is not None else 0.0
+            inside = [s for s in self.samples if lo <= s[0] <= t1 + 0.05]
             window = "warmup+timed"
         sm, mx, reasons = parse(inside)
         return {"sm_mhz": statistics.median(sm) if sm else None,
@@ -565,8 +570,10 @@ def timed_launches(call, sets, steps: int, warmup: int, device, stream, use_grap
     with CUDA events on the launching stream: by default captured into one
     CUDA graph whose replay is timed (host launch gaps do not count), else
     direct launches with events around each.  Returns (total_ms, per-launch
-    ms, wall-clock start, end)."""
+    ms, wall-clock start and end of the timed region, wall-clock start of the
+    warm-up)."""
     import torch
+    t_warm = time.time()
     for i in range(warmup):
         call(sets[i % len(sets)], stream)
     torch.cuda.synchronize(device)
@@ -608,7 +615,7 @@ def timed_launches(call, sets, steps: int, warmup: int, device, stream, use_grap
     total_ms = ev[0][0].elapsed_time(ev[-1][1])
     kernel_ms = total_ms / steps if use_graph else sum(a.elapsed_time(b) for a, b in ev) / steps
     check_status("after the timed launches", stream)
-    return total_ms, kernel_ms, t_wall0, t_wall1
+    return total_ms, kernel_ms, t_wall0, t_wall1, t_warm
 
 
 def roofline_of(w: Workload, flops: float, algo_bytes: float, kernel_ms: float, region_ms: float, peaks, peak_src):
@@ -700,7 +707,7 @@ def run_per_config(device, stream, l2, peaks, peak_src, sampler, steps_tensor: i
         sets, _ = device_sets(w, inp, device, l2)
         call = make_call(w)
         steps = steps_tensor if w.bound == "tensor" else steps_hbm
-        total_ms, kernel_ms, t0, t1 = timed_launches(call, sets, steps, 3, device, stream, use_graph)
+        total_ms, kernel_ms, t0, t1, tw = timed_launches(call, sets, steps, 3, device, stream, use_graph)
         mm = inp.get("masked_m")
         roof = roofline_of(w, w.flops(mm), w.bytes(mm), kernel_ms, total_ms, peaks, peak_src)
         plan = planned_launch(w)
@@ -719,7 +726,7 @@ def run_per_config(device, stream, l2, peaks, peak_src, sampler, steps_tensor: i
             auto = planned_launch(make_workload(base))
             e["auto_picks"] = KERNEL_NAMES[auto["kernel"]]
         if sampler:
-            c = sampler.summary(t0, t1)
+            c = sampler.summary(t0, t1, tw)
             if c["samples"]:
                 e["sm_mhz"] = c["sm_mhz"]
         out.append(e)
@@ -746,22 +753,23 @@ def run_ours(args, w: Workload):
     l2 = int(getattr(props, "L2_cache_size", 0) or 129 * 2**20)
     peaks, peak_src = load_peaks()
 
+    # clock samples start now, so the sampler is running by the warm-up
+    sampler = ClockSampler("GPU-" + str(props.uuid)) if rank == 0 else None
     inp = host_inputs(w)
     stream = torch.cuda.current_stream(device)
     sets, host = device_sets(w, inp, device, l2)
     n_sets = len(sets)
     torch.cuda.synchronize(device)
     call = make_call(w)
-    sampler = ClockSampler("GPU-" + str(props.uuid)) if rank == 0 else None
 
     # ---- timed region: exactly K steps --------------------------------------
     use_graph = args.graph != "off"
-    total_ms, kernel_ms, t_wall0, t_wall1 = timed_launches(
+    total_ms, kernel_ms, t_wall0, t_wall1, t_warm = timed_launches(
         call, sets, args.steps, args.warmup, device, stream, use_graph,
         sync_world=lambda: barrier(world, device))
     total_ms_max = max_over_ranks(total_ms, world, device)
     kernel_ms_max = max_over_ranks(kernel_ms, world, device)
-    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+    clocks = sampler.summary(t_wall0, t_wall1, t_warm) if sampler else None
 
     mm = inp.get("masked_m")
     flops = w.flops(mm)
