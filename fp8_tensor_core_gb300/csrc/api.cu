@@ -840,7 +840,11 @@ int launch(const Problem &p, cudaStream_t stream, const DeviceInfo *forced = nul
                 args.stages &= ~1;
             }
         }
-        const int64_t band = (48ll << 20) / (2 * kTileM * p.K);
+        // Bands of 256-row tiles whose token rows total ~32 MB stay in L2 while
+        // the weight tiles stream past them (8192 x 18432 x 7168: DRAM reads
+        // 641 MB with 48 MB bands, 400 MB with 32 MB, 489 MB with 24 MB;
+        // 600 -> 589 us).
+        const int64_t band = (32ll << 20) / (2 * kTileM * p.K);
         args.raster_band = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(band, m_tiles2)));
         // Pairs with work: every pair for stream-K (or whole tiles beyond one
         // wave); with a tail split, the pairs of the whole waves or the split
