@@ -289,6 +289,9 @@ class ClockSampler:
             return
         self.t = threading.Thread(target=self._read, daemon=True)
         self.t.start()
+        t_end = time.time() + 5.0          # nvidia-smi's first sample can take a second
+        while not self.samples and time.time() < t_end and self.proc.poll() is None:
+            time.sleep(0.02)
 
     def _read(self):
         for line in self.proc.stdout:
