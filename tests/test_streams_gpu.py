@@ -90,3 +90,44 @@ def test_stream_k_calls_on_unordered_streams(small):
         check_masked(bits(Dm[r]), D0, ref_m, abs_m, mm, "masked call %d" % r)
     for i, D in enumerate(Ds):
         check_dense(bits(D), ref_s, abs_s, "small-M call %d" % i)
+
+
+def test_split_pair_tiles_and_swap_on_unordered_streams():
+    """The 4096^3 dense GEMM, whose last partial wave is split along K (its
+    contributors publish FP32 partial tiles through the stream's scratch),
+    on one stream and 16-token SwapAB stream-K calls on another, with no
+    ordering between them: every element of every call against the oracle."""
+    wd = bench.make_workload("dense4096")
+    ws = bench.make_workload("smallm:16:7168:16384:swap")
+    plan = bench.planned_launch(wd)
+    assert plan["kernel"] == fp8g.KERNEL_SM_PAIRS and plan["stream_k"] == 1, plan
+    idn, is_ = bench.host_inputs(wd), bench.host_inputs(ws)
+    Ad, Bd = torch.from_numpy(idn["A"]).cuda(), torch.from_numpy(idn["B"]).cuda()
+    As, Bs = torch.from_numpy(is_["A"]).cuda(), torch.from_numpy(is_["B"]).cuda()
+    n_dense, per_dense = 6, 2
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    Dd = [torch.full((wd.M, wd.N), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(n_dense)]
+    Ds = [torch.full((ws.M, ws.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+          for _ in range(n_dense * per_dense)]
+    start = torch.cuda.Event()
+    torch.cuda.synchronize()
+    start.record(torch.cuda.current_stream())
+    s1.wait_event(start)
+    s2.wait_event(start)
+    for r in range(n_dense):
+        fp8g.fp8_gemm_nt(Ad, Bd, Dd[r], a_dtype=wd.fa, b_dtype=wd.fb, flags=wd.flags, stream=s1)
+        for j in range(per_dense):
+            fp8g.fp8_gemm_nt(As, Bs, Ds[r * per_dense + j], a_dtype=ws.fa, b_dtype=ws.fb, flags=ws.flags,
+                             stream=s2)
+    torch.cuda.synchronize()
+    st = fp8g.fp8g_get_device_status()
+    assert st[0] == fp8g.OK, st
+    ref_d, abs_d = oracle.gemm_nt(idn["A"], idn["B"], wd.fa, wd.fb)
+    ref_s, abs_s = oracle.gemm_nt(is_["A"], is_["B"], ws.fa, ws.fb)
+    first = bits(Dd[0])
+    for r in range(n_dense):
+        got = bits(Dd[r])
+        check_dense(got, ref_d, abs_d, "dense call %d" % r)
+        assert np.array_equal(got, first), "dense call %d differs from the first" % r
+    for i, D in enumerate(Ds):
+        check_dense(bits(D), ref_s, abs_s, "small-M call %d" % i)
