@@ -6,7 +6,14 @@
 One step = one pass of the hot path over one batch of synthetic input: one
 FP8 GEMM (dense D = A.B^T, or the masked grouped MoE-decode GEMM) through
 the C ABI.  Prints ONE JSON line (rank 0).  The default workload is the
-dense 4096^3 E4M3 GEMM (FP32 accumulate, BF16 out) reported in TFLOP/s.
+largest configuration, the dense 8192 x 18432 x 7168 E4M3 projection (FP32
+accumulate, BF16 out), reported in TFLOP/s, with every other configuration
+timed briefly in the line's per_config array.
+
+--mma-microbench instead builds and runs bench_mma.cu: the tensor-core
+instruction costs (plain and block-scaled MMAs, one or two issuers, with and
+without the kernels' stage handshake, SM pairs, scale-set writes), one JSON
+object per line.
 
 Multi-GPU: one process per GPU (torchrun); every rank runs its own shard of
 the same shape (independent output slices, no data-path collective), so
@@ -922,6 +929,20 @@ def run_ours(args, w: Workload):
     return 0
 
 
+def run_mma_microbench() -> int:
+    """Compile bench_mma.cu for sm_103a next to the library and run it."""
+    from fp8_tensor_core_gb300 import build as cuda_build
+    os.makedirs(cuda_build.BUILD, exist_ok=True)
+    exe = os.path.join(cuda_build.BUILD, "bench_mma")
+    src = os.path.join(ROOT, "bench_mma.cu")
+    cmd = [cuda_build.nvcc()] + cuda_build.ARCH + ["-O3", "-std=c++17", "-I", cuda_build.CSRC, "-o", exe, src]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        sys.stderr.write(r.stdout + r.stderr)
+        return r.returncode
+    return subprocess.run([exe]).returncode
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -946,7 +967,11 @@ def main(argv=None):
     ap.add_argument("--per-config-steps-hbm", type=int, default=100,
                     help="timed launches per HBM-bound configuration in per_config")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--mma-microbench", action="store_true",
+                    help="build and run bench_mma.cu (tensor-core instruction costs) instead of a GEMM")
     args = ap.parse_args(argv)
+    if args.mma_microbench:
+        return run_mma_microbench()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     rank, _, _ = dist_setup()

@@ -259,12 +259,13 @@ bool is_device_pointer(const void *p)
 }
 
 // Stages that fit the per-block shared-memory budget beside the control
-// block (FP8G_STAGES(n) caps it; the one-stage debug mode forces 1).
-int pick_stages(const DeviceInfo &d, int stage_bytes, int groups, uint32_t flags)
+// block and `other_bytes` more (FP8G_STAGES(n) caps it; the one-stage debug
+// mode forces 1).
+int pick_stages(const DeviceInfo &d, int stage_bytes, int groups, uint32_t flags, int other_bytes = 0)
 {
     if (flags & FP8G_DEBUG_ONE_STAGE)
         return 1;
-    const int budget = d.smem_optin - ctl_bytes_for(groups) - kSmemAlignPad;
+    const int budget = d.smem_optin - ctl_bytes_for(groups) - kSmemAlignPad - other_bytes;
     int s = std::max(1, std::min(kMaxStages, budget / stage_bytes));
     const int cap = static_cast<int>((flags >> 20) & 15u);
     if (cap > 0)
@@ -899,6 +900,24 @@ int launch(const Problem &p, cudaStream_t stream, const DeviceInfo *forced = nul
     args.tile_n = tile_n;
     if (p.sf_k) {
         plan_blockscaled(args, info, tile_n, static_cast<int>(p.G), p.flags);
+        // 128-element groups: the scale loads use their own ring, issued a
+        // scale set (four K blocks) ahead of the operands, so a stage holds
+        // only the operand tiles -- at 224 columns that leaves room for a
+        // fifth stage.  Measured on GB300 (same box, graph replay, 1x128 /
+        // 128x128 scales), scales riding in the stage of a set's first K
+        // block against the ring: 4096^3 67.9 -> 65.0 us, 8192x7168x18432
+        // 872 -> 818-851 us, 8192x18432x7168 885 -> 858-868 us.  With
+        // 32-element groups (a set per K block) the ring's slot wait at every
+        // K block made 4096^3 slower (101.8 -> 109.5 us): their scales stay in
+        // the stages.
+        if (p.sf_k == 1) {
+            args.sf_ring = kSfRingSlots;
+            args.sf_slot_bytes = sf_stage_bytes(tile_n);
+            args.sf_off = 0;
+            args.stage_bytes = kTileM * kBlockK + tile_n * kBlockK;
+            args.stages = pick_stages(info, args.stage_bytes, static_cast<int>(p.G), p.flags,
+                                      args.sf_ring * args.sf_slot_bytes);
+        }
         if (tile_n > kMaxBlockScaledTile) {   // one accumulator buffer, then the scale sets
             args.acc_bufs = 1;
             args.sf_col0 = tile_n;

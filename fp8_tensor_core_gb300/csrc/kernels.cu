@@ -70,9 +70,10 @@ struct alignas(16) SmemCtl {
     uint64_t tempty[2];
     uint64_t drain;
     uint64_t pair_exit;   // CTA-pair kernel: the peer's "done" arrival
-    uint64_t sffull[kMaxStages];    // this CTA's scale bytes of stage s landed
+    uint64_t sffull[kMaxStages];    // this CTA's scale bytes of stage s (or of ring slot s) landed
     uint64_t sffree[kMaxSfSets];    // TMEM scale set no longer read by any MMA
-    uint64_t sfset_ready[kMaxSfSets];   // SwapAB: scale set written into TMEM by the staging warps
+    uint64_t sfset_ready[kMaxSfSets];   // scale set written into TMEM by the staging warps
+    uint64_t sfslot_free[kSfRingSlots];  // scale ring slot read by the staging warps (single-SM tiles)
     uint64_t drain2;                // SwapAB: completion of the second issuer's tensor-core work
     uint64_t peer_done;             // CTA-pair kernel (even CTA): the odd CTA's loader has stopped
     volatile int32_t peer_issued;   // ... after issuing this many stage fills
@@ -85,6 +86,7 @@ struct alignas(16) SmemCtl {
     int32_t *group_row0;     // [groups] output row of group g's first token row
 };
 static_assert(sizeof(SmemCtl) <= kCtlFixedBytes, "control block too large");
+static_assert(kSfRingSlots <= kMaxStages && kSfRingSlots <= 32, "scale ring barriers and slot masks");
 
 // Warp-uniform bounded wait on an mbarrier phase.  Returns false when the
 // block is aborting (another role timed out) or this wait ran out.
@@ -462,16 +464,18 @@ __device__ __forceinline__ int sf_first_group(int kb, int sf_k) { return sf_k ==
 // TMEM lane quadrant each) and announced on sfset_ready[set] (four
 // arrivals); the MMA issuers only wait for a set and retire it.
 
-// Staging warp, all lanes, for scale load j (the raw bytes of stage_ptr,
-// whose full barrier has passed): build one 32-bit word per row (byte g =
-// K group g of the load), wait until every issuer has retired the set's
-// previous contents, write the set into this warp's lane quadrant -- row r
-// of side A at lane r % 32, column r / 32; side B from column 4 likewise --
-// and arrive (kPair: on the even CTA's barrier, which counts both CTAs'
-// staging warps).  box_b <= 256.  Returns false when a wait gave up.
+// Staging warp, all lanes, for scale load j (raw: its bytes, [4][128] of
+// side A then [4][box_b] of side B, whose full barrier has passed): build
+// one 32-bit word per row (byte g = K group g of the load); if slot_free is
+// given, release the bytes' buffer there (one arrival per staging warp);
+// wait until every issuer has retired the set's previous contents, write
+// the set into this warp's lane quadrant -- row r of side A at lane r % 32,
+// column r / 32; side B from column 4 likewise -- and arrive (kPair: on the
+// even CTA's barrier, which counts both CTAs' staging warps).  box_b <= 256.
+// Returns false when a wait gave up.
 template <bool kPair = false>
-__device__ __forceinline__ bool sf_stage_tmem(SmemCtl &ctl, const GemmArgs &a, const uint8_t *stage_ptr, int box_b,
-                                              int j, uint32_t sets_q, int set_cols)
+__device__ __forceinline__ bool sf_stage_tmem(SmemCtl &ctl, const GemmArgs &a, const uint8_t *raw, int box_b,
+                                              int j, uint32_t sets_q, int set_cols, uint64_t *slot_free = nullptr)
 {
     const int lane = threadIdx.x & 31;
     const int R = a.sf_sets;
@@ -480,8 +484,8 @@ __device__ __forceinline__ bool sf_stage_tmem(SmemCtl &ctl, const GemmArgs &a, c
         return static_cast<uint32_t>(raw[r]) | (static_cast<uint32_t>(raw[box + r]) << 8) |
                (static_cast<uint32_t>(raw[2 * box + r]) << 16) | (static_cast<uint32_t>(raw[3 * box + r]) << 24);
     };
-    const uint8_t *raw_a = stage_ptr + a.sf_off;   // [4][128]
-    const uint8_t *raw_b = raw_a + 4 * kTileM;      // [4][box_b]
+    const uint8_t *raw_a = raw;                 // [4][128]
+    const uint8_t *raw_b = raw_a + 4 * kTileM;  // [4][box_b]
     uint32_t wa[4], wb[8];
 #pragma unroll
     for (int c = 0; c < 4; ++c)
@@ -490,6 +494,11 @@ __device__ __forceinline__ bool sf_stage_tmem(SmemCtl &ctl, const GemmArgs &a, c
     for (int c = 0; c < 8; ++c) {
         const int r = 32 * c + lane;
         wb[c] = r < box_b ? word(raw_b, box_b, r) : 0u;
+    }
+    if (slot_free) {
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_addr(slot_free));
     }
     if (j >= R && !warp_wait(smem_addr(&ctl.sffree[set]), static_cast<uint32_t>((j / R - 1) & 1), ctl, a.timeout_ns,
                              kRoleScales, 400 + set))
@@ -616,10 +625,12 @@ __device__ __forceinline__ int find_group(const SmemCtl &ctl, int groups, int u)
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// Shared-memory carve-up common to both kernels: `stages` stages of
-// `stage_bytes` starting at a 1024-byte aligned base, then the control block.
+// Shared-memory carve-up common to the kernels: `stages` stages of
+// `stage_bytes` starting at a 1024-byte aligned base, the scale ring (if
+// any), then the control block.
 struct Smem {
     uint8_t *stages;
+    uint8_t *sf_ring;
     SmemCtl *ctl;
 };
 
@@ -629,7 +640,8 @@ __device__ __forceinline__ Smem carve(uint8_t *raw, const GemmArgs &a)
     const uint32_t pad = (1024u - (base & 1023u)) & 1023u;
     Smem s;
     s.stages = raw + pad;
-    s.ctl = reinterpret_cast<SmemCtl *>(s.stages + static_cast<size_t>(a.stages) * a.stage_bytes);
+    s.sf_ring = s.stages + static_cast<size_t>(a.stages) * a.stage_bytes;
+    s.ctl = reinterpret_cast<SmemCtl *>(s.sf_ring + static_cast<size_t>(a.sf_ring) * a.sf_slot_bytes);
     int32_t *tables = reinterpret_cast<int32_t *>(reinterpret_cast<uint8_t *>(s.ctl) + kCtlFixedBytes);
     s.ctl->group_prefix = tables;
     s.ctl->group_m = tables + a.groups + 1;
@@ -650,12 +662,17 @@ __device__ __forceinline__ void init_barriers(SmemCtl &ctl, int stages, uint32_t
     }
     mbar_init(smem_addr(&ctl.drain), 1);
     mbar_init(smem_addr(&ctl.drain2), 1);
-    for (int s = 0; s < stages; ++s)
+    // Scale-byte barriers: one per stage, or per ring slot (single-SM tiles,
+    // whatever the stage count).
+    const int sf_bars = stages > kSfRingSlots ? stages : kSfRingSlots;
+    for (int s = 0; s < sf_bars; ++s)
         mbar_init(smem_addr(&ctl.sffull[s]), 1);
     for (int i = 0; i < kMaxSfSets; ++i) {
         mbar_init(smem_addr(&ctl.sffree[i]), issuers);
         mbar_init(smem_addr(&ctl.sfset_ready[i]), 4);   // one arrival per staging warp
     }
+    for (int i = 0; i < kSfRingSlots; ++i)
+        mbar_init(smem_addr(&ctl.sfslot_free[i]), 4);   // one arrival per staging warp
     ctl.abort = 0;
     fence_mbar_init();
 }
@@ -699,14 +716,16 @@ __device__ __forceinline__ void loader_tail(SmemCtl &ctl, const GemmArgs &a, int
     }
 }
 
-// Loader (all lanes), block-scaled single-SM and SwapAB kernels: the scale
-// bytes of a stage complete on their own barrier sffull[s].  `par` holds,
-// per stage, the parity of the number of scale fills posted, `used` which
-// stages ever had one; wait (bounded) until the last fill of each has
-// landed.  Without an abort they all have (the staging warps consumed them).
-__device__ __forceinline__ void sf_loader_drain(SmemCtl &ctl, const GemmArgs &a, uint32_t par, uint32_t used)
+// Loader (all lanes), block-scaled kernels: scale bytes complete on their
+// own barriers sffull[s], one per stage (SM-pair and SwapAB kernels) or per
+// ring slot (single-SM tiles), n_bars of them.  `par` holds, per barrier,
+// the parity of the number of scale fills posted, `used` which ever had
+// one; wait (bounded) until the last fill of each has landed.  Without an
+// abort they all have (the staging warps consumed them).
+__device__ __forceinline__ void sf_loader_drain(SmemCtl &ctl, const GemmArgs &a, uint32_t par, uint32_t used,
+                                                int n_bars)
 {
-    for (int s = 0; s < a.stages; ++s)
+    for (int s = 0; s < n_bars; ++s)
         if ((used >> s) & 1u)
             warp_wait_drain(smem_addr(&ctl.sffull[s]), ((par >> s) & 1u) ^ 1u, a.timeout_ns);
 }
@@ -834,6 +853,24 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
     if (threadIdx.x == 0)
         grid_dep_launch_dependents();
 
+    // Block scales, two ways.  With a ring (a.sf_ring > 0, 128-element
+    // groups) the scale loads form their own sequence, one per scale set --
+    // K blocks 0, 4, 8, ... of each of this CTA's tiles -- into a ring of
+    // a.sf_ring slots, kept one set ahead of the operands so that the staging
+    // warps have written a set into TMEM before its first MMA.  Without one
+    // (32-element groups: a set per K block) each K block's scale bytes ride
+    // in its stage.
+    const bool sf_ring = kBS && a.sf_ring > 0;
+    const int sf_step = a.sf_k == 4 ? 1 : 4;
+    const int sf_ahead = 1;
+    auto sf_advance = [&](int &u, int &kb) {
+        kb += sf_step;
+        if (kb >= a.num_kb) {
+            kb = 0;
+            u += gridDim.x;
+        }
+    };
+
     if (warp == 0) {
         // ------------------------------- loader -------------------------------
         int stage = 0;
@@ -841,17 +878,55 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
         long long issued = 0;
         bool aborted = false;
         const bool drop = (a.flags & FP8G_DEBUG_DROP_FIRST_LOAD) && blockIdx.x == 0;
-        uint32_t sf_par = 0, sf_used = 0;   // per stage: parity of scale fills posted, any posted
+        uint32_t sf_par = 0, sf_used = 0;   // per ring slot (or stage): parity of scale fills posted, any posted
+        int sf_u = blockIdx.x, sf_kb = 0;   // next scale load (its tile and first K block)
+        int sf_posted = 0, sf_reached = 0;  // scale loads posted; scale sets whose first K block was reached
+        // Post the next scale load into slot sf_posted % sf_ring, once the
+        // staging warps have read that slot's previous load.
+        auto sf_post = [&]() -> bool {
+            const int slot = sf_posted % a.sf_ring;
+            if (sf_posted >= a.sf_ring &&
+                !warp_wait(smem_addr(&ctl.sfslot_free[slot]), static_cast<uint32_t>((sf_posted / a.sf_ring - 1) & 1),
+                           ctl, a.timeout_ns, kRoleLoader, 600 + slot))
+                return false;
+            if (lane == 0) {
+                int g, m0, n0, mv;
+                decode(sf_u, g, m0, n0, mv);
+                uint8_t *dst = sm.sf_ring + static_cast<size_t>(slot) * a.sf_slot_bytes;
+                const uint32_t sb = smem_addr(&ctl.sffull[slot]);
+                const int y = sf_first_group(sf_kb, a.sf_k);
+                mbar_arrive_expect_tx(sb, sf_bytes);
+                tma_load_3d(smem_addr(dst), &tm_sa, sb, m0, y, g);
+                tma_load_3d(smem_addr(dst + 4 * kTileM), &tm_sb, sb, n0, y, g);
+            }
+            __syncwarp();
+            sf_par ^= 1u << slot;
+            sf_used |= 1u << slot;
+            ++sf_posted;
+            sf_advance(sf_u, sf_kb);
+            return true;
+        };
         for (int u = blockIdx.x; u < total && !aborted; u += gridDim.x) {
             int g, m0, n0, mv;
             decode(u, g, m0, n0, mv);
             for (int kb = 0; kb < a.num_kb; ++kb) {
+                if (sf_ring && sf_load_at(kb, 0, a.sf_k)) {
+                    ++sf_reached;
+                    while (sf_posted < sf_reached + sf_ahead && sf_u < total) {
+                        if (!sf_post()) {
+                            aborted = true;
+                            break;
+                        }
+                    }
+                    if (aborted)
+                        break;
+                }
                 if (!warp_wait(smem_addr(&ctl.empty[stage]), phase ^ 1u, ctl, a.timeout_ns,
                                kRoleLoader, stage)) {
                     aborted = true;
                     break;
                 }
-                const bool sf = kBS && sf_load_at(kb, 0, a.sf_k) && !(drop && issued == 0);
+                const bool sf = kBS && !sf_ring && sf_load_at(kb, 0, a.sf_k) && !(drop && issued == 0);
                 if (lane == 0 && !(drop && issued == 0)) {
                     uint8_t *sa = sm.stages + static_cast<size_t>(stage) * a.stage_bytes;
                     const uint32_t fb = smem_addr(&ctl.full[stage]);
@@ -880,7 +955,7 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
         }
         loader_tail(ctl, a, stage, phase, issued, aborted, drop);
         if constexpr (kBS)
-            sf_loader_drain(ctl, a, sf_par, sf_used);
+            sf_loader_drain(ctl, a, sf_par, sf_used, sf_ring ? a.sf_ring : a.stages);
     } else if (warp == 1 && !kBS) {
         // ----------------------------- MMA issuer -----------------------------
         const uint32_t idesc = make_idesc(a.a_fmt, a.b_fmt, kTileM, a.tile_n);
@@ -1004,29 +1079,37 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
         mma_drain(ctl, a, issued_any, me == 0 ? &ctl.drain : &ctl.drain2);
     } else if (kBS && warp >= 7) {
         // --------------------- block-scale staging into TMEM ---------------------
+        // Warps 7-10, one per TMEM lane quadrant: scale load j becomes TMEM
+        // scale set j (sf_stage_tmem).  From a ring slot (j % sf_ring),
+        // released as soon as its bytes are in registers; else from the stage
+        // of the set's K block.
         if constexpr (kBS) {
             const uint32_t sets_q = tmem_base + static_cast<uint32_t>(a.sf_col0) +
                                     (static_cast<uint32_t>((warp & 3) * 32) << 16);
+            int su = blockIdx.x, skb = 0;
             int stage = 0;
-            uint32_t sf_par = 0;   // per stage: parity of the next scale fill to wait for
-            int j = -1;
-            bool stop = false;
-            for (int u = blockIdx.x; u < total && !stop; u += gridDim.x) {
-                for (int kb = 0; kb < a.num_kb; ++kb) {
-                    if (sf_load_at(kb, 0, a.sf_k)) {
-                        ++j;
-                        if (!warp_wait(smem_addr(&ctl.sffull[stage]), (sf_par >> stage) & 1u, ctl, a.timeout_ns,
-                                       kRoleScales, stage) ||
-                            !sf_stage_tmem(ctl, a, sm.stages + static_cast<size_t>(stage) * a.stage_bytes, a.tile_n,
-                                           j, sets_q, set_cols)) {
-                            stop = true;
-                            break;
-                        }
-                        sf_par ^= 1u << stage;
-                    }
+            uint32_t st_par = 0;   // per stage: parity of the next scale fill to wait for
+            for (int j = 0; su < total; ++j) {
+                if (sf_ring) {
+                    const int slot = j % a.sf_ring;
+                    if (!warp_wait(smem_addr(&ctl.sffull[slot]), static_cast<uint32_t>((j / a.sf_ring) & 1), ctl,
+                                   a.timeout_ns, kRoleScales, 700 + slot) ||
+                        !sf_stage_tmem(ctl, a, sm.sf_ring + static_cast<size_t>(slot) * a.sf_slot_bytes, a.tile_n, j,
+                                       sets_q, set_cols, &ctl.sfslot_free[slot]))
+                        break;
+                } else {
+                    // every K block carries a scale load (32-element groups):
+                    // the sets follow the stages one to one
+                    if (!warp_wait(smem_addr(&ctl.sffull[stage]), (st_par >> stage) & 1u, ctl, a.timeout_ns,
+                                   kRoleScales, stage) ||
+                        !sf_stage_tmem(ctl, a, sm.stages + static_cast<size_t>(stage) * a.stage_bytes + a.sf_off,
+                                       a.tile_n, j, sets_q, set_cols))
+                        break;
+                    st_par ^= 1u << stage;
                     if (++stage == a.stages)
                         stage = 0;
                 }
+                sf_advance(su, skb);
             }
         }
     } else if (warp >= 2 && warp <= 5) {
@@ -1436,7 +1519,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
         }
         // Scale bytes complete on each CTA's own barriers.
         if constexpr (kBS)
-            sf_loader_drain(ctl, a, sf_par, sf_used);
+            sf_loader_drain(ctl, a, sf_par, sf_used, a.stages);
     } else if (warp == 1 && !kBS) {
         // ----------------------------- MMA issuer -----------------------------
         if (leader) {
@@ -1622,7 +1705,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBS ? kThreadsTmemSc
                         ++j;
                         if (!warp_wait(smem_addr(&ctl.sffull[stage]), (sf_par >> stage) & 1u, ctl, a.timeout_ns,
                                        kRoleScales, stage) ||
-                            !sf_stage_tmem<true>(ctl, a, sm.stages + static_cast<size_t>(stage) * a.stage_bytes,
+                            !sf_stage_tmem<true>(ctl, a,
+                                                 sm.stages + static_cast<size_t>(stage) * a.stage_bytes + a.sf_off,
                                                  a.tile_n, j, sets_q, set_cols)) {
                             aborted = true;
                             break;
@@ -2050,7 +2134,7 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
         }
         loader_tail(ctl, a, stage, phase, issued, aborted, drop);
         if constexpr (kBS)
-            sf_loader_drain(ctl, a, sf_par, sf_used);
+            sf_loader_drain(ctl, a, sf_par, sf_used, a.stages);
     } else if (warp == 1 && !kBS) {
         // ----------------------------- MMA issuer -----------------------------
         // MMA operand A = weight tile (format of B), operand B = token tile
@@ -2201,8 +2285,8 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
                         ++j;
                         if (!warp_wait(smem_addr(&ctl.sffull[stage]), (sf_par >> stage) & 1u, ctl, a.timeout_ns,
                                        kRoleScales, stage) ||
-                            !sf_stage_tmem(ctl, a, sm.stages + static_cast<size_t>(stage) * a.stage_bytes, cap, j,
-                                           sets_q, set_cols)) {
+                            !sf_stage_tmem(ctl, a, sm.stages + static_cast<size_t>(stage) * a.stage_bytes + a.sf_off,
+                                           cap, j, sets_q, set_cols)) {
                             stop = true;
                             break;
                         }
@@ -2463,7 +2547,10 @@ cudaError_t launch_gemm_mn(const CUtensorMap &tm_a, const CUtensorMap &tm_b, con
                            const CUtensorMap &tm_sb, const GemmArgs &args, int grid, size_t smem,
                            cudaStream_t stream)
 {
-    if (smem < smem_bytes_for(args.stages, args.stage_bytes, args.groups) || !dual_ok(args))
+    if (smem < smem_bytes_of(args) || !dual_ok(args) ||
+        (args.sf_k == 1 && (args.sf_ring < 1 || args.sf_ring > kSfRingSlots || args.sf_slot_bytes % 128 != 0 ||
+                            args.sf_slot_bytes < 4 * (kTileM + args.tile_n))) ||
+        (args.sf_k == 4 && args.sf_ring != 0))
         return cudaErrorInvalidValue;
     const bool epi = wants_epi(args);
     if (args.sf_k)
@@ -2492,7 +2579,7 @@ cudaError_t launch_gemm_mn2(const CUtensorMap &tm_a, const CUtensorMap &tm_b, co
 {
     // Grouped problems: plain kernels, whole tiles.
     const bool grouped = args.groups != 1 || args.masked_m != nullptr || args.group_offsets != nullptr;
-    if (smem < smem_bytes_for(args.stages, args.stage_bytes, args.groups) || (grid & 1) ||
+    if (smem < smem_bytes_of(args) || (grid & 1) ||
         (grouped && (args.sf_k || args.k_splits != 1)) || !dual_ok(args))
         return cudaErrorInvalidValue;
     const bool epi = wants_epi(args);
@@ -2520,7 +2607,7 @@ cudaError_t launch_gemm_swap(const CUtensorMap &tm_w, const CUtensorMap &tm_t, c
                              const CUtensorMap &tm_st, const GemmArgs &args, int grid, size_t smem,
                              cudaStream_t stream)
 {
-    if (smem < smem_bytes_for(args.stages, args.stage_bytes, args.groups) || !dual_ok(args))
+    if (smem < smem_bytes_of(args) || !dual_ok(args))
         return cudaErrorInvalidValue;
     const bool epi = wants_epi(args);
     if (args.sf_k)

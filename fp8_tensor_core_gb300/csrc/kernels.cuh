@@ -27,6 +27,7 @@ constexpr int kThreads = 192;        // warp 0 loader, warp 1 MMA issuer, warps 
 constexpr int kThreadsTmemScaled = 352;  // block-scaled instantiations: + warp 6, second MMA issuer,
                                          // and warps 7-10, scale sets into TMEM
 constexpr int kMaxSfSets = 4;        // TMEM block-scale sets in flight
+constexpr int kSfRingSlots = 3;      // single-SM block-scaled tiles: scale loads in flight
 constexpr int kTmemCols = 512;       // two accumulators of up to 256 columns
 constexpr int kAccStride = 256;
 constexpr int kCtlFixedBytes = 768;  // barriers, TMEM slot, flags
@@ -87,6 +88,12 @@ struct GemmArgs {
     int32_t sf_off;            // byte offset of the scale area inside a stage
     int32_t sf_col0;           // first TMEM column of the block-scale sets
     int32_t sf_sets;           // TMEM block-scale sets (2..kMaxSfSets)
+    int32_t sf_ring;           // single-SM tile kernel with 128-element groups (required there): the
+                               // scale loads have a ring of sf_ring slots of sf_slot_bytes after the
+                               // stages, each load issued one scale set ahead of the operands;
+                               // 0 (every other case): scale bytes ride in the stage of their
+                               // first K block
+    int32_t sf_slot_bytes;     // bytes per ring slot: [4][128] side A then [4][tile_n] side B, 128-aligned
     int32_t dual_mma;          // block-scaled SwapAB / single-SM kernels: two MMA-issuing threads,
                                // each with its own accumulators, alternating K blocks
     int32_t tok_box;           // swap kernel: token rows per TMA box of a chunk (a multiple of 16
@@ -136,8 +143,13 @@ inline size_t smem_bytes_for(int stages, int stage_bytes, int groups)
     return static_cast<size_t>(stages) * stage_bytes + ctl_bytes_for(groups) + kSmemAlignPad;
 }
 
-// `smem` must be at least smem_bytes_for(stages, stage_bytes, groups); the
-// host passes the whole per-block budget so that exactly one CTA (and one
+// The same for a planned launch: stages, the scale ring if any, control block.
+inline size_t smem_bytes_of(const GemmArgs &a)
+{
+    return smem_bytes_for(a.stages, a.stage_bytes, a.groups) + static_cast<size_t>(a.sf_ring) * a.sf_slot_bytes;
+}
+
+// `smem` must be at least smem_bytes_of(args); the host passes the whole per-block budget so that exactly one CTA (and one
 // 512-column TMEM allocation) is resident per SM.
 // tm_sa / tm_sb: block-scale maps of the MMA's A and B sides (read only when
 // args.sf_k != 0; any valid map otherwise).

@@ -113,6 +113,17 @@ def test_single_sm_narrow_tiles_two_issuers(tn, gran):
                    seed=527 + tn + gran)
 
 
+@pytest.mark.parametrize("stages", [0, 1, 2])
+@pytest.mark.parametrize("K", [256, 384, 640])
+def test_single_sm_scale_ring_across_tiles(K, stages):
+    """128-element groups on single-SM tiles: the scale loads run one set
+    ahead of the operands in their own three-slot ring.  2-3 tiles per CTA
+    and K of 2, 3 or 5 blocks make the look-ahead cross tile boundaries, with
+    1, 2 or the default number of stages."""
+    flags = OFF | fp8g.SINGLE_SM_TILES | (fp8g.STAGES(stages) if stages else 0)
+    check_dense_bs(4096, 2048, K, 128, flags, seed=560 + K + stages)
+
+
 @pytest.mark.parametrize("gran", [128, 32])
 @pytest.mark.parametrize("issuers", [0, fp8g.TWO_MMA_ISSUERS, fp8g.ONE_MMA_ISSUER])
 def test_dense_pair_many_tiles_and_k_blocks(issuers, gran):
