@@ -6,7 +6,11 @@
 // four MMAs, commit to an empty barrier), for one SM (cta_group::1) and for an
 // SM pair (cta_group::2); and how long four warps take to write one block-scale
 // set into TMEM.  Every SM runs one CTA (or one CTA of a pair), as the kernels
-// do.  All waits are bounded; a wait that runs out sets an error flag.
+// do.  The handshake cases can also stream bytes from L2 into shared memory
+// with bulk copies completing on the full barriers, as the kernels' operand
+// loads do (the MMAs still read the resident operands), to show what that
+// traffic costs the MMA stream.  All waits are bounded; a wait that runs out
+// sets an error flag.
 //
 // Build and run (bench.py --mma-microbench does both):
 //   nvcc -gencode arch=compute_103a,code=sm_103a -O3 -std=c++17 \
@@ -24,6 +28,8 @@ using namespace fp8g;
 namespace {
 
 constexpr int kStages = 4;                  // handshake ring (all on the same resident operands)
+constexpr int kCopyStages = 3;              // ... with copy traffic (one buffer per stage)
+constexpr int kCopyMax = 48 * 1024;         // copy bytes per stage at most
 constexpr int kSetCol = 448;                // TMEM column of the scale set (A side 4, B side 8 columns)
 constexpr uint64_t kLimitNs = 2000000000ull;  // bound on every wait
 constexpr int kThreads = 128;
@@ -41,6 +47,7 @@ enum Mode : int {
 struct Smem {
     uint8_t a[128 * 128];   // A: 128 rows x 128 bytes of K, 128-byte swizzle atoms
     uint8_t b[256 * 128];   // B: up to 256 rows
+    uint8_t copy[kCopyStages][kCopyMax];   // bulk-copy targets (traffic only)
     uint64_t full[kStages];
     uint64_t empty[kStages];
     uint64_t commit_sink;   // per-K-block commits nobody waits for
@@ -73,6 +80,14 @@ __device__ bool warp_wait_bounded(uint32_t bar, uint32_t parity, uint64_t t0, in
     if (!ok && (threadIdx.x & 31) == 0)
         atomicExch(flag, 1);
     return ok;
+}
+
+// Bulk copy global -> this CTA's shared memory, completing on an mbarrier.
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
 }
 
 __device__ void fill_operands(Smem &s)
@@ -138,7 +153,8 @@ __device__ Smem &carve()
 
 // One SM per CTA.  Returns per CTA the nanoseconds from the common start to
 // the completion of every MMA (or of every scale-set write).
-__global__ void __launch_bounds__(kThreads, 1) k_single(int mode, int n, int iters, unsigned long long *ns_out,
+__global__ void __launch_bounds__(kThreads, 1) k_single(int mode, int n, int iters, int copy_bytes,
+                                                        const uint8_t *copy_src, unsigned long long *ns_out,
                                                         int *flag)
 {
     Smem &s = carve();
@@ -196,17 +212,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_single(int mode, int n, int ite
                 break;
         }
     } else if (mode == kPlainHs || mode == kBlockScaledHs) {
+        const int stages = copy_bytes > 0 ? kCopyStages : kStages;
         if (warp == 0) {
-            // producer: frees nothing, just passes each stage on once the MMAs released it
+            // producer: passes each stage on once the MMAs released it, after
+            // copying copy_bytes from L2 into the stage's buffer (if any)
             int st = 0;
             uint32_t ph = 0;
+            const uint8_t *src = copy_src + static_cast<size_t>(blockIdx.x % 16) * kCopyMax * kCopyStages;
             for (int i = 0; i < iters; ++i) {
                 if (!warp_wait_bounded(smem_addr(&s.empty[st]), ph ^ 1u, t0, flag))
                     break;
-                if (lane == 0)
-                    mbar_arrive(smem_addr(&s.full[st]));
+                if (lane == 0) {
+                    const uint32_t fb = smem_addr(&s.full[st]);
+                    if (copy_bytes > 0) {
+                        mbar_arrive_expect_tx(fb, static_cast<uint32_t>(copy_bytes));
+                        for (int off = 0; off < copy_bytes; off += 16384) {
+                            const int len = copy_bytes - off < 16384 ? copy_bytes - off : 16384;
+                            bulk_copy(smem_addr(s.copy[st] + off), src + static_cast<size_t>(st) * kCopyMax + off,
+                                      static_cast<uint32_t>(len), fb);
+                        }
+                    } else {
+                        mbar_arrive(fb);
+                    }
+                }
                 __syncwarp();
-                if (++st == kStages) {
+                if (++st == stages) {
                     st = 0;
                     ph ^= 1u;
                 }
@@ -228,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_single(int mode, int n, int ite
                     mma_commit(smem_addr(&s.empty[st]));
                 }
                 __syncwarp();
-                if (++st == kStages) {
+                if (++st == stages) {
                     st = 0;
                     ph ^= 1u;
                 }
@@ -359,14 +389,17 @@ int main()
     const int grid = sms & ~1;
     unsigned long long *d_ns = nullptr;
     int *d_flag = nullptr;
+    uint8_t *d_copy = nullptr;   // L2-resident copy source: 16 CTA slots of kCopyStages x kCopyMax bytes
     if (check(cudaMalloc(&d_ns, sizeof(unsigned long long) * grid), "malloc") ||
-        check(cudaMalloc(&d_flag, sizeof(int)), "malloc") || check(cudaMemset(d_flag, 0, sizeof(int)), "memset"))
+        check(cudaMalloc(&d_flag, sizeof(int)), "malloc") || check(cudaMemset(d_flag, 0, sizeof(int)), "memset") ||
+        check(cudaMalloc(&d_copy, static_cast<size_t>(16) * kCopyStages * kCopyMax), "malloc") ||
+        check(cudaMemset(d_copy, 0x38, static_cast<size_t>(16) * kCopyStages * kCopyMax), "memset"))
         return 1;
     const int iters = 4096;   // K blocks: 16384 MMAs per issuing CTA
     const char *names[] = {"plain", "block_scaled", "plain", "block_scaled", "plain", "block_scaled", "scale_set_write"};
 
     auto report = [&](const char *kind, int cta_group, int issuers, bool handshake, int n, long long units,
-                      const char *unit) -> int {
+                      const char *unit, int copy_bytes = 0) -> int {
         if (check(cudaDeviceSynchronize(), kind))
             return 1;
         unsigned long long h[512] = {};
@@ -377,24 +410,29 @@ int main()
         for (int i = 0; i < grid; ++i)
             worst = h[i] > worst ? h[i] : worst;
         std::printf("{\"op\": \"%s\", \"cta_group\": %d, \"issuers\": %d, \"handshake\": %s, \"n\": %d, "
-                    "\"ns_per_%s\": %.2f, \"ctas\": %d, \"timed_out\": %s}\n",
-                    kind, cta_group, issuers, handshake ? "true" : "false", n, unit,
+                    "\"copy_bytes_per_kblock\": %d, \"ns_per_%s\": %.2f, \"ctas\": %d, \"timed_out\": %s}\n",
+                    kind, cta_group, issuers, handshake ? "true" : "false", n, copy_bytes, unit,
                     static_cast<double>(worst) / static_cast<double>(units), grid, flag ? "true" : "false");
         std::fflush(stdout);
         return flag;
     };
 
     // one SM per CTA
-    struct Case { int mode, n; };
+    // copy bytes per K block with the handshake: 0, an SM pair's per-SM operand
+    // bytes (256 x 256 tile: 16 KB + 16 KB), and a single SM's at 224 / 256
+    // columns (16 KB + 28 KB / 32 KB)
+    struct Case { int mode, n, copy; };
     const Case cases[] = {
-        {kPlain, 32}, {kPlain, 128}, {kPlain, 224}, {kPlain, 256},
-        {kBlockScaled, 32}, {kBlockScaled, 128}, {kBlockScaled, 224}, {kBlockScaled, 256},
-        {kPlain2, 128}, {kPlain2, 224}, {kBlockScaled2, 128}, {kBlockScaled2, 224},
-        {kPlainHs, 224}, {kPlainHs, 256}, {kBlockScaledHs, 224}, {kBlockScaledHs, 256},
+        {kPlain, 32, 0}, {kPlain, 128, 0}, {kPlain, 224, 0}, {kPlain, 256, 0},
+        {kBlockScaled, 32, 0}, {kBlockScaled, 128, 0}, {kBlockScaled, 224, 0}, {kBlockScaled, 256, 0},
+        {kPlain2, 128, 0}, {kPlain2, 224, 0}, {kBlockScaled2, 128, 0}, {kBlockScaled2, 224, 0},
+        {kPlainHs, 224, 0}, {kPlainHs, 256, 0}, {kBlockScaledHs, 224, 0}, {kBlockScaledHs, 256, 0},
+        {kPlainHs, 256, 32768}, {kPlainHs, 224, 45056}, {kPlainHs, 256, 49152},
+        {kBlockScaledHs, 224, 45056}, {kBlockScaledHs, 256, 49152},
     };
     for (const Case &c : cases) {
         for (int rep = 0; rep < 2; ++rep) {   // the first run warms up
-            k_single<<<grid, kThreads, smem>>>(c.mode, c.n, iters, d_ns, d_flag);
+            k_single<<<grid, kThreads, smem>>>(c.mode, c.n, iters, c.copy, d_copy, d_ns, d_flag);
             if (check(cudaGetLastError(), "launch"))
                 return 1;
             if (rep == 0) {
@@ -404,12 +442,12 @@ int main()
             }
             const int issuers = (c.mode == kPlain2 || c.mode == kBlockScaled2) ? 2 : 1;
             const bool hs = c.mode == kPlainHs || c.mode == kBlockScaledHs;
-            if (report(names[c.mode], 1, issuers, hs, c.n, 4LL * iters, "mma"))
+            if (report(names[c.mode], 1, issuers, hs, c.n, 4LL * iters, "mma", c.copy))
                 return 2;
         }
     }
     for (int rep = 0; rep < 2; ++rep) {
-        k_single<<<grid, kThreads, smem>>>(kScaleSetWrite, 0, iters, d_ns, d_flag);
+        k_single<<<grid, kThreads, smem>>>(kScaleSetWrite, 0, iters, 0, d_copy, d_ns, d_flag);
         if (check(cudaGetLastError(), "launch"))
             return 1;
         if (rep == 1 && report(names[kScaleSetWrite], 1, 4, true, 0, iters, "set"))
@@ -435,6 +473,7 @@ int main()
         }
     }
     std::printf("{\"sm_clock_mhz_attr\": %d}\n", clk_khz / 1000);
+    cudaFree(d_copy);
     cudaFree(d_ns);
     cudaFree(d_flag);
     return 0;
