@@ -3,12 +3,11 @@
 //
 // Some callers cannot let a library call cudaMalloc: a framework whose
 // caching allocator must own every device byte (it accounts, pools and
-// reuses memory and would be bypassed), a serving loop that must not take
-// cudaMalloc's implicit device-wide synchronisation on its latency path, or
-// code that records its launches into a CUDA graph, where allocation calls
-// are not allowed while capturing.  fp8_gemm_nt may allocate its stream-K
-// workspace on first use; this entry point never allocates.  It launches the
-// same k_gemm_swap kernel as fp8_gemm_nt's SwapAB path, pointing the
+// reuses memory and would be bypassed), or a serving loop that must not take
+// cudaMalloc's implicit device-wide synchronisation on its latency path.
+// fp8_gemm_nt may allocate its stream-K workspace on first use; this entry
+// point never allocates.  It launches the same k_gemm_swap kernel as
+// fp8_gemm_nt's SwapAB path, pointing the
 // kernel's stream-K partial tiles and arrival counters at g_noalloc_scratch.
 // Its configuration differs in one respect: every CTA takes a whole SM (all
 // of its shared memory and 512 TMEM columns), while fp8_gemm_nt lets two

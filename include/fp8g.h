@@ -422,9 +422,8 @@ uint64_t fp8g_set_wait_timeout_ns(uint64_t ns);
  * counterpart.)
  *
  * For callers that cannot have a library call cudaMalloc: a framework whose
- * caching allocator must own every device byte, a serving loop that cannot
- * take cudaMalloc's device-wide synchronisation, code recording launches into
- * a CUDA graph (allocation is not allowed while capturing).  fp8_gemm_nt may
+ * caching allocator must own every device byte, or a serving loop that cannot
+ * take cudaMalloc's device-wide synchronisation.  fp8_gemm_nt may
  * allocate its stream-K workspace on first use; this call instead keeps that
  * scratch in one fixed device array of FP8G_NOALLOC_SCRATCH_BYTES (32 MiB)
  * inside the library, which every GPU that loads the library holds until the
@@ -445,9 +444,9 @@ uint64_t fp8g_set_wait_timeout_ns(uint64_t ns);
  *   to 256 tokens (chunks of 224, 240, 256) fit only launches of fewer CTAs.
  *   No cudaMalloc, cudaFree or allocating library routine is called.  The
  *   first call on a device looks up the array's device address and the
- *   device limits (once per device, with that device current): make that
- *   first call before any stream capture.  Each call clears the scratch's
- *   arrival counters with cudaMemsetAsync on `stream` before its launch.
+ *   device limits (once per device, with that device current).  Each call
+ *   clears the scratch's arrival counters with cudaMemsetAsync on `stream`
+ *   before its launch.
  *   All calls on a device share the array: calls that overlap on the GPU
  *   (unordered streams) race on it and give wrong results.
  *   Bounded waits use the default 2 s limit.

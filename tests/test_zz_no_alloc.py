@@ -1,6 +1,6 @@
 """fp8_gemm_nt_noalloc, the entry point that allocates no device memory
 (for callers whose own allocator must own every device byte, or that cannot
-take cudaMalloc's synchronisation or call it during graph capture).  Its
+take cudaMalloc's synchronisation).  Its
 stream-K scratch is a fixed device array inside the library, shared by every
 call, so two calls in a row must both agree with the oracle (and, bit for
 bit, with the allocating entry point that runs the same kernel).
