@@ -7,8 +7,8 @@
 // cudaMalloc's implicit device-wide synchronisation on its latency path.
 // fp8_gemm_nt may allocate its stream-K workspace on first use; this entry
 // point never allocates.  It launches the same k_gemm_swap kernel as
-// fp8_gemm_nt's SwapAB path, pointing the
-// kernel's stream-K partial tiles and arrival counters at g_noalloc_scratch.
+// fp8_gemm_nt's SwapAB path, pointing the kernel's stream-K partial tiles
+// and arrival counters at g_noalloc_scratch.
 // Its configuration differs in one respect: every CTA takes a whole SM (all
 // of its shared memory and 512 TMEM columns), while fp8_gemm_nt lets two
 // launches share an SM for problems of up to 16 tokens.
