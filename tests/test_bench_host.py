@@ -215,3 +215,15 @@ def test_planned_launch_names_the_kernel(monkeypatch):
                          ("grouped:16:160:4096:7168:auto", "k_gemm_swap")]:
         plan = bench.planned_launch(bench.make_workload(name))
         assert bench.KERNEL_NAMES[plan["kernel"]] == kernel, (name, plan)
+
+
+def test_mma_microbench_builds(tmp_path):
+    """bench_mma.cu (bench.py --mma-microbench) compiles for sm_103a against
+    the library's PTX wrappers (no GPU needed to build it)."""
+    from fp8_tensor_core_gb300 import build as cuda_build
+    out = tmp_path / "bench_mma"
+    cmd = [cuda_build.nvcc()] + cuda_build.ARCH + ["-O3", "-std=c++17", "-I", cuda_build.CSRC, "-o", str(out),
+                                                   os.path.join(ROOT, "bench_mma.cu")]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert out.exists()

@@ -143,6 +143,12 @@ def test_dense_mixed_formats(fa, fb):
     check_dense_bs(200, 272, 640, 32, OFF, seed=530 + 2 * fa + fb, fa=fa, fb=fb)
 
 
+@pytest.mark.parametrize("fa,fb", [(E5, E4), (E4, E5), (E5, E5)])
+def test_single_sm_scale_ring_mixed_formats(fa, fb):
+    # 128-element groups on single-SM tiles: the scale ring with E5M2 operands
+    check_dense_bs(384, 672, 1664, 128, OFF | fp8g.SINGLE_SM_TILES, seed=570 + 2 * fa + fb, fa=fa, fb=fb)
+
+
 @pytest.mark.parametrize("kernel", ["pair", "single_sm"])
 def test_dense_one_stage_pipeline(kernel):
     # one stage: a single MMA issuer (two need an even stage count)
