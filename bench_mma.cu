@@ -32,7 +32,7 @@ constexpr int kCopyStages = 3;              // ... with copy traffic (one buffer
 constexpr int kCopyMax = 48 * 1024;         // copy bytes per stage at most
 constexpr int kSetCol = 448;                // TMEM column of the scale set (A side 4, B side 8 columns)
 constexpr uint64_t kLimitNs = 2000000000ull;  // bound on every wait
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;   // warps 0-3 the roles below, warps 4-7 optional scale-set writers
 
 enum Mode : int {
     kPlain = 0,        // one issuer, back-to-back plain MMAs, a commit every 4
@@ -54,6 +54,7 @@ struct Smem {
     uint64_t done[2];       // per issuer: all its MMAs completed
     uint64_t set_done;      // scale-set writes: one arrival per warp
     uint32_t tmem_base;
+    volatile int stop;      // handshake cases: the MMAs are done (stops the scale-set writers)
 };
 
 // %globaltimer with a memory clobber, so that the compiler keeps each read
@@ -154,8 +155,8 @@ __device__ Smem &carve()
 // One SM per CTA.  Returns per CTA the nanoseconds from the common start to
 // the completion of every MMA (or of every scale-set write).
 __global__ void __launch_bounds__(kThreads, 1) k_single(int mode, int n, int iters, int copy_bytes,
-                                                        const uint8_t *copy_src, unsigned long long *ns_out,
-                                                        int *flag)
+                                                        const uint8_t *copy_src, int write_gap_ns,
+                                                        unsigned long long *ns_out, int *flag)
 {
     Smem &s = carve();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -169,6 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_single(int mode, int n, int ite
         mbar_init(smem_addr(&s.done[0]), 1);
         mbar_init(smem_addr(&s.done[1]), 1);
         mbar_init(smem_addr(&s.set_done), 4);
+        s.stop = 0;
         fence_mbar_init();
     }
     __syncthreads();
@@ -198,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_single(int mode, int n, int ite
     __syncthreads();
     const uint64_t t0 = t_start;
 
-    if (mode == kScaleSetWrite) {
+    if (mode == kScaleSetWrite && warp < 4) {
         // Each round: every warp writes its quadrant (tcgen05.st + wait::st),
         // orders it before the arrive and arrives; all four then wait for the
         // round's four arrivals, as an MMA issuer waiting for the set would.
@@ -267,6 +269,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_single(int mode, int n, int ite
                 mma_commit(smem_addr(&s.done[0]));
             __syncwarp();
             warp_wait_bounded(smem_addr(&s.done[0]), 0, t0, flag);
+            if (lane == 0)
+                s.stop = 1;
+        } else if (warp >= 4 && write_gap_ns > 0) {
+            // scale-set writers: every write_gap_ns a set (12 columns per lane
+            // quadrant) into TMEM columns the MMAs do not read, as staging
+            // warps do beside the MMA stream, until the MMAs are done
+            for (int i = 0; i < 1000000 && !s.stop; ++i) {
+                write_scale_set(tb, kSetCol + 16u + static_cast<uint32_t>((i & 1) * 16));
+                __nanosleep(static_cast<unsigned>(write_gap_ns));
+                if (stamp_ns() - t0 > kLimitNs)
+                    break;
+            }
         }
     } else if (warp >= 1 && warp <= issuers) {
         const int me = warp - 1;
@@ -399,7 +413,7 @@ int main()
     const char *names[] = {"plain", "block_scaled", "plain", "block_scaled", "plain", "block_scaled", "scale_set_write"};
 
     auto report = [&](const char *kind, int cta_group, int issuers, bool handshake, int n, long long units,
-                      const char *unit, int copy_bytes = 0) -> int {
+                      const char *unit, int copy_bytes = 0, int write_gap = 0) -> int {
         if (check(cudaDeviceSynchronize(), kind))
             return 1;
         unsigned long long h[512] = {};
@@ -410,8 +424,9 @@ int main()
         for (int i = 0; i < grid; ++i)
             worst = h[i] > worst ? h[i] : worst;
         std::printf("{\"op\": \"%s\", \"cta_group\": %d, \"issuers\": %d, \"handshake\": %s, \"n\": %d, "
-                    "\"copy_bytes_per_kblock\": %d, \"ns_per_%s\": %.2f, \"ctas\": %d, \"timed_out\": %s}\n",
-                    kind, cta_group, issuers, handshake ? "true" : "false", n, copy_bytes, unit,
+                    "\"copy_bytes_per_kblock\": %d, \"set_write_gap_ns\": %d, \"ns_per_%s\": %.2f, \"ctas\": %d, "
+                    "\"timed_out\": %s}\n",
+                    kind, cta_group, issuers, handshake ? "true" : "false", n, copy_bytes, write_gap, unit,
                     static_cast<double>(worst) / static_cast<double>(units), grid, flag ? "true" : "false");
         std::fflush(stdout);
         return flag;
@@ -421,7 +436,7 @@ int main()
     // copy bytes per K block with the handshake: 0, an SM pair's per-SM operand
     // bytes (256 x 256 tile: 16 KB + 16 KB), and a single SM's at 224 / 256
     // columns (16 KB + 28 KB / 32 KB)
-    struct Case { int mode, n, copy; };
+    struct Case { int mode, n, copy, write_gap = 0; };
     const Case cases[] = {
         {kPlain, 32, 0}, {kPlain, 128, 0}, {kPlain, 224, 0}, {kPlain, 256, 0},
         {kBlockScaled, 32, 0}, {kBlockScaled, 128, 0}, {kBlockScaled, 224, 0}, {kBlockScaled, 256, 0},
@@ -429,10 +444,12 @@ int main()
         {kPlainHs, 224, 0}, {kPlainHs, 256, 0}, {kBlockScaledHs, 224, 0}, {kBlockScaledHs, 256, 0},
         {kPlainHs, 256, 32768}, {kPlainHs, 224, 45056}, {kPlainHs, 256, 49152},
         {kBlockScaledHs, 224, 45056}, {kBlockScaledHs, 256, 49152},
+        // with four warps writing a scale set into other TMEM columns every ~1 us
+        {kPlainHs, 224, 0, 1000}, {kBlockScaledHs, 224, 0, 1000}, {kBlockScaledHs, 224, 0, 250},
     };
     for (const Case &c : cases) {
         for (int rep = 0; rep < 2; ++rep) {   // the first run warms up
-            k_single<<<grid, kThreads, smem>>>(c.mode, c.n, iters, c.copy, d_copy, d_ns, d_flag);
+            k_single<<<grid, kThreads, smem>>>(c.mode, c.n, iters, c.copy, d_copy, c.write_gap, d_ns, d_flag);
             if (check(cudaGetLastError(), "launch"))
                 return 1;
             if (rep == 0) {
@@ -442,12 +459,12 @@ int main()
             }
             const int issuers = (c.mode == kPlain2 || c.mode == kBlockScaled2) ? 2 : 1;
             const bool hs = c.mode == kPlainHs || c.mode == kBlockScaledHs;
-            if (report(names[c.mode], 1, issuers, hs, c.n, 4LL * iters, "mma", c.copy))
+            if (report(names[c.mode], 1, issuers, hs, c.n, 4LL * iters, "mma", c.copy, c.write_gap))
                 return 2;
         }
     }
     for (int rep = 0; rep < 2; ++rep) {
-        k_single<<<grid, kThreads, smem>>>(kScaleSetWrite, 0, iters, 0, d_copy, d_ns, d_flag);
+        k_single<<<grid, kThreads, smem>>>(kScaleSetWrite, 0, iters, 0, d_copy, 0, d_ns, d_flag);
         if (check(cudaGetLastError(), "launch"))
             return 1;
         if (rep == 1 && report(names[kScaleSetWrite], 1, 4, true, 0, iters, "set"))
