@@ -5,6 +5,8 @@ stream-K scratch is a fixed device array inside the library, shared by every
 call, so two calls in a row must both agree with the oracle (and, bit for
 bit, with the allocating entry point that runs the same kernel).
 
+A third test checks that the calls take no device memory.
+
 Kept in a file of its own that pytest collects last."""
 import ctypes
 
@@ -78,3 +80,41 @@ def test_noalloc_rejects_problems_beyond_its_scratch(lib):
                                    stream) == 3
     torch.cuda.synchronize()
     assert torch.count_nonzero(D).item() == 0
+
+
+def test_noalloc_takes_no_device_memory(lib):
+    """Calls of the no-allocation entry point leave the device's free memory
+    unchanged, on a stream no call has used before; the same kind of call
+    through fp8_gemm_nt on another new stream does allocate (that stream's
+    stream-K scratch), so the check can see an allocation."""
+    shapes = [(1, 7168, 4096), (16, 4096, 2048), (64, 7168, 4096), (200, 2048, 1024)]
+    bufs = []
+    for M, N, K in shapes:
+        A = torch.from_numpy(synth.normal_fp8((M, K), 700 + M, 0.0, 1.0, synth.E4M3)).cuda()
+        B = torch.from_numpy(synth.normal_fp8((N, K), 701 + N, 0.0, 1.0, synth.E4M3)).cuda()
+        bufs.append((A, B, torch.empty((M, N), dtype=torch.bfloat16, device="cuda"), M, N, K))
+    warm = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for A, B, D, M, N, K in bufs:   # kernels loaded, device limits looked up
+        assert lib.fp8_gemm_nt_noalloc(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, 0, 0, warm) == 0
+    torch.cuda.synchronize()
+    s_new = torch.cuda.Stream()
+    stream = ctypes.c_void_p(s_new.cuda_stream)
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(3):
+        for A, B, D, M, N, K in bufs:
+            assert lib.fp8_gemm_nt_noalloc(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, 0, 0, stream) == 0
+    torch.cuda.synchronize()
+    # (1 MB of slack for the device's own bookkeeping; the library's scratch
+    # of any call is several MB)
+    assert torch.cuda.mem_get_info()[0] >= free0 - (1 << 20)
+    # control: the allocating entry point on a new stream (SwapAB, stream-K)
+    s_ctl = torch.cuda.Stream()
+    A, B, D, M, N, K = bufs[2]
+    assert lib.fp8_gemm_nt(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, 0, 0, 1,
+                           ctypes.c_void_p(s_ctl.cuda_stream)) == 0
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] < free0 - (4 << 20)   # 152 x 2 x 128 x 64 FP32 partial tiles
+    assert lib.fp8g_release_stream(ctypes.c_void_p(s_ctl.cuda_stream)) == 0
+    info = (ctypes.c_int32 * 4)()
+    assert lib.fp8g_get_device_status(info, stream) == 0
+    assert info[0] == 0, tuple(info)
