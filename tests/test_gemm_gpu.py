@@ -131,6 +131,16 @@ def test_dense_shapes(M, N, K, flags):
     check_dense(M, N, K, flags=flags, seed=M * 31 + N * 7 + K)
 
 
+@pytest.mark.parametrize("M,N,K", [(6144, 6144, 1280), (6145, 6136, 1296), (6143, 6144, 1040)])
+def test_dense_page_edge_shapes(M, N, K):
+    """The shape of "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践"
+    §6.1 (M = N = 6144, K = 1280, which failed at random there through a
+    write past a tile's K tail) and its neighbours: M one row either side of
+    a 256-row tile, N 8 short of a tile, K with a 16-byte tail past ten
+    128-byte blocks or three quarters of one.  Every element."""
+    check_dense(M, N, K, flags=AUTO, seed=M + N + K)
+
+
 def test_dense_uniform_256_cube():
     """The 256^3 U[-2,2] E4M3 workload, every element."""
     rep = check_dense(256, 256, 256, dist="uniform", seed=synth.seed_for(0))
