@@ -155,7 +155,7 @@ __device__ Smem &carve()
 // One SM per CTA.  Returns per CTA the nanoseconds from the common start to
 // the completion of every MMA (or of every scale-set write).
 __global__ void __launch_bounds__(kThreads, 1) k_single(int mode, int n, int iters, int copy_bytes,
-                                                        const uint8_t *copy_src, int write_gap_ns,
+                                                        const uint8_t *copy_src, int write_gap_ns, int cols,
                                                         unsigned long long *ns_out, int *flag)
 {
     Smem &s = carve();
@@ -193,7 +193,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_single(int mode, int n, int ite
                               : make_idesc(0, 0, 128, static_cast<uint32_t>(n));
     const uint64_t adesc = smem_desc_k_sw128(smem_addr(s.a));
     const uint64_t bdesc = smem_desc_k_sw128(smem_addr(s.b));
-    const uint32_t sets = tb + kSetCol;
+    // handshake cases: accumulator and scale-set columns (cols = acc << 16 | set; 0: 0 and kSetCol)
+    const uint32_t acc_col = static_cast<uint32_t>(cols) >> 16;
+    const uint32_t set_col = (cols & 0xFFFF) ? static_cast<uint32_t>(cols & 0xFFFF) : static_cast<uint32_t>(kSetCol);
+    if (set_col != kSetCol) {
+        write_scale_set(tb, set_col);
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+    const uint32_t sets = tb + set_col;
     __shared__ unsigned long long t_start;
     if (threadIdx.x == 0)
         t_start = stamp_ns();
@@ -254,9 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_single(int mode, int n, int ite
                 tc_fence_after();
                 if (lane == 0) {
                     if (bs)
-                        issue_kblock<true>(tb, adesc, bdesc, idesc, sets, i, i == 0);
+                        issue_kblock<true>(tb + acc_col, adesc, bdesc, idesc, sets, i, i == 0);
                     else
-                        issue_kblock<false>(tb, adesc, bdesc, idesc, sets, i, i == 0);
+                        issue_kblock<false>(tb + acc_col, adesc, bdesc, idesc, sets, i, i == 0);
                     mma_commit(smem_addr(&s.empty[st]));
                 }
                 __syncwarp();
@@ -413,7 +422,7 @@ int main()
     const char *names[] = {"plain", "block_scaled", "plain", "block_scaled", "plain", "block_scaled", "scale_set_write"};
 
     auto report = [&](const char *kind, int cta_group, int issuers, bool handshake, int n, long long units,
-                      const char *unit, int copy_bytes = 0, int write_gap = 0) -> int {
+                      const char *unit, int copy_bytes = 0, int write_gap = 0, int cols = 0) -> int {
         if (check(cudaDeviceSynchronize(), kind))
             return 1;
         unsigned long long h[512] = {};
@@ -424,9 +433,10 @@ int main()
         for (int i = 0; i < grid; ++i)
             worst = h[i] > worst ? h[i] : worst;
         std::printf("{\"op\": \"%s\", \"cta_group\": %d, \"issuers\": %d, \"handshake\": %s, \"n\": %d, "
-                    "\"copy_bytes_per_kblock\": %d, \"set_write_gap_ns\": %d, \"ns_per_%s\": %.2f, \"ctas\": %d, "
-                    "\"timed_out\": %s}\n",
-                    kind, cta_group, issuers, handshake ? "true" : "false", n, copy_bytes, write_gap, unit,
+                    "\"copy_bytes_per_kblock\": %d, \"set_write_gap_ns\": %d, \"acc_col\": %d, \"set_col\": %d, "
+                    "\"ns_per_%s\": %.2f, \"ctas\": %d, \"timed_out\": %s}\n",
+                    kind, cta_group, issuers, handshake ? "true" : "false", n, copy_bytes, write_gap, cols >> 16,
+                    (cols & 0xFFFF) ? (cols & 0xFFFF) : kSetCol, unit,
                     static_cast<double>(worst) / static_cast<double>(units), grid, flag ? "true" : "false");
         std::fflush(stdout);
         return flag;
@@ -436,7 +446,7 @@ int main()
     // copy bytes per K block with the handshake: 0, an SM pair's per-SM operand
     // bytes (256 x 256 tile: 16 KB + 16 KB), and a single SM's at 224 / 256
     // columns (16 KB + 28 KB / 32 KB)
-    struct Case { int mode, n, copy, write_gap = 0; };
+    struct Case { int mode, n, copy, write_gap = 0, cols = 0; };
     const Case cases[] = {
         {kPlain, 32, 0}, {kPlain, 128, 0}, {kPlain, 224, 0}, {kPlain, 256, 0},
         {kBlockScaled, 32, 0}, {kBlockScaled, 128, 0}, {kBlockScaled, 224, 0}, {kBlockScaled, 256, 0},
@@ -446,10 +456,14 @@ int main()
         {kBlockScaledHs, 224, 45056}, {kBlockScaledHs, 256, 49152},
         // with four warps writing a scale set into other TMEM columns every ~1 us
         {kPlainHs, 224, 0, 1000}, {kBlockScaledHs, 224, 0, 1000}, {kBlockScaledHs, 224, 0, 250},
+        // TMEM placement: accumulator at column 224, scale set at 460 / 472 (the tile kernel's)
+        {kBlockScaledHs, 224, 0, 0, (224 << 16) | 448}, {kBlockScaledHs, 224, 0, 0, 460},
+        {kBlockScaledHs, 224, 0, 0, 472}, {kBlockScaledHs, 224, 0, 0, (224 << 16) | 460},
+        {kPlainHs, 224, 0, 0, (224 << 16) | 448},
     };
     for (const Case &c : cases) {
         for (int rep = 0; rep < 2; ++rep) {   // the first run warms up
-            k_single<<<grid, kThreads, smem>>>(c.mode, c.n, iters, c.copy, d_copy, c.write_gap, d_ns, d_flag);
+            k_single<<<grid, kThreads, smem>>>(c.mode, c.n, iters, c.copy, d_copy, c.write_gap, c.cols, d_ns, d_flag);
             if (check(cudaGetLastError(), "launch"))
                 return 1;
             if (rep == 0) {
@@ -459,12 +473,12 @@ int main()
             }
             const int issuers = (c.mode == kPlain2 || c.mode == kBlockScaled2) ? 2 : 1;
             const bool hs = c.mode == kPlainHs || c.mode == kBlockScaledHs;
-            if (report(names[c.mode], 1, issuers, hs, c.n, 4LL * iters, "mma", c.copy, c.write_gap))
+            if (report(names[c.mode], 1, issuers, hs, c.n, 4LL * iters, "mma", c.copy, c.write_gap, c.cols))
                 return 2;
         }
     }
     for (int rep = 0; rep < 2; ++rep) {
-        k_single<<<grid, kThreads, smem>>>(kScaleSetWrite, 0, iters, 0, d_copy, 0, d_ns, d_flag);
+        k_single<<<grid, kThreads, smem>>>(kScaleSetWrite, 0, iters, 0, d_copy, 0, 0, d_ns, d_flag);
         if (check(cudaGetLastError(), "launch"))
             return 1;
         if (rep == 1 && report(names[kScaleSetWrite], 1, 4, true, 0, iters, "set"))
