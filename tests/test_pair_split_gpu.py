@@ -132,3 +132,69 @@ def test_split_tail_block_scaled_pair_tiles():
     ref, absdot, accb = oracle.gemm_blockscaled(A, B, sfa, sfb, 128, want_accbound=True)
     ok, rep = oracle.check_bf16(bits(D), ref, absdot, acc_bound=accb)
     assert ok, rep
+
+
+# FP8G_STREAM_K: the 28 tiles after the whole waves share 896 K blocks over
+# the 76 pairs in equal ranges of 11-12, so 12 tiles have three contributors
+# and 16 have four (the summing contributor then loads the other three's
+# partial tiles at once); 24 of them start inside another pair's range.
+# Without whole waves and after one.
+@pytest.mark.parametrize("M,N,K", [(512, 3584, 4096), (2048, 3328, 4096)])
+def test_stream_k_three_and_four_contributors_twice(M, N, K):
+    plan = plan_of(M, N, K, flags=fp8g.STREAM_K)
+    assert plan["kernel"] == fp8g.KERNEL_SM_PAIRS and plan["k_split"] == 0, plan
+    A = synth.normal_fp8((M, K), 931 + M, 0.0, 1.0, E4)
+    B = synth.normal_fp8((N, K), 932 + N, 0.0, 1.0, E4)
+    Ad, Bd = dev(A), dev(B)
+    ref, absdot = oracle.gemm_nt(A, B, E4, E4)
+    first = None
+    for call in range(2):
+        D = fp8g.fp8_gemm_nt(Ad, Bd, a_dtype=E4, b_dtype=E4, flags=fp8g.STREAM_K)
+        torch.cuda.synchronize()
+        st = fp8g.fp8g_get_device_status()
+        assert st[0] == fp8g.OK, st
+        got = bits(D)
+        ok, rep = oracle.check_bf16(got, ref, absdot)
+        assert ok, (call, rep)
+        if first is None:
+            first = got
+        else:
+            assert np.array_equal(first, got), "stream-K results differ between calls"
+
+
+def test_stream_k_three_and_four_contributors_integer_exact_and_epilogue():
+    """Integer-valued products make every FP32 partial and sum exact, so the
+    three- and four-contributor sums must equal the oracle bit for bit; the
+    fused epilogue (output scales, alpha, beta*C, bias, ReLU, rounding
+    toward zero) runs on the same tiles."""
+    M, N, K = 512, 3584, 4096
+    assert plan_of(M, N, K, flags=fp8g.STREAM_K)["k_split"] == 0
+    rng = np.random.default_rng(941)
+    # E4M3 codes of -2..2: every partial sum is an integer below 2^14, exact in FP32
+    enc = {-2: 0xC0, -1: 0xB8, 0: 0x00, 1: 0x38, 2: 0x40}
+    A = np.vectorize(enc.get)(rng.choice([-2, -1, 0, 1, 2], (M, K))).astype(np.uint8)
+    B = np.vectorize(enc.get)(rng.choice([-2, -1, 0, 1, 2], (N, K))).astype(np.uint8)
+    D = fp8g.fp8_gemm_nt(dev(A), dev(B), a_dtype=E4, b_dtype=E4, flags=fp8g.STREAM_K)
+    torch.cuda.synchronize()
+    assert fp8g.fp8g_get_device_status()[0] == fp8g.OK
+    ref, absdot = oracle.gemm_nt(A, B, E4, E4)
+    assert np.array_equal(bits(D), ref)
+
+    A = synth.normal_fp8((M, K), 942, 0.0, 1.0, E4)
+    B = synth.normal_fp8((N, K), 943, 0.0, 1.0, E4)
+    sa = np.exp2(rng.uniform(-3, 3, M)).astype(np.float32)
+    sb = np.exp2(rng.uniform(-3, 3, N)).astype(np.float32)
+    C = rng.standard_normal((M, N)).astype(np.float32)
+    Ct = torch.from_numpy(C).to(torch.bfloat16).cuda()
+    Cb = Ct.view(torch.int16).cpu().numpy().view(np.uint16)
+    bias = rng.standard_normal(N).astype(np.float32)
+    _, absS, S = oracle.gemm_nt(A, B, want_exact=True)
+    f = sa.astype(np.float64)[:, None] * sb.astype(np.float64)[None, :]
+    ref, absdot = oracle.epilogue(S * f, absS * np.abs(f), 0.5, 2.0, Cb, bias, True, 1)
+    out = fp8g.fp8_gemm_nt_ex(dev(A), dev(B), scale_a=dev(sa), scale_b=dev(sb),
+                              epilogue={"alpha": 0.5, "beta": 2.0, "C": Ct, "bias": dev(bias), "relu": True,
+                                        "round_mode": 1}, a_dtype=E4, b_dtype=E4, flags=fp8g.STREAM_K)
+    torch.cuda.synchronize()
+    assert fp8g.fp8g_get_device_status()[0] == fp8g.OK
+    ok, rep = oracle.check_bf16(bits(out), ref, absdot)
+    assert ok, rep
