@@ -29,11 +29,14 @@ E4, E5 = synth.E4M3, synth.E5M2
 OFF, ON, AUTO = fp8g.SWAP_OFF, fp8g.SWAP_ON, fp8g.SWAP_AUTO
 SEED = 20261202
 MAC_CAP = 1.2e9           # multiply-adds per problem
+LARGE_MAC_CAP = 12e9      # ... of the large dense ones
 
 DENSE_FLAGS = [AUTO, AUTO, ON, OFF, OFF | fp8g.SINGLE_SM_TILES, OFF | fp8g.STREAM_K, OFF | fp8g.SPLIT_TAIL,
                OFF | fp8g.WHOLE_TILES, ON | fp8g.WHOLE_TILES, ON | fp8g.SHARE_SM, ON | fp8g.NO_SHARE_SM,
                OFF | fp8g.TILE_N(128), OFF | fp8g.TILE_N(160), OFF | fp8g.TILE_N(224), OFF | fp8g.STAGES(2),
                OFF | fp8g.STAGES(3), AUTO | fp8g.DEBUG_ONE_STAGE]
+LARGE_FLAGS = [AUTO, AUTO, OFF | fp8g.SPLIT_TAIL, OFF | fp8g.STREAM_K, OFF | fp8g.TILE_N(128) | fp8g.SPLIT_TAIL,
+               OFF | fp8g.TILE_N(128), OFF | fp8g.TILE_N(224), OFF | fp8g.WHOLE_TILES, OFF | fp8g.SINGLE_SM_TILES]
 GROUPED_FLAGS = [AUTO, AUTO, ON, OFF, OFF | fp8g.PAIR_TILES, ON | fp8g.WHOLE_TILES, OFF | fp8g.STAGES(3)]
 CONTIG_FLAGS = [AUTO, ON, OFF]
 BS_FLAGS = [AUTO, AUTO, ON, OFF, OFF | fp8g.SINGLE_SM_TILES, OFF | fp8g.PAIR_TILES, OFF | fp8g.ONE_MMA_ISSUER,
@@ -71,6 +74,12 @@ def _draw(rng, kind):
         if M * N * K > MAC_CAP:
             return None
         return dict(kind=kind, M=M, N=N, K=K, fa=fa, fb=fb, flags=int(rng.choice(DENSE_FLAGS)))
+    if kind == "dense_large":
+        # many 256-row tiles: whole waves of SM pairs and a split or stream-K tail
+        M, N, K = int(rng.integers(1536, 3073)), 8 * int(rng.integers(160, 401)), 16 * int(rng.integers(128, 257))
+        if M * N * K > LARGE_MAC_CAP:
+            return None
+        return dict(kind="dense", M=M, N=N, K=K, fa=fa, fb=fb, flags=int(rng.choice(LARGE_FLAGS)))
     if kind in ("masked", "bs_masked", "scaled_masked"):
         G = int(rng.integers(1, 13))
         M_max = _log_int(rng, 1, 224 if kind == "bs_masked" else 320)
@@ -114,7 +123,7 @@ def _draw(rng, kind):
                 round_mode=int(rng.integers(4)), alpha=float(rng.choice([1.0, 0.25, -2.0])))
 
 
-COUNTS = [("dense", 64), ("masked", 32), ("contig", 16), ("bs", 32), ("bs_masked", 16), ("scaled_masked", 12),
+COUNTS = [("dense", 64), ("dense_large", 16), ("masked", 32), ("contig", 16), ("bs", 32), ("bs_masked", 16), ("scaled_masked", 12),
           ("epilogue", 24)]
 
 
