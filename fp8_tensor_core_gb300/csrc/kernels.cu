@@ -458,10 +458,9 @@ __device__ __forceinline__ bool sf_load_at(int kb, int kb_first, int sf_k)
 __device__ __forceinline__ int sf_first_group(int kb, int sf_k) { return sf_k == 1 ? (kb & ~3) : 4 * kb; }
 
 // ---- block scales written into TMEM by staging warps ---------------------------------
-// (SwapAB and single-SM kernels.)  A copy of scale factors into TMEM issued
-// by the MMA thread costs it ~100 ns and a block-scaled MMA ~95 ns, so the
-// scale sets are written by four staging warps instead (tcgen05.st, one
-// TMEM lane quadrant each) and announced on sfset_ready[set] (four
+// (All three kernels.)  The scale sets are written by four staging warps
+// (tcgen05.st, one TMEM lane quadrant each), which also turn the copied
+// bytes into the TMEM layout, and announced on sfset_ready[set] (four
 // arrivals); the MMA issuers only wait for a set and retire it.
 
 // Staging warp, all lanes, for scale load j (raw: its bytes, [4][128] of
@@ -473,13 +472,14 @@ __device__ __forceinline__ int sf_first_group(int kb, int sf_k) { return sf_k ==
 // column r / 32; side B from column 4 likewise -- and arrive (kPair: on the
 // even CTA's barrier, which counts both CTAs' staging warps).  box_b <= 256.
 // Returns false when a wait gave up.
+// (The set and the retire parity given: TMEM set `set`, waiting for the
+// retire phase of parity free_par first if wait_free.)
 template <bool kPair = false>
-__device__ __forceinline__ bool sf_stage_tmem(SmemCtl &ctl, const GemmArgs &a, const uint8_t *raw, int box_b,
-                                              int j, uint32_t sets_q, int set_cols, uint64_t *slot_free = nullptr)
+__device__ __forceinline__ bool sf_stage_tmem_set(SmemCtl &ctl, const GemmArgs &a, const uint8_t *raw, int box_b,
+                                                  int set, bool wait_free, uint32_t free_par, uint32_t sets_q,
+                                                  int set_cols, uint64_t *slot_free = nullptr)
 {
     const int lane = threadIdx.x & 31;
-    const int R = a.sf_sets;
-    const int set = j % R;
     auto word = [](const uint8_t *raw, int box, int r) {
         return static_cast<uint32_t>(raw[r]) | (static_cast<uint32_t>(raw[box + r]) << 8) |
                (static_cast<uint32_t>(raw[2 * box + r]) << 16) | (static_cast<uint32_t>(raw[3 * box + r]) << 24);
@@ -500,8 +500,7 @@ __device__ __forceinline__ bool sf_stage_tmem(SmemCtl &ctl, const GemmArgs &a, c
         if (lane == 0)
             mbar_arrive(smem_addr(slot_free));
     }
-    if (j >= R && !warp_wait(smem_addr(&ctl.sffree[set]), static_cast<uint32_t>((j / R - 1) & 1), ctl, a.timeout_ns,
-                             kRoleScales, 400 + set))
+    if (wait_free && !warp_wait(smem_addr(&ctl.sffree[set]), free_par, ctl, a.timeout_ns, kRoleScales, 400 + set))
         return false;
     tc_fence_after();
     const uint32_t t = sets_q + static_cast<uint32_t>(set * set_cols);
@@ -518,6 +517,16 @@ __device__ __forceinline__ bool sf_stage_tmem(SmemCtl &ctl, const GemmArgs &a, c
             mbar_arrive(smem_addr(&ctl.sfset_ready[set]));
     }
     return true;
+}
+
+// Scale load j into TMEM set j % sf_sets.
+template <bool kPair = false>
+__device__ __forceinline__ bool sf_stage_tmem(SmemCtl &ctl, const GemmArgs &a, const uint8_t *raw, int box_b,
+                                              int j, uint32_t sets_q, int set_cols, uint64_t *slot_free = nullptr)
+{
+    const int R = a.sf_sets;
+    return sf_stage_tmem_set<kPair>(ctl, a, raw, box_b, j % R, j >= R, static_cast<uint32_t>((j / R - 1) & 1), sets_q,
+                                    set_cols, slot_free);
 }
 
 // MMA issuer warp, all lanes, at scale load j + 1: retire set j (a commit
@@ -881,6 +890,7 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
         uint32_t sf_par = 0, sf_used = 0;   // per ring slot (or stage): parity of scale fills posted, any posted
         int sf_u = blockIdx.x, sf_kb = 0;   // next scale load (its tile and first K block)
         int sf_posted = 0, sf_reached = 0;  // scale loads posted; scale sets whose first K block was reached
+        int sf_du = -1, sf_g = 0, sf_m0 = 0, sf_n0 = 0;   // the last tile decoded for scale loads
         // Post the next scale load into slot sf_posted % sf_ring, once the
         // staging warps have read that slot's previous load.
         auto sf_post = [&]() -> bool {
@@ -889,9 +899,13 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
                 !warp_wait(smem_addr(&ctl.sfslot_free[slot]), static_cast<uint32_t>((sf_posted / a.sf_ring - 1) & 1),
                            ctl, a.timeout_ns, kRoleLoader, 600 + slot))
                 return false;
+            if (sf_u != sf_du) {
+                int mv;
+                decode(sf_u, sf_g, sf_m0, sf_n0, mv);
+                sf_du = sf_u;
+            }
             if (lane == 0) {
-                int g, m0, n0, mv;
-                decode(sf_u, g, m0, n0, mv);
+                const int g = sf_g, m0 = sf_m0, n0 = sf_n0;
                 uint8_t *dst = sm.sf_ring + static_cast<size_t>(slot) * a.sf_slot_bytes;
                 const uint32_t sb = smem_addr(&ctl.sffull[slot]);
                 const int y = sf_first_group(sf_kb, a.sf_k);
@@ -1026,7 +1040,75 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
         uint32_t acc_phase = 0;
         bool issued_any = false;
         bool ok = true;
-        for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        const bool lean = acc_step == 1 && a.sf_k == 1;
+        if (lean) {
+            // One issuer, 128-element groups: a scale set covers four K
+            // blocks.  The loop is kept as short as the plain kernel's: at a
+            // set switch the retire commit, then the waits for the new set
+            // and for the operands behind one tensor fence, the set's TMEM
+            // slot and phase kept by increment (no division).
+            const int R = a.sf_sets;
+            int cur = -1;            // TMEM scale set in use
+            int nxt = 0;             // the next one
+            uint32_t rpar = 0;       // parity of its ready phase
+            for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+                if (!warp_wait(smem_addr(&ctl.tempty[acc]), acc_phase ^ 1u, ctl, a.timeout_ns, kRoleMma,
+                               100 + acc))
+                    break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * acc_stride);
+                for (int kb = 0; kb < a.num_kb; ++kb) {
+                    if ((kb & 3) == 0) {
+                        if (cur >= 0 && lane == 0)
+                            mma_commit(smem_addr(&ctl.sffree[cur]));
+                        cur = nxt;
+                        if (!warp_wait(smem_addr(&ctl.sfset_ready[cur]), rpar, ctl, a.timeout_ns, kRoleMma,
+                                       300 + cur)) {
+                            ok = false;
+                            break;
+                        }
+                        if (++nxt == R) {
+                            nxt = 0;
+                            rpar ^= 1u;
+                        }
+                        set_tmem = sets_tmem + static_cast<uint32_t>(cur * set_cols);
+                    }
+                    if (!warp_wait(smem_addr(&ctl.full[stage]), phase, ctl, a.timeout_ns, kRoleMma, stage)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t sa = smem_addr(sm.stages + static_cast<size_t>(stage) * a.stage_bytes);
+                        const uint64_t adesc = smem_desc_k_sw128(sa);
+                        const uint64_t bdesc = smem_desc_k_sw128(sa + a_bytes);
+                        const uint32_t id = static_cast<uint32_t>(kb & 3);
+                        const uint32_t idesc = idesc_bs | (id << 4) | (id << 29);
+#pragma unroll
+                        for (int k = 0; k < kBlockK / 32; ++k)
+                            mma_f8f6f4_bs(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, set_tmem, set_tmem + 4u,
+                                          (kb | k) != 0 ? 1u : 0u);
+                        mma_commit(smem_addr(&ctl.empty[stage]));
+                    }
+                    __syncwarp();
+                    issued_any = true;
+                    if (++stage == a.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                if (lane == 0)
+                    mma_commit(smem_addr(&ctl.tfull[acc]));
+                __syncwarp();
+                if (++acc == n_bufs) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+        }
+        for (int u = blockIdx.x; !lean && u < total && ok; u += gridDim.x) {
             if (!warp_wait(smem_addr(&ctl.tempty[acc]), acc_phase ^ 1u, ctl, a.timeout_ns, kRoleMma,
                            100 + acc))
                 break;
@@ -1089,25 +1171,36 @@ __global__ void __launch_bounds__(kBS ? kThreadsTmemScaled : kThreads, 1)
             int su = blockIdx.x, skb = 0;
             int stage = 0;
             uint32_t st_par = 0;   // per stage: parity of the next scale fill to wait for
+            // Load j's ring slot (j % sf_ring) with its fill parity, and its
+            // TMEM set (j % sf_sets) with j / sf_sets, kept by increment.
+            int slot = 0, set = 0;
+            uint32_t slot_par = 0, gen = 0;
             for (int j = 0; su < total; ++j) {
                 if (sf_ring) {
-                    const int slot = j % a.sf_ring;
-                    if (!warp_wait(smem_addr(&ctl.sffull[slot]), static_cast<uint32_t>((j / a.sf_ring) & 1), ctl,
-                                   a.timeout_ns, kRoleScales, 700 + slot) ||
-                        !sf_stage_tmem(ctl, a, sm.sf_ring + static_cast<size_t>(slot) * a.sf_slot_bytes, a.tile_n, j,
-                                       sets_q, set_cols, &ctl.sfslot_free[slot]))
+                    if (!warp_wait(smem_addr(&ctl.sffull[slot]), slot_par, ctl, a.timeout_ns, kRoleScales,
+                                   700 + slot) ||
+                        !sf_stage_tmem_set(ctl, a, sm.sf_ring + static_cast<size_t>(slot) * a.sf_slot_bytes, a.tile_n,
+                                           set, gen > 0, (gen & 1u) ^ 1u, sets_q, set_cols, &ctl.sfslot_free[slot]))
                         break;
+                    if (++slot == a.sf_ring) {
+                        slot = 0;
+                        slot_par ^= 1u;
+                    }
                 } else {
                     // every K block carries a scale load (32-element groups):
                     // the sets follow the stages one to one
                     if (!warp_wait(smem_addr(&ctl.sffull[stage]), (st_par >> stage) & 1u, ctl, a.timeout_ns,
                                    kRoleScales, stage) ||
-                        !sf_stage_tmem(ctl, a, sm.stages + static_cast<size_t>(stage) * a.stage_bytes + a.sf_off,
-                                       a.tile_n, j, sets_q, set_cols))
+                        !sf_stage_tmem_set(ctl, a, sm.stages + static_cast<size_t>(stage) * a.stage_bytes + a.sf_off,
+                                           a.tile_n, set, gen > 0, (gen & 1u) ^ 1u, sets_q, set_cols))
                         break;
                     st_par ^= 1u << stage;
                     if (++stage == a.stages)
                         stage = 0;
+                }
+                if (++set == a.sf_sets) {
+                    set = 0;
+                    ++gen;
                 }
                 sf_advance(su, skb);
             }
