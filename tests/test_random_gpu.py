@@ -162,6 +162,8 @@ def _plan(c, sms=0, smem=0):
 def test_random_cases_are_accepted_and_varied():
     """Host side: the library plans every drawn case for a 152-SM GB300
     (no argument is rejected), and the draw reaches all three kernels."""
+    from fp8_tensor_core_gb300 import build as cuda_build
+    cuda_build.build()          # host planning lives in the library (no GPU needed)
     kernels = set()
     for c in CASES:
         kernels.add(_plan(c, 152, 232448)["kernel"])
